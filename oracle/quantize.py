@@ -1,0 +1,185 @@
+"""Quantize-on-append, fp64 oracle: norm, rotate, bucketize, pack, residual QJL.
+
+What the write-ups say:
+* the vector is normalised and its norm kept aside (A2A TurboQuant explainer,
+  section "Stage 1", first bullet under PolarQuant);
+* it is rotated by the fixed random orthogonal matrix and each coordinate is
+  mapped to a low-bit index by the Lloyd-Max quantizer of the Beta law
+  (same section; Qiita TurboQuant article, "Rotate, then quantize");
+* the two-stage variant rounds with the MSE quantizer first and then applies a
+  1-bit Quantized Johnson-Lindenstrauss transform to the residual so the
+  inner-product estimate becomes unbiased (Qiita, "One more stage so attention
+  does not break"; A2A, "Stage 2: QJL residual correction");
+* attention is then scored straight from the stored indices (A2A, end of
+  "Stage 2").
+
+Readings (the pages are silent or garbled):
+* MSE mode (values) uses b bits per coordinate; PROD mode (keys) uses b-1 bits
+  of Lloyd-Max plus m sign bits of S r, m = d unless stated (A2A "Stage 2"
+  says "1 bit per vector ... +1 or 5"; read as one sign bit per projected
+  coordinate, +1 or -1);
+* S is m x d, standard normal draws rounded to bfloat16, applied to the
+  residual in the rotated domain, r = y - c[idx] with y = Pi x / ||x||;
+* the norms ||x|| and gamma = ||r|| are stored as float16, round to nearest
+  even, saturated at 65504;
+* a zero vector gets n = 0 and y = 0 and then goes through the same steps;
+* a coordinate equal to a boundary goes to the upper cell.
+
+Packed layout (this project's specification; the pages give none):
+* codes: LSB-first bit stream, bit k of coordinate i's index at stream bit
+  b'*i + k, stream bit p in byte p // 8 at bit p % 8; row stride = the byte
+  count rounded up to 16; padding bits 0;
+* signs: bit j = [(S r)_j >= 0] at byte j // 8, bit j % 8; stride rounded up
+  to 16;
+* norm / rnorm: float16 per vector.
+
+Pinned by: per-coordinate MSE equal to the codebook's distortion, the cosine
+figure the A2A page prints for 3 bits, the unbiasedness of the PROD inner
+product over seeds (and the 2/pi bias of 1-bit MSE without it), a hand-worked
+packing example (tests/golden/packing_example.json); the exact byte layout
+itself is this project's spec (parity unpinned beyond that example and the
+round trip).
+"""
+
+import numpy as np
+
+from . import codebook, rotation
+
+
+def fp16_rne(x):
+    """Round float64 to the nearest float16 (ties to even), saturating at 65504.
+
+    Returned as float64 holding the float16 value.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), 65504.0)
+    out = np.empty_like(a)
+    small = a < 2.0**-14
+    out[small] = np.rint(a[small] * 2.0**24) * 2.0**-24  # subnormal spacing
+    m, e = np.frexp(a[~small])
+    out[~small] = np.ldexp(np.rint(m * 2048.0), e - 11)  # 11 significant bits
+    out = np.minimum(out, 65504.0)
+    return np.copysign(out, x)
+
+
+def code_bits(mode, bits):
+    """Lloyd-Max bits per coordinate: b for MSE (values), b-1 for PROD (keys)."""
+    if mode == "mse":
+        if not 1 <= bits <= 4:
+            raise ValueError("MSE bits must be 1..4")
+        return bits
+    if mode == "prod":
+        if not 2 <= bits <= 5:
+            raise ValueError("PROD bits must be 2..5")
+        return bits - 1
+    raise ValueError(mode)
+
+
+def row_stride(nbits_per_row):
+    nbytes = (nbits_per_row + 7) // 8
+    return (nbytes + 15) // 16 * 16
+
+
+def quantize(x, pi, mode, bits, s_matrix=None):
+    """Quantize rows of x (float64 [n, d]).
+
+    Returns a dict with: n (exact norm), norm16, y (rotated unit vector), idx
+    (codes, int64 [n, d]); for PROD also r, gamma, rnorm16, sproj (= S r) and
+    z (bool [n, m]).
+    """
+    x = np.atleast_2d(np.asarray(x, dtype=np.float64))
+    d = x.shape[1]
+    bp = code_bits(mode, bits)
+    c, t = codebook.lloyd_max(d, bp)
+    n = np.sqrt(np.sum(x * x, axis=1))
+    safe = np.where(n > 0, n, 1.0)
+    y = rotation.rotate(pi, x) / safe[:, None]
+    y[n == 0] = 0.0
+    idx = codebook.bucketize(y, t)
+    out = {"n": n, "norm16": fp16_rne(n), "y": y, "idx": idx, "centroids": c, "boundaries": t}
+    if mode == "prod":
+        if s_matrix is None:
+            raise ValueError("PROD mode needs the QJL matrix S")
+        r = y - c[idx]
+        gamma = np.sqrt(np.sum(r * r, axis=1))
+        sproj = r @ np.asarray(s_matrix, dtype=np.float64).T
+        out.update(r=r, gamma=gamma, rnorm16=fp16_rne(gamma), sproj=sproj, z=sproj >= 0.0)
+    return out
+
+
+def pack_codes(idx, bprime):
+    """LSB-first bit stream per row, stride rounded up to 16 bytes."""
+    idx = np.atleast_2d(np.asarray(idx, dtype=np.int64))
+    n, d = idx.shape
+    stride = row_stride(bprime * d)
+    out = np.zeros((n, stride), dtype=np.uint8)
+    for i in range(d):
+        for k in range(bprime):
+            p = bprime * i + k
+            bit = ((idx[:, i] >> k) & 1).astype(np.uint8)
+            out[:, p // 8] |= bit << np.uint8(p % 8)
+    return out
+
+
+def unpack_codes(packed, d, bprime):
+    packed = np.atleast_2d(np.asarray(packed, dtype=np.uint8))
+    idx = np.zeros((packed.shape[0], d), dtype=np.int64)
+    for i in range(d):
+        for k in range(bprime):
+            p = bprime * i + k
+            bit = (packed[:, p // 8] >> np.uint8(p % 8)) & 1
+            idx[:, i] |= bit.astype(np.int64) << k
+    return idx
+
+
+def pack_signs(z):
+    z = np.atleast_2d(np.asarray(z, dtype=bool))
+    n, m = z.shape
+    out = np.zeros((n, row_stride(m)), dtype=np.uint8)
+    for j in range(m):
+        out[:, j // 8] |= z[:, j].astype(np.uint8) << np.uint8(j % 8)
+    return out
+
+
+def unpack_signs(packed, m):
+    packed = np.atleast_2d(np.asarray(packed, dtype=np.uint8))
+    z = np.zeros((packed.shape[0], m), dtype=bool)
+    for j in range(m):
+        z[:, j] = ((packed[:, j // 8] >> np.uint8(j % 8)) & 1) == 1
+    return z
+
+
+def pack(qz, mode, bits):
+    """Packed planes of one quantize() result: codes, signs (PROD), norm, rnorm (PROD)."""
+    d = qz["idx"].shape[1]
+    planes = {
+        "codes": pack_codes(qz["idx"], code_bits(mode, bits)),
+        "norm": qz["norm16"].astype(np.float16),
+    }
+    if mode == "prod":
+        planes["signs"] = pack_signs(qz["z"])
+        planes["rnorm"] = qz["rnorm16"].astype(np.float16)
+    planes["d"] = d
+    return planes
+
+
+def qjl_scale(m):
+    """sqrt(pi/2) / m: E|g| = sqrt(2/pi) for g ~ N(0,1) makes the sign sketch unbiased."""
+    return np.sqrt(np.pi / 2.0) / m
+
+
+def reconstruct(qz, pi, mode, s_matrix=None, use_stored_norms=True):
+    """Explicit dense reconstruction x~ (used only to pin the logit estimator).
+
+    MSE:  x~ = n Pi^T c[idx]
+    PROD: x~ = n Pi^T (c[idx] + sqrt(pi/2)/m * gamma * S^T (2z - 1))
+    """
+    c = qz["centroids"]
+    n = qz["norm16"] if use_stored_norms else qz["n"]
+    yhat = c[qz["idx"]]
+    if mode == "prod":
+        s = np.asarray(s_matrix, dtype=np.float64)
+        g = qz["rnorm16"] if use_stored_norms else qz["gamma"]
+        pm = 2.0 * qz["z"].astype(np.float64) - 1.0
+        yhat = yhat + qjl_scale(s.shape[0]) * g[:, None] * (pm @ s)
+    return n[:, None] * rotation.unrotate(pi, yhat)
