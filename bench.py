@@ -1,0 +1,443 @@
+#!/usr/bin/env python
+"""Benchmark of the TurboQuant hot path on one GB300 (or N replicas).
+
+One step = one online decode step of a Llama-3.1-8B-shaped layer (batch 1,
+32 query / 8 KV heads, d = 128, 32768 cached tokens, randomized-Hadamard
+rotation, keys 3-bit PROD, values 3-bit MSE): quantize-on-append of the new
+token's K and V for every KV head, then decode attention of all query heads
+over the packed cache (query rotation, split-K scan, merge + un-rotation).
+
+Prints one JSON line: value = KV-tokens/s (cached tokens attended per second,
+all ranks), with the dominant kernel's roofline, the quantize half's
+throughput on the cache fill, an end-to-end figure through the C ABI with
+host buffers, the oracle timed on the host cores, and sampled SM clocks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tq|reference]
+"""
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode attn KV-tokens/s & HBM GB/s (% of GB300 peak); quantize vectors/s"
+UNIT = "KV-tokens/s"
+WORKLOAD = dict(name="llama8b_decode_32k", batch=1, hq=32, hkv=8, d=128, seq_len=32768,
+                rotation="rht", k_bits=3, v_bits=3)
+FLUSH_BYTES = 256 << 20  # > 129 MB L2
+SCAN_SOURCES = ["online_kv_cache_quantize_gb300/csrc/decode.cuh", "online_kv_cache_quantize_gb300/csrc/common.cuh"]
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _kernel_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(name, paths, units_scale=1.0):
+    """Per-launch DRAM bytes from a committed ncu summary, if the kernel source is unchanged."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[name]
+        if rec["source_hash"] != _kernel_hash(paths):
+            return None
+        return rec["dram_bytes_per_launch"] * units_scale
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        load = [r for r in rows if (num(r[4]) or 0) > 0] or rows
+        sm = [num(r[1]) for r in load if num(r[1]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in load:
+            for n, v in zip(names, r[6:10]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(load[0][2]),
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(load)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# --------------------------------------------------------------- tq arm ----
+def run_tq(args):
+    import torch
+    import torch.distributed as dist
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from online_kv_cache_quantize_gb300 import binding as B
+    from online_kv_cache_quantize_gb300 import build as bld
+    from online_kv_cache_quantize_gb300 import workloads as W
+
+    if rank == 0:
+        bld.build()
+    if ws > 1:
+        dist.barrier()
+    L = B.load()
+    w = WORKLOAD
+    bsz, hq, hkv, d, T = w["batch"], w["hq"], w["hkv"], w["d"], w["seq_len"]
+    rows = bsz * hkv
+    rot = B.tq_rotation_to_device(B.tq_make_rotation(W.ROT_SEED, d, w["rotation"]))
+    qjl = B.tq_qjl_to_device(B.tq_make_qjl(W.QJL_SEED, d, d))
+    kx, vx = W.decode_kv(bsz, hkv, T, seed=W.DATA_SEED + rank)
+    kdev = torch.from_numpy(kx.reshape(-1, d)).cuda().to(torch.bfloat16)
+    vdev = torch.from_numpy(vx.reshape(-1, d)).cuda().to(torch.bfloat16)
+    del kx, vx
+    kc = B.Cache("prod", w["k_bits"], d, rows=rows, capacity=T)
+    vc = B.Cache("mse", w["v_bits"], d, rows=rows, capacity=T)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    # --- argument blocks built once (the per-step calls only swap events) ---
+    def qargs(cache, x, qj, append=None):
+        a = B.tq_quant_args()
+        a.cache = cache.struct()
+        a.rot = rot.handle
+        a.qjl = qj.handle if qj is not None else None
+        a.x = x.data_ptr()
+        a.x_dtype = B.TQ_BF16
+        a.x_stride = d
+        a.n = x.shape[0]
+        if append is not None:
+            a.append_pos = append.data_ptr()
+            a.heads = hkv
+        return a
+
+    fill_k, fill_v = qargs(kc, kdev, qjl), qargs(vc, vdev, None)
+    q = torch.from_numpy(W.query_vectors((bsz, hq, d), dtype="bf16", seed=W.QUERY_SEED + rank)).cuda().to(torch.bfloat16)
+    knew = torch.from_numpy(W.query_vectors((rows, d), seed=100 + rank)).cuda().to(torch.bfloat16)
+    vnew = torch.from_numpy(W.query_vectors((rows, d), seed=200 + rank)).cuda().to(torch.bfloat16)
+    append = torch.full((bsz,), T - 1, dtype=torch.int32, device="cuda")
+    lens = torch.full((bsz,), T, dtype=torch.int32, device="cuda")
+    out = torch.empty((bsz, hq, d), dtype=torch.float32, device="cuda")
+    step_k, step_v = qargs(kc, knew, qjl, append), qargs(vc, vnew, None, append)
+    da, _keep = B._decode_struct(q, kc, vc, lens, T, rot, qjl, out)
+    wsz = L.tq_attn_decode_workspace(ctypes.byref(da))
+    wsb = B.workspace(wsz)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def check(s, what):
+        if s != 0:
+            raise RuntimeError(f"{what}: {B.status_name(s)} {L.tq_last_error().decode()}")
+
+    def step():
+        check(L.tq_quantize_kv(ctypes.byref(step_k), sp), "append K")
+        check(L.tq_quantize_kv(ctypes.byref(step_v), sp), "append V")
+        check(L.tq_attn_decode(ctypes.byref(da), wsb.data_ptr(), wsz, sp), "decode")
+
+    launches_per_step = 5  # append K, append V, query prep, split-K scan, merge
+
+    # cache fill (quantize all K and V of the context): also the quantize measurement
+    check(L.tq_quantize_kv(ctypes.byref(fill_k), sp), "fill K")
+    check(L.tq_quantize_kv(ctypes.byref(fill_v), sp), "fill V")
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_warm = time.time()
+    n_warm = 0
+    while n_warm < args.warmup or time.time() - t_warm < 1.5:
+        flush.fill_(n_warm & 0xFF)
+        step()
+        n_warm += 1
+        if n_warm % 256 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+
+    # --- quantize measurement: cache fill of the whole context (K and V) ---
+    nq_it = 20
+    qev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nq_it)]
+    for i in range(nq_it):
+        flush.fill_(i & 0xFF)
+        qev[i][0].record(stream)
+        check(L.tq_quantize_kv(ctypes.byref(fill_k), sp), "fill K")
+        check(L.tq_quantize_kv(ctypes.byref(fill_v), sp), "fill V")
+        qev[i][1].record(stream)
+    torch.cuda.synchronize()
+    q_ms = statistics.mean(a.elapsed_time(b) for a, b in qev)
+    q_vectors = 2 * rows * T
+    kbytes = B.tq_code_bytes(d, w["k_bits"] - 1) + B.tq_sign_bytes(d) + 4
+    vbytes = B.tq_code_bytes(d, w["v_bits"]) + 2
+    q_alg_bytes = rows * T * (2 * d * 2) + rows * T * (kbytes + vbytes)
+
+    # --- the timed region: exactly K steps, L2 flushed between them ---
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a_, b_ in sev:  # materialise the raw events so the library can record them
+        a_.record(stream)
+        b_.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        da.scan_begin = sev[i][0].cuda_event
+        da.scan_end = sev[i][1].cuda_event
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    da.scan_begin = None
+    da.scan_end = None
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    scan_ms = [a.elapsed_time(b) for a, b in sev]
+    total_ms = sum(step_ms)
+
+    # --- end to end through the C ABI with host buffers (pinned) ---
+    ne = max(20, min(K, 200))
+    hq_in = q.cpu().pin_memory()
+    hk_in, hv_in = knew.cpu().pin_memory(), vnew.cpu().pin_memory()
+    h_out = torch.empty_like(out, device="cpu").pin_memory()
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ne)]
+    for i in range(ne):
+        flush.fill_(i & 0xFF)
+        eev[i][0].record(stream)
+        q.copy_(hq_in, non_blocking=True)
+        knew.copy_(hk_in, non_blocking=True)
+        vnew.copy_(hv_in, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        eev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in eev)
+    h2d = hq_in.numel() * 2 + hk_in.numel() * 2 + hv_in.numel() * 2
+    d2h = h_out.numel() * 4
+
+    # max over ranks
+    t = torch.tensor([total_ms, e2e_ms, q_ms], dtype=torch.float64, device="cuda")
+    if ws > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms, e2e_ms, q_ms = t.tolist()
+    tokens_per_step = bsz * T
+    value = ws * tokens_per_step * K / (total_ms / 1e3)
+
+    peak, peak_kind = _peaks()
+    scan_alg = rows * T * ((w["k_bits"] - 1) * d // 8 + d // 8 + 4 + w["v_bits"] * d // 8 + 2) + bsz * hq * 2 * d * 4
+    scan_avg_s = statistics.mean(scan_ms) / 1e3
+    achieved = scan_alg / scan_avg_s / 1e9
+    q_achieved = q_alg_bytes / (q_ms / 1e3) / 1e9
+    res = None
+    if rank == 0:
+        res = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": n_warm,
+            "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w["name"], "batch": bsz, "hq": hq, "hkv": hkv, "d": d, "seq_len": T,
+                       "rotation": w["rotation"], "k_bits": w["k_bits"], "v_bits": w["v_bits"],
+                       "step": "append 1 token per KV head (quantize K and V) + decode attention over seq_len tokens",
+                       "l2": "flushed (256 MiB write) before every timed step", "parallelism": f"replicas x{ws}"},
+            "hbm_gbs": {"scan": achieved, "quantize": q_achieved},
+            "roofline": {"kernel": "decode_kernel (split-K scan)", "bound": "hbm", "achieved": achieved,
+                         "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind,
+                         "alg_bytes_per_launch": scan_alg, "avg_launch_us": scan_avg_s * 1e6,
+                         "traffic": _traffic("decode_scan", SCAN_SOURCES)},
+            "quantize": {"vectors_per_s": q_vectors / (q_ms / 1e3), "vectors_per_call": q_vectors,
+                         "workload": "cache fill: 8 KV heads x 32768 tokens, K (3-bit PROD) and V (3-bit MSE), bf16 in",
+                         "roofline": {"bound": "hbm", "achieved": q_achieved, "peak": peak, "unit": "GB/s",
+                                      "frac": q_achieved / peak, "alg_bytes_per_call": q_alg_bytes}},
+            "e2e": {"value": ws * tokens_per_step / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": ne},
+            "gpu_launches": launches_per_step * K,
+            "clocks": clocks,
+        }
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return res
+
+
+# ----------------------------------------------------- oracle (CPU) arm ----
+def oracle_sample(budget_s):
+    """Oracle decode steps on a sample: one KV head and its 4 query heads over
+    `tokens` cached tokens (plus the appended K/V quantize for that head),
+    extrapolated linearly to the full step (all KV heads, all tokens)."""
+    from oracle import attention as oa
+    from oracle import quantize as oq
+    from oracle import rng as orng
+    from oracle import rotation as orot
+    from online_kv_cache_quantize_gb300 import workloads as W
+
+    w = WORKLOAD
+    d, T, hkv, hq = w["d"], w["seq_len"], w["hkv"], w["hq"]
+    g = hq // hkv
+    pi = orot.make_rotation(W.ROT_SEED, d, w["rotation"])
+    s = orng.round_to_bf16(orng.normals(W.QJL_SEED, d * d).reshape(d, d))
+    k, v = W.decode_kv(1, 1, T)
+    k, v = k[0, 0].astype(np.float64), v[0, 0].astype(np.float64)
+    q = W.query_vectors((g, d), dtype="bf16").astype(np.float64)
+
+    caches = {}
+
+    def cache(tokens):  # the oracle's packed cache of the sample, built untimed
+        if tokens not in caches:
+            caches[tokens] = (oq.quantize(k[:tokens], pi, "prod", w["k_bits"], s),
+                              oq.quantize(v[:tokens], pi, "mse", w["v_bits"]))
+        return caches[tokens]
+
+    def one(tokens):
+        kq, vq = cache(tokens)
+        t0 = time.perf_counter()
+        # append: quantize the new token's K and V for this KV head
+        oq.quantize(k[tokens - 1:tokens], pi, "prod", w["k_bits"], s)
+        oq.quantize(v[tokens - 1:tokens], pi, "mse", w["v_bits"])
+        for h in range(g):
+            qp, u = oa.query_prep(q[h], pi, s)
+            lg = oa.key_logits(qp, u, kq["idx"], kq["norm16"], kq["centroids"], kq["rnorm16"], kq["z"], d)
+            sc = lg / np.sqrt(d)
+            p = np.exp(sc - sc.max())
+            p /= p.sum()
+            (p @ (vq["norm16"][:, None] * vq["centroids"][vq["idx"]])) @ pi
+        return time.perf_counter() - t0
+
+    probe = 2048
+    per_token = min(one(probe) for _ in range(3)) / probe
+    tokens = int(max(256, min(T, budget_s / max(per_token, 1e-9))))
+    return one, tokens, hkv
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return None
+    cores = len(os.sched_getaffinity(0))
+    total_budget = 120.0
+    per_step = total_budget / max(1, args.steps + args.warmup)
+    one, tokens, hkv = oracle_sample(per_step)
+    for _ in range(args.warmup):
+        one(tokens)
+    times = [one(tokens) for _ in range(args.steps)]
+    full_step_s = statistics.mean(times) * (WORKLOAD["seq_len"] / tokens) * hkv
+    value = WORKLOAD["batch"] * WORKLOAD["seq_len"] / full_step_s
+    sample = (f"1 of {hkv} KV heads x {tokens} of {WORKLOAD['seq_len']} tokens per step (K/V quantize + 4-head decode), "
+              f"extrapolated linearly to the full step")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": full_step_s * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD["name"], "batch": 1, "hq": WORKLOAD["hq"], "hkv": hkv, "d": 128,
+                       "seq_len": WORKLOAD["seq_len"], "rotation": WORKLOAD["rotation"]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def cpu_baseline_default():
+    """The oracle on a bounded sample (about 15 s), for the default run's line."""
+    cores = len(os.sched_getaffinity(0))
+    one, tokens, hkv = oracle_sample(3.0)
+    one(tokens)
+    times = [one(tokens) for _ in range(4)]
+    full_step_s = statistics.mean(times) * (WORKLOAD["seq_len"] / tokens) * hkv
+    return {"value": WORKLOAD["batch"] * WORKLOAD["seq_len"] / full_step_s, "unit": UNIT, "cores": cores,
+            "kind": "oracle",
+            "sample": f"4 steps of 1/{hkv} KV heads x {tokens} tokens (quantize + 4-head decode), extrapolated to the full step"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["tq", "reference"], default="tq")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        res = run_reference(args)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    ws, rank, _ = _dist()
+    res = run_tq(args)
+    if rank == 0 and res is not None:
+        if ws == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline_default()
+        else:
+            res["cpu_baseline"] = None
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,253 @@
+/*
+ * tq.h - C ABI of libtq, a GB300 (sm_103a) implementation of the TurboQuant
+ * hot path: quantize-on-append of KV head vectors and decode attention scored
+ * directly from the packed codes.
+ *
+ * Sources the operations follow (TurboQuant write-ups):
+ *   [Qiita]  Qiita TurboQuant article (the "3-bit KV cache" explainer)
+ *   [A2A]    A2A TurboQuant explainer "TurboQuant解説：実装方法とLLMメモリ6倍削減効果"
+ *   [DS]     DeepSignal TurboQuant ICLR 2026 article
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" must point to memory of the CUDA device that
+ *     is current on the calling thread; "host" pointers are ordinary memory.
+ *   - All buffers are owned by the caller. The library allocates device
+ *     memory only inside tq_rotation_to_device / tq_qjl_to_device (set-up);
+ *     the hot-path calls never allocate: scratch comes from the caller's
+ *     workspace argument.
+ *   - Hot-path calls are asynchronous on the given stream (NULL = legacy
+ *     default stream). Argument errors are found on the host before any
+ *     launch and return a status; a launch failure returns TQ_ERR_CUDA;
+ *     faults during execution surface at the caller's next synchronisation.
+ *   - No call blocks on the device and no kernel waits on a flag, so no call
+ *     can hang; TQ_ERR_TIMEOUT is reserved.
+ *   - tq_last_error() returns a thread-local message for the last failure.
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* tq_stream; /* same type as cudaStream_t */
+typedef struct CUevent_st* tq_event;   /* same type as cudaEvent_t  */
+
+typedef enum {
+    TQ_OK = 0,
+    TQ_ERR_INVALID_ARG = 1,  /* null pointer, bad size, mismatched handles   */
+    TQ_ERR_UNSUPPORTED = 2,  /* valid but not built: e.g. RHT with d not 2^k  */
+    TQ_ERR_ALIGNMENT = 3,    /* a device pointer or stride breaks alignment  */
+    TQ_ERR_CAPACITY = 4,     /* a slot range runs past the cache capacity    */
+    TQ_ERR_CUDA = 5,         /* a CUDA runtime call failed                   */
+    TQ_ERR_TIMEOUT = 6,      /* reserved                                     */
+    TQ_ERR_WORKSPACE = 7,    /* workspace missing or smaller than required   */
+    TQ_ERR_NO_DEVICE_COPY = 8 /* handle not uploaded with *_to_device        */
+} tq_status;
+
+typedef enum { TQ_ROT_DENSE_QR = 0, TQ_ROT_RHT = 1 } tq_rot_kind;
+typedef enum { TQ_MSE = 0, TQ_PROD = 1 } tq_mode;
+typedef enum { TQ_F32 = 0, TQ_BF16 = 1, TQ_F16 = 2 } tq_dtype;
+
+typedef struct tq_rotation tq_rotation;
+typedef struct tq_qjl tq_qjl;
+
+const char* tq_status_string(tq_status s);
+const char* tq_last_error(void);
+
+/* sizeof of a public struct by name ("tq_cache", "tq_quant_args",
+ * "tq_decode_args", "tq_topk_args"); 0 for an unknown name. Lets bindings
+ * check their struct mirrors against this build. */
+size_t tq_abi_struct_size(const char* name);
+
+/* ------------------------------------------------------------------------ *
+ * Set-up (host).                                                           *
+ * ------------------------------------------------------------------------ */
+
+/* The random stream every random draw of the library uses: SplitMix64
+ * (Steele, Lea & Flood 2014) in counter form, draw k = mix(seed + (k+1)*gamma).
+ * Writes draws start .. start+count-1 to host_out (host, count uint64).
+ * The pages only say the random matrices are generated mathematically once
+ * and cached ([Qiita] "Rotate, then quantize"; [DS] "QJL"). */
+tq_status tq_random_stream(uint64_t seed, uint64_t start, int64_t count, uint64_t* host_out);
+
+/* Data-independent random orthogonal rotation Pi (d x d), y = Pi x.
+ * [A2A] "Stage 1: random rotation": QR factorisation of a Gaussian matrix.
+ * [Qiita] "What you hit when you try it": Walsh-Hadamard approximation.
+ *   kind TQ_ROT_DENSE_QR: G = d*d standard normals (Box-Muller over the
+ *     stream, row-major), Householder QR G = QR, Pi = Q diag(sign(diag R)).
+ *     3 <= d <= 256.
+ *   kind TQ_ROT_RHT: Pi = H diag(s) / sqrt(d), H Sylvester Hadamard
+ *     (H_ij = (-1)^popcount(i&j)), s_i = -1 if bit 63 of draw i is set else
+ *     +1. d a power of two, 4 <= d <= 256 (else TQ_ERR_UNSUPPORTED).
+ * *out receives a host-side handle owned by the caller until
+ * tq_free_rotation. No device memory is touched. */
+tq_status tq_make_rotation(uint64_t seed, int d, int kind, tq_rotation** out);
+
+/* Copies Pi (fp64, d*d, row-major) to host_out (host, caller-owned). */
+tq_status tq_rotation_get(const tq_rotation* rot, double* host_out);
+
+/* *d, *kind receive the handle's size and kind (either may be NULL). */
+tq_status tq_rotation_info(const tq_rotation* rot, int* d, int* kind);
+
+/* Uploads the device copies (fp32 Pi and Pi^T, fp64 Pi, RHT signs) to the
+ * current device. Allocates device memory (set-up, not hot path). Calling it
+ * again is a no-op. Needed before any hot-path call that uses the handle. */
+tq_status tq_rotation_to_device(tq_rotation* rot);
+
+/* Frees host and device memory of the handle; NULL is accepted. */
+tq_status tq_free_rotation(tq_rotation* rot);
+
+/* QJL projection S (m x d) for the residual sign sketch.
+ * [Qiita] "One more stage so attention does not break"; [A2A] "Stage 2".
+ * Entries: standard normals (Box-Muller over the stream of `seed`,
+ * row-major) rounded to the nearest bfloat16, ties to even, so that the
+ * matrix is exact in bf16. 1 <= m <= 256, 3 <= d <= 256. */
+tq_status tq_make_qjl(uint64_t seed, int m, int d, tq_qjl** out);
+tq_status tq_qjl_get(const tq_qjl* qjl, double* host_out); /* m*d row-major */
+tq_status tq_qjl_to_device(tq_qjl* qjl);
+tq_status tq_free_qjl(tq_qjl* qjl);
+
+/* Lloyd-Max codebook of the post-rotation law Beta((d-1)/2,(d-1)/2) on
+ * [-1, 1] ([A2A] "Stage 1"; [Qiita] "Rotate, then quantize").
+ * centroids: host, 2^bits doubles, ascending; boundaries: host, 2^bits - 1
+ * doubles, t_j = (c_j + c_{j+1}) / 2. Exactly symmetric; middle boundary 0.
+ * 1 <= bits <= 4, 3 <= d <= 4096. Computed once per (d, bits), cached. */
+tq_status tq_codebook(int d, int bits, double* centroids, double* boundaries);
+
+/* ------------------------------------------------------------------------ *
+ * Packed cache layout (this library's specification; the pages give none). *
+ * ------------------------------------------------------------------------ *
+ * A cache holds `rows` rows (normally batch*Hkv) of `capacity` slots; slot
+ * s = row * capacity + t. Per slot, structure of arrays:
+ *   codes[s]: code bytes = ceil(cb * d / 8) rounded up to 16, where
+ *             cb = bits (TQ_MSE) or bits - 1 (TQ_PROD). Bit k of coordinate
+ *             i's index is stream bit cb*i + k; stream bit p is bit p%8 of
+ *             byte p/8 (LSB-first). Padding bits are 0.
+ *   signs[s]: (TQ_PROD) sign bytes = ceil(m / 8) rounded up to 16;
+ *             bit j (LSB-first) = [(S r)_j >= 0].
+ *   norm[s]:  fp16 bits of ||x|| (round to nearest even, saturated 65504).
+ *   rnorm[s]: (TQ_PROD) fp16 bits of ||r||, r = Pi x/||x|| - c[idx].
+ * All four plane pointers must be 16-byte aligned (norm/rnorm: 2-byte). */
+typedef struct {
+    int mode;         /* TQ_MSE (values) or TQ_PROD (keys)                   */
+    int bits;         /* MSE: 1..4 Lloyd-Max bits; PROD: 2..5 = (bits-1) + 1 */
+    int d;            /* head dimension                                      */
+    int m;            /* PROD: QJL rows; MSE: ignored                        */
+    int64_t rows;     /* rows in the cache                                   */
+    int64_t capacity; /* slots per row                                       */
+    uint8_t* codes;   /* device [rows*capacity][tq_code_bytes]               */
+    uint8_t* signs;   /* device [rows*capacity][tq_sign_bytes] (PROD)        */
+    uint16_t* norm;   /* device [rows*capacity] fp16 bits                    */
+    uint16_t* rnorm;  /* device [rows*capacity] fp16 bits (PROD)             */
+} tq_cache;
+
+int tq_code_bytes(int d, int code_bits); /* per-slot stride of codes, bytes */
+int tq_sign_bytes(int m);                /* per-slot stride of signs, bytes */
+
+/* ------------------------------------------------------------------------ *
+ * Quantize-on-append.                                                      *
+ * ------------------------------------------------------------------------ *
+ * For each input vector x: n = ||x||; y = Pi x / n (y = 0 if n = 0);
+ * idx_i = #{j : y_i >= t_j}; store codes and fp16(n). PROD mode also:
+ * r = y - c[idx], gamma = ||r||, z_j = [(S r)_j >= 0]; store signs and
+ * fp16(gamma). ([A2A] "Stage 1" and "Stage 2"; [Qiita] "Rotate, then
+ * quantize" and "One more stage so attention does not break".)
+ * Destination slot of vector i:
+ *   dst_slot != NULL  -> dst_slot[i] (device int64 [n]; slots outside
+ *                        [0, rows*capacity) are skipped);
+ *   else append_pos != NULL -> vector i = (b, h) with b = i / heads,
+ *                        h = i % heads, slot = i * capacity + append_pos[b]
+ *                        (device int32 [n / heads]; needs rows == n; a
+ *                        position outside [0, capacity) is skipped);
+ *   else              -> slot0 + i (checked on the host against the cache). */
+typedef struct {
+    tq_cache cache;
+    const tq_rotation* rot; /* uploaded; rot d == cache.d                     */
+    const tq_qjl* qjl;      /* PROD: uploaded, m == cache.m, d == cache.d     */
+    const void* x;          /* device [n][x_stride] of x_dtype                */
+    int x_dtype;            /* TQ_F32, TQ_BF16 or TQ_F16                      */
+    int64_t x_stride;       /* elements between vectors, >= d                 */
+    int64_t n;              /* vectors; 0 is a no-op                          */
+    const int64_t* dst_slot;
+    const int32_t* append_pos;
+    int heads;              /* append_pos mode: vectors per position entry    */
+    int64_t slot0;
+} tq_quant_args;
+
+tq_status tq_quantize_kv(const tq_quant_args* a, tq_stream stream);
+
+/* ------------------------------------------------------------------------ *
+ * Decode attention from the packed cache.                                  *
+ * ------------------------------------------------------------------------ *
+ * For batch b and query head h (KV head g = gqa_map[h]):
+ *   q' = Pi q, u = S q'                       (query rotated once)
+ *   l_t = n_t ( <q', cK[idx_t]> + sqrt(pi/2)/m * gamma_t <u, 2 z_t - 1> )
+ *   p = softmax(scale * l) over t < seq_lens[b]
+ *   a = sum_t p_t nV_t cV[idxV_t]  (rotated domain); out = Pi^T a
+ * ([A2A] end of "Stage 2" and "How to implement": pre-rotated query, dot
+ * products from the indices; softmax and value sum are this library's
+ * reading). A sequence with no visible token gives out = 0.
+ * Split-K over tokens: CTAs write partial (max, sum, a) to the workspace; a
+ * second launch merges them and un-rotates. */
+typedef struct {
+    const void* q;          /* device [batch][hq][d] of q_dtype               */
+    int q_dtype;            /* TQ_F32 or TQ_BF16                              */
+    int batch, hq, hkv, d;  /* d in {64, 128, 256}                            */
+    const int32_t* seq_lens;/* device int32 [batch], each in [0, capacity]    */
+    int max_seq_len;        /* host: upper bound of seq_lens (split plan)     */
+    const int32_t* gqa_map; /* HOST int32 [hq] in [0, hkv), or NULL = h/(hq/hkv);
+                               every KV head must serve the same number G of
+                               query heads, G in {1, 2, 4, 8}                 */
+    const tq_rotation* rot; /* uploaded                                       */
+    const tq_qjl* qjl;      /* uploaded, m == k.m                             */
+    tq_cache k;             /* PROD cache, rows == batch*hkv                  */
+    tq_cache v;             /* MSE cache, rows == batch*hkv                   */
+    float scale;            /* softmax scale; 0 -> 1/sqrt(d)                  */
+    int n_splits;           /* token splits per (b, KV head); 0 -> automatic  */
+    void* out;              /* device [batch][hq][d] of out_dtype             */
+    int out_dtype;          /* TQ_F32 or TQ_BF16                              */
+    float* logits;          /* optional device fp32 [batch][hq][max_seq_len]:
+                               raw l_t (before scale) for t < seq_lens[b]    */
+    tq_event scan_begin;    /* optional: recorded on `stream` right before and */
+    tq_event scan_end;      /* after the split-K scan kernel (for timing it)   */
+} tq_decode_args;
+
+/* Workspace bytes tq_attn_decode needs for these arguments (0 on error). */
+size_t tq_attn_decode_workspace(const tq_decode_args* a);
+
+/* workspace: device, >= tq_attn_decode_workspace(a) bytes, 256-byte aligned,
+ * not used by anything else until the call's work on `stream` completes. */
+tq_status tq_attn_decode(const tq_decode_args* a, void* workspace, size_t ws_bytes, tq_stream stream);
+
+/* ------------------------------------------------------------------------ *
+ * Inner-product search from the codes.                                     *
+ * ------------------------------------------------------------------------ *
+ * [A2A] "Benchmarks and real-world performance" (GloVe d = 200 top-k recall)
+ * and "Applications" (vector databases). Score of database row t for query
+ * q: the decode logit l_t above (PROD database; an MSE database drops the
+ * sign term). Returns per query the k largest scores, ties to the lower row
+ * id, sorted descending. */
+typedef struct {
+    const float* queries;   /* device fp32 [nq][d]                            */
+    int nq, d;
+    const tq_rotation* rot; /* uploaded                                       */
+    const tq_qjl* qjl;      /* uploaded when db.mode == TQ_PROD               */
+    tq_cache db;            /* rows == 1, capacity >= n_db                    */
+    int64_t n_db;
+    int k;                  /* 1..32                                          */
+    int32_t* ids;           /* device int32 [nq][k]                           */
+    float* scores;          /* device fp32 [nq][k]                            */
+} tq_topk_args;
+
+size_t tq_score_topk_workspace(const tq_topk_args* a);
+tq_status tq_score_topk(const tq_topk_args* a, void* workspace, size_t ws_bytes, tq_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H */

@@ -1,0 +1,487 @@
+// C entry points of libtq that touch the GPU: device uploads of the set-up
+// handles, argument validation and the launches of the hot path.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "tq_internal.h"
+#include "tq_launch.h"
+
+namespace tqk {
+cudaError_t launch_quantize_dense(const QuantParams& p, int dtype, int vpl, int prod, int cb, cudaStream_t s);
+cudaError_t launch_quantize_rht(const QuantParams& p, int dtype, int vpl, int prod, int cb, cudaStream_t s);
+}  // namespace tqk
+
+namespace {
+
+using tq::fail;
+
+template <typename T>
+tq_status upload(T** dst, const std::vector<T>& host) {
+    if (cudaMalloc((void**)dst, host.size() * sizeof(T)) != cudaSuccess)
+        return fail(TQ_ERR_CUDA, "cudaMalloc failed while uploading a handle");
+    if (cudaMemcpy(*dst, host.data(), host.size() * sizeof(T), cudaMemcpyHostToDevice) != cudaSuccess)
+        return fail(TQ_ERR_CUDA, "cudaMemcpy failed while uploading a handle");
+    return TQ_OK;
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+tq_status check_rot(const tq_rotation* rot, int d) {
+    if (!rot) return fail(TQ_ERR_INVALID_ARG, "rotation handle is NULL");
+    if (rot->d != d) return fail(TQ_ERR_INVALID_ARG, "rotation d does not match");
+    int dev = -1;
+    cudaGetDevice(&dev);
+    if (rot->device < 0 || !rot->d_pi32) return fail(TQ_ERR_NO_DEVICE_COPY, "rotation not uploaded (tq_rotation_to_device)");
+    if (rot->device != dev) return fail(TQ_ERR_INVALID_ARG, "rotation uploaded to another device");
+    return TQ_OK;
+}
+
+tq_status check_qjl(const tq_qjl* q, int m, int d) {
+    if (!q) return fail(TQ_ERR_INVALID_ARG, "QJL handle is NULL");
+    if (q->d != d || q->m != m) return fail(TQ_ERR_INVALID_ARG, "QJL m/d does not match the cache");
+    int dev = -1;
+    cudaGetDevice(&dev);
+    if (q->device < 0 || !q->d_st32) return fail(TQ_ERR_NO_DEVICE_COPY, "QJL not uploaded (tq_qjl_to_device)");
+    if (q->device != dev) return fail(TQ_ERR_INVALID_ARG, "QJL uploaded to another device");
+    return TQ_OK;
+}
+
+// Validates a cache descriptor; returns the code bits per coordinate.
+tq_status check_cache(const tq_cache& c, const char* what, int* code_bits) {
+    std::string w(what);
+    if (c.mode != TQ_MSE && c.mode != TQ_PROD) return fail(TQ_ERR_INVALID_ARG, w + ": mode must be TQ_MSE or TQ_PROD");
+    if (c.mode == TQ_MSE && (c.bits < 1 || c.bits > 4)) return fail(TQ_ERR_UNSUPPORTED, w + ": MSE bits must be 1..4");
+    if (c.mode == TQ_PROD && (c.bits < 2 || c.bits > 5)) return fail(TQ_ERR_UNSUPPORTED, w + ": PROD bits must be 2..5");
+    if (c.d < 3 || c.d > 256) return fail(TQ_ERR_UNSUPPORTED, w + ": d must be 3..256");
+    if (c.rows < 0 || c.capacity < 0) return fail(TQ_ERR_INVALID_ARG, w + ": negative rows/capacity");
+    if (!c.codes || !c.norm) return fail(TQ_ERR_INVALID_ARG, w + ": codes/norm plane is NULL");
+    if (!aligned(c.codes, 16) || !aligned(c.norm, 2)) return fail(TQ_ERR_ALIGNMENT, w + ": codes must be 16-byte aligned, norm 2-byte");
+    if (c.mode == TQ_PROD) {
+        if (c.m < 1 || c.m > 256) return fail(TQ_ERR_UNSUPPORTED, w + ": m must be 1..256");
+        if (!c.signs || !c.rnorm) return fail(TQ_ERR_INVALID_ARG, w + ": signs/rnorm plane is NULL");
+        if (!aligned(c.signs, 16) || !aligned(c.rnorm, 2)) return fail(TQ_ERR_ALIGNMENT, w + ": signs must be 16-byte aligned, rnorm 2-byte");
+    }
+    *code_bits = c.mode == TQ_PROD ? c.bits - 1 : c.bits;
+    return TQ_OK;
+}
+
+tq_status fill_codebook(int d, int cb, tqk::Codebook* out) {
+    std::vector<double> c, t;
+    tq_status s = tq::codebook(d, cb, c, t);
+    if (s != TQ_OK) return s;
+    std::memset(out, 0, sizeof(*out));
+    out->levels = (int)c.size();
+    for (size_t i = 0; i < c.size(); ++i) out->c[i] = (float)c[i];
+    for (size_t i = 0; i < t.size(); ++i) {
+        out->t[i] = (float)t[i];
+        out->t64[i] = t[i];
+    }
+    for (size_t i = t.size(); i < (size_t)tqk::kMaxLevels - 1; ++i) {
+        out->t[i] = 3.0e38f;
+        out->t64[i] = 1e300;
+    }
+    return TQ_OK;
+}
+
+int vpl_for(int d) {
+    if (d <= 64) return 2;
+    if (d <= 128) return 4;
+    if (d <= 224) return 7;
+    return 8;
+}
+
+tq_status cuda_status(cudaError_t e, const char* where) {
+    if (e == cudaSuccess) return TQ_OK;
+    return fail(TQ_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct DecodePlan {
+    int n_splits = 1, chunk = 1, group = 1;
+    size_t off_q = 0, off_u = 0, off_part = 0, total = 0;
+};
+
+tq_status plan_decode(const tq_decode_args* a, DecodePlan* pl) {
+    if (!a) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: args are NULL");
+    if (a->batch < 1 || a->hq < 1 || a->hkv < 1) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: batch/hq/hkv must be >= 1");
+    if (a->d != 128) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: d must be 128");
+    if (a->hq > 256) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: hq must be <= 256");
+    if (a->max_seq_len < 0) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: max_seq_len < 0");
+    if (a->hq % a->hkv) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: hq must be a multiple of hkv");
+    int g = a->hq / a->hkv;
+    if (g != 1 && g != 2 && g != 4 && g != 8) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: group size must be 1, 2, 4 or 8");
+    pl->group = g;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int L = a->max_seq_len > 0 ? a->max_seq_len : 1;
+    int splits = a->n_splits;
+    if (splits <= 0) {
+        long long units = (long long)a->batch * a->hkv;
+        long long want = ((long long)sms * 8 + units - 1) / units;
+        int chunk = (int)((L + want - 1) / want);
+        chunk = std::max(64, (chunk + 31) / 32 * 32);
+        splits = (L + chunk - 1) / chunk;
+    }
+    if (splits < 1) splits = 1;
+    if (splits > 65535) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: too many splits");
+    pl->n_splits = splits;
+    pl->chunk = (L + splits - 1) / splits;
+    const size_t rows = (size_t)a->batch * a->hq;
+    pl->off_q = 0;
+    pl->off_u = round_up(rows * a->d * sizeof(float), 256);
+    pl->off_part = pl->off_u + round_up(rows * 128 * sizeof(float), 256);
+    pl->total = pl->off_part + round_up(rows * (size_t)splits * (a->d + 2) * sizeof(float), 256);
+    return TQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+tq_status tq_rotation_to_device(tq_rotation* rot) {
+    if (!rot) return fail(TQ_ERR_INVALID_ARG, "tq_rotation_to_device: NULL handle");
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return fail(TQ_ERR_CUDA, "tq_rotation_to_device: no CUDA device");
+    if (rot->device == dev && rot->d_pi32) return TQ_OK;
+    if (rot->device >= 0) return fail(TQ_ERR_INVALID_ARG, "tq_rotation_to_device: already on another device");
+    const int d = rot->d;
+    std::vector<float> pi32((size_t)d * d), pit32((size_t)d * d);
+    for (int i = 0; i < d; ++i)
+        for (int j = 0; j < d; ++j) {
+            pi32[(size_t)i * d + j] = (float)rot->pi[(size_t)i * d + j];
+            pit32[(size_t)j * d + i] = (float)rot->pi[(size_t)i * d + j];
+        }
+    std::vector<float> sg(d, 1.0f);
+    for (int i = 0; i < d && i < (int)rot->signs.size(); ++i) sg[i] = (float)rot->signs[i];
+    tq_status s;
+    if ((s = upload(&rot->d_pi32, pi32)) != TQ_OK) return s;
+    if ((s = upload(&rot->d_pit32, pit32)) != TQ_OK) return s;
+    if ((s = upload(&rot->d_pi64, rot->pi)) != TQ_OK) return s;
+    if ((s = upload(&rot->d_sign, sg)) != TQ_OK) return s;
+    rot->device = dev;
+    return TQ_OK;
+}
+
+tq_status tq_free_rotation(tq_rotation* rot) {
+    if (!rot) return TQ_OK;
+    if (rot->device >= 0) {
+        int cur = -1;
+        cudaGetDevice(&cur);
+        cudaSetDevice(rot->device);
+        cudaFree(rot->d_pi32);
+        cudaFree(rot->d_pit32);
+        cudaFree(rot->d_pi64);
+        cudaFree(rot->d_sign);
+        if (cur >= 0) cudaSetDevice(cur);
+    }
+    delete rot;
+    return TQ_OK;
+}
+
+tq_status tq_qjl_to_device(tq_qjl* q) {
+    if (!q) return fail(TQ_ERR_INVALID_ARG, "tq_qjl_to_device: NULL handle");
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return fail(TQ_ERR_CUDA, "tq_qjl_to_device: no CUDA device");
+    if (q->device == dev && q->d_st32) return TQ_OK;
+    if (q->device >= 0) return fail(TQ_ERR_INVALID_ARG, "tq_qjl_to_device: already on another device");
+    const int m = q->m, d = q->d;
+    std::vector<float> st((size_t)d * m), s32((size_t)m * d);
+    for (int j = 0; j < m; ++j)
+        for (int i = 0; i < d; ++i) {
+            st[(size_t)i * m + j] = (float)q->s[(size_t)j * d + i];
+            s32[(size_t)j * d + i] = (float)q->s[(size_t)j * d + i];
+        }
+    tq_status s;
+    if ((s = upload(&q->d_st32, st)) != TQ_OK) return s;
+    if ((s = upload(&q->d_s32, s32)) != TQ_OK) return s;
+    q->device = dev;
+    return TQ_OK;
+}
+
+tq_status tq_free_qjl(tq_qjl* q) {
+    if (!q) return TQ_OK;
+    if (q->device >= 0) {
+        int cur = -1;
+        cudaGetDevice(&cur);
+        cudaSetDevice(q->device);
+        cudaFree(q->d_st32);
+        cudaFree(q->d_s32);
+        if (cur >= 0) cudaSetDevice(cur);
+    }
+    delete q;
+    return TQ_OK;
+}
+
+tq_status tq_quantize_kv(const tq_quant_args* a, tq_stream stream) {
+    if (!a) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_kv: args are NULL");
+    int cb = 0;
+    tq_status s = check_cache(a->cache, "tq_quantize_kv cache", &cb);
+    if (s != TQ_OK) return s;
+    const tq_cache& c = a->cache;
+    if ((s = check_rot(a->rot, c.d)) != TQ_OK) return s;
+    const bool prod = c.mode == TQ_PROD;
+    if (prod && (s = check_qjl(a->qjl, c.m, c.d)) != TQ_OK) return s;
+    if (a->n < 0) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_kv: n < 0");
+    if (a->n == 0) return TQ_OK;
+    if (!a->x) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_kv: x is NULL");
+    if (a->x_dtype != TQ_F32 && a->x_dtype != TQ_BF16) return fail(TQ_ERR_UNSUPPORTED, "tq_quantize_kv: x_dtype must be TQ_F32 or TQ_BF16");
+    const size_t esz = a->x_dtype == TQ_F32 ? 4 : 2;
+    if (!aligned(a->x, esz)) return fail(TQ_ERR_ALIGNMENT, "tq_quantize_kv: x misaligned for its dtype");
+    if (a->x_stride < c.d) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_kv: x_stride < d");
+    const int64_t total = c.rows * c.capacity;
+    if (a->dst_slot) {
+        if (!aligned(a->dst_slot, 8)) return fail(TQ_ERR_ALIGNMENT, "tq_quantize_kv: dst_slot misaligned");
+    } else if (a->append_pos) {
+        if (a->heads < 1 || a->n % a->heads) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_kv: n must be a multiple of heads");
+        if (a->n != c.rows) return fail(TQ_ERR_CAPACITY, "tq_quantize_kv: append mode needs n == cache rows");
+    } else {
+        if (a->slot0 < 0 || a->slot0 + a->n > total) return fail(TQ_ERR_CAPACITY, "tq_quantize_kv: slot0 + n exceeds rows*capacity");
+    }
+    const bool rht = a->rot->kind == TQ_ROT_RHT;
+    if (rht && c.d != 64 && c.d != 128 && c.d != 256) return fail(TQ_ERR_UNSUPPORTED, "tq_quantize_kv: RHT kernels need d in {64, 128, 256}");
+    if (prod && c.m > 32 * vpl_for(c.d)) return fail(TQ_ERR_UNSUPPORTED, "tq_quantize_kv: m must be <= d rounded up to the kernel width");
+
+    tqk::QuantParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.x = a->x;
+    p.x_stride = a->x_stride;
+    p.n = a->n;
+    p.dst_slot = a->dst_slot;
+    p.append_pos = a->append_pos;
+    p.heads = a->heads;
+    p.slot0 = a->slot0;
+    p.total_slots = total;
+    p.capacity = c.capacity;
+    p.codes = c.codes;
+    p.code_stride = tq_code_bytes(c.d, cb);
+    p.signs = c.signs;
+    p.sign_stride = prod ? tq_sign_bytes(c.m) : 0;
+    p.norm = c.norm;
+    p.rnorm = c.rnorm;
+    p.pit32 = a->rot->d_pit32;
+    p.pi64 = a->rot->d_pi64;
+    p.sgn = a->rot->d_sign;
+    p.st32 = prod ? a->qjl->d_st32 : nullptr;
+    p.d = c.d;
+    p.m = prod ? c.m : 0;
+    p.inv_sqrt_d = (float)(1.0 / std::sqrt((double)c.d));
+    p.guard = rht ? 1.0e-6f : (float)(3.0e-8 * c.d);
+    if ((s = fill_codebook(c.d, cb, &p.cb)) != TQ_OK) return s;
+    const int dtype = a->x_dtype == TQ_F32 ? 0 : 1;
+    const int vpl = vpl_for(c.d);
+    cudaError_t e = rht ? tqk::launch_quantize_rht(p, dtype, vpl, prod ? 1 : 0, cb, (cudaStream_t)stream)
+                        : tqk::launch_quantize_dense(p, dtype, vpl, prod ? 1 : 0, cb, (cudaStream_t)stream);
+    return cuda_status(e, "tq_quantize_kv launch");
+}
+
+size_t tq_attn_decode_workspace(const tq_decode_args* a) {
+    DecodePlan pl;
+    if (plan_decode(a, &pl) != TQ_OK) return 0;
+    return pl.total;
+}
+
+tq_status tq_attn_decode(const tq_decode_args* a, void* workspace, size_t ws_bytes, tq_stream stream) {
+    DecodePlan pl;
+    tq_status s = plan_decode(a, &pl);
+    if (s != TQ_OK) return s;
+    int kb = 0, vb = 0;
+    if ((s = check_cache(a->k, "tq_attn_decode k", &kb)) != TQ_OK) return s;
+    if ((s = check_cache(a->v, "tq_attn_decode v", &vb)) != TQ_OK) return s;
+    if (a->k.mode != TQ_PROD || a->v.mode != TQ_MSE) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: keys must be PROD and values MSE");
+    if (a->k.d != a->d || a->v.d != a->d) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: cache d does not match");
+    if (a->k.m != 128) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: m must be 128");
+    const int64_t rows = (int64_t)a->batch * a->hkv;
+    if (a->k.rows != rows || a->v.rows != rows) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: cache rows must be batch*hkv");
+    if (a->k.capacity != a->v.capacity) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: k and v capacity differ");
+    if (a->max_seq_len > a->k.capacity) return fail(TQ_ERR_CAPACITY, "tq_attn_decode: max_seq_len exceeds the capacity");
+    if ((s = check_rot(a->rot, a->d)) != TQ_OK) return s;
+    if ((s = check_qjl(a->qjl, a->k.m, a->d)) != TQ_OK) return s;
+    if (!a->q || !a->out || !a->seq_lens) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: q/out/seq_lens is NULL");
+    if (a->q_dtype != TQ_F32 && a->q_dtype != TQ_BF16) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: q_dtype must be F32 or BF16");
+    if (a->out_dtype != TQ_F32 && a->out_dtype != TQ_BF16) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: out_dtype must be F32 or BF16");
+    if (!workspace || ws_bytes < pl.total) return fail(TQ_ERR_WORKSPACE, "tq_attn_decode: workspace missing or too small");
+    if (!aligned(workspace, 256)) return fail(TQ_ERR_ALIGNMENT, "tq_attn_decode: workspace must be 256-byte aligned");
+
+    tqk::DecodeParams dp;
+    std::memset(&dp, 0, sizeof(dp));
+    if (a->gqa_map) {
+        std::vector<int> count(a->hkv, 0);
+        for (int h = 0; h < a->hq; ++h) {
+            int g = a->gqa_map[h];
+            if (g < 0 || g >= a->hkv) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: gqa_map entry out of range");
+            if (count[g] >= pl.group) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: every KV head must serve hq/hkv query heads");
+            dp.head_table[g * pl.group + count[g]++] = (int16_t)h;
+        }
+        dp.use_table = 1;
+    }
+    char* ws = (char*)workspace;
+    float* qprime = (float*)(ws + pl.off_q);
+    float* u = (float*)(ws + pl.off_u);
+    float* part = (float*)(ws + pl.off_part);
+    cudaStream_t st = (cudaStream_t)stream;
+
+    tqk::PrepParams pp;
+    std::memset(&pp, 0, sizeof(pp));
+    pp.q = a->q;
+    pp.q_dtype = a->q_dtype == TQ_BF16 ? 1 : 0;
+    pp.rows = (int64_t)a->batch * a->hq;
+    pp.d = a->d;
+    pp.m = a->k.m;
+    pp.pit32 = a->rot->d_pit32;
+    pp.sgn = a->rot->d_sign;
+    pp.rht = a->rot->kind == TQ_ROT_RHT;
+    pp.inv_sqrt_d = (float)(1.0 / std::sqrt((double)a->d));
+    pp.st32 = a->qjl->d_st32;
+    pp.qprime = qprime;
+    pp.u = u;
+    cudaError_t e = tqk::launch_query_prep(pp, st);
+    if (e != cudaSuccess) return cuda_status(e, "tq_attn_decode query prep");
+
+    std::vector<double> kc, kt, vc, vt;
+    if ((s = tq::codebook(a->d, kb, kc, kt)) != TQ_OK) return s;
+    if ((s = tq::codebook(a->d, vb, vc, vt)) != TQ_OK) return s;
+    dp.qprime = qprime;
+    dp.u = u;
+    dp.batch = a->batch;
+    dp.hq = a->hq;
+    dp.hkv = a->hkv;
+    dp.d = a->d;
+    dp.m = a->k.m;
+    dp.group = pl.group;
+    dp.seq_lens = a->seq_lens;
+    dp.capacity = a->k.capacity;
+    dp.kcodes = a->k.codes;
+    dp.kcode_stride = tq_code_bytes(a->d, kb);
+    dp.ksigns = a->k.signs;
+    dp.ksign_stride = tq_sign_bytes(a->k.m);
+    dp.knorm = a->k.norm;
+    dp.krnorm = a->k.rnorm;
+    dp.vcodes = a->v.codes;
+    dp.vcode_stride = tq_code_bytes(a->d, vb);
+    dp.vnorm = a->v.norm;
+    for (size_t i = 0; i < kc.size(); ++i) dp.kc[i] = (float)kc[i];
+    for (size_t i = 0; i < vc.size(); ++i) dp.vc[i] = (float)vc[i];
+    dp.qjl_scale = (float)(std::sqrt(M_PI / 2.0) / a->k.m);
+    const double scale = a->scale != 0.0f ? (double)a->scale : 1.0 / std::sqrt((double)a->d);
+    dp.scale_log2 = (float)(scale * 1.4426950408889634);
+    dp.n_splits = pl.n_splits;
+    dp.chunk = pl.chunk;
+    dp.partial = part;
+    dp.logits = a->logits;
+    dp.max_seq_len = a->max_seq_len;
+    if (a->scan_begin && (e = cudaEventRecord((cudaEvent_t)a->scan_begin, st)) != cudaSuccess)
+        return cuda_status(e, "tq_attn_decode scan_begin");
+    e = tqk::launch_decode(dp, kb, vb, st);
+    if (e != cudaSuccess) return cuda_status(e, "tq_attn_decode scan");
+    if (a->scan_end && (e = cudaEventRecord((cudaEvent_t)a->scan_end, st)) != cudaSuccess)
+        return cuda_status(e, "tq_attn_decode scan_end");
+
+    tqk::CombineParams cp;
+    std::memset(&cp, 0, sizeof(cp));
+    cp.partial = part;
+    cp.rows = a->batch * a->hq;
+    cp.d = a->d;
+    cp.n_splits = pl.n_splits;
+    cp.pi32 = a->rot->d_pi32;
+    cp.sgn = a->rot->d_sign;
+    cp.rht = a->rot->kind == TQ_ROT_RHT;
+    cp.inv_sqrt_d = (float)(1.0 / std::sqrt((double)a->d));
+    cp.out = a->out;
+    cp.out_dtype = a->out_dtype == TQ_BF16 ? 1 : 0;
+    e = tqk::launch_combine(cp, st);
+    return cuda_status(e, "tq_attn_decode combine");
+}
+
+size_t tq_score_topk_workspace(const tq_topk_args* a) {
+    if (!a || a->nq < 0 || a->k < 1 || a->k > 32 || a->d < 3 || a->d > 256 || a->n_db < 0) return 0;
+    const int m = a->db.mode == TQ_PROD ? a->db.m : 0;
+    const int64_t chunk_rows = 4096;
+    const int64_t n_chunks = std::max<int64_t>(1, (a->n_db + chunk_rows - 1) / chunk_rows);
+    size_t q = round_up((size_t)a->nq * a->d * 4, 256);
+    size_t u = round_up((size_t)a->nq * std::max(m, 1) * 4, 256);
+    size_t cs = round_up((size_t)a->nq * n_chunks * a->k * 4, 256);
+    return q + u + 2 * cs;
+}
+
+tq_status tq_score_topk(const tq_topk_args* a, void* workspace, size_t ws_bytes, tq_stream stream) {
+    if (!a) return fail(TQ_ERR_INVALID_ARG, "tq_score_topk: args are NULL");
+    if (a->k < 1 || a->k > 32) return fail(TQ_ERR_UNSUPPORTED, "tq_score_topk: k must be 1..32");
+    if (a->nq < 0 || a->n_db < 0) return fail(TQ_ERR_INVALID_ARG, "tq_score_topk: negative sizes");
+    int cb = 0;
+    tq_status s = check_cache(a->db, "tq_score_topk db", &cb);
+    if (s != TQ_OK) return s;
+    if (a->db.d != a->d) return fail(TQ_ERR_INVALID_ARG, "tq_score_topk: db d does not match");
+    if (a->n_db > a->db.rows * a->db.capacity) return fail(TQ_ERR_CAPACITY, "tq_score_topk: n_db exceeds the db planes");
+    if (a->n_db > 0x7ffffffe) return fail(TQ_ERR_UNSUPPORTED, "tq_score_topk: n_db must fit int32 ids");
+    const bool prod = a->db.mode == TQ_PROD;
+    if ((s = check_rot(a->rot, a->d)) != TQ_OK) return s;
+    if (prod && (s = check_qjl(a->qjl, a->db.m, a->d)) != TQ_OK) return s;
+    if (prod && a->db.m > 32 * vpl_for(a->d)) return fail(TQ_ERR_UNSUPPORTED, "tq_score_topk: m too large for d");
+    if (a->nq == 0) return TQ_OK;
+    if (!a->queries || !a->ids || !a->scores) return fail(TQ_ERR_INVALID_ARG, "tq_score_topk: NULL buffer");
+    if (a->n_db < a->k) return fail(TQ_ERR_INVALID_ARG, "tq_score_topk: n_db < k");
+    size_t need = tq_score_topk_workspace(a);
+    if (!workspace || ws_bytes < need) return fail(TQ_ERR_WORKSPACE, "tq_score_topk: workspace missing or too small");
+    if (!aligned(workspace, 256)) return fail(TQ_ERR_ALIGNMENT, "tq_score_topk: workspace must be 256-byte aligned");
+    const int m = prod ? a->db.m : 0;
+    const int64_t chunk_rows = 4096;
+    const int64_t n_chunks = std::max<int64_t>(1, (a->n_db + chunk_rows - 1) / chunk_rows);
+    char* ws = (char*)workspace;
+    size_t off_u = round_up((size_t)a->nq * a->d * 4, 256);
+    size_t off_cs = off_u + round_up((size_t)a->nq * std::max(m, 1) * 4, 256);
+    size_t off_ci = off_cs + round_up((size_t)a->nq * n_chunks * a->k * 4, 256);
+    cudaStream_t st = (cudaStream_t)stream;
+
+    tqk::PrepParams pp;
+    std::memset(&pp, 0, sizeof(pp));
+    pp.q = a->queries;
+    pp.q_dtype = 0;
+    pp.rows = a->nq;
+    pp.d = a->d;
+    pp.m = m;
+    pp.pit32 = a->rot->d_pit32;
+    pp.sgn = a->rot->d_sign;
+    pp.rht = a->rot->kind == TQ_ROT_RHT;
+    pp.inv_sqrt_d = (float)(1.0 / std::sqrt((double)a->d));
+    pp.st32 = prod ? a->qjl->d_st32 : nullptr;
+    pp.qprime = (float*)ws;
+    pp.u = prod ? (float*)(ws + off_u) : nullptr;
+    cudaError_t e = tqk::launch_query_prep(pp, st);
+    if (e != cudaSuccess) return cuda_status(e, "tq_score_topk query prep");
+
+    tqk::TopkParams tp;
+    std::memset(&tp, 0, sizeof(tp));
+    std::vector<double> c, t;
+    if ((s = tq::codebook(a->d, cb, c, t)) != TQ_OK) return s;
+    for (size_t i = 0; i < c.size(); ++i) tp.c[i] = (float)c[i];
+    tp.qprime = (float*)ws;
+    tp.u = pp.u;
+    tp.nq = a->nq;
+    tp.d = a->d;
+    tp.m = m;
+    tp.codes = a->db.codes;
+    tp.code_stride = tq_code_bytes(a->d, cb);
+    tp.signs = a->db.signs;
+    tp.sign_stride = prod ? tq_sign_bytes(m) : 0;
+    tp.norm = a->db.norm;
+    tp.rnorm = a->db.rnorm;
+    tp.n_db = a->n_db;
+    tp.qjl_scale = prod ? (float)(std::sqrt(M_PI / 2.0) / m) : 0.0f;
+    tp.k = a->k;
+    tp.n_chunks = (int)n_chunks;
+    tp.chunk_rows = chunk_rows;
+    tp.cand_score = (float*)(ws + off_cs);
+    tp.cand_id = (int32_t*)(ws + off_ci);
+    tp.ids = a->ids;
+    tp.scores = a->scores;
+    e = tqk::launch_topk(tp, cb, prod ? 1 : 0, st);
+    return cuda_status(e, "tq_score_topk");
+}
+
+}  // extern "C"

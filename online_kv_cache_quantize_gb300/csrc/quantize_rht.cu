@@ -1,0 +1,23 @@
+// Quantize-on-append, randomized Walsh-Hadamard rotation instantiations.
+#include "quantize.cuh"
+
+namespace tqk {
+
+cudaError_t launch_quantize_rht(const QuantParams& p, int dtype, int vpl, int prod, int cb, cudaStream_t s) {
+    if (dtype == 0) {
+        switch (vpl) {
+            case 2: return launch_quantize_t<float, 2, true>(p, prod, cb, s);
+            case 4: return launch_quantize_t<float, 4, true>(p, prod, cb, s);
+            case 8: return launch_quantize_t<float, 8, true>(p, prod, cb, s);
+        }
+    } else {
+        switch (vpl) {
+            case 2: return launch_quantize_t<__nv_bfloat16, 2, true>(p, prod, cb, s);
+            case 4: return launch_quantize_t<__nv_bfloat16, 4, true>(p, prod, cb, s);
+            case 8: return launch_quantize_t<__nv_bfloat16, 8, true>(p, prod, cb, s);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace tqk

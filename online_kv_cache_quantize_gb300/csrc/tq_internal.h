@@ -1,0 +1,47 @@
+// Internal declarations shared by the host set-up code and the CUDA sources
+// of libtq. Not part of the public ABI (include/tq.h is).
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/tq.h"
+
+struct tq_rotation {
+    int d = 0;
+    int kind = 0;
+    uint64_t seed = 0;
+    std::vector<double> pi;     // d*d row-major, y = Pi x
+    std::vector<double> signs;  // RHT sign layer (d), empty for dense
+    int device = -1;            // device holding the copies, -1 = none
+    float* d_pi32 = nullptr;    // Pi row-major fp32
+    float* d_pit32 = nullptr;   // Pi^T row-major fp32 (PT[j][i] = Pi_ij)
+    double* d_pi64 = nullptr;   // Pi row-major fp64 (exact re-decision path)
+    float* d_sign = nullptr;    // RHT signs fp32 (d)
+};
+
+struct tq_qjl {
+    int m = 0;
+    int d = 0;
+    uint64_t seed = 0;
+    std::vector<double> s;      // m*d row-major, bf16-exact values
+    int device = -1;
+    float* d_st32 = nullptr;    // S^T row-major fp32 (ST[i][j] = S_ji), [d][m]
+    float* d_s32 = nullptr;     // S row-major fp32 [m][d]
+};
+
+namespace tq {
+
+// host set-up math (host.cpp)
+uint64_t splitmix64_at(uint64_t seed, uint64_t k);  // draw k (0-based)
+void gaussians(uint64_t seed, int64_t count, double* out);
+double round_bf16(double x);
+void householder_haar(const double* g, int d, double* pi_out);  // Pi = Q diag(sign diag R)
+tq_status codebook(int d, int bits, std::vector<double>& c, std::vector<double>& t);
+
+// thread-local error message
+tq_status fail(tq_status s, const std::string& msg);
+void clear_error();
+
+}  // namespace tq

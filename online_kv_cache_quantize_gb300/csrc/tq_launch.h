@@ -1,0 +1,129 @@
+// Kernel parameter blocks and launchers of libtq (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tqk {
+
+constexpr int kMaxLevels = 16;  // 2^4 Lloyd-Max cells
+
+// Codebook passed by value in the kernel parameter space: no device buffer.
+struct Codebook {
+    float c[kMaxLevels];
+    float t[kMaxLevels - 1];
+    double t64[kMaxLevels - 1];
+    int levels;
+};
+
+struct QuantParams {
+    const void* x;
+    int64_t x_stride;
+    int64_t n;
+    const int64_t* dst_slot;
+    const int32_t* append_pos;
+    int heads;
+    int64_t slot0;
+    int64_t total_slots;
+    int64_t capacity;
+    uint8_t* codes;
+    int code_stride;
+    uint8_t* signs;
+    int sign_stride;
+    uint16_t* norm;
+    uint16_t* rnorm;
+    const float* pit32;   // dense: Pi^T [d][d]
+    const double* pi64;   // Pi [d][d] fp64
+    const float* sgn;     // RHT signs [d]
+    const float* st32;    // S^T [d][m]
+    int d, m;
+    float inv_sqrt_d;
+    float guard;          // |y - t_j| below this is re-decided in fp64
+    Codebook cb;
+};
+
+// dtype: 0 f32, 1 bf16, 2 f16. rht: 0 dense, 1 RHT. prod: 0 MSE, 1 PROD.
+cudaError_t launch_quantize(const QuantParams& p, int dtype, int rht, int prod, int code_bits,
+                            cudaStream_t s);
+
+struct PrepParams {
+    const void* q;        // [rows][d]
+    int q_dtype;          // 0 f32, 1 bf16
+    int64_t rows;
+    int d, m;
+    const float* pit32;   // dense Pi^T [d][d]
+    const float* sgn;     // RHT signs
+    int rht;
+    float inv_sqrt_d;
+    const float* st32;    // S^T [d][m] or NULL (no u)
+    float* qprime;        // [rows][d]
+    float* u;             // [rows][m] or NULL
+};
+
+cudaError_t launch_query_prep(const PrepParams& p, cudaStream_t s);
+
+struct DecodeParams {
+    const float* qprime;  // [B*Hq][d]
+    const float* u;       // [B*Hq][m]
+    int batch, hq, hkv, d, m, group;
+    const int32_t* seq_lens;
+    const int16_t* heads_of_kv;  // nullptr -> kv*G + j; else HOST-built table in params
+    int16_t head_table[256];     // heads_of_kv table by value: [hkv][G]
+    int use_table;
+    int64_t capacity;
+    const uint8_t* kcodes; int kcode_stride;
+    const uint8_t* ksigns; int ksign_stride;
+    const uint16_t* knorm;
+    const uint16_t* krnorm;
+    const uint8_t* vcodes; int vcode_stride;
+    const uint16_t* vnorm;
+    float kc[kMaxLevels];
+    float vc[kMaxLevels];
+    float qjl_scale;      // sqrt(pi/2)/m
+    float scale_log2;     // softmax scale * log2(e)
+    int n_splits;
+    int chunk;            // tokens per split
+    float* partial;       // [B*Hq][n_splits][d+2]
+    float* logits;        // optional [B*Hq][max_seq_len]
+    int max_seq_len;
+};
+
+cudaError_t launch_decode(const DecodeParams& p, int kbits, int vbits, cudaStream_t s);
+
+struct CombineParams {
+    const float* partial;
+    int rows;             // B*Hq
+    int d, n_splits;
+    const float* pi32;    // dense Pi [d][d] (o_j = sum_i Pi_ij a_i)
+    const float* sgn;     // RHT signs
+    int rht;
+    float inv_sqrt_d;
+    void* out;
+    int out_dtype;        // 0 f32, 1 bf16
+};
+
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
+
+struct TopkParams {
+    const float* qprime;  // [nq][d]
+    const float* u;       // [nq][m] or NULL (MSE)
+    int nq, d, m;
+    const uint8_t* codes; int code_stride;
+    const uint8_t* signs; int sign_stride;
+    const uint16_t* norm;
+    const uint16_t* rnorm;
+    int64_t n_db;
+    float c[kMaxLevels];
+    float qjl_scale;
+    int k;
+    int n_chunks;
+    int64_t chunk_rows;
+    float* cand_score;    // [nq][n_chunks][k]
+    int32_t* cand_id;     // [nq][n_chunks][k]
+    int32_t* ids;
+    float* scores;
+};
+
+cudaError_t launch_topk(const TopkParams& p, int code_bits, int prod, cudaStream_t s);
+
+}  // namespace tqk

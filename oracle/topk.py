@@ -17,18 +17,20 @@ originals is reported as recall (a quality figure, not parity).
 import numpy as np
 
 from . import attention
+from . import quantize as qmod
 
 
 def scores(queries, pi, s_matrix, idx, norm16, centroids, rnorm16=None, z=None):
     """[Q, N] estimated inner products. PROD when z is given, MSE otherwise."""
     queries = np.atleast_2d(np.asarray(queries, dtype=np.float64))
     qp, u = attention.query_prep(queries, pi, s_matrix)
-    m = None if s_matrix is None else np.asarray(s_matrix).shape[0]
-    out = np.empty((queries.shape[0], idx.shape[0]))
-    for i in range(queries.shape[0]):
-        out[i] = attention.key_logits(qp[i], None if u is None else u[i], idx, norm16,
-                                      centroids, rnorm16, z, m)
-    return out
+    # the logit estimator of attention.key_logits, for all queries at once
+    base = centroids[idx] @ qp.T
+    if z is not None:
+        m = np.asarray(s_matrix).shape[0]
+        pm = 2.0 * z.astype(np.float64) - 1.0
+        base = base + qmod.qjl_scale(m) * rnorm16[:, None] * (pm @ u.T)
+    return (norm16[:, None] * base).T
 
 
 def topk(score_matrix, k):

@@ -1,0 +1,94 @@
+"""CPU tests of the C-ABI library: it loads, exports every symbol the header
+declares, its struct layouts match the binding, and its host set-up math
+(random stream, rotations, QJL matrix, codebooks) matches the oracle.
+No compute call needs a GPU here."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from conftest import ROOT
+from oracle import codebook, rng, rotation
+
+
+@pytest.fixture(scope="session")
+def lib():
+    from online_kv_cache_quantize_gb300 import binding, build
+
+    build.build()
+    return binding
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "tq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b(tq_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_symbols_are_exported(lib):
+    names = _header_functions()
+    assert len(names) >= 20
+    cdll = ctypes.CDLL(lib.lib_path())
+    for n in names:
+        assert hasattr(cdll, n), n
+    assert set(names) == set(lib.EXPORTED)
+
+
+def test_struct_layouts_match(lib):
+    lib.load()  # raises on a mismatch
+
+
+def test_random_stream_matches_oracle(lib):
+    assert np.array_equal(lib.tq_random_stream(123, 1000), rng.splitmix64(123, 1000))
+    assert np.array_equal(lib.tq_random_stream(5, 10, start=90), rng.splitmix64(5, 10, start=90))
+
+
+@pytest.mark.parametrize("d,kind", [(16, "dense"), (128, "dense"), (200, "dense"), (64, "rht"), (128, "rht"), (256, "rht")])
+def test_rotation_matches_oracle(lib, d, kind):
+    r = lib.tq_make_rotation(1, d, kind)
+    pi = lib.tq_rotation_get(r)
+    assert np.max(np.abs(pi - rotation.make_rotation(1, d, kind))) < 1e-12
+    assert np.max(np.abs(pi @ pi.T - np.eye(d))) < 1e-12
+
+
+def test_qjl_matrix_matches_oracle(lib):
+    for m, d in ((128, 128), (200, 200), (64, 128)):
+        s = lib.tq_qjl_get(lib.tq_make_qjl(2, m, d))
+        want = rng.round_to_bf16(rng.normals(2, m * d).reshape(m, d))
+        assert np.array_equal(s, want)
+
+
+@pytest.mark.parametrize("d", [16, 128, 200])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+def test_codebook_matches_oracle(lib, d, bits):
+    c, t = lib.tq_codebook(d, bits)
+    co, to = codebook.lloyd_max(d, bits)
+    assert np.max(np.abs(c - co)) < 1e-12 and np.max(np.abs(t - to)) < 1e-12
+    assert np.array_equal(c, -c[::-1]) and t[len(t) // 2] == 0.0
+
+
+def test_layout_sizes(lib):
+    assert lib.tq_code_bytes(128, 2) == 32 and lib.tq_code_bytes(128, 3) == 48
+    assert lib.tq_code_bytes(200, 3) == 80 and lib.tq_code_bytes(200, 1) == 32
+    assert lib.tq_sign_bytes(128) == 16 and lib.tq_sign_bytes(200) == 32
+
+
+def test_argument_errors_are_reported(lib):
+    with pytest.raises(lib.TQError) as e:
+        lib.tq_make_rotation(1, 200, "rht")
+    assert "UNSUPPORTED" in str(e.value)
+    with pytest.raises(lib.TQError):
+        lib.tq_make_rotation(1, 2, "dense")
+    with pytest.raises(lib.TQError):
+        lib.tq_codebook(128, 5)
+    with pytest.raises(lib.TQError):
+        lib.tq_make_qjl(1, 0, 128)
+    L = lib.load()
+    assert L.tq_quantize_kv(None, None) == 1  # TQ_ERR_INVALID_ARG
+    assert L.tq_attn_decode(None, None, 0, None) == 1
+    assert L.tq_score_topk(None, None, 0, None) == 1
+    assert L.tq_attn_decode_workspace(None) == 0
