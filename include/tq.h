@@ -223,6 +223,27 @@ size_t tq_attn_decode_workspace(const tq_decode_args* a);
  * not used by anything else until the call's work on `stream` completes. */
 tq_status tq_attn_decode(const tq_decode_args* a, void* workspace, size_t ws_bytes, tq_stream stream);
 
+/* Decode attention that allocates nothing. No counterpart in the write-ups:
+ * it exists for callers that may not allocate device memory when they run
+ * decode, such as a plugin inside an engine that owns all device memory, work
+ * enqueued during CUDA graph capture, or a runtime that forbids allocation
+ * after start-up. Same arguments and results as tq_attn_decode, but the
+ * scratch is an array compiled into the library, TQ_STATIC_DECODE_SCRATCH_BYTES
+ * per device, held by every device that loads the library until the process
+ * exits; the call itself calls no allocator.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     nothing in it needs to start at zero (each call writes every scratch
+ *     byte it reads). Calls whose work overlaps on the GPU (several streams,
+ *     threads or processes sharing a context) race on it: serialise them.
+ *   - Returns TQ_ERR_WORKSPACE, with a message giving the size needed, when
+ *     the arguments need more scratch than the array holds
+ *     (tq_attn_decode_workspace(a) > TQ_STATIC_DECODE_SCRATCH_BYTES). */
+#define TQ_STATIC_DECODE_SCRATCH_BYTES (8u << 20)
+tq_status tq_attn_decode_static(const tq_decode_args* a, tq_stream stream);
+
 /* ------------------------------------------------------------------------ *
  * Inner-product search from the codes.                                     *
  * ------------------------------------------------------------------------ *

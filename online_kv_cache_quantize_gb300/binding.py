@@ -82,6 +82,7 @@ _SIGS = {
     "tq_quantize_kv": (_STATUS, [ctypes.POINTER(tq_quant_args), ctypes.c_void_p]),
     "tq_attn_decode_workspace": (ctypes.c_size_t, [ctypes.POINTER(tq_decode_args)]),
     "tq_attn_decode": (_STATUS, [ctypes.POINTER(tq_decode_args), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "tq_attn_decode_static": (_STATUS, [ctypes.POINTER(tq_decode_args), ctypes.c_void_p]),
     "tq_score_topk_workspace": (ctypes.c_size_t, [ctypes.POINTER(tq_topk_args)]),
     "tq_score_topk": (_STATUS, [ctypes.POINTER(tq_topk_args), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
 }
@@ -306,6 +307,13 @@ def tq_attn_decode(q, kcache, vcache, seq_lens, max_seq_len, rot, qjl, out, work
     a, _keep = _decode_struct(q, kcache, vcache, seq_lens, max_seq_len, rot, qjl, out, **kw)
     _check(load().tq_attn_decode(ctypes.byref(a), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                  _stream_ptr(stream)), "tq_attn_decode")
+
+
+def tq_attn_decode_static(q, kcache, vcache, seq_lens, max_seq_len, rot, qjl, out, stream=None, **kw):
+    """tq_attn_decode without a workspace: for callers that may not allocate
+    device memory; its scratch is an array inside the library (see tq.h)."""
+    a, _keep = _decode_struct(q, kcache, vcache, seq_lens, max_seq_len, rot, qjl, out, **kw)
+    _check(load().tq_attn_decode_static(ctypes.byref(a), _stream_ptr(stream)), "tq_attn_decode_static")
 
 
 def _topk_struct(queries, db, n_db, rot, qjl, k, ids, scores):

@@ -1,0 +1,61 @@
+"""tq_attn_decode_static, the decode entry point that allocates nothing.
+
+Callers that may not allocate device memory at decode time (an engine plugin
+whose host owns all device memory, work enqueued during CUDA graph capture, a
+runtime that forbids allocation after start-up) use this entry point; its
+scratch is an array inside the library. Its output must match the
+workspace-taking tq_attn_decode on the same inputs, call after call, since the
+array is shared and keeps the previous call's contents.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import parity_util as P
+from online_kv_cache_quantize_gb300 import binding as B
+from online_kv_cache_quantize_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+OUT_TOL = 1e-3
+
+
+def test_static_scratch_decode_matches_workspace_decode():
+    from online_kv_cache_quantize_gb300 import build
+    build.build()
+    d, bsz, hkv, hq, cap = 128, 2, 4, 16, 1024
+    k, v = W.decode_kv(bsz, hkv, cap)
+    rot, qjl = P.handles(d, "rht")
+    kc = B.Cache("prod", 3, d, rows=bsz * hkv, capacity=cap)
+    vc = B.Cache("mse", 3, d, rows=bsz * hkv, capacity=cap)
+    B.tq_quantize_kv(kc, rot, torch.from_numpy(k.reshape(-1, d)).cuda().to(torch.bfloat16), qjl=qjl)
+    B.tq_quantize_kv(vc, rot, torch.from_numpy(v.reshape(-1, d)).cuda().to(torch.bfloat16))
+    lens = torch.tensor([cap, 777], dtype=torch.int32, device="cuda")
+    scale = float(np.abs(v).max()) / np.sqrt(d)
+    for call, seed in enumerate((11, 12)):  # two calls in a row, different queries
+        q = torch.from_numpy(W.query_vectors((bsz, hq, d), seed=seed)).cuda()
+        ref = torch.empty((bsz, hq, d), dtype=torch.float32, device="cuda")
+        ws = B.workspace(B.tq_attn_decode_workspace(q, kc, vc, lens, cap, rot, qjl, ref))
+        B.tq_attn_decode(q, kc, vc, lens, cap, rot, qjl, ref, ws)
+        got = torch.full((bsz, hq, d), float("nan"), dtype=torch.float32, device="cuda")
+        B.tq_attn_decode_static(q, kc, vc, lens, cap, rot, qjl, got)
+        torch.cuda.synchronize()
+        err = float((got - ref).abs().max())
+        assert np.isfinite(err) and err <= OUT_TOL * scale, f"call {call}: max |static - workspace| = {err}"
+
+
+def test_static_scratch_rejects_oversized_arguments():
+    from online_kv_cache_quantize_gb300 import build
+    build.build()
+    d, bsz, hkv, hq, cap = 128, 8, 32, 256, 2048
+    rot, qjl = P.handles(d, "rht")
+    # 2048 query rows x 32 splits x 130 floats = 34 MB of scratch: more than the array holds
+    kc = B.Cache("prod", 3, d, rows=bsz * hkv, capacity=cap)
+    vc = B.Cache("mse", 3, d, rows=bsz * hkv, capacity=cap)
+    q = torch.zeros((bsz, hq, d), device="cuda")
+    out = torch.zeros((bsz, hq, d), device="cuda")
+    lens = torch.full((bsz,), cap, dtype=torch.int32, device="cuda")
+    assert B.tq_attn_decode_workspace(q, kc, vc, lens, cap, rot, qjl, out, n_splits=32) > (8 << 20)
+    with pytest.raises(B.TQError) as e:
+        B.tq_attn_decode_static(q, kc, vc, lens, cap, rot, qjl, out, n_splits=32)
+    assert "WORKSPACE" in str(e.value)
