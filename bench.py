@@ -213,7 +213,7 @@ def run_tq(args):
     sampler.start()
     t_warm = time.time()
     n_warm = 0
-    while n_warm < args.warmup or time.time() - t_warm < 1.5:
+    while n_warm < args.warmup or (not args.quick and time.time() - t_warm < 1.5):
         flush.fill_(n_warm & 0xFF)
         step()
         n_warm += 1
@@ -222,7 +222,7 @@ def run_tq(args):
     torch.cuda.synchronize()
 
     # --- quantize measurement: cache fill of the whole context (K and V) ---
-    nq_it = 20
+    nq_it = 3 if args.quick else 20
     qev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nq_it)]
     for i in range(nq_it):
         flush.fill_(i & 0xFF)
@@ -266,7 +266,7 @@ def run_tq(args):
     total_ms = sum(step_ms)
 
     # --- end to end through the C ABI with host buffers (pinned) ---
-    ne = max(20, min(K, 200))
+    ne = 3 if args.quick else max(20, min(K, 200))
     hq_in = q.cpu().pin_memory()
     hk_in, hv_in = knew.cpu().pin_memory(), vnew.cpu().pin_memory()
     h_out = torch.empty_like(out, device="cpu").pin_memory()
@@ -421,6 +421,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["tq", "reference"], default="tq")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true", help="short run for profiling: no clock window, no oracle timing")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -432,7 +433,7 @@ def main():
     ws, rank, _ = _dist()
     res = run_tq(args)
     if rank == 0 and res is not None:
-        if ws == 1 and not args.no_cpu_baseline:
+        if ws == 1 and not (args.no_cpu_baseline or args.quick):
             res["cpu_baseline"] = cpu_baseline_default()
         else:
             res["cpu_baseline"] = None

@@ -6,6 +6,11 @@
 #include <cstring>
 #include <string>
 #include <vector>
+#include <algorithm>
+#include <map>
+#include <mutex>
+
+#include <cuda_fp16.h>
 
 #include "tq_internal.h"
 #include "tq_launch.h"
@@ -101,6 +106,64 @@ tq_status cuda_status(cudaError_t e, const char* where) {
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// nearest fp16 value of x (normal range), ties to even, as a double
+double fp16_round(double x) {
+    if (x == 0.0) return 0.0;
+    int e = 0;
+    double m = std::frexp(x, &e);
+    return std::ldexp(std::nearbyint(m * 2048.0), e - 11);
+}
+
+uint32_t fp16_bits(double v) { return (uint32_t)__half_as_ushort(__float2half_rn((float)fp16_round(v))); }
+
+// Scale lam for the fp16 centroid tables of the tensor-core scan: among
+// lam = 2^e (1 + k/2^18) with lam * max|c| in [1, 2), the one whose products
+// lam * c_i lie closest (relative) to fp16 values, so the table entries
+// carry the centroids almost exactly. Cached per (d, bits).
+double pick_lambda(int d, int bits, const std::vector<double>& c) {
+    static std::mutex mu;
+    static std::map<std::pair<int, int>, double> cache;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find({d, bits});
+        if (it != cache.end()) return it->second;
+    }
+    double mx = 0.0;
+    for (double v : c) mx = std::max(mx, std::fabs(v));
+    int e = 0;
+    std::frexp(mx, &e);                          // 2^(e-1) <= mx < 2^e
+    const double base = std::ldexp(1.0, 1 - e);  // base * mx in [1, 2)
+    const int n = 1 << 18;
+    double best = 1e300, best_l = base;
+    for (int k = 0; k < n; ++k) {
+        const double l = base * (1.0 + (double)k / n);
+        double err = 0.0;
+        for (size_t v = c.size() / 2; v < c.size() && err < best; ++v) {
+            const double x = l * c[v];
+            err = std::max(err, std::fabs(fp16_round(x) - x) / x);
+        }
+        if (err < best) {
+            best = err;
+            best_l = l;
+        }
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    cache[{d, bits}] = best_l;
+    return best_l;
+}
+
+void pair_table(const std::vector<double>& c, int bits, double lam, uint32_t* out) {
+    const int n = 1 << bits;
+    for (int x = 0; x < n * n; ++x) out[x] = fp16_bits(lam * c[x & (n - 1)]) | (fp16_bits(lam * c[x >> bits]) << 16);
+}
+
+// the part of lam * c that the fp16 table above drops, as a second fp16 table
+void pair_table_lo(const std::vector<double>& c, int bits, double lam, uint32_t* out) {
+    const int n = 1 << bits;
+    auto lo = [&](int i) { return fp16_bits(lam * c[i] - fp16_round(lam * c[i])); };
+    for (int x = 0; x < n * n; ++x) out[x] = lo(x & (n - 1)) | (lo(x >> bits) << 16);
+}
+
 struct DecodePlan {
     int n_splits = 1, chunk = 1, group = 1;
     size_t off_q = 0, off_u = 0, off_part = 0, total = 0;
@@ -119,19 +182,19 @@ tq_status plan_decode(const tq_decode_args* a, DecodePlan* pl) {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // each split covers a multiple of 64 tokens (4 warps x 16-token tiles)
     const int L = a->max_seq_len > 0 ? a->max_seq_len : 1;
-    int splits = a->n_splits;
-    if (splits <= 0) {
+    long long want = a->n_splits;
+    if (want <= 0) {
         long long units = (long long)a->batch * a->hkv;
-        long long want = ((long long)sms * 8 + units - 1) / units;
-        int chunk = (int)((L + want - 1) / want);
-        chunk = std::max(64, (chunk + 31) / 32 * 32);
-        splits = (L + chunk - 1) / chunk;
+        want = ((long long)sms * 4 + units - 1) / units;
     }
-    if (splits < 1) splits = 1;
-    if (splits > 65535) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: too many splits");
+    if (want > 65535) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: too many splits");
+    int chunk = (int)((L + want - 1) / want);
+    chunk = std::max(64, (chunk + 63) / 64 * 64);
+    const int splits = (L + chunk - 1) / chunk;
     pl->n_splits = splits;
-    pl->chunk = (L + splits - 1) / splits;
+    pl->chunk = chunk;
     const size_t rows = (size_t)a->batch * a->hq;
     pl->off_q = 0;
     pl->off_u = round_up(rows * a->d * sizeof(float), 256);
@@ -300,6 +363,7 @@ tq_status tq_attn_decode(const tq_decode_args* a, void* workspace, size_t ws_byt
     if (a->k.rows != rows || a->v.rows != rows) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: cache rows must be batch*hkv");
     if (a->k.capacity != a->v.capacity) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: k and v capacity differ");
     if (a->max_seq_len > a->k.capacity) return fail(TQ_ERR_CAPACITY, "tq_attn_decode: max_seq_len exceeds the capacity");
+    if (a->k.capacity % 16) return fail(TQ_ERR_ALIGNMENT, "tq_attn_decode: cache capacity must be a multiple of 16");
     if ((s = check_rot(a->rot, a->d)) != TQ_OK) return s;
     if ((s = check_qjl(a->qjl, a->k.m, a->d)) != TQ_OK) return s;
     if (!a->q || !a->out || !a->seq_lens) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: q/out/seq_lens is NULL");
@@ -367,6 +431,12 @@ tq_status tq_attn_decode(const tq_decode_args* a, void* workspace, size_t ws_byt
     dp.vnorm = a->v.norm;
     for (size_t i = 0; i < kc.size(); ++i) dp.kc[i] = (float)kc[i];
     for (size_t i = 0; i < vc.size(); ++i) dp.vc[i] = (float)vc[i];
+    const double lam_k = pick_lambda(a->d, kb, kc), lam_v = pick_lambda(a->d, vb, vc);
+    pair_table(kc, kb, lam_k, dp.klut);
+    pair_table_lo(kc, kb, lam_k, dp.klut_lo);
+    pair_table(vc, vb, lam_v, dp.vlut);
+    dp.inv_lam_k = (float)(1.0 / lam_k);
+    dp.inv_lam_v = (float)(1.0 / lam_v);
     dp.qjl_scale = (float)(std::sqrt(M_PI / 2.0) / a->k.m);
     const double scale = a->scale != 0.0f ? (double)a->scale : 1.0 / std::sqrt((double)a->d);
     dp.scale_log2 = (float)(scale * 1.4426950408889634);
@@ -377,7 +447,7 @@ tq_status tq_attn_decode(const tq_decode_args* a, void* workspace, size_t ws_byt
     dp.max_seq_len = a->max_seq_len;
     if (a->scan_begin && (e = cudaEventRecord((cudaEvent_t)a->scan_begin, st)) != cudaSuccess)
         return cuda_status(e, "tq_attn_decode scan_begin");
-    e = tqk::launch_decode(dp, kb, vb, st);
+    e = tqk::launch_decode_mma(dp, kb, vb, st);
     if (e != cudaSuccess) return cuda_status(e, "tq_attn_decode scan");
     if (a->scan_end && (e = cudaEventRecord((cudaEvent_t)a->scan_end, st)) != cudaSuccess)
         return cuda_status(e, "tq_attn_decode scan_end");

@@ -48,6 +48,21 @@ cudaError_t launch_decode(const DecodeParams& p, int kbits, int vbits, cudaStrea
     return cudaErrorInvalidValue;
 }
 
+cudaError_t launch_decode_mma_g1(const DecodeParams& p, int kbits, int vbits, cudaStream_t s);
+cudaError_t launch_decode_mma_g2(const DecodeParams& p, int kbits, int vbits, cudaStream_t s);
+cudaError_t launch_decode_mma_g4(const DecodeParams& p, int kbits, int vbits, cudaStream_t s);
+cudaError_t launch_decode_mma_g8(const DecodeParams& p, int kbits, int vbits, cudaStream_t s);
+
+cudaError_t launch_decode_mma(const DecodeParams& p, int kbits, int vbits, cudaStream_t s) {
+    switch (p.group) {
+        case 1: return launch_decode_mma_g1(p, kbits, vbits, s);
+        case 2: return launch_decode_mma_g2(p, kbits, vbits, s);
+        case 4: return launch_decode_mma_g4(p, kbits, vbits, s);
+        case 8: return launch_decode_mma_g8(p, kbits, vbits, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
     if (p.rows <= 0) return cudaSuccess;
     combine_kernel<<<p.rows, p.d, 0, s>>>(p);

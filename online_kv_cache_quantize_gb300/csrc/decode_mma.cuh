@@ -1,0 +1,390 @@
+// Split-K decode scan on the tensor cores (mma.sync m16n8k16, f16 x f16 -> f32).
+//
+// Same computation as the logit estimator and softmax-weighted value sum of
+// the A2A TurboQuant explainer (end of "Stage 2": scores straight from the
+// stored indices with the query rotated once) and the Qiita TurboQuant
+// article ("One more stage ...": residual sign term):
+//   l_t = n_t ( <q', cK[idx_t]> + sqrt(pi/2)/m * gamma_t <u, 2 z_t - 1> )
+//   a   = sum_t exp(s_t - M) nV_t cV[idxV_t]          (rotated domain)
+// computed per 16-token tile of one KV head for all G query heads at once.
+//
+// Operands are built in registers, never staged as de-quantized tiles:
+//  * keys   A[token][coord] = lam_k * cK[idx] as fp16 (a 2-coordinate lookup
+//           table; lam_k is chosen on the host so that every centroid is very
+//           close to an fp16 value), B[coord][2h+s] = hi/lo fp16 split of
+//           q'_h (s = 0 hi, 1 lo), so the f32 accumulator holds the dot
+//           product to about fp32 accuracy;
+//  * signs  A[token][j] = +-1 (exact), B[j][2h+s] = hi/lo of kappa u_h;
+//  * values A[coord][token] = lam_v * cV[idx] (fp16 table), B[token][2h+s] =
+//           hi/lo of p_t nV_t.
+// The MMA K dimension is permuted (keys: thread c of a quad holds coordinates
+// 32c..32c+31; values: tokens 4c..4c+3) and the value M dimension too (row g
+// holds coordinates 16g..16g+15), so each thread reads contiguous code bits.
+//
+// Tiles are staged per warp with cp.async in a 4-deep ring; the capacity of
+// the cache must be a multiple of 16 so that a tile never leaves its row.
+#pragma once
+
+#include "common.cuh"
+#include "tq_launch.h"
+
+namespace tqk {
+
+constexpr int kMmaWarps = 4;
+constexpr int kMmaStages = 4;
+
+template <int KB, int VB>
+struct MmaTile {
+    static constexpr int KC = 16 * 16 * KB;  // key code bytes (16 tokens x 16*KB)
+    static constexpr int SG = 16 * 16;       // sign bytes (m = 128)
+    static constexpr int NB = 32;            // 16 fp16 scalars
+    static constexpr int VC = 16 * 16 * VB;  // value code bytes
+    static constexpr int OFF_KC = 0;
+    static constexpr int OFF_SG = OFF_KC + KC;
+    static constexpr int OFF_KN = OFF_SG + SG;
+    static constexpr int OFF_KR = OFF_KN + NB;
+    static constexpr int OFF_VC = OFF_KR + NB;
+    static constexpr int OFF_VN = OFF_VC + VC;
+    static constexpr int BYTES = OFF_VN + NB;
+    static constexpr int CHUNKS = BYTES / 16;
+};
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t smem_addr, const void* gptr) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr), "l"(gptr));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;\n" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// hi/lo fp16 split of v: the fp16 bits of the hi part, or of v - hi
+__device__ __forceinline__ uint32_t split_half(float v, int lo) {
+    __half h = __float2half_rn(v);
+    if (lo) h = __float2half_rn(v - __half2float(h));
+    return (uint32_t)__half_as_ushort(h);
+}
+
+// bits [off, off+n) of a little-endian word array; called inside fully
+// unrolled loops so that off and n fold to constants
+__device__ __forceinline__ uint32_t field(const uint32_t* w, int off, int n) {
+    const int W = off >> 5, S = off & 31;
+    const uint32_t v = (S + n <= 32) ? (w[W] >> S) : __funnelshift_r(w[W], w[W + 1], S);
+    return n >= 32 ? v : (v & ((1u << n) - 1u));
+}
+
+template <int KB, int VB, int G>
+__global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(const __grid_constant__ DecodeParams p) {
+    using T = MmaTile<KB, VB>;
+    constexpr int NT = (G + 3) / 4;   // n-tiles of 4 heads (x hi/lo)
+    constexpr int KL = 1 << (2 * KB);  // key pair-table entries
+    constexpr int VL = 1 << (2 * VB);  // value pair-table entries
+    constexpr bool KLO = KB >= 3;      // second (lo) key table for 8+ centroids
+    constexpr int D = 128;
+
+    extern __shared__ __align__(16) unsigned char smem[];
+    unsigned char* stages = smem;
+    uint32_t* klut = reinterpret_cast<uint32_t*>(smem + kMmaWarps * kMmaStages * T::BYTES);
+    uint32_t* klo = klut + KL;
+    uint32_t* vlut = klo + (KLO ? KL : 0);
+    uint32_t* slut = vlut + VL;
+    uint16_t* ps = reinterpret_cast<uint16_t*>(slut + 4);  // [warps][NT][8 n][16 tokens]
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, c = lane & 3;
+    const int split = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
+
+    for (int i = threadIdx.x; i < KL; i += blockDim.x) klut[i] = p.klut[i];
+    if constexpr (KLO)
+        for (int i = threadIdx.x; i < KL; i += blockDim.x) klo[i] = p.klut_lo[i];
+    for (int i = threadIdx.x; i < VL; i += blockDim.x) vlut[i] = p.vlut[i];
+    if (threadIdx.x < 4) {
+        const uint32_t pos = 0x3C00u, neg = 0xBC00u;
+        slut[threadIdx.x] = ((threadIdx.x & 1) ? pos : neg) | (((threadIdx.x & 2) ? pos : neg) << 16);
+    }
+
+    // a length outside [0, min(capacity, max_seq_len)] is clamped into it
+    const int L = max(0, (int)min((int64_t)p.seq_lens[b], min(p.capacity, (int64_t)p.max_seq_len)));
+    const int t0 = split * p.chunk;
+    const int t1 = min(t0 + p.chunk, L);
+    const int ntiles = t1 > t0 ? (t1 - t0 + 15) >> 4 : 0;
+    const int nmine = ntiles > warp ? (ntiles - warp + kMmaWarps - 1) / kMmaWarps : 0;
+    const int64_t rowbase = ((int64_t)b * p.hkv + kv) * p.capacity;
+
+    // ---- B fragments (static for the CTA) ----
+    uint32_t bk[NT][8][2], bs[NT][8][2];
+    int qrow[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int hb = nt * 4 + (g >> 1);  // head of B column n = g
+        const int lo = g & 1;
+        const bool ok = hb < G;
+        int row = 0;
+        if (ok) row = b * p.hq + (p.use_table ? (int)p.head_table[kv * G + hb] : kv * G + hb);
+        const float* qp = p.qprime + (int64_t)row * D;
+        const float* up = p.u + (int64_t)row * D;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int i0 = 32 * c + 4 * kk + 2 * r;
+                const float q0 = ok ? qp[i0] : 0.0f, q1 = ok ? qp[i0 + 1] : 0.0f;
+                const float u0 = ok ? up[i0] * p.qjl_scale : 0.0f, u1 = ok ? up[i0 + 1] * p.qjl_scale : 0.0f;
+                bk[nt][kk][r] = split_half(q0, lo) | (split_half(q1, lo) << 16);
+                bs[nt][kk][r] = split_half(u0, lo) | (split_half(u1, lo) << 16);
+            }
+        }
+        const int hc = nt * 4 + c;  // head whose logits this thread owns
+        qrow[nt] = hc < G ? b * p.hq + (p.use_table ? (int)p.head_table[kv * G + hc] : kv * G + hc) : -1;
+    }
+
+    float M[NT], Zp[NT], acc[NT][8][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        M[nt] = -INFINITY;
+        Zp[nt] = 0.0f;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[nt][mt][r] = 0.0f;
+    }
+    __syncthreads();
+
+    unsigned char* wst = stages + warp * kMmaStages * T::BYTES;
+    const uint32_t wst_s = (uint32_t)__cvta_generic_to_shared(wst);
+    auto issue = [&](int i) {
+        const int tok0 = t0 + 16 * (warp + kMmaWarps * i);
+        const int64_t slot0 = rowbase + tok0;
+        const uint32_t dst = wst_s + (i % kMmaStages) * T::BYTES;
+        for (int q = lane; q < T::CHUNKS; q += 32) {
+            const int off = q * 16;
+            const unsigned char* src;
+            if (off < T::OFF_SG) src = p.kcodes + slot0 * (16 * KB) + off;
+            else if (off < T::OFF_KN) src = p.ksigns + slot0 * 16 + (off - T::OFF_SG);
+            else if (off < T::OFF_KR) src = reinterpret_cast<const unsigned char*>(p.knorm + slot0) + (off - T::OFF_KN);
+            else if (off < T::OFF_VC) src = reinterpret_cast<const unsigned char*>(p.krnorm + slot0) + (off - T::OFF_KR);
+            else if (off < T::OFF_VN) src = p.vcodes + slot0 * (16 * VB) + (off - T::OFF_VC);
+            else src = reinterpret_cast<const unsigned char*>(p.vnorm + slot0) + (off - T::OFF_VN);
+            cp_async16(dst + off, src);
+        }
+    };
+
+#pragma unroll
+    for (int s = 0; s < kMmaStages - 1; ++s) {
+        if (s < nmine) issue(s);
+        cp_async_commit();
+    }
+
+    const float inv_lk = p.inv_lam_k, inv_lv = p.inv_lam_v;
+    uint16_t* wps = ps + warp * NT * 8 * 16;
+
+    for (int i = 0; i < nmine; ++i) {
+        if (i + kMmaStages - 1 < nmine) issue(i + kMmaStages - 1);
+        cp_async_commit();
+        cp_async_wait<kMmaStages - 1>();
+        __syncwarp();
+        const unsigned char* st = wst + (i % kMmaStages) * T::BYTES;
+        const int tok0 = t0 + 16 * (warp + kMmaWarps * i);
+
+        // ---- keys and signs: D[token][2h+s] ----
+        uint32_t kw0[KB + 1], kw1[KB + 1];
+        {
+            const uint32_t* r0 = reinterpret_cast<const uint32_t*>(st + T::OFF_KC + g * 16 * KB) + KB * c;
+            const uint32_t* r1 = reinterpret_cast<const uint32_t*>(st + T::OFF_KC + (g + 8) * 16 * KB) + KB * c;
+#pragma unroll
+            for (int w = 0; w < KB; ++w) {
+                kw0[w] = r0[w];
+                kw1[w] = r1[w];
+            }
+            kw0[KB] = 0u;
+            kw1[KB] = 0u;
+        }
+        const uint32_t sw0 = reinterpret_cast<const uint32_t*>(st + T::OFF_SG + g * 16)[c];
+        const uint32_t sw1 = reinterpret_cast<const uint32_t*>(st + T::OFF_SG + (g + 8) * 16)[c];
+        float dk[NT][4], ds[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                dk[nt][r] = 0.0f;
+                ds[nt][r] = 0.0f;
+            }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t f0 = field(kw0, 4 * KB * kk, 2 * KB), f1 = field(kw1, 4 * KB * kk, 2 * KB);
+            const uint32_t f2 = field(kw0, 4 * KB * kk + 2 * KB, 2 * KB);
+            const uint32_t f3 = field(kw1, 4 * KB * kk + 2 * KB, 2 * KB);
+            const uint32_t a0 = klut[f0], a1 = klut[f1], a2 = klut[f2], a3 = klut[f3];
+            if constexpr (KLO) {
+                const uint32_t l0 = klo[f0], l1 = klo[f1], l2 = klo[f2], l3 = klo[f3];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma16816(dk[nt], l0, l1, l2, l3, bk[nt][kk][0], bk[nt][kk][1]);
+            }
+            const uint32_t s0 = slut[(sw0 >> (4 * kk)) & 3u];
+            const uint32_t s1 = slut[(sw1 >> (4 * kk)) & 3u];
+            const uint32_t s2 = slut[(sw0 >> (4 * kk + 2)) & 3u];
+            const uint32_t s3 = slut[(sw1 >> (4 * kk + 2)) & 3u];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                mma16816(dk[nt], a0, a1, a2, a3, bk[nt][kk][0], bk[nt][kk][1]);
+                mma16816(ds[nt], s0, s1, s2, s3, bs[nt][kk][0], bs[nt][kk][1]);
+            }
+        }
+
+        const uint16_t* kn = reinterpret_cast<const uint16_t*>(st + T::OFF_KN);
+        const uint16_t* kr = reinterpret_cast<const uint16_t*>(st + T::OFF_KR);
+        const uint16_t* vn = reinterpret_cast<const uint16_t*>(st + T::OFF_VN);
+        const bool v0 = tok0 + g < t1, v1 = tok0 + g + 8 < t1;
+        const float kn0 = f16_bits_to_f32(kn[g]), kn1 = f16_bits_to_f32(kn[g + 8]);
+        const float kg0 = f16_bits_to_f32(kr[g]), kg1 = f16_bits_to_f32(kr[g + 8]);
+        const float vn0 = f16_bits_to_f32(vn[g]), vn1 = f16_bits_to_f32(vn[g + 8]);
+
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const bool hv = qrow[nt] >= 0;
+            const float l0 = kn0 * fmaf(kg0, ds[nt][0] + ds[nt][1], (dk[nt][0] + dk[nt][1]) * inv_lk);
+            const float l1 = kn1 * fmaf(kg1, ds[nt][2] + ds[nt][3], (dk[nt][2] + dk[nt][3]) * inv_lk);
+            if (p.logits != nullptr && hv) {
+                if (v0) p.logits[(int64_t)qrow[nt] * p.max_seq_len + tok0 + g] = l0;
+                if (v1) p.logits[(int64_t)qrow[nt] * p.max_seq_len + tok0 + g + 8] = l1;
+            }
+            const float s0 = (v0 && hv) ? l0 * p.scale_log2 : -INFINITY;
+            const float s1 = (v1 && hv) ? l1 * p.scale_log2 : -INFINITY;
+            float m = fmaxf(s0, s1);
+            m = fmaxf(m, __shfl_xor_sync(TQ_FULL_MASK, m, 4));
+            m = fmaxf(m, __shfl_xor_sync(TQ_FULL_MASK, m, 8));
+            m = fmaxf(m, __shfl_xor_sync(TQ_FULL_MASK, m, 16));
+            const float mn = fmaxf(M[nt], m);
+            const float corr = (mn == -INFINITY) ? 1.0f : exp2f(M[nt] - mn);
+            const float p0 = (s0 == -INFINITY) ? 0.0f : exp2f(s0 - mn);
+            const float p1 = (s1 == -INFINITY) ? 0.0f : exp2f(s1 - mn);
+            Zp[nt] = fmaf(Zp[nt], corr, p0 + p1);
+            M[nt] = mn;
+            if (corr != 1.0f) {
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) acc[nt][mt][r] *= corr;
+            }
+            const float w0 = v0 ? p0 * vn0 : 0.0f, w1 = v1 ? p1 * vn1 : 0.0f;
+            uint16_t* row_hi = wps + (nt * 8 + 2 * c) * 16;
+            uint16_t* row_lo = row_hi + 16;
+            row_hi[g] = (uint16_t)split_half(w0, 0);
+            row_lo[g] = (uint16_t)split_half(w0, 1);
+            row_hi[g + 8] = (uint16_t)split_half(w1, 0);
+            row_lo[g + 8] = (uint16_t)split_half(w1, 1);
+        }
+        __syncwarp();
+
+        // ---- values: D[coord][2h+s] += A[coord][token] B[token][2h+s] ----
+        uint32_t bv[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const uint32_t* prow = reinterpret_cast<const uint32_t*>(wps + (nt * 8 + g) * 16);
+            bv[nt][0] = prow[2 * c];      // tokens 4c, 4c+1
+            bv[nt][1] = prow[2 * c + 1];  // tokens 4c+2, 4c+3
+        }
+        // each thread: tokens 4c..4c+3, coordinates 16g..16g+15 (16*VB bits at 16*VB*g)
+        uint32_t vf[4][3];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t* vr = reinterpret_cast<const uint32_t*>(st + T::OFF_VC + (4 * c + j) * 16 * VB);
+            const int bit0 = 16 * VB * g;
+            const int w = bit0 >> 5, sh = bit0 & 31;
+            const uint32_t x0 = vr[w];
+            const uint32_t x1 = (w + 1 < 4 * VB) ? vr[w + 1] : 0u;
+            const uint32_t x2 = (w + 2 < 4 * VB) ? vr[w + 2] : 0u;
+            vf[j][0] = __funnelshift_r(x0, x1, sh);
+            vf[j][1] = __funnelshift_r(x1, x2, sh);
+            vf[j][2] = 0u;
+        }
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            uint32_t x[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) x[j] = vlut[field(vf[j], 2 * VB * mt, 2 * VB)];
+            const uint32_t a0 = prmt(x[0], x[1], 0x5410u);
+            const uint32_t a1 = prmt(x[0], x[1], 0x7632u);
+            const uint32_t a2 = prmt(x[2], x[3], 0x5410u);
+            const uint32_t a3 = prmt(x[2], x[3], 0x7632u);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt][mt], a0, a1, a2, a3, bv[nt][0], bv[nt][1]);
+        }
+        __syncwarp();
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // ---- merge the warps of the CTA and write this split's partials ----
+    float* s_acc = reinterpret_cast<float*>(smem);  // [warps][G][D]
+    float* s_mz = s_acc + kMmaWarps * G * D;        // [warps][G][2]
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        float z = Zp[nt];
+        z += __shfl_xor_sync(TQ_FULL_MASK, z, 4);
+        z += __shfl_xor_sync(TQ_FULL_MASK, z, 8);
+        z += __shfl_xor_sync(TQ_FULL_MASK, z, 16);
+        const int h = nt * 4 + c;
+        if (h < G) {
+            float* dst = s_acc + (warp * G + h) * D;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                dst[16 * g + 2 * mt] = (acc[nt][mt][0] + acc[nt][mt][1]) * inv_lv;
+                dst[16 * g + 2 * mt + 1] = (acc[nt][mt][2] + acc[nt][mt][3]) * inv_lv;
+            }
+            if (g == 0) {
+                s_mz[(warp * G + h) * 2] = M[nt];
+                s_mz[(warp * G + h) * 2 + 1] = z;
+            }
+        }
+    }
+    __syncthreads();
+    const int i = threadIdx.x;  // coordinate 0..127
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        float mstar = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kMmaWarps; ++w) mstar = fmaxf(mstar, s_mz[(w * G + h) * 2]);
+        float z = 0.0f, a = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kMmaWarps; ++w) {
+            const float mw = s_mz[(w * G + h) * 2];
+            const float wt = (mw == -INFINITY) ? 0.0f : exp2f(mw - mstar);
+            z = fmaf(s_mz[(w * G + h) * 2 + 1], wt, z);
+            a = fmaf(s_acc[(w * G + h) * D + i], wt, a);
+        }
+        const int row = b * p.hq + (p.use_table ? (int)p.head_table[kv * G + h] : kv * G + h);
+        float* out = p.partial + ((int64_t)row * p.n_splits + split) * (D + 2);
+        out[i] = a;
+        if (i == 0) {
+            out[D] = mstar;
+            out[D + 1] = z;
+        }
+    }
+}
+
+template <int KB, int VB, int G>
+size_t decode_mma_smem() {
+    using T = MmaTile<KB, VB>;
+    constexpr int NT = (G + 3) / 4;
+    constexpr int KL = 1 << (2 * KB);
+    size_t pipe = (size_t)kMmaWarps * kMmaStages * T::BYTES +
+                  4 * (KL + (KB >= 3 ? KL : 0) + (1 << (2 * VB)) + 4) + 2 * kMmaWarps * NT * 8 * 16;
+    size_t merge = (size_t)kMmaWarps * G * 128 * 4 + kMmaWarps * G * 2 * 4;
+    return pipe > merge ? pipe : merge;
+}
+
+}  // namespace tqk

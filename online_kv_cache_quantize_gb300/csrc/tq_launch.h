@@ -86,7 +86,14 @@ struct DecodeParams {
     float* partial;       // [B*Hq][n_splits][d+2]
     float* logits;        // optional [B*Hq][max_seq_len]
     int max_seq_len;
+    // tensor-core scan: 2-coordinate fp16 pair tables of lam * centroid
+    uint32_t klut[256];
+    uint32_t klut_lo[256];  // residual table lam*c - fp16(lam*c), used for 3-4 bit key codes
+    uint32_t vlut[256];
+    float inv_lam_k, inv_lam_v;
 };
+
+cudaError_t launch_decode_mma(const DecodeParams& p, int kbits, int vbits, cudaStream_t s);
 
 cudaError_t launch_decode(const DecodeParams& p, int kbits, int vbits, cudaStream_t s);
 

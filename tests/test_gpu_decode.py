@@ -95,8 +95,8 @@ def test_single_head_logits_dense():
 def test_gqa4_unit_scale(kbits, vbits, kind):
     """32 q / 8 KV heads, unit-scale N(0,1) data, ragged length."""
     r = np.random.default_rng(kbits * 10 + vbits)
-    k = W.round_bf16(r.standard_normal((1, 8, 1000, 128)).astype(np.float32))
-    v = W.round_bf16(r.standard_normal((1, 8, 1000, 128)).astype(np.float32))
+    k = W.round_bf16(r.standard_normal((1, 8, 1008, 128)).astype(np.float32))
+    v = W.round_bf16(r.standard_normal((1, 8, 1008, 128)).astype(np.float32))
     kc, vc, gk, gv, kq, vq, pi, s = _oracle_caches(k, v, kbits, vbits, kind)
     q = W.query_vectors((1, 32, 128), dtype="bf16")
     out, logits = _gpu_decode(q, gk, gv, [997], kind)
@@ -131,6 +131,14 @@ def test_split_invariance_and_gqa_map():
     _check(q, kc, vc, kq, vq, [2048], pi, s, o2, l2, gqa_map=gmap, out_scale=scale)
     assert np.max(np.abs(o1 - o2)) <= 1e-5 * scale and np.max(np.abs(o1 - o3)) <= 1e-5 * scale
     assert np.array_equal(l1, l2)
+
+
+def test_capacity_must_be_multiple_of_16():
+    k, v = W.decode_kv(1, 1, 40)
+    kc, vc, gk, gv, kq, vq, pi, s = _oracle_caches(k, v, 3, 3, "rht")
+    with pytest.raises(B.TQError) as e:
+        _gpu_decode(W.query_vectors((1, 1, 128)), gk, gv, [40], "rht")
+    assert "ALIGNMENT" in str(e.value)
 
 
 def test_bf16_output():
