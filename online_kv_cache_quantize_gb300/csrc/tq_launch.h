@@ -95,7 +95,6 @@ struct DecodeParams {
 
 cudaError_t launch_decode_mma(const DecodeParams& p, int kbits, int vbits, cudaStream_t s);
 
-cudaError_t launch_decode(const DecodeParams& p, int kbits, int vbits, cudaStream_t s);
 
 struct CombineParams {
     const float* partial;
