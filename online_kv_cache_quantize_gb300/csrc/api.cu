@@ -205,6 +205,38 @@ tq_status plan_decode(const tq_decode_args* a, DecodePlan* pl) {
 
 }  // namespace
 
+namespace {
+
+// B-operand fragments of mma.sync m16n8k16 for a 128 x 128 map y = W x:
+// element (k, n) of n-tile nt is W[sigma(nt, n)][16 kk + k] with the output
+// permutation sigma(nt, n) = 32 (n / 2) + 2 nt + n % 2 (so accumulators land
+// in the quantize kernel's quad layout), stored [kk][nt][lane] as two words.
+template <typename F>
+std::vector<uint2v> mma_b_fragments(F wbits) {
+    std::vector<uint2v> out((size_t)8 * 16 * 32);
+    for (int kk = 0; kk < 8; ++kk)
+        for (int nt = 0; nt < 16; ++nt)
+            for (int lane = 0; lane < 32; ++lane) {
+                const int g = lane >> 2, c = lane & 3;
+                const int o = 32 * (g >> 1) + 2 * nt + (g & 1);
+                auto e = [&](int k) { return (uint32_t)wbits(o, 16 * kk + k); };
+                uint2v v;
+                v.x = e(2 * c) | (e(2 * c + 1) << 16);
+                v.y = e(2 * c + 8) | (e(2 * c + 9) << 16);
+                out[((size_t)kk * 16 + nt) * 32 + lane] = v;
+            }
+    return out;
+}
+
+uint16_t bf16_bits_of(double exact_bf16_value) {
+    const float f = (float)exact_bf16_value;
+    uint32_t u;
+    std::memcpy(&u, &f, 4);
+    return (uint16_t)(u >> 16);
+}
+
+}  // namespace
+
 extern "C" {
 
 tq_status tq_rotation_to_device(tq_rotation* rot) {
@@ -227,6 +259,21 @@ tq_status tq_rotation_to_device(tq_rotation* rot) {
     if ((s = upload(&rot->d_pit32, pit32)) != TQ_OK) return s;
     if ((s = upload(&rot->d_pi64, rot->pi)) != TQ_OK) return s;
     if ((s = upload(&rot->d_sign, sg)) != TQ_OK) return s;
+    if (d == 128 && rot->kind == TQ_ROT_DENSE_QR) {
+        // three bf16 limbs of Pi (about 24 bits), concatenated limb-major
+        std::vector<double> l1((size_t)d * d), l2((size_t)d * d), l3((size_t)d * d);
+        for (size_t i = 0; i < l1.size(); ++i) {
+            l1[i] = tq::round_bf16(rot->pi[i]);
+            l2[i] = tq::round_bf16(rot->pi[i] - l1[i]);
+            l3[i] = tq::round_bf16(rot->pi[i] - l1[i] - l2[i]);
+        }
+        std::vector<uint2v> frag;
+        for (const std::vector<double>* l : {&l1, &l2, &l3}) {
+            auto f = mma_b_fragments([&](int o, int k) { return bf16_bits_of((*l)[(size_t)o * d + k]); });
+            frag.insert(frag.end(), f.begin(), f.end());
+        }
+        if ((s = upload(&rot->d_pi_frag, frag)) != TQ_OK) return s;
+    }
     rot->device = dev;
     return TQ_OK;
 }
@@ -241,6 +288,7 @@ tq_status tq_free_rotation(tq_rotation* rot) {
         cudaFree(rot->d_pit32);
         cudaFree(rot->d_pi64);
         cudaFree(rot->d_sign);
+        cudaFree(rot->d_pi_frag);
         if (cur >= 0) cudaSetDevice(cur);
     }
     delete rot;
@@ -263,6 +311,10 @@ tq_status tq_qjl_to_device(tq_qjl* q) {
     tq_status s;
     if ((s = upload(&q->d_st32, st)) != TQ_OK) return s;
     if ((s = upload(&q->d_s32, s32)) != TQ_OK) return s;
+    if (m == 128 && d == 128) {
+        auto frag = mma_b_fragments([&](int o, int k) { return bf16_bits_of(q->s[(size_t)o * d + k]); });
+        if ((s = upload(&q->d_s_frag, frag)) != TQ_OK) return s;
+    }
     q->device = dev;
     return TQ_OK;
 }
@@ -275,6 +327,7 @@ tq_status tq_free_qjl(tq_qjl* q) {
         cudaSetDevice(q->device);
         cudaFree(q->d_st32);
         cudaFree(q->d_s32);
+        cudaFree(q->d_s_frag);
         if (cur >= 0) cudaSetDevice(cur);
     }
     delete q;
@@ -338,8 +391,19 @@ tq_status tq_quantize_kv(const tq_quant_args* a, tq_stream stream) {
     if ((s = fill_codebook(c.d, cb, &p.cb)) != TQ_OK) return s;
     const int dtype = a->x_dtype == TQ_F32 ? 0 : 1;
     const int vpl = vpl_for(c.d);
-    cudaError_t e = rht ? tqk::launch_quantize_rht(p, dtype, vpl, prod ? 1 : 0, cb, (cudaStream_t)stream)
-                        : tqk::launch_quantize_dense(p, dtype, vpl, prod ? 1 : 0, cb, (cudaStream_t)stream);
+    p.pi_frag = a->rot->d_pi_frag;
+    p.s_frag = prod ? a->qjl->d_s_frag : nullptr;
+    // d = m = 128 with 16-byte aligned rows: the tensor-core kernel; otherwise
+    // the warp-per-vector kernel (any d <= 256)
+    const bool mma = c.d == 128 && (!prod || (c.m == 128 && p.s_frag)) && (rht || p.pi_frag) &&
+                     aligned(a->x, 16) && (a->x_stride * (int64_t)esz) % 16 == 0;
+    cudaError_t e;
+    if (mma)
+        e = tqk::launch_quantize_mma(p, dtype, rht ? 1 : 0, prod ? 1 : 0, cb, (cudaStream_t)stream);
+    else if (rht)
+        e = tqk::launch_quantize_rht(p, dtype, vpl, prod ? 1 : 0, cb, (cudaStream_t)stream);
+    else
+        e = tqk::launch_quantize_dense(p, dtype, vpl, prod ? 1 : 0, cb, (cudaStream_t)stream);
     return cuda_status(e, "tq_quantize_kv launch");
 }
 

@@ -8,6 +8,11 @@
 
 #include "../../include/tq.h"
 
+// two 32-bit words: the B-operand registers of one mma.sync fragment
+struct uint2v {
+    uint32_t x, y;
+};
+
 struct tq_rotation {
     int d = 0;
     int kind = 0;
@@ -19,6 +24,7 @@ struct tq_rotation {
     float* d_pit32 = nullptr;   // Pi^T row-major fp32 (PT[j][i] = Pi_ij)
     double* d_pi64 = nullptr;   // Pi row-major fp64 (exact re-decision path)
     float* d_sign = nullptr;    // RHT signs fp32 (d)
+    uint2v* d_pi_frag = nullptr;  // d = 128 dense: 3 bf16 limbs of Pi^T in mma fragment order
 };
 
 struct tq_qjl {
@@ -29,6 +35,7 @@ struct tq_qjl {
     int device = -1;
     float* d_st32 = nullptr;    // S^T row-major fp32 (ST[i][j] = S_ji), [d][m]
     float* d_s32 = nullptr;     // S row-major fp32 [m][d]
+    uint2v* d_s_frag = nullptr;   // m = d = 128: S (exact bf16) in mma fragment order
 };
 
 namespace tq {

@@ -36,11 +36,16 @@ struct QuantParams {
     const double* pi64;   // Pi [d][d] fp64
     const float* sgn;     // RHT signs [d]
     const float* st32;    // S^T [d][m]
+    const void* pi_frag;  // d = 128 dense: Pi^T limbs in mma fragment order
+    const void* s_frag;   // m = d = 128: S in mma fragment order
     int d, m;
     float inv_sqrt_d;
     float guard;          // |y - t_j| below this is re-decided in fp64
     Codebook cb;
 };
+
+// tensor-core quantize for d = m = 128 (x 16-byte aligned rows)
+cudaError_t launch_quantize_mma(const QuantParams& p, int dtype, int rht, int prod, int code_bits, cudaStream_t s);
 
 // dtype: 0 f32, 1 bf16, 2 f16. rht: 0 dense, 1 RHT. prod: 0 MSE, 1 PROD.
 cudaError_t launch_quantize(const QuantParams& p, int dtype, int rht, int prod, int code_bits,
