@@ -36,7 +36,7 @@ UNIT = "KV-tokens/s"
 WORKLOAD = dict(name="llama8b_decode_32k", batch=1, hq=32, hkv=8, d=128, seq_len=32768,
                 rotation="rht", k_bits=3, v_bits=3)
 FLUSH_BYTES = 256 << 20  # > 129 MB L2
-SCAN_SOURCES = ["online_kv_cache_quantize_gb300/csrc/decode.cuh", "online_kv_cache_quantize_gb300/csrc/common.cuh"]
+SCAN_SOURCES = ["online_kv_cache_quantize_gb300/csrc/decode_mma.cuh", "online_kv_cache_quantize_gb300/csrc/common.cuh"]
 
 
 def _peaks():
@@ -310,7 +310,7 @@ def run_tq(args):
                        "step": "append 1 token per KV head (quantize K and V) + decode attention over seq_len tokens",
                        "l2": "flushed (256 MiB write) before every timed step", "parallelism": f"replicas x{ws}"},
             "hbm_gbs": {"scan": achieved, "quantize": q_achieved},
-            "roofline": {"kernel": "decode_kernel (split-K scan)", "bound": "hbm", "achieved": achieved,
+            "roofline": {"kernel": "decode_mma_kernel (split-K scan)", "bound": "hbm", "achieved": achieved,
                          "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind,
                          "alg_bytes_per_launch": scan_alg, "avg_launch_us": scan_avg_s * 1e6,
                          "traffic": _traffic("decode_scan", SCAN_SOURCES)},
