@@ -66,14 +66,27 @@ __global__ void __launch_bounds__(kPrepWarps * 32) query_prep_kernel(const __gri
         float acc[VPL];
 #pragma unroll
         for (int r = 0; r < VPL; ++r) acc[r] = 0.0f;
-#pragma unroll 8
+#pragma unroll 32
         for (int j = warp; j < d; j += kPrepWarps) {
             const float xj = s_x[j];
             const float* rowp = p.pit32 + (size_t)j * d;
+            bool vec = false;
+            if constexpr (VPL == 4) {
+                if (d == 128) {
+                    const float4 t = __ldg(reinterpret_cast<const float4*>(rowp) + lane);
+                    acc[0] = fmaf(t.x, xj, acc[0]);
+                    acc[1] = fmaf(t.y, xj, acc[1]);
+                    acc[2] = fmaf(t.z, xj, acc[2]);
+                    acc[3] = fmaf(t.w, xj, acc[3]);
+                    vec = true;
+                }
+            }
+            if (!vec) {
 #pragma unroll
-            for (int r = 0; r < VPL; ++r) {
-                const int e = VPL * lane + r;
-                if (e < d) acc[r] = fmaf(__ldg(rowp + e), xj, acc[r]);
+                for (int r = 0; r < VPL; ++r) {
+                    const int e = VPL * lane + r;
+                    if (e < d) acc[r] = fmaf(__ldg(rowp + e), xj, acc[r]);
+                }
             }
         }
 #pragma unroll
@@ -95,14 +108,22 @@ __global__ void __launch_bounds__(kPrepWarps * 32) query_prep_kernel(const __gri
     float acc[8];
 #pragma unroll
     for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
-#pragma unroll 8
+#pragma unroll 32
     for (int i = warp; i < d; i += kPrepWarps) {
         const float qi = s_y[i];
         const float* rowp = p.st32 + (size_t)i * m;
+        if (m == 128) {
+            const float4 t = __ldg(reinterpret_cast<const float4*>(rowp) + lane);
+            acc[0] = fmaf(t.x, qi, acc[0]);
+            acc[1] = fmaf(t.y, qi, acc[1]);
+            acc[2] = fmaf(t.z, qi, acc[2]);
+            acc[3] = fmaf(t.w, qi, acc[3]);
+        } else {
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const int j = mpl * lane + r;
-            if (r < mpl && j < m) acc[r] = fmaf(__ldg(rowp + j), qi, acc[r]);
+            for (int r = 0; r < 8; ++r) {
+                const int j = mpl * lane + r;
+                if (r < mpl && j < m) acc[r] = fmaf(__ldg(rowp + j), qi, acc[r]);
+            }
         }
     }
     __syncthreads();  // s_part reuse
@@ -122,59 +143,55 @@ __global__ void __launch_bounds__(kPrepWarps * 32) query_prep_kernel(const __gri
 
 // ---------------------------------------------------------------------------
 // Merge the splits of one query row and un-rotate: o = Pi^T (a / Z).
-// CTA of 512 threads = (512 / d) groups of d threads; group k sums the splits
-// s = k, k + groups, ... so the partial loads of many splits are in flight.
-// d in {64, 128, 256}.
+// CTA of 1024 threads = (1024 / d) groups of d threads; group k runs an
+// online (max, sum, a) merge over the splits s = k, k + groups, ... in one
+// pass, then the groups are merged through shared memory. d in {64, 128, 256}.
 // ---------------------------------------------------------------------------
-constexpr int kCombineThreads = 512;
-
-__device__ __forceinline__ float block_reduce(float v, float* s_red, bool is_max) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float w = __shfl_xor_sync(TQ_FULL_MASK, v, o);
-        v = is_max ? fmaxf(v, w) : v + w;
-    }
-    __syncthreads();
-    if (lane == 0) s_red[warp] = v;
-    __syncthreads();
-    v = s_red[0];
-    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) v = is_max ? fmaxf(v, s_red[w]) : v + s_red[w];
-    return v;
-}
+constexpr int kCombineThreads = 1024;
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ CombineParams p) {
-    __shared__ float s_red[32];
-    __shared__ float s_part[kCombineThreads];
+    __shared__ float s_m[kCombineThreads];
+    __shared__ float s_z[kCombineThreads];
+    __shared__ float s_v[kCombineThreads];
     __shared__ float s_a[256];
     const int row = blockIdx.x, tid = threadIdx.x, d = p.d, ns = p.n_splits;
     const int groups = kCombineThreads / d;
     const int i = tid % d, grp = tid / d;
     const float* base = p.partial + (int64_t)row * ns * (d + 2);
 
-    float m = -INFINITY;
-    for (int s = tid; s < ns; s += kCombineThreads) m = fmaxf(m, base[(int64_t)s * (d + 2) + d]);
-    const float mstar = block_reduce(m, s_red, true);
-    float z = 0.0f;
-    for (int s = tid; s < ns; s += kCombineThreads) {
-        const float ms = base[(int64_t)s * (d + 2) + d];
-        if (ms != -INFINITY) z = fmaf(base[(int64_t)s * (d + 2) + d + 1], exp2f(ms - mstar), z);
-    }
-    z = block_reduce(z, s_red, false);
-
-    float a = 0.0f;
+    float m = -INFINITY, z = 0.0f, a = 0.0f;
 #pragma unroll 4
     for (int s = grp; s < ns; s += groups) {
         const float* ps = base + (int64_t)s * (d + 2);
-        const float ms = ps[d];
-        if (ms != -INFINITY) a = fmaf(ps[i], exp2f(ms - mstar), a);
+        const float ms = ps[d], zs = ps[d + 1], as = ps[i];
+        if (ms > m) {
+            const float sc = (m == -INFINITY) ? 0.0f : exp2f(m - ms);
+            z *= sc;
+            a *= sc;
+            m = ms;
+        }
+        if (ms != -INFINITY) {
+            const float w = exp2f(ms - m);
+            z = fmaf(zs, w, z);
+            a = fmaf(as, w, a);
+        }
     }
-    s_part[tid] = a;
+    s_m[tid] = m;
+    s_z[tid] = z;
+    s_v[tid] = a;
     __syncthreads();
     if (tid < d) {
-        float t = 0.0f;
-        for (int k = 0; k < groups; ++k) t += s_part[k * d + tid];
-        s_a[tid] = (z > 0.0f) ? t / z : 0.0f;
+        float mstar = -INFINITY;
+        for (int k = 0; k < groups; ++k) mstar = fmaxf(mstar, s_m[k * d + tid]);
+        float zt = 0.0f, at = 0.0f;
+        for (int k = 0; k < groups; ++k) {
+            const float mk = s_m[k * d + tid];
+            if (mk == -INFINITY) continue;
+            const float w = exp2f(mk - mstar);
+            zt = fmaf(s_z[k * d + tid], w, zt);
+            at = fmaf(s_v[k * d + tid], w, at);
+        }
+        s_a[tid] = (zt > 0.0f) ? at / zt : 0.0f;
     }
     __syncthreads();
     float o = 0.0f;
@@ -191,9 +208,15 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
             __syncthreads();
         }
         if (tid < d) o = s_a[tid] * p.sgn[tid] * p.inv_sqrt_d;
-    } else if (tid < d) {
-#pragma unroll 8
-        for (int k = 0; k < d; ++k) o = fmaf(__ldg(p.pi32 + (size_t)k * d + tid), s_a[k], o);
+    } else {
+        // o_i = sum_k Pi[k][i] a_k, the k range split over the groups
+        float part = 0.0f;
+#pragma unroll 4
+        for (int k = grp; k < d; k += groups) part = fmaf(__ldg(p.pi32 + (size_t)k * d + i), s_a[k], part);
+        s_v[tid] = part;
+        __syncthreads();
+        if (tid < d)
+            for (int k = 0; k < groups; ++k) o += s_v[k * d + tid];
     }
     if (tid < d) {
         if (p.out_dtype == 1)

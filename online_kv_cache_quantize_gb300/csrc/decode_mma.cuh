@@ -86,6 +86,19 @@ __device__ __forceinline__ uint32_t field(const uint32_t* w, int off, int n) {
     return n >= 32 ? v : (v & ((1u << n) - 1u));
 }
 
+// 4 * field(w, off, n): the byte offset of a 4-byte table entry, in two ops
+__device__ __forceinline__ uint32_t field4(const uint32_t* w, int off, int n) {
+    const int W = off >> 5, S = off & 31;
+    const uint32_t mask = ((1u << n) - 1u) << 2;
+    if (S + n <= 32) return (S >= 2 ? (w[W] >> (S - 2)) : (w[W] << (2 - S))) & mask;
+    return (__funnelshift_r(w[W], w[W + 1], S) << 2) & mask;
+}
+
+template <typename T>
+__device__ __forceinline__ T lds_at(const void* base, uint32_t byte_off) {
+    return *reinterpret_cast<const T*>(reinterpret_cast<const unsigned char*>(base) + byte_off);
+}
+
 template <int KB, int VB, int G>
 __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(const __grid_constant__ DecodeParams p) {
     using T = MmaTile<KB, VB>;
@@ -97,11 +110,11 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(const __grid
 
     extern __shared__ __align__(16) unsigned char smem[];
     unsigned char* stages = smem;
-    uint32_t* klut = reinterpret_cast<uint32_t*>(smem + kMmaWarps * kMmaStages * T::BYTES);
-    uint32_t* klo = klut + KL;
-    uint32_t* vlut = klo + (KLO ? KL : 0);
-    uint32_t* slut = vlut + VL;
-    uint16_t* ps = reinterpret_cast<uint16_t*>(slut + 4);  // [warps][NT][8 n][16 tokens]
+    uint16_t* ps = reinterpret_cast<uint16_t*>(smem + kMmaWarps * kMmaStages * T::BYTES);  // [warps][NT][8][16]
+    __shared__ uint32_t klut[KL];
+    __shared__ uint32_t klo[KLO ? KL : 1];
+    __shared__ uint32_t vlut[VL];
+    __shared__ __align__(8) uint2 slut4[16];  // 4 sign bits -> (+-1, +-1), (+-1, +-1) as fp16
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
@@ -111,9 +124,10 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(const __grid
     if constexpr (KLO)
         for (int i = threadIdx.x; i < KL; i += blockDim.x) klo[i] = p.klut_lo[i];
     for (int i = threadIdx.x; i < VL; i += blockDim.x) vlut[i] = p.vlut[i];
-    if (threadIdx.x < 4) {
-        const uint32_t pos = 0x3C00u, neg = 0xBC00u;
-        slut[threadIdx.x] = ((threadIdx.x & 1) ? pos : neg) | (((threadIdx.x & 2) ? pos : neg) << 16);
+    if (threadIdx.x < 16) {
+        const uint32_t pos = 0x3C00u, neg = 0xBC00u, e = threadIdx.x;
+        slut4[e].x = ((e & 1) ? pos : neg) | (((e & 2) ? pos : neg) << 16);
+        slut4[e].y = ((e & 4) ? pos : neg) | (((e & 8) ? pos : neg) << 16);
     }
 
     // a length outside [0, min(capacity, max_seq_len)] is clamped into it
@@ -165,20 +179,35 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(const __grid
 
     unsigned char* wst = stages + warp * kMmaStages * T::BYTES;
     const uint32_t wst_s = (uint32_t)__cvta_generic_to_shared(wst);
+    // this lane's chunks of a tile: source for the warp's first tile and the
+    // byte step to its next tile (4 tiles = 64 tokens further on)
+    constexpr int NQ = (T::CHUNKS + 31) / 32;
+    const unsigned char* qsrc[NQ];
+    int64_t qstep[NQ];
+    {
+        const int64_t slot0 = rowbase + t0 + 16 * warp;
+        constexpr int64_t TS = 16 * kMmaWarps;  // tokens between a warp's tiles
+#pragma unroll
+        for (int k = 0; k < NQ; ++k) {
+            const int off = (lane + 32 * k) * 16;
+            const unsigned char* src = p.kcodes;
+            int64_t step = 0;
+            if (off < T::OFF_SG) { src = p.kcodes + slot0 * (16 * KB) + off; step = TS * 16 * KB; }
+            else if (off < T::OFF_KN) { src = p.ksigns + slot0 * 16 + (off - T::OFF_SG); step = TS * 16; }
+            else if (off < T::OFF_KR) { src = reinterpret_cast<const unsigned char*>(p.knorm + slot0) + (off - T::OFF_KN); step = TS * 2; }
+            else if (off < T::OFF_VC) { src = reinterpret_cast<const unsigned char*>(p.krnorm + slot0) + (off - T::OFF_KR); step = TS * 2; }
+            else if (off < T::OFF_VN) { src = p.vcodes + slot0 * (16 * VB) + (off - T::OFF_VC); step = TS * 16 * VB; }
+            else if (off < T::BYTES) { src = reinterpret_cast<const unsigned char*>(p.vnorm + slot0) + (off - T::OFF_VN); step = TS * 2; }
+            qsrc[k] = src;
+            qstep[k] = step;
+        }
+    }
     auto issue = [&](int i) {
-        const int tok0 = t0 + 16 * (warp + kMmaWarps * i);
-        const int64_t slot0 = rowbase + tok0;
         const uint32_t dst = wst_s + (i % kMmaStages) * T::BYTES;
-        for (int q = lane; q < T::CHUNKS; q += 32) {
-            const int off = q * 16;
-            const unsigned char* src;
-            if (off < T::OFF_SG) src = p.kcodes + slot0 * (16 * KB) + off;
-            else if (off < T::OFF_KN) src = p.ksigns + slot0 * 16 + (off - T::OFF_SG);
-            else if (off < T::OFF_KR) src = reinterpret_cast<const unsigned char*>(p.knorm + slot0) + (off - T::OFF_KN);
-            else if (off < T::OFF_VC) src = reinterpret_cast<const unsigned char*>(p.krnorm + slot0) + (off - T::OFF_KR);
-            else if (off < T::OFF_VN) src = p.vcodes + slot0 * (16 * VB) + (off - T::OFF_VC);
-            else src = reinterpret_cast<const unsigned char*>(p.vnorm + slot0) + (off - T::OFF_VN);
-            cp_async16(dst + off, src);
+#pragma unroll
+        for (int k = 0; k < NQ; ++k) {
+            const int off = (lane + 32 * k) * 16;
+            if (off < T::BYTES) cp_async16(dst + off, qsrc[k] + i * qstep[k]);
         }
     };
 
@@ -224,19 +253,21 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(const __grid
             }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t f0 = field(kw0, 4 * KB * kk, 2 * KB), f1 = field(kw1, 4 * KB * kk, 2 * KB);
-            const uint32_t f2 = field(kw0, 4 * KB * kk + 2 * KB, 2 * KB);
-            const uint32_t f3 = field(kw1, 4 * KB * kk + 2 * KB, 2 * KB);
-            const uint32_t a0 = klut[f0], a1 = klut[f1], a2 = klut[f2], a3 = klut[f3];
+            const uint32_t f0 = field4(kw0, 4 * KB * kk, 2 * KB), f1 = field4(kw1, 4 * KB * kk, 2 * KB);
+            const uint32_t f2 = field4(kw0, 4 * KB * kk + 2 * KB, 2 * KB);
+            const uint32_t f3 = field4(kw1, 4 * KB * kk + 2 * KB, 2 * KB);
+            const uint32_t a0 = lds_at<uint32_t>(klut, f0), a1 = lds_at<uint32_t>(klut, f1);
+            const uint32_t a2 = lds_at<uint32_t>(klut, f2), a3 = lds_at<uint32_t>(klut, f3);
             if constexpr (KLO) {
-                const uint32_t l0 = klo[f0], l1 = klo[f1], l2 = klo[f2], l3 = klo[f3];
+                const uint32_t l0 = lds_at<uint32_t>(klo, f0), l1 = lds_at<uint32_t>(klo, f1);
+                const uint32_t l2 = lds_at<uint32_t>(klo, f2), l3 = lds_at<uint32_t>(klo, f3);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) mma16816(dk[nt], l0, l1, l2, l3, bk[nt][kk][0], bk[nt][kk][1]);
             }
-            const uint32_t s0 = slut[(sw0 >> (4 * kk)) & 3u];
-            const uint32_t s1 = slut[(sw1 >> (4 * kk)) & 3u];
-            const uint32_t s2 = slut[(sw0 >> (4 * kk + 2)) & 3u];
-            const uint32_t s3 = slut[(sw1 >> (4 * kk + 2)) & 3u];
+            // four sign bits 4kk..4kk+3 -> registers for slots (0,1) and (2,3)
+            const uint2 sg0 = lds_at<uint2>(slut4, kk == 0 ? (sw0 << 3) & 0x78u : (sw0 >> (4 * kk - 3)) & 0x78u);
+            const uint2 sg1 = lds_at<uint2>(slut4, kk == 0 ? (sw1 << 3) & 0x78u : (sw1 >> (4 * kk - 3)) & 0x78u);
+            const uint32_t s0 = sg0.x, s1 = sg1.x, s2 = sg0.y, s3 = sg1.y;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 mma16816(dk[nt], a0, a1, a2, a3, bk[nt][kk][0], bk[nt][kk][1]);
@@ -315,7 +346,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(const __grid
         for (int mt = 0; mt < 8; ++mt) {
             uint32_t x[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) x[j] = vlut[field(vf[j], 2 * VB * mt, 2 * VB)];
+            for (int j = 0; j < 4; ++j) x[j] = lds_at<uint32_t>(vlut, field4(vf[j], 2 * VB * mt, 2 * VB));
             const uint32_t a0 = prmt(x[0], x[1], 0x5410u);
             const uint32_t a1 = prmt(x[0], x[1], 0x7632u);
             const uint32_t a2 = prmt(x[2], x[3], 0x5410u);
@@ -380,9 +411,7 @@ template <int KB, int VB, int G>
 size_t decode_mma_smem() {
     using T = MmaTile<KB, VB>;
     constexpr int NT = (G + 3) / 4;
-    constexpr int KL = 1 << (2 * KB);
-    size_t pipe = (size_t)kMmaWarps * kMmaStages * T::BYTES +
-                  4 * (KL + (KB >= 3 ? KL : 0) + (1 << (2 * VB)) + 4) + 2 * kMmaWarps * NT * 8 * 16;
+    size_t pipe = (size_t)kMmaWarps * kMmaStages * T::BYTES + 2 * kMmaWarps * NT * 8 * 16;
     size_t merge = (size_t)kMmaWarps * G * 128 * 4 + kMmaWarps * G * 2 * 4;
     return pipe > merge ? pipe : merge;
 }
