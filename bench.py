@@ -33,8 +33,15 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode attn KV-tokens/s & HBM GB/s (% of GB300 peak); quantize vectors/s"
 UNIT = "KV-tokens/s"
-WORKLOAD = dict(name="llama8b_decode_32k", batch=1, hq=32, hkv=8, d=128, seq_len=32768,
-                rotation="rht", k_bits=3, v_bits=3)
+WORKLOADS = {
+    # the default line: one decode step of a Llama-3.1-8B-shaped layer
+    "llama8b_decode_32k": dict(batch=1, hq=32, hkv=8, d=128, seq_len=32768, rotation="rht", k_bits=3, v_bits=3),
+    # other decode shapes (parity cases; measured with --workload)
+    "batched_decode_16x8k": dict(batch=16, hq=32, hkv=8, d=128, seq_len=8192, rotation="rht", k_bits=3, v_bits=3),
+    "long_context_128k": dict(batch=1, hq=64, hkv=8, d=128, seq_len=131072, rotation="rht", k_bits=3, v_bits=4,
+                              heavy_frac=0.01),
+}
+WORKLOAD = dict(name="llama8b_decode_32k", **WORKLOADS["llama8b_decode_32k"])
 FLUSH_BYTES = 256 << 20  # > 129 MB L2
 SCAN_SOURCES = ["online_kv_cache_quantize_gb300/csrc/decode_mma.cuh", "online_kv_cache_quantize_gb300/csrc/common.cuh"]
 
@@ -156,7 +163,7 @@ def run_tq(args):
     rows = bsz * hkv
     rot = B.tq_rotation_to_device(B.tq_make_rotation(W.ROT_SEED, d, w["rotation"]))
     qjl = B.tq_qjl_to_device(B.tq_make_qjl(W.QJL_SEED, d, d))
-    kx, vx = W.decode_kv(bsz, hkv, T, seed=W.DATA_SEED + rank)
+    kx, vx = W.decode_kv(bsz, hkv, T, seed=W.DATA_SEED + rank, heavy_frac=w.get("heavy_frac", 0.0))
     kdev = torch.from_numpy(kx.reshape(-1, d)).cuda().to(torch.bfloat16)
     vdev = torch.from_numpy(vx.reshape(-1, d)).cuda().to(torch.bfloat16)
     del kx, vx
@@ -315,7 +322,8 @@ def run_tq(args):
                          "alg_bytes_per_launch": scan_alg, "avg_launch_us": scan_avg_s * 1e6,
                          "traffic": _traffic("decode_scan", SCAN_SOURCES)},
             "quantize": {"vectors_per_s": q_vectors / (q_ms / 1e3), "vectors_per_call": q_vectors,
-                         "workload": "cache fill: 8 KV heads x 32768 tokens, K (3-bit PROD) and V (3-bit MSE), bf16 in",
+                         "workload": (f"cache fill: {bsz} x {hkv} KV heads x {T} tokens, K ({w['k_bits']}-bit PROD) "
+                                      f"and V ({w['v_bits']}-bit MSE), bf16 in, {w['rotation']}"),
                          "roofline": {"bound": "hbm", "achieved": q_achieved, "peak": peak, "unit": "GB/s",
                                       "frac": q_achieved / peak, "alg_bytes_per_call": q_alg_bytes}},
             "e2e": {"value": ws * tokens_per_step / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -422,9 +430,18 @@ def main():
     ap.add_argument("--impl", choices=["tq", "reference"], default="tq")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true", help="short run for profiling: no clock window, no oracle timing")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama8b_decode_32k")
+    ap.add_argument("--k-bits", type=int, default=None)
+    ap.add_argument("--v-bits", type=int, default=None)
+    ap.add_argument("--rotation", choices=["rht", "dense"], default=None)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    WORKLOAD.clear()
+    WORKLOAD.update(name=args.workload, **WORKLOADS[args.workload])
+    for key, val in (("k_bits", args.k_bits), ("v_bits", args.v_bits), ("rotation", args.rotation)):
+        if val is not None:
+            WORKLOAD[key] = val
     if args.impl == "reference":
         res = run_reference(args)
         if res is not None:

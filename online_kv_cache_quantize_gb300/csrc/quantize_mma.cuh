@@ -17,8 +17,9 @@
 //  * RHT: the Walsh-Hadamard butterflies run in registers in the quad layout
 //    (strides 1..16 inside a thread, 32 and 64 across the quad);
 //  * S r: R split into bf16 hi/lo (16 bits) against S, which is exact in bf16.
-// Codes are decided from the fp32 y, and any coordinate within `guard` of a
-// boundary is re-decided from an fp64 dot product, as in quantize.cuh.
+// Codes are decided from the fp32 y by comparing |y| with the positive
+// boundaries (the codebook is symmetric), and any coordinate within `guard`
+// of a boundary is re-decided from an fp64 dot product, as in quantize.cuh.
 #pragma once
 
 #include "common.cuh"
@@ -27,7 +28,7 @@
 namespace tqk {
 
 constexpr int kQmWarps = 4;
-constexpr int kQmRowWords = 68;  // 128 bf16 + 8 pad = 272 B per smem row (conflict-free quads)
+constexpr int kQmRowWords = 68;  // operand tiles: 128 bf16 + 8 pad per row (conflict-free fragments)
 
 __device__ __forceinline__ void mma16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                               uint32_t b0, uint32_t b1) {
@@ -38,105 +39,137 @@ __device__ __forceinline__ void mma16816_bf16(float (&d)[4], uint32_t a0, uint32
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t bf16_bits(float v) { return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v)); }
+__device__ __forceinline__ void cp_async16_zfill(uint32_t smem_addr, const void* gptr, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_addr), "l"(gptr), "r"(valid ? 16 : 0));
+}
 
-// bf16 pair (lo half = a, hi half = b)
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) { return bf16_bits(a) | (bf16_bits(b) << 16); }
+// two floats -> bf16 pair (lo half = a), round to nearest even
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// fp32 staging tile: coordinate i of row r at r*144 + i + 4*(i/32); the skew
-// puts the four 32-coordinate blocks of a quad in different banks
-__device__ __forceinline__ int xpos(int r, int i) { return r * 144 + i + ((i >> 5) << 2); }
+// Raw staging tile of 16 input rows: element i of row r at byte
+// r * RSB + (i + SK * (i / 32)) * sizeof(XT). The per-32-element skew puts
+// the four blocks of a quad in different banks.
+template <typename XT>
+struct QmStage {
+    static constexpr int ESZ = sizeof(XT);
+    static constexpr int SK = 16 / ESZ;                    // 16-byte skew per block
+    static constexpr int RSB = (128 + 4 * SK) * ESZ;       // 320 (bf16) / 576 (fp32)
+    static constexpr int BYTES = 16 * RSB;
+    __device__ static int off(int r, int i) { return r * RSB + (i + SK * (i >> 5)) * ESZ; }
+};
 
-template <int NLIMB_X>
+template <typename XT>
+__device__ __forceinline__ float stage_at(const unsigned char* t, int r, int i) {
+    if constexpr (sizeof(XT) == 4) return *reinterpret_cast<const float*>(t + QmStage<XT>::off(r, i));
+    else return __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t*>(t + QmStage<XT>::off(r, i))) << 16);
+}
+
+template <typename XT, int NLIMB_X>
 struct QmSmem {
-    // per warp: fp32 copy of the tile (for norms, RHT and the fp64 path) and
-    // bf16 operand tiles (X limbs for the dense GEMM, then R hi/lo)
-    static constexpr int XF_BYTES = 16 * 144 * 4;                     // fp32 rows, see xpos()
-    static constexpr int AT = NLIMB_X > 2 ? NLIMB_X : 2;              // operand tiles
+    static constexpr int AT = NLIMB_X > 2 ? NLIMB_X : 2;  // operand tiles: X limbs, then R hi/lo
     static constexpr int AT_BYTES = AT * 16 * kQmRowWords * 4;
-    static constexpr int WARP_BYTES = XF_BYTES + AT_BYTES;
+    static constexpr int WARP_BYTES = 2 * QmStage<XT>::BYTES + AT_BYTES;  // double-buffered staging
 };
 
 template <typename XT, int CB, bool PROD, bool RHT>
 __global__ void __launch_bounds__(kQmWarps * 32) quantize_mma_kernel(const __grid_constant__ QuantParams p) {
     constexpr int D = 128;
     constexpr int L = 1 << CB;
+    constexpr int H = L / 2;
     constexpr int NLX = (!RHT && sizeof(XT) == 4) ? 3 : 1;  // limbs of X for the dense GEMM
-    using S = QmSmem<NLX>;
+    using S = QmSmem<XT, NLX>;
+    using ST = QmStage<XT>;
     extern __shared__ __align__(16) unsigned char smem[];
-    const uint2* b1 = reinterpret_cast<const uint2*>(smem);                      // dense: 3 limbs
-    const int b1_bytes = RHT ? 0 : 3 * 8 * 16 * 32 * 8;
-    const uint2* b2 = reinterpret_cast<const uint2*>(smem + b1_bytes);           // PROD: S fragments
-    const int b2_bytes = PROD ? 8 * 16 * 32 * 8 : 0;
-    unsigned char* wbase = smem + b1_bytes + b2_bytes;
+    constexpr int B1_BYTES = RHT ? 0 : 3 * 8 * 16 * 32 * 8;
+    constexpr int B2_BYTES = PROD ? 8 * 16 * 32 * 8 : 0;
+    const uint2* b1 = reinterpret_cast<const uint2*>(smem);
+    const uint2* b2 = reinterpret_cast<const uint2*>(smem + B1_BYTES);
     __shared__ float s_cent[kMaxLevels];
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
-    unsigned char* wsm = wbase + warp * S::WARP_BYTES;
-    float* xf = reinterpret_cast<float*>(wsm);                     // [16][144], see xpos()
-    uint32_t* at = reinterpret_cast<uint32_t*>(wsm + S::XF_BYTES);  // [AT][16][68]
+    unsigned char* xs_base = smem + B1_BYTES + B2_BYTES + warp * S::WARP_BYTES;  // 2 raw staging tiles
+    uint32_t* at = reinterpret_cast<uint32_t*>(xs_base + 2 * ST::BYTES);       // [AT][16][68]
+    const uint32_t xs_s = (uint32_t)__cvta_generic_to_shared(xs_base);
 
-    // ---- CTA set-up: B fragments and centroids into shared memory ----
+    // ---- CTA set-up: B fragments (cp.async, all in flight; completed by the
+    // first wait of the tile loop) and centroids into shared memory ----
     {
-        const uint4* src1 = reinterpret_cast<const uint4*>(p.pi_frag);
-        uint4* dst1 = reinterpret_cast<uint4*>(smem);
-        for (int i = threadIdx.x; i < b1_bytes / 16; i += blockDim.x) dst1[i] = src1[i];
-        const uint4* src2 = reinterpret_cast<const uint4*>(p.s_frag);
-        uint4* dst2 = reinterpret_cast<uint4*>(smem + b1_bytes);
-        for (int i = threadIdx.x; i < b2_bytes / 16; i += blockDim.x) dst2[i] = src2[i];
+        const uint32_t s0 = (uint32_t)__cvta_generic_to_shared(smem);
+        const unsigned char* src1 = reinterpret_cast<const unsigned char*>(p.pi_frag);
+#pragma unroll 8
+        for (int i = threadIdx.x; i < B1_BYTES / 16; i += blockDim.x) cp_async16_zfill(s0 + 16 * i, src1 + 16 * i, true);
+        const unsigned char* src2 = reinterpret_cast<const unsigned char*>(p.s_frag);
+#pragma unroll 8
+        for (int i = threadIdx.x; i < B2_BYTES / 16; i += blockDim.x)
+            cp_async16_zfill(s0 + B1_BYTES + 16 * i, src2 + 16 * i, true);
         if (threadIdx.x < kMaxLevels) s_cent[threadIdx.x] = p.cb.c[threadIdx.x];
     }
+    asm volatile("cp.async.commit_group;\n" ::);  // group: B fragments
     float sg[32];
     if constexpr (RHT) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) sg[j] = p.sgn[32 * c + j];
     }
-    __syncthreads();
 
     const int64_t ntiles = (p.n + 15) / 16;
-    for (int64_t tile = (int64_t)blockIdx.x * kQmWarps + warp; tile < ntiles; tile += (int64_t)gridDim.x * kQmWarps) {
-        const int64_t v0 = tile * 16;
-        // ---- stage X (16 rows) as fp32 in shared memory ----
-        {
-            constexpr int EPC = 16 / sizeof(XT);  // elements per 16-byte chunk
-            constexpr int CPR = D / EPC;          // chunks per row
-            for (int q = lane; q < 16 * CPR; q += 32) {
-                const int r = q / CPR, ch = q % CPR;
-                const int64_t v = v0 + r;
-                float* dst = xf + xpos(r, ch * EPC);
-                if (v < p.n) {
-                    const uint4 raw = *reinterpret_cast<const uint4*>(reinterpret_cast<const XT*>(p.x) + v * p.x_stride + ch * EPC);
-                    if constexpr (sizeof(XT) == 4) {
-                        *reinterpret_cast<uint4*>(dst) = raw;
-                    } else {
-                        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    const int64_t tstep = (int64_t)gridDim.x * kQmWarps;
+    // stage 16 input rows of `tile` into buffer `buf` with cp.async (zero-filled past n)
+    auto stage = [&](int64_t tile, int buf) {
+        constexpr int EPC = 16 / ST::ESZ;  // elements per 16-byte chunk
+        constexpr int CPR = D / EPC;       // chunks per row
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            dst[2 * k] = __uint_as_float(w[k] << 16);
-                            dst[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int k = 0; k < EPC; ++k) dst[k] = 0.0f;
-                }
-            }
+        for (int q = lane; q < 16 * CPR; q += 32) {
+            const int r = q / CPR, ch = q % CPR;
+            const int64_t v = tile * 16 + r;
+            const bool ok = v < p.n;
+            const XT* src = reinterpret_cast<const XT*>(p.x) + (ok ? v : 0) * p.x_stride + ch * EPC;
+            cp_async16_zfill(xs_s + buf * ST::BYTES + ST::off(r, ch * EPC), src, ok);
         }
+    };
+    int64_t tile = (int64_t)blockIdx.x * kQmWarps + warp;
+    if (tile < ntiles) stage(tile, 0);
+    asm volatile("cp.async.commit_group;\n" ::);  // group: first tile
+    asm volatile("cp.async.wait_group 1;\n" ::);  // B fragments landed (first tile may still fly)
+    __syncthreads();                               // ... for every warp of the CTA
+    for (int it = 0; tile < ntiles; tile += tstep, ++it) {
+        const int64_t v0 = tile * 16;
+        unsigned char* xs = xs_base + (it & 1) * ST::BYTES;
+        if (tile + tstep < ntiles) stage(tile + tstep, (it + 1) & 1);  // prefetch the next tile
+        asm volatile("cp.async.commit_group;\n" ::);
+        asm volatile("cp.async.wait_group 1;\n" ::);
         __syncwarp();
 
         // ---- quad layout: x of rows g, g+8, coordinates 32c..32c+31 ----
         float y[2][32];
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
-            const float4* src = reinterpret_cast<const float4*>(xf + xpos(g + 8 * rr, 32 * c));
+            const uint4* src = reinterpret_cast<const uint4*>(xs + ST::off(g + 8 * rr, 32 * c));
+            if constexpr (sizeof(XT) == 4) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float4 t = src[k];
-                y[rr][4 * k] = t.x;
-                y[rr][4 * k + 1] = t.y;
-                y[rr][4 * k + 2] = t.z;
-                y[rr][4 * k + 3] = t.w;
+                for (int k = 0; k < 8; ++k) {
+                    const uint4 t = src[k];
+                    y[rr][4 * k] = __uint_as_float(t.x);
+                    y[rr][4 * k + 1] = __uint_as_float(t.y);
+                    y[rr][4 * k + 2] = __uint_as_float(t.z);
+                    y[rr][4 * k + 3] = __uint_as_float(t.w);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint4 t = src[k];
+                    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        y[rr][8 * k + 2 * e] = bf16_lo(w[e]);
+                        y[rr][8 * k + 2 * e + 1] = bf16_hi(w[e]);
+                    }
+                }
             }
         }
         // norms (quad reduction), with a rescaled retry when squares under/overflow
@@ -186,13 +219,13 @@ __global__ void __launch_bounds__(kQmWarps * 32) quantize_mma_kernel(const __gri
                         }
 #pragma unroll
             for (int hb = 1; hb < 4; hb <<= 1) {
-                const bool upper = (c & hb) != 0;
+                const float sgn_self = (c & hb) ? -1.0f : 1.0f;  // upper half: o - y
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const float o = __shfl_xor_sync(TQ_FULL_MASK, y[rr][j], hb);
-                        y[rr][j] = upper ? (o - y[rr][j]) : (y[rr][j] + o);
+                        y[rr][j] = fmaf(sgn_self, y[rr][j], o);
                     }
             }
 #pragma unroll
@@ -202,19 +235,20 @@ __global__ void __launch_bounds__(kQmWarps * 32) quantize_mma_kernel(const __gri
                 for (int j = 0; j < 32; ++j) y[rr][j] *= sc;
             }
         } else {
-            // X limbs -> bf16 operand tiles (natural coordinate order)
-            for (int q = lane; q < 16 * 64; q += 32) {
-                const int r = q >> 6, w = q & 63;
-                const float a = xf[xpos(r, 2 * w)], b = xf[xpos(r, 2 * w + 1)];
-                if constexpr (NLX == 1) {
-                    at[r * kQmRowWords + w] = pack_bf16(a, b);
-                } else {
-                    const float a1 = __bfloat162float(__float2bfloat16_rn(a)), b1v = __bfloat162float(__float2bfloat16_rn(b));
-                    const float a2 = __bfloat162float(__float2bfloat16_rn(a - a1));
-                    const float b2v = __bfloat162float(__float2bfloat16_rn(b - b1v));
-                    at[r * kQmRowWords + w] = pack_bf16(a1, b1v);
-                    at[16 * kQmRowWords + r * kQmRowWords + w] = pack_bf16(a2, b2v);
-                    at[32 * kQmRowWords + r * kQmRowWords + w] = pack_bf16(a - a1 - a2, b - b1v - b2v);
+            // X limbs -> bf16 operand tiles, from this thread's own coordinates
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                uint32_t* t0 = at + (g + 8 * rr) * kQmRowWords + 16 * c;
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    const uint32_t h1 = pack_bf16(y[rr][j], y[rr][j + 1]);
+                    t0[j >> 1] = h1;
+                    if constexpr (NLX == 3) {
+                        const float r0 = y[rr][j] - bf16_lo(h1), r1 = y[rr][j + 1] - bf16_hi(h1);
+                        const uint32_t h2 = pack_bf16(r0, r1);
+                        t0[16 * kQmRowWords + (j >> 1)] = h2;
+                        t0[32 * kQmRowWords + (j >> 1)] = pack_bf16(r0 - bf16_lo(h2), r1 - bf16_hi(h2));
+                    }
                 }
             }
             __syncwarp();
@@ -259,8 +293,12 @@ __global__ void __launch_bounds__(kQmWarps * 32) quantize_mma_kernel(const __gri
             }
         }
 
-        // ---- bucketize with guard band ----
-        uint32_t idxw[2][4];  // packed codes: 32 coordinates x CB bits = CB words per row
+        // ---- bucketize with guard band; for keys y becomes the residual ----
+        // idx = #{t_j <= y}: with the symmetric codebook (t_{H-1} = 0, positive
+        // boundaries t_H..t_{L-2}) and k = #{positive t <= |y|},
+        // idx = H + k for y >= 0 and H - 1 - k for y < 0 (exact ties are inside
+        // the guard band and decided in fp64 below).
+        uint32_t idxw[2][4];
         uint32_t flag[2];
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
@@ -268,26 +306,33 @@ __global__ void __launch_bounds__(kQmWarps * 32) quantize_mma_kernel(const __gri
 #pragma unroll
             for (int w = 0; w < 4; ++w) idxw[rr][w] = 0u;
         }
-        const bool rowok0 = v0 + g < p.n, rowok1 = v0 + g + 8 < p.n;
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
+                const float yv = y[rr][j];
+                const float av = fabsf(yv);
                 int k = 0;
-                float dmin = 3.0e38f;
+                float dmin = av;
+                float cpos = p.cb.c[H];
 #pragma unroll
-                for (int t = 0; t < L - 1; ++t) {
-                    k += (y[rr][j] >= p.cb.t[t]) ? 1 : 0;
-                    dmin = fminf(dmin, fabsf(y[rr][j] - p.cb.t[t]));
+                for (int t = H; t < L - 1; ++t) {
+                    const bool ge = av >= p.cb.t[t];
+                    k += ge ? 1 : 0;
+                    if (PROD) cpos = ge ? p.cb.c[t + 1] : cpos;
+                    dmin = fminf(dmin, fabsf(av - p.cb.t[t]));
                 }
+                const bool pos = yv >= 0.0f;
+                const int idx = pos ? H + k : H - 1 - k;
                 if (!(dmin >= p.guard)) flag[rr] |= 1u << j;
+                if (PROD) y[rr][j] = pos ? yv - cpos : yv + cpos;
                 const int bit = CB * j;
-                idxw[rr][bit >> 5] |= (uint32_t)k << (bit & 31);
-                if ((bit & 31) + CB > 32) idxw[rr][(bit >> 5) + 1] |= (uint32_t)k >> (32 - (bit & 31));
+                idxw[rr][bit >> 5] |= (uint32_t)idx << (bit & 31);
+                if ((bit & 31) + CB > 32) idxw[rr][(bit >> 5) + 1] |= (uint32_t)idx >> (32 - (bit & 31));
             }
         }
-        if (!rowok0) flag[0] = 0u;
-        if (!rowok1) flag[1] = 0u;
+        if (v0 + g >= p.n) flag[0] = 0u;
+        if (v0 + g + 8 >= p.n) flag[1] = 0u;
 
         // fp16 norms; near an fp16 rounding midpoint they are re-rounded from fp64
         uint16_t n16[2];
@@ -303,25 +348,22 @@ __global__ void __launch_bounds__(kQmWarps * 32) quantize_mma_kernel(const __gri
             }
         }
 
-        // ---- fp64 re-decision of flagged coordinates (warp-cooperative) ----
+        // ---- fp64 re-decision of flagged coordinates (warp-cooperative, rare) ----
         if (__any_sync(TQ_FULL_MASK, (flag[0] | flag[1]) != 0u || nclose[0] || nclose[1])) {
-            // fp64 norms of the 16 rows: lane l sums coordinates 4l..4l+3 of each row
-            double n64[2] = {0.0, 0.0};
+            if (nclose[0] || nclose[1]) {
 #pragma unroll 1
-            for (int r = 0; r < 16; ++r) {
-                double s = 0.0;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const double xv = (double)xf[xpos(r, 4 * lane + k)];
-                    s = fma(xv, xv, s);
+                for (int rr = 0; rr < 2; ++rr) {
+                    double s = 0.0;
+#pragma unroll 8
+                    for (int j = 0; j < 32; ++j) {
+                        const double xv = (double)stage_at<XT>(xs, g + 8 * rr, 32 * c + j);
+                        s = fma(xv, xv, s);
+                    }
+                    s += __shfl_xor_sync(TQ_FULL_MASK, s, 1);
+                    s += __shfl_xor_sync(TQ_FULL_MASK, s, 2);
+                    if (nclose[rr]) n16[rr] = __half_as_ushort(__double2half(fmin(sqrt(s), 65504.0)));
                 }
-                s = warp_sum(s);
-                if (r == g) n64[0] = sqrt(s);
-                if (r == g + 8) n64[1] = sqrt(s);
             }
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr)
-                if (nclose[rr]) n16[rr] = __half_as_ushort(__double2half(fmin(n64[rr], 65504.0)));
             while (true) {
                 const unsigned bal = __ballot_sync(TQ_FULL_MASK, (flag[0] | flag[1]) != 0u);
                 if (!bal) break;
@@ -330,43 +372,35 @@ __global__ void __launch_bounds__(kQmWarps * 32) quantize_mma_kernel(const __gri
                 const int j_src = __shfl_sync(TQ_FULL_MASK, __ffs(flag[0] ? flag[0] : flag[1]) - 1, src);
                 const int row = (src >> 2) + 8 * rr_src;
                 const int i = 32 * (src & 3) + j_src;
-                double part = 0.0;
-                if constexpr (RHT) {
+                double part = 0.0, s2 = 0.0;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int e = 4 * lane + k;
-                        const double t = (double)p.sgn[e] * (double)xf[xpos(row, e)];
+                for (int k = 0; k < 4; ++k) {
+                    const int e = 4 * lane + k;
+                    const double xv = (double)stage_at<XT>(xs, row, e);
+                    s2 = fma(xv, xv, s2);
+                    if constexpr (RHT) {
+                        const double t = (double)p.sgn[e] * xv;
                         part += (__popc(i & e) & 1) ? -t : t;
+                    } else {
+                        part = fma(p.pi64[(size_t)i * D + e], xv, part);
                     }
-                } else {
-                    const double* prow = p.pi64 + (size_t)i * D;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) part = fma(prow[4 * lane + k], (double)xf[xpos(row, 4 * lane + k)], part);
                 }
                 part = warp_sum(part);
-                double nrow = 0.0;
-                {
-                    double s = 0.0;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const double xv = (double)xf[xpos(row, 4 * lane + k)];
-                        s = fma(xv, xv, s);
-                    }
-                    nrow = sqrt(warp_sum(s));
-                }
+                const double nrow = sqrt(warp_sum(s2));
                 double y64 = 0.0;
                 if (nrow > 0.0) y64 = RHT ? part / (sqrt((double)D) * nrow) : part / nrow;
                 if (lane == src) {
+                    int k = 0;
+#pragma unroll
+                    for (int t = 0; t < L - 1; ++t) k += (y64 >= p.cb.t64[t]) ? 1 : 0;
+                    const float nv = PROD ? (float)y64 - s_cent[k] : (float)y64;
 #pragma unroll
                     for (int rr = 0; rr < 2; ++rr) {
                         if (rr != rr_src) continue;
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
                             if (j != j_src) continue;
-                            int k = 0;
-#pragma unroll
-                            for (int t = 0; t < L - 1; ++t) k += (y64 >= p.cb.t64[t]) ? 1 : 0;
-                            y[rr][j] = (float)y64;
+                            y[rr][j] = nv;
                             const int bit = CB * j;
                             const uint32_t m0 = ((1u << CB) - 1u) << (bit & 31);
                             idxw[rr][bit >> 5] = (idxw[rr][bit >> 5] & ~m0) | ((uint32_t)k << (bit & 31));
@@ -406,13 +440,19 @@ __global__ void __launch_bounds__(kQmWarps * 32) quantize_mma_kernel(const __gri
         for (int rr = 0; rr < 2; ++rr) {
             if (slot[rr] < 0) continue;
             uint32_t* dst = reinterpret_cast<uint32_t*>(p.codes + slot[rr] * (int64_t)p.code_stride) + CB * c;
+            if constexpr (CB == 2) {
+                *reinterpret_cast<uint2*>(dst) = make_uint2(idxw[rr][0], idxw[rr][1]);
+            } else if constexpr (CB == 4) {
+                *reinterpret_cast<uint4*>(dst) = make_uint4(idxw[rr][0], idxw[rr][1], idxw[rr][2], idxw[rr][3]);
+            } else {
 #pragma unroll
-            for (int w = 0; w < CB; ++w) dst[w] = idxw[rr][w];
+                for (int w = 0; w < CB; ++w) dst[w] = idxw[rr][w];
+            }
             if (c == 0) p.norm[slot[rr]] = n16[rr];
         }
 
         if constexpr (PROD) {
-            // residual, gamma, and R as bf16 hi/lo tiles for the S r GEMM
+            // gamma and R as bf16 hi/lo tiles for the S r GEMM (y holds r)
             float gam[2];
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
@@ -421,17 +461,11 @@ __global__ void __launch_bounds__(kQmWarps * 32) quantize_mma_kernel(const __gri
                 uint32_t* tl = th + 16 * kQmRowWords;
 #pragma unroll
                 for (int j = 0; j < 32; j += 2) {
-                    const int bit0 = CB * j, bit1 = CB * (j + 1);
-                    const uint32_t k0 = ((bit0 & 31) + CB <= 32 ? (idxw[rr][bit0 >> 5] >> (bit0 & 31))
-                                                                 : __funnelshift_r(idxw[rr][bit0 >> 5], idxw[rr][(bit0 >> 5) + 1], bit0 & 31)) & (L - 1);
-                    const uint32_t k1 = ((bit1 & 31) + CB <= 32 ? (idxw[rr][bit1 >> 5] >> (bit1 & 31))
-                                                                 : __funnelshift_r(idxw[rr][bit1 >> 5], idxw[rr][(bit1 >> 5) + 1], bit1 & 31)) & (L - 1);
-                    const float r0 = y[rr][j] - s_cent[k0], r1 = y[rr][j + 1] - s_cent[k1];
+                    const float r0 = y[rr][j], r1 = y[rr][j + 1];
                     g2 = fmaf(r0, r0, fmaf(r1, r1, g2));
-                    const float h0 = __bfloat162float(__float2bfloat16_rn(r0));
-                    const float h1 = __bfloat162float(__float2bfloat16_rn(r1));
-                    th[j >> 1] = pack_bf16(h0, h1);
-                    tl[j >> 1] = pack_bf16(r0 - h0, r1 - h1);
+                    const uint32_t h = pack_bf16(r0, r1);
+                    th[j >> 1] = h;
+                    tl[j >> 1] = pack_bf16(r0 - bf16_lo(h), r1 - bf16_hi(h));
                 }
                 g2 += __shfl_xor_sync(TQ_FULL_MASK, g2, 1);
                 g2 += __shfl_xor_sync(TQ_FULL_MASK, g2, 2);
@@ -478,12 +512,13 @@ __global__ void __launch_bounds__(kQmWarps * 32) quantize_mma_kernel(const __gri
         }
         __syncwarp();
     }
+    asm volatile("cp.async.wait_group 0;\n" ::);
 }
 
 template <typename XT, int CB, bool PROD, bool RHT>
 size_t quantize_mma_smem() {
     constexpr int NLX = (!RHT && sizeof(XT) == 4) ? 3 : 1;
-    return (RHT ? 0 : 3 * 8 * 16 * 32 * 8) + (PROD ? 8 * 16 * 32 * 8 : 0) + (size_t)kQmWarps * QmSmem<NLX>::WARP_BYTES;
+    return (RHT ? 0 : 3 * 8 * 16 * 32 * 8) + (PROD ? 8 * 16 * 32 * 8 : 0) + (size_t)kQmWarps * QmSmem<XT, NLX>::WARP_BYTES;
 }
 
 }  // namespace tqk
