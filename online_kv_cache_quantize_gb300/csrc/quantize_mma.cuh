@@ -350,7 +350,8 @@ __global__ void __launch_bounds__(kQmWarps * 32) quantize_mma_kernel(const __gri
 
         // ---- fp64 re-decision of flagged coordinates (warp-cooperative, rare) ----
         if (__any_sync(TQ_FULL_MASK, (flag[0] | flag[1]) != 0u || nclose[0] || nclose[1])) {
-            if (nclose[0] || nclose[1]) {
+            // warp-uniform condition: the quad sums below shuffle over the full warp
+            if (__any_sync(TQ_FULL_MASK, nclose[0] || nclose[1])) {
 #pragma unroll 1
                 for (int rr = 0; rr < 2; ++rr) {
                     double s = 0.0;

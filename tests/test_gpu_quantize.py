@@ -75,6 +75,36 @@ def test_edge_vectors():
         _run(x, "mse", 4, d, kind, torch.float32, f"edge-{kind}-mse")
 
 
+@pytest.mark.parametrize("kind", ["dense", "rht"])
+@pytest.mark.parametrize("mode,bits", [("prod", 3), ("mse", 3)])
+def test_fp16_norm_midpoints(kind, mode, bits):
+    """Norms exactly halfway between two fp16 values in some rows of a tile and
+    not in the others: the fp64 re-rounding runs for part of a warp's rows and
+    must give the ties-to-even fp16 of the exact norm."""
+    d = 128
+    x = np.random.default_rng(17).standard_normal((48, d)).astype(np.float32)
+    # halfway points with 12 significant bits (squares exact in fp32); the
+    # third rounds up to the even neighbour, the others down
+    mids = [1.0 + 2.0 ** -11, 2049.0, 1.0 + 3 * 2.0 ** -11, 0.5 + 2.0 ** -12, 3.0 + 2.0 ** -10]
+    planted = [0, 5, 9, 16, 30, 33, 47]
+    for k, r in enumerate(planted):
+        mid = mids[k % len(mids)]
+        x[r] = 0.0
+        if k % 2 == 0:
+            x[r, (7 * k) % d] = mid                  # one-hot: the norm is the entry
+        else:
+            x[r, [3, 40, 77, 100]] = mid / 2.0       # four equal entries: norm 2|a|
+    cache = P.gpu_quantize(x, mode, bits, d, kind, dtype=torch.float32)
+    got = P.cache_to_numpy(cache, x.shape[0])
+    pi, s = P.oracle_mats(d, kind, None)
+    qz = oq.quantize(x.astype(np.float64), pi, mode, bits, s if mode == "prod" else None)
+    rows = np.array(planted)
+    assert np.array_equal(qz["n"][rows], np.array([mids[k % len(mids)] for k in range(len(planted))]))
+    assert np.array_equal(got["norm"][rows], qz["norm16"][rows]), "ties-to-even fp16 norm"
+    rep = P.compare_quantized(got, qz, mode, bits, d, s, label=f"fp16-mid-{kind}-{mode}{bits}")
+    assert rep["code_mismatch"] == 0
+
+
 @pytest.mark.parametrize("n", [1, 2, 31, 33])
 def test_ragged_counts(n):
     x = np.random.default_rng(n).standard_normal((n, 128)).astype(np.float32)
