@@ -27,7 +27,13 @@
 
 namespace tqk {
 
-constexpr int kQmWarps = 4;
+constexpr int kQmWarps = 4;  // warps per CTA (3 for fp32 input with the dense rotation)
+constexpr int kQmSmemLimit = 227 * 1024;
+
+// The dense rotation with fp32 input keeps three limbs of X per warp next to
+// the 96 KB of Pi^T fragments, so it runs 3 warps per CTA to stay in 227 KB.
+template <typename XT, bool RHT>
+constexpr int qm_warps() { return (!RHT && sizeof(XT) == 4) ? 3 : kQmWarps; }
 constexpr int kQmRowWords = 68;  // operand tiles: 128 bf16 + 8 pad per row (conflict-free fragments)
 
 __device__ __forceinline__ void mma16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -82,6 +88,7 @@ __global__ void __launch_bounds__(kQmWarps * 32) quantize_mma_kernel(const __gri
     constexpr int L = 1 << CB;
     constexpr int H = L / 2;
     constexpr int NLX = (!RHT && sizeof(XT) == 4) ? 3 : 1;  // limbs of X for the dense GEMM
+    constexpr int NW = qm_warps<XT, RHT>();
     using S = QmSmem<XT, NLX>;
     using ST = QmStage<XT>;
     extern __shared__ __align__(16) unsigned char smem[];
@@ -118,7 +125,7 @@ __global__ void __launch_bounds__(kQmWarps * 32) quantize_mma_kernel(const __gri
     }
 
     const int64_t ntiles = (p.n + 15) / 16;
-    const int64_t tstep = (int64_t)gridDim.x * kQmWarps;
+    const int64_t tstep = (int64_t)gridDim.x * NW;
     // stage 16 input rows of `tile` into buffer `buf` with cp.async (zero-filled past n)
     auto stage = [&](int64_t tile, int buf) {
         constexpr int EPC = 16 / ST::ESZ;  // elements per 16-byte chunk
@@ -132,7 +139,7 @@ __global__ void __launch_bounds__(kQmWarps * 32) quantize_mma_kernel(const __gri
             cp_async16_zfill(xs_s + buf * ST::BYTES + ST::off(r, ch * EPC), src, ok);
         }
     };
-    int64_t tile = (int64_t)blockIdx.x * kQmWarps + warp;
+    int64_t tile = (int64_t)blockIdx.x * NW + warp;
     if (tile < ntiles) stage(tile, 0);
     asm volatile("cp.async.commit_group;\n" ::);  // group: first tile
     asm volatile("cp.async.wait_group 1;\n" ::);  // B fragments landed (first tile may still fly)
@@ -517,9 +524,10 @@ __global__ void __launch_bounds__(kQmWarps * 32) quantize_mma_kernel(const __gri
 }
 
 template <typename XT, int CB, bool PROD, bool RHT>
-size_t quantize_mma_smem() {
+constexpr size_t quantize_mma_smem() {
     constexpr int NLX = (!RHT && sizeof(XT) == 4) ? 3 : 1;
-    return (RHT ? 0 : 3 * 8 * 16 * 32 * 8) + (PROD ? 8 * 16 * 32 * 8 : 0) + (size_t)kQmWarps * QmSmem<XT, NLX>::WARP_BYTES;
+    return (RHT ? 0 : 3 * 8 * 16 * 32 * 8) + (PROD ? 8 * 16 * 32 * 8 : 0) +
+           (size_t)qm_warps<XT, RHT>() * QmSmem<XT, NLX>::WARP_BYTES;
 }
 
 }  // namespace tqk
