@@ -19,8 +19,10 @@
  *     default stream). Argument errors are found on the host before any
  *     launch and return a status; a launch failure returns TQ_ERR_CUDA;
  *     faults during execution surface at the caller's next synchronisation.
- *   - No call blocks on the device and no kernel waits on a flag, so no call
- *     can hang; TQ_ERR_TIMEOUT is reserved.
+ *   - No call blocks on the device. The one kind of device-side wait (the
+ *     decode scan waiting for its bulk copies to land on an mbarrier) gives
+ *     up after one second, records the cause in the device error word and
+ *     lets the kernel return; tq_device_errors reads it (TQ_ERR_TIMEOUT).
  *   - tq_last_error() returns a thread-local message for the last failure.
  */
 #ifndef TQ_H
@@ -43,7 +45,7 @@ typedef enum {
     TQ_ERR_ALIGNMENT = 3,    /* a device pointer or stride breaks alignment  */
     TQ_ERR_CAPACITY = 4,     /* a slot range runs past the cache capacity    */
     TQ_ERR_CUDA = 5,         /* a CUDA runtime call failed                   */
-    TQ_ERR_TIMEOUT = 6,      /* reserved                                     */
+    TQ_ERR_TIMEOUT = 6,      /* a device-side wait ran out (tq_device_errors) */
     TQ_ERR_WORKSPACE = 7,    /* workspace missing or smaller than required   */
     TQ_ERR_NO_DEVICE_COPY = 8 /* handle not uploaded with *_to_device        */
 } tq_status;
@@ -266,6 +268,28 @@ typedef struct {
 
 size_t tq_score_topk_workspace(const tq_topk_args* a);
 tq_status tq_score_topk(const tq_topk_args* a, void* workspace, size_t ws_bytes, tq_stream stream);
+
+/* ------------------------------------------------------------------------ *
+ * Device error word.                                                       *
+ * ------------------------------------------------------------------------ *
+ * Library-level diagnostics; the pages define nothing of the kind. Each
+ * device the library runs on has one 32-bit error word, zero at load time.
+ * A bounded device-side wait that runs out sets a bit instead of spinning:
+ *   TQ_DEVERR_SCAN_WAIT      a decode scan tile's copies did not land within
+ *                            one second; that call's output is not valid
+ *   TQ_DEVERR_SELFTEST_WAIT  tq_selftest_bounded_wait ran out (its purpose)
+ * tq_device_errors synchronises the current device, stores the word in
+ * *flags_out (host, may be NULL), clears it when reset != 0, and returns
+ * TQ_ERR_TIMEOUT when any bit was set, TQ_OK when none was, TQ_ERR_CUDA when
+ * the device could not be read. */
+#define TQ_DEVERR_SCAN_WAIT 1u
+#define TQ_DEVERR_SELFTEST_WAIT 2u
+tq_status tq_device_errors(uint32_t* flags_out, int reset);
+
+/* Self-test of the bounded wait: launches one warp on `stream` that waits on
+ * an mbarrier nothing ever arrives on, for at most limit_us microseconds
+ * (1..1000000), then returns after setting TQ_DEVERR_SELFTEST_WAIT. */
+tq_status tq_selftest_bounded_wait(uint32_t limit_us, tq_stream stream);
 
 #ifdef __cplusplus
 }

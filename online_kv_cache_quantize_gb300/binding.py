@@ -16,6 +16,7 @@ _LIB_PATH = os.path.join(_PKG, "libtq.so")
 _lib = None
 
 TQ_OK = 0
+TQ_ERR_TIMEOUT = 6
 TQ_ROT_DENSE_QR, TQ_ROT_RHT = 0, 1
 TQ_MSE, TQ_PROD = 0, 1
 TQ_F32, TQ_BF16, TQ_F16 = 0, 1, 2
@@ -85,6 +86,8 @@ _SIGS = {
     "tq_attn_decode_static": (_STATUS, [ctypes.POINTER(tq_decode_args), ctypes.c_void_p]),
     "tq_score_topk_workspace": (ctypes.c_size_t, [ctypes.POINTER(tq_topk_args)]),
     "tq_score_topk": (_STATUS, [ctypes.POINTER(tq_topk_args), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "tq_device_errors": (_STATUS, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
+    "tq_selftest_bounded_wait": (_STATUS, [ctypes.c_uint32, ctypes.c_void_p]),
 }
 
 EXPORTED = tuple(_SIGS)
@@ -314,6 +317,24 @@ def tq_attn_decode_static(q, kcache, vcache, seq_lens, max_seq_len, rot, qjl, ou
     device memory; its scratch is an array inside the library (see tq.h)."""
     a, _keep = _decode_struct(q, kcache, vcache, seq_lens, max_seq_len, rot, qjl, out, **kw)
     _check(load().tq_attn_decode_static(ctypes.byref(a), _stream_ptr(stream)), "tq_attn_decode_static")
+
+
+TQ_DEVERR_SCAN_WAIT = 1
+TQ_DEVERR_SELFTEST_WAIT = 2
+
+
+def tq_device_errors(reset=False):
+    """(status, flags) of the current device's error word; synchronises the device."""
+    v = ctypes.c_uint32(0)
+    st = load().tq_device_errors(ctypes.byref(v), 1 if reset else 0)
+    if st not in (TQ_OK, TQ_ERR_TIMEOUT):
+        _check(st, "tq_device_errors")
+    return st, v.value
+
+
+def tq_selftest_bounded_wait(limit_us, stream=None):
+    """One warp waits on an mbarrier nothing arrives on, at most limit_us."""
+    _check(load().tq_selftest_bounded_wait(limit_us, _stream_ptr(stream)), "tq_selftest_bounded_wait")
 
 
 def _topk_struct(queries, db, n_db, rot, qjl, k, ids, scores):

@@ -428,6 +428,8 @@ tq_status tq_attn_decode(const tq_decode_args* a, void* workspace, size_t ws_byt
     if (a->k.capacity != a->v.capacity) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: k and v capacity differ");
     if (a->max_seq_len > a->k.capacity) return fail(TQ_ERR_CAPACITY, "tq_attn_decode: max_seq_len exceeds the capacity");
     if (a->k.capacity % 16) return fail(TQ_ERR_ALIGNMENT, "tq_attn_decode: cache capacity must be a multiple of 16");
+    if (!aligned(a->k.norm, 16) || !aligned(a->k.rnorm, 16) || !aligned(a->v.norm, 16) || !aligned(a->v.codes, 16))
+        return fail(TQ_ERR_ALIGNMENT, "tq_attn_decode: every cache plane must be 16-byte aligned (bulk copies)");
     if ((s = check_rot(a->rot, a->d)) != TQ_OK) return s;
     if ((s = check_qjl(a->qjl, a->k.m, a->d)) != TQ_OK) return s;
     if (!a->q || !a->out || !a->seq_lens) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: q/out/seq_lens is NULL");
@@ -509,6 +511,7 @@ tq_status tq_attn_decode(const tq_decode_args* a, void* workspace, size_t ws_byt
     dp.partial = part;
     dp.logits = a->logits;
     dp.max_seq_len = a->max_seq_len;
+    if ((e = tqk::device_error_word(&dp.err)) != cudaSuccess) return cuda_status(e, "tq_attn_decode error word");
     if (a->scan_begin && (e = cudaEventRecord((cudaEvent_t)a->scan_begin, st)) != cudaSuccess)
         return cuda_status(e, "tq_attn_decode scan_begin");
     e = tqk::launch_decode_mma(dp, kb, vb, st);
@@ -616,6 +619,30 @@ tq_status tq_score_topk(const tq_topk_args* a, void* workspace, size_t ws_bytes,
     tp.scores = a->scores;
     e = tqk::launch_topk(tp, cb, prod ? 1 : 0, st);
     return cuda_status(e, "tq_score_topk");
+}
+
+tq_status tq_device_errors(uint32_t* flags_out, int reset) {
+    uint32_t* word = nullptr;
+    cudaError_t e = tqk::device_error_word(&word);
+    if (e != cudaSuccess) return cuda_status(e, "tq_device_errors");
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_status(e, "tq_device_errors");
+    uint32_t v = 0;
+    if ((e = cudaMemcpy(&v, word, sizeof(v), cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_status(e, "tq_device_errors read");
+    if (reset && (e = cudaMemset(word, 0, sizeof(v))) != cudaSuccess) return cuda_status(e, "tq_device_errors reset");
+    if (reset && (e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_status(e, "tq_device_errors reset");
+    if (flags_out) *flags_out = v;
+    return v ? fail(TQ_ERR_TIMEOUT, "tq_device_errors: a device-side wait ran out (flags " + std::to_string(v) + ")")
+             : TQ_OK;
+}
+
+tq_status tq_selftest_bounded_wait(uint32_t limit_us, tq_stream stream) {
+    if (limit_us < 1 || limit_us > 1000000) return fail(TQ_ERR_INVALID_ARG, "tq_selftest_bounded_wait: limit_us must be 1..1000000");
+    uint32_t* word = nullptr;
+    cudaError_t e = tqk::device_error_word(&word);
+    if (e != cudaSuccess) return cuda_status(e, "tq_selftest_bounded_wait");
+    e = tqk::launch_wait_selftest(word, (uint64_t)limit_us * 1000ull, (cudaStream_t)stream);
+    return cuda_status(e, "tq_selftest_bounded_wait");
 }
 
 }  // extern "C"

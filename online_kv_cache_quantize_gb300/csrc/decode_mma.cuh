@@ -21,11 +21,14 @@
 // 32c..32c+31; values: tokens 4c..4c+3) and the value M dimension too (row g
 // holds coordinates 16g..16g+15), so each thread reads contiguous code bits.
 //
-// Tiles are staged per warp with cp.async in a 4-deep ring; the capacity of
-// the cache must be a multiple of 16 so that a tile never leaves its row.
+// Tiles are staged per warp in a 4-deep ring of shared-memory buffers, each
+// filled by six bulk (TMA) copies -- one per cache plane, issued by lanes 0..5
+// in one instruction -- that complete on the buffer's mbarrier. The capacity
+// of the cache must be a multiple of 16 so that a tile never leaves its row.
 #pragma once
 
 #include "common.cuh"
+#include "pipeline.cuh"
 #include "tq_launch.h"
 
 namespace tqk {
@@ -57,13 +60,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-
-__device__ __forceinline__ void cp_async16(uint32_t smem_addr, const void* gptr) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr), "l"(gptr));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
@@ -115,6 +111,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(const __grid
     __shared__ uint32_t klo[KLO ? KL : 1];
     __shared__ uint32_t vlut[VL];
     __shared__ __align__(8) uint2 slut4[16];  // 4 sign bits -> (+-1, +-1), (+-1, +-1) as fp16
+    __shared__ __align__(8) uint64_t s_bar[kMmaWarps][kMmaStages];  // one per ring buffer
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
@@ -124,6 +121,12 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(const __grid
     if constexpr (KLO)
         for (int i = threadIdx.x; i < KL; i += blockDim.x) klo[i] = p.klut_lo[i];
     for (int i = threadIdx.x; i < VL; i += blockDim.x) vlut[i] = p.vlut[i];
+    const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(&s_bar[warp][0]);
+    if (lane == 0) {
+#pragma unroll
+        for (int st = 0; st < kMmaStages; ++st) mbar_init(bar0 + 8 * st, 1);
+        mbar_init_fence();
+    }
     if (threadIdx.x < 16) {
         const uint32_t pos = 0x3C00u, neg = 0xBC00u, e = threadIdx.x;
         slut4[e].x = ((e & 1) ? pos : neg) | (((e & 2) ? pos : neg) << 16);
@@ -137,6 +140,43 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(const __grid
     const int ntiles = t1 > t0 ? (t1 - t0 + 15) >> 4 : 0;
     const int nmine = ntiles > warp ? (ntiles - warp + kMmaWarps - 1) / kMmaWarps : 0;
     const int64_t rowbase = ((int64_t)b * p.hkv + kv) * p.capacity;
+
+    unsigned char* wst = stages + warp * kMmaStages * T::BYTES;
+    const uint32_t wst_s = (uint32_t)__cvta_generic_to_shared(wst);
+    // lane k < 6 copies cache plane k of a tile: its source for the warp's
+    // first tile, the byte step to the warp's next tile (64 tokens further
+    // on), its offset inside the buffer and its size
+    const unsigned char* csrc = nullptr;
+    int64_t cstep = 0;
+    uint32_t coff = 0, cbytes = 0;
+    {
+        const int64_t slot0 = rowbase + t0 + 16 * warp;
+        constexpr int64_t TS = 16 * kMmaWarps;  // tokens between a warp's tiles
+        switch (lane) {
+            case 0: csrc = p.kcodes + slot0 * (16 * KB); cstep = TS * 16 * KB; coff = T::OFF_KC; cbytes = T::KC; break;
+            case 1: csrc = p.ksigns + slot0 * 16; cstep = TS * 16; coff = T::OFF_SG; cbytes = T::SG; break;
+            case 2: csrc = reinterpret_cast<const unsigned char*>(p.knorm + slot0); cstep = TS * 2; coff = T::OFF_KN; cbytes = T::NB; break;
+            case 3: csrc = reinterpret_cast<const unsigned char*>(p.krnorm + slot0); cstep = TS * 2; coff = T::OFF_KR; cbytes = T::NB; break;
+            case 4: csrc = p.vcodes + slot0 * (16 * VB); cstep = TS * 16 * VB; coff = T::OFF_VC; cbytes = T::VC; break;
+            case 5: csrc = reinterpret_cast<const unsigned char*>(p.vnorm + slot0); cstep = TS * 2; coff = T::OFF_VN; cbytes = T::NB; break;
+            default: break;
+        }
+    }
+    // fill ring buffer i % stages with the warp's tile i
+    auto issue = [&](int i) {
+        const int sb = i % kMmaStages;
+        const uint32_t bar = bar0 + 8 * sb;
+        if (lane == 0) {
+            fence_proxy_async_smem();  // the warp's earlier reads of this buffer come first
+            mbar_arrive_expect_tx(bar, T::BYTES);
+        }
+        if (lane < 6) bulk_g2s(wst_s + sb * T::BYTES + coff, csrc + i * cstep, cbytes, bar);
+    };
+
+    __syncwarp();  // this warp's barriers are initialised (lane 0) before any lane uses them
+#pragma unroll
+    for (int sb = 0; sb < kMmaStages; ++sb)
+        if (sb < nmine) issue(sb);  // the first tiles fly while the B fragments are built
 
     // ---- B fragments (static for the CTA) ----
     uint32_t bk[NT][8][2], bs[NT][8][2];
@@ -175,56 +215,17 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(const __grid
 #pragma unroll
             for (int r = 0; r < 4; ++r) acc[nt][mt][r] = 0.0f;
     }
-    __syncthreads();
 
-    unsigned char* wst = stages + warp * kMmaStages * T::BYTES;
-    const uint32_t wst_s = (uint32_t)__cvta_generic_to_shared(wst);
-    // this lane's chunks of a tile: source for the warp's first tile and the
-    // byte step to its next tile (4 tiles = 64 tokens further on)
-    constexpr int NQ = (T::CHUNKS + 31) / 32;
-    const unsigned char* qsrc[NQ];
-    int64_t qstep[NQ];
-    {
-        const int64_t slot0 = rowbase + t0 + 16 * warp;
-        constexpr int64_t TS = 16 * kMmaWarps;  // tokens between a warp's tiles
-#pragma unroll
-        for (int k = 0; k < NQ; ++k) {
-            const int off = (lane + 32 * k) * 16;
-            const unsigned char* src = p.kcodes;
-            int64_t step = 0;
-            if (off < T::OFF_SG) { src = p.kcodes + slot0 * (16 * KB) + off; step = TS * 16 * KB; }
-            else if (off < T::OFF_KN) { src = p.ksigns + slot0 * 16 + (off - T::OFF_SG); step = TS * 16; }
-            else if (off < T::OFF_KR) { src = reinterpret_cast<const unsigned char*>(p.knorm + slot0) + (off - T::OFF_KN); step = TS * 2; }
-            else if (off < T::OFF_VC) { src = reinterpret_cast<const unsigned char*>(p.krnorm + slot0) + (off - T::OFF_KR); step = TS * 2; }
-            else if (off < T::OFF_VN) { src = p.vcodes + slot0 * (16 * VB) + (off - T::OFF_VC); step = TS * 16 * VB; }
-            else if (off < T::BYTES) { src = reinterpret_cast<const unsigned char*>(p.vnorm + slot0) + (off - T::OFF_VN); step = TS * 2; }
-            qsrc[k] = src;
-            qstep[k] = step;
-        }
-    }
-    auto issue = [&](int i) {
-        const uint32_t dst = wst_s + (i % kMmaStages) * T::BYTES;
-#pragma unroll
-        for (int k = 0; k < NQ; ++k) {
-            const int off = (lane + 32 * k) * 16;
-            if (off < T::BYTES) cp_async16(dst + off, qsrc[k] + i * qstep[k]);
-        }
-    };
-
-#pragma unroll
-    for (int s = 0; s < kMmaStages - 1; ++s) {
-        if (s < nmine) issue(s);
-        cp_async_commit();
-    }
-
+    __syncthreads();  // lookup tables filled
     const float inv_lk = p.inv_lam_k, inv_lv = p.inv_lam_v;
     uint16_t* wps = ps + warp * NT * 8 * 16;
 
-    for (int i = 0; i < nmine; ++i) {
-        if (i + kMmaStages - 1 < nmine) issue(i + kMmaStages - 1);
-        cp_async_commit();
-        cp_async_wait<kMmaStages - 1>();
-        __syncwarp();
+    int i = 0;
+    for (; i < nmine; ++i) {
+        // warp-uniform outcome of the bounded wait on this tile's buffer
+        const bool landed = mbar_wait_bounded(bar0 + 8 * (i % kMmaStages), (i / kMmaStages) & 1, kWaitLimitNs,
+                                              p.err, kErrScanWait);
+        if (!__all_sync(TQ_FULL_MASK, landed)) break;
         const unsigned char* st = wst + (i % kMmaStages) * T::BYTES;
         const int tok0 = t0 + 16 * (warp + kMmaWarps * i);
 
@@ -355,8 +356,15 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(const __grid
             for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt][mt], a0, a1, a2, a3, bv[nt][0], bv[nt][1]);
         }
         __syncwarp();
+        if (i + kMmaStages < nmine) issue(i + kMmaStages);  // refill the buffer just consumed
     }
-    cp_async_wait<0>();
+    if (i < nmine) {
+        // a copy did not land in time (the error word says so and this
+        // split's output is not valid): wait, bounded, for the copies still
+        // in flight before the buffers are reused below
+        for (int j = i; j < nmine && j < i + kMmaStages; ++j)
+            mbar_wait_bounded(bar0 + 8 * (j % kMmaStages), (j / kMmaStages) & 1, kWaitLimitNs, p.err, kErrScanWait);
+    }
     __syncthreads();
 
     // ---- merge the warps of the CTA and write this split's partials ----
@@ -383,7 +391,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(const __grid
         }
     }
     __syncthreads();
-    const int i = threadIdx.x;  // coordinate 0..127
+    const int ci = threadIdx.x;  // coordinate 0..127
 #pragma unroll
     for (int h = 0; h < G; ++h) {
         float mstar = -INFINITY;
@@ -395,12 +403,12 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(const __grid
             const float mw = s_mz[(w * G + h) * 2];
             const float wt = (mw == -INFINITY) ? 0.0f : exp2f(mw - mstar);
             z = fmaf(s_mz[(w * G + h) * 2 + 1], wt, z);
-            a = fmaf(s_acc[(w * G + h) * D + i], wt, a);
+            a = fmaf(s_acc[(w * G + h) * D + ci], wt, a);
         }
         const int row = b * p.hq + (p.use_table ? (int)p.head_table[kv * G + h] : kv * G + h);
         float* out = p.partial + ((int64_t)row * p.n_splits + split) * (D + 2);
-        out[i] = a;
-        if (i == 0) {
+        out[ci] = a;
+        if (ci == 0) {
             out[D] = mstar;
             out[D + 1] = z;
         }

@@ -96,9 +96,16 @@ struct DecodeParams {
     uint32_t klut_lo[256];  // residual table lam*c - fp16(lam*c), used for 3-4 bit key codes
     uint32_t vlut[256];
     float inv_lam_k, inv_lam_v;
+    uint32_t* err;          // device error word (a wait that ran out sets a bit)
 };
 
 cudaError_t launch_decode_mma(const DecodeParams& p, int kbits, int vbits, cudaStream_t s);
+
+// The library's device error word of the current device (bits kErr* of
+// pipeline.cuh), and a kernel that waits on an mbarrier that nothing
+// arrives on for at most limit_ns, so that the bounded wait runs out.
+cudaError_t device_error_word(uint32_t** out);
+cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t s);
 
 
 struct CombineParams {

@@ -83,23 +83,30 @@ def test_fp16_norm_midpoints(kind, mode, bits):
     must give the ties-to-even fp16 of the exact norm."""
     d = 128
     x = np.random.default_rng(17).standard_normal((48, d)).astype(np.float32)
-    # halfway points with 12 significant bits (squares exact in fp32); the
-    # third rounds up to the even neighbour, the others down
-    mids = [1.0 + 2.0 ** -11, 2049.0, 1.0 + 3 * 2.0 ** -11, 0.5 + 2.0 ** -12, 3.0 + 2.0 ** -10]
-    planted = [0, 5, 9, 16, 30, 33, 47]
+    # one-hot rows: the norm is the entry, a halfway point with 12 significant
+    # bits (the third rounds up to its even neighbour, the others down)
+    onehot = [1.0 + 2.0 ** -11, 2049.0, 1.0 + 3 * 2.0 ** -11, 0.5 + 2.0 ** -12]
+    # two-entry rows (a, b) with a^2 + b^2 = c^2 exactly in fp32 and c a
+    # halfway point; a != b, so no rotated coordinate cancels to a tie at 0
+    pairs = [(1995.0, 476.0, 2051.0), (1475.0, 1428.0, 2053.0),
+             (1995.0 / 2048, 476.0 / 2048, 2051.0 / 2048), (1475.0 / 4096, 1428.0 / 4096, 2053.0 / 4096)]
+    planted, want_n = [0, 5, 9, 16, 30, 33, 40, 47], []
     for k, r in enumerate(planted):
-        mid = mids[k % len(mids)]
         x[r] = 0.0
         if k % 2 == 0:
-            x[r, (7 * k) % d] = mid                  # one-hot: the norm is the entry
+            x[r, (7 * k) % d] = onehot[k // 2]
+            want_n.append(onehot[k // 2])
         else:
-            x[r, [3, 40, 77, 100]] = mid / 2.0       # four equal entries: norm 2|a|
+            a, b, c = pairs[k // 2]
+            x[r, 11 + k] = a
+            x[r, 70 + k] = -b
+            want_n.append(c)
     cache = P.gpu_quantize(x, mode, bits, d, kind, dtype=torch.float32)
     got = P.cache_to_numpy(cache, x.shape[0])
     pi, s = P.oracle_mats(d, kind, None)
     qz = oq.quantize(x.astype(np.float64), pi, mode, bits, s if mode == "prod" else None)
     rows = np.array(planted)
-    assert np.array_equal(qz["n"][rows], np.array([mids[k % len(mids)] for k in range(len(planted))]))
+    assert np.array_equal(qz["n"][rows], np.array(want_n))
     assert np.array_equal(got["norm"][rows], qz["norm16"][rows]), "ties-to-even fp16 norm"
     rep = P.compare_quantized(got, qz, mode, bits, d, s, label=f"fp16-mid-{kind}-{mode}{bits}")
     assert rep["code_mismatch"] == 0
