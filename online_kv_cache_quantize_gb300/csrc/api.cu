@@ -166,7 +166,7 @@ void pair_table_lo(const std::vector<double>& c, int bits, double lam, uint32_t*
 
 struct DecodePlan {
     int n_splits = 1, chunk = 1, group = 1;
-    size_t off_q = 0, off_u = 0, off_part = 0, total = 0;
+    size_t off_frag = 0, off_part = 0, total = 0;
 };
 
 tq_status plan_decode(const tq_decode_args* a, DecodePlan* pl) {
@@ -196,9 +196,8 @@ tq_status plan_decode(const tq_decode_args* a, DecodePlan* pl) {
     pl->n_splits = splits;
     pl->chunk = chunk;
     const size_t rows = (size_t)a->batch * a->hq;
-    pl->off_q = 0;
-    pl->off_u = round_up(rows * a->d * sizeof(float), 256);
-    pl->off_part = pl->off_u + round_up(rows * 128 * sizeof(float), 256);
+    pl->off_frag = 0;
+    pl->off_part = round_up(rows * tqk::kFragWords * sizeof(uint32_t), 256);
     pl->total = pl->off_part + round_up(rows * (size_t)splits * (a->d + 2) * sizeof(float), 256);
     return TQ_OK;
 }
@@ -451,8 +450,7 @@ tq_status tq_attn_decode(const tq_decode_args* a, void* workspace, size_t ws_byt
         dp.use_table = 1;
     }
     char* ws = (char*)workspace;
-    float* qprime = (float*)(ws + pl.off_q);
-    float* u = (float*)(ws + pl.off_u);
+    uint32_t* frag = (uint32_t*)(ws + pl.off_frag);
     float* part = (float*)(ws + pl.off_part);
     cudaStream_t st = (cudaStream_t)stream;
 
@@ -468,16 +466,15 @@ tq_status tq_attn_decode(const tq_decode_args* a, void* workspace, size_t ws_byt
     pp.rht = a->rot->kind == TQ_ROT_RHT;
     pp.inv_sqrt_d = (float)(1.0 / std::sqrt((double)a->d));
     pp.st32 = a->qjl->d_st32;
-    pp.qprime = qprime;
-    pp.u = u;
+    pp.frag = frag;
+    pp.qjl_scale = (float)(std::sqrt(M_PI / 2.0) / a->k.m);
     cudaError_t e = tqk::launch_query_prep(pp, st);
     if (e != cudaSuccess) return cuda_status(e, "tq_attn_decode query prep");
 
     std::vector<double> kc, kt, vc, vt;
     if ((s = tq::codebook(a->d, kb, kc, kt)) != TQ_OK) return s;
     if ((s = tq::codebook(a->d, vb, vc, vt)) != TQ_OK) return s;
-    dp.qprime = qprime;
-    dp.u = u;
+    dp.frag = frag;
     dp.batch = a->batch;
     dp.hq = a->hq;
     dp.hkv = a->hkv;

@@ -15,6 +15,32 @@ namespace tqk {
 
 constexpr int kPrepWarps = 8;
 
+// fp16 bits of v (lo = 0) or of v - fp16(v) (lo = 1)
+__device__ __forceinline__ uint32_t half_split(float v, int lo) {
+    __half h = __float2half_rn(v);
+    if (lo) h = __float2half_rn(v - __half2float(h));
+    return (uint32_t)__half_as_ushort(h);
+}
+
+// The decode scan's B operands of one query row (d = m = 128), in the order
+// its threads load them: word ((ks * 2 + lo) * 4 + c) * 16 + 2 * kk + r holds
+// the fp16 pair (coordinates i, i + 1), i = 32c + 4kk + 2r, of the hi (lo =
+// 0) or lo (lo = 1) split of q' (ks = 0) or of qjl_scale * u (ks = 1). The
+// 256 threads of the CTA write one word each; u == NULL gives zero words.
+__device__ __forceinline__ void write_frag(const PrepParams& p, int64_t row, const float* s_q, const float* s_u,
+                                           int tid) {
+    if (tid >= kFragWords) return;
+    const int ks = tid >> 7, lo = (tid >> 6) & 1, c = (tid >> 4) & 3, kk = (tid >> 1) & 7, r = tid & 1;
+    const int i = 32 * c + 4 * kk + 2 * r;
+    uint32_t w = 0u;
+    if (ks == 0) {
+        w = half_split(s_q[i], lo) | (half_split(s_q[i + 1], lo) << 16);
+    } else if (s_u) {
+        w = half_split(s_u[i] * p.qjl_scale, lo) | (half_split(s_u[i + 1] * p.qjl_scale, lo) << 16);
+    }
+    p.frag[row * kFragWords + tid] = w;
+}
+
 // ---------------------------------------------------------------------------
 // One CTA per query row. Lane l of every warp owns outputs VPL*l..VPL*l+VPL-1
 // and warp w accumulates the inputs j = w, w+8, ...: the rows of the
@@ -101,8 +127,12 @@ __global__ void __launch_bounds__(kPrepWarps * 32) query_prep_kernel(const __gri
         }
     }
     __syncthreads();
-    for (int i = tid; i < d; i += blockDim.x) p.qprime[row * d + i] = s_y[i];
-    if (p.u == nullptr) return;
+    if (p.qprime)
+        for (int i = tid; i < d; i += blockDim.x) p.qprime[row * d + i] = s_y[i];
+    if (p.st32 == nullptr) {
+        if (p.frag) write_frag(p, row, s_y, nullptr, tid);
+        return;
+    }
     // u = S q': warp w takes inputs i = w, w+8, ...; lane owns outputs MPL*lane + r
     const int m = p.m, mpl = (m + 31) >> 5;
     float acc[8];
@@ -137,7 +167,12 @@ __global__ void __launch_bounds__(kPrepWarps * 32) query_prep_kernel(const __gri
         float u = 0.0f;
 #pragma unroll
         for (int w = 0; w < kPrepWarps; ++w) u += s_part[w][j];
-        p.u[row * m + j] = u;
+        if (p.u) p.u[row * m + j] = u;
+        s_x[j] = u;  // s_x is free by now
+    }
+    if (p.frag) {
+        __syncthreads();
+        write_frag(p, row, s_y, s_x, tid);
     }
 }
 

@@ -96,7 +96,7 @@ __device__ __forceinline__ T lds_at(const void* base, uint32_t byte_off) {
 }
 
 template <int KB, int VB, int G>
-__global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_kernel(const __grid_constant__ DecodeParams p) {
     using T = MmaTile<KB, VB>;
     constexpr int NT = (G + 3) / 4;   // n-tiles of 4 heads (x hi/lo)
     constexpr int KL = 1 << (2 * KB);  // key pair-table entries
@@ -178,7 +178,8 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(const __grid
     for (int sb = 0; sb < kMmaStages; ++sb)
         if (sb < nmine) issue(sb);  // the first tiles fly while the B fragments are built
 
-    // ---- B fragments (static for the CTA) ----
+    // ---- B fragments (static for the CTA), written by the query prep in the
+    // order this thread reads them: 16 words of q' and 16 of kappa u ----
     uint32_t bk[NT][8][2], bs[NT][8][2];
     int qrow[NT];
 #pragma unroll
@@ -186,20 +187,26 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(const __grid
         const int hb = nt * 4 + (g >> 1);  // head of B column n = g
         const int lo = g & 1;
         const bool ok = hb < G;
-        int row = 0;
-        if (ok) row = b * p.hq + (p.use_table ? (int)p.head_table[kv * G + hb] : kv * G + hb);
-        const float* qp = p.qprime + (int64_t)row * D;
-        const float* up = p.u + (int64_t)row * D;
+        uint4 wk[4], ws[4];
+        if (ok) {
+            const int row = b * p.hq + (p.use_table ? (int)p.head_table[kv * G + hb] : kv * G + hb);
+            const uint4* fk = reinterpret_cast<const uint4*>(p.frag + (int64_t)row * kFragWords + (lo * 4 + c) * 16);
+            const uint4* fs = fk + (2 * 4 * 16) / 4;  // ks = 1
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int i0 = 32 * c + 4 * kk + 2 * r;
-                const float q0 = ok ? qp[i0] : 0.0f, q1 = ok ? qp[i0 + 1] : 0.0f;
-                const float u0 = ok ? up[i0] * p.qjl_scale : 0.0f, u1 = ok ? up[i0 + 1] * p.qjl_scale : 0.0f;
-                bk[nt][kk][r] = split_half(q0, lo) | (split_half(q1, lo) << 16);
-                bs[nt][kk][r] = split_half(u0, lo) | (split_half(u1, lo) << 16);
+            for (int j = 0; j < 4; ++j) {
+                wk[j] = __ldg(fk + j);
+                ws[j] = __ldg(fs + j);
             }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) wk[j] = ws[j] = make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {  // words 4j .. 4j+3 = (kk, r) = (2j, 0), (2j, 1), (2j+1, 0), (2j+1, 1)
+            bk[nt][2 * j][0] = wk[j].x; bk[nt][2 * j][1] = wk[j].y;
+            bk[nt][2 * j + 1][0] = wk[j].z; bk[nt][2 * j + 1][1] = wk[j].w;
+            bs[nt][2 * j][0] = ws[j].x; bs[nt][2 * j][1] = ws[j].y;
+            bs[nt][2 * j + 1][0] = ws[j].z; bs[nt][2 * j + 1][1] = ws[j].w;
         }
         const int hc = nt * 4 + c;  // head whose logits this thread owns
         qrow[nt] = hc < G ? b * p.hq + (p.use_table ? (int)p.head_table[kv * G + hc] : kv * G + hc) : -1;
@@ -244,14 +251,18 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(const __grid
         }
         const uint32_t sw0 = reinterpret_cast<const uint32_t*>(st + T::OFF_SG + g * 16)[c];
         const uint32_t sw1 = reinterpret_cast<const uint32_t*>(st + T::OFF_SG + (g + 8) * 16)[c];
-        float dk[NT][4], ds[NT][4];
+        // two accumulator chains per product (even and odd kk) so that
+        // consecutive MMAs do not wait on each other
+        float dk[2][NT][4], ds[2][NT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int e = 0; e < 2; ++e)
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                dk[nt][r] = 0.0f;
-                ds[nt][r] = 0.0f;
-            }
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    dk[e][nt][r] = 0.0f;
+                    ds[e][nt][r] = 0.0f;
+                }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
             const uint32_t f0 = field4(kw0, 4 * KB * kk, 2 * KB), f1 = field4(kw1, 4 * KB * kk, 2 * KB);
@@ -263,7 +274,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(const __grid
                 const uint32_t l0 = lds_at<uint32_t>(klo, f0), l1 = lds_at<uint32_t>(klo, f1);
                 const uint32_t l2 = lds_at<uint32_t>(klo, f2), l3 = lds_at<uint32_t>(klo, f3);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma16816(dk[nt], l0, l1, l2, l3, bk[nt][kk][0], bk[nt][kk][1]);
+                for (int nt = 0; nt < NT; ++nt) mma16816(dk[kk & 1][nt], l0, l1, l2, l3, bk[nt][kk][0], bk[nt][kk][1]);
             }
             // four sign bits 4kk..4kk+3 -> registers for slots (0,1) and (2,3)
             const uint2 sg0 = lds_at<uint2>(slut4, kk == 0 ? (sw0 << 3) & 0x78u : (sw0 >> (4 * kk - 3)) & 0x78u);
@@ -271,8 +282,8 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(const __grid
             const uint32_t s0 = sg0.x, s1 = sg1.x, s2 = sg0.y, s3 = sg1.y;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                mma16816(dk[nt], a0, a1, a2, a3, bk[nt][kk][0], bk[nt][kk][1]);
-                mma16816(ds[nt], s0, s1, s2, s3, bs[nt][kk][0], bs[nt][kk][1]);
+                mma16816(dk[kk & 1][nt], a0, a1, a2, a3, bk[nt][kk][0], bk[nt][kk][1]);
+                mma16816(ds[kk & 1][nt], s0, s1, s2, s3, bs[nt][kk][0], bs[nt][kk][1]);
             }
         }
 
@@ -287,8 +298,13 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(const __grid
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const bool hv = qrow[nt] >= 0;
-            const float l0 = kn0 * fmaf(kg0, ds[nt][0] + ds[nt][1], (dk[nt][0] + dk[nt][1]) * inv_lk);
-            const float l1 = kn1 * fmaf(kg1, ds[nt][2] + ds[nt][3], (dk[nt][2] + dk[nt][3]) * inv_lk);
+            // column 2h holds the hi split of head h, 2h+1 the lo split
+            const float k0 = (dk[0][nt][0] + dk[1][nt][0]) + (dk[0][nt][1] + dk[1][nt][1]);
+            const float k1 = (dk[0][nt][2] + dk[1][nt][2]) + (dk[0][nt][3] + dk[1][nt][3]);
+            const float s0_ = (ds[0][nt][0] + ds[1][nt][0]) + (ds[0][nt][1] + ds[1][nt][1]);
+            const float s1_ = (ds[0][nt][2] + ds[1][nt][2]) + (ds[0][nt][3] + ds[1][nt][3]);
+            const float l0 = kn0 * fmaf(kg0, s0_, k0 * inv_lk);
+            const float l1 = kn1 * fmaf(kg1, s1_, k1 * inv_lk);
             if (p.logits != nullptr && hv) {
                 if (v0) p.logits[(int64_t)qrow[nt] * p.max_seq_len + tok0 + g] = l0;
                 if (v1) p.logits[(int64_t)qrow[nt] * p.max_seq_len + tok0 + g + 8] = l1;
@@ -305,7 +321,9 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(const __grid
             const float p1 = (s1 == -INFINITY) ? 0.0f : exp2f(s1 - mn);
             Zp[nt] = fmaf(Zp[nt], corr, p0 + p1);
             M[nt] = mn;
-            if (corr != 1.0f) {
+            // the running max of a head rarely moves after the first tiles:
+            // rescale only when it moved for some head of the warp
+            if (__any_sync(TQ_FULL_MASK, corr != 1.0f)) {
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt)
 #pragma unroll

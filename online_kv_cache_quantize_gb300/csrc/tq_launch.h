@@ -61,15 +61,21 @@ struct PrepParams {
     int rht;
     float inv_sqrt_d;
     const float* st32;    // S^T [d][m] or NULL (no u)
-    float* qprime;        // [rows][d]
+    float* qprime;        // [rows][d] or NULL
     float* u;             // [rows][m] or NULL
+    // d = m = 128 decode: the scan's B operands of every query row, fp16
+    // hi/lo splits of q' and of qjl_scale * u in fragment order (kFragWords
+    // words per row; see decode_mma.cuh), or NULL
+    uint32_t* frag;
+    float qjl_scale;
 };
+
+constexpr int kFragWords = 256;
 
 cudaError_t launch_query_prep(const PrepParams& p, cudaStream_t s);
 
 struct DecodeParams {
-    const float* qprime;  // [B*Hq][d]
-    const float* u;       // [B*Hq][m]
+    const uint32_t* frag; // [B*Hq][kFragWords] B operands written by the query prep
     int batch, hq, hkv, d, m, group;
     const int32_t* seq_lens;
     const int16_t* heads_of_kv;  // nullptr -> kv*G + j; else HOST-built table in params
