@@ -43,7 +43,8 @@ WORKLOADS = {
 }
 WORKLOAD = dict(name="llama8b_decode_32k", **WORKLOADS["llama8b_decode_32k"])
 FLUSH_BYTES = 256 << 20  # > 129 MB L2
-SCAN_SOURCES = ["online_kv_cache_quantize_gb300/csrc/decode_mma.cuh", "online_kv_cache_quantize_gb300/csrc/common.cuh"]
+SCAN_SOURCES = ["online_kv_cache_quantize_gb300/csrc/decode_mma.cuh", "online_kv_cache_quantize_gb300/csrc/common.cuh",
+                "online_kv_cache_quantize_gb300/csrc/pipeline.cuh"]
 
 
 def _peaks():
