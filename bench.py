@@ -174,7 +174,7 @@ def run_tq(args):
     sp = stream.cuda_stream
 
     # --- argument blocks built once (the per-step calls only swap events) ---
-    def qargs(cache, x, qj, append=None):
+    def qargs(cache, x, qj):
         a = B.tq_quant_args()
         a.cache = cache.struct()
         a.rot = rot.handle
@@ -183,9 +183,6 @@ def run_tq(args):
         a.x_dtype = B.TQ_BF16
         a.x_stride = d
         a.n = x.shape[0]
-        if append is not None:
-            a.append_pos = append.data_ptr()
-            a.heads = hkv
         return a
 
     fill_k, fill_v = qargs(kc, kdev, qjl), qargs(vc, vdev, None)
@@ -195,7 +192,6 @@ def run_tq(args):
     append = torch.full((bsz,), T - 1, dtype=torch.int32, device="cuda")
     lens = torch.full((bsz,), T, dtype=torch.int32, device="cuda")
     out = torch.empty((bsz, hq, d), dtype=torch.float32, device="cuda")
-    step_k, step_v = qargs(kc, knew, qjl, append), qargs(vc, vnew, None, append)
     da, _keep = B._decode_struct(q, kc, vc, lens, T, rot, qjl, out)
     wsz = L.tq_attn_decode_workspace(ctypes.byref(da))
     wsb = B.workspace(wsz)
@@ -205,10 +201,18 @@ def run_tq(args):
         if s != 0:
             raise RuntimeError(f"{what}: {B.status_name(s)} {L.tq_last_error().decode()}")
 
+    # one decode step through the public API: tq_decode_step appends the new
+    # token's K and V (on the library's side streams) and runs the attention
+    sa = B.tq_step_args()
+    sa.attn = da
+    sa.k_new = knew.data_ptr()
+    sa.v_new = vnew.data_ptr()
+    sa.new_dtype = B.TQ_BF16
+    sa.append_pos = append.data_ptr()
+    assert L.tq_decode_step_workspace(ctypes.byref(sa)) == wsz
+
     def step():
-        check(L.tq_quantize_kv(ctypes.byref(step_k), sp), "append K")
-        check(L.tq_quantize_kv(ctypes.byref(step_v), sp), "append V")
-        check(L.tq_attn_decode(ctypes.byref(da), wsb.data_ptr(), wsz, sp), "decode")
+        check(L.tq_decode_step(ctypes.byref(sa), wsb.data_ptr(), wsz, sp), "decode step")
 
     launches_per_step = 5  # append K, append V, query prep, split-K scan, merge
 
@@ -256,19 +260,22 @@ def run_tq(args):
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    host_s = 0.0
     for i in range(K):
         flush.fill_(i & 0xFF)
-        da.scan_begin = sev[i][0].cuda_event
-        da.scan_end = sev[i][1].cuda_event
+        sa.attn.scan_begin = sev[i][0].cuda_event
+        sa.attn.scan_end = sev[i][1].cuda_event
         ev[i][0].record(stream)
+        h0 = time.perf_counter()
         step()
+        host_s += time.perf_counter() - h0
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    da.scan_begin = None
-    da.scan_end = None
+    sa.attn.scan_begin = None
+    sa.attn.scan_end = None
     step_ms = [a.elapsed_time(b) for a, b in ev]
     scan_ms = [a.elapsed_time(b) for a, b in sev]
     total_ms = sum(step_ms)
@@ -330,6 +337,7 @@ def run_tq(args):
             "e2e": {"value": ws * tokens_per_step / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": ne},
             "gpu_launches": launches_per_step * K,
+            "host_us_per_step": host_s / K * 1e6,
             "clocks": clocks,
         }
     if ws > 1:

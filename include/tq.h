@@ -198,7 +198,7 @@ tq_status tq_quantize_kv(const tq_quant_args* a, tq_stream stream);
 typedef struct {
     const void* q;          /* device [batch][hq][d] of q_dtype               */
     int q_dtype;            /* TQ_F32 or TQ_BF16                              */
-    int batch, hq, hkv, d;  /* d in {64, 128, 256}                            */
+    int batch, hq, hkv, d;  /* d = 128                                        */
     const int32_t* seq_lens;/* device int32 [batch], each in [0, capacity]    */
     int max_seq_len;        /* host: upper bound of seq_lens (split plan)     */
     const int32_t* gqa_map; /* HOST int32 [hq] in [0, hkv), or NULL = h/(hq/hkv);
@@ -245,6 +245,33 @@ tq_status tq_attn_decode(const tq_decode_args* a, void* workspace, size_t ws_byt
  *     (tq_attn_decode_workspace(a) > TQ_STATIC_DECODE_SCRATCH_BYTES). */
 #define TQ_STATIC_DECODE_SCRATCH_BYTES (8u << 20)
 tq_status tq_attn_decode_static(const tq_decode_args* a, tq_stream stream);
+
+/* ------------------------------------------------------------------------ *
+ * One decode step: append the new token's K and V, then attend.            *
+ * ------------------------------------------------------------------------ *
+ * The quantize-on-append of [A2A] "How to implement" (every cache update)
+ * followed by the decode attention above, in one call. Same results, bit
+ * for bit, as tq_quantize_kv(K), tq_quantize_kv(V) and tq_attn_decode on one
+ * stream. The two appends run on streams the library owns (two per device,
+ * created on first use), concurrently with the query preparation on
+ * `stream`; `stream` waits for both before the scan, so all of the step's
+ * work is ordered after what precedes the call on `stream` and before what
+ * follows it (also under CUDA graph capture). Calls are serialised per
+ * process on the host side. */
+typedef struct {
+    tq_decode_args attn;        /* the attention call: caches, q, lengths, out */
+    const void* k_new;          /* device [batch*hkv][d] keys of the new token,
+                                   row b*hkv + h                              */
+    const void* v_new;          /* device [batch*hkv][d] values of the new token */
+    int new_dtype;              /* TQ_F32 or TQ_BF16                           */
+    const int32_t* append_pos;  /* device int32 [batch]: the slot (position)
+                                   the new token takes in every row of batch b;
+                                   outside [0, capacity) skips that batch row */
+} tq_step_args;
+
+/* Workspace bytes of tq_decode_step (that of its attention call; 0 on error). */
+size_t tq_decode_step_workspace(const tq_step_args* a);
+tq_status tq_decode_step(const tq_step_args* a, void* workspace, size_t ws_bytes, tq_stream stream);
 
 /* ------------------------------------------------------------------------ *
  * Inner-product search from the codes.                                     *

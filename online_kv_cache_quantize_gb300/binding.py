@@ -55,6 +55,11 @@ class tq_decode_args(ctypes.Structure):
                 ("scan_begin", ctypes.c_void_p), ("scan_end", ctypes.c_void_p)]
 
 
+class tq_step_args(ctypes.Structure):
+    _fields_ = [("attn", tq_decode_args), ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+                ("new_dtype", ctypes.c_int), ("append_pos", ctypes.c_void_p)]
+
+
 class tq_topk_args(ctypes.Structure):
     _fields_ = [("queries", ctypes.c_void_p), ("nq", ctypes.c_int), ("d", ctypes.c_int),
                 ("rot", ctypes.c_void_p), ("qjl", ctypes.c_void_p), ("db", tq_cache),
@@ -86,6 +91,8 @@ _SIGS = {
     "tq_attn_decode_static": (_STATUS, [ctypes.POINTER(tq_decode_args), ctypes.c_void_p]),
     "tq_score_topk_workspace": (ctypes.c_size_t, [ctypes.POINTER(tq_topk_args)]),
     "tq_score_topk": (_STATUS, [ctypes.POINTER(tq_topk_args), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "tq_decode_step_workspace": (ctypes.c_size_t, [ctypes.POINTER(tq_step_args)]),
+    "tq_decode_step": (_STATUS, [ctypes.POINTER(tq_step_args), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "tq_device_errors": (_STATUS, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "tq_selftest_bounded_wait": (_STATUS, [ctypes.c_uint32, ctypes.c_void_p]),
 }
@@ -110,7 +117,8 @@ def load():
         fn.restype = res
         fn.argtypes = args
     for name, cls in (("tq_cache", tq_cache), ("tq_quant_args", tq_quant_args),
-                      ("tq_decode_args", tq_decode_args), ("tq_topk_args", tq_topk_args)):
+                      ("tq_decode_args", tq_decode_args), ("tq_topk_args", tq_topk_args),
+                      ("tq_step_args", tq_step_args)):
         if lib.tq_abi_struct_size(name.encode()) != ctypes.sizeof(cls):
             raise RuntimeError(f"struct {name} layout differs between libtq.so and the binding")
     _lib = lib
@@ -317,6 +325,33 @@ def tq_attn_decode_static(q, kcache, vcache, seq_lens, max_seq_len, rot, qjl, ou
     device memory; its scratch is an array inside the library (see tq.h)."""
     a, _keep = _decode_struct(q, kcache, vcache, seq_lens, max_seq_len, rot, qjl, out, **kw)
     _check(load().tq_attn_decode_static(ctypes.byref(a), _stream_ptr(stream)), "tq_attn_decode_static")
+
+
+def _step_struct(q, kcache, vcache, seq_lens, max_seq_len, rot, qjl, out, k_new, v_new, append_pos, **kw):
+    attn, keep = _decode_struct(q, kcache, vcache, seq_lens, max_seq_len, rot, qjl, out, **kw)
+    a = tq_step_args()
+    a.attn = attn
+    a.k_new = k_new.data_ptr()
+    a.v_new = v_new.data_ptr()
+    if k_new.dtype != v_new.dtype:
+        raise ValueError("k_new and v_new must have the same dtype")
+    a.new_dtype = _dtype_code(k_new)
+    a.append_pos = append_pos.data_ptr()
+    return a, keep
+
+
+def tq_decode_step_workspace(q, kcache, vcache, seq_lens, max_seq_len, rot, qjl, out, k_new, v_new, append_pos, **kw):
+    a, _keep = _step_struct(q, kcache, vcache, seq_lens, max_seq_len, rot, qjl, out, k_new, v_new, append_pos, **kw)
+    return load().tq_decode_step_workspace(ctypes.byref(a))
+
+
+def tq_decode_step(q, kcache, vcache, seq_lens, max_seq_len, rot, qjl, out, k_new, v_new, append_pos, workspace,
+                   stream=None, **kw):
+    """Append the new token's K and V (rows b*hkv + h of k_new / v_new at slot
+    append_pos[b]) and run decode attention, in one call."""
+    a, _keep = _step_struct(q, kcache, vcache, seq_lens, max_seq_len, rot, qjl, out, k_new, v_new, append_pos, **kw)
+    _check(load().tq_decode_step(ctypes.byref(a), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                 _stream_ptr(stream)), "tq_decode_step")
 
 
 TQ_DEVERR_SCAN_WAIT = 1

@@ -236,6 +236,247 @@ uint16_t bf16_bits_of(double exact_bf16_value) {
 
 }  // namespace
 
+namespace {
+
+// streams and events of tq_decode_step, per device
+constexpr int kMaxStepDevices = 64;
+struct StepStreams {
+    bool ready = false;
+    cudaStream_t sk = nullptr, sv = nullptr;
+    cudaEvent_t fork = nullptr, jk = nullptr, jv = nullptr;
+};
+std::mutex g_step_mutex;
+StepStreams g_step[kMaxStepDevices];
+
+struct QuantLaunch {
+    tqk::QuantParams p;
+    int dtype = 0, vpl = 1, cb = 1;
+    bool rht = false, prod = false, mma = false;
+};
+
+struct DecodeLaunch {
+    DecodePlan pl;
+    tqk::PrepParams pp;
+    tqk::DecodeParams dp;
+    tqk::CombineParams cp;
+    int kb = 0, vb = 0;
+    cudaEvent_t scan_begin = nullptr, scan_end = nullptr;
+};
+
+// Validates a quantize call and fills its launch; *empty = nothing to do.
+tq_status quant_prepare(const tq_quant_args* a, QuantLaunch* L, bool* empty) {
+    *empty = false;
+    if (!a) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_kv: args are NULL");
+    int cb = 0;
+    tq_status s = check_cache(a->cache, "tq_quantize_kv cache", &cb);
+    if (s != TQ_OK) return s;
+    const tq_cache& c = a->cache;
+    if ((s = check_rot(a->rot, c.d)) != TQ_OK) return s;
+    const bool prod = c.mode == TQ_PROD;
+    if (prod && (s = check_qjl(a->qjl, c.m, c.d)) != TQ_OK) return s;
+    if (a->n < 0) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_kv: n < 0");
+    if (a->n == 0) {
+        *empty = true;
+        return TQ_OK;
+    }
+    if (!a->x) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_kv: x is NULL");
+    if (a->x_dtype != TQ_F32 && a->x_dtype != TQ_BF16) return fail(TQ_ERR_UNSUPPORTED, "tq_quantize_kv: x_dtype must be TQ_F32 or TQ_BF16");
+    const size_t esz = a->x_dtype == TQ_F32 ? 4 : 2;
+    if (!aligned(a->x, esz)) return fail(TQ_ERR_ALIGNMENT, "tq_quantize_kv: x misaligned for its dtype");
+    if (a->x_stride < c.d) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_kv: x_stride < d");
+    const int64_t total = c.rows * c.capacity;
+    if (a->dst_slot) {
+        if (!aligned(a->dst_slot, 8)) return fail(TQ_ERR_ALIGNMENT, "tq_quantize_kv: dst_slot misaligned");
+    } else if (a->append_pos) {
+        if (a->heads < 1 || a->n % a->heads) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_kv: n must be a multiple of heads");
+        if (a->n != c.rows) return fail(TQ_ERR_CAPACITY, "tq_quantize_kv: append mode needs n == cache rows");
+    } else {
+        if (a->slot0 < 0 || a->slot0 + a->n > total) return fail(TQ_ERR_CAPACITY, "tq_quantize_kv: slot0 + n exceeds rows*capacity");
+    }
+    const bool rht = a->rot->kind == TQ_ROT_RHT;
+    if (rht && c.d != 64 && c.d != 128 && c.d != 256) return fail(TQ_ERR_UNSUPPORTED, "tq_quantize_kv: RHT kernels need d in {64, 128, 256}");
+    if (prod && c.m > 32 * vpl_for(c.d)) return fail(TQ_ERR_UNSUPPORTED, "tq_quantize_kv: m must be <= d rounded up to the kernel width");
+
+    tqk::QuantParams& p = L->p;
+    std::memset(&p, 0, sizeof(p));
+    p.x = a->x;
+    p.x_stride = a->x_stride;
+    p.n = a->n;
+    p.dst_slot = a->dst_slot;
+    p.append_pos = a->append_pos;
+    p.heads = a->heads;
+    p.slot0 = a->slot0;
+    p.total_slots = total;
+    p.capacity = c.capacity;
+    p.codes = c.codes;
+    p.code_stride = tq_code_bytes(c.d, cb);
+    p.signs = c.signs;
+    p.sign_stride = prod ? tq_sign_bytes(c.m) : 0;
+    p.norm = c.norm;
+    p.rnorm = c.rnorm;
+    p.pit32 = a->rot->d_pit32;
+    p.pi64 = a->rot->d_pi64;
+    p.sgn = a->rot->d_sign;
+    p.st32 = prod ? a->qjl->d_st32 : nullptr;
+    p.d = c.d;
+    p.m = prod ? c.m : 0;
+    p.inv_sqrt_d = (float)(1.0 / std::sqrt((double)c.d));
+    p.guard = rht ? 1.0e-6f : (float)(3.0e-8 * c.d);
+    if ((s = fill_codebook(c.d, cb, &p.cb)) != TQ_OK) return s;
+    L->dtype = a->x_dtype == TQ_F32 ? 0 : 1;
+    L->vpl = vpl_for(c.d);
+    L->rht = rht;
+    L->prod = prod;
+    L->cb = cb;
+    p.pi_frag = a->rot->d_pi_frag;
+    p.s_frag = prod ? a->qjl->d_s_frag : nullptr;
+    // d = m = 128 with 16-byte aligned rows: the tensor-core kernel; otherwise
+    // the warp-per-vector kernel (any d <= 256)
+    L->mma = c.d == 128 && (!prod || (c.m == 128 && p.s_frag)) && (rht || p.pi_frag) && aligned(a->x, 16) &&
+             (a->x_stride * (int64_t)esz) % 16 == 0;
+    return TQ_OK;
+}
+
+cudaError_t quant_launch(const QuantLaunch& L, cudaStream_t st) {
+    if (L.mma) return tqk::launch_quantize_mma(L.p, L.dtype, L.rht ? 1 : 0, L.prod ? 1 : 0, L.cb, st);
+    if (L.rht) return tqk::launch_quantize_rht(L.p, L.dtype, L.vpl, L.prod ? 1 : 0, L.cb, st);
+    return tqk::launch_quantize_dense(L.p, L.dtype, L.vpl, L.prod ? 1 : 0, L.cb, st);
+}
+
+// Validates a decode call and fills its three launches.
+tq_status decode_prepare(const tq_decode_args* a, void* workspace, size_t ws_bytes, DecodeLaunch* D) {
+    DecodePlan& pl = D->pl;
+    tq_status s = plan_decode(a, &pl);
+    if (s != TQ_OK) return s;
+    int kb = 0, vb = 0;
+    if ((s = check_cache(a->k, "tq_attn_decode k", &kb)) != TQ_OK) return s;
+    if ((s = check_cache(a->v, "tq_attn_decode v", &vb)) != TQ_OK) return s;
+    if (a->k.mode != TQ_PROD || a->v.mode != TQ_MSE) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: keys must be PROD and values MSE");
+    if (a->k.d != a->d || a->v.d != a->d) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: cache d does not match");
+    if (a->k.m != 128) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: m must be 128");
+    const int64_t rows = (int64_t)a->batch * a->hkv;
+    if (a->k.rows != rows || a->v.rows != rows) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: cache rows must be batch*hkv");
+    if (a->k.capacity != a->v.capacity) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: k and v capacity differ");
+    if (a->max_seq_len > a->k.capacity) return fail(TQ_ERR_CAPACITY, "tq_attn_decode: max_seq_len exceeds the capacity");
+    if (a->k.capacity % 16) return fail(TQ_ERR_ALIGNMENT, "tq_attn_decode: cache capacity must be a multiple of 16");
+    if (!aligned(a->k.norm, 16) || !aligned(a->k.rnorm, 16) || !aligned(a->v.norm, 16) || !aligned(a->v.codes, 16))
+        return fail(TQ_ERR_ALIGNMENT, "tq_attn_decode: every cache plane must be 16-byte aligned (bulk copies)");
+    if ((s = check_rot(a->rot, a->d)) != TQ_OK) return s;
+    if ((s = check_qjl(a->qjl, a->k.m, a->d)) != TQ_OK) return s;
+    if (!a->q || !a->out || !a->seq_lens) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: q/out/seq_lens is NULL");
+    if (a->q_dtype != TQ_F32 && a->q_dtype != TQ_BF16) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: q_dtype must be F32 or BF16");
+    if (a->out_dtype != TQ_F32 && a->out_dtype != TQ_BF16) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: out_dtype must be F32 or BF16");
+    if (!workspace || ws_bytes < pl.total) return fail(TQ_ERR_WORKSPACE, "tq_attn_decode: workspace missing or too small");
+    if (!aligned(workspace, 256)) return fail(TQ_ERR_ALIGNMENT, "tq_attn_decode: workspace must be 256-byte aligned");
+
+    tqk::DecodeParams& dp = D->dp;
+    std::memset(&dp, 0, sizeof(dp));
+    if (a->gqa_map) {
+        std::vector<int> count(a->hkv, 0);
+        for (int h = 0; h < a->hq; ++h) {
+            int g = a->gqa_map[h];
+            if (g < 0 || g >= a->hkv) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: gqa_map entry out of range");
+            if (count[g] >= pl.group) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: every KV head must serve hq/hkv query heads");
+            dp.head_table[g * pl.group + count[g]++] = (int16_t)h;
+        }
+        dp.use_table = 1;
+    }
+    char* ws = (char*)workspace;
+    uint32_t* frag = (uint32_t*)(ws + pl.off_frag);
+    float* part = (float*)(ws + pl.off_part);
+
+    tqk::PrepParams& pp = D->pp;
+    std::memset(&pp, 0, sizeof(pp));
+    pp.q = a->q;
+    pp.q_dtype = a->q_dtype == TQ_BF16 ? 1 : 0;
+    pp.rows = (int64_t)a->batch * a->hq;
+    pp.d = a->d;
+    pp.m = a->k.m;
+    pp.pit32 = a->rot->d_pit32;
+    pp.sgn = a->rot->d_sign;
+    pp.rht = a->rot->kind == TQ_ROT_RHT;
+    pp.inv_sqrt_d = (float)(1.0 / std::sqrt((double)a->d));
+    pp.st32 = a->qjl->d_st32;
+    pp.frag = frag;
+    pp.qjl_scale = (float)(std::sqrt(M_PI / 2.0) / a->k.m);
+
+    std::vector<double> kc, kt, vc, vt;
+    if ((s = tq::codebook(a->d, kb, kc, kt)) != TQ_OK) return s;
+    if ((s = tq::codebook(a->d, vb, vc, vt)) != TQ_OK) return s;
+    dp.frag = frag;
+    dp.batch = a->batch;
+    dp.hq = a->hq;
+    dp.hkv = a->hkv;
+    dp.d = a->d;
+    dp.m = a->k.m;
+    dp.group = pl.group;
+    dp.seq_lens = a->seq_lens;
+    dp.capacity = a->k.capacity;
+    dp.kcodes = a->k.codes;
+    dp.kcode_stride = tq_code_bytes(a->d, kb);
+    dp.ksigns = a->k.signs;
+    dp.ksign_stride = tq_sign_bytes(a->k.m);
+    dp.knorm = a->k.norm;
+    dp.krnorm = a->k.rnorm;
+    dp.vcodes = a->v.codes;
+    dp.vcode_stride = tq_code_bytes(a->d, vb);
+    dp.vnorm = a->v.norm;
+    for (size_t i = 0; i < kc.size(); ++i) dp.kc[i] = (float)kc[i];
+    for (size_t i = 0; i < vc.size(); ++i) dp.vc[i] = (float)vc[i];
+    const double lam_k = pick_lambda(a->d, kb, kc), lam_v = pick_lambda(a->d, vb, vc);
+    pair_table(kc, kb, lam_k, dp.klut);
+    pair_table_lo(kc, kb, lam_k, dp.klut_lo);
+    pair_table(vc, vb, lam_v, dp.vlut);
+    dp.inv_lam_k = (float)(1.0 / lam_k);
+    dp.inv_lam_v = (float)(1.0 / lam_v);
+    dp.qjl_scale = (float)(std::sqrt(M_PI / 2.0) / a->k.m);
+    const double scale = a->scale != 0.0f ? (double)a->scale : 1.0 / std::sqrt((double)a->d);
+    dp.scale_log2 = (float)(scale * 1.4426950408889634);
+    dp.n_splits = pl.n_splits;
+    dp.chunk = pl.chunk;
+    dp.partial = part;
+    dp.logits = a->logits;
+    dp.max_seq_len = a->max_seq_len;
+    cudaError_t e = tqk::device_error_word(&dp.err);
+    if (e != cudaSuccess) return cuda_status(e, "tq_attn_decode error word");
+    D->kb = kb;
+    D->vb = vb;
+    D->scan_begin = (cudaEvent_t)a->scan_begin;
+    D->scan_end = (cudaEvent_t)a->scan_end;
+
+    tqk::CombineParams& cp = D->cp;
+    std::memset(&cp, 0, sizeof(cp));
+    cp.partial = part;
+    cp.rows = a->batch * a->hq;
+    cp.d = a->d;
+    cp.n_splits = pl.n_splits;
+    cp.pi32 = a->rot->d_pi32;
+    cp.sgn = a->rot->d_sign;
+    cp.rht = a->rot->kind == TQ_ROT_RHT;
+    cp.inv_sqrt_d = (float)(1.0 / std::sqrt((double)a->d));
+    cp.out = a->out;
+    cp.out_dtype = a->out_dtype == TQ_BF16 ? 1 : 0;
+    return TQ_OK;
+}
+
+// Query prep on st, then (after st waits on `waits`) the scan and the merge.
+tq_status decode_launch(const DecodeLaunch& D, cudaStream_t st, const cudaEvent_t* waits, int nwaits) {
+    cudaError_t e = tqk::launch_query_prep(D.pp, st);
+    if (e != cudaSuccess) return cuda_status(e, "tq_attn_decode query prep");
+    for (int i = 0; i < nwaits; ++i)
+        if ((e = cudaStreamWaitEvent(st, waits[i], 0)) != cudaSuccess) return cuda_status(e, "tq_attn_decode join");
+    if (D.scan_begin && (e = cudaEventRecord(D.scan_begin, st)) != cudaSuccess)
+        return cuda_status(e, "tq_attn_decode scan_begin");
+    e = tqk::launch_decode_mma(D.dp, D.kb, D.vb, st);
+    if (e != cudaSuccess) return cuda_status(e, "tq_attn_decode scan");
+    if (D.scan_end && (e = cudaEventRecord(D.scan_end, st)) != cudaSuccess)
+        return cuda_status(e, "tq_attn_decode scan_end");
+    e = tqk::launch_combine(D.cp, st);
+    return cuda_status(e, "tq_attn_decode combine");
+}
+
+}  // namespace
+
 extern "C" {
 
 tq_status tq_rotation_to_device(tq_rotation* rot) {
@@ -334,76 +575,11 @@ tq_status tq_free_qjl(tq_qjl* q) {
 }
 
 tq_status tq_quantize_kv(const tq_quant_args* a, tq_stream stream) {
-    if (!a) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_kv: args are NULL");
-    int cb = 0;
-    tq_status s = check_cache(a->cache, "tq_quantize_kv cache", &cb);
-    if (s != TQ_OK) return s;
-    const tq_cache& c = a->cache;
-    if ((s = check_rot(a->rot, c.d)) != TQ_OK) return s;
-    const bool prod = c.mode == TQ_PROD;
-    if (prod && (s = check_qjl(a->qjl, c.m, c.d)) != TQ_OK) return s;
-    if (a->n < 0) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_kv: n < 0");
-    if (a->n == 0) return TQ_OK;
-    if (!a->x) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_kv: x is NULL");
-    if (a->x_dtype != TQ_F32 && a->x_dtype != TQ_BF16) return fail(TQ_ERR_UNSUPPORTED, "tq_quantize_kv: x_dtype must be TQ_F32 or TQ_BF16");
-    const size_t esz = a->x_dtype == TQ_F32 ? 4 : 2;
-    if (!aligned(a->x, esz)) return fail(TQ_ERR_ALIGNMENT, "tq_quantize_kv: x misaligned for its dtype");
-    if (a->x_stride < c.d) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_kv: x_stride < d");
-    const int64_t total = c.rows * c.capacity;
-    if (a->dst_slot) {
-        if (!aligned(a->dst_slot, 8)) return fail(TQ_ERR_ALIGNMENT, "tq_quantize_kv: dst_slot misaligned");
-    } else if (a->append_pos) {
-        if (a->heads < 1 || a->n % a->heads) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_kv: n must be a multiple of heads");
-        if (a->n != c.rows) return fail(TQ_ERR_CAPACITY, "tq_quantize_kv: append mode needs n == cache rows");
-    } else {
-        if (a->slot0 < 0 || a->slot0 + a->n > total) return fail(TQ_ERR_CAPACITY, "tq_quantize_kv: slot0 + n exceeds rows*capacity");
-    }
-    const bool rht = a->rot->kind == TQ_ROT_RHT;
-    if (rht && c.d != 64 && c.d != 128 && c.d != 256) return fail(TQ_ERR_UNSUPPORTED, "tq_quantize_kv: RHT kernels need d in {64, 128, 256}");
-    if (prod && c.m > 32 * vpl_for(c.d)) return fail(TQ_ERR_UNSUPPORTED, "tq_quantize_kv: m must be <= d rounded up to the kernel width");
-
-    tqk::QuantParams p;
-    std::memset(&p, 0, sizeof(p));
-    p.x = a->x;
-    p.x_stride = a->x_stride;
-    p.n = a->n;
-    p.dst_slot = a->dst_slot;
-    p.append_pos = a->append_pos;
-    p.heads = a->heads;
-    p.slot0 = a->slot0;
-    p.total_slots = total;
-    p.capacity = c.capacity;
-    p.codes = c.codes;
-    p.code_stride = tq_code_bytes(c.d, cb);
-    p.signs = c.signs;
-    p.sign_stride = prod ? tq_sign_bytes(c.m) : 0;
-    p.norm = c.norm;
-    p.rnorm = c.rnorm;
-    p.pit32 = a->rot->d_pit32;
-    p.pi64 = a->rot->d_pi64;
-    p.sgn = a->rot->d_sign;
-    p.st32 = prod ? a->qjl->d_st32 : nullptr;
-    p.d = c.d;
-    p.m = prod ? c.m : 0;
-    p.inv_sqrt_d = (float)(1.0 / std::sqrt((double)c.d));
-    p.guard = rht ? 1.0e-6f : (float)(3.0e-8 * c.d);
-    if ((s = fill_codebook(c.d, cb, &p.cb)) != TQ_OK) return s;
-    const int dtype = a->x_dtype == TQ_F32 ? 0 : 1;
-    const int vpl = vpl_for(c.d);
-    p.pi_frag = a->rot->d_pi_frag;
-    p.s_frag = prod ? a->qjl->d_s_frag : nullptr;
-    // d = m = 128 with 16-byte aligned rows: the tensor-core kernel; otherwise
-    // the warp-per-vector kernel (any d <= 256)
-    const bool mma = c.d == 128 && (!prod || (c.m == 128 && p.s_frag)) && (rht || p.pi_frag) &&
-                     aligned(a->x, 16) && (a->x_stride * (int64_t)esz) % 16 == 0;
-    cudaError_t e;
-    if (mma)
-        e = tqk::launch_quantize_mma(p, dtype, rht ? 1 : 0, prod ? 1 : 0, cb, (cudaStream_t)stream);
-    else if (rht)
-        e = tqk::launch_quantize_rht(p, dtype, vpl, prod ? 1 : 0, cb, (cudaStream_t)stream);
-    else
-        e = tqk::launch_quantize_dense(p, dtype, vpl, prod ? 1 : 0, cb, (cudaStream_t)stream);
-    return cuda_status(e, "tq_quantize_kv launch");
+    QuantLaunch L;
+    bool empty = false;
+    tq_status s = quant_prepare(a, &L, &empty);
+    if (s != TQ_OK || empty) return s;
+    return cuda_status(quant_launch(L, (cudaStream_t)stream), "tq_quantize_kv launch");
 }
 
 size_t tq_attn_decode_workspace(const tq_decode_args* a) {
@@ -413,123 +589,10 @@ size_t tq_attn_decode_workspace(const tq_decode_args* a) {
 }
 
 tq_status tq_attn_decode(const tq_decode_args* a, void* workspace, size_t ws_bytes, tq_stream stream) {
-    DecodePlan pl;
-    tq_status s = plan_decode(a, &pl);
+    DecodeLaunch D;
+    tq_status s = decode_prepare(a, workspace, ws_bytes, &D);
     if (s != TQ_OK) return s;
-    int kb = 0, vb = 0;
-    if ((s = check_cache(a->k, "tq_attn_decode k", &kb)) != TQ_OK) return s;
-    if ((s = check_cache(a->v, "tq_attn_decode v", &vb)) != TQ_OK) return s;
-    if (a->k.mode != TQ_PROD || a->v.mode != TQ_MSE) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: keys must be PROD and values MSE");
-    if (a->k.d != a->d || a->v.d != a->d) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: cache d does not match");
-    if (a->k.m != 128) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: m must be 128");
-    const int64_t rows = (int64_t)a->batch * a->hkv;
-    if (a->k.rows != rows || a->v.rows != rows) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: cache rows must be batch*hkv");
-    if (a->k.capacity != a->v.capacity) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: k and v capacity differ");
-    if (a->max_seq_len > a->k.capacity) return fail(TQ_ERR_CAPACITY, "tq_attn_decode: max_seq_len exceeds the capacity");
-    if (a->k.capacity % 16) return fail(TQ_ERR_ALIGNMENT, "tq_attn_decode: cache capacity must be a multiple of 16");
-    if (!aligned(a->k.norm, 16) || !aligned(a->k.rnorm, 16) || !aligned(a->v.norm, 16) || !aligned(a->v.codes, 16))
-        return fail(TQ_ERR_ALIGNMENT, "tq_attn_decode: every cache plane must be 16-byte aligned (bulk copies)");
-    if ((s = check_rot(a->rot, a->d)) != TQ_OK) return s;
-    if ((s = check_qjl(a->qjl, a->k.m, a->d)) != TQ_OK) return s;
-    if (!a->q || !a->out || !a->seq_lens) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: q/out/seq_lens is NULL");
-    if (a->q_dtype != TQ_F32 && a->q_dtype != TQ_BF16) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: q_dtype must be F32 or BF16");
-    if (a->out_dtype != TQ_F32 && a->out_dtype != TQ_BF16) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: out_dtype must be F32 or BF16");
-    if (!workspace || ws_bytes < pl.total) return fail(TQ_ERR_WORKSPACE, "tq_attn_decode: workspace missing or too small");
-    if (!aligned(workspace, 256)) return fail(TQ_ERR_ALIGNMENT, "tq_attn_decode: workspace must be 256-byte aligned");
-
-    tqk::DecodeParams dp;
-    std::memset(&dp, 0, sizeof(dp));
-    if (a->gqa_map) {
-        std::vector<int> count(a->hkv, 0);
-        for (int h = 0; h < a->hq; ++h) {
-            int g = a->gqa_map[h];
-            if (g < 0 || g >= a->hkv) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: gqa_map entry out of range");
-            if (count[g] >= pl.group) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: every KV head must serve hq/hkv query heads");
-            dp.head_table[g * pl.group + count[g]++] = (int16_t)h;
-        }
-        dp.use_table = 1;
-    }
-    char* ws = (char*)workspace;
-    uint32_t* frag = (uint32_t*)(ws + pl.off_frag);
-    float* part = (float*)(ws + pl.off_part);
-    cudaStream_t st = (cudaStream_t)stream;
-
-    tqk::PrepParams pp;
-    std::memset(&pp, 0, sizeof(pp));
-    pp.q = a->q;
-    pp.q_dtype = a->q_dtype == TQ_BF16 ? 1 : 0;
-    pp.rows = (int64_t)a->batch * a->hq;
-    pp.d = a->d;
-    pp.m = a->k.m;
-    pp.pit32 = a->rot->d_pit32;
-    pp.sgn = a->rot->d_sign;
-    pp.rht = a->rot->kind == TQ_ROT_RHT;
-    pp.inv_sqrt_d = (float)(1.0 / std::sqrt((double)a->d));
-    pp.st32 = a->qjl->d_st32;
-    pp.frag = frag;
-    pp.qjl_scale = (float)(std::sqrt(M_PI / 2.0) / a->k.m);
-    cudaError_t e = tqk::launch_query_prep(pp, st);
-    if (e != cudaSuccess) return cuda_status(e, "tq_attn_decode query prep");
-
-    std::vector<double> kc, kt, vc, vt;
-    if ((s = tq::codebook(a->d, kb, kc, kt)) != TQ_OK) return s;
-    if ((s = tq::codebook(a->d, vb, vc, vt)) != TQ_OK) return s;
-    dp.frag = frag;
-    dp.batch = a->batch;
-    dp.hq = a->hq;
-    dp.hkv = a->hkv;
-    dp.d = a->d;
-    dp.m = a->k.m;
-    dp.group = pl.group;
-    dp.seq_lens = a->seq_lens;
-    dp.capacity = a->k.capacity;
-    dp.kcodes = a->k.codes;
-    dp.kcode_stride = tq_code_bytes(a->d, kb);
-    dp.ksigns = a->k.signs;
-    dp.ksign_stride = tq_sign_bytes(a->k.m);
-    dp.knorm = a->k.norm;
-    dp.krnorm = a->k.rnorm;
-    dp.vcodes = a->v.codes;
-    dp.vcode_stride = tq_code_bytes(a->d, vb);
-    dp.vnorm = a->v.norm;
-    for (size_t i = 0; i < kc.size(); ++i) dp.kc[i] = (float)kc[i];
-    for (size_t i = 0; i < vc.size(); ++i) dp.vc[i] = (float)vc[i];
-    const double lam_k = pick_lambda(a->d, kb, kc), lam_v = pick_lambda(a->d, vb, vc);
-    pair_table(kc, kb, lam_k, dp.klut);
-    pair_table_lo(kc, kb, lam_k, dp.klut_lo);
-    pair_table(vc, vb, lam_v, dp.vlut);
-    dp.inv_lam_k = (float)(1.0 / lam_k);
-    dp.inv_lam_v = (float)(1.0 / lam_v);
-    dp.qjl_scale = (float)(std::sqrt(M_PI / 2.0) / a->k.m);
-    const double scale = a->scale != 0.0f ? (double)a->scale : 1.0 / std::sqrt((double)a->d);
-    dp.scale_log2 = (float)(scale * 1.4426950408889634);
-    dp.n_splits = pl.n_splits;
-    dp.chunk = pl.chunk;
-    dp.partial = part;
-    dp.logits = a->logits;
-    dp.max_seq_len = a->max_seq_len;
-    if ((e = tqk::device_error_word(&dp.err)) != cudaSuccess) return cuda_status(e, "tq_attn_decode error word");
-    if (a->scan_begin && (e = cudaEventRecord((cudaEvent_t)a->scan_begin, st)) != cudaSuccess)
-        return cuda_status(e, "tq_attn_decode scan_begin");
-    e = tqk::launch_decode_mma(dp, kb, vb, st);
-    if (e != cudaSuccess) return cuda_status(e, "tq_attn_decode scan");
-    if (a->scan_end && (e = cudaEventRecord((cudaEvent_t)a->scan_end, st)) != cudaSuccess)
-        return cuda_status(e, "tq_attn_decode scan_end");
-
-    tqk::CombineParams cp;
-    std::memset(&cp, 0, sizeof(cp));
-    cp.partial = part;
-    cp.rows = a->batch * a->hq;
-    cp.d = a->d;
-    cp.n_splits = pl.n_splits;
-    cp.pi32 = a->rot->d_pi32;
-    cp.sgn = a->rot->d_sign;
-    cp.rht = a->rot->kind == TQ_ROT_RHT;
-    cp.inv_sqrt_d = (float)(1.0 / std::sqrt((double)a->d));
-    cp.out = a->out;
-    cp.out_dtype = a->out_dtype == TQ_BF16 ? 1 : 0;
-    e = tqk::launch_combine(cp, st);
-    return cuda_status(e, "tq_attn_decode combine");
+    return decode_launch(D, (cudaStream_t)stream, nullptr, 0);
 }
 
 size_t tq_score_topk_workspace(const tq_topk_args* a) {
@@ -616,6 +679,63 @@ tq_status tq_score_topk(const tq_topk_args* a, void* workspace, size_t ws_bytes,
     tp.scores = a->scores;
     e = tqk::launch_topk(tp, cb, prod ? 1 : 0, st);
     return cuda_status(e, "tq_score_topk");
+}
+
+size_t tq_decode_step_workspace(const tq_step_args* a) { return a ? tq_attn_decode_workspace(&a->attn) : 0; }
+
+tq_status tq_decode_step(const tq_step_args* a, void* workspace, size_t ws_bytes, tq_stream stream) {
+    if (!a) return fail(TQ_ERR_INVALID_ARG, "tq_decode_step: args are NULL");
+    const tq_decode_args& at = a->attn;
+    if (!a->k_new || !a->v_new || !a->append_pos) return fail(TQ_ERR_INVALID_ARG, "tq_decode_step: k_new/v_new/append_pos is NULL");
+    tq_quant_args qk;
+    std::memset(&qk, 0, sizeof(qk));
+    qk.cache = at.k;
+    qk.rot = at.rot;
+    qk.qjl = at.qjl;
+    qk.x = a->k_new;
+    qk.x_dtype = a->new_dtype;
+    qk.x_stride = at.d;
+    qk.n = (int64_t)at.batch * at.hkv;
+    qk.append_pos = a->append_pos;
+    qk.heads = at.hkv;
+    tq_quant_args qv = qk;
+    qv.cache = at.v;
+    qv.qjl = nullptr;
+    qv.x = a->v_new;
+    // everything is validated before anything is enqueued
+    QuantLaunch LK, LV;
+    bool ek = false, ev = false;
+    tq_status s;
+    if ((s = quant_prepare(&qk, &LK, &ek)) != TQ_OK) return s;
+    if ((s = quant_prepare(&qv, &LV, &ev)) != TQ_OK) return s;
+    DecodeLaunch D;
+    if ((s = decode_prepare(&at, workspace, ws_bytes, &D)) != TQ_OK) return s;
+
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e, "tq_decode_step");
+    if (dev < 0 || dev >= kMaxStepDevices) return fail(TQ_ERR_UNSUPPORTED, "tq_decode_step: device ordinal >= 64");
+    std::lock_guard<std::mutex> lk(g_step_mutex);
+    StepStreams& R = g_step[dev];
+    if (!R.ready) {
+        if ((e = cudaStreamCreateWithFlags(&R.sk, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&R.sv, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&R.fork, cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&R.jk, cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&R.jv, cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_status(e, "tq_decode_step: creating its streams");
+        R.ready = true;
+    }
+    const cudaStream_t st = (cudaStream_t)stream;
+    if ((e = cudaEventRecord(R.fork, st)) != cudaSuccess || (e = cudaStreamWaitEvent(R.sk, R.fork, 0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(R.sv, R.fork, 0)) != cudaSuccess)
+        return cuda_status(e, "tq_decode_step fork");
+    if (!ek && (e = quant_launch(LK, R.sk)) != cudaSuccess) return cuda_status(e, "tq_decode_step append K");
+    if ((e = cudaEventRecord(R.jk, R.sk)) != cudaSuccess) return cuda_status(e, "tq_decode_step join K");
+    if (!ev && (e = quant_launch(LV, R.sv)) != cudaSuccess) return cuda_status(e, "tq_decode_step append V");
+    if ((e = cudaEventRecord(R.jv, R.sv)) != cudaSuccess) return cuda_status(e, "tq_decode_step join V");
+    const cudaEvent_t joins[2] = {R.jk, R.jv};
+    return decode_launch(D, st, joins, 2);
 }
 
 tq_status tq_device_errors(uint32_t* flags_out, int reset) {

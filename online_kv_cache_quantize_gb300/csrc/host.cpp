@@ -303,6 +303,7 @@ size_t tq_abi_struct_size(const char* name) {
     if (!std::strcmp(name, "tq_quant_args")) return sizeof(tq_quant_args);
     if (!std::strcmp(name, "tq_decode_args")) return sizeof(tq_decode_args);
     if (!std::strcmp(name, "tq_topk_args")) return sizeof(tq_topk_args);
+    if (!std::strcmp(name, "tq_step_args")) return sizeof(tq_step_args);
     return 0;
 }
 

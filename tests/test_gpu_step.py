@@ -1,0 +1,121 @@
+"""tq_decode_step: append the new token's K and V, then decode, in one call.
+
+Checked two ways: bit for bit against the three separate calls on one stream
+(tq_quantize_kv K, tq_quantize_kv V, tq_attn_decode), and against the fp64
+oracle on the appended cache."""
+
+import numpy as np
+import pytest
+import torch
+
+import parity_util as P
+from oracle import attention as oa
+from oracle import quantize as oq
+from online_kv_cache_quantize_gb300 import binding as B
+from online_kv_cache_quantize_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+OUT_TOL = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from online_kv_cache_quantize_gb300 import build
+    build.build()
+
+
+def _setup(bsz, hkv, hq, cap, kind, kbits, vbits, seed):
+    d = 128
+    k, v = W.decode_kv(bsz, hkv, cap, seed=seed)
+    rot, qjl = P.handles(d, kind)
+    caches = []
+    for _ in range(2):
+        kc = B.Cache("prod", kbits, d, rows=bsz * hkv, capacity=cap)
+        vc = B.Cache("mse", vbits, d, rows=bsz * hkv, capacity=cap)
+        B.tq_quantize_kv(kc, rot, torch.from_numpy(k.reshape(-1, d)).cuda().to(torch.bfloat16), qjl=qjl)
+        B.tq_quantize_kv(vc, rot, torch.from_numpy(v.reshape(-1, d)).cuda().to(torch.bfloat16))
+        caches.append((kc, vc))
+    q = torch.from_numpy(W.query_vectors((bsz, hq, d), seed=seed + 1)).cuda()
+    knew = torch.from_numpy(W.round_bf16(W.query_vectors((bsz * hkv, d), seed=seed + 2) * 2)).cuda().to(torch.bfloat16)
+    vnew = torch.from_numpy(W.round_bf16(W.query_vectors((bsz * hkv, d), seed=seed + 3))).cuda().to(torch.bfloat16)
+    return k, v, rot, qjl, caches, q, knew, vnew
+
+
+@pytest.mark.parametrize("kind,kbits,vbits", [("rht", 3, 3), ("dense", 4, 4), ("rht", 2, 2)])
+def test_step_equals_separate_calls(kind, kbits, vbits):
+    bsz, hkv, hq, cap = 3, 2, 8, 1008
+    k, v, rot, qjl, caches, q, knew, vnew = _setup(bsz, hkv, hq, cap, kind, kbits, vbits, seed=40 + kbits)
+    pos = torch.tensor([500, 1007, -1], dtype=torch.int32, device="cuda")  # the third batch row is not appended
+    lens = torch.tensor([501, 1008, 700], dtype=torch.int32, device="cuda")
+    outs = []
+    # separate calls
+    (kc, vc) = caches[0]
+    B.tq_quantize_kv(kc, rot, knew, qjl=qjl, append_pos=pos, heads=hkv)
+    B.tq_quantize_kv(vc, rot, vnew, append_pos=pos, heads=hkv)
+    out0 = torch.empty((bsz, hq, 128), device="cuda")
+    ws0 = B.workspace(B.tq_attn_decode_workspace(q, kc, vc, lens, cap, rot, qjl, out0))
+    B.tq_attn_decode(q, kc, vc, lens, cap, rot, qjl, out0, ws0)
+    # one step call
+    (kc1, vc1) = caches[1]
+    out1 = torch.empty((bsz, hq, 128), device="cuda")
+    ws1 = B.workspace(B.tq_decode_step_workspace(q, kc1, vc1, lens, cap, rot, qjl, out1, knew, vnew, pos))
+    B.tq_decode_step(q, kc1, vc1, lens, cap, rot, qjl, out1, knew, vnew, pos, ws1)
+    torch.cuda.synchronize()
+    for name in ("codes", "signs", "norm", "rnorm"):
+        assert torch.equal(getattr(kc, name), getattr(kc1, name)), f"K {name}"
+    for name in ("codes", "norm"):
+        assert torch.equal(getattr(vc, name), getattr(vc1, name)), f"V {name}"
+    assert torch.equal(out0, out1)
+
+
+def test_step_against_oracle():
+    """The step's output equals the oracle's decode over the oracle-quantized
+    context plus the appended token."""
+    d, bsz, hkv, hq, cap, kind = 128, 2, 2, 8, 512, "rht"
+    k, v, rot, qjl, caches, q, knew, vnew = _setup(bsz, hkv, hq, cap, kind, 3, 3, seed=70)
+    pos_np = np.array([300, 511], dtype=np.int32)
+    pos = torch.from_numpy(pos_np).cuda()
+    lens_np = pos_np + 1
+    lens = torch.from_numpy(lens_np).cuda()
+    (kc, vc) = caches[0]
+    out = torch.empty((bsz, hq, d), device="cuda")
+    ws = B.workspace(B.tq_decode_step_workspace(q, kc, vc, lens, cap, rot, qjl, out, knew, vnew, pos))
+    B.tq_decode_step(q, kc, vc, lens, cap, rot, qjl, out, knew, vnew, pos, ws)
+    torch.cuda.synchronize()
+    # oracle: the context with the new token written at its slot
+    k2, v2 = k.copy(), v.copy()
+    kn = knew.float().cpu().numpy().reshape(bsz, hkv, d)
+    vn = vnew.float().cpu().numpy().reshape(bsz, hkv, d)
+    for b in range(bsz):
+        k2[b, :, pos_np[b]] = kn[b]
+        v2[b, :, pos_np[b]] = vn[b]
+    pi, s = P.oracle_mats(d, kind)
+    kq = oq.quantize(W.round_bf16(k2).reshape(-1, d).astype(np.float64), pi, "prod", 3, s)
+    vq = oq.quantize(W.round_bf16(v2).reshape(-1, d).astype(np.float64), pi, "mse", 3)
+    sh = (bsz, hkv, cap)
+    kcd = {"idx": kq["idx"].reshape(sh + (d,)), "norm16": kq["norm16"].reshape(sh),
+           "rnorm16": kq["rnorm16"].reshape(sh), "z": kq["z"].reshape(sh + (d,))}
+    vcd = {"idx": vq["idx"].reshape(sh + (d,)), "norm16": vq["norm16"].reshape(sh)}
+    want, _ = oa.decode(q.cpu().numpy().astype(np.float64), kcd, vcd, lens_np.tolist(), pi, s,
+                        kq["centroids"], vq["centroids"])
+    got = out.cpu().numpy()
+    # the tolerance is for unit-scale coordinates: scaled by the largest value
+    # norm over sqrt(d), as in the full-shape decode test
+    scale = np.max(vq["norm16"]) / np.sqrt(d)
+    assert np.max(np.abs(got - want)) <= OUT_TOL * scale, np.max(np.abs(got - want)) / scale
+
+
+def test_step_rejects_bad_args_before_enqueueing():
+    d, bsz, hkv, hq, cap = 128, 1, 2, 8, 64
+    k, v, rot, qjl, caches, q, knew, vnew = _setup(bsz, hkv, hq, cap, "rht", 3, 3, seed=90)
+    (kc, vc) = caches[0]
+    before = kc.codes.clone()
+    pos = torch.tensor([10], dtype=torch.int32, device="cuda")
+    lens = torch.tensor([11], dtype=torch.int32, device="cuda")
+    out = torch.empty((bsz, hq, d), device="cuda")
+    ws = B.workspace(B.tq_decode_step_workspace(q, kc, vc, lens, cap, rot, qjl, out, knew, vnew, pos))
+    with pytest.raises(B.TQError):  # workspace too small: nothing may be enqueued
+        B.tq_decode_step(q, kc, vc, lens, cap, rot, qjl, out, knew, vnew, pos, ws[:16])
+    torch.cuda.synchronize()
+    assert torch.equal(kc.codes, before)
