@@ -318,6 +318,12 @@ tq_status tq_device_errors(uint32_t* flags_out, int reset);
  * (1..1000000), then returns after setting TQ_DEVERR_SELFTEST_WAIT. */
 tq_status tq_selftest_bounded_wait(uint32_t limit_us, tq_stream stream);
 
+/* Self-test of the 5th-generation tensor-core path (tcgen05.mma with TMEM
+ * accumulators) that the search kernel is built on: d[128][n] = a[128][k] *
+ * b[n][k]^T, a and b device fp16 row-major, d device fp32 row-major, n in
+ * {16, 32, 64, 128}, k a multiple of 16 up to 128; one CTA on `stream`. */
+tq_status tq_selftest_umma_gemm(const void* a, const void* b, float* d, int n, int k, tq_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

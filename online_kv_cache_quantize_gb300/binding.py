@@ -95,6 +95,8 @@ _SIGS = {
     "tq_decode_step": (_STATUS, [ctypes.POINTER(tq_step_args), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "tq_device_errors": (_STATUS, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "tq_selftest_bounded_wait": (_STATUS, [ctypes.c_uint32, ctypes.c_void_p]),
+    "tq_selftest_umma_gemm": (_STATUS, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_void_p]),
 }
 
 EXPORTED = tuple(_SIGS)
@@ -370,6 +372,13 @@ def tq_device_errors(reset=False):
 def tq_selftest_bounded_wait(limit_us, stream=None):
     """One warp waits on an mbarrier nothing arrives on, at most limit_us."""
     _check(load().tq_selftest_bounded_wait(limit_us, _stream_ptr(stream)), "tq_selftest_bounded_wait")
+
+
+def tq_selftest_umma_gemm(a, b, d, stream=None):
+    """d[128][n] = a[128][k] @ b[n][k]^T on the tcgen05 tensor-core path (fp16 in, fp32 out)."""
+    n, k = b.shape
+    _check(load().tq_selftest_umma_gemm(a.data_ptr(), b.data_ptr(), d.data_ptr(), n, k, _stream_ptr(stream)),
+           "tq_selftest_umma_gemm")
 
 
 def _topk_struct(queries, db, n_db, rot, qjl, k, ids, scores):

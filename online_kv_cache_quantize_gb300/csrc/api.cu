@@ -753,6 +753,18 @@ tq_status tq_device_errors(uint32_t* flags_out, int reset) {
              : TQ_OK;
 }
 
+tq_status tq_selftest_umma_gemm(const void* a, const void* b, float* d, int n, int k, tq_stream stream) {
+    if (!a || !b || !d) return fail(TQ_ERR_INVALID_ARG, "tq_selftest_umma_gemm: NULL operand");
+    if ((n != 16 && n != 32 && n != 64 && n != 128) || k < 16 || k > 128 || k % 16)
+        return fail(TQ_ERR_UNSUPPORTED, "tq_selftest_umma_gemm: n must be 16/32/64/128 and k a multiple of 16 up to 128");
+    if (!aligned(a, 4) || !aligned(b, 4) || !aligned(d, 4)) return fail(TQ_ERR_ALIGNMENT, "tq_selftest_umma_gemm: misaligned");
+    uint32_t* word = nullptr;
+    cudaError_t e = tqk::device_error_word(&word);
+    if (e != cudaSuccess) return cuda_status(e, "tq_selftest_umma_gemm");
+    e = tqk::launch_umma_selftest(a, b, d, n, k, word, (cudaStream_t)stream);
+    return cuda_status(e, "tq_selftest_umma_gemm");
+}
+
 tq_status tq_selftest_bounded_wait(uint32_t limit_us, tq_stream stream) {
     if (limit_us < 1 || limit_us > 1000000) return fail(TQ_ERR_INVALID_ARG, "tq_selftest_bounded_wait: limit_us must be 1..1000000");
     uint32_t* word = nullptr;

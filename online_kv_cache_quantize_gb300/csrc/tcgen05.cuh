@@ -1,0 +1,97 @@
+// 5th-generation tensor core (tcgen05) building blocks: TMEM allocation,
+// shared-memory matrix descriptors, the kind::f16 instruction descriptor,
+// MMA issue and commit, and accumulator loads from TMEM.
+//
+// Operand layout used throughout (both A [M x K] and B [N x K] K-major, no
+// swizzle): the tile is cut into core matrices of 8 rows x 16 bytes (8 fp16
+// along K), each stored as 128 contiguous bytes. Element (r, k) of a tile
+// whose rows hold KC elements sits at byte
+//     (r / 8) * SBO + (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2,
+// with LBO = 128 (next core matrix along K) and SBO = KC * 16 (next group of
+// 8 rows). One MMA consumes K = 16, i.e. two core matrices along K; the
+// descriptor of k-step s starts 256 * s bytes further on.
+#pragma once
+
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace tqk {
+
+// Shared-memory matrix descriptor, K-major, no swizzle.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);  // bits 0-13: start address / 16
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;  // bits 16-29: leading byte offset / 16
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;  // bits 32-45: stride byte offset / 16
+    d |= (uint64_t)1u << 46;                      // bits 46-47: descriptor version 1
+    // base offset 0, absolute LBO mode 0, layout type 0 (no swizzle)
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32, A and B fp16,
+// both K-major, dense, M x N.
+__host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N) {
+    return (1u << 4)                          // D format: fp32
+           | (0u << 7) | (0u << 10)           // A, B format: fp16
+           | (0u << 15) | (0u << 16)          // A, B K-major
+           | ((uint32_t)(N >> 3) << 17)       // N / 8
+           | ((uint32_t)(M >> 4) << 24);      // M / 16
+}
+
+// TMEM allocation by one whole warp; the base address lands in *smem_dst.
+__device__ __forceinline__ void tmem_alloc(uint32_t smem_dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_dst), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         bool accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
+// Arrive on the mbarrier once every MMA this thread issued so far completed.
+__device__ __forceinline__ void umma_commit(uint32_t mbar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(mbar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+
+// Warp w reads TMEM lanes 32(w % 4) .. +31 (thread t: lane 32(w % 4) + t),
+// 16 consecutive 32-bit columns starting at column offset col of taddr.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+
+// byte offset of element (r, k) in a core-matrix tile whose rows hold kc elements
+__host__ __device__ constexpr uint32_t umma_off(int r, int k, int kc) {
+    return (uint32_t)((r >> 3) * (kc * 16) + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2);
+}
+
+}  // namespace tqk
