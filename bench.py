@@ -47,13 +47,14 @@ SCAN_SOURCES = ["online_kv_cache_quantize_gb300/csrc/decode_mma.cuh", "online_kv
                 "online_kv_cache_quantize_gb300/csrc/pipeline.cuh"]
 
 
-def _peaks():
+def _peaks(key="hbm_gbs"):
+    """(peak, source): the measured HBM copy GB/s or cuBLAS bf16 TFLOP/s, else the fallback."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), "measured"
+        return float(p[key]), "measured"
     except Exception:
-        return 6800.0, "fallback"
+        return (6800.0 if key == "hbm_gbs" else 1900.0), "fallback"
 
 
 def _kernel_hash(paths):
@@ -431,6 +432,95 @@ def cpu_baseline_default():
             "sample": f"4 steps of 1/{hkv} KV heads x {tokens} tokens (quantize + 4-head decode), extrapolated to the full step"}
 
 
+# ------------------------------------------------------------ search ----
+SEARCH = dict(name="vector_search_1m", n_db=1_000_000, nq=10_000, d=200, k=10, rotation="dense")
+SEARCH_METRIC = "vector search queries/s (top-10 scored from the codes)"
+
+
+def run_search(args, mode, bits):
+    """Inner-product top-10 over a 1e6 x 200 database quantized on the GPU:
+    one step = tq_score_topk for all 1e4 queries. Roofline: the tensor pipe,
+    algorithmic 2 * nq * n_db * (d + m) flops per step (m = d for PROD)."""
+    import torch
+    from online_kv_cache_quantize_gb300 import binding as B
+    from online_kv_cache_quantize_gb300 import build as bld
+    from online_kv_cache_quantize_gb300 import workloads as W
+
+    torch.cuda.set_device(0)
+    bld.build()
+    L = B.load()
+    w = SEARCH
+    n, nq, d, k = w["n_db"], w["nq"], w["d"], w["k"]
+    db, qs = W.mixture_vectors(n, d=d, queries=nq)
+    rot = B.tq_rotation_to_device(B.tq_make_rotation(W.ROT_SEED, d, w["rotation"]))
+    qjl = B.tq_qjl_to_device(B.tq_make_qjl(W.QJL_SEED, d, d)) if mode == "prod" else None
+    cache = B.Cache(mode, bits, d, rows=1, capacity=n)
+    B.tq_quantize_kv(cache, rot, torch.from_numpy(db).cuda(), qjl=qjl)
+    del db
+    q = torch.from_numpy(qs).cuda()
+    ids = torch.empty((nq, k), dtype=torch.int32, device="cuda")
+    sc = torch.empty((nq, k), dtype=torch.float32, device="cuda")
+    wsz = B.tq_score_topk_workspace(q, cache, n, rot, qjl, k, ids, sc)
+    wsb = B.workspace(wsz)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        B.tq_score_topk(q, cache, n, rot, qjl, k, ids, sc, wsb)
+
+    sampler = ClockSampler(0)
+    sampler.start()
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        step()
+    torch.cuda.synchronize()
+    K = max(1, min(args.steps, 10))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    # end to end: queries from pinned host memory in, ids and scores out
+    hq = torch.from_numpy(qs).pin_memory()
+    hids = torch.empty_like(ids, device="cpu").pin_memory()
+    hsc = torch.empty_like(sc, device="cpu").pin_memory()
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(3)]
+    for i in range(3):
+        flush.fill_(i & 0xFF)
+        eev[i][0].record(stream)
+        q.copy_(hq, non_blocking=True)
+        step()
+        hids.copy_(ids, non_blocking=True)
+        hsc.copy_(sc, non_blocking=True)
+        eev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in eev)
+    step_s = statistics.mean(ms) / 1e3
+    m = d if mode == "prod" else 0
+    flops = 2.0 * nq * n * (d + m)
+    peak, peak_kind = _peaks("bf16_tflops")
+    achieved = flops / step_s / 1e12
+    return {
+        "metric": SEARCH_METRIC, "value": nq / step_s, "unit": "queries/s", "n_gpus": 1, "steps": K,
+        "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16 (hi/lo split queries), f32 accumulate", "data": "synthetic",
+        "config": {"workload": w["name"], "n_db": n, "nq": nq, "d": d, "k": k, "mode": mode, "bits": bits,
+                   "rotation": w["rotation"], "l2": "flushed (256 MiB write) before every timed step"},
+        "roofline": {"kernel": "topk_umma_kernel (tcgen05 scan)", "bound": "tensor", "achieved": achieved,
+                     "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_kind,
+                     "alg_flops_per_step": flops, "traffic": None},
+        "e2e": {"value": nq / (e2e_ms / 1e3), "unit": "queries/s", "h2d_bytes_per_step": qs.nbytes,
+                "d2h_bytes_per_step": hids.numel() * 4 + hsc.numel() * 4, "steps": 3},
+        "gpu_launches": 3 * K,  # query prep, scan, merge
+        "clocks": clocks,
+        "cpu_baseline": None,
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -443,6 +533,8 @@ def main():
     ap.add_argument("--k-bits", type=int, default=None)
     ap.add_argument("--v-bits", type=int, default=None)
     ap.add_argument("--rotation", choices=["rht", "dense"], default=None)
+    ap.add_argument("--search", choices=["prod2", "prod4", "mse2", "mse4"], default=None,
+                    help="time the 1e6 x 200 inner-product top-10 search instead of the decode step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -451,6 +543,13 @@ def main():
     for key, val in (("k_bits", args.k_bits), ("v_bits", args.v_bits), ("rotation", args.rotation)):
         if val is not None:
             WORKLOAD[key] = val
+    if args.search:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the search has no reference arm here; "
+                              "its oracle parity is in tests/test_gpu_topk.py"}))
+            return
+        print(json.dumps(run_search(args, args.search[:-1], int(args.search[-1]))), flush=True)
+        return
     if args.impl == "reference":
         res = run_reference(args)
         if res is not None:

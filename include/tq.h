@@ -294,7 +294,13 @@ typedef struct {
 } tq_topk_args;
 
 size_t tq_score_topk_workspace(const tq_topk_args* a);
+/* Scores on the tcgen05 tensor cores (database tiles de-quantized into shared
+ * memory, queries as fp16 hi/lo halves, fp32 accumulators in TMEM) when d and
+ * m are at most 256; otherwise on a SIMT kernel. Both rank the same scores. */
 tq_status tq_score_topk(const tq_topk_args* a, void* workspace, size_t ws_bytes, tq_stream stream);
+/* Process-wide switch: on != 0 makes tq_score_topk use the SIMT scan for
+ * every shape (to compare the two); returns the previous setting. */
+int tq_topk_force_simt(int on);
 
 /* ------------------------------------------------------------------------ *
  * Device error word.                                                       *

@@ -238,6 +238,10 @@ uint16_t bf16_bits_of(double exact_bf16_value) {
 
 namespace {
 
+// tq_score_topk uses the SIMT scan even where the tcgen05 scan fits (for
+// comparing the two; see tq_topk_force_simt)
+bool g_topk_simt = false;
+
 // streams and events of tq_decode_step, per device
 constexpr int kMaxStepDevices = 64;
 struct StepStreams {
@@ -677,8 +681,26 @@ tq_status tq_score_topk(const tq_topk_args* a, void* workspace, size_t ws_bytes,
     tp.cand_id = (int32_t*)(ws + off_ci);
     tp.ids = a->ids;
     tp.scores = a->scores;
-    e = tqk::launch_topk(tp, cb, prod ? 1 : 0, st);
+    // the tcgen05 scan where its shared-memory plan fits (d, m <= 256 padded
+    // to a multiple of 16), the SIMT scan otherwise
+    const double lam = pick_lambda(a->d, cb, c);
+    pair_table(c, cb, lam, tp.ktab);
+    pair_table_lo(c, cb, lam, tp.ktab_lo);
+    tp.inv_lam = (float)(1.0 / lam);
+    tp.ks = (int)round_up((size_t)std::max(a->d, m), 16);
+    if ((e = tqk::device_error_word(&tp.err)) != cudaSuccess) return cuda_status(e, "tq_score_topk error word");
+    e = g_topk_simt ? cudaErrorNotSupported : tqk::launch_topk_umma(tp, cb, prod ? 1 : 0, cb >= 3 ? 1 : 0, st);
+    if (e == cudaErrorNotSupported) {
+        (void)cudaGetLastError();  // nothing was launched
+        e = tqk::launch_topk(tp, cb, prod ? 1 : 0, st);
+    }
     return cuda_status(e, "tq_score_topk");
+}
+
+int tq_topk_force_simt(int on) {
+    const int prev = g_topk_simt ? 1 : 0;
+    g_topk_simt = on != 0;
+    return prev;
 }
 
 size_t tq_decode_step_workspace(const tq_step_args* a) { return a ? tq_attn_decode_workspace(&a->attn) : 0; }

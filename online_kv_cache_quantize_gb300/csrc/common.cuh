@@ -46,6 +46,14 @@ __device__ __forceinline__ uint16_t f16_bits_sat(float v) {
 
 __device__ __forceinline__ float f16_bits_to_f32(uint16_t b) { return __half2float(__ushort_as_half(b)); }
 
+// fp16 bits of v (lo = 0) or of v - fp16(v) (lo = 1): the hi/lo split that
+// carries an fp32 operand into fp16 tensor-core products
+__device__ __forceinline__ uint32_t half_split(float v, int lo) {
+    __half h = __float2half_rn(v);
+    if (lo) h = __float2half_rn(v - __half2float(h));
+    return (uint32_t)__half_as_ushort(h);
+}
+
 // Bits [off, off + nbits) of a little-endian bit stream held in 32-bit words,
 // nbits <= 32, reading at most words[off/32] and words[off/32 + 1].
 __device__ __forceinline__ uint32_t stream_bits(const uint32_t* words, int off, int nbits, int nwords) {

@@ -15,13 +15,6 @@ namespace tqk {
 
 constexpr int kPrepWarps = 8;
 
-// fp16 bits of v (lo = 0) or of v - fp16(v) (lo = 1)
-__device__ __forceinline__ uint32_t half_split(float v, int lo) {
-    __half h = __float2half_rn(v);
-    if (lo) h = __float2half_rn(v - __half2float(h));
-    return (uint32_t)__half_as_ushort(h);
-}
-
 // The decode scan's B operands of one query row (d = m = 128), in the order
 // its threads load them: word ((ks * 2 + lo) * 4 + c) * 16 + 2 * kk + r holds
 // the fp16 pair (coordinates i, i + 1), i = 32c + 4kk + 2r, of the hi (lo =

@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_scan_kernel(const __grid
 }
 
 // One warp per query: select the k best of n_chunks * k candidates.
-__global__ void __launch_bounds__(256) topk_merge_kernel(const __grid_constant__ TopkParams p) {
+static __global__ void __launch_bounds__(256) topk_merge_kernel(const __grid_constant__ TopkParams p) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int q = blockIdx.x * 8 + warp;
     if (q >= p.nq) return;

@@ -1,0 +1,340 @@
+// Inner-product search on the 5th-generation tensor cores (tcgen05).
+//
+// Same scores as topk.cuh (A2A TurboQuant explainer, "Benchmarks and
+// real-world performance" and "Applications"; the decode logit estimator
+// l = n (<q', c[idx]> + sqrt(pi/2)/m * gamma <u, 2z - 1>) per database row),
+// computed as a dense contraction: for a tile of 128 database rows and a
+// block of 32 queries,
+//     D[row][2j + s] = sum_i A[row][i] B[2j + s][i]
+// with A the de-quantized rows (lam * centroid as fp16, from a pair table;
+// the fp16 residual of lam * centroid as a second table when the codebook
+// has 8 or more cells; gamma * (2z - 1) for the sign part) and B the queries
+// split into fp16 hi (s = 0) and lo (s = 1) halves (q' against the centroid
+// parts, lam * kappa * u against the sign part). The score is
+// n * (D[row][2j] + D[row][2j + 1]) / lam.
+//
+// Per CTA: 32 queries (B resident in shared memory for the whole chunk) and a
+// chunk of database rows. Per 128-row tile: the packed codes and signs land
+// in a staging buffer by bulk copy (double-buffered, one tile ahead); 256
+// threads de-quantize each A segment into a core-matrix tile (two buffers,
+// so the next segment is built while the tensor core runs on the previous
+// one); one thread issues the MMAs into a 128 x 64 fp32 TMEM accumulator;
+// the epilogue reads it back with tcgen05.ld and keeps per-warp top-k lists,
+// merged per query at the end into the chunk's candidates.
+#include "pipeline.cuh"
+#include "tcgen05.cuh"
+#include "topk.cuh"
+
+namespace tqk {
+
+constexpr int kTuRows = 128;    // database rows per tile (MMA M)
+constexpr int kTuQ = 32;        // queries per CTA
+constexpr int kTuN = 2 * kTuQ;  // MMA N: hi and lo column per query
+constexpr int kTuThreads = 256;
+constexpr int kTuSmemLimit = 227 * 1024 - 4096;  // dynamic part; static tables stay below 4 KB
+
+struct TuLayout {
+    size_t b, a0, a1, st0, st1, sgn, ls, li, total;
+    int kcb, stage_bytes;
+};
+
+__host__ __device__ inline TuLayout tu_layout(int ks, int nseg_b, int code_stride, int sign_stride, int k) {
+    TuLayout L;
+    L.kcb = nseg_b * ks;
+    const size_t bb = (size_t)kTuN * L.kcb * 2;
+    const size_t ab = (size_t)kTuRows * ks * 2;
+    L.stage_bytes = kTuRows * (code_stride + sign_stride) + 16;  // + slack for the 8-byte reads at a row end
+    L.b = 0;
+    L.a0 = bb;
+    L.a1 = L.a0 + ab;
+    L.st0 = L.a1 + ab;
+    L.st1 = L.st0 + ((L.stage_bytes + 127) / 128) * 128;
+    L.sgn = L.st1 + ((L.stage_bytes + 127) / 128) * 128;
+    L.ls = L.sgn + 256 * 16;
+    L.li = L.ls + (size_t)8 * 16 * k * 4;
+    L.total = L.li + (size_t)8 * 16 * k * 4;
+    return L;
+}
+
+template <int CB, bool PROD, bool LO>
+__global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_constant__ TopkParams p) {
+    constexpr int NSEG_A = 1 + (LO ? 1 : 0) + (PROD ? 1 : 0);
+    constexpr int NSEG_B = 1 + (PROD ? 1 : 0);
+    constexpr int NT = 1 << (2 * CB);
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ __align__(8) uint64_t s_bar[2];    // MMA completion per A buffer
+    __shared__ __align__(8) uint64_t s_sbar[2];   // staging copies per buffer
+    __shared__ uint32_t s_tmem;
+    __shared__ uint32_t s_ktab[NT];
+    __shared__ uint32_t s_klo[LO ? NT : 1];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int ks = p.ks, k = p.k, d = p.d, m = p.m;
+    const int cs = p.code_stride, ss = PROD ? p.sign_stride : 0;
+    const TuLayout Lo = tu_layout(ks, NSEG_B, cs, ss, k);
+    const int kcb = Lo.kcb;
+    unsigned char* sB = smem + Lo.b;
+    unsigned char* sA[2] = {smem + Lo.a0, smem + Lo.a1};
+    unsigned char* sSt[2] = {smem + Lo.st0, smem + Lo.st1};
+    const uint4* s_sgn = reinterpret_cast<const uint4*>(smem + Lo.sgn);
+    float* s_ls = reinterpret_cast<float*>(smem + Lo.ls);  // [8 warps][16 queries][k]
+    int* s_li = reinterpret_cast<int*>(smem + Lo.li);
+
+    const int chunk = blockIdx.x;
+    const int q0 = blockIdx.y * kTuQ;
+    const int nq_here = min(kTuQ, p.nq - q0);
+    const int64_t r0 = (int64_t)chunk * p.chunk_rows;
+    const int64_t r1 = min(r0 + p.chunk_rows, p.n_db);
+    const float lam_kappa = p.qjl_scale / p.inv_lam;
+
+    // ---- tables, lists, B tile ----
+    for (int i = tid; i < NT; i += blockDim.x) {
+        s_ktab[i] = p.ktab[i];
+        if constexpr (LO) s_klo[i] = p.ktab_lo[i];
+    }
+    for (int i = tid; i < 256; i += blockDim.x) {
+        // flips that make the fp16 pair (-g, -g) positive where sign bits 2w, 2w+1 of byte i are set
+        uint4 v;
+        v.x = ((uint32_t)(i & 1) << 15) | ((uint32_t)((i >> 1) & 1) << 31);
+        v.y = ((uint32_t)((i >> 2) & 1) << 15) | ((uint32_t)((i >> 3) & 1) << 31);
+        v.z = ((uint32_t)((i >> 4) & 1) << 15) | ((uint32_t)((i >> 5) & 1) << 31);
+        v.w = ((uint32_t)((i >> 6) & 1) << 15) | ((uint32_t)((i >> 7) & 1) << 31);
+        reinterpret_cast<uint4*>(smem + Lo.sgn)[i] = v;
+    }
+    for (int i = tid; i < 8 * 16 * k; i += blockDim.x) {
+        s_ls[i] = -INFINITY;
+        s_li[i] = 0x7fffffff;
+    }
+    for (int e = tid; e < kTuN * (kcb / 2); e += blockDim.x) {
+        const int n = e / (kcb / 2), col = (e % (kcb / 2)) * 2;
+        const int j = n >> 1, hl = n & 1, seg = col / ks, i = col % ks;
+        float v0 = 0.0f, v1 = 0.0f;
+        if (j < nq_here) {
+            if (seg == 0) {
+                const float* qp = p.qprime + (int64_t)(q0 + j) * d;
+                if (i < d) v0 = qp[i];
+                if (i + 1 < d) v1 = qp[i + 1];
+            } else {
+                const float* up = p.u + (int64_t)(q0 + j) * m;
+                if (i < m) v0 = lam_kappa * up[i];
+                if (i + 1 < m) v1 = lam_kappa * up[i + 1];
+            }
+        }
+        *reinterpret_cast<uint32_t*>(sB + umma_off(n, col, kcb)) = half_split(v0, hl) | (half_split(v1, hl) << 16);
+    }
+    const uint32_t bar[2] = {(uint32_t)__cvta_generic_to_shared(&s_bar[0]), (uint32_t)__cvta_generic_to_shared(&s_bar[1])};
+    const uint32_t sbar[2] = {(uint32_t)__cvta_generic_to_shared(&s_sbar[0]),
+                              (uint32_t)__cvta_generic_to_shared(&s_sbar[1])};
+    if (tid == 0) {
+        mbar_init(bar[0], 1);
+        mbar_init(bar[1], 1);
+        mbar_init(sbar[0], 1);
+        mbar_init(sbar[1], 1);
+        mbar_init_fence();
+    }
+    if (warp == 0) {
+        tmem_alloc((uint32_t)__cvta_generic_to_shared(&s_tmem), kTuN);
+        tmem_relinquish();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = s_tmem;
+
+    // staging of tile t (codes then signs of its rows) into buffer t & 1, by thread 0
+    const int64_t ntile = r1 > r0 ? (r1 - r0 + kTuRows - 1) / kTuRows : 0;
+    auto stage = [&](int64_t t) {
+        const int64_t t0 = r0 + t * kTuRows;
+        const int rows = (int)min((int64_t)kTuRows, r1 - t0);
+        const int b = (int)(t & 1);
+        const uint32_t dst = (uint32_t)__cvta_generic_to_shared(sSt[b]);
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(sbar[b], (uint32_t)rows * (cs + ss));
+        bulk_g2s(dst, p.codes + t0 * cs, (uint32_t)rows * cs, sbar[b]);
+        if constexpr (PROD) bulk_g2s(dst + kTuRows * cs, p.signs + t0 * ss, (uint32_t)rows * ss, sbar[b]);
+    };
+    if (tid == 0 && ntile > 0) stage(0);
+
+    const uint32_t idesc = umma_idesc_f16(kTuRows, kTuN);
+    const uint32_t sB_a = (uint32_t)__cvta_generic_to_shared(sB);
+    const uint32_t sA_a[2] = {(uint32_t)__cvta_generic_to_shared(sA[0]), (uint32_t)__cvta_generic_to_shared(sA[1])};
+    const int r = tid & (kTuRows - 1);      // de-quantize: this thread's row in the tile
+    const int half = tid >> 7;              // ... and half of the 8-coordinate units
+    const int units = ks / 8, u0 = half * (units / 2), u1 = u0 + units / 2;
+    const int er = 32 * (warp & 3) + lane;  // epilogue: this thread's row (TMEM lane)
+    const int ecol = 32 * (warp >> 2);      // ... and its 32 columns (16 queries)
+    int step = 0;
+    bool ok = true;
+
+    for (int64_t t = 0; t < ntile && ok; ++t) {
+        const int64_t t0 = r0 + t * kTuRows;
+        const int sb = (int)(t & 1);
+        if (tid == 0 && t + 1 < ntile) stage(t + 1);  // its buffer was last read in tile t - 1
+        ok = !__syncthreads_or(!mbar_wait_bounded(sbar[sb], (uint32_t)((t >> 1) & 1), kWaitLimitNs, p.err, kErrScanWait));
+        if (!ok) break;
+        const unsigned char* crow = sSt[sb] + r * cs;
+        const unsigned char* srow = sSt[sb] + kTuRows * cs + r * ss;
+        const bool rvalid = t0 + r < r1;
+        uint32_t g2 = 0u;
+        if constexpr (PROD) {
+            const uint32_t g16 = rvalid ? (uint32_t)p.rnorm[t0 + r] : 0u;
+            g2 = (g16 | 0x8000u) | ((g16 | 0x8000u) << 16);  // (-gamma, -gamma)
+        }
+        for (int seg = 0; seg < NSEG_A; ++seg) {
+            const int buf = step & 1;
+            if (step >= 2) {
+                ok = !__syncthreads_or(
+                    !mbar_wait_bounded(bar[buf], (uint32_t)(((step - 2) >> 1) & 1), kWaitLimitNs, p.err, kErrScanWait));
+                if (!ok) break;
+            }
+            const bool sign_seg = PROD && seg == NSEG_A - 1;
+            unsigned char* dstA = sA[buf];
+            for (int u = u0; u < u1; ++u) {
+                uint4 w;
+                if (sign_seg) {
+                    const uint4 f = s_sgn[rvalid ? srow[u] : 0];
+                    w = make_uint4(g2 ^ f.x, g2 ^ f.y, g2 ^ f.z, g2 ^ f.w);
+                } else {
+                    // 8 codes: CB bytes starting at byte CB * u of the row
+                    const int o = CB * u;
+                    const uint32_t* wp = reinterpret_cast<const uint32_t*>(crow + (o & ~3));
+                    const uint32_t bits = rvalid ? __funnelshift_r(wp[0], wp[1], 8 * (o & 3)) : 0u;
+                    const uint32_t* tab = (LO && seg == 1) ? s_klo : s_ktab;
+                    constexpr uint32_t M2 = (1u << (2 * CB)) - 1u;
+                    w.x = tab[bits & M2];
+                    w.y = tab[(bits >> (2 * CB)) & M2];
+                    w.z = tab[(bits >> (4 * CB)) & M2];
+                    w.w = tab[CB == 4 ? (bits >> 24) : ((bits >> (6 * CB)) & M2)];
+                }
+                *reinterpret_cast<uint4*>(dstA + umma_off(r, 8 * u, ks)) = w;
+            }
+            fence_proxy_async_smem();  // the tile is read by the tensor core next
+            __syncthreads();
+            if (tid == 0) {
+                tc_fence_after_sync();
+                const int bseg = sign_seg ? 1 : 0;
+                for (int s = 0; s < ks / 16; ++s)
+                    umma_f16(tmem, umma_desc(sA_a[buf] + 256 * s, 128, ks * 16),
+                             umma_desc(sB_a + (uint32_t)(bseg * ks / 8 + 2 * s) * 128, 128, kcb * 16), idesc,
+                             seg > 0 || s > 0);
+                umma_commit(bar[buf]);
+            }
+            ++step;
+        }
+        if (!ok) break;
+        // ---- epilogue: all MMAs of this tile done ----
+        ok = !__syncthreads_or(!mbar_wait_bounded(bar[(step - 1) & 1], (uint32_t)(((step - 1) >> 1) & 1), kWaitLimitNs,
+                                                  p.err, kErrScanWait));
+        if (!ok) break;
+        tc_fence_after_sync();
+        float v[32];
+        {
+            float a[16], b[16];
+            const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)ecol;
+            tmem_ld16(ta, a);
+            tmem_ld16(ta + 16, b);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                v[i] = a[i];
+                v[16 + i] = b[i];
+            }
+        }
+        const int64_t erow = t0 + er;
+        const bool evalid = erow < r1;
+        const float scale = evalid ? f16_bits_to_f32(p.norm[erow]) * p.inv_lam : 0.0f;
+        const int id = (int)erow;
+        float* wls = s_ls + warp * 16 * k;
+        int* wli = s_li + warp * 16 * k;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+            const int j = (ecol >> 1) + jj;
+            if (j < nq_here) {  // warp-uniform
+                const float sc = scale * (v[2 * jj] + v[2 * jj + 1]);
+                float* ls = wls + jj * k;
+                int* li = wli + jj * k;
+                unsigned cand = __ballot_sync(TQ_FULL_MASK, evalid && better(sc, id, ls[k - 1], li[k - 1]));
+                while (cand) {
+                    const int src = __ffs(cand) - 1;
+                    cand &= cand - 1;
+                    const float cs_ = __shfl_sync(TQ_FULL_MASK, sc, src);
+                    const int ci = __shfl_sync(TQ_FULL_MASK, id, src);
+                    if (lane == 0) list_insert(ls, li, k, cs_, ci);
+                    __syncwarp();
+                }
+            }
+        }
+        tc_fence_before_sync();
+        __syncthreads();  // D is overwritten by the next tile's first MMA
+    }
+    if (!ok) {
+        // a wait ran out (the error word says so): let the copies and MMAs
+        // still in flight finish, bounded, before TMEM and smem are released
+        for (int b = 0; b < 2; ++b) {
+            mbar_wait_bounded(sbar[b], 0, kWaitLimitNs, p.err, kErrScanWait);
+            mbar_wait_bounded(sbar[b], 1, kWaitLimitNs, p.err, kErrScanWait);
+        }
+        if (step > 0)
+            mbar_wait_bounded(bar[(step - 1) & 1], (uint32_t)(((step - 1) >> 1) & 1), kWaitLimitNs, p.err, kErrScanWait);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTuN);
+
+    // ---- merge the four warp lists of each query, write the chunk's candidates ----
+    if (tid < nq_here) {
+        const int j = tid;
+        const int base_w = 4 * (j >> 4), jj = j & 15;
+        float* ls0 = s_ls + (base_w * 16 + jj) * k;
+        int* li0 = s_li + (base_w * 16 + jj) * k;
+        for (int w4 = 1; w4 < 4; ++w4) {
+            const float* ls = s_ls + ((base_w + w4) * 16 + jj) * k;
+            const int* li = s_li + ((base_w + w4) * 16 + jj) * k;
+            for (int e = 0; e < k; ++e) list_insert(ls0, li0, k, ls[e], li[e]);
+        }
+        for (int e = 0; e < k; ++e) {
+            const int64_t o = ((int64_t)(q0 + j) * p.n_chunks + chunk) * p.k + e;
+            p.cand_score[o] = ls0[e];
+            p.cand_id[o] = li0[e];
+        }
+    }
+}
+
+template <int CB, bool PROD, bool LO>
+static cudaError_t go_tu(const TopkParams& p, size_t smem, cudaStream_t s) {
+    auto kern = topk_umma_kernel<CB, PROD, LO>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.n_chunks, (p.nq + kTuQ - 1) / kTuQ);
+    kern<<<grid, kTuThreads, smem, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    topk_merge_kernel<<<(p.nq + 7) / 8, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_topk_umma(const TopkParams& p, int cb, int prod, int lo, cudaStream_t s) {
+    if (p.ks < 16 || p.ks > 256 || p.ks % 16 || p.chunk_rows % kTuRows || p.code_stride % 16 ||
+        (prod && p.sign_stride % 16) || p.k < 1 || p.k > kTopkMaxK)
+        return cudaErrorNotSupported;
+    // every 8-code unit the kernel reads lies inside a staged row
+    if (cb * p.ks / 8 > p.code_stride || (prod && p.ks / 8 > p.sign_stride)) return cudaErrorNotSupported;
+    const TuLayout L = tu_layout(p.ks, prod ? 2 : 1, p.code_stride, prod ? p.sign_stride : 0, p.k);
+    if (L.total > (size_t)kTuSmemLimit) return cudaErrorNotSupported;
+    if (p.nq <= 0 || p.n_chunks <= 0) return cudaSuccess;
+#define TQ_TU(CBV)                                                                      \
+    case CBV:                                                                           \
+        if (prod) return lo ? go_tu<CBV, true, true>(p, L.total, s) : go_tu<CBV, true, false>(p, L.total, s); \
+        return lo ? go_tu<CBV, false, true>(p, L.total, s) : go_tu<CBV, false, false>(p, L.total, s);
+    switch (cb) {
+        TQ_TU(1)
+        TQ_TU(2)
+        TQ_TU(3)
+        TQ_TU(4)
+    }
+#undef TQ_TU
+    return cudaErrorNotSupported;
+}
+
+}  // namespace tqk

@@ -149,8 +149,18 @@ struct TopkParams {
     int32_t* cand_id;     // [nq][n_chunks][k]
     int32_t* ids;
     float* scores;
+    // tensor-core scan: lam * centroid fp16 pair tables (hi and the residual
+    // lo), 1 / lam, the segment width (padded d and m) and the error word
+    uint32_t ktab[256];
+    uint32_t ktab_lo[256];
+    float inv_lam;
+    int ks;
+    uint32_t* err;
 };
 
 cudaError_t launch_topk(const TopkParams& p, int code_bits, int prod, cudaStream_t s);
+// tcgen05 search scan + merge; returns cudaErrorNotSupported when the shape
+// does not fit its shared-memory plan (the caller then uses launch_topk)
+cudaError_t launch_topk_umma(const TopkParams& p, int code_bits, int prod, int lo, cudaStream_t s);
 
 }  // namespace tqk

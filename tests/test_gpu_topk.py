@@ -93,3 +93,43 @@ def test_full_size_search_sampled():
     # quality figure only (not parity): overlap with the exact top-10
     truth, _ = ot.exact_topk(qs, db, 10)
     print(f"recall@10 vs exact inner product, 2-bit PROD, 1e6 rows: {ot.recall_at_k(gids, truth):.3f}")
+
+
+@pytest.mark.parametrize("mode,bits", [("prod", 2), ("mse", 4), ("prod", 4)])
+def test_topk_tensor_core_and_simt_paths(mode, bits):
+    """The tcgen05 scan (used for d <= 256) and the SIMT scan rank the same
+    scores: both checked against the oracle on the same oracle-packed codes."""
+    d, n = 200, 9000  # 9000 rows: two full 4096-row chunks and a ragged one
+    db, qs = W.mixture_vectors(n, d=d, queries=45)  # 45 queries: a full and a ragged 32-query block
+    pi, s = P.oracle_mats(d, "dense")
+    qz = oq.quantize(db.astype(np.float64), pi, mode, bits, s if mode == "prod" else None)
+    cache = P.oracle_cache_planes(qz, mode, bits, 1, n)
+    rot, qjl = P.handles(d, "dense")
+    want = ot.scores(qs, pi, s if mode == "prod" else None, qz["idx"], qz["norm16"], qz["centroids"],
+                     qz.get("rnorm16"), qz.get("z"))
+    lib = B.load()
+    results = {}
+    for simt in (0, 1):
+        prev = lib.tq_topk_force_simt(simt)
+        try:
+            results[simt] = _gpu_topk(qs, cache, n, rot, qjl if mode == "prod" else None, 10)
+        finally:
+            lib.tq_topk_force_simt(prev)
+        _check_topk(results[simt][0], results[simt][1], want, 10)
+    assert B.tq_device_errors() == (B.TQ_OK, 0)
+
+
+def test_topk_wide_codes_fall_back():
+    """d = 256 with 4-bit codes and 256 sign bits does not fit the tensor-core
+    scan's shared-memory plan; the SIMT scan serves it with the same parity."""
+    d, n = 256, 3000
+    r = np.random.default_rng(12)
+    db = r.standard_normal((n, d)).astype(np.float32)
+    qs = r.standard_normal((7, d)).astype(np.float32)
+    pi, s = P.oracle_mats(d, "rht")
+    qz = oq.quantize(db.astype(np.float64), pi, "prod", 5, s)
+    cache = P.oracle_cache_planes(qz, "prod", 5, 1, n)
+    rot, qjl = P.handles(d, "rht")
+    gids, gsc = _gpu_topk(qs, cache, n, rot, qjl, 10)
+    want = ot.scores(qs, pi, s, qz["idx"], qz["norm16"], qz["centroids"], qz["rnorm16"], qz["z"])
+    _check_topk(gids, gsc, want, 10)
