@@ -535,6 +535,8 @@ def main():
     ap.add_argument("--rotation", choices=["rht", "dense"], default=None)
     ap.add_argument("--search", choices=["prod2", "prod4", "mse2", "mse4"], default=None,
                     help="time the 1e6 x 200 inner-product top-10 search instead of the decode step")
+    ap.add_argument("--search-rows", type=int, default=None, help="database rows (smaller case for profiling)")
+    ap.add_argument("--search-queries", type=int, default=None, help="queries (smaller case for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -544,6 +546,10 @@ def main():
         if val is not None:
             WORKLOAD[key] = val
     if args.search:
+        if args.search_rows:
+            SEARCH["n_db"] = args.search_rows
+        if args.search_queries:
+            SEARCH["nq"] = args.search_queries
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the search has no reference arm here; "
                               "its oracle parity is in tests/test_gpu_topk.py"}))

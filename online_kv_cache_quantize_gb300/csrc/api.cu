@@ -207,9 +207,12 @@ tq_status plan_decode(const tq_decode_args* a, DecodePlan* pl) {
 namespace {
 
 // B-operand fragments of mma.sync m16n8k16 for a 128 x 128 map y = W x:
-// element (k, n) of n-tile nt is W[sigma(nt, n)][16 kk + k] with the output
-// permutation sigma(nt, n) = 32 (n / 2) + 2 nt + n % 2 (so accumulators land
-// in the quantize kernel's quad layout), stored [kk][nt][lane] as two words.
+// element (k, n) of n-tile nt in k-step kk is W[sigma(nt, n)][pi(kk, k)]
+// with the output permutation sigma(nt, n) = 32 (n / 2) + 2 nt + n % 2 (so
+// accumulators land in the quantize kernel's quad layout) and the input
+// permutation pi(kk, 2c + e) = 32c + 4kk + e, pi(kk, 2c + 8 + e) = 32c + 4kk
+// + 2 + e (so thread c of a quad builds its A fragments from its own
+// coordinates 32c .. 32c + 31), stored [kk][nt][lane] as two words.
 template <typename F>
 std::vector<uint2v> mma_b_fragments(F wbits) {
     std::vector<uint2v> out((size_t)8 * 16 * 32);
@@ -218,7 +221,10 @@ std::vector<uint2v> mma_b_fragments(F wbits) {
             for (int lane = 0; lane < 32; ++lane) {
                 const int g = lane >> 2, c = lane & 3;
                 const int o = 32 * (g >> 1) + 2 * nt + (g & 1);
-                auto e = [&](int k) { return (uint32_t)wbits(o, 16 * kk + k); };
+                auto e = [&](int k) {
+                    const int cc = (k & 7) >> 1, hi = k >> 3, ee = k & 1;
+                    return (uint32_t)wbits(o, 32 * cc + 4 * kk + 2 * hi + ee);
+                };
                 uint2v v;
                 v.x = e(2 * c) | (e(2 * c + 1) << 16);
                 v.y = e(2 * c + 8) | (e(2 * c + 9) << 16);

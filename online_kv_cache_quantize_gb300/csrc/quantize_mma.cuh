@@ -13,7 +13,9 @@
 //  * dense rotation: Y = X Pi^T on the tensor cores, Pi^T split into three
 //    bf16 limbs (about 24 bits), X exact in bf16 or split into three limbs
 //    when it is fp32; the host stores the B operand in fragment order with the
-//    output columns permuted so that the accumulators land in the quad layout;
+//    output columns permuted so that the accumulators land in the quad layout
+//    and the K order permuted so that each thread builds its A fragments in
+//    registers from its own coordinates (k-step kk takes 32c + 4kk .. +3);
 //  * RHT: the Walsh-Hadamard butterflies run in registers in the quad layout
 //    (strides 1..16 inside a thread, 32 and 64 across the quad);
 //  * S r: R split into bf16 hi/lo (16 bits) against S, which is exact in bf16.
@@ -27,14 +29,11 @@
 
 namespace tqk {
 
-constexpr int kQmWarps = 4;  // warps per CTA (3 for fp32 input with the dense rotation)
+constexpr int kQmWarps = 4;  // warps per CTA
 constexpr int kQmSmemLimit = 227 * 1024;
 
-// The dense rotation with fp32 input keeps three limbs of X per warp next to
-// the 96 KB of Pi^T fragments, so it runs 3 warps per CTA to stay in 227 KB.
 template <typename XT, bool RHT>
-constexpr int qm_warps() { return (!RHT && sizeof(XT) == 4) ? 3 : kQmWarps; }
-constexpr int kQmRowWords = 68;  // operand tiles: 128 bf16 + 8 pad per row (conflict-free fragments)
+constexpr int qm_warps() { return kQmWarps; }
 
 __device__ __forceinline__ void mma16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                               uint32_t b0, uint32_t b1) {
@@ -75,21 +74,19 @@ __device__ __forceinline__ float stage_at(const unsigned char* t, int r, int i) 
     else return __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t*>(t + QmStage<XT>::off(r, i))) << 16);
 }
 
-template <typename XT, int NLIMB_X>
+template <typename XT>
 struct QmSmem {
-    static constexpr int AT = NLIMB_X > 2 ? NLIMB_X : 2;  // operand tiles: X limbs, then R hi/lo
-    static constexpr int AT_BYTES = AT * 16 * kQmRowWords * 4;
-    static constexpr int WARP_BYTES = 2 * QmStage<XT>::BYTES + AT_BYTES;  // double-buffered staging
+    static constexpr int WARP_BYTES = 2 * QmStage<XT>::BYTES;  // double-buffered staging
 };
 
 template <typename XT, int CB, bool PROD, bool RHT>
-__global__ void __launch_bounds__(kQmWarps * 32) quantize_mma_kernel(const __grid_constant__ QuantParams p) {
+__global__ void __launch_bounds__(kQmWarps * 32, 3) quantize_mma_kernel(const __grid_constant__ QuantParams p) {
     constexpr int D = 128;
     constexpr int L = 1 << CB;
     constexpr int H = L / 2;
     constexpr int NLX = (!RHT && sizeof(XT) == 4) ? 3 : 1;  // limbs of X for the dense GEMM
     constexpr int NW = qm_warps<XT, RHT>();
-    using S = QmSmem<XT, NLX>;
+    using S = QmSmem<XT>;
     using ST = QmStage<XT>;
     extern __shared__ __align__(16) unsigned char smem[];
     constexpr int B1_BYTES = RHT ? 0 : 3 * 8 * 16 * 32 * 8;
@@ -101,7 +98,6 @@ __global__ void __launch_bounds__(kQmWarps * 32) quantize_mma_kernel(const __gri
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
     unsigned char* xs_base = smem + B1_BYTES + B2_BYTES + warp * S::WARP_BYTES;  // 2 raw staging tiles
-    uint32_t* at = reinterpret_cast<uint32_t*>(xs_base + 2 * ST::BYTES);       // [AT][16][68]
     const uint32_t xs_s = (uint32_t)__cvta_generic_to_shared(xs_base);
 
     // ---- CTA set-up: B fragments (cp.async, all in flight; completed by the
@@ -118,10 +114,12 @@ __global__ void __launch_bounds__(kQmWarps * 32) quantize_mma_kernel(const __gri
         if (threadIdx.x < kMaxLevels) s_cent[threadIdx.x] = p.cb.c[threadIdx.x];
     }
     asm volatile("cp.async.commit_group;\n" ::);  // group: B fragments
-    float sg[32];
+    // RHT signs of this thread's coordinates 32c .. 32c+31 as one mask (bit j
+    // set: coordinate 32c + j is negated), applied by flipping float sign bits
+    uint32_t sgm = 0u;
     if constexpr (RHT) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) sg[j] = p.sgn[32 * c + j];
+        for (int j = 0; j < 32; ++j) sgm |= (p.sgn[32 * c + j] < 0.0f ? 1u : 0u) << j;
     }
 
     const int64_t ntiles = (p.n + 15) / 16;
@@ -212,7 +210,8 @@ __global__ void __launch_bounds__(kQmWarps * 32) quantize_mma_kernel(const __gri
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
-                for (int j = 0; j < 32; ++j) y[rr][j] *= sg[j];
+                for (int j = 0; j < 32; ++j)
+                    y[rr][j] = __int_as_float(__float_as_int(y[rr][j]) ^ (int)((sgm << (31 - j)) & 0x80000000u));
 #pragma unroll
             for (int h = 1; h < 32; h <<= 1)
 #pragma unroll
@@ -242,61 +241,69 @@ __global__ void __launch_bounds__(kQmWarps * 32) quantize_mma_kernel(const __gri
                 for (int j = 0; j < 32; ++j) y[rr][j] *= sc;
             }
         } else {
-            // X limbs -> bf16 operand tiles, from this thread's own coordinates
+            // two passes of 8 n-tiles (output coordinates 32c + 0..15, then
+            // 32c + 16..31) keep the live accumulators at 32 registers; the
+            // first pass's results wait in `first` while y still feeds pass 2
+            float first[8][4];
 #pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                uint32_t* t0 = at + (g + 8 * rr) * kQmRowWords + 16 * c;
+            for (int half = 0; half < 2; ++half) {
+                float acc[8][4];
 #pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    const uint32_t h1 = pack_bf16(y[rr][j], y[rr][j + 1]);
-                    t0[j >> 1] = h1;
-                    if constexpr (NLX == 3) {
-                        const float r0 = y[rr][j] - bf16_lo(h1), r1 = y[rr][j + 1] - bf16_hi(h1);
-                        const uint32_t h2 = pack_bf16(r0, r1);
-                        t0[16 * kQmRowWords + (j >> 1)] = h2;
-                        t0[32 * kQmRowWords + (j >> 1)] = pack_bf16(r0 - bf16_lo(h2), r1 - bf16_hi(h2));
+                for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    // A fragments from this thread's own coordinates 32c + 4kk .. +3
+                    // of rows g (slots 0, 2) and g + 8 (slots 1, 3), as bf16 limbs
+                    uint32_t a[NLX][4];
+#pragma unroll
+                    for (int sl = 0; sl < 4; ++sl) {
+                        const float v0 = y[sl & 1][4 * kk + (sl & 2)], v1 = y[sl & 1][4 * kk + (sl & 2) + 1];
+                        const uint32_t h1 = pack_bf16(v0, v1);
+                        a[0][sl] = h1;
+                        if constexpr (NLX == 3) {
+                            const float r0 = v0 - bf16_lo(h1), r1 = v1 - bf16_hi(h1);
+                            const uint32_t h2 = pack_bf16(r0, r1);
+                            a[1][sl] = h2;
+                            a[2][sl] = pack_bf16(r0 - bf16_lo(h2), r1 - bf16_hi(h2));
+                        }
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < 8; ++nt) {
+                        const int ng = 8 * half + nt;
+                        const uint2 f1 = b1[((0 * 8 + kk) * 16 + ng) * 32 + lane];
+                        const uint2 f2 = b1[((1 * 8 + kk) * 16 + ng) * 32 + lane];
+                        const uint2 f3 = b1[((2 * 8 + kk) * 16 + ng) * 32 + lane];
+                        mma16816_bf16(acc[nt], a[0][0], a[0][1], a[0][2], a[0][3], f1.x, f1.y);
+                        mma16816_bf16(acc[nt], a[0][0], a[0][1], a[0][2], a[0][3], f2.x, f2.y);
+                        mma16816_bf16(acc[nt], a[0][0], a[0][1], a[0][2], a[0][3], f3.x, f3.y);
+                        if constexpr (NLX == 3) {
+                            mma16816_bf16(acc[nt], a[1][0], a[1][1], a[1][2], a[1][3], f1.x, f1.y);
+                            mma16816_bf16(acc[nt], a[1][0], a[1][1], a[1][2], a[1][3], f2.x, f2.y);
+                            mma16816_bf16(acc[nt], a[2][0], a[2][1], a[2][2], a[2][3], f1.x, f1.y);
+                        }
                     }
                 }
-            }
-            __syncwarp();
-            float acc[16][4];
+                if (half == 0) {
 #pragma unroll
-            for (int nt = 0; nt < 16; ++nt)
+                    for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
-#pragma unroll 1
-            for (int kk = 0; kk < 8; ++kk) {
-                uint32_t a[NLX][4];
+                        for (int e = 0; e < 4; ++e) first[nt][e] = acc[nt][e];
+                } else {
+                    // accumulator (row g / g+8, column 2c+e of n-tile nt) = coordinate 32c + 2nt + e
 #pragma unroll
-                for (int l = 0; l < NLX; ++l) {
-                    const uint32_t* t = at + l * 16 * kQmRowWords;
-                    a[l][0] = t[g * kQmRowWords + 8 * kk + c];
-                    a[l][1] = t[(g + 8) * kQmRowWords + 8 * kk + c];
-                    a[l][2] = t[g * kQmRowWords + 8 * kk + 4 + c];
-                    a[l][3] = t[(g + 8) * kQmRowWords + 8 * kk + 4 + c];
-                }
-#pragma unroll
-                for (int nt = 0; nt < 16; ++nt) {
-                    const uint2 f1 = b1[((0 * 8 + kk) * 16 + nt) * 32 + lane];
-                    const uint2 f2 = b1[((1 * 8 + kk) * 16 + nt) * 32 + lane];
-                    const uint2 f3 = b1[((2 * 8 + kk) * 16 + nt) * 32 + lane];
-                    mma16816_bf16(acc[nt], a[0][0], a[0][1], a[0][2], a[0][3], f1.x, f1.y);
-                    mma16816_bf16(acc[nt], a[0][0], a[0][1], a[0][2], a[0][3], f2.x, f2.y);
-                    mma16816_bf16(acc[nt], a[0][0], a[0][1], a[0][2], a[0][3], f3.x, f3.y);
-                    if constexpr (NLX == 3) {
-                        mma16816_bf16(acc[nt], a[1][0], a[1][1], a[1][2], a[1][3], f1.x, f1.y);
-                        mma16816_bf16(acc[nt], a[1][0], a[1][1], a[1][2], a[1][3], f2.x, f2.y);
-                        mma16816_bf16(acc[nt], a[2][0], a[2][1], a[2][2], a[2][3], f1.x, f1.y);
+                    for (int nt = 0; nt < 8; ++nt) {
+                        y[0][2 * nt] = first[nt][0] * inv_n[0];
+                        y[0][2 * nt + 1] = first[nt][1] * inv_n[0];
+                        y[1][2 * nt] = first[nt][2] * inv_n[1];
+                        y[1][2 * nt + 1] = first[nt][3] * inv_n[1];
+                        y[0][16 + 2 * nt] = acc[nt][0] * inv_n[0];
+                        y[0][16 + 2 * nt + 1] = acc[nt][1] * inv_n[0];
+                        y[1][16 + 2 * nt] = acc[nt][2] * inv_n[1];
+                        y[1][16 + 2 * nt + 1] = acc[nt][3] * inv_n[1];
                     }
                 }
-            }
-            // accumulator (row g / g+8, column 2c+e of n-tile nt) = coordinate 32c + 2nt + e
-#pragma unroll
-            for (int nt = 0; nt < 16; ++nt) {
-                y[0][2 * nt] = acc[nt][0] * inv_n[0];
-                y[0][2 * nt + 1] = acc[nt][1] * inv_n[0];
-                y[1][2 * nt] = acc[nt][2] * inv_n[1];
-                y[1][2 * nt + 1] = acc[nt][3] * inv_n[1];
             }
         }
 
@@ -460,56 +467,57 @@ __global__ void __launch_bounds__(kQmWarps * 32) quantize_mma_kernel(const __gri
         }
 
         if constexpr (PROD) {
-            // gamma and R as bf16 hi/lo tiles for the S r GEMM (y holds r)
+            // gamma = ||r|| (y holds r); the S r GEMM takes R as bf16 hi/lo A
+            // fragments straight from this thread's coordinates
             float gam[2];
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
                 float g2 = 0.0f;
-                uint32_t* th = at + (g + 8 * rr) * kQmRowWords + 16 * c;
-                uint32_t* tl = th + 16 * kQmRowWords;
 #pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    const float r0 = y[rr][j], r1 = y[rr][j + 1];
-                    g2 = fmaf(r0, r0, fmaf(r1, r1, g2));
-                    const uint32_t h = pack_bf16(r0, r1);
-                    th[j >> 1] = h;
-                    tl[j >> 1] = pack_bf16(r0 - bf16_lo(h), r1 - bf16_hi(h));
-                }
+                for (int j = 0; j < 32; ++j) g2 = fmaf(y[rr][j], y[rr][j], g2);
                 g2 += __shfl_xor_sync(TQ_FULL_MASK, g2, 1);
                 g2 += __shfl_xor_sync(TQ_FULL_MASK, g2, 2);
                 gam[rr] = sqrtf(g2);
             }
-            __syncwarp();
-            float z[16][4];
+            // R as bf16 hi/lo A fragments for all 8 k-steps (64 registers; y is
+            // dead afterwards), then two passes of 8 n-tiles (16 sign bits
+            // each) so that only 32 accumulators are live at a time
+            uint32_t fr[8][2][4];
 #pragma unroll
-            for (int nt = 0; nt < 16; ++nt)
+            for (int kk = 0; kk < 8; ++kk)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) z[nt][e] = 0.0f;
-#pragma unroll 1
-            for (int kk = 0; kk < 8; ++kk) {
-                uint32_t a[2][4];
-#pragma unroll
-                for (int l = 0; l < 2; ++l) {
-                    const uint32_t* t = at + l * 16 * kQmRowWords;
-                    a[l][0] = t[g * kQmRowWords + 8 * kk + c];
-                    a[l][1] = t[(g + 8) * kQmRowWords + 8 * kk + c];
-                    a[l][2] = t[g * kQmRowWords + 8 * kk + 4 + c];
-                    a[l][3] = t[(g + 8) * kQmRowWords + 8 * kk + 4 + c];
+                for (int sl = 0; sl < 4; ++sl) {
+                    const float v0 = y[sl & 1][4 * kk + (sl & 2)], v1 = y[sl & 1][4 * kk + (sl & 2) + 1];
+                    const uint32_t h = pack_bf16(v0, v1);
+                    fr[kk][0][sl] = h;
+                    fr[kk][1][sl] = pack_bf16(v0 - bf16_lo(h), v1 - bf16_hi(h));
                 }
-#pragma unroll
-                for (int nt = 0; nt < 16; ++nt) {
-                    const uint2 f = b2[(kk * 16 + nt) * 32 + lane];
-                    mma16816_bf16(z[nt], a[0][0], a[0][1], a[0][2], a[0][3], f.x, f.y);
-                    mma16816_bf16(z[nt], a[1][0], a[1][1], a[1][2], a[1][3], f.x, f.y);
-                }
-            }
             uint32_t sw[2] = {0u, 0u};
 #pragma unroll
-            for (int nt = 0; nt < 16; ++nt) {
-                sw[0] |= (z[nt][0] >= 0.0f ? 1u : 0u) << (2 * nt);
-                sw[0] |= (z[nt][1] >= 0.0f ? 1u : 0u) << (2 * nt + 1);
-                sw[1] |= (z[nt][2] >= 0.0f ? 1u : 0u) << (2 * nt);
-                sw[1] |= (z[nt][3] >= 0.0f ? 1u : 0u) << (2 * nt + 1);
+            for (int half = 0; half < 2; ++half) {
+                float z[8][4];
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) z[nt][e] = 0.0f;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+                    for (int nt = 0; nt < 8; ++nt) {
+                        const uint2 f = b2[(kk * 16 + 8 * half + nt) * 32 + lane];
+                        mma16816_bf16(z[nt], fr[kk][0][0], fr[kk][0][1], fr[kk][0][2], fr[kk][0][3], f.x, f.y);
+                        mma16816_bf16(z[nt], fr[kk][1][0], fr[kk][1][1], fr[kk][1][2], fr[kk][1][3], f.x, f.y);
+                    }
+                }
+                // accumulator (row g / g+8, column 2c+e of n-tile nt) = sign bit 2nt + e of the thread's word
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt) {
+                    const int bit = 2 * (8 * half + nt);
+                    sw[0] |= (z[nt][0] >= 0.0f ? 1u : 0u) << bit;
+                    sw[0] |= (z[nt][1] >= 0.0f ? 1u : 0u) << (bit + 1);
+                    sw[1] |= (z[nt][2] >= 0.0f ? 1u : 0u) << bit;
+                    sw[1] |= (z[nt][3] >= 0.0f ? 1u : 0u) << (bit + 1);
+                }
             }
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
@@ -527,7 +535,7 @@ template <typename XT, int CB, bool PROD, bool RHT>
 constexpr size_t quantize_mma_smem() {
     constexpr int NLX = (!RHT && sizeof(XT) == 4) ? 3 : 1;
     return (RHT ? 0 : 3 * 8 * 16 * 32 * 8) + (PROD ? 8 * 16 * 32 * 8 : 0) +
-           (size_t)qm_warps<XT, RHT>() * QmSmem<XT, NLX>::WARP_BYTES;
+           (size_t)qm_warps<XT, RHT>() * QmSmem<XT>::WARP_BYTES;
 }
 
 }  // namespace tqk
