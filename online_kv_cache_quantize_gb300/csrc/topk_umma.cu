@@ -101,26 +101,24 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
         v.w = ((uint32_t)((i >> 6) & 1) << 15) | ((uint32_t)((i >> 7) & 1) << 31);
         reinterpret_cast<uint4*>(smem + Lo.sgn)[i] = v;
     }
-    for (int i = tid; i < 8 * 16 * k; i += blockDim.x) {
-        s_ls[i] = -INFINITY;
-        s_li[i] = 0x7fffffff;
-    }
-    for (int e = tid; e < kTuN * (kcb / 2); e += blockDim.x) {
-        const int n = e / (kcb / 2), col = (e % (kcb / 2)) * 2;
-        const int j = n >> 1, hl = n & 1, seg = col / ks, i = col % ks;
-        float v0 = 0.0f, v1 = 0.0f;
-        if (j < nq_here) {
-            if (seg == 0) {
-                const float* qp = p.qprime + (int64_t)(q0 + j) * d;
-                if (i < d) v0 = qp[i];
-                if (i + 1 < d) v1 = qp[i + 1];
-            } else {
-                const float* up = p.u + (int64_t)(q0 + j) * m;
-                if (i < m) v0 = lam_kappa * up[i];
-                if (i + 1 < m) v1 = lam_kappa * up[i + 1];
-            }
+    // B tile: row 2j + s holds query j's hi (s = 0) or lo (s = 1) fp16 half;
+    // columns [0, ks) are q', [ks, 2 ks) lam * kappa * u (PROD)
+    for (int j = 0; j < kTuQ; ++j) {
+        const bool qv = j < nq_here;
+        const float* qp = p.qprime + (int64_t)(q0 + (qv ? j : 0)) * d;
+        const float* up = PROD ? p.u + (int64_t)(q0 + (qv ? j : 0)) * m : nullptr;
+        for (int col = 2 * tid; col < kcb; col += 2 * blockDim.x) {
+            const bool sgn = col >= ks;
+            const int i = sgn ? col - ks : col;
+            const int lim = sgn ? m : d;
+            const float* src = sgn ? up : qp;
+            const float sc_ = sgn ? lam_kappa : 1.0f;
+            const float v0 = (qv && i < lim) ? sc_ * src[i] : 0.0f;
+            const float v1 = (qv && i + 1 < lim) ? sc_ * src[i + 1] : 0.0f;
+            *reinterpret_cast<uint32_t*>(sB + umma_off(2 * j, col, kcb)) = half_split(v0, 0) | (half_split(v1, 0) << 16);
+            *reinterpret_cast<uint32_t*>(sB + umma_off(2 * j + 1, col, kcb)) =
+                half_split(v0, 1) | (half_split(v1, 1) << 16);
         }
-        *reinterpret_cast<uint32_t*>(sB + umma_off(n, col, kcb)) = half_split(v0, hl) | (half_split(v1, hl) << 16);
     }
     const uint32_t bar[2] = {(uint32_t)__cvta_generic_to_shared(&s_bar[0]), (uint32_t)__cvta_generic_to_shared(&s_bar[1])};
     const uint32_t sbar[2] = {(uint32_t)__cvta_generic_to_shared(&s_sbar[0]),
@@ -166,6 +164,15 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
     const int ecol = 32 * (warp >> 2);      // ... and its 32 columns (16 queries)
     int step = 0;
     bool ok = true;
+    // this warp's top-k list of each of its 16 queries, spread over the lanes:
+    // lane e holds entry e (best first; lanes >= k hold nothing)
+    float lsc[16];
+    int lid[16];
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) {
+        lsc[jj] = -INFINITY;
+        lid[jj] = 0x7fffffff;
+    }
 
     for (int64_t t = 0; t < ntile && ok; ++t) {
         const int64_t t0 = r0 + t * kTuRows;
@@ -245,23 +252,33 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
         const bool evalid = erow < r1;
         const float scale = evalid ? f16_bits_to_f32(p.norm[erow]) * p.inv_lam : 0.0f;
         const int id = (int)erow;
-        float* wls = s_ls + warp * 16 * k;
-        int* wli = s_li + warp * 16 * k;
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
             const int j = (ecol >> 1) + jj;
             if (j < nq_here) {  // warp-uniform
                 const float sc = scale * (v[2 * jj] + v[2 * jj + 1]);
-                float* ls = wls + jj * k;
-                int* li = wli + jj * k;
-                unsigned cand = __ballot_sync(TQ_FULL_MASK, evalid && better(sc, id, ls[k - 1], li[k - 1]));
+                float ts = __shfl_sync(TQ_FULL_MASK, lsc[jj], k - 1);
+                int ti = __shfl_sync(TQ_FULL_MASK, lid[jj], k - 1);
+                unsigned cand = __ballot_sync(TQ_FULL_MASK, evalid && better(sc, id, ts, ti));
                 while (cand) {
                     const int src = __ffs(cand) - 1;
                     cand &= cand - 1;
                     const float cs_ = __shfl_sync(TQ_FULL_MASK, sc, src);
                     const int ci = __shfl_sync(TQ_FULL_MASK, id, src);
-                    if (lane == 0) list_insert(ls, li, k, cs_, ci);
-                    __syncwarp();
+                    if (!better(cs_, ci, ts, ti)) continue;  // the list moved on since the ballot
+                    // entries better than the candidate stay, the rest move one lane down
+                    const int pos = __popc(__ballot_sync(TQ_FULL_MASK, lane < k && better(lsc[jj], lid[jj], cs_, ci)));
+                    const float us = __shfl_up_sync(TQ_FULL_MASK, lsc[jj], 1);
+                    const int ui = __shfl_up_sync(TQ_FULL_MASK, lid[jj], 1);
+                    if (lane == pos) {
+                        lsc[jj] = cs_;
+                        lid[jj] = ci;
+                    } else if (lane > pos) {
+                        lsc[jj] = us;
+                        lid[jj] = ui;
+                    }
+                    ts = __shfl_sync(TQ_FULL_MASK, lsc[jj], k - 1);
+                    ti = __shfl_sync(TQ_FULL_MASK, lid[jj], k - 1);
                 }
             }
         }
@@ -283,6 +300,17 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
     if (warp == 0) tmem_dealloc(tmem, kTuN);
 
     // ---- merge the four warp lists of each query, write the chunk's candidates ----
+    {
+        float* wls = s_ls + warp * 16 * k;
+        int* wli = s_li + warp * 16 * k;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj)
+            if (lane < k) {
+                wls[jj * k + lane] = lsc[jj];
+                wli[jj * k + lane] = lid[jj];
+            }
+    }
+    __syncthreads();
     if (tid < nq_here) {
         const int j = tid;
         const int base_w = 4 * (j >> 4), jj = j & 15;
