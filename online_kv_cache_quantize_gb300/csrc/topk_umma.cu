@@ -34,7 +34,7 @@ constexpr int kTuThreads = 256;
 constexpr int kTuSmemLimit = 227 * 1024 - 4096;  // dynamic part; static tables stay below 4 KB
 
 struct TuLayout {
-    size_t b, a0, a1, st0, st1, sgn, ls, li, total;
+    size_t b, a0, a1, st0, st1, sgn, nrm, ls, li, total;
     int kcb, stage_bytes;
 };
 
@@ -50,7 +50,8 @@ __host__ __device__ inline TuLayout tu_layout(int ks, int nseg_b, int code_strid
     L.st0 = L.a1 + ab;
     L.st1 = L.st0 + ((L.stage_bytes + 127) / 128) * 128;
     L.sgn = L.st1 + ((L.stage_bytes + 127) / 128) * 128;
-    L.ls = L.sgn + 256 * 16;
+    L.nrm = L.sgn + 256 * 16;  // [2 buffers][128 rows] norm, then [2][128] gamma (fp32)
+    L.ls = L.nrm + 4 * kTuRows * 4;
     L.li = L.ls + (size_t)8 * 16 * k * 4;
     L.total = L.li + (size_t)8 * 16 * k * 4;
     return L;
@@ -77,6 +78,8 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
     unsigned char* sA[2] = {smem + Lo.a0, smem + Lo.a1};
     unsigned char* sSt[2] = {smem + Lo.st0, smem + Lo.st1};
     const uint4* s_sgn = reinterpret_cast<const uint4*>(smem + Lo.sgn);
+    float* s_nrm = reinterpret_cast<float*>(smem + Lo.nrm);          // [2][128]: n of each row
+    float* s_gam = s_nrm + 2 * kTuRows;                              // [2][128]: gamma (PROD)
     float* s_ls = reinterpret_cast<float*>(smem + Lo.ls);  // [8 warps][16 queries][k]
     int* s_li = reinterpret_cast<int*>(smem + Lo.li);
 
@@ -157,9 +160,11 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
     const uint32_t idesc = umma_idesc_f16(kTuRows, kTuN);
     const uint32_t sB_a = (uint32_t)__cvta_generic_to_shared(sB);
     const uint32_t sA_a[2] = {(uint32_t)__cvta_generic_to_shared(sA[0]), (uint32_t)__cvta_generic_to_shared(sA[1])};
-    const int r = tid & (kTuRows - 1);      // de-quantize: this thread's row in the tile
-    const int half = tid >> 7;              // ... and half of the 8-coordinate units
-    const int units = ks / 8, u0 = half * (units / 2), u1 = u0 + units / 2;
+    // de-quantize: a warp covers 8 consecutive rows (lane & 7) x 4 units of 8
+    // coordinates (lane >> 3) per pass, so the 16-byte stores of a quarter warp
+    // fill all banks and the staged code rows are read with at most 2-way conflicts
+    const int units = ks / 8, nuq = (units + 3) / 4;
+    const int dr = lane & 7, du = lane >> 3;
     const int er = 32 * (warp & 3) + lane;  // epilogue: this thread's row (TMEM lane)
     const int ecol = 32 * (warp >> 2);      // ... and its 32 columns (16 queries)
     int step = 0;
@@ -174,20 +179,32 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
         lid[jj] = 0x7fffffff;
     }
 
+    // norms of a tile's rows: threads 0..127 load tile t + 1's into registers
+    // during tile t and publish them into the other smem buffer at its end
+    auto load_norms = [&](int64_t t, uint16_t& nv, uint16_t& gv) {
+        const int64_t row = r0 + t * kTuRows + tid;
+        nv = gv = 0;
+        if (tid < kTuRows && t < ntile && row < r1) {
+            nv = p.norm[row];
+            if constexpr (PROD) gv = p.rnorm[row];
+        }
+    };
+    uint16_t nxt_n = 0, nxt_g = 0;
+    load_norms(0, nxt_n, nxt_g);
+    if (tid < kTuRows) {
+        s_nrm[tid] = f16_bits_to_f32(nxt_n);
+        s_gam[tid] = __uint_as_float((uint32_t)nxt_g);  // raw fp16 bits of gamma, carried in a float slot
+    }
+
     for (int64_t t = 0; t < ntile && ok; ++t) {
         const int64_t t0 = r0 + t * kTuRows;
         const int sb = (int)(t & 1);
         if (tid == 0 && t + 1 < ntile) stage(t + 1);  // its buffer was last read in tile t - 1
+        load_norms(t + 1, nxt_n, nxt_g);
         ok = !__syncthreads_or(!mbar_wait_bounded(sbar[sb], (uint32_t)((t >> 1) & 1), kWaitLimitNs, p.err, kErrScanWait));
         if (!ok) break;
-        const unsigned char* crow = sSt[sb] + r * cs;
-        const unsigned char* srow = sSt[sb] + kTuRows * cs + r * ss;
-        const bool rvalid = t0 + r < r1;
-        uint32_t g2 = 0u;
-        if constexpr (PROD) {
-            const uint32_t g16 = rvalid ? (uint32_t)p.rnorm[t0 + r] : 0u;
-            g2 = (g16 | 0x8000u) | ((g16 | 0x8000u) << 16);  // (-gamma, -gamma)
-        }
+        const float* t_nrm = s_nrm + sb * kTuRows;
+        const float* t_gam = s_gam + sb * kTuRows;
         for (int seg = 0; seg < NSEG_A; ++seg) {
             const int buf = step & 1;
             if (step >= 2) {
@@ -197,16 +214,30 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
             }
             const bool sign_seg = PROD && seg == NSEG_A - 1;
             unsigned char* dstA = sA[buf];
-            for (int u = u0; u < u1; ++u) {
+            for (int cmb = warp; cmb < 16 * nuq; cmb += kTuThreads / 32) {
+                const int r = 8 * (cmb & 15) + dr, u = 4 * (cmb >> 4) + du;
+                if (u >= units) continue;
+                const bool rvalid = t0 + r < r1;
                 uint4 w;
                 if (sign_seg) {
-                    const uint4 f = s_sgn[rvalid ? srow[u] : 0];
+                    const uint32_t g16 = __float_as_uint(t_gam[r]);
+                    const uint32_t g2 = (g16 | 0x8000u) | ((g16 | 0x8000u) << 16);  // (-gamma, -gamma)
+                    const uint4 f = s_sgn[rvalid ? sSt[sb][kTuRows * cs + r * ss + u] : 0];
                     w = make_uint4(g2 ^ f.x, g2 ^ f.y, g2 ^ f.z, g2 ^ f.w);
                 } else {
                     // 8 codes: CB bytes starting at byte CB * u of the row
-                    const int o = CB * u;
-                    const uint32_t* wp = reinterpret_cast<const uint32_t*>(crow + (o & ~3));
-                    const uint32_t bits = rvalid ? __funnelshift_r(wp[0], wp[1], 8 * (o & 3)) : 0u;
+                    const unsigned char* crow = sSt[sb] + r * cs;
+                    uint32_t bits = 0u;
+                    if (rvalid) {
+                        if constexpr (CB == 1) bits = crow[u];
+                        else if constexpr (CB == 2) bits = *reinterpret_cast<const uint16_t*>(crow + 2 * u);
+                        else if constexpr (CB == 4) bits = *reinterpret_cast<const uint32_t*>(crow + 4 * u);
+                        else {
+                            const int o = CB * u;
+                            const uint32_t* wp = reinterpret_cast<const uint32_t*>(crow + (o & ~3));
+                            bits = __funnelshift_r(wp[0], wp[1], 8 * (o & 3));
+                        }
+                    }
                     const uint32_t* tab = (LO && seg == 1) ? s_klo : s_ktab;
                     constexpr uint32_t M2 = (1u << (2 * CB)) - 1u;
                     w.x = tab[bits & M2];
@@ -250,7 +281,7 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
         }
         const int64_t erow = t0 + er;
         const bool evalid = erow < r1;
-        const float scale = evalid ? f16_bits_to_f32(p.norm[erow]) * p.inv_lam : 0.0f;
+        const float scale = t_nrm[er] * p.inv_lam;
         const int id = (int)erow;
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
@@ -281,6 +312,10 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
                     ti = __shfl_sync(TQ_FULL_MASK, lid[jj], k - 1);
                 }
             }
+        }
+        if (tid < kTuRows) {  // the next tile's norms into the other buffer
+            s_nrm[(sb ^ 1) * kTuRows + tid] = f16_bits_to_f32(nxt_n);
+            s_gam[(sb ^ 1) * kTuRows + tid] = __uint_as_float((uint32_t)nxt_g);
         }
         tc_fence_before_sync();
         __syncthreads();  // D is overwritten by the next tile's first MMA
