@@ -258,6 +258,8 @@ struct StepStreams {
 std::mutex g_step_mutex;
 StepStreams g_step[kMaxStepDevices];
 
+constexpr int64_t kSmallAppend = 64;  // vectors; at most this many take the warp-per-vector kernel
+
 struct QuantLaunch {
     tqk::QuantParams p;
     int dtype = 0, vpl = 1, cb = 1;
@@ -340,10 +342,12 @@ tq_status quant_prepare(const tq_quant_args* a, QuantLaunch* L, bool* empty) {
     L->cb = cb;
     p.pi_frag = a->rot->d_pi_frag;
     p.s_frag = prod ? a->qjl->d_s_frag : nullptr;
-    // d = m = 128 with 16-byte aligned rows: the tensor-core kernel; otherwise
-    // the warp-per-vector kernel (any d <= 256)
-    L->mma = c.d == 128 && (!prod || (c.m == 128 && p.s_frag)) && (rht || p.pi_frag) && aligned(a->x, 16) &&
-             (a->x_stride * (int64_t)esz) % 16 == 0;
+    // d = m = 128 with 16-byte aligned rows and more than a few tiles: the
+    // tensor-core kernel; otherwise the warp-per-vector kernel (any d <= 256),
+    // which spreads a small append (one token per KV head) over one warp per
+    // vector instead of running it as one mostly empty 16-row tile on one warp
+    L->mma = c.d == 128 && a->n > kSmallAppend && (!prod || (c.m == 128 && p.s_frag)) && (rht || p.pi_frag) &&
+             aligned(a->x, 16) && (a->x_stride * (int64_t)esz) % 16 == 0;
     return TQ_OK;
 }
 

@@ -181,6 +181,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
     __shared__ float s_m[kCombineThreads];
     __shared__ float s_z[kCombineThreads];
     __shared__ float s_v[kCombineThreads];
+    // launched as a programmatic dependent of the scan: wait for its grid to
+    // complete and its partials to be visible (a no-op on a plain launch)
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     __shared__ float s_a[256];
     const int row = blockIdx.x, tid = threadIdx.x, d = p.d, ns = p.n_splits;
     const int groups = kCombineThreads / d;

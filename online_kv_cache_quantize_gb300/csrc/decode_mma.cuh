@@ -385,6 +385,9 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
     }
     __syncthreads();
 
+    // the merge kernel may be scheduled now; it waits for this grid to finish
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+
     // ---- merge the warps of the CTA and write this split's partials ----
     float* s_acc = reinterpret_cast<float*>(smem);  // [warps][G][D]
     float* s_mz = s_acc + kMmaWarps * G * D;        // [warps][G][2]

@@ -160,11 +160,9 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
     const uint32_t idesc = umma_idesc_f16(kTuRows, kTuN);
     const uint32_t sB_a = (uint32_t)__cvta_generic_to_shared(sB);
     const uint32_t sA_a[2] = {(uint32_t)__cvta_generic_to_shared(sA[0]), (uint32_t)__cvta_generic_to_shared(sA[1])};
-    // de-quantize: a warp covers 8 consecutive rows (lane & 7) x 4 units of 8
-    // coordinates (lane >> 3) per pass, so the 16-byte stores of a quarter warp
-    // fill all banks and the staged code rows are read with at most 2-way conflicts
-    const int units = ks / 8, nuq = (units + 3) / 4;
-    const int dr = lane & 7, du = lane >> 3;
+    const int r = tid & (kTuRows - 1);      // de-quantize: this thread's row in the tile
+    const int half = tid >> 7;              // ... and half of the 8-coordinate units
+    const int units = ks / 8, u0 = half * (units / 2), u1 = u0 + units / 2;
     const int er = 32 * (warp & 3) + lane;  // epilogue: this thread's row (TMEM lane)
     const int ecol = 32 * (warp >> 2);      // ... and its 32 columns (16 queries)
     int step = 0;
@@ -214,19 +212,21 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
             }
             const bool sign_seg = PROD && seg == NSEG_A - 1;
             unsigned char* dstA = sA[buf];
-            for (int cmb = warp; cmb < 16 * nuq; cmb += kTuThreads / 32) {
-                const int r = 8 * (cmb & 15) + dr, u = 4 * (cmb >> 4) + du;
-                if (u >= units) continue;
-                const bool rvalid = t0 + r < r1;
+            const bool rvalid = t0 + r < r1;
+            const unsigned char* crow = sSt[sb] + r * cs;
+            const unsigned char* srow = sSt[sb] + kTuRows * cs + r * ss;
+            uint32_t g2 = 0u;
+            if (sign_seg) {
+                const uint32_t g16 = __float_as_uint(t_gam[r]);
+                g2 = (g16 | 0x8000u) | ((g16 | 0x8000u) << 16);  // (-gamma, -gamma)
+            }
+            for (int u = u0; u < u1; ++u) {
                 uint4 w;
                 if (sign_seg) {
-                    const uint32_t g16 = __float_as_uint(t_gam[r]);
-                    const uint32_t g2 = (g16 | 0x8000u) | ((g16 | 0x8000u) << 16);  // (-gamma, -gamma)
-                    const uint4 f = s_sgn[rvalid ? sSt[sb][kTuRows * cs + r * ss + u] : 0];
+                    const uint4 f = s_sgn[rvalid ? srow[u] : 0];
                     w = make_uint4(g2 ^ f.x, g2 ^ f.y, g2 ^ f.z, g2 ^ f.w);
                 } else {
                     // 8 codes: CB bytes starting at byte CB * u of the row
-                    const unsigned char* crow = sSt[sb] + r * cs;
                     uint32_t bits = 0u;
                     if (rvalid) {
                         if constexpr (CB == 1) bits = crow[u];

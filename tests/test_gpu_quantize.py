@@ -112,7 +112,7 @@ def test_fp16_norm_midpoints(kind, mode, bits):
     assert rep["code_mismatch"] == 0
 
 
-@pytest.mark.parametrize("n", [1, 2, 31, 33])
+@pytest.mark.parametrize("n", [1, 2, 31, 33, 64, 65, 100])
 def test_ragged_counts(n):
     x = np.random.default_rng(n).standard_normal((n, 128)).astype(np.float32)
     _run(x, "prod", 4, 128, "rht", torch.float32, f"n{n}")
