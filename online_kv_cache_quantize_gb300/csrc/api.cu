@@ -258,7 +258,7 @@ struct StepStreams {
 std::mutex g_step_mutex;
 StepStreams g_step[kMaxStepDevices];
 
-constexpr int64_t kSmallAppend = 64;  // vectors; at most this many take the warp-per-vector kernel
+constexpr int64_t kSmallAppend = 64;  // MSE appends of at most this many vectors: warp-per-vector kernel
 
 struct QuantLaunch {
     tqk::QuantParams p;
@@ -342,11 +342,14 @@ tq_status quant_prepare(const tq_quant_args* a, QuantLaunch* L, bool* empty) {
     L->cb = cb;
     p.pi_frag = a->rot->d_pi_frag;
     p.s_frag = prod ? a->qjl->d_s_frag : nullptr;
-    // d = m = 128 with 16-byte aligned rows and more than a few tiles: the
-    // tensor-core kernel; otherwise the warp-per-vector kernel (any d <= 256),
-    // which spreads a small append (one token per KV head) over one warp per
-    // vector instead of running it as one mostly empty 16-row tile on one warp
-    L->mma = c.d == 128 && a->n > kSmallAppend && (!prod || (c.m == 128 && p.s_frag)) && (rht || p.pi_frag) &&
+    // d = m = 128 with 16-byte aligned rows: the tensor-core kernel; otherwise
+    // the warp-per-vector kernel (any d <= 256). A small MSE append (one token
+    // per KV head) also takes the warp-per-vector kernel, one warp per vector
+    // instead of one mostly empty 16-row tile on one warp; keys keep the
+    // tensor-core kernel, whose S r product the warp-per-vector kernel would
+    // do as a mat-vec over all of S per warp.
+    const bool small_mse = !prod && a->n <= kSmallAppend;
+    L->mma = c.d == 128 && !small_mse && (!prod || (c.m == 128 && p.s_frag)) && (rht || p.pi_frag) &&
              aligned(a->x, 16) && (a->x_stride * (int64_t)esz) % 16 == 0;
     return TQ_OK;
 }

@@ -90,6 +90,14 @@ __device__ __forceinline__ uint32_t field4(const uint32_t* w, int off, int n) {
     return (__funnelshift_r(w[W], w[W + 1], S) << 2) & mask;
 }
 
+// 2^x with the hardware approximation (a few ulp in fp32; -inf gives +0):
+// the softmax weights only, never the logits
+__device__ __forceinline__ float ex2(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(r) : "f"(x));
+    return r;
+}
+
 template <typename T>
 __device__ __forceinline__ T lds_at(const void* base, uint32_t byte_off) {
     return *reinterpret_cast<const T*>(reinterpret_cast<const unsigned char*>(base) + byte_off);
@@ -316,9 +324,9 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
             m = fmaxf(m, __shfl_xor_sync(TQ_FULL_MASK, m, 8));
             m = fmaxf(m, __shfl_xor_sync(TQ_FULL_MASK, m, 16));
             const float mn = fmaxf(M[nt], m);
-            const float corr = (mn == -INFINITY) ? 1.0f : exp2f(M[nt] - mn);
-            const float p0 = (s0 == -INFINITY) ? 0.0f : exp2f(s0 - mn);
-            const float p1 = (s1 == -INFINITY) ? 0.0f : exp2f(s1 - mn);
+            const float corr = (mn == -INFINITY) ? 1.0f : ex2(M[nt] - mn);
+            const float p0 = (s0 == -INFINITY) ? 0.0f : ex2(s0 - mn);
+            const float p1 = (s1 == -INFINITY) ? 0.0f : ex2(s1 - mn);
             Zp[nt] = fmaf(Zp[nt], corr, p0 + p1);
             M[nt] = mn;
             // the running max of a head rarely moves after the first tiles:
@@ -422,7 +430,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
 #pragma unroll
         for (int w = 0; w < kMmaWarps; ++w) {
             const float mw = s_mz[(w * G + h) * 2];
-            const float wt = (mw == -INFINITY) ? 0.0f : exp2f(mw - mstar);
+            const float wt = (mw == -INFINITY) ? 0.0f : ex2(mw - mstar);
             z = fmaf(s_mz[(w * G + h) * 2 + 1], wt, z);
             a = fmaf(s_acc[(w * G + h) * D + ci], wt, a);
         }
