@@ -30,7 +30,10 @@ namespace tqk {
 constexpr int kTuRows = 128;    // database rows per tile (MMA M)
 constexpr int kTuQ = 32;        // queries per CTA
 constexpr int kTuN = 2 * kTuQ;  // MMA N: hi and lo column per query
-constexpr int kTuThreads = 256;
+constexpr int kTuWarps = 16;
+constexpr int kTuThreads = 32 * kTuWarps;
+constexpr int kTuQpw = kTuQ / (kTuWarps / 4);  // queries per warp in the epilogue (8)
+constexpr int kTuParts = kTuThreads / kTuRows;  // threads per row in the de-quantize (4)
 constexpr int kTuSmemLimit = 227 * 1024 - 4096;  // dynamic part; static tables stay below 4 KB
 
 struct TuLayout {
@@ -52,8 +55,8 @@ __host__ __device__ inline TuLayout tu_layout(int ks, int nseg_b, int code_strid
     L.sgn = L.st1 + ((L.stage_bytes + 127) / 128) * 128;
     L.nrm = L.sgn + 256 * 16;  // [2 buffers][128 rows] norm, then [2][128] gamma (fp32)
     L.ls = L.nrm + 4 * kTuRows * 4;
-    L.li = L.ls + (size_t)8 * 16 * k * 4;
-    L.total = L.li + (size_t)8 * 16 * k * 4;
+    L.li = L.ls + (size_t)kTuWarps * kTuQpw * k * 4;
+    L.total = L.li + (size_t)kTuWarps * kTuQpw * k * 4;
     return L;
 }
 
@@ -80,7 +83,7 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
     const uint4* s_sgn = reinterpret_cast<const uint4*>(smem + Lo.sgn);
     float* s_nrm = reinterpret_cast<float*>(smem + Lo.nrm);          // [2][128]: n of each row
     float* s_gam = s_nrm + 2 * kTuRows;                              // [2][128]: gamma (PROD)
-    float* s_ls = reinterpret_cast<float*>(smem + Lo.ls);  // [8 warps][16 queries][k]
+    float* s_ls = reinterpret_cast<float*>(smem + Lo.ls);  // [warps][queries per warp][k]
     int* s_li = reinterpret_cast<int*>(smem + Lo.li);
 
     const int chunk = blockIdx.x;
@@ -161,18 +164,19 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
     const uint32_t sB_a = (uint32_t)__cvta_generic_to_shared(sB);
     const uint32_t sA_a[2] = {(uint32_t)__cvta_generic_to_shared(sA[0]), (uint32_t)__cvta_generic_to_shared(sA[1])};
     const int r = tid & (kTuRows - 1);      // de-quantize: this thread's row in the tile
-    const int half = tid >> 7;              // ... and half of the 8-coordinate units
-    const int units = ks / 8, u0 = half * (units / 2), u1 = u0 + units / 2;
+    const int part = tid >> 7;              // ... and its share of the 8-coordinate units
+    const int units = ks / 8, upp = (units + kTuParts - 1) / kTuParts;
+    const int u0 = part * upp, u1 = min(units, u0 + upp);
     const int er = 32 * (warp & 3) + lane;  // epilogue: this thread's row (TMEM lane)
-    const int ecol = 32 * (warp >> 2);      // ... and its 32 columns (16 queries)
+    const int ecol = 2 * kTuQpw * (warp >> 2);  // ... and its 2 * kTuQpw columns (kTuQpw queries)
     int step = 0;
     bool ok = true;
-    // this warp's top-k list of each of its 16 queries, spread over the lanes:
-    // lane e holds entry e (best first; lanes >= k hold nothing)
-    float lsc[16];
-    int lid[16];
+    // this warp's top-k list of each of its kTuQpw queries, spread over the
+    // lanes: lane e holds entry e (best first; lanes >= k hold nothing)
+    float lsc[kTuQpw];
+    int lid[kTuQpw];
 #pragma unroll
-    for (int jj = 0; jj < 16; ++jj) {
+    for (int jj = 0; jj < kTuQpw; ++jj) {
         lsc[jj] = -INFINITY;
         lid[jj] = 0x7fffffff;
     }
@@ -220,6 +224,7 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
                 const uint32_t g16 = __float_as_uint(t_gam[r]);
                 g2 = (g16 | 0x8000u) | ((g16 | 0x8000u) << 16);  // (-gamma, -gamma)
             }
+#pragma unroll 4
             for (int u = u0; u < u1; ++u) {
                 uint4 w;
                 if (sign_seg) {
@@ -266,25 +271,16 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
                                                   p.err, kErrScanWait));
         if (!ok) break;
         tc_fence_after_sync();
-        float v[32];
-        {
-            float a[16], b[16];
-            const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)ecol;
-            tmem_ld16(ta, a);
-            tmem_ld16(ta + 16, b);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                v[i] = a[i];
-                v[16 + i] = b[i];
-            }
-        }
+        float v[2 * kTuQpw];
+        static_assert(2 * kTuQpw == 16, "one 16-column TMEM load per warp");
+        tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)ecol, v);
+        tmem_ld_wait();
         const int64_t erow = t0 + er;
         const bool evalid = erow < r1;
         const float scale = t_nrm[er] * p.inv_lam;
         const int id = (int)erow;
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
+        for (int jj = 0; jj < kTuQpw; ++jj) {
             const int j = (ecol >> 1) + jj;
             if (j < nq_here) {  // warp-uniform
                 const float sc = scale * (v[2 * jj] + v[2 * jj + 1]);
@@ -336,10 +332,10 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
 
     // ---- merge the four warp lists of each query, write the chunk's candidates ----
     {
-        float* wls = s_ls + warp * 16 * k;
-        int* wli = s_li + warp * 16 * k;
+        float* wls = s_ls + warp * kTuQpw * k;
+        int* wli = s_li + warp * kTuQpw * k;
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj)
+        for (int jj = 0; jj < kTuQpw; ++jj)
             if (lane < k) {
                 wls[jj * k + lane] = lsc[jj];
                 wli[jj * k + lane] = lid[jj];
@@ -348,12 +344,12 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
     __syncthreads();
     if (tid < nq_here) {
         const int j = tid;
-        const int base_w = 4 * (j >> 4), jj = j & 15;
-        float* ls0 = s_ls + (base_w * 16 + jj) * k;
-        int* li0 = s_li + (base_w * 16 + jj) * k;
+        const int base_w = 4 * (j / kTuQpw), jj = j % kTuQpw;
+        float* ls0 = s_ls + (base_w * kTuQpw + jj) * k;
+        int* li0 = s_li + (base_w * kTuQpw + jj) * k;
         for (int w4 = 1; w4 < 4; ++w4) {
-            const float* ls = s_ls + ((base_w + w4) * 16 + jj) * k;
-            const int* li = s_li + ((base_w + w4) * 16 + jj) * k;
+            const float* ls = s_ls + ((base_w + w4) * kTuQpw + jj) * k;
+            const int* li = s_li + ((base_w + w4) * kTuQpw + jj) * k;
             for (int e = 0; e < k; ++e) list_insert(ls0, li0, k, ls[e], li[e]);
         }
         for (int e = 0; e < k; ++e) {
