@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ __align__(8) uint64_t s_bar[2];    // MMA completion per A buffer
     __shared__ __align__(8) uint64_t s_sbar[2];   // staging copies per buffer
+    __shared__ __align__(8) uint64_t s_abar[2];   // all MMAs of a tile done, per TMEM accumulator
     __shared__ uint32_t s_tmem;
     __shared__ uint32_t s_ktab[NT];
     __shared__ uint32_t s_klo[LO ? NT : 1];
@@ -129,15 +130,19 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
     const uint32_t bar[2] = {(uint32_t)__cvta_generic_to_shared(&s_bar[0]), (uint32_t)__cvta_generic_to_shared(&s_bar[1])};
     const uint32_t sbar[2] = {(uint32_t)__cvta_generic_to_shared(&s_sbar[0]),
                               (uint32_t)__cvta_generic_to_shared(&s_sbar[1])};
+    const uint32_t abar[2] = {(uint32_t)__cvta_generic_to_shared(&s_abar[0]),
+                              (uint32_t)__cvta_generic_to_shared(&s_abar[1])};
     if (tid == 0) {
         mbar_init(bar[0], 1);
         mbar_init(bar[1], 1);
         mbar_init(sbar[0], 1);
         mbar_init(sbar[1], 1);
+        mbar_init(abar[0], 1);
+        mbar_init(abar[1], 1);
         mbar_init_fence();
     }
-    if (warp == 0) {
-        tmem_alloc((uint32_t)__cvta_generic_to_shared(&s_tmem), kTuN);
+    if (warp == 0) {  // two accumulators: tile t's MMAs run while tile t - 1's epilogue reads the other
+        tmem_alloc((uint32_t)__cvta_generic_to_shared(&s_tmem), 2 * kTuN);
         tmem_relinquish();
     }
     fence_proxy_async_smem();
@@ -163,8 +168,11 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
     const uint32_t idesc = umma_idesc_f16(kTuRows, kTuN);
     const uint32_t sB_a = (uint32_t)__cvta_generic_to_shared(sB);
     const uint32_t sA_a[2] = {(uint32_t)__cvta_generic_to_shared(sA[0]), (uint32_t)__cvta_generic_to_shared(sA[1])};
-    const int r = tid & (kTuRows - 1);      // de-quantize: this thread's row in the tile
-    const int part = tid >> 7;              // ... and its share of the 8-coordinate units
+    // de-quantize: warp w takes rows 8w .. 8w+7 (lane & 7) and a quarter of their
+    // 8-coordinate units (lane >> 3): a quarter warp stores 8 rows of one unit
+    // (all banks) and the warp reads 8 rows x 4 units of the staged codes
+    const int r = 8 * warp + (lane & 7);
+    const int part = lane >> 3;
     const int units = ks / 8, upp = (units + kTuParts - 1) / kTuParts;
     const int u0 = part * upp, u1 = min(units, u0 + upp);
     const int er = 32 * (warp & 3) + lane;  // epilogue: this thread's row (TMEM lane)
@@ -197,6 +205,53 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
         s_nrm[tid] = f16_bits_to_f32(nxt_n);
         s_gam[tid] = __uint_as_float((uint32_t)nxt_g);  // raw fp16 bits of gamma, carried in a float slot
     }
+
+    // epilogue of tile te: wait for its MMAs, read its accumulator, update the lists
+    auto epilogue = [&](int64_t te) -> bool {
+        if (__syncthreads_or(!mbar_wait_bounded(abar[te & 1], (uint32_t)((te >> 1) & 1), kWaitLimitNs, p.err,
+                                                kErrScanWait)))
+            return false;
+        tc_fence_after_sync();
+        float v[2 * kTuQpw];
+        static_assert(2 * kTuQpw == 16, "one 16-column TMEM load per warp");
+        tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((te & 1) * kTuN + ecol), v);
+        tmem_ld_wait();
+        const int64_t erow = r0 + te * kTuRows + er;
+        const bool evalid = erow < r1;
+        const float scale = s_nrm[(te & 1) * kTuRows + er] * p.inv_lam;
+        const int id = (int)erow;
+#pragma unroll
+        for (int jj = 0; jj < kTuQpw; ++jj) {
+            const int j = (ecol >> 1) + jj;
+            if (j < nq_here) {  // warp-uniform
+                const float sc = scale * (v[2 * jj] + v[2 * jj + 1]);
+                float ts = __shfl_sync(TQ_FULL_MASK, lsc[jj], k - 1);
+                int ti = __shfl_sync(TQ_FULL_MASK, lid[jj], k - 1);
+                unsigned cand = __ballot_sync(TQ_FULL_MASK, evalid && better(sc, id, ts, ti));
+                while (cand) {
+                    const int src = __ffs(cand) - 1;
+                    cand &= cand - 1;
+                    const float cs_ = __shfl_sync(TQ_FULL_MASK, sc, src);
+                    const int ci = __shfl_sync(TQ_FULL_MASK, id, src);
+                    if (!better(cs_, ci, ts, ti)) continue;  // the list moved on since the ballot
+                    // entries better than the candidate stay, the rest move one lane down
+                    const int pos = __popc(__ballot_sync(TQ_FULL_MASK, lane < k && better(lsc[jj], lid[jj], cs_, ci)));
+                    const float us = __shfl_up_sync(TQ_FULL_MASK, lsc[jj], 1);
+                    const int ui = __shfl_up_sync(TQ_FULL_MASK, lid[jj], 1);
+                    if (lane == pos) {
+                        lsc[jj] = cs_;
+                        lid[jj] = ci;
+                    } else if (lane > pos) {
+                        lsc[jj] = us;
+                        lid[jj] = ui;
+                    }
+                    ts = __shfl_sync(TQ_FULL_MASK, lsc[jj], k - 1);
+                    ti = __shfl_sync(TQ_FULL_MASK, lid[jj], k - 1);
+                }
+            }
+        }
+        return true;
+    };
 
     for (int64_t t = 0; t < ntile && ok; ++t) {
         const int64_t t0 = r0 + t * kTuRows;
@@ -257,65 +312,27 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
             if (tid == 0) {
                 tc_fence_after_sync();
                 const int bseg = sign_seg ? 1 : 0;
+                const uint32_t dacc = tmem + (uint32_t)((t & 1) * kTuN);
                 for (int s = 0; s < ks / 16; ++s)
-                    umma_f16(tmem, umma_desc(sA_a[buf] + 256 * s, 128, ks * 16),
+                    umma_f16(dacc, umma_desc(sA_a[buf] + 256 * s, 128, ks * 16),
                              umma_desc(sB_a + (uint32_t)(bseg * ks / 8 + 2 * s) * 128, 128, kcb * 16), idesc,
                              seg > 0 || s > 0);
                 umma_commit(bar[buf]);
+                if (seg == NSEG_A - 1) umma_commit(abar[t & 1]);
             }
             ++step;
         }
         if (!ok) break;
-        // ---- epilogue: all MMAs of this tile done ----
-        ok = !__syncthreads_or(!mbar_wait_bounded(bar[(step - 1) & 1], (uint32_t)(((step - 1) >> 1) & 1), kWaitLimitNs,
-                                                  p.err, kErrScanWait));
-        if (!ok) break;
-        tc_fence_after_sync();
-        float v[2 * kTuQpw];
-        static_assert(2 * kTuQpw == 16, "one 16-column TMEM load per warp");
-        tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)ecol, v);
-        tmem_ld_wait();
-        const int64_t erow = t0 + er;
-        const bool evalid = erow < r1;
-        const float scale = t_nrm[er] * p.inv_lam;
-        const int id = (int)erow;
-#pragma unroll
-        for (int jj = 0; jj < kTuQpw; ++jj) {
-            const int j = (ecol >> 1) + jj;
-            if (j < nq_here) {  // warp-uniform
-                const float sc = scale * (v[2 * jj] + v[2 * jj + 1]);
-                float ts = __shfl_sync(TQ_FULL_MASK, lsc[jj], k - 1);
-                int ti = __shfl_sync(TQ_FULL_MASK, lid[jj], k - 1);
-                unsigned cand = __ballot_sync(TQ_FULL_MASK, evalid && better(sc, id, ts, ti));
-                while (cand) {
-                    const int src = __ffs(cand) - 1;
-                    cand &= cand - 1;
-                    const float cs_ = __shfl_sync(TQ_FULL_MASK, sc, src);
-                    const int ci = __shfl_sync(TQ_FULL_MASK, id, src);
-                    if (!better(cs_, ci, ts, ti)) continue;  // the list moved on since the ballot
-                    // entries better than the candidate stay, the rest move one lane down
-                    const int pos = __popc(__ballot_sync(TQ_FULL_MASK, lane < k && better(lsc[jj], lid[jj], cs_, ci)));
-                    const float us = __shfl_up_sync(TQ_FULL_MASK, lsc[jj], 1);
-                    const int ui = __shfl_up_sync(TQ_FULL_MASK, lid[jj], 1);
-                    if (lane == pos) {
-                        lsc[jj] = cs_;
-                        lid[jj] = ci;
-                    } else if (lane > pos) {
-                        lsc[jj] = us;
-                        lid[jj] = ui;
-                    }
-                    ts = __shfl_sync(TQ_FULL_MASK, lsc[jj], k - 1);
-                    ti = __shfl_sync(TQ_FULL_MASK, lid[jj], k - 1);
-                }
-            }
-        }
-        if (tid < kTuRows) {  // the next tile's norms into the other buffer
+        // the previous tile's epilogue runs while the tensor core works on this tile
+        if (t > 0 && !(ok = epilogue(t - 1))) break;
+        tc_fence_before_sync();
+        __syncthreads();  // the accumulator just read is overwritten by tile t + 1's first MMA
+        if (tid < kTuRows) {  // the norms of tile t + 1 into the buffer tile t - 1 used
             s_nrm[(sb ^ 1) * kTuRows + tid] = f16_bits_to_f32(nxt_n);
             s_gam[(sb ^ 1) * kTuRows + tid] = __uint_as_float((uint32_t)nxt_g);
         }
-        tc_fence_before_sync();
-        __syncthreads();  // D is overwritten by the next tile's first MMA
     }
+    if (ok && ntile > 0) ok = epilogue(ntile - 1);
     if (!ok) {
         // a wait ran out (the error word says so): let the copies and MMAs
         // still in flight finish, bounded, before TMEM and smem are released
@@ -325,10 +342,12 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
         }
         if (step > 0)
             mbar_wait_bounded(bar[(step - 1) & 1], (uint32_t)(((step - 1) >> 1) & 1), kWaitLimitNs, p.err, kErrScanWait);
+        if (step >= 2)
+            mbar_wait_bounded(bar[(step - 2) & 1], (uint32_t)(((step - 2) >> 1) & 1), kWaitLimitNs, p.err, kErrScanWait);
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kTuN);
+    if (warp == 0) tmem_dealloc(tmem, 2 * kTuN);
 
     // ---- merge the four warp lists of each query, write the chunk's candidates ----
     {
