@@ -166,7 +166,7 @@ void pair_table_lo(const std::vector<double>& c, int bits, double lam, uint32_t*
 
 struct DecodePlan {
     int n_splits = 1, chunk = 1, group = 1;
-    size_t off_frag = 0, off_done = 0, off_part = 0, total = 0;
+    size_t off_frag = 0, off_part = 0, total = 0;
 };
 
 tq_status plan_decode(const tq_decode_args* a, DecodePlan* pl) {
@@ -197,9 +197,8 @@ tq_status plan_decode(const tq_decode_args* a, DecodePlan* pl) {
     pl->chunk = chunk;
     const size_t rows = (size_t)a->batch * a->hq;
     pl->off_frag = 0;
-    pl->off_done = round_up(rows * tqk::kFragWords * sizeof(uint32_t), 256);
-    pl->off_part = pl->off_done + round_up((size_t)a->batch * a->hkv * sizeof(uint32_t), 256);
-    pl->total = pl->off_part + round_up(rows * (size_t)splits * tqk::kPartStride * sizeof(float), 256);
+    pl->off_part = round_up(rows * tqk::kFragWords * sizeof(uint32_t), 256);
+    pl->total = pl->off_part + round_up(rows * (size_t)splits * (a->d + 2) * sizeof(float), 256);
     return TQ_OK;
 }
 
@@ -259,7 +258,7 @@ struct StepStreams {
 std::mutex g_step_mutex;
 StepStreams g_step[kMaxStepDevices];
 
-constexpr int64_t kSmallAppend = 64;  // appends of at most this many vectors: warp-per-vector kernel
+constexpr int64_t kSmallAppend = 64;  // MSE appends of at most this many vectors: warp-per-vector kernel
 
 struct QuantLaunch {
     tqk::QuantParams p;
@@ -271,6 +270,7 @@ struct DecodeLaunch {
     DecodePlan pl;
     tqk::PrepParams pp;
     tqk::DecodeParams dp;
+    tqk::CombineParams cp;
     int kb = 0, vb = 0;
     cudaEvent_t scan_begin = nullptr, scan_end = nullptr;
 };
@@ -343,11 +343,13 @@ tq_status quant_prepare(const tq_quant_args* a, QuantLaunch* L, bool* empty) {
     p.pi_frag = a->rot->d_pi_frag;
     p.s_frag = prod ? a->qjl->d_s_frag : nullptr;
     // d = m = 128 with 16-byte aligned rows: the tensor-core kernel; otherwise
-    // the warp-per-vector kernel (any d <= 256). A small append (one token per
-    // KV head) also takes the warp-per-vector kernel: one warp per vector
-    // instead of one mostly empty 16-row tile on one warp.
-    const bool small = a->n <= kSmallAppend;
-    L->mma = c.d == 128 && !small && (!prod || (c.m == 128 && p.s_frag)) && (rht || p.pi_frag) &&
+    // the warp-per-vector kernel (any d <= 256). A small MSE append (one token
+    // per KV head) also takes the warp-per-vector kernel, one warp per vector
+    // instead of one mostly empty 16-row tile on one warp; keys keep the
+    // tensor-core kernel, whose S r product the warp-per-vector kernel would
+    // do as a mat-vec over all of S per warp.
+    const bool small_mse = !prod && a->n <= kSmallAppend;
+    L->mma = c.d == 128 && !small_mse && (!prod || (c.m == 128 && p.s_frag)) && (rht || p.pi_frag) &&
              aligned(a->x, 16) && (a->x_stride * (int64_t)esz) % 16 == 0;
     return TQ_OK;
 }
@@ -358,7 +360,7 @@ cudaError_t quant_launch(const QuantLaunch& L, cudaStream_t st) {
     return tqk::launch_quantize_dense(L.p, L.dtype, L.vpl, L.prod ? 1 : 0, L.cb, st);
 }
 
-// Validates a decode call and fills its two launches (query prep, scan).
+// Validates a decode call and fills its three launches.
 tq_status decode_prepare(const tq_decode_args* a, void* workspace, size_t ws_bytes, DecodeLaunch* D) {
     DecodePlan& pl = D->pl;
     tq_status s = plan_decode(a, &pl);
@@ -459,23 +461,22 @@ tq_status decode_prepare(const tq_decode_args* a, void* workspace, size_t ws_byt
     D->scan_begin = (cudaEvent_t)a->scan_begin;
     D->scan_end = (cudaEvent_t)a->scan_end;
 
-    // split counters (zeroed by the query prep) and the merge + un-rotation
-    // done by the last CTA of each (b, KV head)
-    uint32_t* done = (uint32_t*)(ws + pl.off_done);
-    pp.done = done;
-    pp.n_done = a->batch * a->hkv;
-    dp.done = done;
-    dp.pi32 = a->rot->d_pi32;
-    dp.sgn = a->rot->d_sign;
-    dp.rht = a->rot->kind == TQ_ROT_RHT ? 1 : 0;
-    dp.inv_sqrt_d = (float)(1.0 / std::sqrt((double)a->d));
-    dp.out = a->out;
-    dp.out_dtype = a->out_dtype == TQ_BF16 ? 1 : 0;
+    tqk::CombineParams& cp = D->cp;
+    std::memset(&cp, 0, sizeof(cp));
+    cp.partial = part;
+    cp.rows = a->batch * a->hq;
+    cp.d = a->d;
+    cp.n_splits = pl.n_splits;
+    cp.pi32 = a->rot->d_pi32;
+    cp.sgn = a->rot->d_sign;
+    cp.rht = a->rot->kind == TQ_ROT_RHT;
+    cp.inv_sqrt_d = (float)(1.0 / std::sqrt((double)a->d));
+    cp.out = a->out;
+    cp.out_dtype = a->out_dtype == TQ_BF16 ? 1 : 0;
     return TQ_OK;
 }
 
-// Query prep on st, then (after st waits on `waits`) the scan, which also
-// merges the splits and writes the output.
+// Query prep on st, then (after st waits on `waits`) the scan and the merge.
 tq_status decode_launch(const DecodeLaunch& D, cudaStream_t st, const cudaEvent_t* waits, int nwaits) {
     cudaError_t e = tqk::launch_query_prep(D.pp, st);
     if (e != cudaSuccess) return cuda_status(e, "tq_attn_decode query prep");
@@ -487,7 +488,8 @@ tq_status decode_launch(const DecodeLaunch& D, cudaStream_t st, const cudaEvent_
     if (e != cudaSuccess) return cuda_status(e, "tq_attn_decode scan");
     if (D.scan_end && (e = cudaEventRecord(D.scan_end, st)) != cudaSuccess)
         return cuda_status(e, "tq_attn_decode scan_end");
-    return TQ_OK;
+    e = tqk::launch_combine(D.cp, st);
+    return cuda_status(e, "tq_attn_decode combine");
 }
 
 }  // namespace

@@ -28,4 +28,23 @@ cudaError_t launch_decode_mma(const DecodeParams& p, int kbits, int vbits, cudaS
     return cudaErrorInvalidValue;
 }
 
+// Programmatic dependent launch: the merge's CTAs may be scheduled while the
+// scan's last CTAs still run (the scan signals launch_dependents once its
+// tiles are done); the merge waits for the scan grid to complete before it
+// reads a partial (griddepcontrol.wait).
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
+    if (p.rows <= 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.rows);
+    cfg.blockDim = dim3(kCombineThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, combine_kernel, p);
+}
+
 }  // namespace tqk

@@ -1,6 +1,6 @@
-// Decode attention before the split-K scan: query preparation (the query is
-// rotated once, q' = Pi q, and projected, u = S q'). The merge of the splits
-// and the single un-rotation o = Pi^T (a / Z) close the scan kernel.
+// Decode attention around the split-K scan: query preparation (the query is
+// rotated once, q' = Pi q, and projected, u = S q') and the merge of the
+// splits followed by the single un-rotation o = Pi^T (a / Z).
 //
 // Follows: A2A TurboQuant explainer, end of "Stage 2" and "How to implement"
 // (the fused kernel rotates the query once and scores from the indices). The
@@ -49,7 +49,6 @@ __global__ void __launch_bounds__(kPrepWarps * 32) query_prep_kernel(const __gri
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
     const int64_t row = blockIdx.x;
     const int d = p.d;
-    if (p.done && tid == 0 && row < p.n_done) p.done[row] = 0u;  // the scan's split counters
     for (int i = tid; i < d; i += blockDim.x) {
         s_x[i] = p.q_dtype == 1 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.q)[row * d + i])
                                 : reinterpret_cast<const float*>(p.q)[row * d + i];
@@ -167,6 +166,94 @@ __global__ void __launch_bounds__(kPrepWarps * 32) query_prep_kernel(const __gri
     if (p.frag) {
         __syncthreads();
         write_frag(p, row, s_y, s_x, tid);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Merge the splits of one query row and un-rotate: o = Pi^T (a / Z).
+// CTA of 1024 threads = (1024 / d) groups of d threads; group k runs an
+// online (max, sum, a) merge over the splits s = k, k + groups, ... in one
+// pass, then the groups are merged through shared memory. d in {64, 128, 256}.
+// ---------------------------------------------------------------------------
+constexpr int kCombineThreads = 1024;
+
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ CombineParams p) {
+    __shared__ float s_m[kCombineThreads];
+    __shared__ float s_z[kCombineThreads];
+    __shared__ float s_v[kCombineThreads];
+    // launched as a programmatic dependent of the scan: wait for its grid to
+    // complete and its partials to be visible (a no-op on a plain launch)
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    __shared__ float s_a[256];
+    const int row = blockIdx.x, tid = threadIdx.x, d = p.d, ns = p.n_splits;
+    const int groups = kCombineThreads / d;
+    const int i = tid % d, grp = tid / d;
+    const float* base = p.partial + (int64_t)row * ns * (d + 2);
+
+    float m = -INFINITY, z = 0.0f, a = 0.0f;
+#pragma unroll 4
+    for (int s = grp; s < ns; s += groups) {
+        const float* ps = base + (int64_t)s * (d + 2);
+        const float ms = ps[d], zs = ps[d + 1], as = ps[i];
+        if (ms > m) {
+            const float sc = (m == -INFINITY) ? 0.0f : exp2f(m - ms);
+            z *= sc;
+            a *= sc;
+            m = ms;
+        }
+        if (ms != -INFINITY) {
+            const float w = exp2f(ms - m);
+            z = fmaf(zs, w, z);
+            a = fmaf(as, w, a);
+        }
+    }
+    s_m[tid] = m;
+    s_z[tid] = z;
+    s_v[tid] = a;
+    __syncthreads();
+    if (tid < d) {
+        float mstar = -INFINITY;
+        for (int k = 0; k < groups; ++k) mstar = fmaxf(mstar, s_m[k * d + tid]);
+        float zt = 0.0f, at = 0.0f;
+        for (int k = 0; k < groups; ++k) {
+            const float mk = s_m[k * d + tid];
+            if (mk == -INFINITY) continue;
+            const float w = exp2f(mk - mstar);
+            zt = fmaf(s_z[k * d + tid], w, zt);
+            at = fmaf(s_v[k * d + tid], w, at);
+        }
+        s_a[tid] = (zt > 0.0f) ? at / zt : 0.0f;
+    }
+    __syncthreads();
+    float o = 0.0f;
+    if (p.rht) {
+        // o = s * (H a) / sqrt(d): in-place Walsh-Hadamard on shared memory
+        for (int h = 1; h < d; h <<= 1) {
+            float v = 0.0f, w = 0.0f;
+            if (tid < d) {
+                v = s_a[tid];
+                w = s_a[tid ^ h];
+            }
+            __syncthreads();
+            if (tid < d) s_a[tid] = (tid & h) ? (w - v) : (v + w);
+            __syncthreads();
+        }
+        if (tid < d) o = s_a[tid] * p.sgn[tid] * p.inv_sqrt_d;
+    } else {
+        // o_i = sum_k Pi[k][i] a_k, the k range split over the groups
+        float part = 0.0f;
+#pragma unroll 4
+        for (int k = grp; k < d; k += groups) part = fmaf(__ldg(p.pi32 + (size_t)k * d + i), s_a[k], part);
+        s_v[tid] = part;
+        __syncthreads();
+        if (tid < d)
+            for (int k = 0; k < groups; ++k) o += s_v[k * d + tid];
+    }
+    if (tid < d) {
+        if (p.out_dtype == 1)
+            reinterpret_cast<__nv_bfloat16*>(p.out)[(int64_t)row * d + tid] = __float2bfloat16_rn(o);
+        else
+            reinterpret_cast<float*>(p.out)[(int64_t)row * d + tid] = o;
     }
 }
 

@@ -21,9 +21,6 @@
 // 32c..32c+31; values: tokens 4c..4c+3) and the value M dimension too (row g
 // holds coordinates 16g..16g+15), so each thread reads contiguous code bits.
 //
-// The last CTA of each (b, KV head) merges the splits and un-rotates
-// (merge_splits), so the decode needs no separate merge launch.
-//
 // Tiles are staged per warp in a 4-deep ring of shared-memory buffers, each
 // filled by six bulk (TMA) copies -- one per cache plane, issued by lanes 0..5
 // in one instruction -- that complete on the buffer's mbarrier. The capacity
@@ -104,114 +101,6 @@ __device__ __forceinline__ float ex2(float x) {
 template <typename T>
 __device__ __forceinline__ T lds_at(const void* base, uint32_t byte_off) {
     return *reinterpret_cast<const T*>(reinterpret_cast<const unsigned char*>(base) + byte_off);
-}
-
-// Merge the n_splits partials (M, Z, a) of the G query heads of (b, kv) and
-// write o = Pi^T (a / Z). Warp w merges the splits s = w, w + 4, ... (lane l:
-// coordinates 4l .. 4l+3), then the four warps are merged per coordinate; the
-// un-rotation is an in-register Walsh-Hadamard transform per head (RHT) or a
-// mat-vec with Pi for all heads at once (dense). sm: >= G * 2592 bytes.
-template <int G>
-__device__ __forceinline__ void merge_splits(const DecodeParams& p, int b, int kv, float* sm) {
-    constexpr int D = 128;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
-    const int ns = p.n_splits;
-    float* s_m = sm;                       // [G][warps]
-    float* s_z = s_m + G * kMmaWarps;      // [G][warps]
-    float* s_a = s_z + G * kMmaWarps;      // [G][warps][D]
-    float* s_r = s_a + G * kMmaWarps * D;  // [G][D]: a / Z
-    int rows[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) rows[h] = b * p.hq + (p.use_table ? (int)p.head_table[kv * G + h] : kv * G + h);
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        const float* base = p.partial + (int64_t)rows[h] * ns * kPartStride;
-        float m = -INFINITY, z = 0.0f, a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-#pragma unroll 4
-        for (int s = warp; s < ns; s += kMmaWarps) {
-            const float* ps = base + (int64_t)s * kPartStride;
-            const float ms = ps[D], zs = ps[D + 1];
-            const float4 as = *reinterpret_cast<const float4*>(ps + 4 * lane);
-            const float mn = fmaxf(m, ms);
-            if (mn != -INFINITY) {  // the same split for the whole warp: uniform
-                const float co = (m == -INFINITY) ? 0.0f : ex2(m - mn);
-                const float cn = (ms == -INFINITY) ? 0.0f : ex2(ms - mn);
-                z = fmaf(z, co, zs * cn);
-                a0 = fmaf(a0, co, as.x * cn);
-                a1 = fmaf(a1, co, as.y * cn);
-                a2 = fmaf(a2, co, as.z * cn);
-                a3 = fmaf(a3, co, as.w * cn);
-                m = mn;
-            }
-        }
-        if (lane == 0) {
-            s_m[h * kMmaWarps + warp] = m;
-            s_z[h * kMmaWarps + warp] = z;
-        }
-        *reinterpret_cast<float4*>(s_a + (h * kMmaWarps + warp) * D + 4 * lane) = make_float4(a0, a1, a2, a3);
-    }
-    __syncthreads();
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        float mstar = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kMmaWarps; ++w) mstar = fmaxf(mstar, s_m[h * kMmaWarps + w]);
-        float z = 0.0f, a = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kMmaWarps; ++w) {
-            const float mw = s_m[h * kMmaWarps + w];
-            const float wt = (mw == -INFINITY) ? 0.0f : ex2(mw - mstar);
-            z = fmaf(s_z[h * kMmaWarps + w], wt, z);
-            a = fmaf(s_a[(h * kMmaWarps + w) * D + tid], wt, a);
-        }
-        s_r[h * D + tid] = z > 0.0f ? a / z : 0.0f;  // a sequence with no visible token gives 0
-    }
-    __syncthreads();
-    auto put = [&](int h, int i, float o) {
-        if (p.out_dtype == 1)
-            reinterpret_cast<__nv_bfloat16*>(p.out)[(int64_t)rows[h] * D + i] = __float2bfloat16_rn(o);
-        else
-            reinterpret_cast<float*>(p.out)[(int64_t)rows[h] * D + i] = o;
-    };
-    if (p.rht) {
-        // o = s * (H a) / sqrt(d); warp w takes heads w, w + 4, ...: lane l holds
-        // coordinates 4l .. 4l+3 (index bits 0-1 in the thread, 2-6 across lanes)
-#pragma unroll
-        for (int h = warp; h < G; h += kMmaWarps) {
-            float y[4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r) y[r] = s_r[h * D + 4 * lane + r];
-            float t0 = y[0] + y[1], t1 = y[0] - y[1], t2 = y[2] + y[3], t3 = y[2] - y[3];
-            y[0] = t0 + t2;
-            y[2] = t0 - t2;
-            y[1] = t1 + t3;
-            y[3] = t1 - t3;
-#pragma unroll
-            for (int hb = 1; hb < 32; hb <<= 1) {
-                const bool upper = (lane & hb) != 0;
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const float o = __shfl_xor_sync(TQ_FULL_MASK, y[r], hb);
-                    y[r] = upper ? (o - y[r]) : (y[r] + o);
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < 4; ++r) put(h, 4 * lane + r, y[r] * p.sgn[4 * lane + r] * p.inv_sqrt_d);
-        }
-    } else {
-        // o_i = sum_k Pi[k][i] a_k for every head; thread tid = coordinate i
-        float o[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) o[h] = 0.0f;
-#pragma unroll 8
-        for (int k = 0; k < D; ++k) {
-            const float pk = __ldg(p.pi32 + k * D + tid);
-#pragma unroll
-            for (int h = 0; h < G; ++h) o[h] = fmaf(pk, s_r[h * D + k], o[h]);
-        }
-#pragma unroll
-        for (int h = 0; h < G; ++h) put(h, tid, o[h]);
-    }
 }
 
 template <int KB, int VB, int G>
@@ -504,6 +393,9 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
     }
     __syncthreads();
 
+    // the merge kernel may be scheduled now; it waits for this grid to finish
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+
     // ---- merge the warps of the CTA and write this split's partials ----
     float* s_acc = reinterpret_cast<float*>(smem);  // [warps][G][D]
     float* s_mz = s_acc + kMmaWarps * G * D;        // [warps][G][2]
@@ -543,25 +435,13 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
             a = fmaf(s_acc[(w * G + h) * D + ci], wt, a);
         }
         const int row = b * p.hq + (p.use_table ? (int)p.head_table[kv * G + h] : kv * G + h);
-        float* out = p.partial + ((int64_t)row * p.n_splits + split) * kPartStride;
+        float* out = p.partial + ((int64_t)row * p.n_splits + split) * (D + 2);
         out[ci] = a;
         if (ci == 0) {
             out[D] = mstar;
             out[D + 1] = z;
         }
     }
-
-    // ---- the last CTA of this (b, KV head) to finish merges all its splits ----
-    __shared__ int s_last;
-    __syncthreads();  // this CTA's partials are written
-    if (threadIdx.x == 0) {
-        __threadfence();
-        s_last = atomicAdd(p.done + ((int64_t)b * p.hkv + kv), 1u) == (unsigned)(p.n_splits - 1);
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();  // every split's partials are visible
-    merge_splits<G>(p, b, kv, reinterpret_cast<float*>(smem));
 }
 
 template <int KB, int VB, int G>
@@ -570,8 +450,6 @@ size_t decode_mma_smem() {
     constexpr int NT = (G + 3) / 4;
     size_t pipe = (size_t)kMmaWarps * kMmaStages * T::BYTES + 2 * kMmaWarps * NT * 8 * 16;
     size_t merge = (size_t)kMmaWarps * G * 128 * 4 + kMmaWarps * G * 2 * 4;
-    size_t tail = (size_t)G * (2 * kMmaWarps + kMmaWarps * 128 + 128) * 4;  // merge_splits
-    if (tail > merge) merge = tail;
     return pipe > merge ? pipe : merge;
 }
 

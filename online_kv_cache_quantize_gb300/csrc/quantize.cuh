@@ -257,8 +257,7 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quantize_kernel(const __grid
             float acc[8];
 #pragma unroll
             for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
-#pragma unroll 8
-            for (int i = 0; i < d; ++i) {  // unrolled: eight rows of S^T in flight
+            for (int i = 0; i < d; ++i) {
                 const float ri = s_buf[warp][i];
                 const float* row = p.st32 + (size_t)i * m;
 #pragma unroll

@@ -68,8 +68,6 @@ struct PrepParams {
     // words per row; see decode_mma.cuh), or NULL
     uint32_t* frag;
     float qjl_scale;
-    uint32_t* done;       // decode: per (b, KV head) split counters, zeroed here (rows >= n_done skip)
-    int n_done;
 };
 
 constexpr int kFragWords = 256;
@@ -96,7 +94,7 @@ struct DecodeParams {
     float scale_log2;     // softmax scale * log2(e)
     int n_splits;
     int chunk;            // tokens per split
-    float* partial;       // [B*Hq][n_splits][kPartStride]: a (d floats), M, Z
+    float* partial;       // [B*Hq][n_splits][d+2]
     float* logits;        // optional [B*Hq][max_seq_len]
     int max_seq_len;
     // tensor-core scan: 2-coordinate fp16 pair tables of lam * centroid
@@ -105,17 +103,7 @@ struct DecodeParams {
     uint32_t vlut[256];
     float inv_lam_k, inv_lam_v;
     uint32_t* err;          // device error word (a wait that ran out sets a bit)
-    // merge of the splits by the last CTA of each (b, KV head), and the un-rotation
-    uint32_t* done;         // [B*Hkv] split counters, zero when the scan starts
-    const float* pi32;      // dense Pi [d][d] (o_j = sum_i Pi_ij a_i)
-    const float* sgn;       // RHT signs [d]
-    int rht;
-    float inv_sqrt_d;
-    void* out;              // [B*Hq][d]
-    int out_dtype;          // 0 f32, 1 bf16
 };
-
-constexpr int kPartStride = 132;  // floats per split partial: 128 of a, M, Z, 2 pad (16-byte rows)
 
 cudaError_t launch_decode_mma(const DecodeParams& p, int kbits, int vbits, cudaStream_t s);
 
@@ -129,7 +117,19 @@ cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t 
 cudaError_t launch_umma_selftest(const void* a, const void* b, float* d, int n, int k, uint32_t* err, cudaStream_t s);
 
 
+struct CombineParams {
+    const float* partial;
+    int rows;             // B*Hq
+    int d, n_splits;
+    const float* pi32;    // dense Pi [d][d] (o_j = sum_i Pi_ij a_i)
+    const float* sgn;     // RHT signs
+    int rht;
+    float inv_sqrt_d;
+    void* out;
+    int out_dtype;        // 0 f32, 1 bf16
+};
 
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 
 struct TopkParams {
     const float* qprime;  // [nq][d]
