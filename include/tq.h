@@ -19,10 +19,11 @@
  *     default stream). Argument errors are found on the host before any
  *     launch and return a status; a launch failure returns TQ_ERR_CUDA;
  *     faults during execution surface at the caller's next synchronisation.
- *   - No call blocks on the device. The one kind of device-side wait (the
- *     decode scan waiting for its bulk copies to land on an mbarrier) gives
- *     up after one second, records the cause in the device error word and
- *     lets the kernel return; tq_device_errors reads it (TQ_ERR_TIMEOUT).
+ *   - No call blocks on the device. The one kind of device-side wait (a
+ *     kernel waiting for its bulk copies or tensor-core products to land on
+ *     an mbarrier) gives up after one second, records the cause in the device
+ *     error word and lets the kernel return; tq_device_errors reads it
+ *     (TQ_ERR_TIMEOUT).
  *   - tq_last_error() returns a thread-local message for the last failure.
  */
 #ifndef TQ_H
@@ -311,12 +312,15 @@ int tq_topk_force_simt(int on);
  *   TQ_DEVERR_SCAN_WAIT      a decode scan tile's copies did not land within
  *                            one second; that call's output is not valid
  *   TQ_DEVERR_SELFTEST_WAIT  tq_selftest_bounded_wait ran out (its purpose)
+ *   TQ_DEVERR_QUANT_WAIT     a quantize CTA's operand fragments did not land
+ *                            within one second; that call's output is not valid
  * tq_device_errors synchronises the current device, stores the word in
  * *flags_out (host, may be NULL), clears it when reset != 0, and returns
  * TQ_ERR_TIMEOUT when any bit was set, TQ_OK when none was, TQ_ERR_CUDA when
  * the device could not be read. */
 #define TQ_DEVERR_SCAN_WAIT 1u
 #define TQ_DEVERR_SELFTEST_WAIT 2u
+#define TQ_DEVERR_QUANT_WAIT 4u
 tq_status tq_device_errors(uint32_t* flags_out, int reset);
 
 /* Self-test of the bounded wait: launches one warp on `stream` that waits on

@@ -359,6 +359,7 @@ def tq_decode_step(q, kcache, vcache, seq_lens, max_seq_len, rot, qjl, out, k_ne
 
 TQ_DEVERR_SCAN_WAIT = 1
 TQ_DEVERR_SELFTEST_WAIT = 2
+TQ_DEVERR_QUANT_WAIT = 4
 
 
 def tq_device_errors(reset=False):

@@ -335,6 +335,7 @@ tq_status quant_prepare(const tq_quant_args* a, QuantLaunch* L, bool* empty) {
     p.inv_sqrt_d = (float)(1.0 / std::sqrt((double)c.d));
     p.guard = rht ? 1.0e-6f : (float)(3.0e-8 * c.d);
     if ((s = fill_codebook(c.d, cb, &p.cb)) != TQ_OK) return s;
+    if (cudaError_t ew = tqk::device_error_word(&p.err); ew != cudaSuccess) return cuda_status(ew, "tq_quantize_kv error word");
     L->dtype = a->x_dtype == TQ_F32 ? 0 : 1;
     L->vpl = vpl_for(c.d);
     L->rht = rht;

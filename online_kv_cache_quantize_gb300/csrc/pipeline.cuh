@@ -17,6 +17,7 @@ namespace tqk {
 // bits of the device error word
 constexpr uint32_t kErrScanWait = 1u;      // a scan tile's copy did not complete in time
 constexpr uint32_t kErrSelfTestWait = 2u;  // the bounded-wait self-test ran out (expected)
+constexpr uint32_t kErrQuantWait = 4u;     // a quantize CTA's operand fragments did not land in time
 
 // a copy from HBM lands within microseconds; one second means it never will
 constexpr uint64_t kWaitLimitNs = 1000000000ull;

@@ -25,6 +25,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "pipeline.cuh"
 #include "tq_launch.h"
 
 namespace tqk {
@@ -100,20 +101,36 @@ __global__ void __launch_bounds__(kQmWarps * 32, 3) quantize_mma_kernel(const __
     unsigned char* xs_base = smem + B1_BYTES + B2_BYTES + warp * S::WARP_BYTES;  // 2 raw staging tiles
     const uint32_t xs_s = (uint32_t)__cvta_generic_to_shared(xs_base);
 
-    // ---- CTA set-up: B fragments (cp.async, all in flight; completed by the
-    // first wait of the tile loop) and centroids into shared memory ----
-    {
-        const uint32_t s0 = (uint32_t)__cvta_generic_to_shared(smem);
-        const unsigned char* src1 = reinterpret_cast<const unsigned char*>(p.pi_frag);
-#pragma unroll 8
-        for (int i = threadIdx.x; i < B1_BYTES / 16; i += blockDim.x) cp_async16_zfill(s0 + 16 * i, src1 + 16 * i, true);
-        const unsigned char* src2 = reinterpret_cast<const unsigned char*>(p.s_frag);
-#pragma unroll 8
-        for (int i = threadIdx.x; i < B2_BYTES / 16; i += blockDim.x)
-            cp_async16_zfill(s0 + B1_BYTES + 16 * i, src2 + 16 * i, true);
-        if (threadIdx.x < kMaxLevels) s_cent[threadIdx.x] = p.cb.c[threadIdx.x];
+    // ---- CTA set-up: the B fragments by bulk copies on an mbarrier that each
+    // warp waits on only before its first tensor-core product (so the load
+    // overlaps the first tile's norm, rotation and bucketize), and the
+    // centroids into shared memory ----
+    __shared__ __align__(8) uint64_t s_fbar;
+    const uint32_t fbar = (uint32_t)__cvta_generic_to_shared(&s_fbar);
+    constexpr int FRAG_BYTES = B1_BYTES + B2_BYTES;
+    if (threadIdx.x == 0) {
+        mbar_init(fbar, 1);
+        mbar_init_fence();
+        if constexpr (FRAG_BYTES > 0) {
+            const uint32_t s0 = (uint32_t)__cvta_generic_to_shared(smem);
+            mbar_arrive_expect_tx(fbar, FRAG_BYTES);
+            constexpr int CH = 16384;
+            for (int o = 0; o < B1_BYTES; o += CH)
+                bulk_g2s(s0 + o, reinterpret_cast<const unsigned char*>(p.pi_frag) + o, CH, fbar);
+            for (int o = 0; o < B2_BYTES; o += CH)
+                bulk_g2s(s0 + B1_BYTES + o, reinterpret_cast<const unsigned char*>(p.s_frag) + o, CH, fbar);
+        }
     }
-    asm volatile("cp.async.commit_group;\n" ::);  // group: B fragments
+    if (threadIdx.x < kMaxLevels) s_cent[threadIdx.x] = p.cb.c[threadIdx.x];
+    bool frag_ready = FRAG_BYTES == 0, failed = false;
+    // warp-uniform: true once the fragments are in shared memory
+    auto frags = [&]() -> bool {
+        if (!frag_ready) {
+            const bool ok = mbar_wait_bounded(fbar, 0, kWaitLimitNs, p.err, kErrQuantWait);
+            frag_ready = __all_sync(TQ_FULL_MASK, ok);
+        }
+        return frag_ready;
+    };
     // RHT signs of this thread's coordinates 32c .. 32c+31 as one mask (bit j
     // set: coordinate 32c + j is negated), applied by flipping float sign bits
     uint32_t sgm = 0u;
@@ -140,9 +157,8 @@ __global__ void __launch_bounds__(kQmWarps * 32, 3) quantize_mma_kernel(const __
     int64_t tile = (int64_t)blockIdx.x * NW + warp;
     if (tile < ntiles) stage(tile, 0);
     asm volatile("cp.async.commit_group;\n" ::);  // group: first tile
-    asm volatile("cp.async.wait_group 1;\n" ::);  // B fragments landed (first tile may still fly)
-    __syncthreads();                               // ... for every warp of the CTA
-    for (int it = 0; tile < ntiles; tile += tstep, ++it) {
+    __syncthreads();  // centroids and the barrier's initialisation, for every warp
+    for (int it = 0; tile < ntiles && !failed; tile += tstep, ++it) {
         const int64_t v0 = tile * 16;
         unsigned char* xs = xs_base + (it & 1) * ST::BYTES;
         if (tile + tstep < ntiles) stage(tile + tstep, (it + 1) & 1);  // prefetch the next tile
@@ -241,6 +257,10 @@ __global__ void __launch_bounds__(kQmWarps * 32, 3) quantize_mma_kernel(const __
                 for (int j = 0; j < 32; ++j) y[rr][j] *= sc;
             }
         } else {
+            if (!frags()) {  // the fragments never landed (the error word says so)
+                failed = true;
+                break;
+            }
             // two passes of 8 n-tiles (output coordinates 32c + 0..15, then
             // 32c + 16..31) keep the live accumulators at 32 registers; the
             // first pass's results wait in `first` while y still feeds pass 2
@@ -479,6 +499,10 @@ __global__ void __launch_bounds__(kQmWarps * 32, 3) quantize_mma_kernel(const __
                 g2 += __shfl_xor_sync(TQ_FULL_MASK, g2, 2);
                 gam[rr] = sqrtf(g2);
             }
+            if (!frags()) {
+                failed = true;
+                break;
+            }
             // R as bf16 hi/lo A fragments for all 8 k-steps (64 registers; y is
             // dead afterwards), then two passes of 8 n-tiles (16 sign bits
             // each) so that only 32 accumulators are live at a time
@@ -529,6 +553,9 @@ __global__ void __launch_bounds__(kQmWarps * 32, 3) quantize_mma_kernel(const __
         __syncwarp();
     }
     asm volatile("cp.async.wait_group 0;\n" ::);
+    // a warp with no tile (or that gave up) still lets the fragment copies land
+    // before the CTA's shared memory is released
+    if (!frag_ready) mbar_wait_bounded(fbar, 0, kWaitLimitNs, p.err, kErrQuantWait);
 }
 
 template <typename XT, int CB, bool PROD, bool RHT>

@@ -79,8 +79,11 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
     const TuLayout Lo = tu_layout(ks, NSEG_B, cs, ss, k);
     const int kcb = Lo.kcb;
     unsigned char* sB = smem + Lo.b;
-    unsigned char* sA[2] = {smem + Lo.a0, smem + Lo.a1};
-    unsigned char* sSt[2] = {smem + Lo.st0, smem + Lo.st1};
+    // buffer x of a pair at base + x * stride (no arrays indexed at run time)
+    unsigned char* const sA0 = smem + Lo.a0;
+    const size_t sA_stride = Lo.a1 - Lo.a0;
+    unsigned char* const sSt0 = smem + Lo.st0;
+    const size_t sSt_stride = Lo.st1 - Lo.st0;
     const uint4* s_sgn = reinterpret_cast<const uint4*>(smem + Lo.sgn);
     float* s_nrm = reinterpret_cast<float*>(smem + Lo.nrm);          // [2][128]: n of each row
     float* s_gam = s_nrm + 2 * kTuRows;                              // [2][128]: gamma (PROD)
@@ -127,18 +130,17 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
                 half_split(v0, 1) | (half_split(v1, 1) << 16);
         }
     }
-    const uint32_t bar[2] = {(uint32_t)__cvta_generic_to_shared(&s_bar[0]), (uint32_t)__cvta_generic_to_shared(&s_bar[1])};
-    const uint32_t sbar[2] = {(uint32_t)__cvta_generic_to_shared(&s_sbar[0]),
-                              (uint32_t)__cvta_generic_to_shared(&s_sbar[1])};
-    const uint32_t abar[2] = {(uint32_t)__cvta_generic_to_shared(&s_abar[0]),
-                              (uint32_t)__cvta_generic_to_shared(&s_abar[1])};
+    // mbarrier x of each pair at base + 8 x
+    const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(&s_bar[0]);
+    const uint32_t sbar0 = (uint32_t)__cvta_generic_to_shared(&s_sbar[0]);
+    const uint32_t abar0 = (uint32_t)__cvta_generic_to_shared(&s_abar[0]);
     if (tid == 0) {
-        mbar_init(bar[0], 1);
-        mbar_init(bar[1], 1);
-        mbar_init(sbar[0], 1);
-        mbar_init(sbar[1], 1);
-        mbar_init(abar[0], 1);
-        mbar_init(abar[1], 1);
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(bar0 + 8 * x, 1);
+            mbar_init(sbar0 + 8 * x, 1);
+            mbar_init(abar0 + 8 * x, 1);
+        }
         mbar_init_fence();
     }
     if (warp == 0) {  // two accumulators: tile t's MMAs run while tile t - 1's epilogue reads the other
@@ -157,17 +159,21 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
         const int64_t t0 = r0 + t * kTuRows;
         const int rows = (int)min((int64_t)kTuRows, r1 - t0);
         const int b = (int)(t & 1);
-        const uint32_t dst = (uint32_t)__cvta_generic_to_shared(sSt[b]);
+        const uint32_t dst = (uint32_t)__cvta_generic_to_shared(sSt0 + b * sSt_stride);
+        const uint32_t sb_ = sbar0 + 8 * b;
         fence_proxy_async_smem();
-        mbar_arrive_expect_tx(sbar[b], (uint32_t)rows * (cs + ss));
-        bulk_g2s(dst, p.codes + t0 * cs, (uint32_t)rows * cs, sbar[b]);
-        if constexpr (PROD) bulk_g2s(dst + kTuRows * cs, p.signs + t0 * ss, (uint32_t)rows * ss, sbar[b]);
+        mbar_arrive_expect_tx(sb_, (uint32_t)rows * (cs + ss));
+        bulk_g2s(dst, p.codes + t0 * cs, (uint32_t)rows * cs, sb_);
+        if constexpr (PROD) bulk_g2s(dst + kTuRows * cs, p.signs + t0 * ss, (uint32_t)rows * ss, sb_);
     };
     if (tid == 0 && ntile > 0) stage(0);
 
     const uint32_t idesc = umma_idesc_f16(kTuRows, kTuN);
-    const uint32_t sB_a = (uint32_t)__cvta_generic_to_shared(sB);
-    const uint32_t sA_a[2] = {(uint32_t)__cvta_generic_to_shared(sA[0]), (uint32_t)__cvta_generic_to_shared(sA[1])};
+    const uint32_t sA_a0 = (uint32_t)__cvta_generic_to_shared(sA0);
+    // MMA descriptors of k-step 0; k-step s starts 256 s bytes (16 s in the
+    // descriptor's address field) further on
+    const uint64_t descA0 = umma_desc(sA_a0, 128, ks * 16);
+    const uint64_t descB0 = umma_desc((uint32_t)__cvta_generic_to_shared(sB), 128, kcb * 16);
     // de-quantize: warp w takes rows 8w .. 8w+7 (lane & 7) and a quarter of their
     // 8-coordinate units (lane >> 3): a quarter warp stores 8 rows of one unit
     // (all banks) and the warp reads 8 rows x 4 units of the staged codes
@@ -208,7 +214,7 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
 
     // epilogue of tile te: wait for its MMAs, read its accumulator, update the lists
     auto epilogue = [&](int64_t te) -> bool {
-        if (__syncthreads_or(!mbar_wait_bounded(abar[te & 1], (uint32_t)((te >> 1) & 1), kWaitLimitNs, p.err,
+        if (__syncthreads_or(!mbar_wait_bounded(abar0 + 8 * (uint32_t)(te & 1), (uint32_t)((te >> 1) & 1), kWaitLimitNs, p.err,
                                                 kErrScanWait)))
             return false;
         tc_fence_after_sync();
@@ -258,7 +264,7 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
         const int sb = (int)(t & 1);
         if (tid == 0 && t + 1 < ntile) stage(t + 1);  // its buffer was last read in tile t - 1
         load_norms(t + 1, nxt_n, nxt_g);
-        ok = !__syncthreads_or(!mbar_wait_bounded(sbar[sb], (uint32_t)((t >> 1) & 1), kWaitLimitNs, p.err, kErrScanWait));
+        ok = !__syncthreads_or(!mbar_wait_bounded(sbar0 + 8 * sb, (uint32_t)((t >> 1) & 1), kWaitLimitNs, p.err, kErrScanWait));
         if (!ok) break;
         const float* t_nrm = s_nrm + sb * kTuRows;
         const float* t_gam = s_gam + sb * kTuRows;
@@ -266,21 +272,24 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
             const int buf = step & 1;
             if (step >= 2) {
                 ok = !__syncthreads_or(
-                    !mbar_wait_bounded(bar[buf], (uint32_t)(((step - 2) >> 1) & 1), kWaitLimitNs, p.err, kErrScanWait));
+                    !mbar_wait_bounded(bar0 + 8 * buf, (uint32_t)(((step - 2) >> 1) & 1), kWaitLimitNs, p.err, kErrScanWait));
                 if (!ok) break;
             }
             const bool sign_seg = PROD && seg == NSEG_A - 1;
-            unsigned char* dstA = sA[buf];
+            unsigned char* dstA = sA0 + buf * sA_stride;
             const bool rvalid = t0 + r < r1;
-            const unsigned char* crow = sSt[sb] + r * cs;
-            const unsigned char* srow = sSt[sb] + kTuRows * cs + r * ss;
+            const unsigned char* crow = sSt0 + sb * sSt_stride + r * cs;
+            const unsigned char* srow = sSt0 + sb * sSt_stride + kTuRows * cs + r * ss;
             uint32_t g2 = 0u;
             if (sign_seg) {
                 const uint32_t g16 = __float_as_uint(t_gam[r]);
                 g2 = (g16 | 0x8000u) | ((g16 | 0x8000u) << 16);  // (-gamma, -gamma)
             }
-#pragma unroll 4
-            for (int u = u0; u < u1; ++u) {
+            static_assert(256 / 8 / kTuParts <= 8, "at most 8 units per thread");
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {  // fixed trip count: predicated, no loop branches
+                const int u = u0 + q;
+                if (u >= u1) break;
                 uint4 w;
                 if (sign_seg) {
                     const uint4 f = s_sgn[rvalid ? srow[u] : 0];
@@ -314,11 +323,10 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
                 const int bseg = sign_seg ? 1 : 0;
                 const uint32_t dacc = tmem + (uint32_t)((t & 1) * kTuN);
                 for (int s = 0; s < ks / 16; ++s)
-                    umma_f16(dacc, umma_desc(sA_a[buf] + 256 * s, 128, ks * 16),
-                             umma_desc(sB_a + (uint32_t)(bseg * ks / 8 + 2 * s) * 128, 128, kcb * 16), idesc,
-                             seg > 0 || s > 0);
-                umma_commit(bar[buf]);
-                if (seg == NSEG_A - 1) umma_commit(abar[t & 1]);
+                    umma_f16(dacc, descA0 + (uint64_t)((buf * sA_stride + 256 * s) >> 4),
+                             descB0 + (uint64_t)((bseg * ks / 8 + 2 * s) * 8), idesc, seg > 0 || s > 0);
+                umma_commit(bar0 + 8 * buf);
+                if (seg == NSEG_A - 1) umma_commit(abar0 + 8 * (uint32_t)(t & 1));
             }
             ++step;
         }
@@ -337,13 +345,13 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
         // a wait ran out (the error word says so): let the copies and MMAs
         // still in flight finish, bounded, before TMEM and smem are released
         for (int b = 0; b < 2; ++b) {
-            mbar_wait_bounded(sbar[b], 0, kWaitLimitNs, p.err, kErrScanWait);
-            mbar_wait_bounded(sbar[b], 1, kWaitLimitNs, p.err, kErrScanWait);
+            mbar_wait_bounded(sbar0 + 8 * b, 0, kWaitLimitNs, p.err, kErrScanWait);
+            mbar_wait_bounded(sbar0 + 8 * b, 1, kWaitLimitNs, p.err, kErrScanWait);
         }
         if (step > 0)
-            mbar_wait_bounded(bar[(step - 1) & 1], (uint32_t)(((step - 1) >> 1) & 1), kWaitLimitNs, p.err, kErrScanWait);
+            mbar_wait_bounded(bar0 + 8 * ((step - 1) & 1), (uint32_t)(((step - 1) >> 1) & 1), kWaitLimitNs, p.err, kErrScanWait);
         if (step >= 2)
-            mbar_wait_bounded(bar[(step - 2) & 1], (uint32_t)(((step - 2) >> 1) & 1), kWaitLimitNs, p.err, kErrScanWait);
+            mbar_wait_bounded(bar0 + 8 * ((step - 2) & 1), (uint32_t)(((step - 2) >> 1) & 1), kWaitLimitNs, p.err, kErrScanWait);
     }
     tc_fence_before_sync();
     __syncthreads();

@@ -42,6 +42,7 @@ struct QuantParams {
     float inv_sqrt_d;
     float guard;          // |y - t_j| below this is re-decided in fp64
     Codebook cb;
+    uint32_t* err;        // device error word (a wait that ran out sets a bit)
 };
 
 // tensor-core quantize for d = m = 128 (x 16-byte aligned rows)
