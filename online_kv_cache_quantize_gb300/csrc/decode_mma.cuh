@@ -21,9 +21,9 @@
 // 32c..32c+31; values: tokens 4c..4c+3) and the value M dimension too (row g
 // holds coordinates 16g..16g+15), so each thread reads contiguous code bits.
 //
-// Tiles are staged per warp in a 4-deep ring of shared-memory buffers, each
-// filled by six bulk (TMA) copies -- one per cache plane, issued by lanes 0..5
-// in one instruction -- that complete on the buffer's mbarrier. The capacity
+// Tiles are staged in a 4-deep ring of CTA-wide shared-memory stages, each
+// holding one tile per warp (64 tokens) and filled by six bulk (TMA) copies
+// -- one per cache plane -- that complete on the stage's mbarrier. The capacity
 // of the cache must be a multiple of 16 so that a tile never leaves its row.
 #pragma once
 
@@ -119,7 +119,8 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
     __shared__ uint32_t klo[KLO ? KL : 1];
     __shared__ uint32_t vlut[VL];
     __shared__ __align__(8) uint2 slut4[16];  // 4 sign bits -> (+-1, +-1), (+-1, +-1) as fp16
-    __shared__ __align__(8) uint64_t s_bar[kMmaWarps][kMmaStages];  // one per ring buffer
+    __shared__ __align__(8) uint64_t s_bar[kMmaStages];  // one per stage of the CTA ring
+    __shared__ uint32_t s_cnt[kMmaStages];                // warps done with a stage, cumulative
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
@@ -129,10 +130,13 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
     if constexpr (KLO)
         for (int i = threadIdx.x; i < KL; i += blockDim.x) klo[i] = p.klut_lo[i];
     for (int i = threadIdx.x; i < VL; i += blockDim.x) vlut[i] = p.vlut[i];
-    const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(&s_bar[warp][0]);
-    if (lane == 0) {
+    const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(&s_bar[0]);
+    if (threadIdx.x == 0) {
 #pragma unroll
-        for (int st = 0; st < kMmaStages; ++st) mbar_init(bar0 + 8 * st, 1);
+        for (int sb = 0; sb < kMmaStages; ++sb) {
+            mbar_init(bar0 + 8 * sb, 1);
+            s_cnt[sb] = 0u;
+        }
         mbar_init_fence();
     }
     if (threadIdx.x < 16) {
@@ -149,42 +153,32 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
     const int nmine = ntiles > warp ? (ntiles - warp + kMmaWarps - 1) / kMmaWarps : 0;
     const int64_t rowbase = ((int64_t)b * p.hkv + kv) * p.capacity;
 
-    unsigned char* wst = stages + warp * kMmaStages * T::BYTES;
-    const uint32_t wst_s = (uint32_t)__cvta_generic_to_shared(wst);
-    // lane k < 6 copies cache plane k of a tile: its source for the warp's
-    // first tile, the byte step to the warp's next tile (64 tokens further
-    // on), its offset inside the buffer and its size
-    const unsigned char* csrc = nullptr;
-    int64_t cstep = 0;
-    uint32_t coff = 0, cbytes = 0;
-    {
-        const int64_t slot0 = rowbase + t0 + 16 * warp;
-        constexpr int64_t TS = 16 * kMmaWarps;  // tokens between a warp's tiles
-        switch (lane) {
-            case 0: csrc = p.kcodes + slot0 * (16 * KB); cstep = TS * 16 * KB; coff = T::OFF_KC; cbytes = T::KC; break;
-            case 1: csrc = p.ksigns + slot0 * 16; cstep = TS * 16; coff = T::OFF_SG; cbytes = T::SG; break;
-            case 2: csrc = reinterpret_cast<const unsigned char*>(p.knorm + slot0); cstep = TS * 2; coff = T::OFF_KN; cbytes = T::NB; break;
-            case 3: csrc = reinterpret_cast<const unsigned char*>(p.krnorm + slot0); cstep = TS * 2; coff = T::OFF_KR; cbytes = T::NB; break;
-            case 4: csrc = p.vcodes + slot0 * (16 * VB); cstep = TS * 16 * VB; coff = T::OFF_VC; cbytes = T::VC; break;
-            case 5: csrc = reinterpret_cast<const unsigned char*>(p.vnorm + slot0); cstep = TS * 2; coff = T::OFF_VN; cbytes = T::NB; break;
-            default: break;
-        }
-    }
-    // fill ring buffer i % stages with the warp's tile i
-    auto issue = [&](int i) {
-        const int sb = i % kMmaStages;
-        const uint32_t bar = bar0 + 8 * sb;
-        if (lane == 0) {
-            fence_proxy_async_smem();  // the warp's earlier reads of this buffer come first
-            mbar_arrive_expect_tx(bar, T::BYTES);
-        }
-        if (lane < 6) bulk_g2s(wst_s + sb * T::BYTES + coff, csrc + i * cstep, cbytes, bar);
+    // ---- CTA ring: stage sb holds one group of kMmaWarps consecutive tiles (64
+    // tokens, warp w's tile at position w), plane by plane: the region of plane
+    // X starts at kMmaWarps * T::OFF_X, so each plane of a group is one bulk
+    // copy. Group i goes to stage i % kMmaStages; the last warp done with a
+    // group (a cumulative counter per stage) refills its stage with group
+    // i + kMmaStages. ----
+    constexpr int SB = kMmaWarps * T::BYTES;
+    const uint32_t stages_s = (uint32_t)__cvta_generic_to_shared(stages);
+    const int ngroups = (ntiles + kMmaWarps - 1) / kMmaWarps;
+    auto issue_group = [&](int gi) {  // one thread
+        const int sb = gi % kMmaStages;
+        const int ntg = min(kMmaWarps, ntiles - kMmaWarps * gi);  // tiles in the group
+        const int64_t slot = rowbase + t0 + 16 * kMmaWarps * gi;
+        const uint32_t dst = stages_s + sb * SB, bar = bar0 + 8 * sb;
+        const uint32_t ntok = 16u * (uint32_t)ntg;
+        fence_proxy_async_smem();  // the warps' reads of this stage come first
+        mbar_arrive_expect_tx(bar, (uint32_t)ntg * T::BYTES);
+        bulk_g2s(dst + kMmaWarps * T::OFF_KC, p.kcodes + slot * (16 * KB), ntok * 16 * KB, bar);
+        bulk_g2s(dst + kMmaWarps * T::OFF_SG, p.ksigns + slot * 16, ntok * 16, bar);
+        bulk_g2s(dst + kMmaWarps * T::OFF_KN, p.knorm + slot, ntok * 2, bar);
+        bulk_g2s(dst + kMmaWarps * T::OFF_KR, p.krnorm + slot, ntok * 2, bar);
+        bulk_g2s(dst + kMmaWarps * T::OFF_VC, p.vcodes + slot * (16 * VB), ntok * 16 * VB, bar);
+        bulk_g2s(dst + kMmaWarps * T::OFF_VN, p.vnorm + slot, ntok * 2, bar);
     };
-
-    __syncwarp();  // this warp's barriers are initialised (lane 0) before any lane uses them
-#pragma unroll
-    for (int sb = 0; sb < kMmaStages; ++sb)
-        if (sb < nmine) issue(sb);  // the first tiles fly while the B fragments are built
+    if (threadIdx.x == 0)
+        for (int gi = 0; gi < kMmaStages && gi < ngroups; ++gi) issue_group(gi);  // in flight during the set-up
 
     // ---- B fragments (static for the CTA), written by the query prep in the
     // order this thread reads them: 16 words of q' and 16 of kappa u ----
@@ -241,14 +235,21 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
         const bool landed = mbar_wait_bounded(bar0 + 8 * (i % kMmaStages), (i / kMmaStages) & 1, kWaitLimitNs,
                                               p.err, kErrScanWait);
         if (!__all_sync(TQ_FULL_MASK, landed)) break;
-        const unsigned char* st = wst + (i % kMmaStages) * T::BYTES;
+        // this warp's tile inside the stage: plane X at kMmaWarps * OFF_X + warp * (size of X)
+        const unsigned char* st = stages + (i % kMmaStages) * SB;
+        const unsigned char* p_kc = st + kMmaWarps * T::OFF_KC + warp * T::KC;
+        const unsigned char* p_sg = st + kMmaWarps * T::OFF_SG + warp * T::SG;
+        const unsigned char* p_kn = st + kMmaWarps * T::OFF_KN + warp * T::NB;
+        const unsigned char* p_kr = st + kMmaWarps * T::OFF_KR + warp * T::NB;
+        const unsigned char* p_vc = st + kMmaWarps * T::OFF_VC + warp * T::VC;
+        const unsigned char* p_vn = st + kMmaWarps * T::OFF_VN + warp * T::NB;
         const int tok0 = t0 + 16 * (warp + kMmaWarps * i);
 
         // ---- keys and signs: D[token][2h+s] ----
         uint32_t kw0[KB + 1], kw1[KB + 1];
         {
-            const uint32_t* r0 = reinterpret_cast<const uint32_t*>(st + T::OFF_KC + g * 16 * KB) + KB * c;
-            const uint32_t* r1 = reinterpret_cast<const uint32_t*>(st + T::OFF_KC + (g + 8) * 16 * KB) + KB * c;
+            const uint32_t* r0 = reinterpret_cast<const uint32_t*>(p_kc + g * 16 * KB) + KB * c;
+            const uint32_t* r1 = reinterpret_cast<const uint32_t*>(p_kc + (g + 8) * 16 * KB) + KB * c;
 #pragma unroll
             for (int w = 0; w < KB; ++w) {
                 kw0[w] = r0[w];
@@ -257,8 +258,8 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
             kw0[KB] = 0u;
             kw1[KB] = 0u;
         }
-        const uint32_t sw0 = reinterpret_cast<const uint32_t*>(st + T::OFF_SG + g * 16)[c];
-        const uint32_t sw1 = reinterpret_cast<const uint32_t*>(st + T::OFF_SG + (g + 8) * 16)[c];
+        const uint32_t sw0 = reinterpret_cast<const uint32_t*>(p_sg + g * 16)[c];
+        const uint32_t sw1 = reinterpret_cast<const uint32_t*>(p_sg + (g + 8) * 16)[c];
         // two accumulator chains per product (even and odd kk) so that
         // consecutive MMAs do not wait on each other
         float dk[2][NT][4], ds[2][NT][4];
@@ -295,9 +296,9 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
             }
         }
 
-        const uint16_t* kn = reinterpret_cast<const uint16_t*>(st + T::OFF_KN);
-        const uint16_t* kr = reinterpret_cast<const uint16_t*>(st + T::OFF_KR);
-        const uint16_t* vn = reinterpret_cast<const uint16_t*>(st + T::OFF_VN);
+        const uint16_t* kn = reinterpret_cast<const uint16_t*>(p_kn);
+        const uint16_t* kr = reinterpret_cast<const uint16_t*>(p_kr);
+        const uint16_t* vn = reinterpret_cast<const uint16_t*>(p_vn);
         const bool v0 = tok0 + g < t1, v1 = tok0 + g + 8 < t1;
         const float kn0 = f16_bits_to_f32(kn[g]), kn1 = f16_bits_to_f32(kn[g + 8]);
         const float kg0 = f16_bits_to_f32(kr[g]), kg1 = f16_bits_to_f32(kr[g + 8]);
@@ -359,7 +360,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
         uint32_t vf[4][3];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const uint32_t* vr = reinterpret_cast<const uint32_t*>(st + T::OFF_VC + (4 * c + j) * 16 * VB);
+            const uint32_t* vr = reinterpret_cast<const uint32_t*>(p_vc + (4 * c + j) * 16 * VB);
             const int bit0 = 16 * VB * g;
             const int w = bit0 >> 5, sh = bit0 & 31;
             const uint32_t x0 = vr[w];
@@ -382,7 +383,15 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
             for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt][mt], a0, a1, a2, a3, bv[nt][0], bv[nt][1]);
         }
         __syncwarp();
-        if (i + kMmaStages < nmine) issue(i + kMmaStages);  // refill the buffer just consumed
+        if (lane == 0) {  // done with this stage; the last warp of the group refills it
+            const int sb = i % kMmaStages;
+            const uint32_t arrivals = (uint32_t)min(kMmaWarps, ntiles - kMmaWarps * i);
+            __threadfence_block();
+            const uint32_t before = atomicAdd(&s_cnt[sb], 1u);
+            // cumulative count: every earlier group of this stage was complete (kMmaWarps arrivals)
+            if (before == (uint32_t)(kMmaWarps * (i / kMmaStages)) + arrivals - 1u && i + kMmaStages < ngroups)
+                issue_group(i + kMmaStages);
+        }
     }
     if (i < nmine) {
         // a copy did not land in time (the error word says so and this
