@@ -189,10 +189,15 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
     // lanes: lane e holds entry e (best first; lanes >= k hold nothing)
     float lsc[kTuQpw];
     int lid[kTuQpw];
+    // the k-th entry of each list (the admission threshold), the same in every lane
+    float thr_s[kTuQpw];
+    int thr_i[kTuQpw];
 #pragma unroll
     for (int jj = 0; jj < kTuQpw; ++jj) {
         lsc[jj] = -INFINITY;
         lid[jj] = 0x7fffffff;
+        thr_s[jj] = -INFINITY;
+        thr_i[jj] = 0x7fffffff;
     }
 
     // norms of a tile's rows: threads 0..127 load tile t + 1's into registers
@@ -231,9 +236,10 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
             const int j = (ecol >> 1) + jj;
             if (j < nq_here) {  // warp-uniform
                 const float sc = scale * (v[2 * jj] + v[2 * jj + 1]);
-                float ts = __shfl_sync(TQ_FULL_MASK, lsc[jj], k - 1);
-                int ti = __shfl_sync(TQ_FULL_MASK, lid[jj], k - 1);
-                unsigned cand = __ballot_sync(TQ_FULL_MASK, evalid && better(sc, id, ts, ti));
+                float ts = thr_s[jj];
+                int ti = thr_i[jj];
+                // cheap filter (>=); the exact rule (equal scores: lower id first) is applied below
+                unsigned cand = __ballot_sync(TQ_FULL_MASK, evalid && sc >= ts);
                 while (cand) {
                     const int src = __ffs(cand) - 1;
                     cand &= cand - 1;
@@ -254,6 +260,8 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
                     ts = __shfl_sync(TQ_FULL_MASK, lsc[jj], k - 1);
                     ti = __shfl_sync(TQ_FULL_MASK, lid[jj], k - 1);
                 }
+                thr_s[jj] = ts;
+                thr_i[jj] = ti;
             }
         }
         return true;
