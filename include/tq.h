@@ -166,13 +166,17 @@ int tq_sign_bytes(int m);                /* per-slot stride of signs, bytes */
  *                        h = i % heads, slot = i * capacity + append_pos[b]
  *                        (device int32 [n / heads]; needs rows == n; a
  *                        position outside [0, capacity) is skipped);
- *   else              -> slot0 + i (checked on the host against the cache). */
+ *   else              -> slot0 + i (checked on the host against the cache).
+ * Kernels: d = 128 (keys m = 128) and n <= 256, one CTA per vector (an append
+ * costs a few microseconds however few vectors it has); d = 128 and more
+ * vectors, 16 vectors per warp with the rotation and S r on the tensor cores;
+ * any other d, one warp per vector. All follow the same precision rules. */
 typedef struct {
     tq_cache cache;
     const tq_rotation* rot; /* uploaded; rot d == cache.d                     */
     const tq_qjl* qjl;      /* PROD: uploaded, m == cache.m, d == cache.d     */
     const void* x;          /* device [n][x_stride] of x_dtype                */
-    int x_dtype;            /* TQ_F32, TQ_BF16 or TQ_F16                      */
+    int x_dtype;            /* TQ_F32 or TQ_BF16                              */
     int64_t x_stride;       /* elements between vectors, >= d                 */
     int64_t n;              /* vectors; 0 is a no-op                          */
     const int64_t* dst_slot;
@@ -251,14 +255,15 @@ tq_status tq_attn_decode_static(const tq_decode_args* a, tq_stream stream);
  * One decode step: append the new token's K and V, then attend.            *
  * ------------------------------------------------------------------------ *
  * The quantize-on-append of [A2A] "How to implement" (every cache update)
- * followed by the decode attention above, in one call. Same results, bit
- * for bit, as tq_quantize_kv(K), tq_quantize_kv(V) and tq_attn_decode on one
- * stream. The two appends run on streams the library owns (two per device,
- * created on first use), concurrently with the query preparation on
- * `stream`; `stream` waits for both before the scan, so all of the step's
- * work is ordered after what precedes the call on `stream` and before what
- * follows it (also under CUDA graph capture). Calls are serialised per
- * process on the host side. */
+ * followed by the decode attention above, in one call, as three launches on
+ * `stream`: the query preparation with both appends (one CTA per query row
+ * and per appended vector), then the scan and the merge, each a programmatic
+ * dependent of the launch before it (it may start while that one finishes
+ * and waits for its results). Same results, bit for bit, as tq_quantize_kv(K),
+ * tq_quantize_kv(V) and tq_attn_decode on one stream when batch * hkv is at
+ * most 256 (up to that count tq_quantize_kv takes the same per-vector
+ * kernel). All of the step's work is ordered after what precedes the call
+ * on `stream` and before what follows it (also under CUDA graph capture). */
 typedef struct {
     tq_decode_args attn;        /* the attention call: caches, q, lengths, out */
     const void* k_new;          /* device [batch*hkv][d] keys of the new token,

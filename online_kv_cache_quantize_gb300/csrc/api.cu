@@ -248,23 +248,32 @@ namespace {
 // comparing the two; see tq_topk_force_simt)
 bool g_topk_simt = false;
 
-// streams and events of tq_decode_step, per device
-constexpr int kMaxStepDevices = 64;
-struct StepStreams {
-    bool ready = false;
-    cudaStream_t sk = nullptr, sv = nullptr;
-    cudaEvent_t fork = nullptr, jk = nullptr, jv = nullptr;
-};
-std::mutex g_step_mutex;
-StepStreams g_step[kMaxStepDevices];
-
-constexpr int64_t kSmallAppend = 64;  // MSE appends of at most this many vectors: warp-per-vector kernel
+// Appends of at most this many vectors (d = 128, keys m = 128) take the
+// CTA-per-vector kernel: a few microseconds of latency however few vectors
+// there are, where the 16-vector tiles of the tensor-core kernel would leave
+// one warp working through a serial chain per tile.
+constexpr int64_t kSmallAppend = 256;
 
 struct QuantLaunch {
     tqk::QuantParams p;
     int dtype = 0, vpl = 1, cb = 1;
-    bool rht = false, prod = false, mma = false;
+    bool rht = false, prod = false, mma = false, small = false;
 };
+
+// the append role of the step-prep launch for one quantize call
+void step_append(const QuantLaunch& L, tqk::StepPrepParams* sp) {
+    if (L.prod) {
+        sp->k = L.p;
+        sp->k_dtype = L.dtype;
+        sp->k_cb = L.cb;
+        sp->k_rht = L.rht ? 1 : 0;
+    } else {
+        sp->v = L.p;
+        sp->v_dtype = L.dtype;
+        sp->v_cb = L.cb;
+        sp->v_rht = L.rht ? 1 : 0;
+    }
+}
 
 struct DecodeLaunch {
     DecodePlan pl;
@@ -343,19 +352,22 @@ tq_status quant_prepare(const tq_quant_args* a, QuantLaunch* L, bool* empty) {
     L->cb = cb;
     p.pi_frag = a->rot->d_pi_frag;
     p.s_frag = prod ? a->qjl->d_s_frag : nullptr;
-    // d = m = 128 with 16-byte aligned rows: the tensor-core kernel; otherwise
-    // the warp-per-vector kernel (any d <= 256). A small MSE append (one token
-    // per KV head) also takes the warp-per-vector kernel, one warp per vector
-    // instead of one mostly empty 16-row tile on one warp; keys keep the
-    // tensor-core kernel, whose S r product the warp-per-vector kernel would
-    // do as a mat-vec over all of S per warp.
-    const bool small_mse = !prod && a->n <= kSmallAppend;
-    L->mma = c.d == 128 && !small_mse && (!prod || (c.m == 128 && p.s_frag)) && (rht || p.pi_frag) &&
+    // d = 128 (keys m = 128): up to kSmallAppend vectors the CTA-per-vector
+    // kernel, more the tensor-core kernel (16-byte aligned rows); otherwise
+    // the warp-per-vector kernel (any d <= 256)
+    L->small = c.d == 128 && (!prod || c.m == 128) && a->n <= kSmallAppend;
+    L->mma = c.d == 128 && !L->small && (!prod || (c.m == 128 && p.s_frag)) && (rht || p.pi_frag) &&
              aligned(a->x, 16) && (a->x_stride * (int64_t)esz) % 16 == 0;
     return TQ_OK;
 }
 
 cudaError_t quant_launch(const QuantLaunch& L, cudaStream_t st) {
+    if (L.small) {
+        tqk::StepPrepParams sp;
+        std::memset(&sp, 0, sizeof(sp));
+        step_append(L, &sp);
+        return tqk::launch_step_prep(sp, st);
+    }
     if (L.mma) return tqk::launch_quantize_mma(L.p, L.dtype, L.rht ? 1 : 0, L.prod ? 1 : 0, L.cb, st);
     if (L.rht) return tqk::launch_quantize_rht(L.p, L.dtype, L.vpl, L.prod ? 1 : 0, L.cb, st);
     return tqk::launch_quantize_dense(L.p, L.dtype, L.vpl, L.prod ? 1 : 0, L.cb, st);
@@ -477,12 +489,18 @@ tq_status decode_prepare(const tq_decode_args* a, void* workspace, size_t ws_byt
     return TQ_OK;
 }
 
-// Query prep on st, then (after st waits on `waits`) the scan and the merge.
-tq_status decode_launch(const DecodeLaunch& D, cudaStream_t st, const cudaEvent_t* waits, int nwaits) {
-    cudaError_t e = tqk::launch_query_prep(D.pp, st);
+// The step-prep launch (the query prep, plus the appends a decode step adds
+// to `sp`), then the scan and the merge, each a programmatic dependent of the
+// launch before it on st.
+tq_status decode_launch(const DecodeLaunch& D, cudaStream_t st, tqk::StepPrepParams* sp) {
+    tqk::StepPrepParams own;
+    if (!sp) {
+        std::memset(&own, 0, sizeof(own));
+        sp = &own;
+    }
+    sp->pp = D.pp;
+    cudaError_t e = tqk::launch_step_prep(*sp, st);
     if (e != cudaSuccess) return cuda_status(e, "tq_attn_decode query prep");
-    for (int i = 0; i < nwaits; ++i)
-        if ((e = cudaStreamWaitEvent(st, waits[i], 0)) != cudaSuccess) return cuda_status(e, "tq_attn_decode join");
     if (D.scan_begin && (e = cudaEventRecord(D.scan_begin, st)) != cudaSuccess)
         return cuda_status(e, "tq_attn_decode scan_begin");
     e = tqk::launch_decode_mma(D.dp, D.kb, D.vb, st);
@@ -610,7 +628,7 @@ tq_status tq_attn_decode(const tq_decode_args* a, void* workspace, size_t ws_byt
     DecodeLaunch D;
     tq_status s = decode_prepare(a, workspace, ws_bytes, &D);
     if (s != TQ_OK) return s;
-    return decode_launch(D, (cudaStream_t)stream, nullptr, 0);
+    return decode_launch(D, (cudaStream_t)stream, nullptr);
 }
 
 size_t tq_score_topk_workspace(const tq_topk_args* a) {
@@ -751,32 +769,13 @@ tq_status tq_decode_step(const tq_step_args* a, void* workspace, size_t ws_bytes
     if ((s = quant_prepare(&qv, &LV, &ev)) != TQ_OK) return s;
     DecodeLaunch D;
     if ((s = decode_prepare(&at, workspace, ws_bytes, &D)) != TQ_OK) return s;
-
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_status(e, "tq_decode_step");
-    if (dev < 0 || dev >= kMaxStepDevices) return fail(TQ_ERR_UNSUPPORTED, "tq_decode_step: device ordinal >= 64");
-    std::lock_guard<std::mutex> lk(g_step_mutex);
-    StepStreams& R = g_step[dev];
-    if (!R.ready) {
-        if ((e = cudaStreamCreateWithFlags(&R.sk, cudaStreamNonBlocking)) != cudaSuccess ||
-            (e = cudaStreamCreateWithFlags(&R.sv, cudaStreamNonBlocking)) != cudaSuccess ||
-            (e = cudaEventCreateWithFlags(&R.fork, cudaEventDisableTiming)) != cudaSuccess ||
-            (e = cudaEventCreateWithFlags(&R.jk, cudaEventDisableTiming)) != cudaSuccess ||
-            (e = cudaEventCreateWithFlags(&R.jv, cudaEventDisableTiming)) != cudaSuccess)
-            return cuda_status(e, "tq_decode_step: creating its streams");
-        R.ready = true;
-    }
-    const cudaStream_t st = (cudaStream_t)stream;
-    if ((e = cudaEventRecord(R.fork, st)) != cudaSuccess || (e = cudaStreamWaitEvent(R.sk, R.fork, 0)) != cudaSuccess ||
-        (e = cudaStreamWaitEvent(R.sv, R.fork, 0)) != cudaSuccess)
-        return cuda_status(e, "tq_decode_step fork");
-    if (!ek && (e = quant_launch(LK, R.sk)) != cudaSuccess) return cuda_status(e, "tq_decode_step append K");
-    if ((e = cudaEventRecord(R.jk, R.sk)) != cudaSuccess) return cuda_status(e, "tq_decode_step join K");
-    if (!ev && (e = quant_launch(LV, R.sv)) != cudaSuccess) return cuda_status(e, "tq_decode_step append V");
-    if ((e = cudaEventRecord(R.jv, R.sv)) != cudaSuccess) return cuda_status(e, "tq_decode_step join V");
-    const cudaEvent_t joins[2] = {R.jk, R.jv};
-    return decode_launch(D, st, joins, 2);
+    // the appends ride in the query prep's launch (one CTA per vector, the
+    // kernel tq_quantize_kv uses for up to kSmallAppend vectors)
+    tqk::StepPrepParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    if (!ek) step_append(LK, &sp);
+    if (!ev) step_append(LV, &sp);
+    return decode_launch(D, (cudaStream_t)stream, &sp);
 }
 
 tq_status tq_device_errors(uint32_t* flags_out, int reset) {

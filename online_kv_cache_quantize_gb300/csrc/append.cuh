@@ -1,0 +1,213 @@
+// Quantize-on-append for a few vectors at a time (the decode step's new
+// token of every KV head): one CTA role of 128 threads per vector, thread i
+// owns coordinate i (d = 128; keys have m = 128 sign rows).
+//
+// Same steps as quantize.cuh (A2A TurboQuant explainer, "Stage 1" and
+// "Stage 2"; Qiita TurboQuant article, "Rotate, then quantize" and "One more
+// stage so attention does not break"): n = ||x||, y = Pi x / n, Lloyd-Max
+// codes, and for keys r = y - c[idx], gamma = ||r||, z = [S r >= 0]. Spread
+// over 128 threads, every step is a few dependent instructions, so a vector
+// costs a few microseconds of latency instead of the serial chain of one
+// warp working through a 16-row tile.
+//
+// Precision as in quantize.cuh: y in fp32 (RHT by butterflies, dense rotation
+// as an fp32 dot product), any coordinate within `guard` of a boundary
+// re-decided from an fp64 dot product, the fp16 norm re-rounded from fp64
+// near a rounding midpoint; S r as an fp32 dot product of each sign row.
+#pragma once
+
+#include "common.cuh"
+#include "tq_launch.h"
+
+namespace tqk {
+
+constexpr int kAppendThreads = 128;
+
+struct AppendSmem {
+    float x[128];       // the input, fp32
+    float y[128];       // butterfly exchange, then the residual r
+    float cent[kMaxLevels];
+    float red[4];
+    double red64[4];
+    uint32_t cw[16];    // packed codes: at most 4 bits x 128 coordinates
+};
+
+// barrier 1 over the 128 threads of an append role (the CTA may hold more
+// threads, which have left by then)
+__device__ __forceinline__ void append_sync() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
+
+// true in every thread when v is true in any of the 128 threads
+__device__ __forceinline__ bool append_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, 1, 128, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u)
+        : "memory");
+    return r != 0;
+}
+
+// sums over the 128 threads in a fixed order (the same value in every thread)
+__device__ __forceinline__ float append_sum(float v, AppendSmem& s) {
+    v = warp_sum(v);
+    if ((threadIdx.x & 31) == 0) s.red[threadIdx.x >> 5] = v;
+    append_sync();
+    const float r = (s.red[0] + s.red[1]) + (s.red[2] + s.red[3]);
+    append_sync();
+    return r;
+}
+__device__ __forceinline__ double append_sum64(double v, AppendSmem& s) {
+    v = warp_sum(v);
+    if ((threadIdx.x & 31) == 0) s.red64[threadIdx.x >> 5] = v;
+    append_sync();
+    const double r = (s.red64[0] + s.red64[1]) + (s.red64[2] + s.red64[3]);
+    append_sync();
+    return r;
+}
+__device__ __forceinline__ float append_max(float v, AppendSmem& s) {
+    v = warp_max(v);
+    if ((threadIdx.x & 31) == 0) s.red[threadIdx.x >> 5] = v;
+    append_sync();
+    const float r = fmaxf(fmaxf(s.red[0], s.red[1]), fmaxf(s.red[2], s.red[3]));
+    append_sync();
+    return r;
+}
+
+// Quantizes vector v of p into its cache slot. Called by threads 0..127 of a
+// CTA, all with the same v. xdtype: 0 f32, 1 bf16; cb: code bits per
+// coordinate (b - 1 for keys); prod: keys (residual signs); rht: the random-
+// sign Walsh-Hadamard rotation, else the dense Pi.
+__device__ __forceinline__ void append_vector(const QuantParams& p, int xdtype, int cb, bool prod, bool rht, int64_t v,
+                                              AppendSmem& s) {
+    constexpr int D = 128;
+    const int i = threadIdx.x, lane = i & 31, warp = i >> 5;
+    const int L = 1 << cb;
+
+    int64_t slot;
+    if (p.dst_slot) {
+        slot = p.dst_slot[v];
+    } else if (p.append_pos) {
+        const int32_t pos = p.append_pos[v / p.heads];
+        slot = (pos >= 0 && pos < p.capacity) ? v * p.capacity + pos : -1;
+    } else {
+        slot = p.slot0 + v;
+    }
+    if (slot < 0 || slot >= p.total_slots) return;  // the same in all 128 threads
+
+    if (i < kMaxLevels) s.cent[i] = p.cb.c[i];
+    if (i < 16) s.cw[i] = 0u;
+    const float xi = xdtype == 1 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.x)[v * p.x_stride + i])
+                                 : reinterpret_cast<const float*>(p.x)[v * p.x_stride + i];
+    s.x[i] = xi;
+
+    // ---- norm, with a rescaled retry when the squares under/overflow ----
+    const float ss = append_sum(xi * xi, s);  // its barriers also publish s.x, s.cent and s.cw
+    float n32 = sqrtf(ss);
+    if (!(ss > 1.0e-30f && ss < 1.0e30f)) {
+        const float amax = append_max(fabsf(xi), s);
+        const float ia = amax > 0.0f ? 1.0f / amax : 0.0f;
+        const float s2 = append_sum((xi * ia) * (xi * ia), s);
+        n32 = amax * sqrtf(s2);
+    }
+    const float inv_n = n32 > 0.0f ? 1.0f / n32 : 0.0f;
+
+    // ---- rotation: y_i = (Pi x)_i / n ----
+    float y;
+    if (rht) {
+        // H (s * x): strides 1..16 across the lanes of a warp, 32 and 64
+        // across the four warps as one 4-point transform through shared memory
+        y = xi * p.sgn[i];
+#pragma unroll
+        for (int h = 1; h < 32; h <<= 1) {
+            const float o = __shfl_xor_sync(TQ_FULL_MASK, y, h);
+            y = (lane & h) ? (o - y) : (y + o);
+        }
+        s.y[i] = y;
+        append_sync();
+        const float v0 = s.y[lane], v1 = s.y[lane + 32], v2 = s.y[lane + 64], v3 = s.y[lane + 96];
+        const float a0 = (warp & 1) ? (v0 - v1) : (v0 + v1);
+        const float a1 = (warp & 1) ? (v2 - v3) : (v2 + v3);
+        y = (warp & 2) ? (a0 - a1) : (a0 + a1);
+        y *= p.inv_sqrt_d * inv_n;
+    } else {
+        // row i of Pi is column i of Pi^T: coalesced over the threads
+        float acc = 0.0f;
+#pragma unroll 16
+        for (int e = 0; e < D; ++e) acc = fmaf(__ldg(p.pit32 + e * D + i), s.x[e], acc);
+        y = acc * inv_n;
+    }
+
+    // ---- bucketize with the guard band ----
+    int k = 0;
+    float dmin = 3.0e38f;
+#pragma unroll
+    for (int t = 0; t < kMaxLevels - 1; ++t) {
+        if (t < L - 1) {
+            k += (y >= p.cb.t[t]) ? 1 : 0;
+            dmin = fminf(dmin, fabsf(y - p.cb.t[t]));
+        }
+    }
+    const bool flag = !(dmin >= p.guard);
+
+    // fp16 norm; near an fp16 rounding midpoint it is re-rounded from fp64
+    uint16_t n16 = f16_bits_sat(n32);
+    bool nclose = false;
+    if (n32 > 0.0f && n32 < 65504.0f) {
+        const float dn = __half2float(__float2half_rd(n32));
+        const float up = __half2float(__float2half_ru(n32));
+        nclose = dn != up && fabsf(n32 - 0.5f * (dn + up)) <= 1.0e-6f * n32;
+    }
+
+    // ---- fp64 re-decision (rare) ----
+    if (append_any(flag || nclose)) {
+        const double n64 = sqrt(append_sum64((double)xi * (double)xi, s));
+        if (nclose) n16 = __half_as_ushort(__double2half(fmin(n64, 65504.0)));
+        if (flag) {
+            double part = 0.0;
+            if (rht) {
+                for (int e = 0; e < D; ++e) {
+                    const double t = (double)p.sgn[e] * (double)s.x[e];
+                    part += (__popc(i & e) & 1) ? -t : t;
+                }
+            } else {
+                for (int e = 0; e < D; ++e) part = fma(p.pi64[(size_t)i * D + e], (double)s.x[e], part);
+            }
+            double y64 = 0.0;
+            if (n64 > 0.0) y64 = rht ? part / (sqrt((double)D) * n64) : part / n64;
+            k = 0;
+#pragma unroll
+            for (int t = 0; t < kMaxLevels - 1; ++t)
+                if (t < L - 1) k += (y64 >= p.cb.t64[t]) ? 1 : 0;
+            y = (float)y64;
+        }
+    }
+
+    // ---- pack: code bits cb*i .. cb*i + cb - 1 of the LSB-first stream ----
+    const int bit = cb * i;
+    atomicOr(&s.cw[bit >> 5], (uint32_t)k << (bit & 31));
+    if ((bit & 31) + cb > 32) atomicOr(&s.cw[(bit >> 5) + 1], (uint32_t)k >> (32 - (bit & 31)));
+
+    float gamma = 0.0f;
+    if (prod) {
+        // r = y - c[idx], gamma = ||r||, z_j = [(S r)_j >= 0]
+        const float r = y - s.cent[k];
+        gamma = sqrtf(append_sum(r * r, s));
+        s.y[i] = r;  // the butterfly reads of s.y finished before append_sum's barriers
+        append_sync();
+        // row j = i of S is column i of S^T: coalesced over the threads
+        float z = 0.0f;
+#pragma unroll 16
+        for (int e = 0; e < D; ++e) z = fmaf(__ldg(p.st32 + e * D + i), s.y[e], z);
+        const uint32_t zb = __ballot_sync(TQ_FULL_MASK, z >= 0.0f);  // sign bits 32 warp .. +31
+        if (lane == 0) reinterpret_cast<uint32_t*>(p.signs + slot * (int64_t)p.sign_stride)[warp] = zb;
+    } else {
+        append_sync();  // the packed words are complete
+    }
+    if (i < (p.code_stride >> 2)) reinterpret_cast<uint32_t*>(p.codes + slot * (int64_t)p.code_stride)[i] = s.cw[i];
+    if (i == 0) {
+        p.norm[slot] = n16;
+        if (prod) p.rnorm[slot] = f16_bits_sat(gamma);
+    }
+}
+
+}  // namespace tqk

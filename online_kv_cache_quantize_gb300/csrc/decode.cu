@@ -1,7 +1,41 @@
-// Decode attention launches: query preparation, split-K scan dispatch, merge.
+// Decode attention launches: query preparation (fused with the decode
+// step's appends), split-K scan dispatch, merge.
+#include "append.cuh"
 #include "decode.cuh"
 
 namespace tqk {
+
+// The decode step's work before its scan in one launch: query prep rows
+// (decode.cuh) and the appended key and value vectors (append.cuh).
+__global__ void __launch_bounds__(kPrepWarps * 32) step_prep_kernel(const __grid_constant__ StepPrepParams p) {
+    // the scan that follows on the stream may be scheduled now: it waits for
+    // this grid to complete before it reads anything written here
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    __shared__ AppendSmem s;
+    int64_t b = blockIdx.x;
+    if (b < p.pp.rows) {
+        prep_row<4>(p.pp, b);
+        return;
+    }
+    b -= p.pp.rows;
+    if (threadIdx.x >= kAppendThreads) return;
+    if (b < p.k.n) {
+        append_vector(p.k, p.k_dtype, p.k_cb, true, p.k_rht != 0, b, s);
+        return;
+    }
+    b -= p.k.n;
+    if (b < p.v.n) append_vector(p.v, p.v_dtype, p.v_cb, false, p.v_rht != 0, b, s);
+}
+
+cudaError_t launch_step_prep(const StepPrepParams& p, cudaStream_t s) {
+    const int64_t ctas = p.pp.rows + p.k.n + p.v.n;
+    if (ctas <= 0) return cudaSuccess;
+    if (ctas > 0x7fffffff || (p.pp.rows > 0 && p.pp.d != 128) || (p.k.n > 0 && (p.k.d != 128 || p.k.m != 128)) ||
+        (p.v.n > 0 && p.v.d != 128))
+        return cudaErrorInvalidValue;
+    step_prep_kernel<<<(unsigned)ctas, kPrepWarps * 32, 0, s>>>(p);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_query_prep(const PrepParams& p, cudaStream_t s) {
     if (p.rows <= 0) return cudaSuccess;

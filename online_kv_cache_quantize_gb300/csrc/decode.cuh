@@ -35,19 +35,18 @@ __device__ __forceinline__ void write_frag(const PrepParams& p, int64_t row, con
 }
 
 // ---------------------------------------------------------------------------
-// One CTA per query row. Lane l of every warp owns outputs VPL*l..VPL*l+VPL-1
+// One CTA (256 threads) per query row. Lane l of every warp owns outputs VPL*l..VPL*l+VPL-1
 // and warp w accumulates the inputs j = w, w+8, ...: the rows of the
 // transposed matrices are read with independent loads, all in flight at once,
 // and the 8 partial vectors are summed through shared memory.
 // ---------------------------------------------------------------------------
 template <int VPL>
-__global__ void __launch_bounds__(kPrepWarps * 32) query_prep_kernel(const __grid_constant__ PrepParams p) {
+__device__ __forceinline__ void prep_row(const PrepParams& p, int64_t row) {
     constexpr int DMAX = 32 * VPL;
     __shared__ float s_x[256];
     __shared__ float s_y[256];
     __shared__ float s_part[kPrepWarps][256];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
-    const int64_t row = blockIdx.x;
     const int d = p.d;
     for (int i = tid; i < d; i += blockDim.x) {
         s_x[i] = p.q_dtype == 1 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.q)[row * d + i])
@@ -167,6 +166,11 @@ __global__ void __launch_bounds__(kPrepWarps * 32) query_prep_kernel(const __gri
         __syncthreads();
         write_frag(p, row, s_y, s_x, tid);
     }
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(kPrepWarps * 32) query_prep_kernel(const __grid_constant__ PrepParams p) {
+    prep_row<VPL>(p, blockIdx.x);
 }
 
 // ---------------------------------------------------------------------------

@@ -145,6 +145,10 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
         slut4[e].y = ((e & 4) ? pos : neg) | (((e & 8) ? pos : neg) << 16);
     }
 
+    // launched as a programmatic dependent of the query prep (which also
+    // appends the step's new tokens): everything below reads what it wrote
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+
     // a length outside [0, min(capacity, max_seq_len)] is clamped into it
     const int L = max(0, (int)min((int64_t)p.seq_lens[b], min(p.capacity, (int64_t)p.max_seq_len)));
     const int t0 = split * p.chunk;
@@ -451,6 +455,27 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
             out[D + 1] = z;
         }
     }
+}
+
+template <int KB, int VB, int G>
+size_t decode_mma_smem();
+
+// Launches the scan as a programmatic dependent of the launch before it on
+// the stream: its CTAs may become resident and set up while that launch runs,
+// and wait for it (griddepcontrol.wait) before reading anything.
+template <int KB, int VB, int G>
+cudaError_t launch_decode_mma_t(const DecodeParams& p, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.n_splits, (unsigned)p.hkv, (unsigned)p.batch);
+    cfg.blockDim = dim3(kMmaWarps * 32);
+    cfg.dynamicSmemBytes = decode_mma_smem<KB, VB, G>();
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<KB, VB, G>, p);
 }
 
 template <int KB, int VB, int G>

@@ -5,9 +5,7 @@ namespace tqk {
 
 template <int KB, int VB>
 static cudaError_t go(const DecodeParams& p, cudaStream_t s) {
-    dim3 grid(p.n_splits, p.hkv, p.batch), block(kMmaWarps * 32);
-    decode_mma_kernel<KB, VB, 1><<<grid, block, decode_mma_smem<KB, VB, 1>(), s>>>(p);
-    return cudaGetLastError();
+    return launch_decode_mma_t<KB, VB, 1>(p, s);
 }
 
 template <int KB>

@@ -75,6 +75,21 @@ constexpr int kFragWords = 256;
 
 cudaError_t launch_query_prep(const PrepParams& p, cudaStream_t s);
 
+// One launch for the work a decode step does before its scan: the query prep
+// of pp.rows query rows (d = 128) and the quantize-on-append of k.n key and
+// v.n value vectors (d = m = 128), one CTA per query row or vector. Any part
+// may be empty. The scan launched right after it on the same stream may
+// start early (programmatic dependent launch) and waits for it to finish.
+struct StepPrepParams {
+    PrepParams pp;
+    QuantParams k, v;
+    int k_dtype, v_dtype;  // 0 f32, 1 bf16
+    int k_cb, v_cb;        // code bits per coordinate (keys b - 1)
+    int k_rht, v_rht;
+};
+
+cudaError_t launch_step_prep(const StepPrepParams& p, cudaStream_t s);
+
 struct DecodeParams {
     const uint32_t* frag; // [B*Hq][kFragWords] B operands written by the query prep
     int batch, hq, hkv, d, m, group;
