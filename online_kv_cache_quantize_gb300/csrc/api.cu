@@ -198,7 +198,7 @@ tq_status plan_decode(const tq_decode_args* a, DecodePlan* pl) {
     const size_t rows = (size_t)a->batch * a->hq;
     pl->off_frag = 0;
     pl->off_part = round_up(rows * tqk::kFragWords * sizeof(uint32_t), 256);
-    pl->total = pl->off_part + round_up(rows * (size_t)splits * (a->d + 2) * sizeof(float), 256);
+    pl->total = pl->off_part + round_up(rows * (size_t)splits * (a->d + tqk::kPartPad) * sizeof(float), 256);
     return TQ_OK;
 }
 
@@ -339,6 +339,7 @@ tq_status quant_prepare(const tq_quant_args* a, QuantLaunch* L, bool* empty) {
     p.pi64 = a->rot->d_pi64;
     p.sgn = a->rot->d_sign;
     p.st32 = prod ? a->qjl->d_st32 : nullptr;
+    p.s16 = prod ? a->qjl->d_s16 : nullptr;
     p.d = c.d;
     p.m = prod ? c.m : 0;
     p.inv_sqrt_d = (float)(1.0 / std::sqrt((double)c.d));
@@ -427,6 +428,7 @@ tq_status decode_prepare(const tq_decode_args* a, void* workspace, size_t ws_byt
     pp.rht = a->rot->kind == TQ_ROT_RHT;
     pp.inv_sqrt_d = (float)(1.0 / std::sqrt((double)a->d));
     pp.st32 = a->qjl->d_st32;
+    pp.s16 = a->qjl->d_s16;
     pp.frag = frag;
     pp.qjl_scale = (float)(std::sqrt(M_PI / 2.0) / a->k.m);
 
@@ -588,6 +590,13 @@ tq_status tq_qjl_to_device(tq_qjl* q) {
     if ((s = upload(&q->d_st32, st)) != TQ_OK) return s;
     if ((s = upload(&q->d_s32, s32)) != TQ_OK) return s;
     if (m == 128 && d == 128) {
+        // the append kernel's copy of S: 16-byte unit (u, j) = S[j][8u .. 8u+7] at u * 128 + j
+        std::vector<uint16_t> s16((size_t)m * d);
+        for (int u = 0; u < d / 8; ++u)
+            for (int j = 0; j < m; ++j)
+                for (int e = 0; e < 8; ++e)
+                    s16[((size_t)u * m + j) * 8 + e] = bf16_bits_of(q->s[(size_t)j * d + 8 * u + e]);
+        if ((s = upload(&q->d_s16, s16)) != TQ_OK) return s;
         auto frag = mma_b_fragments([&](int o, int k) { return bf16_bits_of(q->s[(size_t)o * d + k]); });
         if ((s = upload(&q->d_s_frag, frag)) != TQ_OK) return s;
     }
@@ -603,6 +612,7 @@ tq_status tq_free_qjl(tq_qjl* q) {
         cudaSetDevice(q->device);
         cudaFree(q->d_st32);
         cudaFree(q->d_s32);
+        cudaFree(q->d_s16);
         cudaFree(q->d_s_frag);
         if (cur >= 0) cudaSetDevice(cur);
     }
@@ -775,6 +785,7 @@ tq_status tq_decode_step(const tq_step_args* a, void* workspace, size_t ws_bytes
     std::memset(&sp, 0, sizeof(sp));
     if (!ek) step_append(LK, &sp);
     if (!ev) step_append(LV, &sp);
+    D.dp.append_pos = a->append_pos;
     return decode_launch(D, (cudaStream_t)stream, &sp);
 }
 

@@ -21,23 +21,28 @@
 
 namespace tqk {
 
-constexpr int kAppendThreads = 128;
+// threads of a CTA of the decode step's prep launch (one query row or one
+// appended vector per CTA)
+constexpr int kStepThreads = 128;
 
-struct AppendSmem {
+// shared memory of one CTA of that launch, whichever its role
+struct StepSmem {
+    uint4 s[16 * 128];  // S as bf16, 16-byte unit (q, j) = S[j][8q .. 8q+7] at q * 128 + j
     float x[128];       // the input, fp32
-    float y[128];       // butterfly exchange, then the residual r
+    __align__(16) float y[128];  // butterfly exchange, then the residual r (append) or q' (query)
+    float qp[128];      // query: q' = Pi q
+    float u[128];       // query: u = S q'
     float cent[kMaxLevels];
     float red[4];
     double red64[4];
     uint32_t cw[16];    // packed codes: at most 4 bits x 128 coordinates
 };
 
-// barrier 1 over the 128 threads of an append role (the CTA may hold more
-// threads, which have left by then)
-__device__ __forceinline__ void append_sync() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
+// barrier 1 over the 128 threads of the CTA
+__device__ __forceinline__ void step_sync() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
 
 // true in every thread when v is true in any of the 128 threads
-__device__ __forceinline__ bool append_any(bool v) {
+__device__ __forceinline__ bool step_any(bool v) {
     uint32_t r;
     asm volatile(
         "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, 1, 128, q;\n selp.u32 %0, 1, 0, p;\n}\n"
@@ -48,37 +53,93 @@ __device__ __forceinline__ bool append_any(bool v) {
 }
 
 // sums over the 128 threads in a fixed order (the same value in every thread)
-__device__ __forceinline__ float append_sum(float v, AppendSmem& s) {
+__device__ __forceinline__ float step_sum(float v, StepSmem& s) {
     v = warp_sum(v);
     if ((threadIdx.x & 31) == 0) s.red[threadIdx.x >> 5] = v;
-    append_sync();
+    step_sync();
     const float r = (s.red[0] + s.red[1]) + (s.red[2] + s.red[3]);
-    append_sync();
+    step_sync();
     return r;
 }
-__device__ __forceinline__ double append_sum64(double v, AppendSmem& s) {
+__device__ __forceinline__ double step_sum64(double v, StepSmem& s) {
     v = warp_sum(v);
     if ((threadIdx.x & 31) == 0) s.red64[threadIdx.x >> 5] = v;
-    append_sync();
+    step_sync();
     const double r = (s.red64[0] + s.red64[1]) + (s.red64[2] + s.red64[3]);
-    append_sync();
+    step_sync();
     return r;
 }
-__device__ __forceinline__ float append_max(float v, AppendSmem& s) {
+__device__ __forceinline__ float step_max(float v, StepSmem& s) {
     v = warp_max(v);
     if ((threadIdx.x & 31) == 0) s.red[threadIdx.x >> 5] = v;
-    append_sync();
+    step_sync();
     const float r = fmaxf(fmaxf(s.red[0], s.red[1]), fmaxf(s.red[2], s.red[3]));
-    append_sync();
+    step_sync();
     return r;
 }
 
-// Quantizes vector v of p into its cache slot. Called by threads 0..127 of a
-// CTA, all with the same v. xdtype: 0 f32, 1 bf16; cb: code bits per
+// Starts the copy of S (m = d = 128, bf16, unit layout above) into s.s:
+// sixteen 16-byte cp.async per thread, one commit group. The caller waits
+// (cp.async.wait_group 0) and then synchronises before reading s.s.
+__device__ __forceinline__ void stage_s(const uint16_t* s16, StepSmem& s) {
+    const uint32_t dst = (uint32_t)__cvta_generic_to_shared(s.s);
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+        const int unit = u * kStepThreads + (int)threadIdx.x;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst + 16 * unit),
+                     "l"(reinterpret_cast<const uint4*>(s16) + unit)
+                     : "memory");
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+
+// (S v)_j for j = threadIdx.x: row j of the staged S (exact bf16 -> fp32)
+// against v in shared memory, summed in coordinate order
+__device__ __forceinline__ float s_row_dot(const StepSmem& s, const float* v) {
+    const int j = threadIdx.x;
+    float z = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        const uint4 sr = s.s[q * kStepThreads + j];
+        const float4 r0 = *reinterpret_cast<const float4*>(v + 8 * q);
+        const float4 r1 = *reinterpret_cast<const float4*>(v + 8 * q + 4);
+        z = fmaf(__uint_as_float(sr.x << 16), r0.x, z);
+        z = fmaf(__uint_as_float(sr.x & 0xffff0000u), r0.y, z);
+        z = fmaf(__uint_as_float(sr.y << 16), r0.z, z);
+        z = fmaf(__uint_as_float(sr.y & 0xffff0000u), r0.w, z);
+        z = fmaf(__uint_as_float(sr.z << 16), r1.x, z);
+        z = fmaf(__uint_as_float(sr.z & 0xffff0000u), r1.y, z);
+        z = fmaf(__uint_as_float(sr.w << 16), r1.z, z);
+        z = fmaf(__uint_as_float(sr.w & 0xffff0000u), r1.w, z);
+    }
+    return z;
+}
+
+// (H t)_i for i = threadIdx.x over the 128 threads of the CTA (t is thread
+// i's element, H the Sylvester Walsh-Hadamard matrix): strides 1..16 across
+// the lanes of a warp, 32 and 64 as one 4-point transform over the four warps
+// through s.y. The caller writes s.y again only after a later barrier.
+__device__ __forceinline__ float wht128(float t, StepSmem& s) {
+    const int i = threadIdx.x, lane = i & 31, warp = i >> 5;
+#pragma unroll
+    for (int h = 1; h < 32; h <<= 1) {
+        const float o = __shfl_xor_sync(TQ_FULL_MASK, t, h);
+        t = (lane & h) ? (o - t) : (t + o);
+    }
+    s.y[i] = t;
+    step_sync();
+    const float v0 = s.y[lane], v1 = s.y[lane + 32], v2 = s.y[lane + 64], v3 = s.y[lane + 96];
+    const float a0 = (warp & 1) ? (v0 - v1) : (v0 + v1);
+    const float a1 = (warp & 1) ? (v2 - v3) : (v2 + v3);
+    return (warp & 2) ? (a0 - a1) : (a0 + a1);
+}
+
+// Quantizes vector v of p into its cache slot. Called by the 128 threads of
+// a CTA, all with the same v. xdtype: 0 f32, 1 bf16; cb: code bits per
 // coordinate (b - 1 for keys); prod: keys (residual signs); rht: the random-
 // sign Walsh-Hadamard rotation, else the dense Pi.
 __device__ __forceinline__ void append_vector(const QuantParams& p, int xdtype, int cb, bool prod, bool rht, int64_t v,
-                                              AppendSmem& s) {
+                                              StepSmem& s) {
     constexpr int D = 128;
     const int i = threadIdx.x, lane = i & 31, warp = i >> 5;
     const int L = 1 << cb;
@@ -94,6 +155,11 @@ __device__ __forceinline__ void append_vector(const QuantParams& p, int xdtype, 
     }
     if (slot < 0 || slot >= p.total_slots) return;  // the same in all 128 threads
 
+    // keys: S (32 KB of bf16) is copied into shared memory now and used last,
+    // so the copy hides behind the norm, rotation and bucketize; 16-byte unit
+    // (q, j) = S[j][8q .. 8q + 7] sits at unit q * 128 + j in both places, so
+    // the copy is contiguous and thread j's reads of its row are conflict-free
+    if (prod) stage_s(p.s16, s);
     if (i < kMaxLevels) s.cent[i] = p.cb.c[i];
     if (i < 16) s.cw[i] = 0u;
     const float xi = xdtype == 1 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.x)[v * p.x_stride + i])
@@ -101,12 +167,12 @@ __device__ __forceinline__ void append_vector(const QuantParams& p, int xdtype, 
     s.x[i] = xi;
 
     // ---- norm, with a rescaled retry when the squares under/overflow ----
-    const float ss = append_sum(xi * xi, s);  // its barriers also publish s.x, s.cent and s.cw
+    const float ss = step_sum(xi * xi, s);  // its barriers also publish s.x, s.cent and s.cw
     float n32 = sqrtf(ss);
     if (!(ss > 1.0e-30f && ss < 1.0e30f)) {
-        const float amax = append_max(fabsf(xi), s);
+        const float amax = step_max(fabsf(xi), s);
         const float ia = amax > 0.0f ? 1.0f / amax : 0.0f;
-        const float s2 = append_sum((xi * ia) * (xi * ia), s);
+        const float s2 = step_sum((xi * ia) * (xi * ia), s);
         n32 = amax * sqrtf(s2);
     }
     const float inv_n = n32 > 0.0f ? 1.0f / n32 : 0.0f;
@@ -114,25 +180,11 @@ __device__ __forceinline__ void append_vector(const QuantParams& p, int xdtype, 
     // ---- rotation: y_i = (Pi x)_i / n ----
     float y;
     if (rht) {
-        // H (s * x): strides 1..16 across the lanes of a warp, 32 and 64
-        // across the four warps as one 4-point transform through shared memory
-        y = xi * p.sgn[i];
-#pragma unroll
-        for (int h = 1; h < 32; h <<= 1) {
-            const float o = __shfl_xor_sync(TQ_FULL_MASK, y, h);
-            y = (lane & h) ? (o - y) : (y + o);
-        }
-        s.y[i] = y;
-        append_sync();
-        const float v0 = s.y[lane], v1 = s.y[lane + 32], v2 = s.y[lane + 64], v3 = s.y[lane + 96];
-        const float a0 = (warp & 1) ? (v0 - v1) : (v0 + v1);
-        const float a1 = (warp & 1) ? (v2 - v3) : (v2 + v3);
-        y = (warp & 2) ? (a0 - a1) : (a0 + a1);
-        y *= p.inv_sqrt_d * inv_n;
+        y = wht128(xi * p.sgn[i], s) * (p.inv_sqrt_d * inv_n);
     } else {
         // row i of Pi is column i of Pi^T: coalesced over the threads
         float acc = 0.0f;
-#pragma unroll 16
+#pragma unroll 32
         for (int e = 0; e < D; ++e) acc = fmaf(__ldg(p.pit32 + e * D + i), s.x[e], acc);
         y = acc * inv_n;
     }
@@ -159,8 +211,8 @@ __device__ __forceinline__ void append_vector(const QuantParams& p, int xdtype, 
     }
 
     // ---- fp64 re-decision (rare) ----
-    if (append_any(flag || nclose)) {
-        const double n64 = sqrt(append_sum64((double)xi * (double)xi, s));
+    if (step_any(flag || nclose)) {
+        const double n64 = sqrt(step_sum64((double)xi * (double)xi, s));
         if (nclose) n16 = __half_as_ushort(__double2half(fmin(n64, 65504.0)));
         if (flag) {
             double part = 0.0;
@@ -191,17 +243,15 @@ __device__ __forceinline__ void append_vector(const QuantParams& p, int xdtype, 
     if (prod) {
         // r = y - c[idx], gamma = ||r||, z_j = [(S r)_j >= 0]
         const float r = y - s.cent[k];
-        gamma = sqrtf(append_sum(r * r, s));
-        s.y[i] = r;  // the butterfly reads of s.y finished before append_sum's barriers
-        append_sync();
-        // row j = i of S is column i of S^T: coalesced over the threads
-        float z = 0.0f;
-#pragma unroll 16
-        for (int e = 0; e < D; ++e) z = fmaf(__ldg(p.st32 + e * D + i), s.y[e], z);
+        gamma = sqrtf(step_sum(r * r, s));
+        s.y[i] = r;  // the butterfly reads of s.y finished before step_sum's barriers
+        asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+        step_sync();  // r and every thread's part of S
+        const float z = s_row_dot(s, s.y);  // (S r)_i
         const uint32_t zb = __ballot_sync(TQ_FULL_MASK, z >= 0.0f);  // sign bits 32 warp .. +31
         if (lane == 0) reinterpret_cast<uint32_t*>(p.signs + slot * (int64_t)p.sign_stride)[warp] = zb;
     } else {
-        append_sync();  // the packed words are complete
+        step_sync();  // the packed words are complete
     }
     if (i < (p.code_stride >> 2)) reinterpret_cast<uint32_t*>(p.codes + slot * (int64_t)p.code_stride)[i] = s.cw[i];
     if (i == 0) {

@@ -7,18 +7,56 @@ namespace tqk {
 
 // The decode step's work before its scan in one launch: query prep rows
 // (decode.cuh) and the appended key and value vectors (append.cuh).
-__global__ void __launch_bounds__(kPrepWarps * 32) step_prep_kernel(const __grid_constant__ StepPrepParams p) {
+
+// Query prep of one row (d = m = 128) by the 128 threads of a CTA, thread i
+// owning coordinate i: q' = Pi q (random-sign Walsh-Hadamard by butterflies,
+// or the dense Pi), u = S q' from S staged in shared memory, and the scan's
+// B operands (the same words as write_frag in decode.cuh).
+__device__ __forceinline__ void prep_row128(const PrepParams& p, int64_t row, StepSmem& s) {
+    constexpr int D = 128;
+    const int i = threadIdx.x;
+    const bool want_u = p.st32 != nullptr;
+    if (want_u) stage_s(p.s16, s);  // lands while q' is formed
+    const float qi = p.q_dtype == 1 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.q)[row * D + i])
+                                    : reinterpret_cast<const float*>(p.q)[row * D + i];
+    float y;
+    if (p.rht) {
+        y = wht128(qi * p.sgn[i], s) * p.inv_sqrt_d;
+    } else {
+        s.x[i] = qi;
+        step_sync();
+        float acc = 0.0f;
+#pragma unroll 32
+        for (int e = 0; e < D; ++e) acc = fmaf(__ldg(p.pit32 + e * D + i), s.x[e], acc);
+        y = acc;
+    }
+    s.qp[i] = y;
+    if (p.qprime) p.qprime[row * D + i] = y;
+    if (want_u) {
+        asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+        step_sync();  // q' and all of S
+        const float u = s_row_dot(s, s.qp);
+        if (p.u) p.u[row * D + i] = u;
+        s.u[i] = u;
+    }
+    if (p.frag) {
+        step_sync();
+        write_frag(p, row, s.qp, want_u ? s.u : nullptr, i);
+        write_frag(p, row, s.qp, want_u ? s.u : nullptr, i + kStepThreads);
+    }
+}
+
+__global__ void __launch_bounds__(kStepThreads) step_prep_kernel(const __grid_constant__ StepPrepParams p) {
     // the scan that follows on the stream may be scheduled now: it waits for
     // this grid to complete before it reads anything written here
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-    __shared__ AppendSmem s;
+    __shared__ StepSmem s;
     int64_t b = blockIdx.x;
     if (b < p.pp.rows) {
-        prep_row<4>(p.pp, b);
+        prep_row128(p.pp, b, s);
         return;
     }
     b -= p.pp.rows;
-    if (threadIdx.x >= kAppendThreads) return;
     if (b < p.k.n) {
         append_vector(p.k, p.k_dtype, p.k_cb, true, p.k_rht != 0, b, s);
         return;
@@ -30,10 +68,11 @@ __global__ void __launch_bounds__(kPrepWarps * 32) step_prep_kernel(const __grid
 cudaError_t launch_step_prep(const StepPrepParams& p, cudaStream_t s) {
     const int64_t ctas = p.pp.rows + p.k.n + p.v.n;
     if (ctas <= 0) return cudaSuccess;
-    if (ctas > 0x7fffffff || (p.pp.rows > 0 && p.pp.d != 128) || (p.k.n > 0 && (p.k.d != 128 || p.k.m != 128)) ||
+    if (ctas > 0x7fffffff || (p.pp.rows > 0 && (p.pp.d != 128 || (p.pp.st32 && (p.pp.m != 128 || !p.pp.s16)))) ||
+        (p.k.n > 0 && (p.k.d != 128 || p.k.m != 128 || !p.k.s16)) ||
         (p.v.n > 0 && p.v.d != 128))
         return cudaErrorInvalidValue;
-    step_prep_kernel<<<(unsigned)ctas, kPrepWarps * 32, 0, s>>>(p);
+    step_prep_kernel<<<(unsigned)ctas, kStepThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 

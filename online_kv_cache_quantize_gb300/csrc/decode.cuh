@@ -175,55 +175,84 @@ __global__ void __launch_bounds__(kPrepWarps * 32) query_prep_kernel(const __gri
 
 // ---------------------------------------------------------------------------
 // Merge the splits of one query row and un-rotate: o = Pi^T (a / Z).
-// CTA of 1024 threads = (1024 / d) groups of d threads; group k runs an
-// online (max, sum, a) merge over the splits s = k, k + groups, ... in one
-// pass, then the groups are merged through shared memory. d in {64, 128, 256}.
+// CTA of 1024 threads = 1024 / (d / 4) groups of d / 4 threads, thread c4 of
+// a group owning coordinates 4 c4 .. 4 c4 + 3. Group k merges the splits
+// k, k + groups, ... (online max, sum and a), loading kCombinePer of them at
+// once so that their loads are in flight together; then the groups are
+// merged through shared memory. d in {64, 128, 256}.
 // ---------------------------------------------------------------------------
 constexpr int kCombineThreads = 1024;
+constexpr int kCombinePer = 4;
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ CombineParams p) {
-    __shared__ float s_m[kCombineThreads];
-    __shared__ float s_z[kCombineThreads];
-    __shared__ float s_v[kCombineThreads];
+    __shared__ float s_m[64];
+    __shared__ float s_z[64];
+    __shared__ __align__(16) float s_v[kCombineThreads * 4];
+    __shared__ float s_a[256];
     // launched as a programmatic dependent of the scan: wait for its grid to
     // complete and its partials to be visible (a no-op on a plain launch)
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
-    __shared__ float s_a[256];
     const int row = blockIdx.x, tid = threadIdx.x, d = p.d, ns = p.n_splits;
-    const int groups = kCombineThreads / d;
-    const int i = tid % d, grp = tid / d;
-    const float* base = p.partial + (int64_t)row * ns * (d + 2);
+    const int tpr = d >> 2, groups = kCombineThreads / tpr;
+    const int grp = tid / tpr, c4 = tid % tpr;
+    const int stride = d + kPartPad;
+    const float* base = p.partial + (int64_t)row * ns * stride;
 
-    float m = -INFINITY, z = 0.0f, a = 0.0f;
-#pragma unroll 4
-    for (int s = grp; s < ns; s += groups) {
-        const float* ps = base + (int64_t)s * (d + 2);
-        const float ms = ps[d], zs = ps[d + 1], as = ps[i];
-        if (ms > m) {
-            const float sc = (m == -INFINITY) ? 0.0f : exp2f(m - ms);
-            z *= sc;
-            a *= sc;
-            m = ms;
+    float m = -INFINITY, z = 0.0f;
+    float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int s0 = grp; s0 < ns; s0 += groups * kCombinePer) {
+        float4 av[kCombinePer];
+        float mv[kCombinePer], zv[kCombinePer];
+#pragma unroll
+        for (int k = 0; k < kCombinePer; ++k) {
+            const int s = s0 + k * groups;
+            mv[k] = -INFINITY;
+            zv[k] = 0.0f;
+            av[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (s < ns) {
+                const float* ps = base + (int64_t)s * stride;
+                av[k] = *reinterpret_cast<const float4*>(ps + 4 * c4);
+                mv[k] = ps[d];
+                zv[k] = ps[d + 1];
+            }
         }
-        if (ms != -INFINITY) {
-            const float w = exp2f(ms - m);
-            z = fmaf(zs, w, z);
-            a = fmaf(as, w, a);
+#pragma unroll
+        for (int k = 0; k < kCombinePer; ++k) {
+            const float ms = mv[k];
+            if (ms > m) {
+                const float sc = (m == -INFINITY) ? 0.0f : exp2f(m - ms);
+                z *= sc;
+                a.x *= sc;
+                a.y *= sc;
+                a.z *= sc;
+                a.w *= sc;
+                m = ms;
+            }
+            if (ms != -INFINITY) {
+                const float w = exp2f(ms - m);
+                z = fmaf(zv[k], w, z);
+                a.x = fmaf(av[k].x, w, a.x);
+                a.y = fmaf(av[k].y, w, a.y);
+                a.z = fmaf(av[k].z, w, a.z);
+                a.w = fmaf(av[k].w, w, a.w);
+            }
         }
     }
-    s_m[tid] = m;
-    s_z[tid] = z;
-    s_v[tid] = a;
+    *reinterpret_cast<float4*>(&s_v[grp * d + 4 * c4]) = a;
+    if (c4 == 0) {
+        s_m[grp] = m;
+        s_z[grp] = z;
+    }
     __syncthreads();
     if (tid < d) {
         float mstar = -INFINITY;
-        for (int k = 0; k < groups; ++k) mstar = fmaxf(mstar, s_m[k * d + tid]);
+        for (int k = 0; k < groups; ++k) mstar = fmaxf(mstar, s_m[k]);
         float zt = 0.0f, at = 0.0f;
         for (int k = 0; k < groups; ++k) {
-            const float mk = s_m[k * d + tid];
+            const float mk = s_m[k];
             if (mk == -INFINITY) continue;
             const float w = exp2f(mk - mstar);
-            zt = fmaf(s_z[k * d + tid], w, zt);
+            zt = fmaf(s_z[k], w, zt);
             at = fmaf(s_v[k * d + tid], w, at);
         }
         s_a[tid] = (zt > 0.0f) ? at / zt : 0.0f;
@@ -231,27 +260,36 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
     __syncthreads();
     float o = 0.0f;
     if (p.rht) {
-        // o = s * (H a) / sqrt(d): in-place Walsh-Hadamard on shared memory
-        for (int h = 1; h < d; h <<= 1) {
-            float v = 0.0f, w = 0.0f;
-            if (tid < d) {
-                v = s_a[tid];
-                w = s_a[tid ^ h];
+        // o = s * (H a) / sqrt(d): strides 1..16 across the lanes of a warp,
+        // the rest as one (d / 32)-point transform over the first d / 32
+        // warps through shared memory (s_v is free again)
+        if (tid < d) {
+            const int lane = tid & 31, w = tid >> 5;
+            float y = s_a[tid];
+#pragma unroll
+            for (int h = 1; h < 32; h <<= 1) {
+                const float t = __shfl_xor_sync(TQ_FULL_MASK, y, h);
+                y = (lane & h) ? (t - y) : (y + t);
             }
-            __syncthreads();
-            if (tid < d) s_a[tid] = (tid & h) ? (w - v) : (v + w);
-            __syncthreads();
+            s_v[tid] = y;
+            asm volatile("bar.sync 1, %0;\n" ::"r"(d) : "memory");  // the first d threads only
+            float acc = 0.0f;
+            for (int k = 0; k < (d >> 5); ++k) {
+                const float t = s_v[lane + 32 * k];
+                acc += (__popc(w & k) & 1) ? -t : t;
+            }
+            o = acc * p.sgn[tid] * p.inv_sqrt_d;
         }
-        if (tid < d) o = s_a[tid] * p.sgn[tid] * p.inv_sqrt_d;
     } else {
-        // o_i = sum_k Pi[k][i] a_k, the k range split over the groups
+        // o_i = sum_k Pi[k][i] a_k, the k range split over 1024 / d groups of d threads
+        const int ug = kCombineThreads / d, i = tid % d, ugrp = tid / d;
         float part = 0.0f;
 #pragma unroll 4
-        for (int k = grp; k < d; k += groups) part = fmaf(__ldg(p.pi32 + (size_t)k * d + i), s_a[k], part);
+        for (int k = ugrp; k < d; k += ug) part = fmaf(__ldg(p.pi32 + (size_t)k * d + i), s_a[k], part);
         s_v[tid] = part;
         __syncthreads();
         if (tid < d)
-            for (int k = 0; k < groups; ++k) o += s_v[k * d + tid];
+            for (int k = 0; k < ug; ++k) o += s_v[k * d + tid];
     }
     if (tid < d) {
         if (p.out_dtype == 1)

@@ -145,10 +145,6 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
         slut4[e].y = ((e & 4) ? pos : neg) | (((e & 8) ? pos : neg) << 16);
     }
 
-    // launched as a programmatic dependent of the query prep (which also
-    // appends the step's new tokens): everything below reads what it wrote
-    asm volatile("griddepcontrol.wait;\n" ::: "memory");
-
     // a length outside [0, min(capacity, max_seq_len)] is clamped into it
     const int L = max(0, (int)min((int64_t)p.seq_lens[b], min(p.capacity, (int64_t)p.max_seq_len)));
     const int t0 = split * p.chunk;
@@ -181,8 +177,22 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
         bulk_g2s(dst + kMmaWarps * T::OFF_VC, p.vcodes + slot * (16 * VB), ntok * 16 * VB, bar);
         bulk_g2s(dst + kMmaWarps * T::OFF_VN, p.vnorm + slot, ntok * 2, bar);
     };
-    if (threadIdx.x == 0)
-        for (int gi = 0; gi < kMmaStages && gi < ngroups; ++gi) issue_group(gi);  // in flight during the set-up
+    // Launched as a programmatic dependent of the query prep, which writes the
+    // B operands and, in a decode step, appends the new token of each batch
+    // row at append_pos[b]: griddepcontrol.wait returns once that launch has
+    // completed. A split whose tiles do not hold the appended slot reads
+    // nothing the prep writes into the cache, so its first copies go out
+    // before the wait and overlap the prep.
+    bool early = true;
+    if (p.append_pos != nullptr) {
+        const int ap = p.append_pos[b];
+        early = !(ap >= t0 && ap < t0 + 16 * ntiles);
+    }
+    if (early && threadIdx.x == 0)
+        for (int gi = 0; gi < kMmaStages && gi < ngroups; ++gi) issue_group(gi);
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    if (!early && threadIdx.x == 0)
+        for (int gi = 0; gi < kMmaStages && gi < ngroups; ++gi) issue_group(gi);
 
     // ---- B fragments (static for the CTA), written by the query prep in the
     // order this thread reads them: 16 words of q' and 16 of kappa u ----
@@ -448,7 +458,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
             a = fmaf(s_acc[(w * G + h) * D + ci], wt, a);
         }
         const int row = b * p.hq + (p.use_table ? (int)p.head_table[kv * G + h] : kv * G + h);
-        float* out = p.partial + ((int64_t)row * p.n_splits + split) * (D + 2);
+        float* out = p.partial + ((int64_t)row * p.n_splits + split) * (D + kPartPad);
         out[ci] = a;
         if (ci == 0) {
             out[D] = mstar;

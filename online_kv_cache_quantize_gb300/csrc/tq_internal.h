@@ -35,6 +35,7 @@ struct tq_qjl {
     int device = -1;
     float* d_st32 = nullptr;    // S^T row-major fp32 (ST[i][j] = S_ji), [d][m]
     float* d_s32 = nullptr;     // S row-major fp32 [m][d]
+    uint16_t* d_s16 = nullptr;  // m = d = 128: S as bf16 bits (exact), 16-byte unit (q, j) = S[j][8q .. 8q+7] at q * 128 + j
     uint2v* d_s_frag = nullptr;   // m = d = 128: S (exact bf16) in mma fragment order
 };
 

@@ -36,6 +36,7 @@ struct QuantParams {
     const double* pi64;   // Pi [d][d] fp64
     const float* sgn;     // RHT signs [d]
     const float* st32;    // S^T [d][m]
+    const uint16_t* s16;  // m = d = 128: S as bf16 bits, 16-byte unit (q, j) = S[j][8q .. 8q+7] at q * 128 + j
     const void* pi_frag;  // d = 128 dense: Pi^T limbs in mma fragment order
     const void* s_frag;   // m = d = 128: S in mma fragment order
     int d, m;
@@ -62,6 +63,7 @@ struct PrepParams {
     int rht;
     float inv_sqrt_d;
     const float* st32;    // S^T [d][m] or NULL (no u)
+    const uint16_t* s16;  // m = d = 128: S as bf16 in the append kernel's unit layout (the decode prep)
     float* qprime;        // [rows][d] or NULL
     float* u;             // [rows][m] or NULL
     // d = m = 128 decode: the scan's B operands of every query row, fp16
@@ -72,6 +74,10 @@ struct PrepParams {
 };
 
 constexpr int kFragWords = 256;
+
+// floats per split partial row of the decode scan: a[0..d), M at d, Z at d + 1,
+// padded so every row starts on a 16-byte boundary
+constexpr int kPartPad = 4;
 
 cudaError_t launch_query_prep(const PrepParams& p, cudaStream_t s);
 
@@ -94,6 +100,10 @@ struct DecodeParams {
     const uint32_t* frag; // [B*Hq][kFragWords] B operands written by the query prep
     int batch, hq, hkv, d, m, group;
     const int32_t* seq_lens;
+    // decode step: the slot its prep launch appends in each batch row (the
+    // scan waits for that launch before copying the tile holding it); NULL
+    // when the prep appends nothing
+    const int32_t* append_pos;
     const int16_t* heads_of_kv;  // nullptr -> kv*G + j; else HOST-built table in params
     int16_t head_table[256];     // heads_of_kv table by value: [hkv][G]
     int use_table;
@@ -110,7 +120,7 @@ struct DecodeParams {
     float scale_log2;     // softmax scale * log2(e)
     int n_splits;
     int chunk;            // tokens per split
-    float* partial;       // [B*Hq][n_splits][d+2]
+    float* partial;       // [B*Hq][n_splits][d + kPartPad]: a, then M and Z
     float* logits;        // optional [B*Hq][max_seq_len]
     int max_seq_len;
     // tensor-core scan: 2-coordinate fp16 pair tables of lam * centroid

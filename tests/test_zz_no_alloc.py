@@ -49,7 +49,7 @@ def test_static_scratch_rejects_oversized_arguments():
     build.build()
     d, bsz, hkv, hq, cap = 128, 8, 32, 256, 2048
     rot, qjl = P.handles(d, "rht")
-    # 2048 query rows x 32 splits x 130 floats = 34 MB of scratch: more than the array holds
+    # 2048 query rows x 32 splits x 132 floats = 35 MB of scratch: more than the array holds
     kc = B.Cache("prod", 3, d, rows=bsz * hkv, capacity=cap)
     vc = B.Cache("mse", 3, d, rows=bsz * hkv, capacity=cap)
     q = torch.zeros((bsz, hq, d), device="cuda")
