@@ -338,6 +338,10 @@ tq_status tq_selftest_bounded_wait(uint32_t limit_us, tq_stream stream);
  * b[n][k]^T, a and b device fp16 row-major, d device fp32 row-major, n in
  * {16, 32, 64, 128}, k a multiple of 16 up to 128; one CTA on `stream`. */
 tq_status tq_selftest_umma_gemm(const void* a, const void* b, float* d, int n, int k, tq_stream stream);
+/* The same product with the A operand taken from tensor memory: a is written
+ * into TMEM with tcgen05.st (row r in lane r, two fp16 along k per 32-bit
+ * column) and tcgen05.mma reads it there, as the search kernel does. */
+tq_status tq_selftest_umma_gemm_tmem_a(const void* a, const void* b, float* d, int n, int k, tq_stream stream);
 
 #ifdef __cplusplus
 }

@@ -98,6 +98,8 @@ _SIGS = {
     "tq_selftest_bounded_wait": (_STATUS, [ctypes.c_uint32, ctypes.c_void_p]),
     "tq_selftest_umma_gemm": (_STATUS, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_void_p]),
+    "tq_selftest_umma_gemm_tmem_a": (_STATUS, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_void_p]),
 }
 
 EXPORTED = tuple(_SIGS)
@@ -376,11 +378,12 @@ def tq_selftest_bounded_wait(limit_us, stream=None):
     _check(load().tq_selftest_bounded_wait(limit_us, _stream_ptr(stream)), "tq_selftest_bounded_wait")
 
 
-def tq_selftest_umma_gemm(a, b, d, stream=None):
-    """d[128][n] = a[128][k] @ b[n][k]^T on the tcgen05 tensor-core path (fp16 in, fp32 out)."""
+def tq_selftest_umma_gemm(a, b, d, stream=None, a_in_tmem=False):
+    """d[128][n] = a[128][k] @ b[n][k]^T on the tcgen05 tensor-core path (fp16 in, fp32 out);
+    a_in_tmem: the MMA reads A from tensor memory instead of shared memory."""
     n, k = b.shape
-    _check(load().tq_selftest_umma_gemm(a.data_ptr(), b.data_ptr(), d.data_ptr(), n, k, _stream_ptr(stream)),
-           "tq_selftest_umma_gemm")
+    fn = load().tq_selftest_umma_gemm_tmem_a if a_in_tmem else load().tq_selftest_umma_gemm
+    _check(fn(a.data_ptr(), b.data_ptr(), d.data_ptr(), n, k, _stream_ptr(stream)), "tq_selftest_umma_gemm")
 
 
 def _topk_struct(queries, db, n_db, rot, qjl, k, ids, scores):

@@ -804,7 +804,8 @@ tq_status tq_device_errors(uint32_t* flags_out, int reset) {
              : TQ_OK;
 }
 
-tq_status tq_selftest_umma_gemm(const void* a, const void* b, float* d, int n, int k, tq_stream stream) {
+namespace {
+tq_status umma_selftest(const void* a, const void* b, float* d, int n, int k, int a_tmem, tq_stream stream) {
     if (!a || !b || !d) return fail(TQ_ERR_INVALID_ARG, "tq_selftest_umma_gemm: NULL operand");
     if ((n != 16 && n != 32 && n != 64 && n != 128) || k < 16 || k > 128 || k % 16)
         return fail(TQ_ERR_UNSUPPORTED, "tq_selftest_umma_gemm: n must be 16/32/64/128 and k a multiple of 16 up to 128");
@@ -812,8 +813,17 @@ tq_status tq_selftest_umma_gemm(const void* a, const void* b, float* d, int n, i
     uint32_t* word = nullptr;
     cudaError_t e = tqk::device_error_word(&word);
     if (e != cudaSuccess) return cuda_status(e, "tq_selftest_umma_gemm");
-    e = tqk::launch_umma_selftest(a, b, d, n, k, word, (cudaStream_t)stream);
+    e = tqk::launch_umma_selftest(a, b, d, n, k, a_tmem, word, (cudaStream_t)stream);
     return cuda_status(e, "tq_selftest_umma_gemm");
+}
+}  // namespace
+
+tq_status tq_selftest_umma_gemm(const void* a, const void* b, float* d, int n, int k, tq_stream stream) {
+    return umma_selftest(a, b, d, n, k, 0, stream);
+}
+
+tq_status tq_selftest_umma_gemm_tmem_a(const void* a, const void* b, float* d, int n, int k, tq_stream stream) {
+    return umma_selftest(a, b, d, n, k, 1, stream);
 }
 
 tq_status tq_selftest_bounded_wait(uint32_t limit_us, tq_stream stream) {

@@ -13,31 +13,44 @@
 // parts, lam * kappa * u against the sign part). The score is
 // n * (D[row][2j] + D[row][2j + 1]) / lam.
 //
-// Per CTA: 32 queries (B resident in shared memory for the whole chunk) and a
-// chunk of database rows. Per 128-row tile: the packed codes and signs land
-// in a staging buffer by bulk copy (double-buffered, one tile ahead); 256
-// threads de-quantize each A segment into a core-matrix tile (two buffers,
-// so the next segment is built while the tensor core runs on the previous
-// one); one thread issues the MMAs into a 128 x 64 fp32 TMEM accumulator;
-// the epilogue reads it back with tcgen05.ld and keeps per-warp top-k lists,
-// merged per query at the end into the chunk's candidates.
+// Warp-specialised CTA (32 queries, a chunk of database rows, 128-row tiles):
+//  * control warp: bulk copies of each tile's packed codes and signs into a
+//    ring of staging buffers, and the MMAs (tcgen05.mma, A read from tensor
+//    memory, B = the queries resident in shared memory) into one of two
+//    128 x 64 fp32 TMEM accumulators, committed to mbarriers;
+//  * 8 producer warps: de-quantize each A segment of a tile straight into
+//    tensor memory (tcgen05.st; row r in TMEM lane r, two fp16 per column)
+//    through a ring of segment slots, so the de-quantized tile never touches
+//    shared memory;
+//  * 8 epilogue warps: read a finished accumulator (tcgen05.ld) and keep
+//    per-warp top-k lists of their rows, merged per query at the end of the
+//    chunk into its candidates.
+// The roles hand over through mbarriers (full / empty pairs); every wait is
+// bounded, and a wait that runs out stops the CTA after draining what it has
+// in flight.
 #include "pipeline.cuh"
 #include "tcgen05.cuh"
 #include "topk.cuh"
 
 namespace tqk {
 
-constexpr int kTuRows = 128;    // database rows per tile (MMA M)
-constexpr int kTuQ = 32;        // queries per CTA
-constexpr int kTuN = 2 * kTuQ;  // MMA N: hi and lo column per query
-constexpr int kTuWarps = 16;
+constexpr int kTuRows = 128;            // database rows per tile (MMA M, TMEM lanes)
+constexpr int kTuQ = 32;                // queries per CTA
+constexpr int kTuN = 2 * kTuQ;          // MMA N: hi and lo column per query
+constexpr int kTuProd = 8;              // producer warps
+constexpr int kTuEpi = 8;               // epilogue warps
+constexpr int kTuCtl = kTuProd + kTuEpi;  // the control warp's index
+constexpr int kTuWarps = kTuCtl + 1;
 constexpr int kTuThreads = 32 * kTuWarps;
-constexpr int kTuQpw = kTuQ / (kTuWarps / 4);  // queries per warp in the epilogue (8)
-constexpr int kTuParts = kTuThreads / kTuRows;  // threads per row in the de-quantize (4)
-constexpr int kTuSmemLimit = 227 * 1024 - 4096;  // dynamic part; static tables stay below 4 KB
+constexpr int kTuQpw = kTuQ / 2;        // queries per epilogue warp
+constexpr int kTuStages = 4;            // staging buffers
+constexpr int kTuASlots = 3;            // A segment slots in TMEM
+constexpr uint32_t kTuCols = 512;       // TMEM columns held by the CTA
+constexpr int kTuSmemLimit = 227 * 1024 - 4096;  // dynamic part; static part below 4 KB
+constexpr int kTuSmemMin = 116 * 1024;  // at most one CTA per SM: it holds all of TMEM
 
 struct TuLayout {
-    size_t b, a0, a1, st0, st1, sgn, nrm, ls, li, total;
+    size_t b, st, sgn, ls, li, total;
     int kcb, stage_bytes;
 };
 
@@ -45,19 +58,23 @@ __host__ __device__ inline TuLayout tu_layout(int ks, int nseg_b, int code_strid
     TuLayout L;
     L.kcb = nseg_b * ks;
     const size_t bb = (size_t)kTuN * L.kcb * 2;
-    const size_t ab = (size_t)kTuRows * ks * 2;
-    L.stage_bytes = kTuRows * (code_stride + sign_stride) + 16;  // + slack for the 8-byte reads at a row end
+    // + 128: a half-row read may run past the last row's codes (into unused bytes)
+    L.stage_bytes = (kTuRows * (code_stride + sign_stride) + 128 + 127) / 128 * 128;
     L.b = 0;
-    L.a0 = bb;
-    L.a1 = L.a0 + ab;
-    L.st0 = L.a1 + ab;
-    L.st1 = L.st0 + ((L.stage_bytes + 127) / 128) * 128;
-    L.sgn = L.st1 + ((L.stage_bytes + 127) / 128) * 128;
-    L.nrm = L.sgn + 256 * 16;  // [2 buffers][128 rows] norm, then [2][128] gamma (fp32)
-    L.ls = L.nrm + 4 * kTuRows * 4;
-    L.li = L.ls + (size_t)kTuWarps * kTuQpw * k * 4;
-    L.total = L.li + (size_t)kTuWarps * kTuQpw * k * 4;
+    L.st = (bb + 127) / 128 * 128;
+    L.sgn = L.st + (size_t)kTuStages * L.stage_bytes;
+    L.ls = L.sgn + 256 * 16;
+    L.li = L.ls + (size_t)kTuEpi * kTuQpw * k * 4;
+    L.total = L.li + (size_t)kTuEpi * kTuQpw * k * 4;
     return L;
+}
+
+// bits [8 * byte0, 8 * byte0 + nb) of a little-endian word array (folded to
+// constants inside unrolled loops)
+__device__ __forceinline__ uint32_t tu_bits(const uint32_t* w, int bit0, int nb) {
+    const int W = bit0 >> 5, S = bit0 & 31;
+    const uint32_t v = (S == 0) ? w[W] : __funnelshift_r(w[W], w[W + 1], S);
+    return nb >= 32 ? v : (v & ((1u << nb) - 1u));
 }
 
 template <int CB, bool PROD, bool LO>
@@ -65,11 +82,13 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
     constexpr int NSEG_A = 1 + (LO ? 1 : 0) + (PROD ? 1 : 0);
     constexpr int NSEG_B = 1 + (PROD ? 1 : 0);
     constexpr int NT = 1 << (2 * CB);
+    constexpr int HW = 4 * CB;  // words of codes per half row (8 pairs of 16 codes)
     extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ __align__(8) uint64_t s_bar[2];    // MMA completion per A buffer
-    __shared__ __align__(8) uint64_t s_sbar[2];   // staging copies per buffer
-    __shared__ __align__(8) uint64_t s_abar[2];   // all MMAs of a tile done, per TMEM accumulator
+    __shared__ __align__(8) uint64_t s_stf[kTuStages], s_ste[kTuStages];  // staging full / empty
+    __shared__ __align__(8) uint64_t s_af[kTuASlots], s_ae[kTuASlots];    // A slot full / empty
+    __shared__ __align__(8) uint64_t s_cf[2], s_ce[2];                    // accumulator full / empty
     __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
     __shared__ uint32_t s_ktab[NT];
     __shared__ uint32_t s_klo[LO ? NT : 1];
 
@@ -78,16 +97,12 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
     const int cs = p.code_stride, ss = PROD ? p.sign_stride : 0;
     const TuLayout Lo = tu_layout(ks, NSEG_B, cs, ss, k);
     const int kcb = Lo.kcb;
+    const int npair = ks / 16;  // pairs of 8-coordinate units per segment
+    const uint32_t scols = (uint32_t)(ks / 2);  // TMEM columns per A segment
     unsigned char* sB = smem + Lo.b;
-    // buffer x of a pair at base + x * stride (no arrays indexed at run time)
-    unsigned char* const sA0 = smem + Lo.a0;
-    const size_t sA_stride = Lo.a1 - Lo.a0;
-    unsigned char* const sSt0 = smem + Lo.st0;
-    const size_t sSt_stride = Lo.st1 - Lo.st0;
+    unsigned char* const sSt0 = smem + Lo.st;
     const uint4* s_sgn = reinterpret_cast<const uint4*>(smem + Lo.sgn);
-    float* s_nrm = reinterpret_cast<float*>(smem + Lo.nrm);          // [2][128]: n of each row
-    float* s_gam = s_nrm + 2 * kTuRows;                              // [2][128]: gamma (PROD)
-    float* s_ls = reinterpret_cast<float*>(smem + Lo.ls);  // [warps][queries per warp][k]
+    float* s_ls = reinterpret_cast<float*>(smem + Lo.ls);  // [epilogue warp][query][k]
     int* s_li = reinterpret_cast<int*>(smem + Lo.li);
 
     const int chunk = blockIdx.x;
@@ -95,9 +110,10 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
     const int nq_here = min(kTuQ, p.nq - q0);
     const int64_t r0 = (int64_t)chunk * p.chunk_rows;
     const int64_t r1 = min(r0 + p.chunk_rows, p.n_db);
+    const int64_t ntile = r1 > r0 ? (r1 - r0 + kTuRows - 1) / kTuRows : 0;
     const float lam_kappa = p.qjl_scale / p.inv_lam;
 
-    // ---- tables, lists, B tile ----
+    // ---- tables, B tile, barriers, TMEM (all threads) ----
     for (int i = tid; i < NT; i += blockDim.x) {
         s_ktab[i] = p.ktab[i];
         if constexpr (LO) s_klo[i] = p.ktab_lo[i];
@@ -113,278 +129,326 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
     }
     // B tile: row 2j + s holds query j's hi (s = 0) or lo (s = 1) fp16 half;
     // columns [0, ks) are q', [ks, 2 ks) lam * kappa * u (PROD)
-    for (int j = 0; j < kTuQ; ++j) {
+    for (int e = tid; e < kTuQ * (kcb / 2); e += blockDim.x) {
+        const int j = e / (kcb / 2), col = 2 * (e % (kcb / 2));
         const bool qv = j < nq_here;
-        const float* qp = p.qprime + (int64_t)(q0 + (qv ? j : 0)) * d;
-        const float* up = PROD ? p.u + (int64_t)(q0 + (qv ? j : 0)) * m : nullptr;
-        for (int col = 2 * tid; col < kcb; col += 2 * blockDim.x) {
-            const bool sgn = col >= ks;
-            const int i = sgn ? col - ks : col;
-            const int lim = sgn ? m : d;
-            const float* src = sgn ? up : qp;
-            const float sc_ = sgn ? lam_kappa : 1.0f;
-            const float v0 = (qv && i < lim) ? sc_ * src[i] : 0.0f;
-            const float v1 = (qv && i + 1 < lim) ? sc_ * src[i + 1] : 0.0f;
-            *reinterpret_cast<uint32_t*>(sB + umma_off(2 * j, col, kcb)) = half_split(v0, 0) | (half_split(v1, 0) << 16);
-            *reinterpret_cast<uint32_t*>(sB + umma_off(2 * j + 1, col, kcb)) =
-                half_split(v0, 1) | (half_split(v1, 1) << 16);
-        }
+        const bool sgn = col >= ks;
+        const int i = sgn ? col - ks : col;
+        const int lim = sgn ? m : d;
+        const float* src = sgn ? p.u + (int64_t)(q0 + (qv ? j : 0)) * m : p.qprime + (int64_t)(q0 + (qv ? j : 0)) * d;
+        const float sc_ = sgn ? lam_kappa : 1.0f;
+        const float v0 = (qv && i < lim) ? sc_ * src[i] : 0.0f;
+        const float v1 = (qv && i + 1 < lim) ? sc_ * src[i + 1] : 0.0f;
+        *reinterpret_cast<uint32_t*>(sB + umma_off(2 * j, col, kcb)) = half_split(v0, 0) | (half_split(v1, 0) << 16);
+        *reinterpret_cast<uint32_t*>(sB + umma_off(2 * j + 1, col, kcb)) = half_split(v0, 1) | (half_split(v1, 1) << 16);
     }
-    // mbarrier x of each pair at base + 8 x
-    const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(&s_bar[0]);
-    const uint32_t sbar0 = (uint32_t)__cvta_generic_to_shared(&s_sbar[0]);
-    const uint32_t abar0 = (uint32_t)__cvta_generic_to_shared(&s_abar[0]);
+    const uint32_t stf0 = (uint32_t)__cvta_generic_to_shared(&s_stf[0]);
+    const uint32_t ste0 = (uint32_t)__cvta_generic_to_shared(&s_ste[0]);
+    const uint32_t af0 = (uint32_t)__cvta_generic_to_shared(&s_af[0]);
+    const uint32_t ae0 = (uint32_t)__cvta_generic_to_shared(&s_ae[0]);
+    const uint32_t cf0 = (uint32_t)__cvta_generic_to_shared(&s_cf[0]);
+    const uint32_t ce0 = (uint32_t)__cvta_generic_to_shared(&s_ce[0]);
     if (tid == 0) {
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-            mbar_init(bar0 + 8 * x, 1);
-            mbar_init(sbar0 + 8 * x, 1);
-            mbar_init(abar0 + 8 * x, 1);
+        for (int x = 0; x < kTuStages; ++x) {
+            mbar_init(stf0 + 8 * x, 1);
+            mbar_init(ste0 + 8 * x, kTuProd);
         }
+        for (int x = 0; x < kTuASlots; ++x) {
+            mbar_init(af0 + 8 * x, kTuProd);
+            mbar_init(ae0 + 8 * x, 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(cf0 + 8 * x, 1);
+            mbar_init(ce0 + 8 * x, kTuEpi);
+        }
+        s_abort = 0;
         mbar_init_fence();
     }
-    if (warp == 0) {  // two accumulators: tile t's MMAs run while tile t - 1's epilogue reads the other
-        tmem_alloc((uint32_t)__cvta_generic_to_shared(&s_tmem), 2 * kTuN);
+    if (warp == kTuCtl) {
+        tmem_alloc((uint32_t)__cvta_generic_to_shared(&s_tmem), kTuCols);
         tmem_relinquish();
     }
-    fence_proxy_async_smem();
+    fence_proxy_async_smem();  // the B tile is read by the tensor core
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = s_tmem;
+    volatile int* abort_flag = &s_abort;
 
-    // staging of tile t (codes then signs of its rows) into buffer t & 1, by thread 0
-    const int64_t ntile = r1 > r0 ? (r1 - r0 + kTuRows - 1) / kTuRows : 0;
+    // staging of tile t (codes then signs of its rows) into buffer t % kTuStages
     auto stage = [&](int64_t t) {
         const int64_t t0 = r0 + t * kTuRows;
         const int rows = (int)min((int64_t)kTuRows, r1 - t0);
-        const int b = (int)(t & 1);
-        const uint32_t dst = (uint32_t)__cvta_generic_to_shared(sSt0 + b * sSt_stride);
-        const uint32_t sb_ = sbar0 + 8 * b;
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(sb_, (uint32_t)rows * (cs + ss));
-        bulk_g2s(dst, p.codes + t0 * cs, (uint32_t)rows * cs, sb_);
-        if constexpr (PROD) bulk_g2s(dst + kTuRows * cs, p.signs + t0 * ss, (uint32_t)rows * ss, sb_);
+        const int b = (int)(t % kTuStages);
+        const uint32_t dst = (uint32_t)__cvta_generic_to_shared(sSt0 + (size_t)b * Lo.stage_bytes);
+        const uint32_t bar = stf0 + 8 * b;
+        mbar_arrive_expect_tx(bar, (uint32_t)rows * (cs + ss));
+        bulk_g2s(dst, p.codes + t0 * cs, (uint32_t)rows * cs, bar);
+        if constexpr (PROD) bulk_g2s(dst + kTuRows * cs, p.signs + t0 * ss, (uint32_t)rows * ss, bar);
     };
-    if (tid == 0 && ntile > 0) stage(0);
 
-    const uint32_t idesc = umma_idesc_f16(kTuRows, kTuN);
-    const uint32_t sA_a0 = (uint32_t)__cvta_generic_to_shared(sA0);
-    // MMA descriptors of k-step 0; k-step s starts 256 s bytes (16 s in the
-    // descriptor's address field) further on
-    const uint64_t descA0 = umma_desc(sA_a0, 128, ks * 16);
-    const uint64_t descB0 = umma_desc((uint32_t)__cvta_generic_to_shared(sB), 128, kcb * 16);
-    // de-quantize: warp w takes rows 8w .. 8w+7 (lane & 7) and a quarter of their
-    // 8-coordinate units (lane >> 3): a quarter warp stores 8 rows of one unit
-    // (all banks) and the warp reads 8 rows x 4 units of the staged codes
-    const int r = 8 * warp + (lane & 7);
-    const int part = lane >> 3;
-    const int units = ks / 8, upp = (units + kTuParts - 1) / kTuParts;
-    const int u0 = part * upp, u1 = min(units, u0 + upp);
-    const int er = 32 * (warp & 3) + lane;  // epilogue: this thread's row (TMEM lane)
-    const int ecol = 2 * kTuQpw * (warp >> 2);  // ... and its 2 * kTuQpw columns (kTuQpw queries)
-    int step = 0;
-    bool ok = true;
-    // this warp's top-k list of each of its kTuQpw queries, spread over the
-    // lanes: lane e holds entry e (best first; lanes >= k hold nothing)
-    float lsc[kTuQpw];
-    int lid[kTuQpw];
-    // the k-th entry of each list (the admission threshold), the same in every lane
-    float thr_s[kTuQpw];
-    int thr_i[kTuQpw];
+    if (warp < kTuProd) {
+        // ================= producers =================
+        // thread: row r (its TMEM lane) and half h of every segment (pairs
+        // 8h .. 8h + 7 of 16-code pairs; pairs >= npair are not written)
+        const int r = 32 * (warp & 3) + lane;
+        const int h = warp >> 2;
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        uint16_t g_next = 0;
+        if (PROD && ntile > 0 && r0 + r < r1) g_next = p.rnorm[r0 + r];
+        for (int64_t t = 0; t < ntile; ++t) {
+            const int b = (int)(t % kTuStages);
+            if (!mbar_wait_bounded(stf0 + 8 * b, (uint32_t)((t / kTuStages) & 1), kWaitLimitNs, p.err, kErrScanWait)) {
+                *abort_flag = 1;
+                break;
+            }
+            const bool rvalid = r0 + t * kTuRows + r < r1;
+            const unsigned char* st = sSt0 + (size_t)b * Lo.stage_bytes;
+            // this thread's half row of codes (16 CB bytes) and of sign bits (16 bytes)
+            uint32_t cw[HW + 1];
+            {
+                const uint4* src = reinterpret_cast<const uint4*>(st + (size_t)r * cs + 16 * CB * h);
 #pragma unroll
-    for (int jj = 0; jj < kTuQpw; ++jj) {
-        lsc[jj] = -INFINITY;
-        lid[jj] = 0x7fffffff;
-        thr_s[jj] = -INFINITY;
-        thr_i[jj] = 0x7fffffff;
-    }
-
-    // norms of a tile's rows: threads 0..127 load tile t + 1's into registers
-    // during tile t and publish them into the other smem buffer at its end
-    auto load_norms = [&](int64_t t, uint16_t& nv, uint16_t& gv) {
-        const int64_t row = r0 + t * kTuRows + tid;
-        nv = gv = 0;
-        if (tid < kTuRows && t < ntile && row < r1) {
-            nv = p.norm[row];
-            if constexpr (PROD) gv = p.rnorm[row];
-        }
-    };
-    uint16_t nxt_n = 0, nxt_g = 0;
-    load_norms(0, nxt_n, nxt_g);
-    if (tid < kTuRows) {
-        s_nrm[tid] = f16_bits_to_f32(nxt_n);
-        s_gam[tid] = __uint_as_float((uint32_t)nxt_g);  // raw fp16 bits of gamma, carried in a float slot
-    }
-
-    // epilogue of tile te: wait for its MMAs, read its accumulator, update the lists
-    auto epilogue = [&](int64_t te) -> bool {
-        if (__syncthreads_or(!mbar_wait_bounded(abar0 + 8 * (uint32_t)(te & 1), (uint32_t)((te >> 1) & 1), kWaitLimitNs, p.err,
-                                                kErrScanWait)))
-            return false;
-        tc_fence_after_sync();
-        float v[2 * kTuQpw];
-        static_assert(2 * kTuQpw == 16, "one 16-column TMEM load per warp");
-        tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((te & 1) * kTuN + ecol), v);
-        tmem_ld_wait();
-        const int64_t erow = r0 + te * kTuRows + er;
-        const bool evalid = erow < r1;
-        const float scale = s_nrm[(te & 1) * kTuRows + er] * p.inv_lam;
-        const int id = (int)erow;
-#pragma unroll
-        for (int jj = 0; jj < kTuQpw; ++jj) {
-            const int j = (ecol >> 1) + jj;
-            if (j < nq_here) {  // warp-uniform
-                const float sc = scale * (v[2 * jj] + v[2 * jj + 1]);
-                float ts = thr_s[jj];
-                int ti = thr_i[jj];
-                // cheap filter (>=); the exact rule (equal scores: lower id first) is applied below
-                unsigned cand = __ballot_sync(TQ_FULL_MASK, evalid && sc >= ts);
-                while (cand) {
-                    const int src = __ffs(cand) - 1;
-                    cand &= cand - 1;
-                    const float cs_ = __shfl_sync(TQ_FULL_MASK, sc, src);
-                    const int ci = __shfl_sync(TQ_FULL_MASK, id, src);
-                    if (!better(cs_, ci, ts, ti)) continue;  // the list moved on since the ballot
-                    // entries better than the candidate stay, the rest move one lane down
-                    const int pos = __popc(__ballot_sync(TQ_FULL_MASK, lane < k && better(lsc[jj], lid[jj], cs_, ci)));
-                    const float us = __shfl_up_sync(TQ_FULL_MASK, lsc[jj], 1);
-                    const int ui = __shfl_up_sync(TQ_FULL_MASK, lid[jj], 1);
-                    if (lane == pos) {
-                        lsc[jj] = cs_;
-                        lid[jj] = ci;
-                    } else if (lane > pos) {
-                        lsc[jj] = us;
-                        lid[jj] = ui;
-                    }
-                    ts = __shfl_sync(TQ_FULL_MASK, lsc[jj], k - 1);
-                    ti = __shfl_sync(TQ_FULL_MASK, lid[jj], k - 1);
+                for (int q = 0; q < CB; ++q) {
+                    const uint4 v = rvalid ? src[q] : make_uint4(0u, 0u, 0u, 0u);
+                    cw[4 * q] = v.x;
+                    cw[4 * q + 1] = v.y;
+                    cw[4 * q + 2] = v.z;
+                    cw[4 * q + 3] = v.w;
                 }
-                thr_s[jj] = ts;
-                thr_i[jj] = ti;
+                cw[HW] = 0u;
             }
-        }
-        return true;
-    };
-
-    for (int64_t t = 0; t < ntile && ok; ++t) {
-        const int64_t t0 = r0 + t * kTuRows;
-        const int sb = (int)(t & 1);
-        if (tid == 0 && t + 1 < ntile) stage(t + 1);  // its buffer was last read in tile t - 1
-        load_norms(t + 1, nxt_n, nxt_g);
-        ok = !__syncthreads_or(!mbar_wait_bounded(sbar0 + 8 * sb, (uint32_t)((t >> 1) & 1), kWaitLimitNs, p.err, kErrScanWait));
-        if (!ok) break;
-        const float* t_nrm = s_nrm + sb * kTuRows;
-        const float* t_gam = s_gam + sb * kTuRows;
-        for (int seg = 0; seg < NSEG_A; ++seg) {
-            const int buf = step & 1;
-            if (step >= 2) {
-                ok = !__syncthreads_or(
-                    !mbar_wait_bounded(bar0 + 8 * buf, (uint32_t)(((step - 2) >> 1) & 1), kWaitLimitNs, p.err, kErrScanWait));
-                if (!ok) break;
-            }
-            const bool sign_seg = PROD && seg == NSEG_A - 1;
-            unsigned char* dstA = sA0 + buf * sA_stride;
-            const bool rvalid = t0 + r < r1;
-            const unsigned char* crow = sSt0 + sb * sSt_stride + r * cs;
-            const unsigned char* srow = sSt0 + sb * sSt_stride + kTuRows * cs + r * ss;
-            uint32_t g2 = 0u;
-            if (sign_seg) {
-                const uint32_t g16 = __float_as_uint(t_gam[r]);
-                g2 = (g16 | 0x8000u) | ((g16 | 0x8000u) << 16);  // (-gamma, -gamma)
-            }
-            static_assert(256 / 8 / kTuParts <= 8, "at most 8 units per thread");
+            uint4 sgw = make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (PROD)
+                if (rvalid) sgw = *reinterpret_cast<const uint4*>(st + (size_t)kTuRows * cs + (size_t)r * ss + 16 * h);
+            const uint16_t g16 = g_next;  // gamma of row r of this tile (fp16 bits)
+            if (PROD && t + 1 < ntile && r0 + (t + 1) * kTuRows + r < r1) g_next = p.rnorm[r0 + (t + 1) * kTuRows + r];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ste0 + 8 * b);  // the staged rows were read into registers
+            bool ok = true;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {  // fixed trip count: predicated, no loop branches
-                const int u = u0 + q;
-                if (u >= u1) break;
-                uint4 w;
-                if (sign_seg) {
-                    const uint4 f = s_sgn[rvalid ? srow[u] : 0];
-                    w = make_uint4(g2 ^ f.x, g2 ^ f.y, g2 ^ f.z, g2 ^ f.w);
-                } else {
-                    // 8 codes: CB bytes starting at byte CB * u of the row
-                    uint32_t bits = 0u;
-                    if (rvalid) {
-                        if constexpr (CB == 1) bits = crow[u];
-                        else if constexpr (CB == 2) bits = *reinterpret_cast<const uint16_t*>(crow + 2 * u);
-                        else if constexpr (CB == 4) bits = *reinterpret_cast<const uint32_t*>(crow + 4 * u);
-                        else {
-                            const int o = CB * u;
-                            const uint32_t* wp = reinterpret_cast<const uint32_t*>(crow + (o & ~3));
-                            bits = __funnelshift_r(wp[0], wp[1], 8 * (o & 3));
+            for (int seg = 0; seg < NSEG_A; ++seg) {
+                const int64_t g = t * NSEG_A + seg;
+                const int x = (int)(g % kTuASlots);
+                if (g >= kTuASlots &&
+                    !mbar_wait_bounded(ae0 + 8 * x, (uint32_t)(((g / kTuASlots) - 1) & 1), kWaitLimitNs, p.err,
+                                       kErrScanWait)) {
+                    ok = false;
+                    break;
+                }
+                const bool sign_seg = PROD && seg == NSEG_A - 1;
+                const uint32_t* tab = (LO && seg == 1) ? s_klo : s_ktab;
+                const uint32_t g2 = (sign_seg && rvalid) ? ((g16 | 0x8000u) | ((uint32_t)(g16 | 0x8000u) << 16)) : 0u;
+                const uint32_t sb[4] = {sgw.x, sgw.y, sgw.z, sgw.w};
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (8 * h + j >= npair) break;
+                    uint32_t v[8];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int u = 2 * j + e;  // unit within the half row
+                        if (sign_seg) {
+                            const uint4 f = s_sgn[(sb[u >> 2] >> (8 * (u & 3))) & 0xFFu];
+                            v[4 * e] = g2 ^ f.x;
+                            v[4 * e + 1] = g2 ^ f.y;
+                            v[4 * e + 2] = g2 ^ f.z;
+                            v[4 * e + 3] = g2 ^ f.w;
+                        } else {
+                            constexpr uint32_t M2 = (1u << (2 * CB)) - 1u;
+                            const uint32_t bits = tu_bits(cw, 8 * CB * u, 8 * CB);
+                            v[4 * e] = tab[bits & M2];
+                            v[4 * e + 1] = tab[(bits >> (2 * CB)) & M2];
+                            v[4 * e + 2] = tab[(bits >> (4 * CB)) & M2];
+                            v[4 * e + 3] = tab[CB == 4 ? (bits >> 24) : ((bits >> (6 * CB)) & M2)];
                         }
                     }
-                    const uint32_t* tab = (LO && seg == 1) ? s_klo : s_ktab;
-                    constexpr uint32_t M2 = (1u << (2 * CB)) - 1u;
-                    w.x = tab[bits & M2];
-                    w.y = tab[(bits >> (2 * CB)) & M2];
-                    w.z = tab[(bits >> (4 * CB)) & M2];
-                    w.w = tab[CB == 4 ? (bits >> 24) : ((bits >> (6 * CB)) & M2)];
+                    tmem_st8(lane_addr + kTuN * 2u + (uint32_t)x * scols + 8u * (uint32_t)(8 * h + j), v);
                 }
-                *reinterpret_cast<uint4*>(dstA + umma_off(r, 8 * u, ks)) = w;
+                tmem_st_wait();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(af0 + 8 * x);
             }
-            fence_proxy_async_smem();  // the tile is read by the tensor core next
-            __syncthreads();
-            if (tid == 0) {
-                tc_fence_after_sync();
-                const int bseg = sign_seg ? 1 : 0;
-                const uint32_t dacc = tmem + (uint32_t)((t & 1) * kTuN);
-                for (int s = 0; s < ks / 16; ++s)
-                    umma_f16(dacc, descA0 + (uint64_t)((buf * sA_stride + 256 * s) >> 4),
-                             descB0 + (uint64_t)((bseg * ks / 8 + 2 * s) * 8), idesc, seg > 0 || s > 0);
-                umma_commit(bar0 + 8 * buf);
-                if (seg == NSEG_A - 1) umma_commit(abar0 + 8 * (uint32_t)(t & 1));
+            if (!ok || *abort_flag) {
+                *abort_flag = 1;
+                break;
             }
-            ++step;
         }
-        if (!ok) break;
-        // the previous tile's epilogue runs while the tensor core works on this tile
-        if (t > 0 && !(ok = epilogue(t - 1))) break;
-        tc_fence_before_sync();
-        __syncthreads();  // the accumulator just read is overwritten by tile t + 1's first MMA
-        if (tid < kTuRows) {  // the norms of tile t + 1 into the buffer tile t - 1 used
-            s_nrm[(sb ^ 1) * kTuRows + tid] = f16_bits_to_f32(nxt_n);
-            s_gam[(sb ^ 1) * kTuRows + tid] = __uint_as_float((uint32_t)nxt_g);
+    } else if (warp < kTuCtl) {
+        // ================= epilogue =================
+        const int ew = warp - kTuProd;           // 0..7
+        const int er = 32 * (warp & 3) + lane;   // this thread's row (TMEM lane)
+        const int jq0 = kTuQpw * (ew >> 2);      // its queries jq0 .. jq0 + 15
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        // top-k list of each query over this warp's rows, spread over the
+        // lanes (lane e holds entry e, best first); thr_s: the k-th score
+        float lsc[kTuQpw];
+        int lid[kTuQpw];
+        float thr_s[kTuQpw];
+#pragma unroll
+        for (int jj = 0; jj < kTuQpw; ++jj) {
+            lsc[jj] = -INFINITY;
+            lid[jj] = 0x7fffffff;
+            thr_s[jj] = -INFINITY;
         }
-    }
-    if (ok && ntile > 0) ok = epilogue(ntile - 1);
-    if (!ok) {
-        // a wait ran out (the error word says so): let the copies and MMAs
-        // still in flight finish, bounded, before TMEM and smem are released
-        for (int b = 0; b < 2; ++b) {
-            mbar_wait_bounded(sbar0 + 8 * b, 0, kWaitLimitNs, p.err, kErrScanWait);
-            mbar_wait_bounded(sbar0 + 8 * b, 1, kWaitLimitNs, p.err, kErrScanWait);
+        uint16_t n_next = 0;
+        if (ntile > 0 && r0 + er < r1) n_next = p.norm[r0 + er];
+        for (int64_t t = 0; t < ntile; ++t) {
+            const int ab = (int)(t & 1);
+            const int64_t erow = r0 + t * kTuRows + er;
+            const bool evalid = erow < r1;
+            const float scale = f16_bits_to_f32(n_next) * p.inv_lam;
+            if (t + 1 < ntile && erow + kTuRows < r1) n_next = p.norm[erow + kTuRows];
+            if (!mbar_wait_bounded(cf0 + 8 * ab, (uint32_t)((t >> 1) & 1), kWaitLimitNs, p.err, kErrScanWait)) {
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after_sync();
+            const int id = (int)erow;
+            // two halves of 8 queries (16 columns) each, so that only 16
+            // accumulator values are live at a time
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float v[16];
+                tmem_ld16(lane_addr + (uint32_t)(ab * kTuN + 2 * jq0 + 16 * hf), v);
+                tmem_ld_wait();
+                if (hf == 1) {
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(ce0 + 8 * ab);  // the accumulator may be overwritten
+                }
+#pragma unroll
+                for (int j8 = 0; j8 < 8; ++j8) {
+                    const int jj = 8 * hf + j8;
+                    if (jq0 + jj >= nq_here) continue;  // warp-uniform
+                    const float sc = scale * (v[2 * j8] + v[2 * j8 + 1]);
+                    // cheap filter (>=); the exact rule (equal scores: lower id first) is applied below
+                    unsigned cand = __ballot_sync(TQ_FULL_MASK, evalid && sc >= thr_s[jj]);
+                    if (!cand) continue;
+                    while (cand) {
+                        const int src = __ffs(cand) - 1;
+                        cand &= cand - 1;
+                        const float cs_ = __shfl_sync(TQ_FULL_MASK, sc, src);
+                        const int ci = __shfl_sync(TQ_FULL_MASK, id, src);
+                        const float ts = __shfl_sync(TQ_FULL_MASK, lsc[jj], k - 1);
+                        const int ti = __shfl_sync(TQ_FULL_MASK, lid[jj], k - 1);
+                        if (!better(cs_, ci, ts, ti)) continue;  // the list moved on since the ballot
+                        // entries better than the candidate stay, the rest move one lane down
+                        const int pos = __popc(__ballot_sync(TQ_FULL_MASK, lane < k && better(lsc[jj], lid[jj], cs_, ci)));
+                        const float us = __shfl_up_sync(TQ_FULL_MASK, lsc[jj], 1);
+                        const int ui = __shfl_up_sync(TQ_FULL_MASK, lid[jj], 1);
+                        if (lane == pos) {
+                            lsc[jj] = cs_;
+                            lid[jj] = ci;
+                        } else if (lane > pos) {
+                            lsc[jj] = us;
+                            lid[jj] = ui;
+                        }
+                    }
+                    thr_s[jj] = __shfl_sync(TQ_FULL_MASK, lsc[jj], k - 1);
+                }
+            }
+            if (*abort_flag) break;
         }
-        if (step > 0)
-            mbar_wait_bounded(bar0 + 8 * ((step - 1) & 1), (uint32_t)(((step - 1) >> 1) & 1), kWaitLimitNs, p.err, kErrScanWait);
-        if (step >= 2)
-            mbar_wait_bounded(bar0 + 8 * ((step - 2) & 1), (uint32_t)(((step - 2) >> 1) & 1), kWaitLimitNs, p.err, kErrScanWait);
-    }
-    tc_fence_before_sync();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 2 * kTuN);
-
-    // ---- merge the four warp lists of each query, write the chunk's candidates ----
-    {
-        float* wls = s_ls + warp * kTuQpw * k;
-        int* wli = s_li + warp * kTuQpw * k;
+        float* wls = s_ls + ew * kTuQpw * k;
+        int* wli = s_li + ew * kTuQpw * k;
 #pragma unroll
         for (int jj = 0; jj < kTuQpw; ++jj)
             if (lane < k) {
                 wls[jj * k + lane] = lsc[jj];
                 wli[jj * k + lane] = lid[jj];
             }
+    } else if (lane == 0) {
+        // ================= control =================
+        const uint32_t idesc = umma_idesc_f16(kTuRows, kTuN);
+        const uint64_t descB0 = umma_desc((uint32_t)__cvta_generic_to_shared(sB), 128, kcb * 16);
+        const int64_t npre = min((int64_t)kTuStages - 1, ntile);
+        for (int64_t t = 0; t < npre; ++t) stage(t);
+        int64_t staged = npre;
+        int64_t seg_done = 0;  // segments whose MMAs were issued and committed
+        bool ok = true;
+        for (int64_t t = 0; t < ntile && ok; ++t) {
+            const int ab = (int)(t & 1);
+            // the epilogue has read this accumulator's previous tile
+            if (t >= 2 && !mbar_wait_bounded(ce0 + 8 * ab, (uint32_t)(((t >> 1) - 1) & 1), kWaitLimitNs, p.err,
+                                             kErrScanWait)) {
+                ok = false;
+                break;
+            }
+            const uint32_t dacc = tmem + (uint32_t)(ab * kTuN);
+            for (int seg = 0; seg < NSEG_A; ++seg) {
+                const int64_t g = t * NSEG_A + seg;
+                const int x = (int)(g % kTuASlots);
+                if (!mbar_wait_bounded(af0 + 8 * x, (uint32_t)((g / kTuASlots) & 1), kWaitLimitNs, p.err,
+                                       kErrScanWait)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const int bseg = (PROD && seg == NSEG_A - 1) ? 1 : 0;
+                const uint32_t a_col = tmem + kTuN * 2u + (uint32_t)x * scols;
+                for (int s = 0; s < ks / 16; ++s)
+                    umma_f16_ta(dacc, a_col + 8u * s, descB0 + (uint64_t)((bseg * ks / 8 + 2 * s) * 8), idesc,
+                                seg > 0 || s > 0);
+                umma_commit(ae0 + 8 * x);
+                ++seg_done;
+            }
+            if (!ok) break;
+            umma_commit(cf0 + 8 * ab);
+            // next copy: tile `staged` into buffer staged % kTuStages, which the
+            // producers released (right after reading it) for tile staged - kTuStages
+            if (staged < ntile) {
+                const int64_t prev = staged - kTuStages;
+                if (prev >= 0 && !mbar_wait_bounded(ste0 + 8 * (int)(prev % kTuStages),
+                                                    (uint32_t)((prev / kTuStages) & 1), kWaitLimitNs, p.err,
+                                                    kErrScanWait)) {
+                    ok = false;
+                    break;
+                }
+                fence_proxy_async_smem();
+                stage(staged);
+                ++staged;
+            }
+            if (*abort_flag) ok = false;
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            // let the copies and MMAs in flight finish (bounded) before the
+            // staging buffers and TMEM are released: the copies of tiles not
+            // yet consumed, and the last MMA commit
+            for (int64_t t = max((int64_t)0, staged - kTuStages); t < staged; ++t)
+                mbar_wait_bounded(stf0 + 8 * (int)(t % kTuStages), (uint32_t)((t / kTuStages) & 1), kWaitLimitNs,
+                                  p.err, kErrScanWait);
+            if (seg_done > 0) {
+                const int64_t g = seg_done - 1;
+                mbar_wait_bounded(ae0 + 8 * (int)(g % kTuASlots), (uint32_t)((g / kTuASlots) & 1), kWaitLimitNs,
+                                  p.err, kErrScanWait);
+            }
+        } else if (ntile > 0) {
+            // every MMA completed once the epilogue has seen the last accumulator;
+            // the control thread waits for the last commit all the same
+            const int64_t g = seg_done - 1;
+            mbar_wait_bounded(ae0 + 8 * (int)(g % kTuASlots), (uint32_t)((g / kTuASlots) & 1), kWaitLimitNs, p.err,
+                              kErrScanWait);
+        }
     }
+    tc_fence_before_sync();
     __syncthreads();
+    if (warp == kTuCtl) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTuCols);
+    }
+
+    // ---- merge the four warp lists of each query, write the chunk's candidates ----
     if (tid < nq_here) {
         const int j = tid;
-        const int base_w = 4 * (j / kTuQpw), jj = j % kTuQpw;
-        float* ls0 = s_ls + (base_w * kTuQpw + jj) * k;
-        int* li0 = s_li + (base_w * kTuQpw + jj) * k;
+        const int qh = j / kTuQpw, jj = j % kTuQpw;  // epilogue warps 4 qh .. 4 qh + 3 hold query j
+        float* ls0 = s_ls + ((4 * qh) * kTuQpw + jj) * k;
+        int* li0 = s_li + ((4 * qh) * kTuQpw + jj) * k;
         for (int w4 = 1; w4 < 4; ++w4) {
-            const float* ls = s_ls + ((base_w + w4) * kTuQpw + jj) * k;
-            const int* li = s_li + ((base_w + w4) * kTuQpw + jj) * k;
+            const float* ls = s_ls + ((4 * qh + w4) * kTuQpw + jj) * k;
+            const int* li = s_li + ((4 * qh + w4) * kTuQpw + jj) * k;
             for (int e = 0; e < k; ++e) list_insert(ls0, li0, k, ls[e], li[e]);
         }
         for (int e = 0; e < k; ++e) {
@@ -398,6 +462,8 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
 template <int CB, bool PROD, bool LO>
 static cudaError_t go_tu(const TopkParams& p, size_t smem, cudaStream_t s) {
     auto kern = topk_umma_kernel<CB, PROD, LO>;
+    // at least kTuSmemMin: one CTA per SM, since each holds all 512 TMEM columns
+    smem = smem < (size_t)kTuSmemMin ? (size_t)kTuSmemMin : smem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(p.n_chunks, (p.nq + kTuQ - 1) / kTuQ);

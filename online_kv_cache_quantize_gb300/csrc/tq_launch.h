@@ -140,7 +140,9 @@ cudaError_t device_error_word(uint32_t** out);
 cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t s);
 // D [128 x n] = A [128 x k] B [n x k]^T (fp16 in, fp32 out) through tcgen05;
 // n in {16, 32, 64, 128}, k a multiple of 16 up to 128
-cudaError_t launch_umma_selftest(const void* a, const void* b, float* d, int n, int k, uint32_t* err, cudaStream_t s);
+// a_tmem != 0: A goes through TMEM (tcgen05.st) and the MMA reads it there
+cudaError_t launch_umma_selftest(const void* a, const void* b, float* d, int n, int k, int a_tmem, uint32_t* err,
+                                 cudaStream_t s);
 
 
 struct CombineParams {

@@ -59,11 +59,13 @@ def test_decode_leaves_the_error_word_clear():
     assert bool(torch.isfinite(out).all())
 
 
+@pytest.mark.parametrize("a_in_tmem", [False, True])
 @pytest.mark.parametrize("n,k", [(16, 16), (32, 48), (64, 64), (128, 128), (64, 128)])
-def test_tcgen05_gemm_matches_cpu(n, k):
+def test_tcgen05_gemm_matches_cpu(n, k, a_in_tmem):
     """The tcgen05 path (core-matrix smem descriptors, kind::f16 instruction
-    descriptor, TMEM accumulators read back with tcgen05.ld) against an exact
-    CPU product: small integers, so every sum is exact in fp32."""
+    descriptor, TMEM accumulators read back with tcgen05.ld; A from shared
+    memory or written into TMEM with tcgen05.st) against an exact CPU product:
+    small integers, so every sum is exact in fp32."""
     import numpy as np
     rng = np.random.default_rng(n * 1000 + k)
     a = rng.integers(-3, 4, size=(128, k)).astype(np.float16)
@@ -71,6 +73,6 @@ def test_tcgen05_gemm_matches_cpu(n, k):
     want = a.astype(np.float64) @ b.astype(np.float64).T
     B.tq_device_errors(reset=True)
     d = torch.full((128, n), float("nan"), device="cuda")
-    B.tq_selftest_umma_gemm(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda(), d)
+    B.tq_selftest_umma_gemm(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda(), d, a_in_tmem=a_in_tmem)
     assert B.tq_device_errors() == (B.TQ_OK, 0)
     assert np.array_equal(d.cpu().numpy().astype(np.float64), want)
