@@ -330,7 +330,8 @@ tq_status tq_device_errors(uint32_t* flags_out, int reset);
 
 /* Self-test of the bounded wait: launches one warp on `stream` that waits on
  * an mbarrier nothing ever arrives on, for at most limit_us microseconds
- * (1..1000000), then returns after setting TQ_DEVERR_SELFTEST_WAIT. */
+ * (1..1000000; a wait checks its limit at least every 20 us, between
+ * suspensions), then returns after setting TQ_DEVERR_SELFTEST_WAIT. */
 tq_status tq_selftest_bounded_wait(uint32_t limit_us, tq_stream stream);
 
 /* Self-test of the 5th-generation tensor-core path (tcgen05.mma with TMEM

@@ -72,13 +72,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended for up to hint_ns while
+// the phase is incomplete (it resumes when the phase completes), so a waiting
+// warp does not spin through issue slots other warps need.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// one suspension of a bounded wait: far below the limit, far above a copy's latency
+constexpr uint32_t kWaitSuspendNs = 20000u;
+
 // Waits for the phase with the given parity to complete, at most `limit_ns`.
 // On time-out sets `code` in *err (if err is not null) and returns false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns, uint32_t* err,
                                                   uint32_t code) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_suspend(bar, parity, kWaitSuspendNs)) {
         if (global_ns() - t0 > limit_ns) {
             if (err) atomicOr(err, code);
             return false;

@@ -50,7 +50,7 @@ constexpr int kTuSmemLimit = 227 * 1024 - 4096;  // dynamic part; static part be
 constexpr int kTuSmemMin = 116 * 1024;  // at most one CTA per SM: it holds all of TMEM
 
 struct TuLayout {
-    size_t b, st, sgn, ls, li, total;
+    size_t b, st, sgn, kb, ls, li, total;
     int kcb, stage_bytes;
 };
 
@@ -63,7 +63,8 @@ __host__ __device__ inline TuLayout tu_layout(int ks, int nseg_b, int code_strid
     L.b = 0;
     L.st = (bb + 127) / 128 * 128;
     L.sgn = L.st + (size_t)kTuStages * L.stage_bytes;
-    L.ls = L.sgn + 256 * 16;
+    L.kb = L.sgn + 256 * 16;  // byte table of the codes (1- and 2-bit codes)
+    L.ls = L.kb + 256 * 16;
     L.li = L.ls + (size_t)kTuEpi * kTuQpw * k * 4;
     L.total = L.li + (size_t)kTuEpi * kTuQpw * k * 4;
     return L;
@@ -102,6 +103,10 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
     unsigned char* sB = smem + Lo.b;
     unsigned char* const sSt0 = smem + Lo.st;
     const uint4* s_sgn = reinterpret_cast<const uint4*>(smem + Lo.sgn);
+    // 1- and 2-bit codes: one code byte -> its 8 / 4 coordinates' pair-table
+    // words in one lookup (16 / 8 bytes), instead of 4 / 2 lookups of pairs
+    constexpr bool KBYTE = CB <= 2;
+    const unsigned char* s_kb = smem + Lo.kb;
     float* s_ls = reinterpret_cast<float*>(smem + Lo.ls);  // [epilogue warp][query][k]
     int* s_li = reinterpret_cast<int*>(smem + Lo.li);
 
@@ -127,6 +132,14 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
         v.w = ((uint32_t)((i >> 6) & 1) << 15) | ((uint32_t)((i >> 7) & 1) << 31);
         reinterpret_cast<uint4*>(smem + Lo.sgn)[i] = v;
     }
+    if constexpr (KBYTE)
+        for (int i = tid; i < 256; i += blockDim.x) {
+            if constexpr (CB == 1)
+                reinterpret_cast<uint4*>(smem + Lo.kb)[i] =
+                    make_uint4(p.ktab[i & 3], p.ktab[(i >> 2) & 3], p.ktab[(i >> 4) & 3], p.ktab[i >> 6]);
+            else
+                reinterpret_cast<uint2*>(smem + Lo.kb)[i] = make_uint2(p.ktab[i & 15], p.ktab[i >> 4]);
+        }
     // B tile: row 2j + s holds query j's hi (s = 0) or lo (s = 1) fp16 half;
     // columns [0, ks) are q', [ks, 2 ks) lam * kappa * u (PROD)
     for (int e = tid; e < kTuQ * (kcb / 2); e += blockDim.x) {
@@ -253,6 +266,20 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
                             v[4 * e + 1] = g2 ^ f.y;
                             v[4 * e + 2] = g2 ^ f.z;
                             v[4 * e + 3] = g2 ^ f.w;
+                        } else if constexpr (KBYTE && CB == 1) {
+                            const uint4 f = reinterpret_cast<const uint4*>(s_kb)[(cw[u >> 2] >> (8 * (u & 3))) & 0xFFu];
+                            v[4 * e] = f.x;
+                            v[4 * e + 1] = f.y;
+                            v[4 * e + 2] = f.z;
+                            v[4 * e + 3] = f.w;
+                        } else if constexpr (KBYTE) {
+                            const uint32_t w16 = cw[u >> 1] >> (16 * (u & 1));
+                            const uint2 f0 = reinterpret_cast<const uint2*>(s_kb)[w16 & 0xFFu];
+                            const uint2 f1 = reinterpret_cast<const uint2*>(s_kb)[(w16 >> 8) & 0xFFu];
+                            v[4 * e] = f0.x;
+                            v[4 * e + 1] = f0.y;
+                            v[4 * e + 2] = f1.x;
+                            v[4 * e + 3] = f1.y;
                         } else {
                             constexpr uint32_t M2 = (1u << (2 * CB)) - 1u;
                             const uint32_t bits = tu_bits(cw, 8 * CB * u, 8 * CB);
