@@ -731,10 +731,12 @@ tq_status tq_score_topk(const tq_topk_args* a, void* workspace, size_t ws_bytes,
     tp.inv_lam = (float)(1.0 / lam);
     tp.ks = (int)round_up((size_t)std::max(a->d, m), 16);
     if ((e = tqk::device_error_word(&tp.err)) != cudaSuccess) return cuda_status(e, "tq_score_topk error word");
-    // the tensor-core scan takes 4x longer chunks (fewer list insertions per
-    // row); it needs no more candidate slots than the workspace holds
+    // the tensor-core scan takes 16x longer chunks: a list restarts once per
+    // chunk, so longer chunks mean fewer insertions per row (the expected
+    // count per list grows only with the log of its rows); it needs no more
+    // candidate slots than the workspace holds
     tqk::TopkParams tu = tp;
-    tu.chunk_rows = 4 * chunk_rows;
+    tu.chunk_rows = 16 * chunk_rows;
     tu.n_chunks = (int)std::max<int64_t>(1, (a->n_db + tu.chunk_rows - 1) / tu.chunk_rows);
     e = g_topk_simt ? cudaErrorNotSupported : tqk::launch_topk_umma(tu, cb, prod ? 1 : 0, cb >= 3 ? 1 : 0, st);
     if (e == cudaErrorNotSupported) {

@@ -344,22 +344,32 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
                     __syncwarp();
                     if (lane == 0) mbar_arrive(ce0 + 8 * ab);  // the accumulator may be overwritten
                 }
+                // lane-local admission test of the 8 queries first (one compare
+                // each with the list's k-th score), so that a tile where no
+                // row beats any list costs one vote for the 8 queries
+                float sc[8];
+                uint32_t mine = 0u;
 #pragma unroll
                 for (int j8 = 0; j8 < 8; ++j8) {
                     const int jj = 8 * hf + j8;
-                    if (jq0 + jj >= nq_here) continue;  // warp-uniform
-                    const float sc = scale * (v[2 * j8] + v[2 * j8 + 1]);
-                    // cheap filter (>=); the exact rule (equal scores: lower id first) is applied below
-                    unsigned cand = __ballot_sync(TQ_FULL_MASK, evalid && sc >= thr_s[jj]);
+                    sc[j8] = scale * (v[2 * j8] + v[2 * j8 + 1]);
+                    if (evalid && jq0 + jj < nq_here && sc[j8] >= thr_s[jj]) mine |= 1u << j8;
+                }
+                if (!__any_sync(TQ_FULL_MASK, mine != 0u)) continue;
+#pragma unroll
+                for (int j8 = 0; j8 < 8; ++j8) {
+                    const int jj = 8 * hf + j8;
+                    // the exact rule (equal scores: lower id first) is applied in the insert
+                    unsigned cand = __ballot_sync(TQ_FULL_MASK, (mine >> j8) & 1u);
                     if (!cand) continue;
                     while (cand) {
                         const int src = __ffs(cand) - 1;
                         cand &= cand - 1;
-                        const float cs_ = __shfl_sync(TQ_FULL_MASK, sc, src);
+                        const float cs_ = __shfl_sync(TQ_FULL_MASK, sc[j8], src);
                         const int ci = __shfl_sync(TQ_FULL_MASK, id, src);
                         const float ts = __shfl_sync(TQ_FULL_MASK, lsc[jj], k - 1);
                         const int ti = __shfl_sync(TQ_FULL_MASK, lid[jj], k - 1);
-                        if (!better(cs_, ci, ts, ti)) continue;  // the list moved on since the ballot
+                        if (!better(cs_, ci, ts, ti)) continue;  // the list moved on since the test
                         // entries better than the candidate stay, the rest move one lane down
                         const int pos = __popc(__ballot_sync(TQ_FULL_MASK, lane < k && better(lsc[jj], lid[jj], cs_, ci)));
                         const float us = __shfl_up_sync(TQ_FULL_MASK, lsc[jj], 1);
