@@ -14,10 +14,12 @@
 // n * (D[row][2j] + D[row][2j + 1]) / lam.
 //
 // Warp-specialised CTA (32 queries, a chunk of database rows, 128-row tiles):
-//  * control warp: bulk copies of each tile's packed codes and signs into a
-//    ring of staging buffers, and the MMAs (tcgen05.mma, A read from tensor
-//    memory, B = the queries resident in shared memory) into one of two
-//    128 x 64 fp32 TMEM accumulators, committed to mbarriers;
+//  * copy warp: bulk copies of each tile's packed codes and signs into a
+//    ring of staging buffers;
+//  * MMA warp: the MMAs (tcgen05.mma, A read from tensor memory, B = the
+//    queries resident in shared memory) into one of two 128 x 64 fp32 TMEM
+//    accumulators, committed to mbarriers (kept free of other work, since
+//    its thread waits while the tensor core takes each MMA);
 //  * 8 producer warps: de-quantize each A segment of a tile straight into
 //    tensor memory (tcgen05.st; row r in TMEM lane r, two fp16 per column)
 //    through a ring of segment slots, so the de-quantized tile never touches
@@ -39,8 +41,9 @@ constexpr int kTuQ = 32;                // queries per CTA
 constexpr int kTuN = 2 * kTuQ;          // MMA N: hi and lo column per query
 constexpr int kTuProd = 8;              // producer warps
 constexpr int kTuEpi = 8;               // epilogue warps
-constexpr int kTuCtl = kTuProd + kTuEpi;  // the control warp's index
-constexpr int kTuWarps = kTuCtl + 1;
+constexpr int kTuCtl = kTuProd + kTuEpi;  // the MMA warp's index
+constexpr int kTuCopy = kTuCtl + 1;       // the copy warp's index
+constexpr int kTuWarps = kTuCopy + 1;
 constexpr int kTuThreads = 32 * kTuWarps;
 constexpr int kTuQpw = kTuQ / 2;        // queries per epilogue warp
 constexpr int kTuStages = 4;            // staging buffers
@@ -395,13 +398,10 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
                 wls[jj * k + lane] = lsc[jj];
                 wli[jj * k + lane] = lid[jj];
             }
-    } else if (lane == 0) {
-        // ================= control =================
+    } else if (warp == kTuCtl && lane == 0) {
+        // ================= MMA issue =================
         const uint32_t idesc = umma_idesc_f16(kTuRows, kTuN);
         const uint64_t descB0 = umma_desc((uint32_t)__cvta_generic_to_shared(sB), 128, kcb * 16);
-        const int64_t npre = min((int64_t)kTuStages - 1, ntile);
-        for (int64_t t = 0; t < npre; ++t) stage(t);
-        int64_t staged = npre;
         int64_t seg_done = 0;  // segments whose MMAs were issued and committed
         bool ok = true;
         for (int64_t t = 0; t < ntile && ok; ++t) {
@@ -432,42 +432,39 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
             }
             if (!ok) break;
             umma_commit(cf0 + 8 * ab);
-            // next copy: tile `staged` into buffer staged % kTuStages, which the
-            // producers released (right after reading it) for tile staged - kTuStages
-            if (staged < ntile) {
-                const int64_t prev = staged - kTuStages;
-                if (prev >= 0 && !mbar_wait_bounded(ste0 + 8 * (int)(prev % kTuStages),
-                                                    (uint32_t)((prev / kTuStages) & 1), kWaitLimitNs, p.err,
-                                                    kErrScanWait)) {
-                    ok = false;
-                    break;
-                }
-                fence_proxy_async_smem();
-                stage(staged);
-                ++staged;
-            }
             if (*abort_flag) ok = false;
         }
-        if (!ok) {
-            *abort_flag = 1;
-            // let the copies and MMAs in flight finish (bounded) before the
-            // staging buffers and TMEM are released: the copies of tiles not
-            // yet consumed, and the last MMA commit
-            for (int64_t t = max((int64_t)0, staged - kTuStages); t < staged; ++t)
-                mbar_wait_bounded(stf0 + 8 * (int)(t % kTuStages), (uint32_t)((t / kTuStages) & 1), kWaitLimitNs,
-                                  p.err, kErrScanWait);
-            if (seg_done > 0) {
-                const int64_t g = seg_done - 1;
-                mbar_wait_bounded(ae0 + 8 * (int)(g % kTuASlots), (uint32_t)((g / kTuASlots) & 1), kWaitLimitNs,
-                                  p.err, kErrScanWait);
-            }
-        } else if (ntile > 0) {
-            // every MMA completed once the epilogue has seen the last accumulator;
-            // the control thread waits for the last commit all the same
+        if (!ok) *abort_flag = 1;
+        // the MMAs in flight finish (bounded wait on the last commit) before
+        // TMEM is released
+        if (seg_done > 0) {
             const int64_t g = seg_done - 1;
             mbar_wait_bounded(ae0 + 8 * (int)(g % kTuASlots), (uint32_t)((g / kTuASlots) & 1), kWaitLimitNs, p.err,
                               kErrScanWait);
         }
+    } else if (warp == kTuCopy && lane == 0) {
+        // ================= bulk copies =================
+        // tile t goes into buffer t % kTuStages once the producers released
+        // it (right after reading it into registers) for tile t - kTuStages
+        int64_t issued = 0;
+        for (int64_t t = 0; t < ntile; ++t) {
+            const int64_t prev = t - kTuStages;
+            if (prev >= 0 && !mbar_wait_bounded(ste0 + 8 * (int)(prev % kTuStages), (uint32_t)((prev / kTuStages) & 1),
+                                                kWaitLimitNs, p.err, kErrScanWait)) {
+                *abort_flag = 1;
+                break;
+            }
+            fence_proxy_async_smem();
+            stage(t);
+            issued = t + 1;
+            if (*abort_flag) break;
+        }
+        // every copy issued has landed (bounded) before the staging buffers
+        // are released: at once when the producers consumed them, and on the
+        // way out of a wait that ran out
+        for (int64_t t = max((int64_t)0, issued - kTuStages); t < issued; ++t)
+            mbar_wait_bounded(stf0 + 8 * (int)(t % kTuStages), (uint32_t)((t / kTuStages) & 1), kWaitLimitNs, p.err,
+                              kErrScanWait);
     }
     tc_fence_before_sync();
     __syncthreads();
