@@ -4,7 +4,7 @@
 // real-world performance" and "Applications"; the decode logit estimator
 // l = n (<q', c[idx]> + sqrt(pi/2)/m * gamma <u, 2z - 1>) per database row),
 // computed as a dense contraction: for a tile of 128 database rows and a
-// block of 32 queries,
+// block of 64 queries,
 //     D[row][2j + s] = sum_i A[row][i] B[2j + s][i]
 // with A the de-quantized rows (lam * centroid as fp16, from a pair table;
 // the fp16 residual of lam * centroid as a second table when the codebook
@@ -13,20 +13,21 @@
 // parts, lam * kappa * u against the sign part). The score is
 // n * (D[row][2j] + D[row][2j + 1]) / lam.
 //
-// Warp-specialised CTA (32 queries, a chunk of database rows, 128-row tiles):
+// Warp-specialised CTA (64 queries, a chunk of database rows, 128-row tiles):
 //  * copy warp: bulk copies of each tile's packed codes and signs into a
 //    ring of staging buffers;
 //  * MMA warp: the MMAs (tcgen05.mma, A read from tensor memory, B = the
-//    queries resident in shared memory) into one of two 128 x 64 fp32 TMEM
+//    queries resident in shared memory) into one of two 128 x 128 fp32 TMEM
 //    accumulators, committed to mbarriers (kept free of other work, since
 //    its thread waits while the tensor core takes each MMA);
 //  * 8 producer warps: de-quantize each A segment of a tile straight into
 //    tensor memory (tcgen05.st; row r in TMEM lane r, two fp16 per column)
 //    through a ring of segment slots, so the de-quantized tile never touches
 //    shared memory;
-//  * 8 epilogue warps: read a finished accumulator (tcgen05.ld) and keep
-//    per-warp top-k lists of their rows, merged per query at the end of the
-//    chunk into its candidates.
+//  * 16 epilogue warps: read a finished accumulator (tcgen05.ld) and keep
+//    per-warp top-k lists of their rows (in shared memory, with the k-th
+//    score of each in registers as the admission threshold), merged per
+//    query at the end of the chunk into its candidates.
 // The roles hand over through mbarriers (full / empty pairs); every wait is
 // bounded, and a wait that runs out stops the CTA after draining what it has
 // in flight.
@@ -37,17 +38,17 @@
 namespace tqk {
 
 constexpr int kTuRows = 128;            // database rows per tile (MMA M, TMEM lanes)
-constexpr int kTuQ = 32;                // queries per CTA
+constexpr int kTuQ = 64;                // queries per CTA
 constexpr int kTuN = 2 * kTuQ;          // MMA N: hi and lo column per query
 constexpr int kTuProd = 8;              // producer warps
-constexpr int kTuEpi = 8;               // epilogue warps
+constexpr int kTuEpi = 16;              // epilogue warps (4 per TMEM lane quarter)
 constexpr int kTuCtl = kTuProd + kTuEpi;  // the MMA warp's index
 constexpr int kTuCopy = kTuCtl + 1;       // the copy warp's index
 constexpr int kTuWarps = kTuCopy + 1;
 constexpr int kTuThreads = 32 * kTuWarps;
-constexpr int kTuQpw = kTuQ / 2;        // queries per epilogue warp
+constexpr int kTuQpw = kTuQ / 4;        // queries per epilogue warp (16)
 constexpr int kTuStages = 4;            // staging buffers
-constexpr int kTuASlots = 3;            // A segment slots in TMEM
+constexpr int kTuASlots = 2;            // A segment slots in TMEM (after the two accumulators)
 constexpr uint32_t kTuCols = 512;       // TMEM columns held by the CTA
 constexpr int kTuSmemLimit = 227 * 1024 - 4096;  // dynamic part; static part below 4 KB
 constexpr int kTuSmemMin = 116 * 1024;  // at most one CTA per SM: it holds all of TMEM
@@ -306,21 +307,23 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
         }
     } else if (warp < kTuCtl) {
         // ================= epilogue =================
-        const int ew = warp - kTuProd;           // 0..7
+        const int ew = warp - kTuProd;           // 0..15: quarter ew % 4, query group ew / 4
         const int er = 32 * (warp & 3) + lane;   // this thread's row (TMEM lane)
-        const int jq0 = kTuQpw * (ew >> 2);      // its queries jq0 .. jq0 + 15
+        const int jq0 = kTuQpw * (ew >> 2);      // its queries jq0 .. jq0 + kTuQpw - 1
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        // top-k list of each query over this warp's rows, spread over the
-        // lanes (lane e holds entry e, best first); thr_s: the k-th score
-        float lsc[kTuQpw];
-        int lid[kTuQpw];
+        // top-k list of each query over this warp's rows in shared memory
+        // (entries best first) and, in registers, its k-th score: the
+        // admission threshold
+        float* const wls = s_ls + ew * kTuQpw * k;
+        int* const wli = s_li + ew * kTuQpw * k;
+        for (int e = lane; e < kTuQpw * k; e += 32) {
+            wls[e] = -INFINITY;
+            wli[e] = 0x7fffffff;
+        }
+        __syncwarp();
         float thr_s[kTuQpw];
 #pragma unroll
-        for (int jj = 0; jj < kTuQpw; ++jj) {
-            lsc[jj] = -INFINITY;
-            lid[jj] = 0x7fffffff;
-            thr_s[jj] = -INFINITY;
-        }
+        for (int jj = 0; jj < kTuQpw; ++jj) thr_s[jj] = -INFINITY;
         uint16_t n_next = 0;
         if (ntile > 0 && r0 + er < r1) n_next = p.norm[r0 + er];
         for (int64_t t = 0; t < ntile; ++t) {
@@ -335,14 +338,14 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
             }
             tc_fence_after_sync();
             const int id = (int)erow;
-            // two halves of 8 queries (16 columns) each, so that only 16
+            // four groups of 8 queries (16 columns) each, so that only 16
             // accumulator values are live at a time
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
+            for (int hf = 0; hf < kTuQpw / 8; ++hf) {
                 float v[16];
                 tmem_ld16(lane_addr + (uint32_t)(ab * kTuN + 2 * jq0 + 16 * hf), v);
                 tmem_ld_wait();
-                if (hf == 1) {
+                if (hf == kTuQpw / 8 - 1) {
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(ce0 + 8 * ab);  // the accumulator may be overwritten
@@ -362,42 +365,39 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
 #pragma unroll
                 for (int j8 = 0; j8 < 8; ++j8) {
                     const int jj = 8 * hf + j8;
-                    // the exact rule (equal scores: lower id first) is applied in the insert
                     unsigned cand = __ballot_sync(TQ_FULL_MASK, (mine >> j8) & 1u);
                     if (!cand) continue;
+                    float* const ls = wls + jj * k;
+                    int* const li = wli + jj * k;
                     while (cand) {
                         const int src = __ffs(cand) - 1;
                         cand &= cand - 1;
                         const float cs_ = __shfl_sync(TQ_FULL_MASK, sc[j8], src);
                         const int ci = __shfl_sync(TQ_FULL_MASK, id, src);
-                        const float ts = __shfl_sync(TQ_FULL_MASK, lsc[jj], k - 1);
-                        const int ti = __shfl_sync(TQ_FULL_MASK, lid[jj], k - 1);
+                        // lane e holds entry e; the exact rule (equal scores:
+                        // lower id first) decides against the k-th entry
+                        const float my = lane < k ? ls[lane] : -INFINITY;
+                        const int myi = lane < k ? li[lane] : 0x7fffffff;
+                        const float ts = __shfl_sync(TQ_FULL_MASK, my, k - 1);
+                        const int ti = __shfl_sync(TQ_FULL_MASK, myi, k - 1);
                         if (!better(cs_, ci, ts, ti)) continue;  // the list moved on since the test
-                        // entries better than the candidate stay, the rest move one lane down
-                        const int pos = __popc(__ballot_sync(TQ_FULL_MASK, lane < k && better(lsc[jj], lid[jj], cs_, ci)));
-                        const float us = __shfl_up_sync(TQ_FULL_MASK, lsc[jj], 1);
-                        const int ui = __shfl_up_sync(TQ_FULL_MASK, lid[jj], 1);
-                        if (lane == pos) {
-                            lsc[jj] = cs_;
-                            lid[jj] = ci;
-                        } else if (lane > pos) {
-                            lsc[jj] = us;
-                            lid[jj] = ui;
+                        // entries better than the candidate stay, the rest move one slot down
+                        const int pos = __popc(__ballot_sync(TQ_FULL_MASK, lane < k && better(my, myi, cs_, ci)));
+                        if (lane >= pos && lane < k - 1) {
+                            ls[lane + 1] = my;
+                            li[lane + 1] = myi;
                         }
+                        if (lane == pos) {
+                            ls[lane] = cs_;
+                            li[lane] = ci;
+                        }
+                        __syncwarp();
                     }
-                    thr_s[jj] = __shfl_sync(TQ_FULL_MASK, lsc[jj], k - 1);
+                    thr_s[jj] = ls[k - 1];
                 }
             }
             if (*abort_flag) break;
         }
-        float* wls = s_ls + ew * kTuQpw * k;
-        int* wli = s_li + ew * kTuQpw * k;
-#pragma unroll
-        for (int jj = 0; jj < kTuQpw; ++jj)
-            if (lane < k) {
-                wls[jj * k + lane] = lsc[jj];
-                wli[jj * k + lane] = lid[jj];
-            }
     } else if (warp == kTuCtl && lane == 0) {
         // ================= MMA issue =================
         const uint32_t idesc = umma_idesc_f16(kTuRows, kTuN);
