@@ -142,6 +142,24 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of a list of floats over the ranks of the default
+    process group (the slowest rank's times); the values themselves on one rank."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(world_size, units_per_step, steps, total_ms):
+    """Whole-job units per second: each of world_size replicas processed
+    units_per_step per step for `steps` steps in total_ms (the slowest rank's)."""
+    return world_size * units_per_step * steps / (total_ms / 1e3)
+
+
 # --------------------------------------------------------------- tq arm ----
 def run_tq(args):
     import torch
@@ -314,13 +332,10 @@ def run_tq(args):
     h2d = h_in.numel() * h_in.element_size()
     d2h = h_out.numel() * h_out.element_size()
 
-    # max over ranks
-    t = torch.tensor([total_ms, e2e_ms, q_ms], dtype=torch.float64, device="cuda")
-    if ws > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms, q_ms = t.tolist()
+    # the slowest rank's times
+    total_ms, e2e_ms, q_ms = max_over_ranks([total_ms, e2e_ms, q_ms], "cuda")
     tokens_per_step = bsz * T
-    value = ws * tokens_per_step * K / (total_ms / 1e3)
+    value = job_throughput(ws, tokens_per_step, K, total_ms)
 
     peak, peak_kind = _peaks()
     scan_alg = rows * T * ((w["k_bits"] - 1) * d // 8 + d // 8 + 4 + w["v_bits"] * d // 8 + 2) + bsz * hq * 2 * d * 4
@@ -347,7 +362,7 @@ def run_tq(args):
                                       f"and V ({w['v_bits']}-bit MSE), bf16 in, {w['rotation']}"),
                          "roofline": {"bound": "hbm", "achieved": q_achieved, "peak": peak, "unit": "GB/s",
                                       "frac": q_achieved / peak, "alg_bytes_per_call": q_alg_bytes}},
-            "e2e": {"value": ws * tokens_per_step / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "e2e": {"value": job_throughput(ws, tokens_per_step, 1, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": ne},
             "gpu_launches": launches_per_step * K,
             "host_us_per_step": host_s / K * 1e6,

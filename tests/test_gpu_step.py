@@ -119,3 +119,60 @@ def test_step_rejects_bad_args_before_enqueueing():
         B.tq_decode_step(q, kc, vc, lens, cap, rot, qjl, out, knew, vnew, pos, ws[:16])
     torch.cuda.synchronize()
     assert torch.equal(kc.codes, before)
+
+
+def test_full_size_step_sampled():
+    """The benchmarked step at its full shape and in its launch configuration
+    (1 x 32 q / 8 KV heads, 32768 tokens, K 3-bit PROD / V 3-bit MSE, RHT,
+    the new token appended at the last slot): sampled query heads, and the
+    appended slot's packed bytes, against the oracle."""
+    d, bsz, hkv, hq, T, kind = 128, 1, 8, 32, 32768, "rht"
+    k, v = W.decode_kv(bsz, hkv, T, seed=5)
+    rot, qjl = P.handles(d, kind)
+    kc = B.Cache("prod", 3, d, rows=bsz * hkv, capacity=T)
+    vc = B.Cache("mse", 3, d, rows=bsz * hkv, capacity=T)
+    # the context up to slot T - 2 comes from the GPU's cache fill; slot T - 1 from the step
+    B.tq_quantize_kv(kc, rot, torch.from_numpy(k.reshape(-1, d)).cuda().to(torch.bfloat16), qjl=qjl)
+    B.tq_quantize_kv(vc, rot, torch.from_numpy(v.reshape(-1, d)).cuda().to(torch.bfloat16))
+    q = torch.from_numpy(W.query_vectors((bsz, hq, d), dtype="bf16", seed=6)).cuda().to(torch.bfloat16)
+    knew = torch.from_numpy(W.round_bf16(W.query_vectors((bsz * hkv, d), seed=7) * 2)).cuda().to(torch.bfloat16)
+    vnew = torch.from_numpy(W.round_bf16(W.query_vectors((bsz * hkv, d), seed=8))).cuda().to(torch.bfloat16)
+    pos = torch.full((bsz,), T - 1, dtype=torch.int32, device="cuda")
+    lens = torch.full((bsz,), T, dtype=torch.int32, device="cuda")
+    out = torch.empty((bsz, hq, d), device="cuda")
+    ws = B.workspace(B.tq_decode_step_workspace(q, kc, vc, lens, T, rot, qjl, out, knew, vnew, pos))
+    B.tq_decode_step(q, kc, vc, lens, T, rot, qjl, out, knew, vnew, pos, ws)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+
+    pi, s = P.oracle_mats(d, kind)
+    kn = knew.float().cpu().numpy().reshape(hkv, d)
+    vn = vnew.float().cpu().numpy().reshape(hkv, d)
+    qn = q.float().cpu().numpy()
+    # the appended slot: the GPU's packed record against the oracle's quantization of the new token
+    got_k = P.cache_to_numpy(kc, hkv * T)
+    got_v = P.cache_to_numpy(vc, hkv * T)
+    last = np.arange(hkv) * T + (T - 1)
+    for name, mode, xn, g in (("k", "prod", kn, got_k), ("v", "mse", vn, got_v)):
+        qz = oq.quantize(xn.astype(np.float64), pi, mode, 3, s if mode == "prod" else None)
+        sub = {key: val[last] for key, val in g.items()}
+        rep = P.compare_quantized(sub, qz, mode, 3, d, s, label=f"appended-{name}")
+        assert rep["code_mismatch"] == 0
+    scale = None
+    for h in (0, 17, 31):
+        kv = h // (hq // hkv)
+        kx = k[0, kv].copy()
+        vx = v[0, kv].copy()
+        kx[T - 1] = kn[kv]
+        vx[T - 1] = vn[kv]
+        kq = oq.quantize(W.round_bf16(kx).astype(np.float64), pi, "prod", 3, s)
+        vq = oq.quantize(W.round_bf16(vx).astype(np.float64), pi, "mse", 3)
+        qp, u = oa.query_prep(qn[0, h].astype(np.float64), pi, s)
+        lg = oa.key_logits(qp, u, kq["idx"], kq["norm16"], kq["centroids"], kq["rnorm16"], kq["z"], d)
+        vhat = vq["norm16"][:, None] * vq["centroids"][vq["idx"]]
+        sc = lg / np.sqrt(d)
+        pr = np.exp(sc - sc.max())
+        pr /= pr.sum()
+        want = (pr @ vhat) @ pi
+        scale = np.max(vq["norm16"]) / np.sqrt(d)
+        assert np.max(np.abs(got[0, h] - want)) <= OUT_TOL * scale, (h, np.max(np.abs(got[0, h] - want)) / scale)
