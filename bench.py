@@ -318,22 +318,42 @@ def run_tq(args):
     ne = 3 if args.quick else max(20, min(K, 200))
     h_in = inbuf.cpu().pin_memory()  # query | new keys | new values, as a caller would stage them
     h_out = torch.empty_like(out, device="cpu").pin_memory()
+    # (a) the step on pinned host buffers: its kernels read the query and the
+    # new K and V from host memory and write the output there (no copy
+    # operations; the bytes cross the CPU-GPU link inside the kernels)
+    da_h, _keep_h = B._decode_struct(h_in[: q.numel()].view(q.shape), kc, vc, lens, T, rot, qjl, h_out)
+    sa_h = B.tq_step_args()
+    sa_h.attn = da_h
+    sa_h.k_new = h_in.data_ptr() + q.numel() * 2
+    sa_h.v_new = h_in.data_ptr() + (q.numel() + knew.numel()) * 2
+    sa_h.new_dtype = B.TQ_BF16
+    sa_h.append_pos = append.data_ptr()
     eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ne)]
     for i in range(ne):
         flush.fill_(i & 0xFF)
         eev[i][0].record(stream)
+        check(L.tq_decode_step(ctypes.byref(sa_h), wsb.data_ptr(), wsz, sp), "decode step (host buffers)")
+        eev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in eev)
+    # (b) the same with explicit copies: host -> device into the step's
+    # device buffers, the step, device -> host of the output
+    mev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ne)]
+    for i in range(ne):
+        flush.fill_(i & 0xFF)
+        mev[i][0].record(stream)
         inbuf.copy_(h_in, non_blocking=True)
         step()
         h_out.copy_(out, non_blocking=True)
-        eev[i][1].record(stream)
+        mev[i][1].record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
-    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in eev)
+    e2e_copy_ms = statistics.mean(a.elapsed_time(b) for a, b in mev)
     h2d = h_in.numel() * h_in.element_size()
     d2h = h_out.numel() * h_out.element_size()
 
     # the slowest rank's times
-    total_ms, e2e_ms, q_ms = max_over_ranks([total_ms, e2e_ms, q_ms], "cuda")
+    total_ms, e2e_ms, e2e_copy_ms, q_ms = max_over_ranks([total_ms, e2e_ms, e2e_copy_ms, q_ms], "cuda")
     tokens_per_step = bsz * T
     value = job_throughput(ws, tokens_per_step, K, total_ms)
 
@@ -363,7 +383,12 @@ def run_tq(args):
                          "roofline": {"bound": "hbm", "achieved": q_achieved, "peak": peak, "unit": "GB/s",
                                       "frac": q_achieved / peak, "alg_bytes_per_call": q_alg_bytes}},
             "e2e": {"value": job_throughput(ws, tokens_per_step, 1, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": ne},
+                    "d2h_bytes_per_step": d2h, "steps": ne,
+                    "transfer": "zero-copy: the step's kernels read the query and the new K and V from pinned host "
+                                "memory and write the output to pinned host memory (CPU-GPU link inside the kernels)",
+                    "with_memcpy": {"value": job_throughput(ws, tokens_per_step, 1, e2e_copy_ms), "unit": UNIT,
+                                    "transfer": "cudaMemcpyAsync host->device of the inputs and device->host of "
+                                                "the output around the step, on its stream"}},
             "gpu_launches": launches_per_step * K,
             "host_us_per_step": host_s / K * 1e6,
             "clocks": clocks,

@@ -201,7 +201,8 @@ tq_status tq_quantize_kv(const tq_quant_args* a, tq_stream stream);
  * Split-K over tokens: CTAs write partial (max, sum, a) to the workspace; a
  * second launch merges them and un-rotates. */
 typedef struct {
-    const void* q;          /* device [batch][hq][d] of q_dtype               */
+    const void* q;          /* device [batch][hq][d] of q_dtype (or pinned host
+                               memory the GPU addresses, see below)           */
     int q_dtype;            /* TQ_F32 or TQ_BF16                              */
     int batch, hq, hkv, d;  /* d = 128                                        */
     const int32_t* seq_lens;/* device int32 [batch], each in [0, capacity]    */
@@ -215,7 +216,8 @@ typedef struct {
     tq_cache v;             /* MSE cache, rows == batch*hkv                   */
     float scale;            /* softmax scale; 0 -> 1/sqrt(d)                  */
     int n_splits;           /* token splits per (b, KV head); 0 -> automatic  */
-    void* out;              /* device [batch][hq][d] of out_dtype             */
+    void* out;              /* device [batch][hq][d] of out_dtype (or pinned
+                               host memory the GPU addresses, see below)      */
     int out_dtype;          /* TQ_F32 or TQ_BF16                              */
     float* logits;          /* optional device fp32 [batch][hq][max_seq_len]:
                                raw l_t (before scale) for t < seq_lens[b]    */
@@ -263,7 +265,13 @@ tq_status tq_attn_decode_static(const tq_decode_args* a, tq_stream stream);
  * tq_quantize_kv(V) and tq_attn_decode on one stream when batch * hkv is at
  * most 256 (up to that count tq_quantize_kv takes the same per-vector
  * kernel). All of the step's work is ordered after what precedes the call
- * on `stream` and before what follows it (also under CUDA graph capture). */
+ * on `stream` and before what follows it (also under CUDA graph capture).
+ * q, k_new, v_new and out may be pinned host memory that the GPU addresses
+ * directly (cudaHostAlloc / cudaHostRegister under unified addressing; on a
+ * Grace-Blackwell node the host memory is reached over NVLink-C2C): the
+ * kernels then read the inputs and write the output there, with no copy
+ * operation, and the output is in host memory once the step's work on
+ * `stream` has completed. Same results, bit for bit, as on device buffers. */
 typedef struct {
     tq_decode_args attn;        /* the attention call: caches, q, lengths, out */
     const void* k_new;          /* device [batch*hkv][d] keys of the new token,

@@ -176,3 +176,30 @@ def test_full_size_step_sampled():
         want = (pr @ vhat) @ pi
         scale = np.max(vq["norm16"]) / np.sqrt(d)
         assert np.max(np.abs(got[0, h] - want)) <= OUT_TOL * scale, (h, np.max(np.abs(got[0, h] - want)) / scale)
+
+
+def test_step_with_pinned_host_io():
+    """The step's query, new keys and values and its output may live in pinned
+    host memory, which the GPU addresses directly (unified addressing; on a
+    Grace-Blackwell node over NVLink-C2C): the kernels read the inputs and
+    write the output there, with no copy. Same results, bit for bit, as the
+    same step on device buffers."""
+    bsz, hkv, hq, cap = 2, 2, 8, 512
+    k, v, rot, qjl, caches, q, knew, vnew = _setup(bsz, hkv, hq, cap, "rht", 3, 3, seed=80)
+    pos = torch.tensor([200, 511], dtype=torch.int32, device="cuda")
+    lens = torch.tensor([201, 512], dtype=torch.int32, device="cuda")
+    (kc, vc) = caches[0]
+    out0 = torch.empty((bsz, hq, 128), device="cuda")
+    ws0 = B.workspace(B.tq_decode_step_workspace(q, kc, vc, lens, cap, rot, qjl, out0, knew, vnew, pos))
+    B.tq_decode_step(q, kc, vc, lens, cap, rot, qjl, out0, knew, vnew, pos, ws0)
+    (kc1, vc1) = caches[1]
+    qh, kh, vh = q.cpu().pin_memory(), knew.cpu().pin_memory(), vnew.cpu().pin_memory()
+    outh = torch.full((bsz, hq, 128), float("nan")).pin_memory()
+    ws1 = B.workspace(B.tq_decode_step_workspace(qh, kc1, vc1, lens, cap, rot, qjl, outh, kh, vh, pos))
+    B.tq_decode_step(qh, kc1, vc1, lens, cap, rot, qjl, outh, kh, vh, pos, ws1)
+    torch.cuda.synchronize()
+    assert torch.equal(out0.cpu(), outh)
+    for name in ("codes", "signs", "norm", "rnorm"):
+        assert torch.equal(getattr(kc, name), getattr(kc1, name)), f"K {name}"
+    for name in ("codes", "norm"):
+        assert torch.equal(getattr(vc, name), getattr(vc1, name)), f"V {name}"
