@@ -18,12 +18,13 @@ constexpr int kPrepWarps = 8;
 // The decode scan's B operands of one query row (d = m = 128), in the order
 // its threads load them: word ((ks * 2 + lo) * 4 + c) * 16 + 2 * kk + r holds
 // the fp16 pair (coordinates i, i + 1), i = 32c + 4kk + 2r, of the hi (lo =
-// 0) or lo (lo = 1) split of q' (ks = 0) or of qjl_scale * u (ks = 1). The
-// 256 threads of the CTA write one word each; u == NULL gives zero words.
+// 0) or lo (lo = 1) split of q' (ks = 0) or of qjl_scale * u (ks = 1). Writes
+// word `wi` (0 .. kFragWords - 1) from q' and u in shared memory; u == NULL
+// gives zero words.
 __device__ __forceinline__ void write_frag(const PrepParams& p, int64_t row, const float* s_q, const float* s_u,
-                                           int tid) {
-    if (tid >= kFragWords) return;
-    const int ks = tid >> 7, lo = (tid >> 6) & 1, c = (tid >> 4) & 3, kk = (tid >> 1) & 7, r = tid & 1;
+                                           int wi) {
+    if (wi >= kFragWords) return;
+    const int ks = wi >> 7, lo = (wi >> 6) & 1, c = (wi >> 4) & 3, kk = (wi >> 1) & 7, r = wi & 1;
     const int i = 32 * c + 4 * kk + 2 * r;
     uint32_t w = 0u;
     if (ks == 0) {
@@ -31,11 +32,12 @@ __device__ __forceinline__ void write_frag(const PrepParams& p, int64_t row, con
     } else if (s_u) {
         w = half_split(s_u[i] * p.qjl_scale, lo) | (half_split(s_u[i + 1] * p.qjl_scale, lo) << 16);
     }
-    p.frag[row * kFragWords + tid] = w;
+    p.frag[row * kFragWords + wi] = w;
 }
 
 // ---------------------------------------------------------------------------
-// One CTA (256 threads) per query row. Lane l of every warp owns outputs VPL*l..VPL*l+VPL-1
+// The search's query prep (any d <= 256): one CTA (256 threads) per query
+// row. Lane l of every warp owns outputs VPL*l..VPL*l+VPL-1
 // and warp w accumulates the inputs j = w, w+8, ...: the rows of the
 // transposed matrices are read with independent loads, all in flight at once,
 // and the 8 partial vectors are summed through shared memory.
@@ -121,10 +123,7 @@ __device__ __forceinline__ void prep_row(const PrepParams& p, int64_t row) {
     __syncthreads();
     if (p.qprime)
         for (int i = tid; i < d; i += blockDim.x) p.qprime[row * d + i] = s_y[i];
-    if (p.st32 == nullptr) {
-        if (p.frag) write_frag(p, row, s_y, nullptr, tid);
-        return;
-    }
+    if (p.st32 == nullptr) return;
     // u = S q': warp w takes inputs i = w, w+8, ...; lane owns outputs MPL*lane + r
     const int m = p.m, mpl = (m + 31) >> 5;
     float acc[8];
@@ -160,11 +159,6 @@ __device__ __forceinline__ void prep_row(const PrepParams& p, int64_t row) {
 #pragma unroll
         for (int w = 0; w < kPrepWarps; ++w) u += s_part[w][j];
         if (p.u) p.u[row * m + j] = u;
-        s_x[j] = u;  // s_x is free by now
-    }
-    if (p.frag) {
-        __syncthreads();
-        write_frag(p, row, s_y, s_x, tid);
     }
 }
 

@@ -49,6 +49,20 @@ __device__ __forceinline__ void cp_async16_zfill(uint32_t smem_addr, const void*
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_addr), "l"(gptr), "r"(valid ? 16 : 0));
 }
 
+// packed fp32 pairs (one instruction for two lanes of a register pair);
+// each lane rounds exactly as the scalar operation would
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+// (a + b, a - b) for both lanes of the pairs, bit-identical to the scalar forms
+__device__ __forceinline__ void butterfly2(float& a0, float& a1, float& b0, float& b1) {
+    const float2 a = f2(a0, a1), b = f2(b0, b1);
+    const float2 s = __fadd2_rn(a, b);
+    const float2 d = __ffma2_rn(b, f2(-1.0f, -1.0f), a);  // a - b, one rounding
+    a0 = s.x;
+    a1 = s.y;
+    b0 = d.x;
+    b1 = d.y;
+}
+
 // two floats -> bf16 pair (lo half = a), round to nearest even
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -197,9 +211,13 @@ __global__ void __launch_bounds__(kQmWarps * 32, 3) quantize_mma_kernel(const __
         float n32[2], inv_n[2];
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
-            float ss = 0.0f;
+            float2 s2v = f2(0.0f, 0.0f);  // even and odd coordinates, packed
 #pragma unroll
-            for (int j = 0; j < 32; ++j) ss = fmaf(y[rr][j], y[rr][j], ss);
+            for (int j = 0; j < 32; j += 2) {
+                const float2 v = f2(y[rr][j], y[rr][j + 1]);
+                s2v = __ffma2_rn(v, v, s2v);
+            }
+            float ss = s2v.x + s2v.y;
             ss += __shfl_xor_sync(TQ_FULL_MASK, ss, 1);
             ss += __shfl_xor_sync(TQ_FULL_MASK, ss, 2);
             n32[rr] = sqrtf(ss);
@@ -229,32 +247,43 @@ __global__ void __launch_bounds__(kQmWarps * 32, 3) quantize_mma_kernel(const __
                 for (int j = 0; j < 32; ++j)
                     y[rr][j] = __int_as_float(__float_as_int(y[rr][j]) ^ (int)((sgm << (31 - j)) & 0x80000000u));
 #pragma unroll
-            for (int h = 1; h < 32; h <<= 1)
+            for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {  // stride 1: within a pair
+                    const float a = y[rr][j], b = y[rr][j + 1];
+                    y[rr][j] = a + b;
+                    y[rr][j + 1] = a - b;
+                }
+#pragma unroll
+            for (int h = 2; h < 32; h <<= 1)  // strides 2..16: two butterflies per packed pair
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if ((j & h) == 0) {
-                            const float a = y[rr][j], b = y[rr][j + h];
-                            y[rr][j] = a + b;
-                            y[rr][j + h] = a - b;
-                        }
+                    for (int j = 0; j < 32; j += 2)
+                        if ((j & h) == 0) butterfly2(y[rr][j], y[rr][j + 1], y[rr][j + h], y[rr][j + h + 1]);
 #pragma unroll
             for (int hb = 1; hb < 4; hb <<= 1) {
                 const float sgn_self = (c & hb) ? -1.0f : 1.0f;  // upper half: o - y
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float o = __shfl_xor_sync(TQ_FULL_MASK, y[rr][j], hb);
-                        y[rr][j] = fmaf(sgn_self, y[rr][j], o);
+                    for (int j = 0; j < 32; j += 2) {
+                        const float o0 = __shfl_xor_sync(TQ_FULL_MASK, y[rr][j], hb);
+                        const float o1 = __shfl_xor_sync(TQ_FULL_MASK, y[rr][j + 1], hb);
+                        const float2 r = __ffma2_rn(f2(sgn_self, sgn_self), f2(y[rr][j], y[rr][j + 1]), f2(o0, o1));
+                        y[rr][j] = r.x;
+                        y[rr][j + 1] = r.y;
                     }
             }
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
                 const float sc = p.inv_sqrt_d * inv_n[rr];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) y[rr][j] *= sc;
+                for (int j = 0; j < 32; j += 2) {
+                    const float2 r = __fmul2_rn(f2(y[rr][j], y[rr][j + 1]), f2(sc, sc));
+                    y[rr][j] = r.x;
+                    y[rr][j + 1] = r.y;
+                }
             }
         } else {
             if (!frags()) {  // the fragments never landed (the error word says so)
@@ -492,9 +521,13 @@ __global__ void __launch_bounds__(kQmWarps * 32, 3) quantize_mma_kernel(const __
             float gam[2];
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
-                float g2 = 0.0f;
+                float2 g2v = f2(0.0f, 0.0f);  // even and odd coordinates, packed
 #pragma unroll
-                for (int j = 0; j < 32; ++j) g2 = fmaf(y[rr][j], y[rr][j], g2);
+                for (int j = 0; j < 32; j += 2) {
+                    const float2 v = f2(y[rr][j], y[rr][j + 1]);
+                    g2v = __ffma2_rn(v, v, g2v);
+                }
+                float g2 = g2v.x + g2v.y;
                 g2 += __shfl_xor_sync(TQ_FULL_MASK, g2, 1);
                 g2 += __shfl_xor_sync(TQ_FULL_MASK, g2, 2);
                 gam[rr] = sqrtf(g2);
