@@ -416,3 +416,69 @@ def workspace(nbytes, device="cuda"):
     import torch
 
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+class QuantizedKVCache:
+    """One attention layer's packed KV cache with the decode loop's two calls:
+    `prefill` quantizes a context into it and `step` appends one token per
+    batch row and attends (the write-ups' "quantize on every cache update,
+    then attend"; tq_quantize_kv and tq_decode_step). Keys are PROD (k_bits,
+    QJL signs), values MSE (v_bits); both share one rotation. The per-row
+    lengths live on the device; this class only keeps the handles, the
+    planes and a workspace, and forms the calls' arguments."""
+
+    def __init__(self, batch, hq, hkv, capacity, d=128, k_bits=3, v_bits=3, rotation="rht", rot_seed=1, qjl_seed=2,
+                 device="cuda"):
+        import torch
+
+        if hq % hkv:
+            raise ValueError("hq must be a multiple of hkv")
+        self.batch, self.hq, self.hkv, self.capacity, self.d = batch, hq, hkv, capacity, d
+        self.rot = tq_rotation_to_device(tq_make_rotation(rot_seed, d, rotation))
+        self.qjl = tq_qjl_to_device(tq_make_qjl(qjl_seed, d, d))
+        self.k = Cache("prod", k_bits, d, rows=batch * hkv, capacity=capacity, device=device)
+        self.v = Cache("mse", v_bits, d, rows=batch * hkv, capacity=capacity, device=device)
+        self.lengths = torch.zeros(batch, dtype=torch.int32, device=device)
+        self._ws = None
+
+    def prefill(self, k, v, lengths):
+        """k, v: device [batch, hkv, T, d] (f32 or bf16), T <= capacity; row b
+        holds lengths[b] valid tokens (a host sequence of ints)."""
+        import torch
+
+        b, h, t, d = k.shape
+        if (b, h, d) != (self.batch, self.hkv, self.d) or tuple(v.shape) != tuple(k.shape) or t > self.capacity:
+            raise ValueError("k and v must be [batch, hkv, T <= capacity, d]")
+        lens = [int(x) for x in lengths]
+        if len(lens) != b or min(lens) < 0 or max(lens) > t:
+            raise ValueError("lengths must give 0 <= length <= T per batch row")
+        # slot of token j of (b, h): (b * hkv + h) * capacity + j; tokens past a row's length are skipped
+        j = torch.arange(t, device=k.device, dtype=torch.int64)
+        rows = torch.arange(b * h, device=k.device, dtype=torch.int64)
+        slots = rows[:, None] * self.capacity + j[None, :]
+        valid = j[None, :] < torch.tensor(lens, device=k.device, dtype=torch.int64).repeat_interleave(h)[:, None]
+        slots = torch.where(valid, slots, torch.full_like(slots, -1)).reshape(-1).contiguous()
+        tq_quantize_kv(self.k, self.rot, k.reshape(-1, d), qjl=self.qjl, dst_slot=slots)
+        tq_quantize_kv(self.v, self.rot, v.reshape(-1, d), dst_slot=slots)
+        self.lengths.copy_(torch.tensor(lens, dtype=torch.int32))
+
+    def step(self, q, k_new, v_new, out=None, stream=None):
+        """Appends k_new / v_new (device [batch, hkv, d]) at each row's current
+        length and attends with q (device [batch, hq, d]); returns out
+        ([batch, hq, d], fp32 unless given). The caller keeps every length
+        below the capacity."""
+        import torch
+
+        if out is None:
+            out = torch.empty((self.batch, self.hq, self.d), dtype=torch.float32, device=q.device)
+        kn = k_new.reshape(self.batch * self.hkv, self.d)
+        vn = v_new.reshape(self.batch * self.hkv, self.d)
+        new_lens = self.lengths + 1
+        need = tq_decode_step_workspace(q, self.k, self.v, new_lens, self.capacity, self.rot, self.qjl, out, kn, vn,
+                                        self.lengths)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = workspace(need, device=q.device)
+        tq_decode_step(q, self.k, self.v, new_lens, self.capacity, self.rot, self.qjl, out, kn, vn, self.lengths,
+                       self._ws, stream=stream)
+        self.lengths = new_lens
+        return out

@@ -203,3 +203,43 @@ def test_step_with_pinned_host_io():
         assert torch.equal(getattr(kc, name), getattr(kc1, name)), f"K {name}"
     for name in ("codes", "norm"):
         assert torch.equal(getattr(vc, name), getattr(vc1, name)), f"V {name}"
+
+
+def test_quantized_kv_cache_wrapper_matches_the_calls():
+    """QuantizedKVCache.prefill + step equal the tq_quantize_kv / tq_decode_step
+    calls they stand for, bit for bit, and the lengths advance by one."""
+    d, bsz, hkv, hq, cap, T0 = 128, 2, 2, 8, 256, 100
+    k, v = W.decode_kv(bsz, hkv, T0, seed=33)
+    kt = torch.from_numpy(k).cuda().to(torch.bfloat16)
+    vt = torch.from_numpy(v).cuda().to(torch.bfloat16)
+    c = B.QuantizedKVCache(bsz, hq, hkv, cap, d=d, k_bits=3, v_bits=3, rotation="rht")
+    c.prefill(kt, vt, [T0, 60])
+    # the same through the calls
+    kc = B.Cache("prod", 3, d, rows=bsz * hkv, capacity=cap)
+    vc = B.Cache("mse", 3, d, rows=bsz * hkv, capacity=cap)
+    slots = np.full((bsz, hkv, T0), -1, dtype=np.int64)
+    for b, n in enumerate([T0, 60]):
+        for h in range(hkv):
+            slots[b, h, :n] = (b * hkv + h) * cap + np.arange(n)
+    st = torch.from_numpy(slots.reshape(-1)).cuda()
+    B.tq_quantize_kv(kc, c.rot, kt.reshape(-1, d), qjl=c.qjl, dst_slot=st)
+    B.tq_quantize_kv(vc, c.rot, vt.reshape(-1, d), dst_slot=st)
+    lens = torch.tensor([T0, 60], dtype=torch.int32, device="cuda")
+    for s in range(3):
+        q = torch.from_numpy(W.query_vectors((bsz, hq, d), seed=40 + s)).cuda()
+        kn = torch.from_numpy(W.round_bf16(W.query_vectors((bsz, hkv, d), seed=50 + s))).cuda().to(torch.bfloat16)
+        vn = torch.from_numpy(W.round_bf16(W.query_vectors((bsz, hkv, d), seed=60 + s))).cuda().to(torch.bfloat16)
+        got = c.step(q, kn, vn)
+        out = torch.empty((bsz, hq, d), device="cuda")
+        new = lens + 1
+        ws = B.workspace(B.tq_decode_step_workspace(q, kc, vc, new, cap, c.rot, c.qjl, out,
+                                                    kn.reshape(-1, d), vn.reshape(-1, d), lens))
+        B.tq_decode_step(q, kc, vc, new, cap, c.rot, c.qjl, out, kn.reshape(-1, d), vn.reshape(-1, d), lens, ws)
+        lens = new
+        torch.cuda.synchronize()
+        assert torch.equal(got, out), s
+    assert c.lengths.tolist() == [T0 + 3, 63]
+    for name in ("codes", "signs", "norm", "rnorm"):
+        assert torch.equal(getattr(c.k, name), getattr(kc, name)), name
+    for name in ("codes", "norm"):
+        assert torch.equal(getattr(c.v, name), getattr(vc, name)), name
