@@ -593,7 +593,6 @@ __global__ void __launch_bounds__(kQmWarps * 32, 3) quantize_mma_kernel(const __
 
 template <typename XT, int CB, bool PROD, bool RHT>
 constexpr size_t quantize_mma_smem() {
-    constexpr int NLX = (!RHT && sizeof(XT) == 4) ? 3 : 1;
     return (RHT ? 0 : 3 * 8 * 16 * 32 * 8) + (PROD ? 8 * 16 * 32 * 8 : 0) +
            (size_t)qm_warps<XT, RHT>() * QmSmem<XT>::WARP_BYTES;
 }
