@@ -243,3 +243,33 @@ def test_quantized_kv_cache_wrapper_matches_the_calls():
         assert torch.equal(getattr(c.k, name), getattr(kc, name)), name
     for name in ("codes", "norm"):
         assert torch.equal(getattr(c.v, name), getattr(vc, name)), name
+
+
+def test_step_captured_in_a_cuda_graph():
+    """The step's three launches (the last two programmatic dependents) record
+    into a CUDA graph; a replay gives the same cache and output, bit for bit,
+    as the same step run eagerly."""
+    bsz, hkv, hq, cap = 2, 2, 8, 512
+    k, v, rot, qjl, caches, q, knew, vnew = _setup(bsz, hkv, hq, cap, "rht", 3, 3, seed=85)
+    pos = torch.tensor([123, 400], dtype=torch.int32, device="cuda")
+    lens = torch.tensor([124, 401], dtype=torch.int32, device="cuda")
+    (kc, vc) = caches[0]
+    out0 = torch.empty((bsz, hq, 128), device="cuda")
+    ws0 = B.workspace(B.tq_decode_step_workspace(q, kc, vc, lens, cap, rot, qjl, out0, knew, vnew, pos))
+    B.tq_decode_step(q, kc, vc, lens, cap, rot, qjl, out0, knew, vnew, pos, ws0)
+    (kc1, vc1) = caches[1]
+    out1 = torch.full((bsz, hq, 128), float("nan"), device="cuda")
+    ws1 = B.workspace(B.tq_decode_step_workspace(q, kc1, vc1, lens, cap, rot, qjl, out1, knew, vnew, pos))
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        B.tq_decode_step(q, kc1, vc1, lens, cap, rot, qjl, out1, knew, vnew, pos, ws1)
+    assert bool(torch.isnan(out1).all())  # captured, not run
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out0, out1)
+    for name in ("codes", "signs", "norm", "rnorm"):
+        assert torch.equal(getattr(kc, name), getattr(kc1, name)), f"K {name}"
+    for name in ("codes", "norm"):
+        assert torch.equal(getattr(vc, name), getattr(vc1, name)), f"V {name}"
+    assert B.tq_device_errors() == (B.TQ_OK, 0)
