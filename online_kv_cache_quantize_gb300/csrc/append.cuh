@@ -94,25 +94,26 @@ __device__ __forceinline__ void stage_s(const uint16_t* s16, StepSmem& s) {
 }
 
 // (S v)_j for j = threadIdx.x: row j of the staged S (exact bf16 -> fp32)
-// against v in shared memory, summed in coordinate order
+// against v in shared memory, as four interleaved partial sums (coordinates
+// 2q and 2q + 1 of each quarter of a 16-byte unit), added at the end
 __device__ __forceinline__ float s_row_dot(const StepSmem& s, const float* v) {
     const int j = threadIdx.x;
-    float z = 0.0f;
+    float z0 = 0.0f, z1 = 0.0f, z2 = 0.0f, z3 = 0.0f;
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
         const uint4 sr = s.s[q * kStepThreads + j];
         const float4 r0 = *reinterpret_cast<const float4*>(v + 8 * q);
         const float4 r1 = *reinterpret_cast<const float4*>(v + 8 * q + 4);
-        z = fmaf(__uint_as_float(sr.x << 16), r0.x, z);
-        z = fmaf(__uint_as_float(sr.x & 0xffff0000u), r0.y, z);
-        z = fmaf(__uint_as_float(sr.y << 16), r0.z, z);
-        z = fmaf(__uint_as_float(sr.y & 0xffff0000u), r0.w, z);
-        z = fmaf(__uint_as_float(sr.z << 16), r1.x, z);
-        z = fmaf(__uint_as_float(sr.z & 0xffff0000u), r1.y, z);
-        z = fmaf(__uint_as_float(sr.w << 16), r1.z, z);
-        z = fmaf(__uint_as_float(sr.w & 0xffff0000u), r1.w, z);
+        z0 = fmaf(__uint_as_float(sr.x << 16), r0.x, z0);
+        z0 = fmaf(__uint_as_float(sr.x & 0xffff0000u), r0.y, z0);
+        z1 = fmaf(__uint_as_float(sr.y << 16), r0.z, z1);
+        z1 = fmaf(__uint_as_float(sr.y & 0xffff0000u), r0.w, z1);
+        z2 = fmaf(__uint_as_float(sr.z << 16), r1.x, z2);
+        z2 = fmaf(__uint_as_float(sr.z & 0xffff0000u), r1.y, z2);
+        z3 = fmaf(__uint_as_float(sr.w << 16), r1.z, z3);
+        z3 = fmaf(__uint_as_float(sr.w & 0xffff0000u), r1.w, z3);
     }
-    return z;
+    return (z0 + z1) + (z2 + z3);
 }
 
 // (H t)_i for i = threadIdx.x over the 128 threads of the CTA (t is thread
@@ -182,11 +183,17 @@ __device__ __forceinline__ void append_vector(const QuantParams& p, int xdtype, 
     if (rht) {
         y = wht128(xi * p.sgn[i], s) * (p.inv_sqrt_d * inv_n);
     } else {
-        // row i of Pi is column i of Pi^T: coalesced over the threads
-        float acc = 0.0f;
-#pragma unroll 32
-        for (int e = 0; e < D; ++e) acc = fmaf(__ldg(p.pit32 + e * D + i), s.x[e], acc);
-        y = acc * inv_n;
+        // row i of Pi is column i of Pi^T: coalesced over the threads; four
+        // interleaved partial sums
+        float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+#pragma unroll 8
+        for (int e = 0; e < D; e += 4) {
+            a0 = fmaf(__ldg(p.pit32 + e * D + i), s.x[e], a0);
+            a1 = fmaf(__ldg(p.pit32 + (e + 1) * D + i), s.x[e + 1], a1);
+            a2 = fmaf(__ldg(p.pit32 + (e + 2) * D + i), s.x[e + 2], a2);
+            a3 = fmaf(__ldg(p.pit32 + (e + 3) * D + i), s.x[e + 3], a3);
+        }
+        y = ((a0 + a1) + (a2 + a3)) * inv_n;
     }
 
     // ---- bucketize with the guard band ----

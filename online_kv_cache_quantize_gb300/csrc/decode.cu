@@ -25,10 +25,15 @@ __device__ __forceinline__ void prep_row128(const PrepParams& p, int64_t row, St
     } else {
         s.x[i] = qi;
         step_sync();
-        float acc = 0.0f;
-#pragma unroll 32
-        for (int e = 0; e < D; ++e) acc = fmaf(__ldg(p.pit32 + e * D + i), s.x[e], acc);
-        y = acc;
+        float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;  // four interleaved partial sums
+#pragma unroll 8
+        for (int e = 0; e < D; e += 4) {
+            a0 = fmaf(__ldg(p.pit32 + e * D + i), s.x[e], a0);
+            a1 = fmaf(__ldg(p.pit32 + (e + 1) * D + i), s.x[e + 1], a1);
+            a2 = fmaf(__ldg(p.pit32 + (e + 2) * D + i), s.x[e + 2], a2);
+            a3 = fmaf(__ldg(p.pit32 + (e + 3) * D + i), s.x[e + 3], a3);
+        }
+        y = (a0 + a1) + (a2 + a3);
     }
     s.qp[i] = y;
     if (p.qprime) p.qprime[row * D + i] = y;
