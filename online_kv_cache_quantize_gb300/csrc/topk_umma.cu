@@ -338,8 +338,9 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
             }
             tc_fence_after_sync();
             const int id = (int)erow;
-            // four groups of 8 queries (16 columns) each, so that only 16
-            // accumulator values are live at a time
+            // two groups of 8 queries (16 columns) each, so that only 16
+            // accumulator values are live at a time (releasing the accumulator
+            // before any compute was measured slower)
 #pragma unroll
             for (int hf = 0; hf < kTuQpw / 8; ++hf) {
                 float v[16];
