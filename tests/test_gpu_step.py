@@ -121,16 +121,24 @@ def test_step_rejects_bad_args_before_enqueueing():
     assert torch.equal(kc.codes, before)
 
 
-def test_full_size_step_sampled():
-    """The benchmarked step at its full shape and in its launch configuration
-    (1 x 32 q / 8 KV heads, 32768 tokens, K 3-bit PROD / V 3-bit MSE, RHT,
-    the new token appended at the last slot): sampled query heads, and the
-    appended slot's packed bytes, against the oracle."""
-    d, bsz, hkv, hq, T, kind = 128, 1, 8, 32, 32768, "rht"
-    k, v = W.decode_kv(bsz, hkv, T, seed=5)
+@pytest.mark.parametrize("bsz,hkv,hq,T,kbits,vbits,heavy,samples", [
+    # the bench's default line: Llama-3.1-8B decode, 32768 tokens
+    (1, 8, 32, 32768, 3, 3, 0.0, [(0, 0), (0, 17), (0, 31)]),
+    # batched decode: 16 sequences of 8192 tokens
+    (16, 8, 32, 8192, 3, 3, 0.0, [(0, 5), (9, 20), (15, 31)]),
+    # long context: 131072 tokens, 64 q / 8 KV heads, K 3-bit / V 4-bit, 1 % of tokens with norm x 10
+    (1, 8, 64, 131072, 3, 4, 0.01, [(0, 3), (0, 62)]),
+])
+def test_full_size_step_sampled(bsz, hkv, hq, T, kbits, vbits, heavy, samples):
+    """The benchmarked step at the workloads' full shapes and in the bench's
+    launch configuration (RHT, the new token appended at the last slot of
+    every sequence): the appended slots' packed records and sampled query
+    heads against the oracle."""
+    d, kind = 128, "rht"
+    k, v = W.decode_kv(bsz, hkv, T, seed=5, heavy_frac=heavy)
     rot, qjl = P.handles(d, kind)
-    kc = B.Cache("prod", 3, d, rows=bsz * hkv, capacity=T)
-    vc = B.Cache("mse", 3, d, rows=bsz * hkv, capacity=T)
+    kc = B.Cache("prod", kbits, d, rows=bsz * hkv, capacity=T)
+    vc = B.Cache("mse", vbits, d, rows=bsz * hkv, capacity=T)
     # the context up to slot T - 2 comes from the GPU's cache fill; slot T - 1 from the step
     B.tq_quantize_kv(kc, rot, torch.from_numpy(k.reshape(-1, d)).cuda().to(torch.bfloat16), qjl=qjl)
     B.tq_quantize_kv(vc, rot, torch.from_numpy(v.reshape(-1, d)).cuda().to(torch.bfloat16))
@@ -146,28 +154,28 @@ def test_full_size_step_sampled():
     got = out.cpu().numpy()
 
     pi, s = P.oracle_mats(d, kind)
-    kn = knew.float().cpu().numpy().reshape(hkv, d)
-    vn = vnew.float().cpu().numpy().reshape(hkv, d)
+    kn = knew.float().cpu().numpy().reshape(bsz, hkv, d)
+    vn = vnew.float().cpu().numpy().reshape(bsz, hkv, d)
     qn = q.float().cpu().numpy()
-    # the appended slot: the GPU's packed record against the oracle's quantization of the new token
-    got_k = P.cache_to_numpy(kc, hkv * T)
-    got_v = P.cache_to_numpy(vc, hkv * T)
-    last = np.arange(hkv) * T + (T - 1)
-    for name, mode, xn, g in (("k", "prod", kn, got_k), ("v", "mse", vn, got_v)):
-        qz = oq.quantize(xn.astype(np.float64), pi, mode, 3, s if mode == "prod" else None)
+    # the appended slots: the GPU's packed records against the oracle's quantization of the new tokens
+    got_k = P.cache_to_numpy(kc, bsz * hkv * T)
+    got_v = P.cache_to_numpy(vc, bsz * hkv * T)
+    last = np.arange(bsz * hkv) * T + (T - 1)
+    for name, mode, bits, xn, g in (("k", "prod", kbits, kn, got_k), ("v", "mse", vbits, vn, got_v)):
+        qz = oq.quantize(xn.reshape(-1, d).astype(np.float64), pi, mode, bits, s if mode == "prod" else None)
         sub = {key: val[last] for key, val in g.items()}
-        rep = P.compare_quantized(sub, qz, mode, 3, d, s, label=f"appended-{name}")
+        rep = P.compare_quantized(sub, qz, mode, bits, d, s, label=f"appended-{name}")
         assert rep["code_mismatch"] == 0
-    scale = None
-    for h in (0, 17, 31):
+    del got_k, got_v
+    for b, h in samples:
         kv = h // (hq // hkv)
-        kx = k[0, kv].copy()
-        vx = v[0, kv].copy()
-        kx[T - 1] = kn[kv]
-        vx[T - 1] = vn[kv]
-        kq = oq.quantize(W.round_bf16(kx).astype(np.float64), pi, "prod", 3, s)
-        vq = oq.quantize(W.round_bf16(vx).astype(np.float64), pi, "mse", 3)
-        qp, u = oa.query_prep(qn[0, h].astype(np.float64), pi, s)
+        kx = k[b, kv].copy()
+        vx = v[b, kv].copy()
+        kx[T - 1] = kn[b, kv]
+        vx[T - 1] = vn[b, kv]
+        kq = oq.quantize(W.round_bf16(kx).astype(np.float64), pi, "prod", kbits, s)
+        vq = oq.quantize(W.round_bf16(vx).astype(np.float64), pi, "mse", vbits)
+        qp, u = oa.query_prep(qn[b, h].astype(np.float64), pi, s)
         lg = oa.key_logits(qp, u, kq["idx"], kq["norm16"], kq["centroids"], kq["rnorm16"], kq["z"], d)
         vhat = vq["norm16"][:, None] * vq["centroids"][vq["idx"]]
         sc = lg / np.sqrt(d)
@@ -175,7 +183,8 @@ def test_full_size_step_sampled():
         pr /= pr.sum()
         want = (pr @ vhat) @ pi
         scale = np.max(vq["norm16"]) / np.sqrt(d)
-        assert np.max(np.abs(got[0, h] - want)) <= OUT_TOL * scale, (h, np.max(np.abs(got[0, h] - want)) / scale)
+        err = np.max(np.abs(got[b, h] - want)) / scale
+        assert err <= OUT_TOL, (b, h, err)
 
 
 def test_step_with_pinned_host_io():
