@@ -65,16 +65,22 @@ def _kernel_hash(paths):
     return h.hexdigest()[:16]
 
 
-def _traffic(name, paths, units_scale=1.0):
-    """Per-launch DRAM bytes from a committed ncu summary, if the kernel source is unchanged."""
+def _traffic(name, paths, workload, alg_bytes):
+    """Per-launch DRAM bytes from a committed ncu capture, if the kernel source
+    is unchanged: as captured on the record's own workload, else scaled to
+    this launch by its algorithmic bytes (the scan's traffic grows with the
+    cache it reads). Returns (bytes or None, how)."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)[name]
         if rec["source_hash"] != _kernel_hash(paths):
-            return None
-        return rec["dram_bytes_per_launch"] * units_scale
+            return None, "kernel changed since the capture"
+        if rec["workload_name"] == workload:
+            return rec["dram_bytes_per_launch"], "captured on this workload"
+        return (rec["dram_bytes_per_launch"] * alg_bytes / rec["alg_bytes_per_launch"],
+                f"scaled from the {rec['workload_name']} capture by algorithmic bytes")
     except Exception:
-        return None
+        return None, "no capture"
 
 
 class ClockSampler:
@@ -361,6 +367,7 @@ def run_tq(args):
     scan_alg = rows * T * ((w["k_bits"] - 1) * d // 8 + d // 8 + 4 + w["v_bits"] * d // 8 + 2) + bsz * hq * 2 * d * 4
     scan_avg_s = statistics.mean(scan_ms) / 1e3
     achieved = scan_alg / scan_avg_s / 1e9
+    traffic, traffic_how = _traffic("decode_scan", SCAN_SOURCES, w["name"], scan_alg)
     q_achieved = q_alg_bytes / (q_ms / 1e3) / 1e9
     res = None
     if rank == 0:
@@ -376,7 +383,7 @@ def run_tq(args):
             "roofline": {"kernel": "decode_mma_kernel (split-K scan)", "bound": "hbm", "achieved": achieved,
                          "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind,
                          "alg_bytes_per_launch": scan_alg, "avg_launch_us": scan_avg_s * 1e6,
-                         "traffic": _traffic("decode_scan", SCAN_SOURCES)},
+                         "traffic": traffic, "traffic_source": traffic_how},
             "quantize": {"vectors_per_s": q_vectors / (q_ms / 1e3), "vectors_per_call": q_vectors,
                          "workload": (f"cache fill: {bsz} x {hkv} KV heads x {T} tokens, K ({w['k_bits']}-bit PROD) "
                                       f"and V ({w['v_bits']}-bit MSE), bf16 in, {w['rotation']}"),
