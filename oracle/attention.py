@@ -39,7 +39,7 @@ def query_prep(q, pi, s_matrix=None):
 
 def key_logits(qprime, u, idx, norm16, centroids, rnorm16=None, z=None, m=None):
     """l_t for one query against T keys. idx [T, d]; z [T, m] bool."""
-    base = centroids[idx] @ qprime
+    base = qmod.coord_centroids(centroids, idx) @ qprime
     if z is not None:
         pm = 2.0 * z.astype(np.float64) - 1.0
         base = base + qmod.qjl_scale(m) * rnorm16 * (pm @ u)
@@ -98,7 +98,7 @@ def decode(q, kcache, vcache, seq_lens, pi, s_matrix, k_centroids, v_centroids,
             s = s - np.max(s)
             p = np.exp(s)
             p = p / np.sum(p)
-            vhat = vcache["norm16"][b, kv, :L, None] * v_centroids[vcache["idx"][b, kv, :L]]
+            vhat = vcache["norm16"][b, kv, :L, None] * qmod.coord_centroids(v_centroids, vcache["idx"][b, kv, :L])
             a = p @ vhat
             out[b, h] = a @ np.asarray(pi)
             logits[b][h] = l

@@ -14,10 +14,17 @@ Pinned by those printed figures (tests).
 """
 
 
-def bytes_per_vector(mode, bits, d, m=None, padded=False):
-    """Bytes one quantized vector occupies (codes + signs + float16 scalars)."""
+def bytes_per_vector(mode, bits, d, m=None, padded=False, bits2=None):
+    """Bytes one quantized vector occupies (codes + signs + float16 scalars);
+    bits2: the second channel group's bits of a fractional rate (half the
+    coordinates of every 16, see quantize.in_first_group)."""
     bprime = bits - 1 if mode == "prod" else bits
-    code_bytes = (bprime * d + 7) // 8
+    code_bits = bprime * d
+    if bits2 is not None:
+        b2 = bits2 - 1 if mode == "prod" else bits2
+        n1 = sum(1 for i in range(d) if i % 16 < 8)
+        code_bits = bprime * n1 + b2 * (d - n1)
+    code_bytes = (code_bits + 7) // 8
     if padded:
         code_bytes = (code_bytes + 15) // 16 * 16
     total = code_bytes + 2
@@ -30,8 +37,8 @@ def bytes_per_vector(mode, bits, d, m=None, padded=False):
     return total
 
 
-def bits_per_value(mode, bits, d, m=None):
-    return 8.0 * bytes_per_vector(mode, bits, d, m) / d
+def bits_per_value(mode, bits, d, m=None, bits2=None):
+    return 8.0 * bytes_per_vector(mode, bits, d, m, bits2=bits2) / d
 
 
 def ratio_vs_fp16(mode, bits, d, m=None):

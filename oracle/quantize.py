@@ -25,9 +25,20 @@ Readings (the pages are silent or garbled):
 * a zero vector gets n = 0 and y = 0 and then goes through the same steps;
 * a coordinate equal to a boundary goes to the upper cell.
 
+Fractional bit-rates (2.5 / 3.5 bits per channel, Qiita "Which bit-width is
+lossless" and A2A "Benchmarks and real-world performance" quote them; the
+mechanism is not on the pages): the plainest reading, two groups of channels
+at different bit widths, each with its own Lloyd-Max codebook of the same Beta
+law. After the rotation every coordinate has that law, so which coordinates
+carry the extra bit is free; this project puts coordinate i in the first group
+(`bits`) when i mod 16 < 8 and in the second (`bits2`) otherwise, and packs
+the codes in coordinate order, each with its own width. 2.5 bits = b 3 / 2,
+3.5 = 4 / 3 (for keys, b counts the sign bit: code widths b - 1).
+
 Packed layout (this project's specification; the pages give none):
 * codes: LSB-first bit stream, bit k of coordinate i's index at stream bit
-  b'*i + k, stream bit p in byte p // 8 at bit p % 8; row stride = the byte
+  o_i + k with o_i the sum of the widths of coordinates 0 .. i-1 (b'*i for one
+  width), stream bit p in byte p // 8 at bit p % 8; row stride = the byte
   count rounded up to 16; padding bits 0;
 * signs: bit j = [(S r)_j >= 0] at byte j // 8, bit j % 8; stride rounded up
   to 16;
@@ -80,12 +91,36 @@ def row_stride(nbits_per_row):
     return (nbytes + 15) // 16 * 16
 
 
-def quantize(x, pi, mode, bits, s_matrix=None):
-    """Quantize rows of x (float64 [n, d]).
+def in_first_group(d):
+    """bool [d]: coordinate i takes the first width (i mod 16 < 8)."""
+    return (np.arange(d) % 16) < 8
+
+
+def code_widths(d, mode, bits, bits2=None):
+    """Code bits of each coordinate: one width, or the two groups' widths."""
+    bp = code_bits(mode, bits)
+    if bits2 is None or bits2 == bits:
+        return np.full(d, bp, dtype=np.int64)
+    return np.where(in_first_group(d), bp, code_bits(mode, bits2)).astype(np.int64)
+
+
+def coord_centroids(centroids, idx):
+    """The centroid value of every code: centroids is one table [L] or one
+    table per coordinate [d, L] (two-group caches); idx [..., d]."""
+    c = np.asarray(centroids)
+    if c.ndim == 1:
+        return c[idx]
+    return c[np.arange(c.shape[0]), idx]
+
+
+def quantize(x, pi, mode, bits, s_matrix=None, bits2=None):
+    """Quantize rows of x (float64 [n, d]); bits2: the second group's bits of
+    a fractional-rate cache (None: every coordinate at `bits`).
 
     Returns a dict with: n (exact norm), norm16, y (rotated unit vector), idx
-    (codes, int64 [n, d]); for PROD also r, gamma, rnorm16, sproj (= S r) and
-    z (bool [n, m]).
+    (codes, int64 [n, d]), centroids ([L], or [d, L] with each coordinate's
+    table when there are two groups), boundaries (likewise), widths; for PROD
+    also r, gamma, rnorm16, sproj (= S r) and z (bool [n, m]).
     """
     x = np.atleast_2d(np.asarray(x, dtype=np.float64))
     d = x.shape[1]
@@ -95,27 +130,49 @@ def quantize(x, pi, mode, bits, s_matrix=None):
     safe = np.where(n > 0, n, 1.0)
     y = rotation.rotate(pi, x) / safe[:, None]
     y[n == 0] = 0.0
-    idx = codebook.bucketize(y, t)
-    out = {"n": n, "norm16": fp16_rne(n), "y": y, "idx": idx, "centroids": c, "boundaries": t}
+    widths = code_widths(d, mode, bits, bits2)
+    if np.all(widths == bp):
+        idx = codebook.bucketize(y, t)
+    else:
+        # each group bucketized with its own codebook; tables padded to a common length
+        c2, t2 = codebook.lloyd_max(d, code_bits(mode, bits2))
+        first = in_first_group(d)
+        idx = np.where(first, codebook.bucketize(y, t), codebook.bucketize(y, t2))
+        lmax = max(len(c), len(c2))
+        ctab = np.full((d, lmax), np.nan)
+        ttab = np.full((d, lmax - 1), np.nan)
+        ctab[first, : len(c)] = c
+        ctab[~first, : len(c2)] = c2
+        ttab[first, : len(t)] = t
+        ttab[~first, : len(t2)] = t2
+        c, t = ctab, ttab
+    out = {"n": n, "norm16": fp16_rne(n), "y": y, "idx": idx, "centroids": c, "boundaries": t, "widths": widths}
     if mode == "prod":
         if s_matrix is None:
             raise ValueError("PROD mode needs the QJL matrix S")
-        r = y - c[idx]
+        r = y - coord_centroids(c, idx)
         gamma = np.sqrt(np.sum(r * r, axis=1))
         sproj = r @ np.asarray(s_matrix, dtype=np.float64).T
         out.update(r=r, gamma=gamma, rnorm16=fp16_rne(gamma), sproj=sproj, z=sproj >= 0.0)
     return out
 
 
+def _widths(d, bprime):
+    w = np.asarray(bprime, dtype=np.int64)
+    return np.full(d, int(w), dtype=np.int64) if w.ndim == 0 else w
+
+
 def pack_codes(idx, bprime):
-    """LSB-first bit stream per row, stride rounded up to 16 bytes."""
+    """LSB-first bit stream per row, stride rounded up to 16 bytes; bprime is
+    one width or the width of every coordinate."""
     idx = np.atleast_2d(np.asarray(idx, dtype=np.int64))
     n, d = idx.shape
-    stride = row_stride(bprime * d)
-    out = np.zeros((n, stride), dtype=np.uint8)
+    w = _widths(d, bprime)
+    off = np.concatenate([[0], np.cumsum(w)])
+    out = np.zeros((n, row_stride(int(off[-1]))), dtype=np.uint8)
     for i in range(d):
-        for k in range(bprime):
-            p = bprime * i + k
+        for k in range(int(w[i])):
+            p = int(off[i]) + k
             bit = ((idx[:, i] >> k) & 1).astype(np.uint8)
             out[:, p // 8] |= bit << np.uint8(p % 8)
     return out
@@ -123,10 +180,12 @@ def pack_codes(idx, bprime):
 
 def unpack_codes(packed, d, bprime):
     packed = np.atleast_2d(np.asarray(packed, dtype=np.uint8))
+    w = _widths(d, bprime)
+    off = np.concatenate([[0], np.cumsum(w)])
     idx = np.zeros((packed.shape[0], d), dtype=np.int64)
     for i in range(d):
-        for k in range(bprime):
-            p = bprime * i + k
+        for k in range(int(w[i])):
+            p = int(off[i]) + k
             bit = (packed[:, p // 8] >> np.uint8(p % 8)) & 1
             idx[:, i] |= bit.astype(np.int64) << k
     return idx
@@ -149,11 +208,11 @@ def unpack_signs(packed, m):
     return z
 
 
-def pack(qz, mode, bits):
+def pack(qz, mode, bits, bits2=None):
     """Packed planes of one quantize() result: codes, signs (PROD), norm, rnorm (PROD)."""
     d = qz["idx"].shape[1]
     planes = {
-        "codes": pack_codes(qz["idx"], code_bits(mode, bits)),
+        "codes": pack_codes(qz["idx"], code_widths(d, mode, bits, bits2)),
         "norm": qz["norm16"].astype(np.float16),
     }
     if mode == "prod":
@@ -174,9 +233,8 @@ def reconstruct(qz, pi, mode, s_matrix=None, use_stored_norms=True):
     MSE:  x~ = n Pi^T c[idx]
     PROD: x~ = n Pi^T (c[idx] + sqrt(pi/2)/m * gamma * S^T (2z - 1))
     """
-    c = qz["centroids"]
     n = qz["norm16"] if use_stored_norms else qz["n"]
-    yhat = c[qz["idx"]]
+    yhat = coord_centroids(qz["centroids"], qz["idx"])
     if mode == "prod":
         s = np.asarray(s_matrix, dtype=np.float64)
         g = qz["rnorm16"] if use_stored_norms else qz["gamma"]

@@ -76,12 +76,12 @@ def test_cosine_at_three_bits_matches_printed_figure():
     assert round(theory, 3) == fig
 
 
-def _estimates(q, k, d, bits, seeds, mode):
+def _estimates(q, k, d, bits, seeds, mode, bits2=None):
     out = np.empty(seeds)
     for s in range(seeds):
         pi = rotation.dense_rotation(10_000 + s, d)
         smat = rng.round_to_bf16(rng.normals(90_000 + s, d * d).reshape(d, d)) if mode == "prod" else None
-        qz = quantize.quantize(k[None], pi, mode, bits, smat)
+        qz = quantize.quantize(k[None], pi, mode, bits, smat, bits2=bits2)
         qp, u = attention.query_prep(q, pi, smat)
         c = qz["centroids"]
         if mode == "prod":
@@ -160,3 +160,77 @@ def test_footprint_matches_printed_turbo_figures():
     assert footprint.bytes_per_vector("mse", 3, 128) == 50
     assert footprint.bytes_per_vector("prod", 3, 200, padded=True) == 64 + 32 + 4
     assert footprint.bytes_per_vector("prod", 2, 200, padded=True) == 32 + 32 + 4
+
+
+# ---- fractional bit-rates: two channel groups (i mod 16 < 8 at `bits`, the rest at `bits2`) ----
+
+@pytest.mark.parametrize("mode,bits", [("mse", 3), ("prod", 3), ("prod", 4)])
+def test_two_groups_of_equal_width_are_the_single_width_quantizer(mode, bits):
+    d = 128
+    pi = rotation.dense_rotation(1, d)
+    smat = rng.round_to_bf16(rng.normals(2, d * d).reshape(d, d)) if mode == "prod" else None
+    x = np.random.default_rng(8).standard_normal((40, d))
+    a = quantize.quantize(x, pi, mode, bits, smat)
+    b = quantize.quantize(x, pi, mode, bits, smat, bits2=bits)
+    assert np.array_equal(a["idx"], b["idx"])
+    assert np.array_equal(quantize.pack(a, mode, bits)["codes"], quantize.pack(b, mode, bits, bits)["codes"])
+
+
+def test_two_group_packing_by_hand():
+    """d = 16, widths 2 (coordinates 0..7) and 1 (8..15), LSB first: codes
+    3,0,1,2,3,0,1,2 give bit pairs 11 00 10 01 -> 0b10010011 = 0x93 twice;
+    codes 1,0,1,1,0,0,1,0 give 0b01001101 = 0x4d; padded to 16 bytes."""
+    idx = np.array([[3, 0, 1, 2, 3, 0, 1, 2, 1, 0, 1, 1, 0, 0, 1, 0]])
+    w = quantize.code_widths(16, "prod", 3, 2)
+    assert w.tolist() == [2] * 8 + [1] * 8
+    got = quantize.pack_codes(idx, w)
+    assert got[0].tobytes() == bytes([0x93, 0x93, 0x4D] + [0] * 13)
+    assert np.array_equal(quantize.unpack_codes(got, 16, w), idx)
+
+
+@pytest.mark.parametrize("bits,bits2", [(3, 2), (4, 3)])
+def test_two_group_mse_per_group_equals_each_distortion(bits, bits2):
+    """Each group is quantized with its own Lloyd-Max codebook of the same
+    Beta law: per coordinate E[(y_i - c[idx_i])^2] = D_bits on the first
+    group and D_bits2 on the second."""
+    d, n = 128, 20000
+    pi = rotation.dense_rotation(1, d)
+    qz = quantize.quantize(_unit_rows(n, d, 9), pi, "mse", bits, bits2=bits2)
+    err = (qz["y"] - quantize.coord_centroids(qz["centroids"], qz["idx"])) ** 2
+    first = quantize.in_first_group(d)
+    for sel, b in ((first, bits), (~first, bits2)):
+        e = err[:, sel].ravel()
+        assert abs(e.mean() - codebook.distortion(d, b)) < 4 * e.std() / np.sqrt(e.size)
+
+
+def test_two_group_prod_inner_product_is_unbiased():
+    """Keys at 2.5 bits (3 / 2): the estimate still averages to <q,k> over seeds."""
+    d, seeds = 32, 3000
+    r = np.random.default_rng(1)
+    k = r.standard_normal(d) * 3
+    q = 0.8 * k / np.linalg.norm(k) * 2 + 0.6 * r.standard_normal(d)
+    est = _estimates(q, k, d, 3, seeds, "prod", bits2=2)
+    assert abs(est.mean() - q @ k) < 3.5 * est.std() / np.sqrt(seeds)
+
+
+def test_two_group_estimator_equals_dense_reconstruction():
+    d, n = 64, 50
+    pi = rotation.dense_rotation(1, d)
+    smat = rng.round_to_bf16(rng.normals(2, d * d).reshape(d, d))
+    x = np.random.default_rng(6).standard_normal((n, d)) * 5
+    q = np.random.default_rng(7).standard_normal(d)
+    qz = quantize.quantize(x, pi, "prod", 4, smat, bits2=3)
+    qp, u = attention.query_prep(q, pi, smat)
+    l = attention.key_logits(qp, u, qz["idx"], qz["norm16"], qz["centroids"], qz["rnorm16"], qz["z"], d)
+    xt = quantize.reconstruct(qz, pi, "prod", smat)
+    assert np.max(np.abs(l - xt @ q)) < 1e-10 * np.max(np.abs(l))
+
+
+def test_two_group_footprint():
+    """2.5 and 3.5 bits per channel: keys 1.5 / 2.5 code bits + 1 sign bit per
+    coordinate plus two float16 scalars per 128 coordinates."""
+    assert footprint.bytes_per_vector("prod", 3, 128, bits2=2) == 24 + 16 + 4
+    assert footprint.bits_per_value("prod", 3, 128, bits2=2) == 2.75
+    assert footprint.bytes_per_vector("prod", 4, 128, bits2=3) == 40 + 16 + 4
+    assert footprint.bits_per_value("prod", 4, 128, bits2=3) == 3.75
+    assert footprint.bytes_per_vector("mse", 3, 128, bits2=2) == 40 + 2
