@@ -134,7 +134,17 @@ tq_status tq_codebook(int d, int bits, double* centroids, double* boundaries);
  *             bit j (LSB-first) = [(S r)_j >= 0].
  *   norm[s]:  fp16 bits of ||x|| (round to nearest even, saturated 65504).
  *   rnorm[s]: (TQ_PROD) fp16 bits of ||r||, r = Pi x/||x|| - c[idx].
- * All four plane pointers must be 16-byte aligned (norm/rnorm: 2-byte). */
+ * All four plane pointers must be 16-byte aligned (norm/rnorm: 2-byte).
+ *
+ * Fractional bit-rates (bits2 != 0 and != bits; the 2.5 / 3.5 bits per
+ * channel the Qiita article's tables quote, read as two channel groups):
+ * coordinate i takes `bits` when i % 16 < 8 and `bits2` otherwise, each
+ * group with its own Lloyd-Max codebook of the same law; codes are packed in
+ * coordinate order with their own widths (coordinate i starts after the bits
+ * of coordinates 0 .. i-1), stride tq_code_bytes2 (rounded up to 8 bytes, so
+ * the smaller width saves memory). Supported: d = 128 and bits2 = bits - 1
+ * (keys 3/2 = 2.5 and 4/3 = 3.5 bits, values likewise). tq_quantize_kv takes
+ * them; the decode entry points and the search return TQ_ERR_UNSUPPORTED. */
 typedef struct {
     int mode;         /* TQ_MSE (values) or TQ_PROD (keys)                   */
     int bits;         /* MSE: 1..4 Lloyd-Max bits; PROD: 2..5 = (bits-1) + 1 */
@@ -146,9 +156,15 @@ typedef struct {
     uint8_t* signs;   /* device [rows*capacity][tq_sign_bytes] (PROD)        */
     uint16_t* norm;   /* device [rows*capacity] fp16 bits                    */
     uint16_t* rnorm;  /* device [rows*capacity] fp16 bits (PROD)             */
+    int bits2;        /* 0: every coordinate at `bits`; else the second
+                         channel group's bits (fractional rates, see above)  */
 } tq_cache;
 
 int tq_code_bytes(int d, int code_bits); /* per-slot stride of codes, bytes */
+/* per-slot stride of a two-group cache's codes (code bits of the coordinates
+ * with i % 16 < 8, of the others): the bit count rounded up to 8 bytes;
+ * equals tq_code_bytes(d, code_bits) when the two are equal */
+int tq_code_bytes2(int d, int code_bits, int code_bits2);
 int tq_sign_bytes(int m);                /* per-slot stride of signs, bytes */
 
 /* ------------------------------------------------------------------------ *

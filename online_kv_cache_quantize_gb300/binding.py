@@ -35,7 +35,7 @@ class tq_cache(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int), ("bits", ctypes.c_int), ("d", ctypes.c_int), ("m", ctypes.c_int),
                 ("rows", ctypes.c_int64), ("capacity", ctypes.c_int64),
                 ("codes", ctypes.c_void_p), ("signs", ctypes.c_void_p),
-                ("norm", ctypes.c_void_p), ("rnorm", ctypes.c_void_p)]
+                ("norm", ctypes.c_void_p), ("rnorm", ctypes.c_void_p), ("bits2", ctypes.c_int)]
 
 
 class tq_quant_args(ctypes.Structure):
@@ -84,6 +84,7 @@ _SIGS = {
     "tq_free_qjl": (_STATUS, [ctypes.c_void_p]),
     "tq_codebook": (_STATUS, [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
     "tq_code_bytes": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
+    "tq_code_bytes2": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "tq_sign_bytes": (ctypes.c_int, [ctypes.c_int]),
     "tq_quantize_kv": (_STATUS, [ctypes.POINTER(tq_quant_args), ctypes.c_void_p]),
     "tq_attn_decode_workspace": (ctypes.c_size_t, [ctypes.POINTER(tq_decode_args)]),
@@ -224,16 +225,22 @@ def tq_sign_bytes(m):
 class Cache:
     """Device planes of a packed cache (torch tensors owned by this object)."""
 
-    def __init__(self, mode, bits, d, rows, capacity, m=None, device="cuda"):
+    def __init__(self, mode, bits, d, rows, capacity, m=None, device="cuda", bits2=None):
+        """bits2: the second channel group's bits of a fractional-rate cache
+        (coordinates with i % 16 >= 8), None for one width."""
         import torch
 
         self.mode = MODES.get(mode, mode)
         self.bits, self.d, self.rows, self.capacity = bits, d, rows, capacity
+        self.bits2 = bits2 if bits2 is not None and bits2 != bits else None
         self.m = (m if m is not None else d) if self.mode == TQ_PROD else 0
         cb = bits - 1 if self.mode == TQ_PROD else bits
         self.code_bits = cb
         n = rows * capacity
-        self.code_stride = tq_code_bytes(d, cb)
+        if self.bits2 is None:
+            self.code_stride = tq_code_bytes(d, cb)
+        else:
+            self.code_stride = load().tq_code_bytes2(d, cb, self.bits2 - 1 if self.mode == TQ_PROD else self.bits2)
         self.codes = torch.zeros((n, self.code_stride), dtype=torch.uint8, device=device)
         self.norm = torch.zeros(n, dtype=torch.int16, device=device)
         if self.mode == TQ_PROD:
@@ -248,7 +255,8 @@ class Cache:
     def struct(self):
         return tq_cache(self.mode, self.bits, self.d, self.m, self.rows, self.capacity,
                         self.codes.data_ptr(), self.signs.data_ptr() if self.signs is not None else None,
-                        self.norm.data_ptr(), self.rnorm.data_ptr() if self.rnorm is not None else None)
+                        self.norm.data_ptr(), self.rnorm.data_ptr() if self.rnorm is not None else None,
+                        self.bits2 or 0)
 
     def bytes_per_slot(self):
         return self.code_stride + 2 + (self.sign_stride + 2 if self.mode == TQ_PROD else 0)

@@ -56,7 +56,10 @@ tq_status check_qjl(const tq_qjl* q, int m, int d) {
 }
 
 // Validates a cache descriptor; returns the code bits per coordinate.
-tq_status check_cache(const tq_cache& c, const char* what, int* code_bits) {
+// code bits of the two channel groups (equal for a one-width cache) and
+// the codes' per-slot stride
+tq_status check_cache(const tq_cache& c, const char* what, int* code_bits, int* code_bits2 = nullptr,
+                      int* code_stride = nullptr) {
     std::string w(what);
     if (c.mode != TQ_MSE && c.mode != TQ_PROD) return fail(TQ_ERR_INVALID_ARG, w + ": mode must be TQ_MSE or TQ_PROD");
     if (c.mode == TQ_MSE && (c.bits < 1 || c.bits > 4)) return fail(TQ_ERR_UNSUPPORTED, w + ": MSE bits must be 1..4");
@@ -71,6 +74,17 @@ tq_status check_cache(const tq_cache& c, const char* what, int* code_bits) {
         if (!aligned(c.signs, 16) || !aligned(c.rnorm, 2)) return fail(TQ_ERR_ALIGNMENT, w + ": signs must be 16-byte aligned, rnorm 2-byte");
     }
     *code_bits = c.mode == TQ_PROD ? c.bits - 1 : c.bits;
+    int cb2 = *code_bits;
+    if (c.bits2 != 0 && c.bits2 != c.bits) {
+        if (c.bits2 != c.bits - 1)
+            return fail(TQ_ERR_UNSUPPORTED, w + ": a fractional-rate cache needs bits2 = bits - 1 (3/2 or 4/3)");
+        if (c.d != 128) return fail(TQ_ERR_UNSUPPORTED, w + ": a fractional-rate cache needs d = 128");
+        if (c.mode == TQ_MSE && (c.bits < 2 || c.bits > 4)) return fail(TQ_ERR_UNSUPPORTED, w + ": MSE bits/bits2 out of range");
+        if (c.mode == TQ_PROD && (c.bits < 3 || c.bits > 5)) return fail(TQ_ERR_UNSUPPORTED, w + ": PROD bits/bits2 out of range");
+        cb2 = c.mode == TQ_PROD ? c.bits2 - 1 : c.bits2;
+    }
+    if (code_bits2) *code_bits2 = cb2;
+    if (code_stride) *code_stride = tq_code_bytes2(c.d, *code_bits, cb2);
     return TQ_OK;
 }
 
@@ -288,8 +302,8 @@ struct DecodeLaunch {
 tq_status quant_prepare(const tq_quant_args* a, QuantLaunch* L, bool* empty) {
     *empty = false;
     if (!a) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_kv: args are NULL");
-    int cb = 0;
-    tq_status s = check_cache(a->cache, "tq_quantize_kv cache", &cb);
+    int cb = 0, cb2 = 0, cstride = 0;
+    tq_status s = check_cache(a->cache, "tq_quantize_kv cache", &cb, &cb2, &cstride);
     if (s != TQ_OK) return s;
     const tq_cache& c = a->cache;
     if ((s = check_rot(a->rot, c.d)) != TQ_OK) return s;
@@ -330,7 +344,7 @@ tq_status quant_prepare(const tq_quant_args* a, QuantLaunch* L, bool* empty) {
     p.total_slots = total;
     p.capacity = c.capacity;
     p.codes = c.codes;
-    p.code_stride = tq_code_bytes(c.d, cb);
+    p.code_stride = cstride;
     p.signs = c.signs;
     p.sign_stride = prod ? tq_sign_bytes(c.m) : 0;
     p.norm = c.norm;
@@ -345,6 +359,8 @@ tq_status quant_prepare(const tq_quant_args* a, QuantLaunch* L, bool* empty) {
     p.inv_sqrt_d = (float)(1.0 / std::sqrt((double)c.d));
     p.guard = rht ? 1.0e-6f : (float)(3.0e-8 * c.d);
     if ((s = fill_codebook(c.d, cb, &p.cb)) != TQ_OK) return s;
+    p.code_bits2 = cb2 != cb ? cb2 : 0;
+    if (p.code_bits2 && (s = fill_codebook(c.d, cb2, &p.cb2)) != TQ_OK) return s;
     if (cudaError_t ew = tqk::device_error_word(&p.err); ew != cudaSuccess) return cuda_status(ew, "tq_quantize_kv error word");
     L->dtype = a->x_dtype == TQ_F32 ? 0 : 1;
     L->vpl = vpl_for(c.d);
@@ -356,7 +372,9 @@ tq_status quant_prepare(const tq_quant_args* a, QuantLaunch* L, bool* empty) {
     // d = 128 (keys m = 128): up to kSmallAppend vectors the CTA-per-vector
     // kernel, more the tensor-core kernel (16-byte aligned rows); otherwise
     // the warp-per-vector kernel (any d <= 256)
-    L->small = c.d == 128 && (!prod || c.m == 128) && a->n <= kSmallAppend;
+    // (a two-width cache always takes the CTA-per-vector kernel)
+    L->small = c.d == 128 && (!prod || c.m == 128) && (a->n <= kSmallAppend || p.code_bits2 != 0);
+    if (p.code_bits2 && prod && c.m != 128) return fail(TQ_ERR_UNSUPPORTED, "tq_quantize_kv: a fractional-rate key cache needs m = 128");
     L->mma = c.d == 128 && !L->small && (!prod || (c.m == 128 && p.s_frag)) && (rht || p.pi_frag) &&
              aligned(a->x, 16) && (a->x_stride * (int64_t)esz) % 16 == 0;
     return TQ_OK;
@@ -379,9 +397,10 @@ tq_status decode_prepare(const tq_decode_args* a, void* workspace, size_t ws_byt
     DecodePlan& pl = D->pl;
     tq_status s = plan_decode(a, &pl);
     if (s != TQ_OK) return s;
-    int kb = 0, vb = 0;
-    if ((s = check_cache(a->k, "tq_attn_decode k", &kb)) != TQ_OK) return s;
-    if ((s = check_cache(a->v, "tq_attn_decode v", &vb)) != TQ_OK) return s;
+    int kb = 0, vb = 0, kb2 = 0, vb2 = 0;
+    if ((s = check_cache(a->k, "tq_attn_decode k", &kb, &kb2)) != TQ_OK) return s;
+    if ((s = check_cache(a->v, "tq_attn_decode v", &vb, &vb2)) != TQ_OK) return s;
+    if (kb2 != kb || vb2 != vb) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: fractional-rate caches are not supported yet");
     if (a->k.mode != TQ_PROD || a->v.mode != TQ_MSE) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: keys must be PROD and values MSE");
     if (a->k.d != a->d || a->v.d != a->d) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: cache d does not match");
     if (a->k.m != 128) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: m must be 128");
@@ -656,9 +675,10 @@ tq_status tq_score_topk(const tq_topk_args* a, void* workspace, size_t ws_bytes,
     if (!a) return fail(TQ_ERR_INVALID_ARG, "tq_score_topk: args are NULL");
     if (a->k < 1 || a->k > 32) return fail(TQ_ERR_UNSUPPORTED, "tq_score_topk: k must be 1..32");
     if (a->nq < 0 || a->n_db < 0) return fail(TQ_ERR_INVALID_ARG, "tq_score_topk: negative sizes");
-    int cb = 0;
-    tq_status s = check_cache(a->db, "tq_score_topk db", &cb);
+    int cb = 0, cb2 = 0;
+    tq_status s = check_cache(a->db, "tq_score_topk db", &cb, &cb2);
     if (s != TQ_OK) return s;
+    if (cb2 != cb) return fail(TQ_ERR_UNSUPPORTED, "tq_score_topk: fractional-rate databases are not supported");
     if (a->db.d != a->d) return fail(TQ_ERR_INVALID_ARG, "tq_score_topk: db d does not match");
     if (a->n_db > a->db.rows * a->db.capacity) return fail(TQ_ERR_CAPACITY, "tq_score_topk: n_db exceeds the db planes");
     if (a->n_db > 0x7ffffffe) return fail(TQ_ERR_UNSUPPORTED, "tq_score_topk: n_db must fit int32 ids");

@@ -33,6 +33,7 @@ struct StepSmem {
     float qp[128];      // query: q' = Pi q
     float u[128];       // query: u = S q'
     float cent[kMaxLevels];
+    float cent2[kMaxLevels];  // the second channel group's centroids (two-width caches)
     float red[4];
     double red64[4];
     uint32_t cw[16];    // packed codes: at most 4 bits x 128 coordinates
@@ -143,7 +144,12 @@ __device__ __forceinline__ void append_vector(const QuantParams& p, int xdtype, 
                                               StepSmem& s) {
     constexpr int D = 128;
     const int i = threadIdx.x, lane = i & 31, warp = i >> 5;
-    const int L = 1 << cb;
+    // two channel groups (fractional rates): coordinates with i % 16 >= 8
+    // take the second width and codebook
+    const bool second = p.code_bits2 != 0 && (i & 15) >= 8;
+    const int cbi = second ? p.code_bits2 : cb;
+    const Codebook* book = second ? &p.cb2 : &p.cb;
+    const int L = 1 << cbi;
 
     int64_t slot;
     if (p.dst_slot) {
@@ -161,7 +167,10 @@ __device__ __forceinline__ void append_vector(const QuantParams& p, int xdtype, 
     // (q, j) = S[j][8q .. 8q + 7] sits at unit q * 128 + j in both places, so
     // the copy is contiguous and thread j's reads of its row are conflict-free
     if (prod) stage_s(p.s16, s);
-    if (i < kMaxLevels) s.cent[i] = p.cb.c[i];
+    if (i < kMaxLevels) {
+        s.cent[i] = p.cb.c[i];
+        s.cent2[i] = p.cb2.c[i];
+    }
     if (i < 16) s.cw[i] = 0u;
     const float xi = xdtype == 1 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.x)[v * p.x_stride + i])
                                  : reinterpret_cast<const float*>(p.x)[v * p.x_stride + i];
@@ -202,8 +211,8 @@ __device__ __forceinline__ void append_vector(const QuantParams& p, int xdtype, 
 #pragma unroll
     for (int t = 0; t < kMaxLevels - 1; ++t) {
         if (t < L - 1) {
-            k += (y >= p.cb.t[t]) ? 1 : 0;
-            dmin = fminf(dmin, fabsf(y - p.cb.t[t]));
+            k += (y >= book->t[t]) ? 1 : 0;
+            dmin = fminf(dmin, fabsf(y - book->t[t]));
         }
     }
     const bool flag = !(dmin >= p.guard);
@@ -236,20 +245,23 @@ __device__ __forceinline__ void append_vector(const QuantParams& p, int xdtype, 
             k = 0;
 #pragma unroll
             for (int t = 0; t < kMaxLevels - 1; ++t)
-                if (t < L - 1) k += (y64 >= p.cb.t64[t]) ? 1 : 0;
+                if (t < L - 1) k += (y64 >= book->t64[t]) ? 1 : 0;
             y = (float)y64;
         }
     }
 
-    // ---- pack: code bits cb*i .. cb*i + cb - 1 of the LSB-first stream ----
-    const int bit = cb * i;
+    // ---- pack: coordinate i's code at its stream offset (cb * i for one
+    // width; with two, each block of 16 coordinates holds 8 codes of each) ----
+    const int bit = p.code_bits2 == 0
+                        ? cb * i
+                        : (i >> 4) * 8 * (cb + p.code_bits2) + (second ? 8 * cb + (i & 7) * p.code_bits2 : (i & 7) * cb);
     atomicOr(&s.cw[bit >> 5], (uint32_t)k << (bit & 31));
-    if ((bit & 31) + cb > 32) atomicOr(&s.cw[(bit >> 5) + 1], (uint32_t)k >> (32 - (bit & 31)));
+    if ((bit & 31) + cbi > 32) atomicOr(&s.cw[(bit >> 5) + 1], (uint32_t)k >> (32 - (bit & 31)));
 
     float gamma = 0.0f;
     if (prod) {
         // r = y - c[idx], gamma = ||r||, z_j = [(S r)_j >= 0]
-        const float r = y - s.cent[k];
+        const float r = y - (second ? s.cent2[k] : s.cent[k]);
         gamma = sqrtf(step_sum(r * r, s));
         s.y[i] = r;  // the butterfly reads of s.y finished before step_sum's barriers
         asm volatile("cp.async.wait_group 0;\n" ::: "memory");

@@ -393,6 +393,15 @@ int tq_code_bytes(int d, int code_bits) {
     return (bytes + 15) / 16 * 16;
 }
 
+int tq_code_bytes2(int d, int code_bits, int code_bits2) {
+    if (code_bits2 == code_bits) return tq_code_bytes(d, code_bits);
+    if (d <= 0 || code_bits <= 0 || code_bits2 <= 0) return 0;
+    int n1 = 0;
+    for (int i = 0; i < d; ++i) n1 += (i % 16) < 8 ? 1 : 0;
+    const int bytes = (code_bits * n1 + code_bits2 * (d - n1) + 7) / 8;
+    return (bytes + 7) / 8 * 8;
+}
+
 int tq_sign_bytes(int m) {
     if (m <= 0) return 0;
     return ((m + 7) / 8 + 15) / 16 * 16;

@@ -43,6 +43,10 @@ struct QuantParams {
     float inv_sqrt_d;
     float guard;          // |y - t_j| below this is re-decided in fp64
     Codebook cb;
+    // two channel groups (fractional rates): coordinates with i % 16 >= 8
+    // take code_bits2 bits and codebook cb2; 0 = every coordinate as cb
+    int code_bits2;
+    Codebook cb2;
     uint32_t* err;        // device error word (a wait that ran out sets a bit)
 };
 

@@ -39,7 +39,8 @@ Packed layout (this project's specification; the pages give none):
 * codes: LSB-first bit stream, bit k of coordinate i's index at stream bit
   o_i + k with o_i the sum of the widths of coordinates 0 .. i-1 (b'*i for one
   width), stream bit p in byte p // 8 at bit p % 8; row stride = the byte
-  count rounded up to 16; padding bits 0;
+  count rounded up to 16 (to 8 with two widths, so the narrower group saves
+  memory); padding bits 0;
 * signs: bit j = [(S r)_j >= 0] at byte j // 8, bit j % 8; stride rounded up
   to 16;
 * norm / rnorm: float16 per vector.
@@ -169,7 +170,11 @@ def pack_codes(idx, bprime):
     n, d = idx.shape
     w = _widths(d, bprime)
     off = np.concatenate([[0], np.cumsum(w)])
-    out = np.zeros((n, row_stride(int(off[-1]))), dtype=np.uint8)
+    if np.all(w == w[0]):
+        stride = row_stride(int(off[-1]))
+    else:
+        stride = ((int(off[-1]) + 7) // 8 + 7) // 8 * 8
+    out = np.zeros((n, stride), dtype=np.uint8)
     for i in range(d):
         for k in range(int(w[i])):
             p = int(off[i]) + k

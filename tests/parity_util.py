@@ -45,13 +45,13 @@ def oracle_mats(d, kind, m=None):
     return pi, s
 
 
-def gpu_quantize(x_np, mode, bits, d, kind, dtype=torch.float32, m=None, rot=None, qjl=None):
+def gpu_quantize(x_np, mode, bits, d, kind, dtype=torch.float32, m=None, rot=None, qjl=None, bits2=None):
     """Quantize rows of x on the GPU into a fresh cache (rows=1, capacity=n)."""
     if rot is None:
         rot, qjl = handles(d, kind, m)
     x = torch.from_numpy(np.ascontiguousarray(x_np, dtype=np.float32)).to("cuda").to(dtype)
     n = x.shape[0]
-    cache = B.Cache(mode, bits, d, rows=1, capacity=max(n, 1), m=m)
+    cache = B.Cache(mode, bits, d, rows=1, capacity=max(n, 1), m=m, bits2=bits2)
     B.tq_quantize_kv(cache, rot, x, qjl=qjl if mode == "prod" else None)
     torch.cuda.synchronize()
     return cache
@@ -77,9 +77,9 @@ def _near_fp16_midpoint(v, rel):
     return np.min(np.abs(mids - v[None]), axis=0) <= rel * np.maximum(v, 1e-30)
 
 
-def compare_quantized(got, qz, mode, bits, d, s_matrix=None, label=""):
+def compare_quantized(got, qz, mode, bits, d, s_matrix=None, label="", bits2=None):
     """Returns a report dict; raises AssertionError on a parity failure."""
-    bp = oq.code_bits(mode, bits)
+    bp = oq.code_widths(d, mode, bits, bits2)
     n = qz["idx"].shape[0]
     gidx = oq.unpack_codes(got["codes"], d, bp)
     # layout: GPU bytes == spec packing of the GPU's own codes
@@ -112,11 +112,11 @@ def compare_quantized(got, qz, mode, bits, d, s_matrix=None, label=""):
     return rep
 
 
-def oracle_cache_planes(qz, mode, bits, rows, capacity, device="cuda", m=None):
+def oracle_cache_planes(qz, mode, bits, rows, capacity, device="cuda", m=None, bits2=None):
     """Upload the ORACLE's packed planes into a GPU Cache (oracle -> GPU only)."""
     d = qz["idx"].shape[1]
-    planes = oq.pack(qz, mode, bits)
-    cache = B.Cache(mode, bits, d, rows=rows, capacity=capacity, m=m)
+    planes = oq.pack(qz, mode, bits, bits2)
+    cache = B.Cache(mode, bits, d, rows=rows, capacity=capacity, m=m, bits2=bits2)
     n = qz["idx"].shape[0]
     assert n == rows * capacity
     cache.codes.copy_(torch.from_numpy(planes["codes"]))

@@ -17,15 +17,15 @@ def _built():
     build.build()
 
 
-def _run(x, mode, bits, d, kind, dtype, label, m=None):
+def _run(x, mode, bits, d, kind, dtype, label, m=None, bits2=None):
     xin = np.asarray(x, dtype=np.float32)
     if dtype == torch.bfloat16:
         xin = W.round_bf16(xin)
-    cache = P.gpu_quantize(xin, mode, bits, d, kind, dtype=dtype, m=m)
+    cache = P.gpu_quantize(xin, mode, bits, d, kind, dtype=dtype, m=m, bits2=bits2)
     got = P.cache_to_numpy(cache, xin.shape[0])
     pi, s = P.oracle_mats(d, kind, m)
-    qz = oq.quantize(xin.astype(np.float64), pi, mode, bits, s if mode == "prod" else None)
-    return P.compare_quantized(got, qz, mode, bits, d, s, label=label)
+    qz = oq.quantize(xin.astype(np.float64), pi, mode, bits, s if mode == "prod" else None, bits2=bits2)
+    return P.compare_quantized(got, qz, mode, bits, d, s, label=label, bits2=bits2)
 
 
 def test_outlier_keys_dense_prod3_fp32():
@@ -168,3 +168,23 @@ def test_full_size_prefill_sampled():
         got = {key: val[rows] for key, val in P.cache_to_numpy(cache).items()}
         qz = oq.quantize(xf[rows].astype(np.float64), pi, mode, 3, s if mode == "prod" else None)
         P.compare_quantized(got, qz, mode, 3, d, s, label=f"prefill-{name}")
+
+
+@pytest.mark.parametrize("kind", ["rht", "dense"])
+@pytest.mark.parametrize("mode,bits", [("prod", 3), ("prod", 4), ("mse", 3), ("mse", 4)])
+def test_two_width_caches(kind, mode, bits):
+    """Fractional rates (2.5 / 3.5 bits per channel): coordinates with
+    i % 16 < 8 at `bits`, the rest at `bits - 1`, each group with its own
+    codebook, codes packed in coordinate order with an 8-byte stride."""
+    k, v = W.decode_kv(1, 2, 700, heavy_frac=0.01)
+    x = (k if mode == "prod" else v).reshape(-1, 128)
+    _run(x, mode, bits, 128, kind, torch.bfloat16, f"{kind}-{mode}{bits}/{bits - 1}", bits2=bits - 1)
+
+
+def test_two_width_rejections():
+    rot, qjl = P.handles(128, "rht")
+    from online_kv_cache_quantize_gb300 import binding as B
+    x = torch.zeros((4, 128), device="cuda")
+    bad = B.Cache("mse", 4, 128, rows=1, capacity=4, bits2=2)  # only bits2 = bits - 1
+    with pytest.raises(B.TQError):
+        B.tq_quantize_kv(bad, rot, x)

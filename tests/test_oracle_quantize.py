@@ -179,12 +179,13 @@ def test_two_groups_of_equal_width_are_the_single_width_quantizer(mode, bits):
 def test_two_group_packing_by_hand():
     """d = 16, widths 2 (coordinates 0..7) and 1 (8..15), LSB first: codes
     3,0,1,2,3,0,1,2 give bit pairs 11 00 10 01 -> 0b10010011 = 0x93 twice;
-    codes 1,0,1,1,0,0,1,0 give 0b01001101 = 0x4d; padded to 16 bytes."""
+    codes 1,0,1,1,0,0,1,0 give 0b01001101 = 0x4d; a two-width row is padded
+    to 8 bytes (not 16), so the narrower group saves memory."""
     idx = np.array([[3, 0, 1, 2, 3, 0, 1, 2, 1, 0, 1, 1, 0, 0, 1, 0]])
     w = quantize.code_widths(16, "prod", 3, 2)
     assert w.tolist() == [2] * 8 + [1] * 8
     got = quantize.pack_codes(idx, w)
-    assert got[0].tobytes() == bytes([0x93, 0x93, 0x4D] + [0] * 13)
+    assert got[0].tobytes() == bytes([0x93, 0x93, 0x4D] + [0] * 5)
     assert np.array_equal(quantize.unpack_codes(got, 16, w), idx)
 
 
