@@ -40,11 +40,22 @@ WORKLOADS = {
     "batched_decode_16x8k": dict(batch=16, hq=32, hkv=8, d=128, seq_len=8192, rotation="rht", k_bits=3, v_bits=3),
     "long_context_128k": dict(batch=1, hq=64, hkv=8, d=128, seq_len=131072, rotation="rht", k_bits=3, v_bits=4,
                               heavy_frac=0.01),
+    # fractional-rate caches (second channel group, coordinates i % 16 >= 8, one bit narrower)
+    "llama8b_decode_32k_2p5bit": dict(batch=1, hq=32, hkv=8, d=128, seq_len=32768, rotation="rht", k_bits=3, v_bits=3,
+                                      k_bits2=2, v_bits2=2),
+    "llama8b_decode_32k_3p5bit": dict(batch=1, hq=32, hkv=8, d=128, seq_len=32768, rotation="rht", k_bits=4, v_bits=4,
+                                      k_bits2=3, v_bits2=3),
 }
 WORKLOAD = dict(name="llama8b_decode_32k", **WORKLOADS["llama8b_decode_32k"])
 FLUSH_BYTES = 256 << 20  # > 129 MB L2
 SCAN_SOURCES = ["online_kv_cache_quantize_gb300/csrc/decode_mma.cuh", "online_kv_cache_quantize_gb300/csrc/common.cuh",
                 "online_kv_cache_quantize_gb300/csrc/pipeline.cuh"]
+
+
+def _bits(w, kv):
+    """'3', or '3/2' for a fractional-rate cache (bits of the two channel groups)."""
+    b2 = w.get(kv + "_bits2")
+    return f"{w[kv + '_bits']}/{b2}" if b2 else str(w[kv + "_bits"])
 
 
 def _peaks(key="hbm_gbs"):
@@ -193,8 +204,8 @@ def run_tq(args):
     kdev = torch.from_numpy(kx.reshape(-1, d)).cuda().to(torch.bfloat16)
     vdev = torch.from_numpy(vx.reshape(-1, d)).cuda().to(torch.bfloat16)
     del kx, vx
-    kc = B.Cache("prod", w["k_bits"], d, rows=rows, capacity=T)
-    vc = B.Cache("mse", w["v_bits"], d, rows=rows, capacity=T)
+    kc = B.Cache("prod", w["k_bits"], d, rows=rows, capacity=T, bits2=w.get("k_bits2"))
+    vc = B.Cache("mse", w["v_bits"], d, rows=rows, capacity=T, bits2=w.get("v_bits2"))
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
 
@@ -275,8 +286,8 @@ def run_tq(args):
     torch.cuda.synchronize()
     q_ms = statistics.mean(a.elapsed_time(b) for a, b in qev)
     q_vectors = 2 * rows * T
-    kbytes = B.tq_code_bytes(d, w["k_bits"] - 1) + B.tq_sign_bytes(d) + 4
-    vbytes = B.tq_code_bytes(d, w["v_bits"]) + 2
+    kbytes = kc.code_stride + B.tq_sign_bytes(d) + 4
+    vbytes = vc.code_stride + 2
     q_alg_bytes = rows * T * (2 * d * 2) + rows * T * (kbytes + vbytes)
 
     # --- the timed region: exactly K steps, L2 flushed between them ---
@@ -364,7 +375,9 @@ def run_tq(args):
     value = job_throughput(ws, tokens_per_step, K, total_ms)
 
     peak, peak_kind = _peaks()
-    scan_alg = rows * T * ((w["k_bits"] - 1) * d // 8 + d // 8 + 4 + w["v_bits"] * d // 8 + 2) + bsz * hq * 2 * d * 4
+    # per token: codes (the packed bit count), signs (m = d bits), two fp16
+    # norms for K, one for V; plus each query row's B operands
+    scan_alg = rows * T * (kc.code_stride + d // 8 + 4 + vc.code_stride + 2) + bsz * hq * 2 * d * 4
     scan_avg_s = statistics.mean(scan_ms) / 1e3
     achieved = scan_alg / scan_avg_s / 1e9
     traffic, traffic_how = _traffic("decode_scan", SCAN_SOURCES, w["name"], scan_alg)
@@ -377,6 +390,7 @@ def run_tq(args):
             "dtype": "f32", "data": "synthetic",
             "config": {"workload": w["name"], "batch": bsz, "hq": hq, "hkv": hkv, "d": d, "seq_len": T,
                        "rotation": w["rotation"], "k_bits": w["k_bits"], "v_bits": w["v_bits"],
+                       **({"k_bits2": w["k_bits2"], "v_bits2": w["v_bits2"]} if w.get("k_bits2") else {}),
                        "step": "append 1 token per KV head (quantize K and V) + decode attention over seq_len tokens",
                        "l2": "flushed (256 MiB write) before every timed step", "parallelism": f"replicas x{ws}"},
             "hbm_gbs": {"scan": achieved, "quantize": q_achieved},
@@ -385,8 +399,8 @@ def run_tq(args):
                          "alg_bytes_per_launch": scan_alg, "avg_launch_us": scan_avg_s * 1e6,
                          "traffic": traffic, "traffic_source": traffic_how},
             "quantize": {"vectors_per_s": q_vectors / (q_ms / 1e3), "vectors_per_call": q_vectors,
-                         "workload": (f"cache fill: {bsz} x {hkv} KV heads x {T} tokens, K ({w['k_bits']}-bit PROD) "
-                                      f"and V ({w['v_bits']}-bit MSE), bf16 in, {w['rotation']}"),
+                         "workload": (f"cache fill: {bsz} x {hkv} KV heads x {T} tokens, K ({_bits(w, 'k')}-bit PROD) "
+                                      f"and V ({_bits(w, 'v')}-bit MSE), bf16 in, {w['rotation']}"),
                          "roofline": {"bound": "hbm", "achieved": q_achieved, "peak": peak, "unit": "GB/s",
                                       "frac": q_achieved / peak, "alg_bytes_per_call": q_alg_bytes}},
             "e2e": {"value": job_throughput(ws, tokens_per_step, 1, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -430,23 +444,23 @@ def oracle_sample(budget_s):
 
     def cache(tokens):  # the oracle's packed cache of the sample, built untimed
         if tokens not in caches:
-            caches[tokens] = (oq.quantize(k[:tokens], pi, "prod", w["k_bits"], s),
-                              oq.quantize(v[:tokens], pi, "mse", w["v_bits"]))
+            caches[tokens] = (oq.quantize(k[:tokens], pi, "prod", w["k_bits"], s, bits2=w.get("k_bits2")),
+                              oq.quantize(v[:tokens], pi, "mse", w["v_bits"], bits2=w.get("v_bits2")))
         return caches[tokens]
 
     def one(tokens):
         kq, vq = cache(tokens)
         t0 = time.perf_counter()
         # append: quantize the new token's K and V for this KV head
-        oq.quantize(k[tokens - 1:tokens], pi, "prod", w["k_bits"], s)
-        oq.quantize(v[tokens - 1:tokens], pi, "mse", w["v_bits"])
+        oq.quantize(k[tokens - 1:tokens], pi, "prod", w["k_bits"], s, bits2=w.get("k_bits2"))
+        oq.quantize(v[tokens - 1:tokens], pi, "mse", w["v_bits"], bits2=w.get("v_bits2"))
         for h in range(g):
             qp, u = oa.query_prep(q[h], pi, s)
             lg = oa.key_logits(qp, u, kq["idx"], kq["norm16"], kq["centroids"], kq["rnorm16"], kq["z"], d)
             sc = lg / np.sqrt(d)
             p = np.exp(sc - sc.max())
             p /= p.sum()
-            (p @ (vq["norm16"][:, None] * vq["centroids"][vq["idx"]])) @ pi
+            (p @ (vq["norm16"][:, None] * oq.coord_centroids(vq["centroids"], vq["idx"]))) @ pi
         return time.perf_counter() - t0
 
     probe = 2048

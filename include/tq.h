@@ -144,7 +144,9 @@ tq_status tq_codebook(int d, int bits, double* centroids, double* boundaries);
  * of coordinates 0 .. i-1), stride tq_code_bytes2 (rounded up to 8 bytes, so
  * the smaller width saves memory). Supported: d = 128 and bits2 = bits - 1
  * (keys 3/2 = 2.5 and 4/3 = 3.5 bits, values likewise). tq_quantize_kv takes
- * them; the decode entry points and the search return TQ_ERR_UNSUPPORTED. */
+ * them; the decode entry points take them when the key and the value cache
+ * are both fractional-rate (one of each kind: TQ_ERR_UNSUPPORTED); the search
+ * returns TQ_ERR_UNSUPPORTED. */
 typedef struct {
     int mode;         /* TQ_MSE (values) or TQ_PROD (keys)                   */
     int bits;         /* MSE: 1..4 Lloyd-Max bits; PROD: 2..5 = (bits-1) + 1 */

@@ -232,7 +232,7 @@ class Cache:
 
         self.mode = MODES.get(mode, mode)
         self.bits, self.d, self.rows, self.capacity = bits, d, rows, capacity
-        self.bits2 = bits2 if bits2 is not None and bits2 != bits else None
+        self.bits2 = bits2 if bits2 and bits2 != bits else None
         self.m = (m if m is not None else d) if self.mode == TQ_PROD else 0
         cb = bits - 1 if self.mode == TQ_PROD else bits
         self.code_bits = cb
@@ -436,7 +436,7 @@ class QuantizedKVCache:
     planes and a workspace, and forms the calls' arguments."""
 
     def __init__(self, batch, hq, hkv, capacity, d=128, k_bits=3, v_bits=3, rotation="rht", rot_seed=1, qjl_seed=2,
-                 device="cuda"):
+                 device="cuda", k_bits2=None, v_bits2=None):
         import torch
 
         if hq % hkv:
@@ -444,8 +444,8 @@ class QuantizedKVCache:
         self.batch, self.hq, self.hkv, self.capacity, self.d = batch, hq, hkv, capacity, d
         self.rot = tq_rotation_to_device(tq_make_rotation(rot_seed, d, rotation))
         self.qjl = tq_qjl_to_device(tq_make_qjl(qjl_seed, d, d))
-        self.k = Cache("prod", k_bits, d, rows=batch * hkv, capacity=capacity, device=device)
-        self.v = Cache("mse", v_bits, d, rows=batch * hkv, capacity=capacity, device=device)
+        self.k = Cache("prod", k_bits, d, rows=batch * hkv, capacity=capacity, device=device, bits2=k_bits2)
+        self.v = Cache("mse", v_bits, d, rows=batch * hkv, capacity=capacity, device=device, bits2=v_bits2)
         self.lengths = torch.zeros(batch, dtype=torch.int32, device=device)
         self._ws = None
 

@@ -133,13 +133,15 @@ uint32_t fp16_bits(double v) { return (uint32_t)__half_as_ushort(__float2half_rn
 // Scale lam for the fp16 centroid tables of the tensor-core scan: among
 // lam = 2^e (1 + k/2^18) with lam * max|c| in [1, 2), the one whose products
 // lam * c_i lie closest (relative) to fp16 values, so the table entries
-// carry the centroids almost exactly. Cached per (d, bits).
-double pick_lambda(int d, int bits, const std::vector<double>& c) {
+// carry the centroids almost exactly. c holds the positive centroids of one
+// codebook, or of both groups of a fractional-rate cache (one lam serves
+// both tables). Cached per (d, key).
+double pick_lambda(int d, int key, const std::vector<double>& c) {
     static std::mutex mu;
     static std::map<std::pair<int, int>, double> cache;
     {
         std::lock_guard<std::mutex> lk(mu);
-        auto it = cache.find({d, bits});
+        auto it = cache.find({d, key});
         if (it != cache.end()) return it->second;
     }
     double mx = 0.0;
@@ -152,7 +154,7 @@ double pick_lambda(int d, int bits, const std::vector<double>& c) {
     for (int k = 0; k < n; ++k) {
         const double l = base * (1.0 + (double)k / n);
         double err = 0.0;
-        for (size_t v = c.size() / 2; v < c.size() && err < best; ++v) {
+        for (size_t v = 0; v < c.size() && err < best; ++v) {
             const double x = l * c[v];
             err = std::max(err, std::fabs(fp16_round(x) - x) / x);
         }
@@ -162,8 +164,16 @@ double pick_lambda(int d, int bits, const std::vector<double>& c) {
         }
     }
     std::lock_guard<std::mutex> lk(mu);
-    cache[{d, bits}] = best_l;
+    cache[{d, key}] = best_l;
     return best_l;
+}
+
+// the positive centroids of the codebooks of code bits cb and cb2 (a
+// Lloyd-Max codebook is symmetric about 0, sorted ascending)
+std::vector<double> positive_centroids(const std::vector<double>& c, const std::vector<double>* c2) {
+    std::vector<double> out(c.begin() + c.size() / 2, c.end());
+    if (c2) out.insert(out.end(), c2->begin() + c2->size() / 2, c2->end());
+    return out;
 }
 
 void pair_table(const std::vector<double>& c, int bits, double lam, uint32_t* out) {
@@ -295,6 +305,7 @@ struct DecodeLaunch {
     tqk::DecodeParams dp;
     tqk::CombineParams cp;
     int kb = 0, vb = 0;
+    bool two = false;  // fractional-rate key and value caches
     cudaEvent_t scan_begin = nullptr, scan_end = nullptr;
 };
 
@@ -400,7 +411,9 @@ tq_status decode_prepare(const tq_decode_args* a, void* workspace, size_t ws_byt
     int kb = 0, vb = 0, kb2 = 0, vb2 = 0;
     if ((s = check_cache(a->k, "tq_attn_decode k", &kb, &kb2)) != TQ_OK) return s;
     if ((s = check_cache(a->v, "tq_attn_decode v", &vb, &vb2)) != TQ_OK) return s;
-    if (kb2 != kb || vb2 != vb) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: fractional-rate caches are not supported yet");
+    const bool two = kb2 != kb;
+    if ((vb2 != vb) != two)
+        return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: keys and values must both be fractional-rate caches, or neither");
     if (a->k.mode != TQ_PROD || a->v.mode != TQ_MSE) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: keys must be PROD and values MSE");
     if (a->k.d != a->d || a->v.d != a->d) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: cache d does not match");
     if (a->k.m != 128) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: m must be 128");
@@ -451,9 +464,11 @@ tq_status decode_prepare(const tq_decode_args* a, void* workspace, size_t ws_byt
     pp.frag = frag;
     pp.qjl_scale = (float)(std::sqrt(M_PI / 2.0) / a->k.m);
 
-    std::vector<double> kc, kt, vc, vt;
+    std::vector<double> kc, kt, vc, vt, kc2, vc2;
     if ((s = tq::codebook(a->d, kb, kc, kt)) != TQ_OK) return s;
     if ((s = tq::codebook(a->d, vb, vc, vt)) != TQ_OK) return s;
+    if (two && (s = tq::codebook(a->d, kb2, kc2, kt)) != TQ_OK) return s;
+    if (two && (s = tq::codebook(a->d, vb2, vc2, vt)) != TQ_OK) return s;
     dp.frag = frag;
     dp.batch = a->batch;
     dp.hq = a->hq;
@@ -464,20 +479,26 @@ tq_status decode_prepare(const tq_decode_args* a, void* workspace, size_t ws_byt
     dp.seq_lens = a->seq_lens;
     dp.capacity = a->k.capacity;
     dp.kcodes = a->k.codes;
-    dp.kcode_stride = tq_code_bytes(a->d, kb);
+    dp.kcode_stride = tq_code_bytes2(a->d, kb, kb2);
     dp.ksigns = a->k.signs;
     dp.ksign_stride = tq_sign_bytes(a->k.m);
     dp.knorm = a->k.norm;
     dp.krnorm = a->k.rnorm;
     dp.vcodes = a->v.codes;
-    dp.vcode_stride = tq_code_bytes(a->d, vb);
+    dp.vcode_stride = tq_code_bytes2(a->d, vb, vb2);
     dp.vnorm = a->v.norm;
     for (size_t i = 0; i < kc.size(); ++i) dp.kc[i] = (float)kc[i];
     for (size_t i = 0; i < vc.size(); ++i) dp.vc[i] = (float)vc[i];
-    const double lam_k = pick_lambda(a->d, kb, kc), lam_v = pick_lambda(a->d, vb, vc);
+    const double lam_k = pick_lambda(a->d, 16 * kb + kb2, positive_centroids(kc, two ? &kc2 : nullptr));
+    const double lam_v = pick_lambda(a->d, 16 * vb + vb2, positive_centroids(vc, two ? &vc2 : nullptr));
     pair_table(kc, kb, lam_k, dp.klut);
     pair_table_lo(kc, kb, lam_k, dp.klut_lo);
     pair_table(vc, vb, lam_v, dp.vlut);
+    if (two) {
+        pair_table(kc2, kb2, lam_k, dp.klut2);
+        pair_table_lo(kc2, kb2, lam_k, dp.klut2_lo);
+        pair_table(vc2, vb2, lam_v, dp.vlut2);
+    }
     dp.inv_lam_k = (float)(1.0 / lam_k);
     dp.inv_lam_v = (float)(1.0 / lam_v);
     dp.qjl_scale = (float)(std::sqrt(M_PI / 2.0) / a->k.m);
@@ -492,6 +513,7 @@ tq_status decode_prepare(const tq_decode_args* a, void* workspace, size_t ws_byt
     if (e != cudaSuccess) return cuda_status(e, "tq_attn_decode error word");
     D->kb = kb;
     D->vb = vb;
+    D->two = two;
     D->scan_begin = (cudaEvent_t)a->scan_begin;
     D->scan_end = (cudaEvent_t)a->scan_end;
 
@@ -524,7 +546,7 @@ tq_status decode_launch(const DecodeLaunch& D, cudaStream_t st, tqk::StepPrepPar
     if (e != cudaSuccess) return cuda_status(e, "tq_attn_decode query prep");
     if (D.scan_begin && (e = cudaEventRecord(D.scan_begin, st)) != cudaSuccess)
         return cuda_status(e, "tq_attn_decode scan_begin");
-    e = tqk::launch_decode_mma(D.dp, D.kb, D.vb, st);
+    e = tqk::launch_decode_mma(D.dp, D.kb, D.vb, D.two, st);
     if (e != cudaSuccess) return cuda_status(e, "tq_attn_decode scan");
     if (D.scan_end && (e = cudaEventRecord(D.scan_end, st)) != cudaSuccess)
         return cuda_status(e, "tq_attn_decode scan_end");
@@ -745,7 +767,7 @@ tq_status tq_score_topk(const tq_topk_args* a, void* workspace, size_t ws_bytes,
     tp.scores = a->scores;
     // the tcgen05 scan where its shared-memory plan fits (d, m <= 256 padded
     // to a multiple of 16), the SIMT scan otherwise
-    const double lam = pick_lambda(a->d, cb, c);
+    const double lam = pick_lambda(a->d, 16 * cb + cb, positive_centroids(c, nullptr));
     pair_table(c, cb, lam, tp.ktab);
     pair_table_lo(c, cb, lam, tp.ktab_lo);
     tp.inv_lam = (float)(1.0 / lam);

@@ -91,17 +91,17 @@ cudaError_t launch_query_prep(const PrepParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_decode_mma_g1(const DecodeParams& p, int kbits, int vbits, cudaStream_t s);
-cudaError_t launch_decode_mma_g2(const DecodeParams& p, int kbits, int vbits, cudaStream_t s);
-cudaError_t launch_decode_mma_g4(const DecodeParams& p, int kbits, int vbits, cudaStream_t s);
-cudaError_t launch_decode_mma_g8(const DecodeParams& p, int kbits, int vbits, cudaStream_t s);
+cudaError_t launch_decode_mma_g1(const DecodeParams& p, int kbits, int vbits, bool two, cudaStream_t s);
+cudaError_t launch_decode_mma_g2(const DecodeParams& p, int kbits, int vbits, bool two, cudaStream_t s);
+cudaError_t launch_decode_mma_g4(const DecodeParams& p, int kbits, int vbits, bool two, cudaStream_t s);
+cudaError_t launch_decode_mma_g8(const DecodeParams& p, int kbits, int vbits, bool two, cudaStream_t s);
 
-cudaError_t launch_decode_mma(const DecodeParams& p, int kbits, int vbits, cudaStream_t s) {
+cudaError_t launch_decode_mma(const DecodeParams& p, int kbits, int vbits, bool two, cudaStream_t s) {
     switch (p.group) {
-        case 1: return launch_decode_mma_g1(p, kbits, vbits, s);
-        case 2: return launch_decode_mma_g2(p, kbits, vbits, s);
-        case 4: return launch_decode_mma_g4(p, kbits, vbits, s);
-        case 8: return launch_decode_mma_g8(p, kbits, vbits, s);
+        case 1: return launch_decode_mma_g1(p, kbits, vbits, two, s);
+        case 2: return launch_decode_mma_g2(p, kbits, vbits, two, s);
+        case 4: return launch_decode_mma_g4(p, kbits, vbits, two, s);
+        case 8: return launch_decode_mma_g8(p, kbits, vbits, two, s);
     }
     return cudaErrorInvalidValue;
 }

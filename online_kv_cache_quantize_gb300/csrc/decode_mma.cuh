@@ -25,6 +25,14 @@
 // holding one tile per warp (64 tokens) and filled by six bulk (TMA) copies
 // -- one per cache plane -- that complete on the stage's mbarrier. The capacity
 // of the cache must be a multiple of 16 so that a tile never leaves its row.
+//
+// Fractional-rate caches (two channel groups, the Qiita article's 2.5 / 3.5
+// bit rows): coordinate i has KB code bits when i % 16 < 8 and KB2 otherwise
+// (values VB / VB2), codes packed in coordinate order, 8 (KB + KB2) bytes per
+// token. With the K permutation above, thread c's k-steps kk = 0, 1, 4, 5 hold
+// first-group coordinates and kk = 2, 3, 6, 7 second-group ones; with the M
+// permutation, value m-tiles 0..3 are first-group and 4..7 second-group.
+// Each group has its own pair table, both scaled by one lam.
 #pragma once
 
 #include "common.cuh"
@@ -36,12 +44,14 @@ namespace tqk {
 constexpr int kMmaWarps = 4;
 constexpr int kMmaStages = 4;
 
-template <int KB, int VB>
+template <int KB, int VB, int KB2 = KB, int VB2 = VB>
 struct MmaTile {
-    static constexpr int KC = 16 * 16 * KB;  // key code bytes (16 tokens x 16*KB)
-    static constexpr int SG = 16 * 16;       // sign bytes (m = 128)
-    static constexpr int NB = 32;            // 16 fp16 scalars
-    static constexpr int VC = 16 * 16 * VB;  // value code bytes
+    static constexpr int KS = 8 * (KB + KB2);  // key code bytes per token
+    static constexpr int VS = 8 * (VB + VB2);  // value code bytes per token
+    static constexpr int KC = 16 * KS;         // key code bytes (16 tokens)
+    static constexpr int SG = 16 * 16;         // sign bytes (m = 128)
+    static constexpr int NB = 32;              // 16 fp16 scalars
+    static constexpr int VC = 16 * VS;         // value code bytes
     static constexpr int OFF_KC = 0;
     static constexpr int OFF_SG = OFF_KC + KC;
     static constexpr int OFF_KN = OFF_SG + SG;
@@ -103,12 +113,26 @@ __device__ __forceinline__ T lds_at(const void* base, uint32_t byte_off) {
     return *reinterpret_cast<const T*>(reinterpret_cast<const unsigned char*>(base) + byte_off);
 }
 
-template <int KB, int VB, int G>
+// the bit offset of key k-step kk in thread c's run of 32 coordinates
+// (fractional rates: k-steps 2, 3, 6, 7 are second-group)
+template <int KB, int KB2>
+__device__ __forceinline__ constexpr int key_off(int kk) {
+    return (kk >> 2) * 8 * (KB + KB2) + ((kk & 3) == 0 ? 0 : (kk & 3) == 1 ? 4 * KB : (kk & 3) == 2 ? 8 * KB : 8 * KB + 4 * KB2);
+}
+// the bit offset of value m-tile mt in thread g's run of 16 coordinates
+template <int VB, int VB2>
+__device__ __forceinline__ constexpr int val_off(int mt) {
+    return mt < 4 ? 2 * VB * mt : 8 * VB + 2 * VB2 * (mt - 4);
+}
+
+template <int KB, int VB, int G, int KB2 = KB, int VB2 = VB>
 __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_kernel(const __grid_constant__ DecodeParams p) {
-    using T = MmaTile<KB, VB>;
+    using T = MmaTile<KB, VB, KB2, VB2>;
     constexpr int NT = (G + 3) / 4;   // n-tiles of 4 heads (x hi/lo)
+    constexpr bool K2 = KB2 != KB, V2 = VB2 != VB;  // two channel groups
     constexpr int KL = 1 << (2 * KB);  // key pair-table entries
     constexpr int VL = 1 << (2 * VB);  // value pair-table entries
+    constexpr int KL2 = K2 ? 1 << (2 * KB2) : 1, VL2 = V2 ? 1 << (2 * VB2) : 1;
     constexpr bool KLO = KB >= 3;      // second (lo) key table for 8+ centroids
     constexpr int D = 128;
 
@@ -118,6 +142,9 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
     __shared__ uint32_t klut[KL];
     __shared__ uint32_t klo[KLO ? KL : 1];
     __shared__ uint32_t vlut[VL];
+    __shared__ uint32_t klut2[KL2];
+    __shared__ uint32_t klo2[(KLO && K2) ? KL2 : 1];
+    __shared__ uint32_t vlut2[VL2];
     __shared__ __align__(8) uint2 slut4[16];  // 4 sign bits -> (+-1, +-1), (+-1, +-1) as fp16
     __shared__ __align__(8) uint64_t s_bar[kMmaStages];  // one per stage of the CTA ring
     __shared__ uint32_t s_cnt[kMmaStages];                // warps done with a stage, cumulative
@@ -130,6 +157,13 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
     if constexpr (KLO)
         for (int i = threadIdx.x; i < KL; i += blockDim.x) klo[i] = p.klut_lo[i];
     for (int i = threadIdx.x; i < VL; i += blockDim.x) vlut[i] = p.vlut[i];
+    if constexpr (K2) {
+        for (int i = threadIdx.x; i < KL2; i += blockDim.x) klut2[i] = p.klut2[i];
+        if constexpr (KLO)
+            for (int i = threadIdx.x; i < KL2; i += blockDim.x) klo2[i] = p.klut2_lo[i];
+    }
+    if constexpr (V2)
+        for (int i = threadIdx.x; i < VL2; i += blockDim.x) vlut2[i] = p.vlut2[i];
     const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(&s_bar[0]);
     if (threadIdx.x == 0) {
 #pragma unroll
@@ -170,11 +204,11 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
         const uint32_t ntok = 16u * (uint32_t)ntg;
         fence_proxy_async_smem();  // the warps' reads of this stage come first
         mbar_arrive_expect_tx(bar, (uint32_t)ntg * T::BYTES);
-        bulk_g2s(dst + kMmaWarps * T::OFF_KC, p.kcodes + slot * (16 * KB), ntok * 16 * KB, bar);
+        bulk_g2s(dst + kMmaWarps * T::OFF_KC, p.kcodes + slot * T::KS, ntok * T::KS, bar);
         bulk_g2s(dst + kMmaWarps * T::OFF_SG, p.ksigns + slot * 16, ntok * 16, bar);
         bulk_g2s(dst + kMmaWarps * T::OFF_KN, p.knorm + slot, ntok * 2, bar);
         bulk_g2s(dst + kMmaWarps * T::OFF_KR, p.krnorm + slot, ntok * 2, bar);
-        bulk_g2s(dst + kMmaWarps * T::OFF_VC, p.vcodes + slot * (16 * VB), ntok * 16 * VB, bar);
+        bulk_g2s(dst + kMmaWarps * T::OFF_VC, p.vcodes + slot * T::VS, ntok * T::VS, bar);
         bulk_g2s(dst + kMmaWarps * T::OFF_VN, p.vnorm + slot, ntok * 2, bar);
     };
     // Launched as a programmatic dependent of the query prep, which writes the
@@ -260,18 +294,37 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
         const int tok0 = t0 + 16 * (warp + kMmaWarps * i);
 
         // ---- keys and signs: D[token][2h+s] ----
-        uint32_t kw0[KB + 1], kw1[KB + 1];
-        {
-            const uint32_t* r0 = reinterpret_cast<const uint32_t*>(p_kc + g * 16 * KB) + KB * c;
-            const uint32_t* r1 = reinterpret_cast<const uint32_t*>(p_kc + (g + 8) * 16 * KB) + KB * c;
+        // thread c's 32 coordinates: 16 (KB + KB2) bits from bit 16 c (KB + KB2)
+        constexpr int KWN = (KB + KB2 + 1) / 2;  // words holding them
+        uint32_t kw0[KWN + 1], kw1[KWN + 1];
+        if constexpr (!K2) {
+            const uint32_t* r0 = reinterpret_cast<const uint32_t*>(p_kc + g * T::KS) + KB * c;
+            const uint32_t* r1 = reinterpret_cast<const uint32_t*>(p_kc + (g + 8) * T::KS) + KB * c;
 #pragma unroll
             for (int w = 0; w < KB; ++w) {
                 kw0[w] = r0[w];
                 kw1[w] = r1[w];
             }
-            kw0[KB] = 0u;
-            kw1[KB] = 0u;
+        } else {
+            // an odd KB + KB2 starts odd c's run half way into a word
+            constexpr int TW = T::KS / 4;  // words per token
+            const int wb = (c * (KB + KB2)) >> 1, sh = ((c * (KB + KB2)) & 1) * 16;
+            const uint32_t* r0 = reinterpret_cast<const uint32_t*>(p_kc + g * T::KS) + wb;
+            const uint32_t* r1 = reinterpret_cast<const uint32_t*>(p_kc + (g + 8) * T::KS) + wb;
+            uint32_t x0[KWN + 1], x1[KWN + 1];
+#pragma unroll
+            for (int w = 0; w <= KWN; ++w) {
+                x0[w] = wb + w < TW ? r0[w] : 0u;
+                x1[w] = wb + w < TW ? r1[w] : 0u;
+            }
+#pragma unroll
+            for (int w = 0; w < KWN; ++w) {
+                kw0[w] = __funnelshift_r(x0[w], x0[w + 1], sh);
+                kw1[w] = __funnelshift_r(x1[w], x1[w + 1], sh);
+            }
         }
+        kw0[KWN] = 0u;
+        kw1[KWN] = 0u;
         const uint32_t sw0 = reinterpret_cast<const uint32_t*>(p_sg + g * 16)[c];
         const uint32_t sw1 = reinterpret_cast<const uint32_t*>(p_sg + (g + 8) * 16)[c];
         // two accumulator chains per product (even and odd kk) so that
@@ -288,14 +341,18 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
                 }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t f0 = field4(kw0, 4 * KB * kk, 2 * KB), f1 = field4(kw1, 4 * KB * kk, 2 * KB);
-            const uint32_t f2 = field4(kw0, 4 * KB * kk + 2 * KB, 2 * KB);
-            const uint32_t f3 = field4(kw1, 4 * KB * kk + 2 * KB, 2 * KB);
-            const uint32_t a0 = lds_at<uint32_t>(klut, f0), a1 = lds_at<uint32_t>(klut, f1);
-            const uint32_t a2 = lds_at<uint32_t>(klut, f2), a3 = lds_at<uint32_t>(klut, f3);
+            const bool first = !K2 || (kk & 3) < 2;
+            const int kw = first ? KB : KB2, ko = key_off<KB, KB2>(kk);
+            const uint32_t* tab = first ? klut : klut2;
+            const uint32_t* tlo = first ? klo : klo2;
+            const uint32_t f0 = field4(kw0, ko, 2 * kw), f1 = field4(kw1, ko, 2 * kw);
+            const uint32_t f2 = field4(kw0, ko + 2 * kw, 2 * kw);
+            const uint32_t f3 = field4(kw1, ko + 2 * kw, 2 * kw);
+            const uint32_t a0 = lds_at<uint32_t>(tab, f0), a1 = lds_at<uint32_t>(tab, f1);
+            const uint32_t a2 = lds_at<uint32_t>(tab, f2), a3 = lds_at<uint32_t>(tab, f3);
             if constexpr (KLO) {
-                const uint32_t l0 = lds_at<uint32_t>(klo, f0), l1 = lds_at<uint32_t>(klo, f1);
-                const uint32_t l2 = lds_at<uint32_t>(klo, f2), l3 = lds_at<uint32_t>(klo, f3);
+                const uint32_t l0 = lds_at<uint32_t>(tlo, f0), l1 = lds_at<uint32_t>(tlo, f1);
+                const uint32_t l2 = lds_at<uint32_t>(tlo, f2), l3 = lds_at<uint32_t>(tlo, f3);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) mma16816(dk[kk & 1][nt], l0, l1, l2, l3, bk[nt][kk][0], bk[nt][kk][1]);
             }
@@ -370,16 +427,17 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
             bv[nt][0] = prow[2 * c];      // tokens 4c, 4c+1
             bv[nt][1] = prow[2 * c + 1];  // tokens 4c+2, 4c+3
         }
-        // each thread: tokens 4c..4c+3, coordinates 16g..16g+15 (16*VB bits at 16*VB*g)
+        // each thread: tokens 4c..4c+3, coordinates 16g..16g+15 (8 (VB + VB2)
+        // bits from bit 8 (VB + VB2) g)
         uint32_t vf[4][3];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const uint32_t* vr = reinterpret_cast<const uint32_t*>(p_vc + (4 * c + j) * 16 * VB);
-            const int bit0 = 16 * VB * g;
+            const uint32_t* vr = reinterpret_cast<const uint32_t*>(p_vc + (4 * c + j) * T::VS);
+            const int bit0 = 8 * (VB + VB2) * g;
             const int w = bit0 >> 5, sh = bit0 & 31;
             const uint32_t x0 = vr[w];
-            const uint32_t x1 = (w + 1 < 4 * VB) ? vr[w + 1] : 0u;
-            const uint32_t x2 = (w + 2 < 4 * VB) ? vr[w + 2] : 0u;
+            const uint32_t x1 = (w + 1 < T::VS / 4) ? vr[w + 1] : 0u;
+            const uint32_t x2 = (w + 2 < T::VS / 4) ? vr[w + 2] : 0u;
             vf[j][0] = __funnelshift_r(x0, x1, sh);
             vf[j][1] = __funnelshift_r(x1, x2, sh);
             vf[j][2] = 0u;
@@ -388,7 +446,9 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
         for (int mt = 0; mt < 8; ++mt) {
             uint32_t x[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) x[j] = lds_at<uint32_t>(vlut, field4(vf[j], 2 * VB * mt, 2 * VB));
+            for (int j = 0; j < 4; ++j)
+                x[j] = (!V2 || mt < 4) ? lds_at<uint32_t>(vlut, field4(vf[j], val_off<VB, VB2>(mt), 2 * VB))
+                                       : lds_at<uint32_t>(vlut2, field4(vf[j], val_off<VB, VB2>(mt), 2 * VB2));
             const uint32_t a0 = prmt(x[0], x[1], 0x5410u);
             const uint32_t a1 = prmt(x[0], x[1], 0x7632u);
             const uint32_t a2 = prmt(x[2], x[3], 0x5410u);
@@ -467,34 +527,74 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (G > 4 ? 2 : 4)) decode_mma_ke
     }
 }
 
-template <int KB, int VB, int G>
+template <int KB, int VB, int G, int KB2 = KB, int VB2 = VB>
 size_t decode_mma_smem();
 
 // Launches the scan as a programmatic dependent of the launch before it on
 // the stream: its CTAs may become resident and set up while that launch runs,
 // and wait for it (griddepcontrol.wait) before reading anything.
-template <int KB, int VB, int G>
+template <int KB, int VB, int G, int KB2 = KB, int VB2 = VB>
 cudaError_t launch_decode_mma_t(const DecodeParams& p, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.n_splits, (unsigned)p.hkv, (unsigned)p.batch);
     cfg.blockDim = dim3(kMmaWarps * 32);
-    cfg.dynamicSmemBytes = decode_mma_smem<KB, VB, G>();
+    cfg.dynamicSmemBytes = decode_mma_smem<KB, VB, G, KB2, VB2>();
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<KB, VB, G>, p);
+    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<KB, VB, G, KB2, VB2>, p);
 }
 
-template <int KB, int VB, int G>
+template <int KB, int VB, int G, int KB2, int VB2>
 size_t decode_mma_smem() {
-    using T = MmaTile<KB, VB>;
+    using T = MmaTile<KB, VB, KB2, VB2>;
     constexpr int NT = (G + 3) / 4;
     size_t pipe = (size_t)kMmaWarps * kMmaStages * T::BYTES + 2 * kMmaWarps * NT * 8 * 16;
     size_t merge = (size_t)kMmaWarps * G * 128 * 4 + kMmaWarps * G * 2 * 4;
     return pipe > merge ? pipe : merge;
+}
+
+}  // namespace tqk
+
+namespace tqk {
+
+// Instantiations for one G: every single-width (KB, VB) in 1..4, and the
+// fractional-rate caches with both keys and values split into two groups
+// (KB2 = KB - 1, VB2 = VB - 1).
+template <int G, int KB, int KB2>
+cudaError_t decode_mma_v(const DecodeParams& p, int vb, cudaStream_t s) {
+    constexpr bool two = KB2 != KB;
+    switch (vb) {
+        case 1:
+            if constexpr (!two) return launch_decode_mma_t<KB, 1, G>(p, s);
+            break;
+        case 2: return launch_decode_mma_t<KB, 2, G, KB2, two ? 1 : 2>(p, s);
+        case 3: return launch_decode_mma_t<KB, 3, G, KB2, two ? 2 : 3>(p, s);
+        case 4: return launch_decode_mma_t<KB, 4, G, KB2, two ? 3 : 4>(p, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <int G>
+cudaError_t dispatch_decode_mma(const DecodeParams& p, int kbits, int vbits, bool two, cudaStream_t s) {
+    if (!two) {
+        switch (kbits) {
+            case 1: return decode_mma_v<G, 1, 1>(p, vbits, s);
+            case 2: return decode_mma_v<G, 2, 2>(p, vbits, s);
+            case 3: return decode_mma_v<G, 3, 3>(p, vbits, s);
+            case 4: return decode_mma_v<G, 4, 4>(p, vbits, s);
+        }
+    } else {
+        switch (kbits) {
+            case 2: return decode_mma_v<G, 2, 1>(p, vbits, s);
+            case 3: return decode_mma_v<G, 3, 2>(p, vbits, s);
+            case 4: return decode_mma_v<G, 4, 3>(p, vbits, s);
+        }
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace tqk

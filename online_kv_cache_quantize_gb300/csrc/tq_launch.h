@@ -131,11 +131,17 @@ struct DecodeParams {
     uint32_t klut[256];
     uint32_t klut_lo[256];  // residual table lam*c - fp16(lam*c), used for 3-4 bit key codes
     uint32_t vlut[256];
+    // fractional-rate caches: the second channel group's tables (same lam)
+    uint32_t klut2[64];
+    uint32_t klut2_lo[64];
+    uint32_t vlut2[64];
     float inv_lam_k, inv_lam_v;
     uint32_t* err;          // device error word (a wait that ran out sets a bit)
 };
 
-cudaError_t launch_decode_mma(const DecodeParams& p, int kbits, int vbits, cudaStream_t s);
+// two: keys and values are both fractional-rate caches (code bits kbits /
+// kbits - 1 and vbits / vbits - 1)
+cudaError_t launch_decode_mma(const DecodeParams& p, int kbits, int vbits, bool two, cudaStream_t s);
 
 // The library's device error word of the current device (bits kErr* of
 // pipeline.cuh), and a kernel that waits on an mbarrier that nothing

@@ -27,18 +27,19 @@ def _built():
     build.build()
 
 
-def _oracle_caches(k, v, kbits, vbits, kind, d=128):
-    """Oracle-quantized caches: returns (unpacked dicts, GPU caches, oracle qz)."""
+def _oracle_caches(k, v, kbits, vbits, kind, d=128, kbits2=None, vbits2=None):
+    """Oracle-quantized caches: returns (unpacked dicts, GPU caches, oracle qz);
+    kbits2 / vbits2: the second channel group's bits of fractional-rate caches."""
     bsz, hkv, cap, _ = k.shape
     pi, s = P.oracle_mats(d, kind)
-    kq = oq.quantize(k.reshape(-1, d).astype(np.float64), pi, "prod", kbits, s)
-    vq = oq.quantize(v.reshape(-1, d).astype(np.float64), pi, "mse", vbits)
+    kq = oq.quantize(k.reshape(-1, d).astype(np.float64), pi, "prod", kbits, s, bits2=kbits2)
+    vq = oq.quantize(v.reshape(-1, d).astype(np.float64), pi, "mse", vbits, bits2=vbits2)
     sh = (bsz, hkv, cap)
     kc = {"idx": kq["idx"].reshape(sh + (d,)), "norm16": kq["norm16"].reshape(sh),
           "rnorm16": kq["rnorm16"].reshape(sh), "z": kq["z"].reshape(sh + (d,))}
     vc = {"idx": vq["idx"].reshape(sh + (d,)), "norm16": vq["norm16"].reshape(sh)}
-    gk = P.oracle_cache_planes(kq, "prod", kbits, bsz * hkv, cap)
-    gv = P.oracle_cache_planes(vq, "mse", vbits, bsz * hkv, cap)
+    gk = P.oracle_cache_planes(kq, "prod", kbits, bsz * hkv, cap, bits2=kbits2)
+    gv = P.oracle_cache_planes(vq, "mse", vbits, bsz * hkv, cap, bits2=vbits2)
     return kc, vc, gk, gv, kq, vq, pi, s
 
 
@@ -178,3 +179,41 @@ def test_full_decode_shape_gpu_quantize_then_decode():
         want = (p @ vhat) @ pi
         scale = np.max(vq["norm16"]) / np.sqrt(d)
         assert np.max(np.abs(out[0, h] - want)) <= OUT_TOL * scale, h
+
+
+@pytest.mark.parametrize("kbits,vbits", [(3, 3), (4, 4), (5, 4), (3, 2), (4, 2)])
+@pytest.mark.parametrize("kind", ["rht", "dense"])
+def test_fractional_rate_caches(kbits, vbits, kind):
+    """Two-group caches (coordinates with i % 16 < 8 at bits, the rest at
+    bits - 1): keys PROD 3/2 and values MSE 3/2 make the 2.5-bit cache, 4/3 and
+    4/3 the 3.5-bit one; 32 q / 8 KV heads, outlier data, ragged length."""
+    k, v = W.decode_kv(1, 8, 1008, heavy_frac=0.05, seed=kbits * 10 + vbits)
+    kc, vc, gk, gv, kq, vq, pi, s = _oracle_caches(k, v, kbits, vbits, kind, kbits2=kbits - 1, vbits2=vbits - 1)
+    q = W.query_vectors((1, 32, 128), dtype="bf16")
+    out, logits = _gpu_decode(q, gk, gv, [997], kind)
+    scale = np.max(vc["norm16"]) / np.sqrt(128)
+    _check(q, kc, vc, kq, vq, [997], pi, s, out, logits, out_scale=scale)
+
+
+@pytest.mark.parametrize("group", [1, 8])
+def test_fractional_rate_group_sizes_and_batch(group):
+    """2.5-bit caches, batch 3 with lengths (0, 17, 300), group sizes 1 and 8."""
+    hkv, cap = 2, 320
+    k, v = W.decode_kv(3, hkv, cap, heavy_frac=0.05)
+    kc, vc, gk, gv, kq, vq, pi, s = _oracle_caches(k, v, 3, 3, "rht", kbits2=2, vbits2=2)
+    q = W.query_vectors((3, hkv * group, 128))
+    lens = [0, 17, 300]
+    out, logits = _gpu_decode(q, gk, gv, lens, "rht")
+    scale = np.max(vc["norm16"]) / np.sqrt(128)
+    _check(q, kc, vc, kq, vq, lens, pi, s, out, logits, out_scale=scale)
+
+
+def test_fractional_rate_mixed_caches_rejected():
+    """Keys at a fractional rate with whole-width values (or the reverse) are
+    not taken: TQ_ERR_UNSUPPORTED, nothing launched."""
+    k, v = W.decode_kv(1, 2, 64)
+    for kb2, vb2 in ((2, None), (None, 2)):
+        kc, vc, gk, gv, kq, vq, pi, s = _oracle_caches(k, v, 3, 3, "rht", kbits2=kb2, vbits2=vb2)
+        with pytest.raises(B.TQError) as e:
+            _gpu_decode(W.query_vectors((1, 8, 128)), gk, gv, [64], "rht")
+        assert "UNSUPPORTED" in str(e.value)

@@ -25,14 +25,14 @@ def _built():
     build.build()
 
 
-def _setup(bsz, hkv, hq, cap, kind, kbits, vbits, seed):
+def _setup(bsz, hkv, hq, cap, kind, kbits, vbits, seed, kbits2=0, vbits2=0):
     d = 128
     k, v = W.decode_kv(bsz, hkv, cap, seed=seed)
     rot, qjl = P.handles(d, kind)
     caches = []
     for _ in range(2):
-        kc = B.Cache("prod", kbits, d, rows=bsz * hkv, capacity=cap)
-        vc = B.Cache("mse", vbits, d, rows=bsz * hkv, capacity=cap)
+        kc = B.Cache("prod", kbits, d, rows=bsz * hkv, capacity=cap, bits2=kbits2)
+        vc = B.Cache("mse", vbits, d, rows=bsz * hkv, capacity=cap, bits2=vbits2)
         B.tq_quantize_kv(kc, rot, torch.from_numpy(k.reshape(-1, d)).cuda().to(torch.bfloat16), qjl=qjl)
         B.tq_quantize_kv(vc, rot, torch.from_numpy(v.reshape(-1, d)).cuda().to(torch.bfloat16))
         caches.append((kc, vc))
@@ -42,10 +42,13 @@ def _setup(bsz, hkv, hq, cap, kind, kbits, vbits, seed):
     return k, v, rot, qjl, caches, q, knew, vnew
 
 
-@pytest.mark.parametrize("kind,kbits,vbits", [("rht", 3, 3), ("dense", 4, 4), ("rht", 2, 2)])
-def test_step_equals_separate_calls(kind, kbits, vbits):
+@pytest.mark.parametrize("kind,kbits,vbits,frac", [("rht", 3, 3, False), ("dense", 4, 4, False), ("rht", 2, 2, False),
+                                                    ("rht", 3, 3, True), ("dense", 4, 4, True)])
+def test_step_equals_separate_calls(kind, kbits, vbits, frac):
+    """frac: fractional-rate caches (second channel group at bits - 1)."""
     bsz, hkv, hq, cap = 3, 2, 8, 1008
-    k, v, rot, qjl, caches, q, knew, vnew = _setup(bsz, hkv, hq, cap, kind, kbits, vbits, seed=40 + kbits)
+    b2 = dict(kbits2=kbits - 1, vbits2=vbits - 1) if frac else {}
+    k, v, rot, qjl, caches, q, knew, vnew = _setup(bsz, hkv, hq, cap, kind, kbits, vbits, seed=40 + kbits, **b2)
     pos = torch.tensor([500, 1007, -1], dtype=torch.int32, device="cuda")  # the third batch row is not appended
     lens = torch.tensor([501, 1008, 700], dtype=torch.int32, device="cuda")
     outs = []
@@ -69,11 +72,13 @@ def test_step_equals_separate_calls(kind, kbits, vbits):
     assert torch.equal(out0, out1)
 
 
-def test_step_against_oracle():
+@pytest.mark.parametrize("kbits,vbits,kbits2,vbits2", [(3, 3, None, None), (3, 3, 2, 2), (4, 4, 3, 3)])
+def test_step_against_oracle(kbits, vbits, kbits2, vbits2):
     """The step's output equals the oracle's decode over the oracle-quantized
-    context plus the appended token."""
+    context plus the appended token; whole-width, 2.5-bit and 3.5-bit caches."""
     d, bsz, hkv, hq, cap, kind = 128, 2, 2, 8, 512, "rht"
-    k, v, rot, qjl, caches, q, knew, vnew = _setup(bsz, hkv, hq, cap, kind, 3, 3, seed=70)
+    k, v, rot, qjl, caches, q, knew, vnew = _setup(bsz, hkv, hq, cap, kind, kbits, vbits, seed=70,
+                                                   kbits2=kbits2 or 0, vbits2=vbits2 or 0)
     pos_np = np.array([300, 511], dtype=np.int32)
     pos = torch.from_numpy(pos_np).cuda()
     lens_np = pos_np + 1
@@ -91,8 +96,8 @@ def test_step_against_oracle():
         k2[b, :, pos_np[b]] = kn[b]
         v2[b, :, pos_np[b]] = vn[b]
     pi, s = P.oracle_mats(d, kind)
-    kq = oq.quantize(W.round_bf16(k2).reshape(-1, d).astype(np.float64), pi, "prod", 3, s)
-    vq = oq.quantize(W.round_bf16(v2).reshape(-1, d).astype(np.float64), pi, "mse", 3)
+    kq = oq.quantize(W.round_bf16(k2).reshape(-1, d).astype(np.float64), pi, "prod", kbits, s, bits2=kbits2)
+    vq = oq.quantize(W.round_bf16(v2).reshape(-1, d).astype(np.float64), pi, "mse", vbits, bits2=vbits2)
     sh = (bsz, hkv, cap)
     kcd = {"idx": kq["idx"].reshape(sh + (d,)), "norm16": kq["norm16"].reshape(sh),
            "rnorm16": kq["rnorm16"].reshape(sh), "z": kq["z"].reshape(sh + (d,))}
