@@ -103,3 +103,28 @@ def decode(q, kcache, vcache, seq_lens, pi, s_matrix, k_centroids, v_centroids,
             out[b, h] = a @ np.asarray(pi)
             logits[b][h] = l
     return out, logits
+
+
+def prefill(q, kcache, vcache, q_start, pi, s_matrix, k_centroids, v_centroids, scale=None, gqa_map=None):
+    """Chunked-prefill attention over a quantized cache (causal).
+
+    Readings (the write-ups give decode only; prefill is the other shape of
+    the same attention, over 32k-128k contexts): q [B, C, Hq, d] holds the
+    queries of C consecutive tokens of each sequence, the first at position
+    q_start[b]; the cache already holds those tokens' keys and values (the
+    chunk is quantized on append like every other token), and query i of
+    sequence b sees slots 0 .. q_start[b] + i (a causal mask), capped at the
+    cache's capacity. Each query is therefore one decode over its visible
+    prefix; this is written as exactly that.
+
+    Returns out [B, C, Hq, d].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    bsz, c, hq, d = q.shape
+    cap = kcache["idx"].shape[2]
+    out = np.zeros((bsz, c, hq, d))
+    for i in range(c):
+        lens = [min(max(int(q_start[b]) + i + 1, 0), cap) for b in range(bsz)]
+        out[:, i], _ = decode(q[:, i], kcache, vcache, lens, pi, s_matrix, k_centroids, v_centroids,
+                              scale=scale, gqa_map=gqa_map)
+    return out

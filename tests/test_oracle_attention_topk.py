@@ -108,3 +108,55 @@ def test_search_scores_match_logit_estimator_and_recall_improves_with_bits():
         ids, _ = topk.topk(sc, 10)
         rec[bits] = topk.recall_at_k(ids, truth)
     assert rec[4] > rec[2] > 0.3
+
+
+def _causal_attention(q, k, v, start):
+    """Textbook causal attention for a chunk of queries at positions start,
+    start+1, ...: softmax(Q K^T / sqrt(d) + M) V with M[i, t] = -inf for t > start + i."""
+    c, d = q.shape
+    s = q @ k.T / np.sqrt(d)
+    mask = np.arange(k.shape[0])[None, :] <= (start + np.arange(c))[:, None]
+    s = np.where(mask, s, -np.inf)
+    w = np.exp(s - s.max(axis=1, keepdims=True))
+    return (w / w.sum(axis=1, keepdims=True)) @ v
+
+
+def test_prefill_equals_causal_attention_on_reconstructions():
+    """prefill() = causal masked softmax attention (one matrix expression) over
+    the explicit reconstructions, chunk starting mid-sequence, GQA 2, whole
+    width and two-group caches."""
+    bsz, c, hq, hkv, t, d = 2, 5, 4, 2, 23, 32
+    pi = rotation.dense_rotation(1, d)
+    smat = rng.round_to_bf16(rng.normals(2, d * d).reshape(d, d))
+    r = np.random.default_rng(9)
+    k = r.standard_normal((bsz, hkv, t, d)) * 3
+    v = r.standard_normal((bsz, hkv, t, d))
+    q = r.standard_normal((bsz, c, hq, d))
+    start = np.array([11, 0])
+    for bits2 in (None, 2):
+        kq = quantize.quantize(k.reshape(-1, d), pi, "prod", 3, smat, bits2=bits2)
+        vq = quantize.quantize(v.reshape(-1, d), pi, "mse", 3, bits2=bits2)
+        sh = (bsz, hkv, t)
+        kc = {"idx": kq["idx"].reshape(sh + (d,)), "norm16": kq["norm16"].reshape(sh),
+              "rnorm16": kq["rnorm16"].reshape(sh), "z": kq["z"].reshape(sh + (d,))}
+        vc = {"idx": vq["idx"].reshape(sh + (d,)), "norm16": vq["norm16"].reshape(sh)}
+        out = attention.prefill(q, kc, vc, start, pi, smat, kq["centroids"], vq["centroids"])
+        kt = quantize.reconstruct(kq, pi, "prod", smat).reshape(bsz, hkv, t, d)
+        vt = quantize.reconstruct(vq, pi, "mse").reshape(bsz, hkv, t, d)
+        for b in range(bsz):
+            for h in range(hq):
+                kv = h // (hq // hkv)
+                want = _causal_attention(q[b, :, h], kt[b, kv], vt[b, kv], start[b])
+                assert np.max(np.abs(out[b, :, h] - want)) < 1e-10, (bits2, b, h)
+
+
+def test_prefill_of_one_token_is_decode():
+    b, hq, hkv, t, d = 2, 4, 2, 19, 32
+    pi = rotation.dense_rotation(1, d)
+    smat = rng.round_to_bf16(rng.normals(2, d * d).reshape(d, d))
+    kq, vq, kc, vc = _quantized_cache(b, hkv, t, d, 3, pi, smat, 4, 2)
+    q = np.random.default_rng(5).standard_normal((b, hq, d))
+    start = np.array([18, 6])
+    out = attention.prefill(q[:, None], kc, vc, start, pi, smat, kq["centroids"], vq["centroids"])
+    want, _ = attention.decode(q, kc, vc, start + 1, pi, smat, kq["centroids"], vq["centroids"])
+    assert np.array_equal(out[:, 0], want)
