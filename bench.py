@@ -594,6 +594,132 @@ def run_search(args, mode, bits):
     }
 
 
+PREFILL = {
+    # a 512-token chunk of a Llama-3.1-8B-shaped layer at the end of a 32768-token context
+    "llama8b_prefill_512_at_32k": dict(batch=1, chunk=512, hq=32, hkv=8, d=128, context=32768, rotation="rht",
+                                       k_bits=3, v_bits=3),
+}
+PREFILL_METRIC = "chunked-prefill tokens/s (causal attention of the chunk over the packed cache)"
+
+
+def prefill_oracle_sample(w, budget_s=3.0):
+    """The oracle's time per query row of the prefill workload (one KV head's
+    prefix quantized untimed, then rows at the chunk's last token timed until
+    the budget is spent)."""
+    from oracle import attention as oa
+    from oracle import quantize as oq
+    from online_kv_cache_quantize_gb300 import workloads as W
+
+    d, n = w["d"], w["context"]
+    from oracle import rng as orng, rotation as orot
+
+    pi = orot.make_rotation(W.ROT_SEED, d, w["rotation"])
+    s = orng.round_to_bf16(orng.normals(W.QJL_SEED, d * d).reshape(d, d))
+    k, v = W.decode_kv(1, 1, n)
+    kq = oq.quantize(k[0, 0].astype(np.float64), pi, "prod", w["k_bits"], s)
+    vq = oq.quantize(v[0, 0].astype(np.float64), pi, "mse", w["v_bits"])
+    q = W.query_vectors((8, d), dtype="bf16").astype(np.float64)
+    rows, t0 = 0, time.perf_counter()
+    while rows < 8 and (rows == 0 or time.perf_counter() - t0 < budget_s):
+        qp, u = oa.query_prep(q[rows], pi, s)
+        lg = oa.key_logits(qp, u, kq["idx"], kq["norm16"], kq["centroids"], kq["rnorm16"], kq["z"], d)
+        sc = lg / np.sqrt(d)
+        p = np.exp(sc - sc.max())
+        p /= p.sum()
+        (p @ (vq["norm16"][:, None] * oq.coord_centroids(vq["centroids"], vq["idx"]))) @ pi
+        rows += 1
+    return (time.perf_counter() - t0) / rows, rows
+
+
+def run_prefill(args, name):
+    import torch
+    from online_kv_cache_quantize_gb300 import binding as B
+    from online_kv_cache_quantize_gb300 import build as bld
+    from online_kv_cache_quantize_gb300 import workloads as W
+
+    torch.cuda.set_device(0)
+    bld.build()
+    w = dict(name=name, **PREFILL[name])
+    bsz, C, hq, hkv, d, T = w["batch"], w["chunk"], w["hq"], w["hkv"], w["d"], w["context"]
+    rot = B.tq_rotation_to_device(B.tq_make_rotation(W.ROT_SEED, d, w["rotation"]))
+    qjl = B.tq_qjl_to_device(B.tq_make_qjl(W.QJL_SEED, d, d))
+    k, v = W.decode_kv(bsz, hkv, T)
+    kc = B.Cache("prod", w["k_bits"], d, rows=bsz * hkv, capacity=T)
+    vc = B.Cache("mse", w["v_bits"], d, rows=bsz * hkv, capacity=T)
+    B.tq_quantize_kv(kc, rot, torch.from_numpy(k.reshape(-1, d)).cuda().to(torch.bfloat16), qjl=qjl)
+    B.tq_quantize_kv(vc, rot, torch.from_numpy(v.reshape(-1, d)).cuda().to(torch.bfloat16))
+    del k, v
+    qh = torch.from_numpy(W.query_vectors((bsz, C, hq, d), dtype="bf16")).to(torch.bfloat16)
+    q = qh.cuda()
+    qs = torch.full((bsz,), T - C, dtype=torch.int32, device="cuda")
+    out = torch.empty((bsz, C, hq, d), dtype=torch.bfloat16, device="cuda")
+    wsb = B.workspace(B.tq_attn_prefill_workspace(q, kc, vc, qs, T, rot, qjl, out))
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        B.tq_attn_prefill(q, kc, vc, qs, T, rot, qjl, out, wsb)
+
+    sampler = ClockSampler(0)
+    sampler.start()
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        step()
+    torch.cuda.synchronize()
+    K = max(1, min(args.steps, 20))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    # end to end: the chunk's queries from pinned host memory in, the output out
+    qpin = qh.pin_memory()
+    opin = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(3)]
+    for i in range(3):
+        flush.fill_(i & 0xFF)
+        eev[i][0].record(stream)
+        q.copy_(qpin, non_blocking=True)
+        step()
+        opin.copy_(out, non_blocking=True)
+        eev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    step_s = statistics.mean(a.elapsed_time(b) for a, b in ev) / 1e3
+    e2e_s = statistics.mean(a.elapsed_time(b) for a, b in eev) / 1e3
+    # per visible (query row, key token) pair: <q', c> (2d), the sign term (2m),
+    # the value accumulation (2d)
+    pairs = bsz * hq * sum(T - C + i + 1 for i in range(C))
+    flops = pairs * 2.0 * (d + d + d)
+    peak, peak_kind = _peaks("bf16_tflops")
+    achieved = flops / step_s / 1e12
+    res = {
+        "metric": PREFILL_METRIC, "value": bsz * C / step_s, "unit": "tokens/s", "n_gpus": 1, "steps": K,
+        "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16 (hi/lo splits), f32 accumulate", "data": "synthetic",
+        "config": {"workload": name, "batch": bsz, "chunk": C, "hq": hq, "hkv": hkv, "d": d, "context": T,
+                   "q_start": T - C, "rotation": w["rotation"], "k_bits": w["k_bits"], "v_bits": w["v_bits"],
+                   "l2": "flushed (256 MiB write) before every timed step"},
+        "roofline": {"kernel": "prefill_mma_kernel (mma.sync)", "bound": "tensor", "achieved": achieved,
+                     "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_kind,
+                     "alg_flops_per_step": flops, "traffic": None},
+        "e2e": {"value": bsz * C / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": qpin.numel() * 2,
+                "d2h_bytes_per_step": opin.numel() * 2, "steps": 3},
+        "gpu_launches": 3 * K,  # query prep, scan, merge
+        "clocks": clocks,
+        "cpu_baseline": None,
+    }
+    if not (args.no_cpu_baseline or args.quick):
+        t_row, rows = prefill_oracle_sample(w)
+        res["cpu_baseline"] = {"value": 1.0 / (t_row * hq), "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+                               "kind": "oracle",
+                               "sample": f"{rows} query rows at the chunk's last token over the {T}-token prefix "
+                                         f"of one KV head (prefix quantized untimed); a chunk token is {hq} rows"}
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -610,6 +736,8 @@ def main():
                     help="time the 1e6 x 200 inner-product top-10 search instead of the decode step")
     ap.add_argument("--search-rows", type=int, default=None, help="database rows (smaller case for profiling)")
     ap.add_argument("--search-queries", type=int, default=None, help="queries (smaller case for profiling)")
+    ap.add_argument("--prefill", choices=sorted(PREFILL), default=None,
+                    help="time chunked-prefill attention instead of the decode step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -628,6 +756,14 @@ def main():
                               "its oracle parity is in tests/test_gpu_topk.py"}))
             return
         print(json.dumps(run_search(args, args.search[:-1], int(args.search[-1]))), flush=True)
+        return
+    if args.prefill:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the prefill line has no reference arm here; "
+                              "its oracle parity is in tests/test_gpu_prefill.py and its cpu_baseline times the "
+                              "oracle"}))
+            return
+        print(json.dumps(run_prefill(args, args.prefill)), flush=True)
         return
     if args.impl == "reference":
         res = run_reference(args)

@@ -306,6 +306,43 @@ size_t tq_decode_step_workspace(const tq_step_args* a);
 tq_status tq_decode_step(const tq_step_args* a, void* workspace, size_t ws_bytes, tq_stream stream);
 
 /* ------------------------------------------------------------------------ *
+ * Chunked-prefill attention from the packed cache.                         *
+ * ------------------------------------------------------------------------ *
+ * The decode attention above for a chunk of C consecutive tokens of each
+ * sequence at once (the 32k-128k+ context windows of [A2A] "The KV cache
+ * bottleneck in modern LLMs"): query i of sequence b is the token at position
+ * q_start[b] + i and sees the cache slots 0 .. q_start[b] + i (causal; capped
+ * at min(capacity, max_context)); the chunk's own keys and values must have
+ * been quantized into the cache before the call (tq_quantize_kv), like every
+ * other token. Query head h reads KV head h / (hq / hkv). The logits, softmax
+ * and value sum are decode's; the write-ups give decode only, so the causal
+ * chunk is this library's reading. A query with no visible slot gives 0.
+ * Kernels: query prep (q' and u), the tensor-core scan (64 query rows per CTA
+ * against 16-token tiles, split over the tokens), and the decode merge. */
+typedef struct {
+    const void* q;          /* device [batch][chunk][hq][d] of q_dtype         */
+    int q_dtype;            /* TQ_F32 or TQ_BF16                              */
+    int batch, chunk, hq, hkv, d;  /* d = 128; hq / hkv in {1, 2, 4, 8}       */
+    const int32_t* q_start; /* device int32 [batch]: position of the chunk's
+                               first token in each sequence                   */
+    int max_context;        /* host: upper bound of q_start[b] + chunk (the
+                               split plan); <= capacity                       */
+    const tq_rotation* rot; /* uploaded                                       */
+    const tq_qjl* qjl;      /* uploaded, m == k.m                             */
+    tq_cache k;             /* PROD cache, rows == batch*hkv, m = 128         */
+    tq_cache v;             /* MSE cache, rows == batch*hkv                   */
+    float scale;            /* softmax scale; 0 -> 1/sqrt(d)                  */
+    int n_splits;           /* token splits; 0 -> automatic                   */
+    void* out;              /* device [batch][chunk][hq][d] of out_dtype       */
+    int out_dtype;          /* TQ_F32 or TQ_BF16                              */
+} tq_prefill_args;
+
+/* Workspace bytes of tq_attn_prefill (0 on invalid arguments); the workspace
+ * must be 256-byte aligned. */
+size_t tq_attn_prefill_workspace(const tq_prefill_args* a);
+tq_status tq_attn_prefill(const tq_prefill_args* a, void* workspace, size_t ws_bytes, tq_stream stream);
+
+/* ------------------------------------------------------------------------ *
  * Inner-product search from the codes.                                     *
  * ------------------------------------------------------------------------ *
  * [A2A] "Benchmarks and real-world performance" (GloVe d = 200 top-k recall)

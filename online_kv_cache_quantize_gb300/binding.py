@@ -60,6 +60,15 @@ class tq_step_args(ctypes.Structure):
                 ("new_dtype", ctypes.c_int), ("append_pos", ctypes.c_void_p)]
 
 
+class tq_prefill_args(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("q_dtype", ctypes.c_int),
+                ("batch", ctypes.c_int), ("chunk", ctypes.c_int), ("hq", ctypes.c_int), ("hkv", ctypes.c_int),
+                ("d", ctypes.c_int), ("q_start", ctypes.c_void_p), ("max_context", ctypes.c_int),
+                ("rot", ctypes.c_void_p), ("qjl", ctypes.c_void_p), ("k", tq_cache), ("v", tq_cache),
+                ("scale", ctypes.c_float), ("n_splits", ctypes.c_int), ("out", ctypes.c_void_p),
+                ("out_dtype", ctypes.c_int)]
+
+
 class tq_topk_args(ctypes.Structure):
     _fields_ = [("queries", ctypes.c_void_p), ("nq", ctypes.c_int), ("d", ctypes.c_int),
                 ("rot", ctypes.c_void_p), ("qjl", ctypes.c_void_p), ("db", tq_cache),
@@ -89,6 +98,8 @@ _SIGS = {
     "tq_quantize_kv": (_STATUS, [ctypes.POINTER(tq_quant_args), ctypes.c_void_p]),
     "tq_attn_decode_workspace": (ctypes.c_size_t, [ctypes.POINTER(tq_decode_args)]),
     "tq_attn_decode": (_STATUS, [ctypes.POINTER(tq_decode_args), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "tq_attn_prefill_workspace": (ctypes.c_size_t, [ctypes.POINTER(tq_prefill_args)]),
+    "tq_attn_prefill": (_STATUS, [ctypes.POINTER(tq_prefill_args), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "tq_attn_decode_static": (_STATUS, [ctypes.POINTER(tq_decode_args), ctypes.c_void_p]),
     "tq_score_topk_workspace": (ctypes.c_size_t, [ctypes.POINTER(tq_topk_args)]),
     "tq_score_topk": (_STATUS, [ctypes.POINTER(tq_topk_args), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
@@ -124,7 +135,7 @@ def load():
         fn.argtypes = args
     for name, cls in (("tq_cache", tq_cache), ("tq_quant_args", tq_quant_args),
                       ("tq_decode_args", tq_decode_args), ("tq_topk_args", tq_topk_args),
-                      ("tq_step_args", tq_step_args)):
+                      ("tq_step_args", tq_step_args), ("tq_prefill_args", tq_prefill_args)):
         if lib.tq_abi_struct_size(name.encode()) != ctypes.sizeof(cls):
             raise RuntimeError(f"struct {name} layout differs between libtq.so and the binding")
     _lib = lib
@@ -331,6 +342,39 @@ def tq_attn_decode(q, kcache, vcache, seq_lens, max_seq_len, rot, qjl, out, work
     a, _keep = _decode_struct(q, kcache, vcache, seq_lens, max_seq_len, rot, qjl, out, **kw)
     _check(load().tq_attn_decode(ctypes.byref(a), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                  _stream_ptr(stream)), "tq_attn_decode")
+
+
+def _prefill_struct(q, kcache, vcache, q_start, max_context, rot, qjl, out, scale=0.0, n_splits=0):
+    b, c, hq, d = q.shape
+    a = tq_prefill_args()
+    a.q = q.data_ptr()
+    a.q_dtype = _dtype_code(q)
+    a.batch, a.chunk, a.hq, a.hkv, a.d = b, c, hq, kcache.rows // b, d
+    a.q_start = q_start.data_ptr()
+    a.max_context = max_context
+    a.rot = rot.handle
+    a.qjl = qjl.handle
+    a.k = kcache.struct()
+    a.v = vcache.struct()
+    a.scale = scale
+    a.n_splits = n_splits
+    a.out = out.data_ptr()
+    a.out_dtype = _dtype_code(out)
+    return a
+
+
+def tq_attn_prefill_workspace(q, kcache, vcache, q_start, max_context, rot, qjl, out, **kw):
+    a = _prefill_struct(q, kcache, vcache, q_start, max_context, rot, qjl, out, **kw)
+    return load().tq_attn_prefill_workspace(ctypes.byref(a))
+
+
+def tq_attn_prefill(q, kcache, vcache, q_start, max_context, rot, qjl, out, workspace, stream=None, **kw):
+    """Chunked-prefill attention: q [batch][chunk][hq][d], the chunk of each
+    sequence starting at position q_start[b] (device int32) and already
+    quantized into the caches; writes out [batch][chunk][hq][d]."""
+    a = _prefill_struct(q, kcache, vcache, q_start, max_context, rot, qjl, out, **kw)
+    _check(load().tq_attn_prefill(ctypes.byref(a), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                  _stream_ptr(stream)), "tq_attn_prefill")
 
 
 def tq_attn_decode_static(q, kcache, vcache, seq_lens, max_seq_len, rot, qjl, out, stream=None, **kw):

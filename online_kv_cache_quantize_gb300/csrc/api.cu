@@ -188,6 +188,33 @@ void pair_table_lo(const std::vector<double>& c, int bits, double lam, uint32_t*
     for (int x = 0; x < n * n; ++x) out[x] = lo(x & (n - 1)) | (lo(x >> bits) << 16);
 }
 
+// The tensor-core scans' centroid tables (decode and prefill): pair tables of
+// lam * c for the key codes (with the lo residual table) and the value codes,
+// and of the second channel group when the caches are fractional-rate.
+template <typename P>
+tq_status scan_tables(int d, int kb, int kb2, int vb, int vb2, P* p) {
+    const bool two = kb2 != kb;
+    std::vector<double> kc, vc, kc2, vc2, t;
+    tq_status s;
+    if ((s = tq::codebook(d, kb, kc, t)) != TQ_OK) return s;
+    if ((s = tq::codebook(d, vb, vc, t)) != TQ_OK) return s;
+    if (two && (s = tq::codebook(d, kb2, kc2, t)) != TQ_OK) return s;
+    if (two && (s = tq::codebook(d, vb2, vc2, t)) != TQ_OK) return s;
+    const double lam_k = pick_lambda(d, 16 * kb + kb2, positive_centroids(kc, two ? &kc2 : nullptr));
+    const double lam_v = pick_lambda(d, 16 * vb + vb2, positive_centroids(vc, two ? &vc2 : nullptr));
+    pair_table(kc, kb, lam_k, p->klut);
+    pair_table_lo(kc, kb, lam_k, p->klut_lo);
+    pair_table(vc, vb, lam_v, p->vlut);
+    if (two) {
+        pair_table(kc2, kb2, lam_k, p->klut2);
+        pair_table_lo(kc2, kb2, lam_k, p->klut2_lo);
+        pair_table(vc2, vb2, lam_v, p->vlut2);
+    }
+    p->inv_lam_k = (float)(1.0 / lam_k);
+    p->inv_lam_v = (float)(1.0 / lam_v);
+    return TQ_OK;
+}
+
 struct DecodePlan {
     int n_splits = 1, chunk = 1, group = 1;
     size_t off_frag = 0, off_part = 0, total = 0;
@@ -464,11 +491,9 @@ tq_status decode_prepare(const tq_decode_args* a, void* workspace, size_t ws_byt
     pp.frag = frag;
     pp.qjl_scale = (float)(std::sqrt(M_PI / 2.0) / a->k.m);
 
-    std::vector<double> kc, kt, vc, vt, kc2, vc2;
+    std::vector<double> kc, kt, vc, vt;
     if ((s = tq::codebook(a->d, kb, kc, kt)) != TQ_OK) return s;
     if ((s = tq::codebook(a->d, vb, vc, vt)) != TQ_OK) return s;
-    if (two && (s = tq::codebook(a->d, kb2, kc2, kt)) != TQ_OK) return s;
-    if (two && (s = tq::codebook(a->d, vb2, vc2, vt)) != TQ_OK) return s;
     dp.frag = frag;
     dp.batch = a->batch;
     dp.hq = a->hq;
@@ -489,18 +514,7 @@ tq_status decode_prepare(const tq_decode_args* a, void* workspace, size_t ws_byt
     dp.vnorm = a->v.norm;
     for (size_t i = 0; i < kc.size(); ++i) dp.kc[i] = (float)kc[i];
     for (size_t i = 0; i < vc.size(); ++i) dp.vc[i] = (float)vc[i];
-    const double lam_k = pick_lambda(a->d, 16 * kb + kb2, positive_centroids(kc, two ? &kc2 : nullptr));
-    const double lam_v = pick_lambda(a->d, 16 * vb + vb2, positive_centroids(vc, two ? &vc2 : nullptr));
-    pair_table(kc, kb, lam_k, dp.klut);
-    pair_table_lo(kc, kb, lam_k, dp.klut_lo);
-    pair_table(vc, vb, lam_v, dp.vlut);
-    if (two) {
-        pair_table(kc2, kb2, lam_k, dp.klut2);
-        pair_table_lo(kc2, kb2, lam_k, dp.klut2_lo);
-        pair_table(vc2, vb2, lam_v, dp.vlut2);
-    }
-    dp.inv_lam_k = (float)(1.0 / lam_k);
-    dp.inv_lam_v = (float)(1.0 / lam_v);
+    if ((s = scan_tables(a->d, kb, kb2, vb, vb2, &dp)) != TQ_OK) return s;
     dp.qjl_scale = (float)(std::sqrt(M_PI / 2.0) / a->k.m);
     const double scale = a->scale != 0.0f ? (double)a->scale : 1.0 / std::sqrt((double)a->d);
     dp.scale_log2 = (float)(scale * 1.4426950408889634);
@@ -831,6 +845,155 @@ tq_status tq_decode_step(const tq_step_args* a, void* workspace, size_t ws_bytes
     if (!ev) step_append(LV, &sp);
     D.dp.append_pos = a->append_pos;
     return decode_launch(D, (cudaStream_t)stream, &sp);
+}
+
+}  // extern "C"
+
+namespace {
+
+struct PrefillPlan {
+    int group = 0, n_splits = 0, split_tokens = 0, lim_cap = 0;
+    size_t off_u = 0, off_part = 0, total = 0;
+};
+
+tq_status plan_prefill(const tq_prefill_args* a, PrefillPlan* pl) {
+    if (!a) return fail(TQ_ERR_INVALID_ARG, "tq_attn_prefill: args are NULL");
+    if (a->batch < 1 || a->chunk < 0 || a->hq < 1 || a->hkv < 1)
+        return fail(TQ_ERR_INVALID_ARG, "tq_attn_prefill: batch/hq/hkv must be >= 1 and chunk >= 0");
+    if (a->d != 128) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: d must be 128");
+    if (a->hq % a->hkv) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: hq must be a multiple of hkv");
+    const int g = a->hq / a->hkv;
+    if (g != 1 && g != 2 && g != 4 && g != 8) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: hq / hkv must be 1, 2, 4 or 8");
+    if (a->max_context < 0) return fail(TQ_ERR_INVALID_ARG, "tq_attn_prefill: max_context < 0");
+    if (a->max_context > a->k.capacity) return fail(TQ_ERR_CAPACITY, "tq_attn_prefill: max_context exceeds the capacity");
+    const int64_t rows = (int64_t)a->batch * a->chunk * a->hq;
+    if (rows > (1ll << 31) / 128) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: too many query rows");
+    const int64_t qbs = ((int64_t)a->chunk * g + tqk::kPfRows - 1) / tqk::kPfRows;
+    if (qbs > 0x7fffffff || (int64_t)a->batch * a->hkv > 65535)
+        return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: grid too large");
+    pl->group = g;
+    pl->lim_cap = a->max_context;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int ctx = std::max(a->max_context, 1);
+    long long want = a->n_splits;
+    if (want <= 0) {  // about four CTAs per SM (two resident)
+        const long long base = std::max<long long>(1, qbs * a->batch * a->hkv);
+        want = ((long long)sms * 4 + base - 1) / base;
+    }
+    if (want > 65535) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: too many splits");
+    int st = (int)((ctx + want - 1) / want);
+    st = std::max(64, (st + 63) / 64 * 64);
+    pl->split_tokens = st;
+    pl->n_splits = (ctx + st - 1) / st;
+    const size_t r = (size_t)rows;
+    pl->off_u = round_up(r * 128 * sizeof(float), 256);
+    pl->off_part = pl->off_u + round_up(r * 128 * sizeof(float), 256);
+    pl->total = std::max<size_t>(256, pl->off_part + round_up(r * (size_t)pl->n_splits * (128 + tqk::kPartPad) * sizeof(float), 256));
+    return TQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t tq_attn_prefill_workspace(const tq_prefill_args* a) {
+    PrefillPlan pl;
+    if (plan_prefill(a, &pl) != TQ_OK) return 0;
+    return pl.total;
+}
+
+tq_status tq_attn_prefill(const tq_prefill_args* a, void* workspace, size_t ws_bytes, tq_stream stream) {
+    PrefillPlan pl;
+    tq_status s = plan_prefill(a, &pl);
+    if (s != TQ_OK) return s;
+    int kb = 0, vb = 0, kb2 = 0, vb2 = 0;
+    if ((s = check_cache(a->k, "tq_attn_prefill k", &kb, &kb2)) != TQ_OK) return s;
+    if ((s = check_cache(a->v, "tq_attn_prefill v", &vb, &vb2)) != TQ_OK) return s;
+    const bool two = kb2 != kb;
+    if ((vb2 != vb) != two)
+        return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: keys and values must both be fractional-rate caches, or neither");
+    if (a->k.mode != TQ_PROD || a->v.mode != TQ_MSE) return fail(TQ_ERR_INVALID_ARG, "tq_attn_prefill: keys must be PROD and values MSE");
+    if (a->k.d != a->d || a->v.d != a->d) return fail(TQ_ERR_INVALID_ARG, "tq_attn_prefill: cache d does not match");
+    if (a->k.m != 128) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: m must be 128");
+    const int64_t kvrows = (int64_t)a->batch * a->hkv;
+    if (a->k.rows != kvrows || a->v.rows != kvrows) return fail(TQ_ERR_INVALID_ARG, "tq_attn_prefill: cache rows must be batch*hkv");
+    if (a->k.capacity != a->v.capacity) return fail(TQ_ERR_INVALID_ARG, "tq_attn_prefill: k and v capacity differ");
+    if (a->k.capacity % 16) return fail(TQ_ERR_ALIGNMENT, "tq_attn_prefill: cache capacity must be a multiple of 16");
+    if (!aligned(a->k.norm, 16) || !aligned(a->k.rnorm, 16) || !aligned(a->v.norm, 16) || !aligned(a->v.codes, 16))
+        return fail(TQ_ERR_ALIGNMENT, "tq_attn_prefill: every cache plane must be 16-byte aligned (bulk copies)");
+    if ((s = check_rot(a->rot, a->d)) != TQ_OK) return s;
+    if ((s = check_qjl(a->qjl, a->k.m, a->d)) != TQ_OK) return s;
+    if (a->chunk == 0) return TQ_OK;
+    if (!a->q || !a->out || !a->q_start) return fail(TQ_ERR_INVALID_ARG, "tq_attn_prefill: q/out/q_start is NULL");
+    if (a->q_dtype != TQ_F32 && a->q_dtype != TQ_BF16) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: q_dtype must be F32 or BF16");
+    if (a->out_dtype != TQ_F32 && a->out_dtype != TQ_BF16) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: out_dtype must be F32 or BF16");
+    if (!workspace || ws_bytes < pl.total) return fail(TQ_ERR_WORKSPACE, "tq_attn_prefill: workspace missing or too small");
+    if (!aligned(workspace, 256)) return fail(TQ_ERR_ALIGNMENT, "tq_attn_prefill: workspace must be 256-byte aligned");
+
+    char* ws = (char*)workspace;
+    const int64_t rows = (int64_t)a->batch * a->chunk * a->hq;
+    tqk::PrepParams pp;
+    std::memset(&pp, 0, sizeof(pp));
+    pp.q = a->q;
+    pp.q_dtype = a->q_dtype == TQ_BF16 ? 1 : 0;
+    pp.rows = rows;
+    pp.d = a->d;
+    pp.m = a->k.m;
+    pp.pit32 = a->rot->d_pit32;
+    pp.sgn = a->rot->d_sign;
+    pp.rht = a->rot->kind == TQ_ROT_RHT;
+    pp.inv_sqrt_d = (float)(1.0 / std::sqrt((double)a->d));
+    pp.st32 = a->qjl->d_st32;
+    pp.qprime = (float*)ws;
+    pp.u = (float*)(ws + pl.off_u);
+
+    tqk::PrefillParams fp;
+    std::memset(&fp, 0, sizeof(fp));
+    fp.qprime = pp.qprime;
+    fp.u = pp.u;
+    fp.batch = a->batch;
+    fp.chunk = a->chunk;
+    fp.hq = a->hq;
+    fp.hkv = a->hkv;
+    fp.group = pl.group;
+    fp.q_start = a->q_start;
+    fp.lim_cap = pl.lim_cap;
+    fp.capacity = a->k.capacity;
+    fp.kcodes = a->k.codes;
+    fp.ksigns = a->k.signs;
+    fp.knorm = a->k.norm;
+    fp.krnorm = a->k.rnorm;
+    fp.vcodes = a->v.codes;
+    fp.vnorm = a->v.norm;
+    if ((s = scan_tables(a->d, kb, kb2, vb, vb2, &fp)) != TQ_OK) return s;
+    fp.qjl_scale = (float)(std::sqrt(M_PI / 2.0) / a->k.m);
+    const double scale = a->scale != 0.0f ? (double)a->scale : 1.0 / std::sqrt((double)a->d);
+    fp.scale_log2 = (float)(scale * 1.4426950408889634);
+    fp.n_splits = pl.n_splits;
+    fp.split_tokens = pl.split_tokens;
+    fp.partial = (float*)(ws + pl.off_part);
+    cudaError_t e = tqk::device_error_word(&fp.err);
+    if (e != cudaSuccess) return cuda_status(e, "tq_attn_prefill error word");
+
+    tqk::CombineParams cp;
+    std::memset(&cp, 0, sizeof(cp));
+    cp.partial = fp.partial;
+    cp.rows = (int)rows;
+    cp.d = a->d;
+    cp.n_splits = pl.n_splits;
+    cp.pi32 = a->rot->d_pi32;
+    cp.sgn = a->rot->d_sign;
+    cp.rht = a->rot->kind == TQ_ROT_RHT;
+    cp.inv_sqrt_d = (float)(1.0 / std::sqrt((double)a->d));
+    cp.out = a->out;
+    cp.out_dtype = a->out_dtype == TQ_BF16 ? 1 : 0;
+
+    cudaStream_t st = (cudaStream_t)stream;
+    if ((e = tqk::launch_query_prep(pp, st)) != cudaSuccess) return cuda_status(e, "tq_attn_prefill query prep");
+    if ((e = tqk::launch_prefill_mma(fp, kb, vb, two, st)) != cudaSuccess) return cuda_status(e, "tq_attn_prefill scan");
+    return cuda_status(tqk::launch_combine(cp, st), "tq_attn_prefill merge");
 }
 
 tq_status tq_device_errors(uint32_t* flags_out, int reset) {

@@ -304,6 +304,7 @@ size_t tq_abi_struct_size(const char* name) {
     if (!std::strcmp(name, "tq_decode_args")) return sizeof(tq_decode_args);
     if (!std::strcmp(name, "tq_topk_args")) return sizeof(tq_topk_args);
     if (!std::strcmp(name, "tq_step_args")) return sizeof(tq_step_args);
+    if (!std::strcmp(name, "tq_prefill_args")) return sizeof(tq_prefill_args);
     return 0;
 }
 

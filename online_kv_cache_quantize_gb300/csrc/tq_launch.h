@@ -143,6 +143,40 @@ struct DecodeParams {
 // kbits - 1 and vbits / vbits - 1)
 cudaError_t launch_decode_mma(const DecodeParams& p, int kbits, int vbits, bool two, cudaStream_t s);
 
+// Chunked prefill: C query tokens x G heads per KV head against the cache,
+// causal (query i sees slots 0 .. q_start[b] + i). kPfRows query rows per CTA.
+constexpr int kPfRows = 64;
+struct PrefillParams {
+    const float* qprime;  // [rows][128] q' = Pi q, rows = (b * chunk + i) * hq + h
+    const float* u;       // [rows][128] u = S q'
+    int batch, chunk, hq, hkv, group;
+    const int32_t* q_start;  // [batch] position of the chunk's first token
+    int lim_cap;          // visible slots are capped at min(capacity, max_context)
+    int64_t capacity;
+    const uint8_t* kcodes;
+    const uint8_t* ksigns;
+    const uint16_t* knorm;
+    const uint16_t* krnorm;
+    const uint8_t* vcodes;
+    const uint16_t* vnorm;
+    uint32_t klut[256];
+    uint32_t klut_lo[256];
+    uint32_t vlut[256];
+    uint32_t klut2[64];
+    uint32_t klut2_lo[64];
+    uint32_t vlut2[64];
+    float inv_lam_k, inv_lam_v;
+    float qjl_scale;      // sqrt(pi/2)/m
+    float scale_log2;     // softmax scale * log2(e)
+    int n_splits;
+    int split_tokens;     // tokens per split (a multiple of 64)
+    float* partial;       // [rows][n_splits][128 + kPartPad]: a, then M and Z
+    uint32_t* err;
+};
+
+// two: keys and values are both fractional-rate caches
+cudaError_t launch_prefill_mma(const PrefillParams& p, int kbits, int vbits, bool two, cudaStream_t s);
+
 // The library's device error word of the current device (bits kErr* of
 // pipeline.cuh), and a kernel that waits on an mbarrier that nothing
 // arrives on for at most limit_ns, so that the bounded wait runs out.

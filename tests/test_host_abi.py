@@ -92,3 +92,5 @@ def test_argument_errors_are_reported(lib):
     assert L.tq_attn_decode(None, None, 0, None) == 1
     assert L.tq_score_topk(None, None, 0, None) == 1
     assert L.tq_attn_decode_workspace(None) == 0
+    assert L.tq_attn_prefill(None, None, 0, None) == 1
+    assert L.tq_attn_prefill_workspace(None) == 0
