@@ -738,6 +738,7 @@ def main():
     ap.add_argument("--search-queries", type=int, default=None, help="queries (smaller case for profiling)")
     ap.add_argument("--prefill", choices=sorted(PREFILL), default=None,
                     help="time chunked-prefill attention instead of the decode step")
+    ap.add_argument("--prefill-context", type=int, default=None, help="context length (smaller case for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -763,6 +764,8 @@ def main():
                               "its oracle parity is in tests/test_gpu_prefill.py and its cpu_baseline times the "
                               "oracle"}))
             return
+        if args.prefill_context:
+            PREFILL[args.prefill]["context"] = args.prefill_context
         print(json.dumps(run_prefill(args, args.prefill)), flush=True)
         return
     if args.impl == "reference":
