@@ -409,12 +409,13 @@ tq_status quant_prepare(const tq_quant_args* a, QuantLaunch* L, bool* empty) {
     p.s_frag = prod ? a->qjl->d_s_frag : nullptr;
     // d = 128 (keys m = 128): up to kSmallAppend vectors the CTA-per-vector
     // kernel, more the tensor-core kernel (16-byte aligned rows); otherwise
-    // the warp-per-vector kernel (any d <= 256)
-    // (a two-width cache always takes the CTA-per-vector kernel)
-    L->small = c.d == 128 && (!prod || c.m == 128) && (a->n <= kSmallAppend || p.code_bits2 != 0);
+    // the warp-per-vector kernel (any d <= 256). A two-width cache takes the
+    // CTA-per-vector kernel where the tensor-core one does not apply.
     if (p.code_bits2 && prod && c.m != 128) return fail(TQ_ERR_UNSUPPORTED, "tq_quantize_kv: a fractional-rate key cache needs m = 128");
-    L->mma = c.d == 128 && !L->small && (!prod || (c.m == 128 && p.s_frag)) && (rht || p.pi_frag) &&
-             aligned(a->x, 16) && (a->x_stride * (int64_t)esz) % 16 == 0;
+    const bool mma_ok = c.d == 128 && (!prod || (c.m == 128 && p.s_frag)) && (rht || p.pi_frag) &&
+                        aligned(a->x, 16) && (a->x_stride * (int64_t)esz) % 16 == 0;
+    L->small = c.d == 128 && (!prod || c.m == 128) && (a->n <= kSmallAppend || (p.code_bits2 != 0 && !mma_ok));
+    L->mma = !L->small && mma_ok;
     return TQ_OK;
 }
 
@@ -425,6 +426,8 @@ cudaError_t quant_launch(const QuantLaunch& L, cudaStream_t st) {
         step_append(L, &sp);
         return tqk::launch_step_prep(sp, st);
     }
+    if (L.mma && L.p.code_bits2)
+        return tqk::launch_quantize_mma2(L.p, L.dtype, L.rht ? 1 : 0, L.prod ? 1 : 0, L.cb, st);
     if (L.mma) return tqk::launch_quantize_mma(L.p, L.dtype, L.rht ? 1 : 0, L.prod ? 1 : 0, L.cb, st);
     if (L.rht) return tqk::launch_quantize_rht(L.p, L.dtype, L.vpl, L.prod ? 1 : 0, L.cb, st);
     return tqk::launch_quantize_dense(L.p, L.dtype, L.vpl, L.prod ? 1 : 0, L.cb, st);

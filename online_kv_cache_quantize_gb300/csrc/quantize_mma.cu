@@ -5,23 +5,7 @@ namespace tqk {
 
 template <typename XT, int CB, bool PROD, bool RHT>
 static cudaError_t go(const QuantParams& p, cudaStream_t s) {
-    if (p.n <= 0) return cudaSuccess;
-    auto kern = quantize_mma_kernel<XT, CB, PROD, RHT>;
-    constexpr int NW = qm_warps<XT, RHT>();
-    constexpr size_t smem = quantize_mma_smem<XT, CB, PROD, RHT>();
-    static_assert(smem + kMaxLevels * sizeof(float) <= kQmSmemLimit, "shared memory above the per-CTA limit");
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NW * 32, smem);
-    if (per_sm < 1) per_sm = 1;
-    const int64_t tiles = (p.n + 15) / 16;
-    int64_t blocks = (tiles + NW - 1) / NW;
-    if (blocks > (int64_t)sms * per_sm) blocks = (int64_t)sms * per_sm;
-    kern<<<(unsigned)blocks, NW * 32, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_quantize_mma_t<XT, CB, PROD, RHT>(p, s);
 }
 
 template <typename XT, bool PROD, bool RHT>

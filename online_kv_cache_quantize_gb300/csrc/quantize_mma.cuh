@@ -94,11 +94,40 @@ struct QmSmem {
     static constexpr int WARP_BYTES = 2 * QmStage<XT>::BYTES;  // double-buffered staging
 };
 
-template <typename XT, int CB, bool PROD, bool RHT>
+// Cell of one coordinate against a symmetric codebook of CBX bits (the
+// positive boundaries only, see below): returns the code, sets dmin (the
+// distance of |y| to the nearest boundary) and, for keys, cpos = the centroid
+// magnitude of the cell.
+template <int CBX, bool PROD>
+__device__ __forceinline__ int qm_cell(const Codebook& cbk, float yv, float& dmin, float& cpos) {
+    constexpr int LX = 1 << CBX, HX = LX / 2;
+    const float av = fabsf(yv);
+    int k = 0;
+    dmin = av;
+    cpos = cbk.c[HX];
+#pragma unroll
+    for (int t = HX; t < LX - 1; ++t) {
+        const bool ge = av >= cbk.t[t];
+        k += ge ? 1 : 0;
+        if (PROD) cpos = ge ? cbk.c[t + 1] : cpos;
+        dmin = fminf(dmin, fabsf(av - cbk.t[t]));
+    }
+    return yv >= 0.0f ? HX + k : HX - 1 - k;
+}
+
+// bit offset of coordinate j (0..31) in a thread's run of codes: CB bits each,
+// or (fractional rates, CB2 != CB) CB bits when j % 16 < 8 and CB2 otherwise
+template <int CB, int CB2>
+__device__ __forceinline__ constexpr int qm_bit(int j) {
+    return CB2 == CB ? CB * j
+                     : (j >> 4) * 8 * (CB + CB2) + ((j & 15) < 8 ? (j & 7) * CB : 8 * CB + (j & 7) * CB2);
+}
+
+template <typename XT, int CB, bool PROD, bool RHT, int CB2 = CB>
 __global__ void __launch_bounds__(kQmWarps * 32, 3) quantize_mma_kernel(const __grid_constant__ QuantParams p) {
     constexpr int D = 128;
     constexpr int L = 1 << CB;
-    constexpr int H = L / 2;
+    constexpr bool TWO = CB2 != CB;  // two channel groups (fractional rate)
     constexpr int NLX = (!RHT && sizeof(XT) == 4) ? 3 : 1;  // limbs of X for the dense GEMM
     constexpr int NW = qm_warps<XT, RHT>();
     using S = QmSmem<XT>;
@@ -109,6 +138,7 @@ __global__ void __launch_bounds__(kQmWarps * 32, 3) quantize_mma_kernel(const __
     const uint2* b1 = reinterpret_cast<const uint2*>(smem);
     const uint2* b2 = reinterpret_cast<const uint2*>(smem + B1_BYTES);
     __shared__ float s_cent[kMaxLevels];
+    __shared__ float s_cent2[TWO ? kMaxLevels : 1];
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
@@ -136,6 +166,8 @@ __global__ void __launch_bounds__(kQmWarps * 32, 3) quantize_mma_kernel(const __
         }
     }
     if (threadIdx.x < kMaxLevels) s_cent[threadIdx.x] = p.cb.c[threadIdx.x];
+    if constexpr (TWO)
+        if (threadIdx.x < kMaxLevels) s_cent2[threadIdx.x] = p.cb2.c[threadIdx.x];
     bool frag_ready = FRAG_BYTES == 0, failed = false;
     // warp-uniform: true once the fragments are in shared memory
     auto frags = [&]() -> bool {
@@ -374,24 +406,15 @@ __global__ void __launch_bounds__(kQmWarps * 32, 3) quantize_mma_kernel(const __
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const float yv = y[rr][j];
-                const float av = fabsf(yv);
-                int k = 0;
-                float dmin = av;
-                float cpos = p.cb.c[H];
-#pragma unroll
-                for (int t = H; t < L - 1; ++t) {
-                    const bool ge = av >= p.cb.t[t];
-                    k += ge ? 1 : 0;
-                    if (PROD) cpos = ge ? p.cb.c[t + 1] : cpos;
-                    dmin = fminf(dmin, fabsf(av - p.cb.t[t]));
-                }
-                const bool pos = yv >= 0.0f;
-                const int idx = pos ? H + k : H - 1 - k;
+                const bool sec = TWO && (j & 15) >= 8;  // second channel group
+                const int w = sec ? CB2 : CB;
+                float dmin, cpos;
+                const int idx = sec ? qm_cell<CB2, PROD>(p.cb2, yv, dmin, cpos) : qm_cell<CB, PROD>(p.cb, yv, dmin, cpos);
                 if (!(dmin >= p.guard)) flag[rr] |= 1u << j;
-                if (PROD) y[rr][j] = pos ? yv - cpos : yv + cpos;
-                const int bit = CB * j;
+                if (PROD) y[rr][j] = yv >= 0.0f ? yv - cpos : yv + cpos;
+                const int bit = qm_bit<CB, CB2>(j);
                 idxw[rr][bit >> 5] |= (uint32_t)idx << (bit & 31);
-                if ((bit & 31) + CB > 32) idxw[rr][(bit >> 5) + 1] |= (uint32_t)idx >> (32 - (bit & 31));
+                if ((bit & 31) + w > 32) idxw[rr][(bit >> 5) + 1] |= (uint32_t)idx >> (32 - (bit & 31));
             }
         }
         if (v0 + g >= p.n) flag[0] = 0u;
@@ -454,10 +477,16 @@ __global__ void __launch_bounds__(kQmWarps * 32, 3) quantize_mma_kernel(const __
                 double y64 = 0.0;
                 if (nrow > 0.0) y64 = RHT ? part / (sqrt((double)D) * nrow) : part / nrow;
                 if (lane == src) {
+                    const bool sec = TWO && (j_src & 15) >= 8;
                     int k = 0;
+                    if (sec) {
 #pragma unroll
-                    for (int t = 0; t < L - 1; ++t) k += (y64 >= p.cb.t64[t]) ? 1 : 0;
-                    const float nv = PROD ? (float)y64 - s_cent[k] : (float)y64;
+                        for (int t = 0; t < (1 << CB2) - 1; ++t) k += (y64 >= p.cb2.t64[t]) ? 1 : 0;
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < L - 1; ++t) k += (y64 >= p.cb.t64[t]) ? 1 : 0;
+                    }
+                    const float nv = PROD ? (float)y64 - (sec ? s_cent2[k] : s_cent[k]) : (float)y64;
 #pragma unroll
                     for (int rr = 0; rr < 2; ++rr) {
                         if (rr != rr_src) continue;
@@ -465,12 +494,13 @@ __global__ void __launch_bounds__(kQmWarps * 32, 3) quantize_mma_kernel(const __
                         for (int j = 0; j < 32; ++j) {
                             if (j != j_src) continue;
                             y[rr][j] = nv;
-                            const int bit = CB * j;
-                            const uint32_t m0 = ((1u << CB) - 1u) << (bit & 31);
+                            const int w = (TWO && (j & 15) >= 8) ? CB2 : CB;
+                            const int bit = qm_bit<CB, CB2>(j);
+                            const uint32_t m0 = ((1u << w) - 1u) << (bit & 31);
                             idxw[rr][bit >> 5] = (idxw[rr][bit >> 5] & ~m0) | ((uint32_t)k << (bit & 31));
-                            if ((bit & 31) + CB > 32) {
+                            if ((bit & 31) + w > 32) {
                                 const int sh = 32 - (bit & 31);
-                                const uint32_t m1 = ((1u << CB) - 1u) >> sh;
+                                const uint32_t m1 = ((1u << w) - 1u) >> sh;
                                 idxw[rr][(bit >> 5) + 1] = (idxw[rr][(bit >> 5) + 1] & ~m1) | ((uint32_t)k >> sh);
                             }
                         }
@@ -503,6 +533,15 @@ __global__ void __launch_bounds__(kQmWarps * 32, 3) quantize_mma_kernel(const __
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
             if (slot[rr] < 0) continue;
+            if constexpr (TWO) {
+                // this thread's 16 (CB + CB2) bits are CB + CB2 half-words from
+                // half-word c (CB + CB2) of the slot (half-word aligned for odd c)
+                uint16_t* d16 = reinterpret_cast<uint16_t*>(p.codes + slot[rr] * (int64_t)p.code_stride) + c * (CB + CB2);
+#pragma unroll
+                for (int h = 0; h < CB + CB2; ++h) d16[h] = (uint16_t)(idxw[rr][h >> 1] >> (16 * (h & 1)));
+                if (c == 0) p.norm[slot[rr]] = n16[rr];
+                continue;
+            }
             uint32_t* dst = reinterpret_cast<uint32_t*>(p.codes + slot[rr] * (int64_t)p.code_stride) + CB * c;
             if constexpr (CB == 2) {
                 *reinterpret_cast<uint2*>(dst) = make_uint2(idxw[rr][0], idxw[rr][1]);
@@ -595,6 +634,29 @@ template <typename XT, int CB, bool PROD, bool RHT>
 constexpr size_t quantize_mma_smem() {
     return (RHT ? 0 : 3 * 8 * 16 * 32 * 8) + (PROD ? 8 * 16 * 32 * 8 : 0) +
            (size_t)qm_warps<XT, RHT>() * QmSmem<XT>::WARP_BYTES;
+}
+
+// One launch: a persistent grid of at most (SMs x resident CTAs) CTAs, each
+// warp taking tiles of 16 vectors.
+template <typename XT, int CB, bool PROD, bool RHT, int CB2 = CB>
+cudaError_t launch_quantize_mma_t(const QuantParams& p, cudaStream_t s) {
+    if (p.n <= 0) return cudaSuccess;
+    auto kern = quantize_mma_kernel<XT, CB, PROD, RHT, CB2>;
+    constexpr int NW = qm_warps<XT, RHT>();
+    constexpr size_t smem = quantize_mma_smem<XT, CB, PROD, RHT>();
+    static_assert(smem + 2 * kMaxLevels * sizeof(float) <= kQmSmemLimit, "shared memory above the per-CTA limit");
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NW * 32, smem);
+    if (per_sm < 1) per_sm = 1;
+    const int64_t tiles = (p.n + 15) / 16;
+    int64_t blocks = (tiles + NW - 1) / NW;
+    if (blocks > (int64_t)sms * per_sm) blocks = (int64_t)sms * per_sm;
+    kern<<<(unsigned)blocks, NW * 32, smem, s>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace tqk

@@ -52,6 +52,9 @@ struct QuantParams {
 
 // tensor-core quantize for d = m = 128 (x 16-byte aligned rows)
 cudaError_t launch_quantize_mma(const QuantParams& p, int dtype, int rht, int prod, int code_bits, cudaStream_t s);
+// fractional-rate caches: code_bits for the coordinates with i % 16 < 8,
+// p.code_bits2 = code_bits - 1 for the others
+cudaError_t launch_quantize_mma2(const QuantParams& p, int dtype, int rht, int prod, int code_bits, cudaStream_t s);
 
 // dtype: 0 f32, 1 bf16, 2 f16. rht: 0 dense, 1 RHT. prod: 0 MSE, 1 PROD.
 cudaError_t launch_quantize(const QuantParams& p, int dtype, int rht, int prod, int code_bits,

@@ -171,14 +171,25 @@ def test_full_size_prefill_sampled():
 
 
 @pytest.mark.parametrize("kind", ["rht", "dense"])
-@pytest.mark.parametrize("mode,bits", [("prod", 3), ("prod", 4), ("mse", 3), ("mse", 4)])
+@pytest.mark.parametrize("mode,bits", [("prod", 3), ("prod", 4), ("prod", 5), ("mse", 2), ("mse", 3), ("mse", 4)])
 def test_two_width_caches(kind, mode, bits):
     """Fractional rates (2.5 / 3.5 bits per channel): coordinates with
     i % 16 < 8 at `bits`, the rest at `bits - 1`, each group with its own
-    codebook, codes packed in coordinate order with an 8-byte stride."""
+    codebook, codes packed in coordinate order with an 8-byte stride. 1400
+    vectors: the tensor-core kernel."""
     k, v = W.decode_kv(1, 2, 700, heavy_frac=0.01)
     x = (k if mode == "prod" else v).reshape(-1, 128)
     _run(x, mode, bits, 128, kind, torch.bfloat16, f"{kind}-{mode}{bits}/{bits - 1}", bits2=bits - 1)
+
+
+@pytest.mark.parametrize("n,dtype", [(200, torch.bfloat16), (1000, torch.float32), (4133, torch.bfloat16)])
+def test_two_width_sizes_and_dtypes(n, dtype):
+    """Two-width caches through the CTA-per-vector kernel (200 vectors), fp32
+    input on the dense rotation, and a ragged multi-CTA size."""
+    x = np.random.default_rng(n).standard_normal((n, 128)).astype(np.float32) * 2
+    kind = "dense" if dtype == torch.float32 else "rht"
+    _run(x, "prod", 4, 128, kind, dtype, f"two-width n={n}", bits2=3)
+    _run(x, "mse", 3, 128, kind, dtype, f"two-width n={n}", bits2=2)
 
 
 def test_two_width_rejections():
