@@ -471,10 +471,12 @@ def workspace(nbytes, device="cuda"):
 
 
 class QuantizedKVCache:
-    """One attention layer's packed KV cache with the decode loop's two calls:
-    `prefill` quantizes a context into it and `step` appends one token per
-    batch row and attends (the write-ups' "quantize on every cache update,
-    then attend"; tq_quantize_kv and tq_decode_step). Keys are PROD (k_bits,
+    """One attention layer's packed KV cache with the decode loop's calls:
+    `prefill` quantizes a context into it, `prefill_chunk` appends a chunk of
+    tokens per batch row and attends with the chunk's queries (causal), and
+    `step` appends one token per batch row and attends (the write-ups'
+    "quantize on every cache update, then attend"; tq_quantize_kv,
+    tq_attn_prefill and tq_decode_step). Keys are PROD (k_bits,
     QJL signs), values MSE (v_bits); both share one rotation. The per-row
     lengths live on the device; this class only keeps the handles, the
     planes and a workspace, and forms the calls' arguments."""
@@ -491,6 +493,7 @@ class QuantizedKVCache:
         self.k = Cache("prod", k_bits, d, rows=batch * hkv, capacity=capacity, device=device, bits2=k_bits2)
         self.v = Cache("mse", v_bits, d, rows=batch * hkv, capacity=capacity, device=device, bits2=v_bits2)
         self.lengths = torch.zeros(batch, dtype=torch.int32, device=device)
+        self._host_lengths = [0] * batch  # the same lengths, for the launch plans
         self._ws = None
 
     def prefill(self, k, v, lengths):
@@ -513,6 +516,41 @@ class QuantizedKVCache:
         tq_quantize_kv(self.k, self.rot, k.reshape(-1, d), qjl=self.qjl, dst_slot=slots)
         tq_quantize_kv(self.v, self.rot, v.reshape(-1, d), dst_slot=slots)
         self.lengths.copy_(torch.tensor(lens, dtype=torch.int32))
+        self._host_lengths = lens
+
+    def prefill_chunk(self, q, k, v, out=None, stream=None):
+        """Appends a chunk of C tokens to every batch row (k, v: device
+        [batch, hkv, C, d]) at the row's current length, then attends with the
+        chunk's queries (device [batch, C, hq, d]; query i sees the row's
+        tokens up to and including chunk token i). Returns out
+        ([batch, C, hq, d], fp32 unless given)."""
+        import torch
+
+        b, h, c, d = k.shape
+        if (b, h, d) != (self.batch, self.hkv, self.d) or tuple(v.shape) != tuple(k.shape):
+            raise ValueError("k and v must be [batch, hkv, C, d]")
+        if tuple(q.shape) != (b, c, self.hq, d):
+            raise ValueError("q must be [batch, C, hq, d]")
+        max_context = max(self._host_lengths) + c
+        if max_context > self.capacity:
+            raise ValueError("the chunk does not fit the capacity")
+        if out is None:
+            out = torch.empty((b, c, self.hq, d), dtype=torch.float32, device=q.device)
+        # slot of chunk token j of (b, h): (b * hkv + h) * capacity + lengths[b] + j
+        j = torch.arange(c, device=k.device, dtype=torch.int64)
+        rows = torch.arange(b * h, device=k.device, dtype=torch.int64)
+        start = self.lengths.to(torch.int64).repeat_interleave(h)
+        slots = (rows[:, None] * self.capacity + start[:, None] + j[None, :]).reshape(-1).contiguous()
+        tq_quantize_kv(self.k, self.rot, k.reshape(-1, d), qjl=self.qjl, dst_slot=slots, stream=stream)
+        tq_quantize_kv(self.v, self.rot, v.reshape(-1, d), dst_slot=slots, stream=stream)
+        need = tq_attn_prefill_workspace(q, self.k, self.v, self.lengths, max_context, self.rot, self.qjl, out)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = workspace(need, device=q.device)
+        tq_attn_prefill(q, self.k, self.v, self.lengths, max_context, self.rot, self.qjl, out, self._ws,
+                        stream=stream)
+        self.lengths = self.lengths + c
+        self._host_lengths = [x + c for x in self._host_lengths]
+        return out
 
     def step(self, q, k_new, v_new, out=None, stream=None):
         """Appends k_new / v_new (device [batch, hkv, d]) at each row's current
@@ -533,4 +571,5 @@ class QuantizedKVCache:
         tq_decode_step(q, self.k, self.v, new_lens, self.capacity, self.rot, self.qjl, out, kn, vn, self.lengths,
                        self._ws, stream=stream)
         self.lengths = new_lens
+        self._host_lengths = [x + 1 for x in self._host_lengths]
         return out

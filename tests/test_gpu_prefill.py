@@ -187,3 +187,45 @@ def test_prefill_llama8b_chunk_end_of_32k_sampled():
             p /= p.sum()
             want = (p @ (vq["norm16"][:n, None] * vq["centroids"][vq["idx"][:n]])) @ pi
             assert np.max(np.abs(out[0, i, h] - want)) <= OUT_TOL * scale, (kv, i, j)
+
+
+def test_quantized_kv_cache_prefill_chunk_then_step():
+    """QuantizedKVCache: prefill 200 / 150 tokens, append a 48-token chunk and
+    attend with its queries (against the oracle's causal prefill of the
+    combined context), then one decode step continues from the new lengths."""
+    d, bsz, hkv, hq, cap, C = 128, 2, 2, 8, 256, 48
+    cache = B.QuantizedKVCache(bsz, hq, hkv, cap, k_bits=3, v_bits=3, rotation="rht", rot_seed=W.ROT_SEED,
+                               qjl_seed=W.QJL_SEED)
+    k, v = W.decode_kv(bsz, hkv, cap, seed=21)
+    lens = [200, 150]
+    cache.prefill(torch.from_numpy(k[:, :, :200]).cuda(), torch.from_numpy(v[:, :, :200]).cuda(), lens)
+    # the chunk's keys and values go to slots lens[b] .. lens[b] + C - 1 of each row
+    kc_np = np.stack([k[b, :, lens[b]:lens[b] + C] for b in range(bsz)])
+    vc_np = np.stack([v[b, :, lens[b]:lens[b] + C] for b in range(bsz)])
+    q = W.query_vectors((bsz, C, hq, d), seed=22)
+    out = cache.prefill_chunk(torch.from_numpy(q).cuda(), torch.from_numpy(kc_np).cuda(),
+                              torch.from_numpy(vc_np).cuda())
+    torch.cuda.synchronize()
+    pi, s = P.oracle_mats(d, "rht")
+    # the oracle's cache: every row's first lens[b] + C tokens are the ones written
+    kq = oq.quantize(k.reshape(-1, d).astype(np.float64), pi, "prod", 3, s)
+    vq = oq.quantize(v.reshape(-1, d).astype(np.float64), pi, "mse", 3)
+    sh = (bsz, hkv, cap)
+    kcd = {"idx": kq["idx"].reshape(sh + (d,)), "norm16": kq["norm16"].reshape(sh),
+           "rnorm16": kq["rnorm16"].reshape(sh), "z": kq["z"].reshape(sh + (d,))}
+    vcd = {"idx": vq["idx"].reshape(sh + (d,)), "norm16": vq["norm16"].reshape(sh)}
+    want = oa.prefill(q.astype(np.float64), kcd, vcd, lens, pi, s, kq["centroids"], vq["centroids"])
+    scale = np.max(vq["norm16"]) / np.sqrt(d)
+    assert np.max(np.abs(out.cpu().numpy() - want)) <= OUT_TOL * scale
+    assert cache.lengths.cpu().tolist() == [lens[0] + C, lens[1] + C]
+    # one decode step at the new lengths equals tq_attn_decode over the same cache
+    kn = torch.from_numpy(W.round_bf16(W.query_vectors((bsz, hkv, d), seed=23))).cuda()
+    vn = torch.from_numpy(W.round_bf16(W.query_vectors((bsz, hkv, d), seed=24))).cuda()
+    qd = torch.from_numpy(W.query_vectors((bsz, hq, d), seed=25)).cuda()
+    o1 = cache.step(qd, kn, vn).clone()
+    new_lens = torch.tensor([lens[0] + C + 1, lens[1] + C + 1], dtype=torch.int32, device="cuda")
+    o2 = torch.empty_like(o1)
+    ws = B.workspace(B.tq_attn_decode_workspace(qd, cache.k, cache.v, new_lens, cap, cache.rot, cache.qjl, o2))
+    B.tq_attn_decode(qd, cache.k, cache.v, new_lens, cap, cache.rot, cache.qjl, o2, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
