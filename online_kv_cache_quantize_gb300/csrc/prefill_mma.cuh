@@ -33,9 +33,19 @@
 // merged and un-rotated by the decode merge kernel.
 #pragma once
 
+#include <type_traits>
+
 #include "decode_mma.cuh"
 
 namespace tqk {
+
+// 8 * field(w, off, n): the byte offset of an 8-byte table entry
+__device__ __forceinline__ uint32_t field8(const uint32_t* w, int off, int n) {
+    const int W = off >> 5, S = off & 31;
+    const uint32_t mask = ((1u << n) - 1u) << 3;
+    if (S + n <= 32) return (S >= 3 ? (w[W] >> (S - 3)) : (w[W] << (3 - S))) & mask;
+    return (__funnelshift_r(w[W], w[W + 1], S) << 3) & mask;
+}
 
 constexpr int kPfWarps = 4;
 constexpr int kPfStages = 4;
@@ -56,11 +66,13 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_mma_kernel(const __g
     // A fragments of the CTA's query rows: [warp][kk][part][lane], part 0 / 1 =
     // hi / lo of q', 2 / 3 = hi / lo of kappa u (four registers each)
     uint4* qf = reinterpret_cast<uint4*>(smem + kPfStages * SB);
-    __shared__ uint32_t klut[KL];
-    __shared__ uint32_t klo[KLO ? KL : 1];
+    // key pair tables: 4-byte entries, or for 3-4 bit codes 8-byte entries
+    // holding the fp16 pair and its lo residual pair
+    __shared__ uint32_t klut[KLO ? 1 : KL];
+    __shared__ __align__(8) uint2 klut8[KLO ? KL : 1];
     __shared__ uint32_t vlut[VL];
-    __shared__ uint32_t klut2[KL2];
-    __shared__ uint32_t klo2[(KLO && K2) ? KL2 : 1];
+    __shared__ uint32_t klut2[(K2 && !KLO) ? KL2 : 1];
+    __shared__ __align__(8) uint2 klut8_2[(K2 && KLO) ? KL2 : 1];
     __shared__ uint32_t vlut2[VL2];
     __shared__ __align__(8) uint2 slut4[16];
     __shared__ __align__(8) uint64_t s_bar[kPfStages];
@@ -72,14 +84,16 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_mma_kernel(const __g
     const int b = blockIdx.z / p.hkv, kv = blockIdx.z % p.hkv;
     const int G = p.group;
 
-    for (int i = threadIdx.x; i < KL; i += blockDim.x) klut[i] = p.klut[i];
-    if constexpr (KLO)
-        for (int i = threadIdx.x; i < KL; i += blockDim.x) klo[i] = p.klut_lo[i];
+    for (int i = threadIdx.x; i < KL; i += blockDim.x) {
+        if constexpr (KLO) klut8[i] = make_uint2(p.klut[i], p.klut_lo[i]);
+        else klut[i] = p.klut[i];
+    }
     for (int i = threadIdx.x; i < VL; i += blockDim.x) vlut[i] = p.vlut[i];
     if constexpr (K2) {
-        for (int i = threadIdx.x; i < KL2; i += blockDim.x) klut2[i] = p.klut2[i];
-        if constexpr (KLO)
-            for (int i = threadIdx.x; i < KL2; i += blockDim.x) klo2[i] = p.klut2_lo[i];
+        for (int i = threadIdx.x; i < KL2; i += blockDim.x) {
+            if constexpr (KLO) klut8_2[i] = make_uint2(p.klut2[i], p.klut2_lo[i]);
+            else klut2[i] = p.klut2[i];
+        }
     }
     if constexpr (V2)
         for (int i = threadIdx.x; i < VL2; i += blockDim.x) vlut2[i] = p.vlut2[i];
@@ -187,167 +201,162 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_mma_kernel(const __g
     const float inv_lk = p.inv_lam_k, inv_lv = p.inv_lam_v;
     const uint4* wq = qf + warp * 8 * 4 * 32 + lane;
 
-    int gi = 0;
-    for (; gi < ngroups; ++gi) {
-        const bool landed = mbar_wait_bounded(bar0 + 8 * (gi % kPfStages), (gi / kPfStages) & 1, kWaitLimitNs,
-                                              p.err, kErrScanWait);
-        if (!__all_sync(TQ_FULL_MASK, landed)) break;
-        const unsigned char* st = stages + (gi % kPfStages) * SB;
-        const int ntg = min(kPfWarps, ntiles - kPfWarps * gi);
-        for (int tt = 0; tt < ntg; ++tt) {
-            const int tok0 = t0 + 16 * (kPfWarps * gi + tt);
-            if (tok0 >= wlim) break;
-            const unsigned char* p_kc = st + kPfWarps * T::OFF_KC + tt * T::KC;
-            const unsigned char* p_sg = st + kPfWarps * T::OFF_SG + tt * T::SG;
-            const uint32_t* p_kn = reinterpret_cast<const uint32_t*>(st + kPfWarps * T::OFF_KN + tt * T::NB);
-            const uint32_t* p_kr = reinterpret_cast<const uint32_t*>(st + kPfWarps * T::OFF_KR + tt * T::NB);
-            const unsigned char* p_vc = st + kPfWarps * T::OFF_VC + tt * T::VC;
-            const uint32_t* p_vn = reinterpret_cast<const uint32_t*>(st + kPfWarps * T::OFF_VN + tt * T::NB);
+    // One step over NS consecutive 16-token tiles of a stage (two, or one at
+    // the end of a split): S for 8 NS tokens per A-fragment load, then the
+    // online softmax, then O += P V one 16-token tile at a time.
+    auto step = [&](auto ns_tag, const unsigned char* st, int tt, int tok0) {
+        constexpr int NS = decltype(ns_tag)::value;
+        constexpr int NT = 2 * NS;  // key n-tiles of 8 tokens; this thread's B column is token 8 nt + g
+        const unsigned char* p_kc = st + kPfWarps * T::OFF_KC + tt * T::KC;
+        const unsigned char* p_sg = st + kPfWarps * T::OFF_SG + tt * T::SG;
+        const uint32_t* p_kn = reinterpret_cast<const uint32_t*>(st + kPfWarps * T::OFF_KN + tt * T::NB);
+        const uint32_t* p_kr = reinterpret_cast<const uint32_t*>(st + kPfWarps * T::OFF_KR + tt * T::NB);
+        const unsigned char* p_vc = st + kPfWarps * T::OFF_VC + tt * T::VC;
+        const uint32_t* p_vn = reinterpret_cast<const uint32_t*>(st + kPfWarps * T::OFF_VN + tt * T::NB);
 
-            // ---- S: n-tile 0 = tokens 0..7 (this thread's B column: token g),
-            // n-tile 1 = tokens 8..15 (token g + 8) ----
-            constexpr int KWN = (KB + KB2 + 1) / 2;
-            uint32_t kw0[KWN + 1], kw1[KWN + 1];
-            if constexpr (!K2) {
-                const uint32_t* r0 = reinterpret_cast<const uint32_t*>(p_kc + g * T::KS) + KB * c;
-                const uint32_t* r1 = reinterpret_cast<const uint32_t*>(p_kc + (g + 8) * T::KS) + KB * c;
+        // ---- S = Q K^T (+ the sign term) ----
+        constexpr int KWN = (KB + KB2 + 1) / 2;
+        uint32_t kw[NT][KWN + 1], sw[NT];
 #pragma unroll
-                for (int w = 0; w < KB; ++w) {
-                    kw0[w] = r0[w];
-                    kw1[w] = r1[w];
-                }
+        for (int nt = 0; nt < NT; ++nt) {
+            const int tok = 8 * nt + g;
+            if constexpr (!K2) {
+                const uint32_t* r = reinterpret_cast<const uint32_t*>(p_kc + tok * T::KS) + KB * c;
+#pragma unroll
+                for (int w = 0; w < KB; ++w) kw[nt][w] = r[w];
             } else {
+                // an odd KB + KB2 starts odd c's run half way into a word
                 constexpr int TW = T::KS / 4;
                 const int wb = (c * (KB + KB2)) >> 1, sh = ((c * (KB + KB2)) & 1) * 16;
-                const uint32_t* r0 = reinterpret_cast<const uint32_t*>(p_kc + g * T::KS) + wb;
-                const uint32_t* r1 = reinterpret_cast<const uint32_t*>(p_kc + (g + 8) * T::KS) + wb;
-                uint32_t x0[KWN + 1], x1[KWN + 1];
+                const uint32_t* r = reinterpret_cast<const uint32_t*>(p_kc + tok * T::KS) + wb;
+                uint32_t x[KWN + 1];
 #pragma unroll
-                for (int w = 0; w <= KWN; ++w) {
-                    x0[w] = wb + w < TW ? r0[w] : 0u;
-                    x1[w] = wb + w < TW ? r1[w] : 0u;
-                }
+                for (int w = 0; w <= KWN; ++w) x[w] = wb + w < TW ? r[w] : 0u;
 #pragma unroll
-                for (int w = 0; w < KWN; ++w) {
-                    kw0[w] = __funnelshift_r(x0[w], x0[w + 1], sh);
-                    kw1[w] = __funnelshift_r(x1[w], x1[w + 1], sh);
+                for (int w = 0; w < KWN; ++w) kw[nt][w] = __funnelshift_r(x[w], x[w + 1], sh);
+            }
+            kw[nt][KWN] = 0u;
+            sw[nt] = reinterpret_cast<const uint32_t*>(p_sg + tok * 16)[c];
+        }
+        float sk[NT][4], ss[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) sk[nt][r] = ss[nt][r] = 0.0f;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint4 qh = wq[(kk * 4 + 0) * 32], ql = wq[(kk * 4 + 1) * 32];
+            const uint4 uh = wq[(kk * 4 + 2) * 32], ul = wq[(kk * 4 + 3) * 32];
+            const bool first = !K2 || (kk & 3) < 2;
+            const int kw_ = first ? KB : KB2, ko = key_off<KB, KB2>(kk);
+            uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                if constexpr (KLO) {  // one 8-byte entry: (hi pair, lo pair)
+                    const uint2* t8 = first ? klut8 : klut8_2;
+                    const uint2 e0 = lds_at<uint2>(t8, field8(kw[nt], ko, 2 * kw_));
+                    const uint2 e1 = lds_at<uint2>(t8, field8(kw[nt], ko + 2 * kw_, 2 * kw_));
+                    bh[nt][0] = e0.x; bl[nt][0] = e0.y;
+                    bh[nt][1] = e1.x; bl[nt][1] = e1.y;
+                } else {
+                    const uint32_t* tab = first ? klut : klut2;
+                    bh[nt][0] = lds_at<uint32_t>(tab, field4(kw[nt], ko, 2 * kw_));
+                    bh[nt][1] = lds_at<uint32_t>(tab, field4(kw[nt], ko + 2 * kw_, 2 * kw_));
                 }
             }
-            kw0[KWN] = 0u;
-            kw1[KWN] = 0u;
-            const uint32_t sw0 = reinterpret_cast<const uint32_t*>(p_sg + g * 16)[c];
-            const uint32_t sw1 = reinterpret_cast<const uint32_t*>(p_sg + (g + 8) * 16)[c];
-            float sk[2][2][4], ss[2][2][4];  // [kk parity][n-tile][reg]
 #pragma unroll
-            for (int e = 0; e < 2; ++e)
+            for (int nt = 0; nt < NT; ++nt) mma16816(sk[nt], qh.x, qh.y, qh.z, qh.w, bh[nt][0], bh[nt][1]);
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
+            for (int nt = 0; nt < NT; ++nt) mma16816(sk[nt], ql.x, ql.y, ql.z, ql.w, bh[nt][0], bh[nt][1]);
+            if constexpr (KLO) {
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) sk[e][nt][r] = ss[e][nt][r] = 0.0f;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint4 qh = wq[(kk * 4 + 0) * 32], ql = wq[(kk * 4 + 1) * 32];
-                const uint4 uh = wq[(kk * 4 + 2) * 32], ul = wq[(kk * 4 + 3) * 32];
-                const bool first = !K2 || (kk & 3) < 2;
-                const int kw = first ? KB : KB2, ko = key_off<KB, KB2>(kk);
-                const uint32_t* tab = first ? klut : klut2;
-                const uint32_t* tlo = first ? klo : klo2;
-                const uint32_t f0 = field4(kw0, ko, 2 * kw), f1 = field4(kw1, ko, 2 * kw);
-                const uint32_t f2 = field4(kw0, ko + 2 * kw, 2 * kw);
-                const uint32_t f3 = field4(kw1, ko + 2 * kw, 2 * kw);
-                const uint32_t b00 = lds_at<uint32_t>(tab, f0), b01 = lds_at<uint32_t>(tab, f2);
-                const uint32_t b10 = lds_at<uint32_t>(tab, f1), b11 = lds_at<uint32_t>(tab, f3);
-                const int e = kk & 1;
-                mma16816(sk[e][0], qh.x, qh.y, qh.z, qh.w, b00, b01);
-                mma16816(sk[e][1], qh.x, qh.y, qh.z, qh.w, b10, b11);
-                mma16816(sk[e][0], ql.x, ql.y, ql.z, ql.w, b00, b01);
-                mma16816(sk[e][1], ql.x, ql.y, ql.z, ql.w, b10, b11);
-                if constexpr (KLO) {
-                    const uint32_t l00 = lds_at<uint32_t>(tlo, f0), l01 = lds_at<uint32_t>(tlo, f2);
-                    const uint32_t l10 = lds_at<uint32_t>(tlo, f1), l11 = lds_at<uint32_t>(tlo, f3);
-                    mma16816(sk[e][0], qh.x, qh.y, qh.z, qh.w, l00, l01);
-                    mma16816(sk[e][1], qh.x, qh.y, qh.z, qh.w, l10, l11);
-                }
-                const uint2 sg0 = lds_at<uint2>(slut4, kk == 0 ? (sw0 << 3) & 0x78u : (sw0 >> (4 * kk - 3)) & 0x78u);
-                const uint2 sg1 = lds_at<uint2>(slut4, kk == 0 ? (sw1 << 3) & 0x78u : (sw1 >> (4 * kk - 3)) & 0x78u);
-                mma16816(ss[e][0], uh.x, uh.y, uh.z, uh.w, sg0.x, sg0.y);
-                mma16816(ss[e][1], uh.x, uh.y, uh.z, uh.w, sg1.x, sg1.y);
-                mma16816(ss[e][0], ul.x, ul.y, ul.z, ul.w, sg0.x, sg0.y);
-                mma16816(ss[e][1], ul.x, ul.y, ul.z, ul.w, sg1.x, sg1.y);
+                for (int nt = 0; nt < NT; ++nt) mma16816(sk[nt], qh.x, qh.y, qh.z, qh.w, bl[nt][0], bl[nt][1]);
             }
+            uint2 sg[NT];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                sg[nt] = lds_at<uint2>(slut4, kk == 0 ? (sw[nt] << 3) & 0x78u : (sw[nt] >> (4 * kk - 3)) & 0x78u);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma16816(ss[nt], uh.x, uh.y, uh.z, uh.w, sg[nt].x, sg[nt].y);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma16816(ss[nt], ul.x, ul.y, ul.z, ul.w, sg[nt].x, sg[nt].y);
+        }
 
-            // ---- logits and the online softmax: this thread's columns are tokens
-            // 2c, 2c + 1 (n-tile 0) and 8 + 2c, 9 + 2c (n-tile 1) ----
-            const uint32_t knw[2] = {p_kn[c], p_kn[4 + c]}, krw[2] = {p_kr[c], p_kr[4 + c]};
-            const uint32_t vnw[2] = {p_vn[c], p_vn[4 + c]};
-            float s[2][4];
-            float mt[2] = {-INFINITY, -INFINITY};
+        // ---- logits and the online softmax: this thread's columns of n-tile
+        // nt are tokens 8 nt + 2c and 8 nt + 2c + 1 ----
+        float s_[NT][4];
+        float mt[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < NT; ++nt) {
+            const uint32_t knw = p_kn[4 * nt + c], krw = p_kr[4 * nt + c];
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int hi = r & 1, row = r >> 1;
-                    const int tok = tok0 + 8 * nt + 2 * c + hi;
-                    const float kn = f16_bits_to_f32((uint16_t)(knw[nt] >> (16 * hi)));
-                    const float kg = f16_bits_to_f32((uint16_t)(krw[nt] >> (16 * hi)));
-                    const float kdot = sk[0][nt][r] + sk[1][nt][r];
-                    const float sdot = ss[0][nt][r] + ss[1][nt][r];
-                    const float l = kn * fmaf(kg, sdot, kdot * inv_lk);
-                    s[nt][r] = tok < lim[row] ? l * p.scale_log2 : -INFINITY;
-                    mt[row] = fmaxf(mt[row], s[nt][r]);
-                }
-            float corr[2];
-#pragma unroll
-            for (int row = 0; row < 2; ++row) {
-                float m = mt[row];
-                m = fmaxf(m, __shfl_xor_sync(TQ_FULL_MASK, m, 1));
-                m = fmaxf(m, __shfl_xor_sync(TQ_FULL_MASK, m, 2));
-                const float mn = fmaxf(M[row], m);
-                corr[row] = (mn == -INFINITY) ? 1.0f : ex2(M[row] - mn);
-                M[row] = mn;
+            for (int r = 0; r < 4; ++r) {
+                const int hi = r & 1, row = r >> 1;
+                const int tok = tok0 + 8 * nt + 2 * c + hi;
+                const float kn = f16_bits_to_f32((uint16_t)(knw >> (16 * hi)));
+                const float kg = f16_bits_to_f32((uint16_t)(krw >> (16 * hi)));
+                const float l = kn * fmaf(kg, ss[nt][r], sk[nt][r] * inv_lk);
+                s_[nt][r] = tok < lim[row] ? l * p.scale_log2 : -INFINITY;
+                mt[row] = fmaxf(mt[row], s_[nt][r]);
             }
-            float w[2][4];
-            float zs[2] = {0.0f, 0.0f};
+        }
+        float corr[2];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+        for (int row = 0; row < 2; ++row) {
+            float m = mt[row];
+            m = fmaxf(m, __shfl_xor_sync(TQ_FULL_MASK, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(TQ_FULL_MASK, m, 2));
+            const float mn = fmaxf(M[row], m);
+            corr[row] = (mn == -INFINITY) ? 1.0f : ex2(M[row] - mn);
+            M[row] = mn;
+        }
+        float zs[2] = {0.0f, 0.0f};
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int hi = r & 1, row = r >> 1;
-                    const float pr = (s[nt][r] == -INFINITY) ? 0.0f : ex2(s[nt][r] - M[row]);
-                    zs[row] += pr;
-                    w[nt][r] = pr * f16_bits_to_f32((uint16_t)(vnw[nt] >> (16 * hi)));
-                }
-            Zp[0] = fmaf(Zp[0], corr[0], zs[0]);
-            Zp[1] = fmaf(Zp[1], corr[1], zs[1]);
-            if (__any_sync(TQ_FULL_MASK, corr[0] != 1.0f || corr[1] != 1.0f)) {
+        for (int nt = 0; nt < NT; ++nt) {
+            const uint32_t vnw = p_vn[4 * nt + c];
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        O[j][h][0] *= corr[0];
-                        O[j][h][1] *= corr[0];
-                        O[j][h][2] *= corr[1];
-                        O[j][h][3] *= corr[1];
-                    }
+            for (int r = 0; r < 4; ++r) {
+                const int hi = r & 1, row = r >> 1;
+                const float pr = (s_[nt][r] == -INFINITY) ? 0.0f : ex2(s_[nt][r] - M[row]);
+                zs[row] += pr;
+                s_[nt][r] = pr * f16_bits_to_f32((uint16_t)(vnw >> (16 * hi)));  // now p * nV
             }
-            // A fragment of P V (tokens along K): registers 0..3 = (row g, tokens
-            // 2c, 2c+1), (row g+8, same), (row g, 8+2c, 9+2c), (row g+8, same)
+        }
+        Zp[0] = fmaf(Zp[0], corr[0], zs[0]);
+        Zp[1] = fmaf(Zp[1], corr[1], zs[1]);
+        if (__any_sync(TQ_FULL_MASK, corr[0] != 1.0f || corr[1] != 1.0f)) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    O[j][h][0] *= corr[0];
+                    O[j][h][1] *= corr[0];
+                    O[j][h][2] *= corr[1];
+                    O[j][h][3] *= corr[1];
+                }
+        }
+
+        // ---- O += P V, one 16-token tile at a time ----
+#pragma unroll
+        for (int t16 = 0; t16 < NS; ++t16) {
+            // A fragment (tokens along K): registers 0..3 = (row g, tokens 2c,
+            // 2c+1), (row g+8, same), (row g, 8+2c, 9+2c), (row g+8, same)
             uint32_t ph[4], pl[4];
 #pragma unroll
             for (int lo = 0; lo < 2; ++lo) {
                 uint32_t* dstp = lo ? pl : ph;
-                dstp[0] = split_half(w[0][0], lo) | (split_half(w[0][1], lo) << 16);
-                dstp[1] = split_half(w[0][2], lo) | (split_half(w[0][3], lo) << 16);
-                dstp[2] = split_half(w[1][0], lo) | (split_half(w[1][1], lo) << 16);
-                dstp[3] = split_half(w[1][2], lo) | (split_half(w[1][3], lo) << 16);
+                const float(&w0)[4] = s_[2 * t16];
+                const float(&w1)[4] = s_[2 * t16 + 1];
+                dstp[0] = split_half(w0[0], lo) | (split_half(w0[1], lo) << 16);
+                dstp[1] = split_half(w0[2], lo) | (split_half(w0[3], lo) << 16);
+                dstp[2] = split_half(w1[0], lo) | (split_half(w1[1], lo) << 16);
+                dstp[3] = split_half(w1[2], lo) | (split_half(w1[3], lo) << 16);
             }
-
-            // ---- O += P V: value codes of tokens 2c, 2c+1, 8+2c, 9+2c,
-            // coordinates 16g .. 16g+15 ----
+            // value codes of tokens 2c, 2c+1, 8+2c, 9+2c, coordinates 16g .. 16g+15
             uint32_t vf[4][3];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const int tok = 2 * c + (q & 1) + 8 * (q >> 1);
+                const int tok = 16 * t16 + 2 * c + (q & 1) + 8 * (q >> 1);
                 const uint32_t* vr = reinterpret_cast<const uint32_t*>(p_vc + tok * T::VS);
                 const int bit0 = 8 * (VB + VB2) * g;
                 const int wd = bit0 >> 5, sh = bit0 & 31;
@@ -371,6 +380,26 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_mma_kernel(const __g
                 mma16816(O[j][1], ph[0], ph[1], ph[2], ph[3], o0, o1);
                 mma16816(O[j][0], pl[0], pl[1], pl[2], pl[3], e0, e1);
                 mma16816(O[j][1], pl[0], pl[1], pl[2], pl[3], o0, o1);
+            }
+        }
+    };
+
+    int gi = 0;
+    for (; gi < ngroups; ++gi) {
+        const bool landed = mbar_wait_bounded(bar0 + 8 * (gi % kPfStages), (gi / kPfStages) & 1, kWaitLimitNs,
+                                              p.err, kErrScanWait);
+        if (!__all_sync(TQ_FULL_MASK, landed)) break;
+        const unsigned char* st = stages + (gi % kPfStages) * SB;
+        const int ntg = min(kPfWarps, ntiles - kPfWarps * gi);
+        for (int tt = 0; tt < ntg;) {
+            const int tok0 = t0 + 16 * (kPfWarps * gi + tt);
+            if (tok0 >= wlim) break;
+            if (tt + 1 < ntg) {
+                step(std::integral_constant<int, 2>{}, st, tt, tok0);
+                tt += 2;
+            } else {
+                step(std::integral_constant<int, 1>{}, st, tt, tok0);
+                tt += 1;
             }
         }
         __syncwarp();
