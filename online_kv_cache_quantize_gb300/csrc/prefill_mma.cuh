@@ -39,6 +39,17 @@
 
 namespace tqk {
 
+// fp16 hi/lo splits of a pair (a in the low half): hi = fp16(a), lo =
+// fp16(a - hi), each pair converted by one instruction; the same values as
+// split_half
+__device__ __forceinline__ void split_half2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const __half2 h = __floats2half2_rn(a, b);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 // 8 * field(w, off, n): the byte offset of an 8-byte table entry
 __device__ __forceinline__ uint32_t field8(const uint32_t* w, int off, int n) {
     const int W = off >> 5, S = off & 31;
@@ -342,16 +353,10 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_mma_kernel(const __g
             // A fragment (tokens along K): registers 0..3 = (row g, tokens 2c,
             // 2c+1), (row g+8, same), (row g, 8+2c, 9+2c), (row g+8, same)
             uint32_t ph[4], pl[4];
-#pragma unroll
-            for (int lo = 0; lo < 2; ++lo) {
-                uint32_t* dstp = lo ? pl : ph;
-                const float(&w0)[4] = s_[2 * t16];
-                const float(&w1)[4] = s_[2 * t16 + 1];
-                dstp[0] = split_half(w0[0], lo) | (split_half(w0[1], lo) << 16);
-                dstp[1] = split_half(w0[2], lo) | (split_half(w0[3], lo) << 16);
-                dstp[2] = split_half(w1[0], lo) | (split_half(w1[1], lo) << 16);
-                dstp[3] = split_half(w1[2], lo) | (split_half(w1[3], lo) << 16);
-            }
+            split_half2(s_[2 * t16][0], s_[2 * t16][1], ph[0], pl[0]);
+            split_half2(s_[2 * t16][2], s_[2 * t16][3], ph[1], pl[1]);
+            split_half2(s_[2 * t16 + 1][0], s_[2 * t16 + 1][1], ph[2], pl[2]);
+            split_half2(s_[2 * t16 + 1][2], s_[2 * t16 + 1][3], ph[3], pl[3]);
             // value codes of tokens 2c, 2c+1, 8+2c, 9+2c, coordinates 16g .. 16g+15
             uint32_t vf[4][3];
 #pragma unroll
