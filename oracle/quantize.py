@@ -164,8 +164,9 @@ def _widths(d, bprime):
 
 
 def pack_codes(idx, bprime):
-    """LSB-first bit stream per row, stride rounded up to 16 bytes; bprime is
-    one width or the width of every coordinate."""
+    """LSB-first bit stream per row; bprime is one width (stride rounded up to
+    16 bytes) or the width of every coordinate (two widths: stride rounded up
+    to 8 bytes)."""
     idx = np.atleast_2d(np.asarray(idx, dtype=np.int64))
     n, d = idx.shape
     w = _widths(d, bprime)

@@ -77,6 +77,40 @@ def test_layout_sizes(lib):
     assert lib.tq_sign_bytes(128) == 16 and lib.tq_sign_bytes(200) == 32
 
 
+def test_two_width_code_stride_matches_oracle(lib):
+    """Fractional-rate stride: the packed bit count rounded up to 8 bytes
+    (24 / 40 / 56 B for code bits 2/1, 3/2, 4/3 at d = 128), as the oracle's
+    packing lays it out; equal widths give the one-width stride."""
+    from oracle import quantize as oq
+    L = lib.load()
+    for cb, cb2, want in ((2, 1, 24), (3, 2, 40), (4, 3, 56)):
+        assert L.tq_code_bytes2(128, cb, cb2) == want
+        idx = np.zeros((1, 128), dtype=np.int64)
+        assert oq.pack_codes(idx, [cb if i % 16 < 8 else cb2 for i in range(128)]).shape[1] == want
+    for cb in (1, 2, 3, 4):
+        assert L.tq_code_bytes2(128, cb, cb) == L.tq_code_bytes(128, cb)
+
+
+def test_prefill_workspace_plan_on_the_host(lib):
+    """The prefill plan (no device work): q' and u rows plus the split
+    partials; invalid shapes give 0."""
+    import ctypes
+    L = lib.load()
+    a = lib.tq_prefill_args()
+    a.batch, a.chunk, a.hq, a.hkv, a.d, a.max_context = 1, 512, 32, 8, 128, 32768
+    a.k.capacity = 32768
+    a.n_splits = 3
+    rows = 512 * 32
+    want = 2 * rows * 128 * 4 + rows * 3 * (128 + 4) * 4
+    assert L.tq_attn_prefill_workspace(ctypes.byref(a)) == want
+    a.hq = 12  # 12 / 8 is not a group size
+    assert L.tq_attn_prefill_workspace(ctypes.byref(a)) == 0
+    a.hq, a.max_context = 32, 40000  # beyond the capacity
+    assert L.tq_attn_prefill_workspace(ctypes.byref(a)) == 0
+    a.max_context, a.d = 32768, 64
+    assert L.tq_attn_prefill_workspace(ctypes.byref(a)) == 0
+
+
 def test_argument_errors_are_reported(lib):
     with pytest.raises(lib.TQError) as e:
         lib.tq_make_rotation(1, 200, "rht")
