@@ -316,7 +316,7 @@ tq_status tq_decode_step(const tq_step_args* a, void* workspace, size_t ws_bytes
  * q_start[b] + i and sees the cache slots 0 .. q_start[b] + i (causal; capped
  * at min(capacity, max_context)); the chunk's own keys and values must have
  * been quantized into the cache before the call (tq_quantize_kv), like every
- * other token. Query head h reads KV head h / (hq / hkv). The logits, softmax
+ * other token. Query head h reads KV head gqa_map[h] (default h / (hq / hkv)). The logits, softmax
  * and value sum are decode's; the write-ups give decode only, so the causal
  * chunk is this library's reading. A query with no visible slot gives 0.
  * Kernels: query prep (q' and u), the tensor-core scan (64 query rows per CTA
@@ -329,6 +329,8 @@ typedef struct {
                                first token in each sequence                   */
     int max_context;        /* host: upper bound of q_start[b] + chunk (the
                                split plan); <= capacity                       */
+    const int32_t* gqa_map; /* HOST int32 [hq] in [0, hkv), or NULL = h/(hq/hkv);
+                               every KV head must serve hq/hkv query heads    */
     const tq_rotation* rot; /* uploaded                                       */
     const tq_qjl* qjl;      /* uploaded, m == k.m                             */
     tq_cache k;             /* PROD cache, rows == batch*hkv, m = 128         */

@@ -64,7 +64,7 @@ class tq_prefill_args(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("q_dtype", ctypes.c_int),
                 ("batch", ctypes.c_int), ("chunk", ctypes.c_int), ("hq", ctypes.c_int), ("hkv", ctypes.c_int),
                 ("d", ctypes.c_int), ("q_start", ctypes.c_void_p), ("max_context", ctypes.c_int),
-                ("rot", ctypes.c_void_p), ("qjl", ctypes.c_void_p), ("k", tq_cache), ("v", tq_cache),
+                ("gqa_map", ctypes.c_void_p), ("rot", ctypes.c_void_p), ("qjl", ctypes.c_void_p), ("k", tq_cache), ("v", tq_cache),
                 ("scale", ctypes.c_float), ("n_splits", ctypes.c_int), ("out", ctypes.c_void_p),
                 ("out_dtype", ctypes.c_int)]
 
@@ -344,9 +344,13 @@ def tq_attn_decode(q, kcache, vcache, seq_lens, max_seq_len, rot, qjl, out, work
                                  _stream_ptr(stream)), "tq_attn_decode")
 
 
-def _prefill_struct(q, kcache, vcache, q_start, max_context, rot, qjl, out, scale=0.0, n_splits=0):
+def _prefill_struct(q, kcache, vcache, q_start, max_context, rot, qjl, out, scale=0.0, n_splits=0, gqa_map=None):
     b, c, hq, d = q.shape
     a = tq_prefill_args()
+    keep = None
+    if gqa_map is not None:
+        keep = np.ascontiguousarray(gqa_map, dtype=np.int32)
+        a.gqa_map = keep.ctypes.data
     a.q = q.data_ptr()
     a.q_dtype = _dtype_code(q)
     a.batch, a.chunk, a.hq, a.hkv, a.d = b, c, hq, kcache.rows // b, d
@@ -360,11 +364,11 @@ def _prefill_struct(q, kcache, vcache, q_start, max_context, rot, qjl, out, scal
     a.n_splits = n_splits
     a.out = out.data_ptr()
     a.out_dtype = _dtype_code(out)
-    return a
+    return a, keep
 
 
 def tq_attn_prefill_workspace(q, kcache, vcache, q_start, max_context, rot, qjl, out, **kw):
-    a = _prefill_struct(q, kcache, vcache, q_start, max_context, rot, qjl, out, **kw)
+    a, _keep = _prefill_struct(q, kcache, vcache, q_start, max_context, rot, qjl, out, **kw)
     return load().tq_attn_prefill_workspace(ctypes.byref(a))
 
 
@@ -372,7 +376,7 @@ def tq_attn_prefill(q, kcache, vcache, q_start, max_context, rot, qjl, out, work
     """Chunked-prefill attention: q [batch][chunk][hq][d], the chunk of each
     sequence starting at position q_start[b] (device int32) and already
     quantized into the caches; writes out [batch][chunk][hq][d]."""
-    a = _prefill_struct(q, kcache, vcache, q_start, max_context, rot, qjl, out, **kw)
+    a, _keep = _prefill_struct(q, kcache, vcache, q_start, max_context, rot, qjl, out, **kw)
     _check(load().tq_attn_prefill(ctypes.byref(a), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                   _stream_ptr(stream)), "tq_attn_prefill")
 

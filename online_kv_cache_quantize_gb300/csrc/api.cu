@@ -869,6 +869,7 @@ tq_status plan_prefill(const tq_prefill_args* a, PrefillPlan* pl) {
     if (g != 1 && g != 2 && g != 4 && g != 8) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: hq / hkv must be 1, 2, 4 or 8");
     if (a->max_context < 0) return fail(TQ_ERR_INVALID_ARG, "tq_attn_prefill: max_context < 0");
     if (a->max_context > a->k.capacity) return fail(TQ_ERR_CAPACITY, "tq_attn_prefill: max_context exceeds the capacity");
+    if (a->hq > 256) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: hq must be <= 256");
     const int64_t rows = (int64_t)a->batch * a->chunk * a->hq;
     if (rows > (1ll << 31) / 128) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: too many query rows");
     const int64_t qbs = ((int64_t)a->chunk * g + tqk::kPfRows - 1) / tqk::kPfRows;
@@ -962,6 +963,16 @@ tq_status tq_attn_prefill(const tq_prefill_args* a, void* workspace, size_t ws_b
     fp.hkv = a->hkv;
     fp.group = pl.group;
     fp.q_start = a->q_start;
+    if (a->gqa_map) {
+        std::vector<int> count(a->hkv, 0);
+        for (int h = 0; h < a->hq; ++h) {
+            const int g = a->gqa_map[h];
+            if (g < 0 || g >= a->hkv) return fail(TQ_ERR_INVALID_ARG, "tq_attn_prefill: gqa_map entry out of range");
+            if (count[g] >= pl.group) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: every KV head must serve hq/hkv query heads");
+            fp.head_table[g * pl.group + count[g]++] = (int16_t)h;
+        }
+        fp.use_table = 1;
+    }
     fp.lim_cap = pl.lim_cap;
     fp.capacity = a->k.capacity;
     fp.kcodes = a->k.codes;

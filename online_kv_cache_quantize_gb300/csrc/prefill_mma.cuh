@@ -123,8 +123,9 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_mma_kernel(const __g
         mbar_init_fence();
     }
 
-    // ---- the rows: CTA row q = qb * 64 + warp * 16 + rho is chunk token q / G,
-    // head kv * G + q % G; this thread's rows are rho = g and g + 8 ----
+    // ---- the rows: CTA row q = qb * 64 + warp * 16 + rho is chunk token q / G
+    // and the (q % G)-th query head of KV head kv; this thread's rows are
+    // rho = g and g + 8 ----
     const int qs = p.q_start[b];
     int lim[2];
     int64_t qrow[2];
@@ -133,7 +134,8 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) prefill_mma_kernel(const __g
         const int q = qb * kPfRows + warp * 16 + g + 8 * r;
         const int i = q / G;
         const bool ok = i < p.chunk;
-        qrow[r] = ok ? ((int64_t)b * p.chunk + i) * p.hq + kv * G + (q - i * G) : -1;
+        const int j = kv * G + (q - i * G);
+        qrow[r] = ok ? ((int64_t)b * p.chunk + i) * p.hq + (p.use_table ? (int)p.head_table[j] : j) : -1;
         lim[r] = ok ? max(0, min(qs + i + 1, p.lim_cap)) : 0;
     }
     // the CTA's last chunk token bounds the tokens any of its rows can see

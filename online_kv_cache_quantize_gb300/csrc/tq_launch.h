@@ -154,6 +154,8 @@ struct PrefillParams {
     const float* u;       // [rows][128] u = S q'
     int batch, chunk, hq, hkv, group;
     const int32_t* q_start;  // [batch] position of the chunk's first token
+    int16_t head_table[256];  // query heads of KV head kv: head_table[kv * group + j]
+    int use_table;            // 0: head kv * group + j
     int lim_cap;          // visible slots are capped at min(capacity, max_context)
     int64_t capacity;
     const uint8_t* kcodes;

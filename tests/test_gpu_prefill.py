@@ -42,20 +42,22 @@ def _caches(k, v, kbits, vbits, kind, kbits2=None, vbits2=None):
     return kc, vc, gk, gv, kq, vq, pi, s
 
 
-def _gpu_prefill(q, gk, gv, q_start, max_context, kind, n_splits=0, out_dtype=torch.float32, q_dtype=torch.float32):
+def _gpu_prefill(q, gk, gv, q_start, max_context, kind, n_splits=0, out_dtype=torch.float32, q_dtype=torch.float32,
+                 gqa_map=None):
     bsz, c, hq, d = q.shape
     rot, qjl = P.handles(d, kind)
     qt = torch.from_numpy(np.ascontiguousarray(q, dtype=np.float32)).cuda().to(q_dtype)
     qs = torch.tensor(q_start, dtype=torch.int32, device="cuda")
     out = torch.full((bsz, c, hq, d), float("nan"), dtype=out_dtype, device="cuda")
-    ws = B.workspace(B.tq_attn_prefill_workspace(qt, gk, gv, qs, max_context, rot, qjl, out, n_splits=n_splits))
-    B.tq_attn_prefill(qt, gk, gv, qs, max_context, rot, qjl, out, ws, n_splits=n_splits)
+    kw = dict(n_splits=n_splits, gqa_map=gqa_map)
+    ws = B.workspace(B.tq_attn_prefill_workspace(qt, gk, gv, qs, max_context, rot, qjl, out, **kw))
+    B.tq_attn_prefill(qt, gk, gv, qs, max_context, rot, qjl, out, ws, **kw)
     torch.cuda.synchronize()
     return out.float().cpu().numpy()
 
 
-def _check(q, kc, vc, kq, vq, q_start, pi, s, out):
-    want = oa.prefill(q.astype(np.float64), kc, vc, q_start, pi, s, kq["centroids"], vq["centroids"])
+def _check(q, kc, vc, kq, vq, q_start, pi, s, out, gqa_map=None):
+    want = oa.prefill(q.astype(np.float64), kc, vc, q_start, pi, s, kq["centroids"], vq["centroids"], gqa_map=gqa_map)
     scale = max(np.max(vc["norm16"]) / np.sqrt(q.shape[-1]), 1e-30)
     err = np.max(np.abs(out - want))
     assert err <= OUT_TOL * scale, f"max abs err {err:.3g} > {OUT_TOL * scale:.3g}"
@@ -86,6 +88,16 @@ def test_prefill_group_sizes(group, chunk):
     q_start = [400]
     out = _gpu_prefill(q, gk, gv, q_start, cap, "rht")
     _check(q, kc, vc, kq, vq, q_start, pi, s, out)
+
+
+def test_prefill_permuted_gqa_map():
+    """A permuted query-head -> KV-head map (as decode takes) is honoured."""
+    k, v = W.decode_kv(1, 4, 384, seed=31)
+    kc, vc, gk, gv, kq, vq, pi, s = _caches(k, v, 3, 3, "dense")
+    q = W.query_vectors((1, 20, 16, 128), seed=32)
+    gmap = np.array([3, 2, 1, 0] * 4, dtype=np.int32)
+    out = _gpu_prefill(q, gk, gv, [364], 384, "dense", gqa_map=gmap)
+    _check(q, kc, vc, kq, vq, [364], pi, s, out, gqa_map=gmap)
 
 
 def test_prefill_first_chunk_causal_triangle():
