@@ -320,7 +320,8 @@ tq_status tq_decode_step(const tq_step_args* a, void* workspace, size_t ws_bytes
  * and value sum are decode's; the write-ups give decode only, so the causal
  * chunk is this library's reading. A query with no visible slot gives 0.
  * Kernels: query prep (q' and u), the tensor-core scan (64 query rows per CTA
- * against 16-token tiles, split over the tokens), and the decode merge. */
+ * against 16-token tiles, split over the tokens), and a merge of the splits
+ * (one warp per query row) with the un-rotation. */
 typedef struct {
     const void* q;          /* device [batch][chunk][hq][d] of q_dtype         */
     int q_dtype;            /* TQ_F32 or TQ_BF16                              */
@@ -337,7 +338,8 @@ typedef struct {
     tq_cache v;             /* MSE cache, rows == batch*hkv                   */
     float scale;            /* softmax scale; 0 -> 1/sqrt(d)                  */
     int n_splits;           /* token splits; 0 -> automatic                   */
-    void* out;              /* device [batch][chunk][hq][d] of out_dtype       */
+    void* out;              /* device [batch][chunk][hq][d] of out_dtype,
+                               16-byte aligned                                */
     int out_dtype;          /* TQ_F32 or TQ_BF16                              */
 } tq_prefill_args;
 

@@ -933,6 +933,7 @@ tq_status tq_attn_prefill(const tq_prefill_args* a, void* workspace, size_t ws_b
     if (!a->q || !a->out || !a->q_start) return fail(TQ_ERR_INVALID_ARG, "tq_attn_prefill: q/out/q_start is NULL");
     if (a->q_dtype != TQ_F32 && a->q_dtype != TQ_BF16) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: q_dtype must be F32 or BF16");
     if (a->out_dtype != TQ_F32 && a->out_dtype != TQ_BF16) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: out_dtype must be F32 or BF16");
+    if (!aligned(a->out, 16)) return fail(TQ_ERR_ALIGNMENT, "tq_attn_prefill: out must be 16-byte aligned (vector stores)");
     if (!workspace || ws_bytes < pl.total) return fail(TQ_ERR_WORKSPACE, "tq_attn_prefill: workspace missing or too small");
     if (!aligned(workspace, 256)) return fail(TQ_ERR_ALIGNMENT, "tq_attn_prefill: workspace must be 256-byte aligned");
 
@@ -1007,7 +1008,7 @@ tq_status tq_attn_prefill(const tq_prefill_args* a, void* workspace, size_t ws_b
     cudaStream_t st = (cudaStream_t)stream;
     if ((e = tqk::launch_query_prep(pp, st)) != cudaSuccess) return cuda_status(e, "tq_attn_prefill query prep");
     if ((e = tqk::launch_prefill_mma(fp, kb, vb, two, st)) != cudaSuccess) return cuda_status(e, "tq_attn_prefill scan");
-    return cuda_status(tqk::launch_combine(cp, st), "tq_attn_prefill merge");
+    return cuda_status(tqk::launch_merge_rows(cp, st), "tq_attn_prefill merge");
 }
 
 tq_status tq_device_errors(uint32_t* flags_out, int reset) {

@@ -125,4 +125,21 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, combine_kernel, p);
 }
 
+// The few-splits merge (d = 128), also a programmatic dependent of the scan.
+cudaError_t launch_merge_rows(const CombineParams& p, cudaStream_t s) {
+    if (p.rows <= 0) return cudaSuccess;
+    if (p.d != 128) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((p.rows + kMergeWarps - 1) / kMergeWarps));
+    cfg.blockDim = dim3(kMergeWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, merge_rows_kernel, p);
+}
+
 }  // namespace tqk

@@ -293,4 +293,83 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
     }
 }
 
+// ---------------------------------------------------------------------------
+// Merge of a few splits per row (the chunked prefill: thousands of rows, a
+// handful of splits each): one warp per row, lane l owning coordinates
+// 4l .. 4l+3 (d = 128). The same arithmetic as combine_kernel: M* = max M_s,
+// Z = sum Z_s 2^(M_s - M*), a = sum a_s 2^(M_s - M*) / Z, then o = Pi^T a
+// (RHT: s * (H a) / sqrt(d) with H by butterflies in the thread for
+// strides 1, 2 and shuffles for 4 .. 64; dense: coalesced rows of Pi).
+// ---------------------------------------------------------------------------
+constexpr int kMergeWarps = 8;
+
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_rows_kernel(const __grid_constant__ CombineParams p) {
+    __shared__ __align__(16) float s_a[kMergeWarps][128];
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int row = blockIdx.x * kMergeWarps + warp;
+    if (row >= p.rows) return;
+    const int ns = p.n_splits, stride = 128 + kPartPad;
+    const float* base = p.partial + (int64_t)row * ns * stride;
+    float mstar = -INFINITY;
+    for (int s = 0; s < ns; ++s) mstar = fmaxf(mstar, base[(int64_t)s * stride + 128]);
+    float z = 0.0f;
+    float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (mstar != -INFINITY) {
+        for (int s = 0; s < ns; ++s) {
+            const float* ps = base + (int64_t)s * stride;
+            const float ms = ps[128];
+            if (ms == -INFINITY) continue;
+            const float w = exp2f(ms - mstar);
+            const float4 av = *reinterpret_cast<const float4*>(ps + 4 * lane);
+            z = fmaf(ps[129], w, z);
+            a.x = fmaf(av.x, w, a.x);
+            a.y = fmaf(av.y, w, a.y);
+            a.z = fmaf(av.z, w, a.z);
+            a.w = fmaf(av.w, w, a.w);
+        }
+    }
+    const float inv = z > 0.0f ? 1.0f / z : 0.0f;
+    float y[4] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv};
+    float o[4];
+    if (p.rht) {
+        // strides 1 and 2 inside the thread, then 4 .. 64 across the lanes
+        float t0 = y[0] + y[1], t1 = y[0] - y[1], t2 = y[2] + y[3], t3 = y[2] - y[3];
+        y[0] = t0 + t2; y[2] = t0 - t2; y[1] = t1 + t3; y[3] = t1 - t3;
+#pragma unroll
+        for (int h = 1; h < 32; h <<= 1)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float t = __shfl_xor_sync(TQ_FULL_MASK, y[r], h);
+                y[r] = (lane & h) ? (t - y[r]) : (y[r] + t);
+            }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) o[r] = y[r] * p.sgn[4 * lane + r] * p.inv_sqrt_d;
+    } else {
+        *reinterpret_cast<float4*>(&s_a[warp][4 * lane]) = make_float4(y[0], y[1], y[2], y[3]);
+        __syncwarp();
+        o[0] = o[1] = o[2] = o[3] = 0.0f;
+#pragma unroll 8
+        for (int k = 0; k < 128; ++k) {
+            const float ak = s_a[warp][k];
+            const float4 pk = __ldg(reinterpret_cast<const float4*>(p.pi32 + (size_t)k * 128) + lane);
+            o[0] = fmaf(pk.x, ak, o[0]);
+            o[1] = fmaf(pk.y, ak, o[1]);
+            o[2] = fmaf(pk.z, ak, o[2]);
+            o[3] = fmaf(pk.w, ak, o[3]);
+        }
+    }
+    if (p.out_dtype == 1) {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (int64_t)row * 128 + 4 * lane;
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(o[0], o[1]), hi = __floats2bfloat162_rn(o[2], o[3]);
+        uint2 w;
+        w.x = *reinterpret_cast<const uint32_t*>(&lo);
+        w.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(out) = w;
+    } else {
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + (int64_t)row * 128 + 4 * lane) =
+            make_float4(o[0], o[1], o[2], o[3]);
+    }
+}
+
 }  // namespace tqk

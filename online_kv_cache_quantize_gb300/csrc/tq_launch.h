@@ -207,6 +207,8 @@ struct CombineParams {
 };
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
+// the same merge for many rows with few splits each (d = 128): a warp per row
+cudaError_t launch_merge_rows(const CombineParams& p, cudaStream_t s);
 
 struct TopkParams {
     const float* qprime;  // [nq][d]
