@@ -951,6 +951,7 @@ tq_status tq_attn_prefill(const tq_prefill_args* a, void* workspace, size_t ws_b
     pp.rht = a->rot->kind == TQ_ROT_RHT;
     pp.inv_sqrt_d = (float)(1.0 / std::sqrt((double)a->d));
     pp.st32 = a->qjl->d_st32;
+    pp.s16 = a->qjl->d_s16;
     pp.qprime = (float*)ws;
     pp.u = (float*)(ws + pl.off_u);
 
@@ -1006,7 +1007,7 @@ tq_status tq_attn_prefill(const tq_prefill_args* a, void* workspace, size_t ws_b
     cp.out_dtype = a->out_dtype == TQ_BF16 ? 1 : 0;
 
     cudaStream_t st = (cudaStream_t)stream;
-    if ((e = tqk::launch_query_prep(pp, st)) != cudaSuccess) return cuda_status(e, "tq_attn_prefill query prep");
+    if ((e = tqk::launch_rows_prep(pp, st)) != cudaSuccess) return cuda_status(e, "tq_attn_prefill query prep");
     if ((e = tqk::launch_prefill_mma(fp, kb, vb, two, st)) != cudaSuccess) return cuda_status(e, "tq_attn_prefill scan");
     return cuda_status(tqk::launch_merge_rows(cp, st), "tq_attn_prefill merge");
 }

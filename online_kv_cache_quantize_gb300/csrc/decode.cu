@@ -12,11 +12,12 @@ namespace tqk {
 // owning coordinate i: q' = Pi q (random-sign Walsh-Hadamard by butterflies,
 // or the dense Pi), u = S q' from S staged in shared memory, and the scan's
 // B operands (the same words as write_frag in decode.cuh).
-__device__ __forceinline__ void prep_row128(const PrepParams& p, int64_t row, StepSmem& s) {
+// stage: copy S into shared memory here (false: the caller already has)
+__device__ __forceinline__ void prep_row128(const PrepParams& p, int64_t row, StepSmem& s, bool stage = true) {
     constexpr int D = 128;
     const int i = threadIdx.x;
     const bool want_u = p.st32 != nullptr;
-    if (want_u) stage_s(p.s16, s);  // lands while q' is formed
+    if (want_u && stage) stage_s(p.s16, s);  // lands while q' is formed
     const float qi = p.q_dtype == 1 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.q)[row * D + i])
                                     : reinterpret_cast<const float*>(p.q)[row * D + i];
     float y;
@@ -78,6 +79,30 @@ cudaError_t launch_step_prep(const StepPrepParams& p, cudaStream_t s) {
         (p.v.n > 0 && p.v.d != 128))
         return cudaErrorInvalidValue;
     step_prep_kernel<<<(unsigned)ctas, kStepThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+// Query prep of many rows (the chunked prefill): kPrepRows rows per CTA, S
+// staged in shared memory once per CTA instead of read once per row; writes
+// q' and u in fp32.
+constexpr int kPrepRows = 8;
+
+__global__ void __launch_bounds__(kStepThreads) rows_prep_kernel(const __grid_constant__ PrepParams p) {
+    __shared__ StepSmem s;
+    if (p.st32 != nullptr) stage_s(p.s16, s);
+    const int64_t r0 = (int64_t)blockIdx.x * kPrepRows;
+    for (int k = 0; k < kPrepRows && r0 + k < p.rows; ++k) {
+        if (k) step_sync();  // the previous row's reads of the shared rows are done
+        prep_row128(p, r0 + k, s, false);
+    }
+}
+
+cudaError_t launch_rows_prep(const PrepParams& p, cudaStream_t s) {
+    if (p.rows <= 0) return cudaSuccess;
+    if (p.d != 128 || p.frag || (p.st32 && (p.m != 128 || !p.s16))) return cudaErrorInvalidValue;
+    const int64_t ctas = (p.rows + kPrepRows - 1) / kPrepRows;
+    if (ctas > 0x7fffffff) return cudaErrorInvalidValue;
+    rows_prep_kernel<<<(unsigned)ctas, kStepThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -87,6 +87,9 @@ constexpr int kFragWords = 256;
 constexpr int kPartPad = 4;
 
 cudaError_t launch_query_prep(const PrepParams& p, cudaStream_t s);
+// d = 128 rows in fp32 (q' and u; m = 128 with S in its unit layout): several
+// rows per CTA sharing one copy of S
+cudaError_t launch_rows_prep(const PrepParams& p, cudaStream_t s);
 
 // One launch for the work a decode step does before its scan: the query prep
 // of pp.rows query rows (d = 128) and the quantize-on-append of k.n key and
