@@ -91,6 +91,25 @@ def test_two_width_code_stride_matches_oracle(lib):
         assert L.tq_code_bytes2(128, cb, cb) == L.tq_code_bytes(128, cb)
 
 
+def test_decode_workspace_plan_on_the_host(lib):
+    """The decode plan (no device work): 1 KB of B operands per query row plus
+    the split partials, splits of a multiple of 64 tokens; invalid shapes give 0."""
+    import ctypes
+    L = lib.load()
+    a = lib.tq_decode_args()
+    a.batch, a.hq, a.hkv, a.d, a.max_seq_len, a.n_splits = 1, 32, 8, 128, 32768, 74
+    rows = 32
+    chunk = -(-32768 // 74)
+    chunk = max(64, -(-chunk // 64) * 64)
+    splits = -(-32768 // chunk)
+    want = rows * 1024 + rows * splits * (128 + 4) * 4
+    assert L.tq_attn_decode_workspace(ctypes.byref(a)) == want
+    a.hq = 24  # 24 / 8 = 3 is not a group size
+    assert L.tq_attn_decode_workspace(ctypes.byref(a)) == 0
+    a.hq, a.d = 32, 96
+    assert L.tq_attn_decode_workspace(ctypes.byref(a)) == 0
+
+
 def test_prefill_workspace_plan_on_the_host(lib):
     """The prefill plan (no device work): q' and u rows plus the split
     partials; invalid shapes give 0."""
