@@ -567,7 +567,11 @@ tq_status decode_launch(const DecodeLaunch& D, cudaStream_t st, tqk::StepPrepPar
     if (e != cudaSuccess) return cuda_status(e, "tq_attn_decode scan");
     if (D.scan_end && (e = cudaEventRecord(D.scan_end, st)) != cudaSuccess)
         return cuda_status(e, "tq_attn_decode scan_end");
-    e = tqk::launch_combine(D.cp, st);
+    // many rows with few splits each (batched decode): one warp per row;
+    // otherwise the wide merge, whose 1024 threads per row load the splits of
+    // a long row in one round of latency
+    const bool few = D.cp.n_splits <= 16 && D.cp.rows >= 128 && D.cp.d == 128 && aligned(D.cp.out, 16);
+    e = few ? tqk::launch_merge_rows(D.cp, st) : tqk::launch_combine(D.cp, st);
     return cuda_status(e, "tq_attn_decode combine");
 }
 

@@ -117,6 +117,24 @@ def test_group_sizes_batch_and_empty(group):
     _check(q, kc, vc, kq, vq, lens, pi, s, out, logits, out_scale=scale)
 
 
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_many_rows_few_splits(out_dtype):
+    """Batch 8 x 32 query heads (256 rows) over 512 tokens: few splits per
+    row, so the warp-per-row merge runs; RHT and dense."""
+    for kind in ("rht", "dense"):
+        k, v = W.decode_kv(8, 4, 512, seed=41)
+        kc, vc, gk, gv, kq, vq, pi, s = _oracle_caches(k, v, 3, 3, kind)
+        q = W.query_vectors((8, 32, 128), seed=42)
+        lens = [512, 1, 0, 300, 511, 64, 65, 200]
+        out, logits = _gpu_decode(q, gk, gv, lens, kind, out_dtype=out_dtype, with_logits=out_dtype == torch.float32)
+        scale = np.max(vc["norm16"]) / np.sqrt(128)
+        if out_dtype == torch.float32:
+            _check(q, kc, vc, kq, vq, lens, pi, s, out, logits, out_scale=scale)
+        else:
+            want, _ = oa.decode(q.astype(np.float64), kc, vc, lens, pi, s, kq["centroids"], vq["centroids"])
+            assert np.max(np.abs(out - want)) <= 2.0**-8 * np.max(np.abs(want)) + OUT_TOL * scale
+
+
 def test_split_invariance_and_gqa_map():
     """n_splits = 1 and automatic splits agree; a permuted GQA map is honoured."""
     hkv, cap = 4, 2048
