@@ -37,6 +37,7 @@ struct StepSmem {
     float red[4];
     double red64[4];
     uint32_t cw[16];    // packed codes: at most 4 bits x 128 coordinates
+    int fsel;           // the flagged coordinate being re-decided
 };
 
 // barrier 1 over the 128 threads of the CTA
@@ -215,7 +216,7 @@ __device__ __forceinline__ void append_vector(const QuantParams& p, int xdtype, 
             dmin = fminf(dmin, fabsf(y - book->t[t]));
         }
     }
-    const bool flag = !(dmin >= p.guard);
+    bool flag = !(dmin >= p.guard);
 
     // fp16 norm; near an fp16 rounding midpoint it is re-rounded from fp64
     uint16_t n16 = f16_bits_sat(n32);
@@ -226,27 +227,37 @@ __device__ __forceinline__ void append_vector(const QuantParams& p, int xdtype, 
         nclose = dn != up && fabsf(n32 - 0.5f * (dn + up)) <= 1.0e-6f * n32;
     }
 
-    // ---- fp64 re-decision (rare) ----
+    // ---- fp64 re-decision (rare): the norm from an fp64 sum, and each
+    // flagged coordinate's y from an fp64 dot product shared by the 128
+    // threads (one term each, then a block sum) -- one thread alone would
+    // run 128 dependent fp64 operations, long where the fp64 pipe is narrow ----
     if (step_any(flag || nclose)) {
         const double n64 = sqrt(step_sum64((double)xi * (double)xi, s));
         if (nclose) n16 = __half_as_ushort(__double2half(fmin(n64, 65504.0)));
-        if (flag) {
-            double part = 0.0;
+        while (step_any(flag)) {
+            if (i == 0) s.fsel = D;
+            step_sync();
+            if (flag) atomicMin(&s.fsel, i);
+            step_sync();
+            const int fi = s.fsel;  // the lowest flagged coordinate; thread i adds term i
+            double t;
             if (rht) {
-                for (int e = 0; e < D; ++e) {
-                    const double t = (double)p.sgn[e] * (double)s.x[e];
-                    part += (__popc(i & e) & 1) ? -t : t;
-                }
+                t = (double)p.sgn[i] * (double)s.x[i];
+                if (__popc(fi & i) & 1) t = -t;
             } else {
-                for (int e = 0; e < D; ++e) part = fma(p.pi64[(size_t)i * D + e], (double)s.x[e], part);
+                t = p.pi64[(size_t)fi * D + i] * (double)s.x[i];
             }
-            double y64 = 0.0;
-            if (n64 > 0.0) y64 = rht ? part / (sqrt((double)D) * n64) : part / n64;
-            k = 0;
+            const double part = step_sum64(t, s);
+            if (i == fi) {
+                double y64 = 0.0;
+                if (n64 > 0.0) y64 = rht ? part / (sqrt((double)D) * n64) : part / n64;
+                k = 0;
 #pragma unroll
-            for (int t = 0; t < kMaxLevels - 1; ++t)
-                if (t < L - 1) k += (y64 >= book->t64[t]) ? 1 : 0;
-            y = (float)y64;
+                for (int tt = 0; tt < kMaxLevels - 1; ++tt)
+                    if (tt < L - 1) k += (y64 >= book->t64[tt]) ? 1 : 0;
+                y = (float)y64;
+                flag = false;
+            }
         }
     }
 
