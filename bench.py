@@ -243,7 +243,7 @@ def run_tq(args):
             raise RuntimeError(f"{what}: {B.status_name(s)} {L.tq_last_error().decode()}")
 
     # one decode step through the public API: tq_decode_step appends the new
-    # token's K and V (on the library's side streams) and runs the attention
+    # token's K and V and runs the attention, all on the caller's stream
     sa = B.tq_step_args()
     sa.attn = da
     sa.k_new = knew.data_ptr()
@@ -264,13 +264,20 @@ def run_tq(args):
 
     sampler = ClockSampler(local)
     sampler.start()
-    t_warm = time.time()
+    # exactly --warmup untimed steps, then (only if asked) a further
+    # time-based warm-up, reported separately
     n_warm = 0
-    while n_warm < args.warmup or (not args.quick and time.time() - t_warm < 1.5):
+    for _ in range(args.warmup):
         flush.fill_(n_warm & 0xFF)
         step()
         n_warm += 1
-        if n_warm % 256 == 0:
+    torch.cuda.synchronize()
+    n_extra, t_warm = 0, time.time()
+    while time.time() - t_warm < args.warmup_seconds:
+        flush.fill_(n_extra & 0xFF)
+        step()
+        n_extra += 1
+        if n_extra % 256 == 0:
             torch.cuda.synchronize()
     torch.cuda.synchronize()
 
@@ -352,7 +359,18 @@ def run_tq(args):
         check(L.tq_decode_step(ctypes.byref(sa_h), wsb.data_ptr(), wsz, sp), "decode step (host buffers)")
         eev[i][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in eev)
+    e2e_dev_ms = statistics.mean(a.elapsed_time(b) for a, b in eev)
+    # host wall clock per step, as a caller sees it: submit the step, wait
+    # for its stream, the output is then readable in pinned host memory; no
+    # flush or other work in front of it (so host submission is not hidden)
+    wall = []
+    for i in range(ne):
+        h0 = time.perf_counter()
+        check(L.tq_decode_step(ctypes.byref(sa_h), wsb.data_ptr(), wsz, sp), "decode step (host buffers)")
+        stream.synchronize()
+        _ = float(h_out[0, 0, 0])  # the result, read on the host
+        wall.append(time.perf_counter() - h0)
+    e2e_ms = statistics.mean(wall) * 1e3
     # (b) the same with explicit copies: host -> device into the step's
     # device buffers, the step, device -> host of the output
     mev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ne)]
@@ -364,13 +382,24 @@ def run_tq(args):
         h_out.copy_(out, non_blocking=True)
         mev[i][1].record(stream)
     torch.cuda.synchronize()
+    e2e_copy_dev_ms = statistics.mean(a.elapsed_time(b) for a, b in mev)
+    wall = []
+    for i in range(ne):
+        h0 = time.perf_counter()
+        inbuf.copy_(h_in, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+        _ = float(h_out[0, 0, 0])
+        wall.append(time.perf_counter() - h0)
+    e2e_copy_ms = statistics.mean(wall) * 1e3
     clocks = sampler.stop()
-    e2e_copy_ms = statistics.mean(a.elapsed_time(b) for a, b in mev)
     h2d = h_in.numel() * h_in.element_size()
     d2h = h_out.numel() * h_out.element_size()
 
     # the slowest rank's times
-    total_ms, e2e_ms, e2e_copy_ms, q_ms = max_over_ranks([total_ms, e2e_ms, e2e_copy_ms, q_ms], "cuda")
+    total_ms, e2e_ms, e2e_copy_ms, q_ms, e2e_dev_ms, e2e_copy_dev_ms = max_over_ranks(
+        [total_ms, e2e_ms, e2e_copy_ms, q_ms, e2e_dev_ms, e2e_copy_dev_ms], "cuda")
     tokens_per_step = bsz * T
     value = job_throughput(ws, tokens_per_step, K, total_ms)
 
@@ -386,6 +415,7 @@ def run_tq(args):
     if rank == 0:
         res = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": n_warm,
+            "warmup_extra_steps": n_extra,
             "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
             "config": {"workload": w["name"], "batch": bsz, "hq": hq, "hkv": hkv, "d": d, "seq_len": T,
@@ -404,10 +434,16 @@ def run_tq(args):
                          "roofline": {"bound": "hbm", "achieved": q_achieved, "peak": peak, "unit": "GB/s",
                                       "frac": q_achieved / peak, "alg_bytes_per_call": q_alg_bytes}},
             "e2e": {"value": job_throughput(ws, tokens_per_step, 1, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": ne,
+                    "d2h_bytes_per_step": d2h, "steps": ne, "ms_per_step": e2e_ms,
+                    "clock": "host wall clock (time.perf_counter) per step: submit, stream synchronize, output "
+                             "read on the host; no flush in front",
                     "transfer": "zero-copy: the step's kernels read the query and the new K and V from pinned host "
                                 "memory and write the output to pinned host memory (CPU-GPU link inside the kernels)",
+                    "device_events": {"value": job_throughput(ws, tokens_per_step, 1, e2e_dev_ms), "unit": UNIT,
+                                      "clock": "CUDA events around the step on its stream, L2 flushed before each"},
                     "with_memcpy": {"value": job_throughput(ws, tokens_per_step, 1, e2e_copy_ms), "unit": UNIT,
+                                    "ms_per_step": e2e_copy_ms, "clock": "host wall clock, as above",
+                                    "device_events": job_throughput(ws, tokens_per_step, 1, e2e_copy_dev_ms),
                                     "transfer": "cudaMemcpyAsync host->device of the inputs and device->host of "
                                                 "the output around the step, on its stream"}},
             "gpu_launches": launches_per_step * K,
@@ -480,12 +516,15 @@ def run_reference(args):
     for _ in range(args.warmup):
         one(tokens)
     times = [one(tokens) for _ in range(args.steps)]
-    full_step_s = statistics.mean(times) * (WORKLOAD["seq_len"] / tokens) * hkv
+    sample_s = statistics.mean(times)
+    full_step_s = sample_s * (WORKLOAD["seq_len"] / tokens) * hkv
     value = WORKLOAD["batch"] * WORKLOAD["seq_len"] / full_step_s
     sample = (f"1 of {hkv} KV heads x {tokens} of {WORKLOAD['seq_len']} tokens per step (K/V quantize + 4-head decode), "
               f"extrapolated linearly to the full step")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": full_step_s * 1e3,
+            "ms_per_step_is": "extrapolated from the measured sample (sample_ms_per_step) to the full step",
+            "sample_ms_per_step": sample_s * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD["name"], "batch": 1, "hq": WORKLOAD["hq"], "hkv": hkv, "d": 128,
                        "seq_len": WORKLOAD["seq_len"], "rotation": WORKLOAD["rotation"]},
@@ -725,6 +764,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--warmup-seconds", type=float, default=0.0,
+                    help="extra time-based warm-up after the --warmup steps (reported as warmup_extra_steps)")
     ap.add_argument("--impl", choices=["tq", "reference"], default="tq")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true", help="short run for profiling: no clock window, no oracle timing")

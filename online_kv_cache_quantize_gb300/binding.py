@@ -16,7 +16,9 @@ _LIB_PATH = os.path.join(_PKG, "libtq.so")
 _lib = None
 
 TQ_OK = 0
+TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED = 1, 2
 TQ_ERR_TIMEOUT = 6
+TQ_ERR_WORKSPACE = 7
 TQ_ROT_DENSE_QR, TQ_ROT_RHT = 0, 1
 TQ_MSE, TQ_PROD = 0, 1
 TQ_F32, TQ_BF16, TQ_F16 = 0, 1, 2

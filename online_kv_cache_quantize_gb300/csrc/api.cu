@@ -459,9 +459,6 @@ tq_status decode_prepare(const tq_decode_args* a, void* workspace, size_t ws_byt
     if (!a->q || !a->out || !a->seq_lens) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: q/out/seq_lens is NULL");
     if (a->q_dtype != TQ_F32 && a->q_dtype != TQ_BF16) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: q_dtype must be F32 or BF16");
     if (a->out_dtype != TQ_F32 && a->out_dtype != TQ_BF16) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: out_dtype must be F32 or BF16");
-    if (!workspace || ws_bytes < pl.total) return fail(TQ_ERR_WORKSPACE, "tq_attn_decode: workspace missing or too small");
-    if (!aligned(workspace, 256)) return fail(TQ_ERR_ALIGNMENT, "tq_attn_decode: workspace must be 256-byte aligned");
-
     tqk::DecodeParams& dp = D->dp;
     std::memset(&dp, 0, sizeof(dp));
     if (a->gqa_map) {
@@ -474,6 +471,9 @@ tq_status decode_prepare(const tq_decode_args* a, void* workspace, size_t ws_byt
         }
         dp.use_table = 1;
     }
+    // the workspace last: every other argument error takes precedence
+    if (!workspace || ws_bytes < pl.total) return fail(TQ_ERR_WORKSPACE, "tq_attn_decode: workspace missing or too small");
+    if (!aligned(workspace, 256)) return fail(TQ_ERR_ALIGNMENT, "tq_attn_decode: workspace must be 256-byte aligned");
     char* ws = (char*)workspace;
     uint32_t* frag = (uint32_t*)(ws + pl.off_frag);
     float* part = (float*)(ws + pl.off_part);

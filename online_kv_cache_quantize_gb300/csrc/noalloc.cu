@@ -29,13 +29,6 @@ void* g_scratch_addr[kMaxDevices] = {};
 
 extern "C" tq_status tq_attn_decode_static(const tq_decode_args* a, tq_stream stream) {
     if (!a) return tq::fail(TQ_ERR_INVALID_ARG, "tq_attn_decode_static: args are NULL");
-    const size_t need = tq_attn_decode_workspace(a);
-    if (need == 0) return TQ_ERR_INVALID_ARG;  // message set by the planner
-    if (need > (size_t)TQ_STATIC_DECODE_SCRATCH_BYTES)
-        return tq::fail(TQ_ERR_WORKSPACE, "tq_attn_decode_static: these arguments need " + std::to_string(need) +
-                                              " bytes of scratch; the static array holds " +
-                                              std::to_string((size_t)TQ_STATIC_DECODE_SCRATCH_BYTES) +
-                                              " (use tq_attn_decode with a workspace)");
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return tq::fail(TQ_ERR_CUDA, std::string("tq_attn_decode_static: ") + cudaGetErrorString(e));
@@ -53,7 +46,17 @@ extern "C" tq_status tq_attn_decode_static(const tq_decode_args* a, tq_stream st
         }
         ptr = g_scratch_addr[dev];
     }
-    // every scratch byte the decode reads is written earlier in the same call,
-    // so nothing needs clearing between calls
-    return tq_attn_decode(a, ptr, (size_t)TQ_STATIC_DECODE_SCRATCH_BYTES, stream);
+    // tq_attn_decode checks every argument first and the scratch size last,
+    // so an invalid call gets the same status here as there; only the
+    // message of a too-small scratch is made specific to the static array.
+    // Every scratch byte the decode reads is written earlier in the same
+    // call, so nothing needs clearing between calls.
+    const tq_status s = tq_attn_decode(a, ptr, (size_t)TQ_STATIC_DECODE_SCRATCH_BYTES, stream);
+    if (s == TQ_ERR_WORKSPACE)
+        return tq::fail(TQ_ERR_WORKSPACE, "tq_attn_decode_static: these arguments need " +
+                                              std::to_string(tq_attn_decode_workspace(a)) +
+                                              " bytes of scratch; the static array holds " +
+                                              std::to_string((size_t)TQ_STATIC_DECODE_SCRATCH_BYTES) +
+                                              " (use tq_attn_decode with a workspace)");
+    return s;
 }
