@@ -457,8 +457,8 @@ def run_tq(args):
 
 
 # ----------------------------------------------------- oracle (CPU) arm ----
-def oracle_sample(budget_s):
-    """Oracle decode steps on a sample: one KV head and its 4 query heads over
+def oracle_sample(budget_s, w=None):
+    """Oracle decode steps on a sample: one KV head and its G query heads over
     `tokens` cached tokens (plus the appended K/V quantize for that head),
     extrapolated linearly to the full step (all KV heads, all tokens)."""
     from oracle import attention as oa
@@ -467,12 +467,12 @@ def oracle_sample(budget_s):
     from oracle import rotation as orot
     from online_kv_cache_quantize_gb300 import workloads as W
 
-    w = WORKLOAD
+    w = WORKLOAD if w is None else w
     d, T, hkv, hq = w["d"], w["seq_len"], w["hkv"], w["hq"]
     g = hq // hkv
     pi = orot.make_rotation(W.ROT_SEED, d, w["rotation"])
     s = orng.round_to_bf16(orng.normals(W.QJL_SEED, d * d).reshape(d, d))
-    k, v = W.decode_kv(1, 1, T)
+    k, v = W.decode_kv(1, 1, min(T, 32768), heavy_frac=w.get("heavy_frac", 0.0))
     k, v = k[0, 0].astype(np.float64), v[0, 0].astype(np.float64)
     q = W.query_vectors((g, d), dtype="bf16").astype(np.float64)
 
@@ -501,7 +501,7 @@ def oracle_sample(budget_s):
 
     probe = 2048
     per_token = min(one(probe) for _ in range(3)) / probe
-    tokens = int(max(256, min(T, budget_s / max(per_token, 1e-9))))
+    tokens = int(max(256, min(T, k.shape[0], budget_s / max(per_token, 1e-9))))
     return one, tokens, hkv
 
 
@@ -759,6 +759,231 @@ def run_prefill(args, name):
     return res
 
 
+# ----------------------------------------------------- extra workloads ----
+# Every workload line of the hot path's measurement plan, printed inside the
+# default JSON line (key "workloads") so that one run records all of them.
+EXTRA_DECODE = {
+    "llama8b_decode_32k_k4v4": dict(batch=1, hq=32, hkv=8, d=128, seq_len=32768, rotation="rht", k_bits=4, v_bits=4),
+    "llama8b_decode_32k_dense": dict(batch=1, hq=32, hkv=8, d=128, seq_len=32768, rotation="dense", k_bits=3,
+                                     v_bits=3),
+    **{f"batched_decode_16x8k_k{b}v{b}_{rot}": dict(batch=16, hq=32, hkv=8, d=128, seq_len=8192, rotation=rot,
+                                                    k_bits=b, v_bits=b)
+       for rot in ("rht", "dense") for b in (2, 3, 4)},
+    "long_context_128k": WORKLOADS["long_context_128k"],
+    "llama8b_decode_32k_2p5bit": WORKLOADS["llama8b_decode_32k_2p5bit"],
+    "llama8b_decode_32k_3p5bit": WORKLOADS["llama8b_decode_32k_3p5bit"],
+}
+
+
+def _fill_bytes_per_vector(kc, vc, d):
+    """(K, V) packed bytes per token and KV head as the plan counts them:
+    codes, m = d sign bits and two fp16 norms for K; codes and one fp16 for V."""
+    return kc.code_stride + d // 8 + 4, vc.code_stride + 2
+
+
+def measure_decode(name, w, K, warmup, flush, data, cpu=True):
+    """One decode workload: cache fill (the quantize line), warm-up, K timed
+    steps (tq_decode_step, L2 flushed before each), the scan's own events."""
+    import torch
+    from online_kv_cache_quantize_gb300 import binding as B
+    from online_kv_cache_quantize_gb300 import workloads as W
+
+    L = B.load()
+    bsz, hq, hkv, d, T = w["batch"], w["hq"], w["hkv"], w["d"], w["seq_len"]
+    rows = bsz * hkv
+    key = (bsz, hkv, T, w.get("heavy_frac", 0.0))
+    if key not in data:
+        data.clear()
+        torch.cuda.empty_cache()
+        kx, vx = W.decode_kv(bsz, hkv, T, heavy_frac=w.get("heavy_frac", 0.0))
+        data[key] = (torch.from_numpy(kx.reshape(-1, d)).cuda().to(torch.bfloat16),
+                     torch.from_numpy(vx.reshape(-1, d)).cuda().to(torch.bfloat16))
+        del kx, vx
+    kdev, vdev = data[key]
+    rot = B.tq_rotation_to_device(B.tq_make_rotation(W.ROT_SEED, d, w["rotation"]))
+    qjl = B.tq_qjl_to_device(B.tq_make_qjl(W.QJL_SEED, d, d))
+    kc = B.Cache("prod", w["k_bits"], d, rows=rows, capacity=T, bits2=w.get("k_bits2"))
+    vc = B.Cache("mse", w["v_bits"], d, rows=rows, capacity=T, bits2=w.get("v_bits2"))
+    stream = torch.cuda.current_stream()
+    kb, vb = _fill_bytes_per_vector(kc, vc, d)
+
+    # cache fill = the quantize measurement (K and V of every token)
+    qev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(4)]
+    for i, (a, b) in enumerate(qev):
+        flush.fill_(i & 0xFF)
+        a.record(stream)
+        B.tq_quantize_kv(kc, rot, kdev, qjl=qjl)
+        B.tq_quantize_kv(vc, rot, vdev)
+        b.record(stream)
+    torch.cuda.synchronize()
+    q_ms = statistics.mean(a.elapsed_time(b) for a, b in qev[1:])
+    q_alg = rows * T * (2 * d * 2) + rows * T * (kb + vb)
+
+    q = torch.from_numpy(W.query_vectors((bsz, hq, d), dtype="bf16")).cuda().to(torch.bfloat16)
+    knew = torch.from_numpy(W.query_vectors((rows, d), seed=100)).cuda().to(torch.bfloat16)
+    vnew = torch.from_numpy(W.query_vectors((rows, d), seed=200)).cuda().to(torch.bfloat16)
+    append = torch.full((bsz,), T - 1, dtype=torch.int32, device="cuda")
+    lens = torch.full((bsz,), T, dtype=torch.int32, device="cuda")
+    out = torch.empty((bsz, hq, d), dtype=torch.float32, device="cuda")
+    da, _keep = B._decode_struct(q, kc, vc, lens, T, rot, qjl, out)
+    sa = B.tq_step_args()
+    sa.attn = da
+    sa.k_new, sa.v_new, sa.new_dtype, sa.append_pos = knew.data_ptr(), vnew.data_ptr(), B.TQ_BF16, append.data_ptr()
+    wsz = L.tq_decode_step_workspace(ctypes.byref(sa))
+    wsb = B.workspace(wsz)
+    sp = stream.cuda_stream
+
+    def step():
+        st = L.tq_decode_step(ctypes.byref(sa), wsb.data_ptr(), wsz, sp)
+        if st != 0:
+            raise RuntimeError(f"{name}: {B.status_name(st)} {L.tq_last_error().decode()}")
+
+    for i in range(warmup):
+        flush.fill_(i & 0xFF)
+        step()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a_, b_ in sev:
+        a_.record(stream)
+        b_.record(stream)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        sa.attn.scan_begin = sev[i][0].cuda_event
+        sa.attn.scan_end = sev[i][1].cuda_event
+        step()
+    torch.cuda.synchronize()
+    step_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    scan_s = statistics.mean(a.elapsed_time(b) for a, b in sev) / 1e3
+    peak, peak_kind = _peaks()
+    scan_alg = rows * T * (kb + vb) + bsz * hq * 2 * d * 4
+    achieved = scan_alg / scan_s / 1e9
+    traffic, traffic_how = _traffic("decode_scan", SCAN_SOURCES, name, scan_alg)
+    q_ach = q_alg / (q_ms / 1e3) / 1e9
+    fp16_bytes = rows * T * 2 * d * 2
+    res = {
+        "value": bsz * T / (step_ms / 1e3), "unit": UNIT, "ms_per_step": step_ms, "steps": K, "warmup": warmup,
+        "config": {"workload": name, **{k_: v_ for k_, v_ in w.items()}, "l2": "flushed before every timed step"},
+        "roofline": {"kernel": "decode_mma_kernel (split-K scan)", "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind,
+                     "alg_bytes_per_launch": scan_alg, "avg_launch_us": scan_s * 1e6, "traffic": traffic,
+                     "traffic_source": traffic_how},
+        "quantize": {"vectors_per_s": 2 * rows * T / (q_ms / 1e3), "vectors_per_call": 2 * rows * T,
+                     "ms_per_call": q_ms,
+                     "workload": f"cache fill: K ({_bits(w, 'k')}-bit PROD) and V ({_bits(w, 'v')}-bit MSE), bf16 in",
+                     "roofline": {"bound": "hbm", "achieved": q_ach, "peak": peak, "unit": "GB/s",
+                                  "frac": q_ach / peak, "alg_bytes_per_call": q_alg}},
+        "footprint": {"cache_bytes": rows * T * (kb + vb), "fp16_bytes": fp16_bytes,
+                      "ratio_vs_fp16": fp16_bytes / (rows * T * (kb + vb)),
+                      "bits_per_value": 8.0 * (kb + vb) / (2 * d)},
+        "gpu_launches": 3 * K,
+    }
+    if w["rotation"] == "dense":
+        # the dense rotation's tensor work: 2 d^2 per vector, + 2 m d for keys
+        flops = rows * T * (2.0 * d * d) * 2 + rows * T * (2.0 * d * d)
+        tpeak, tkind = _peaks("bf16_tflops")
+        res["quantize"]["tensor"] = {"alg_flops_per_call": flops, "achieved_tflops": flops / (q_ms / 1e3) / 1e12,
+                                     "peak": tpeak, "frac": flops / (q_ms / 1e3) / 1e12 / tpeak}
+    if cpu:
+        one, tokens, hkv_ = oracle_sample(1.0, w)
+        one(tokens)
+        t = statistics.mean(one(tokens) for _ in range(2))
+        full_s = t * (T / tokens) * hkv_ * bsz
+        res["cpu_baseline"] = {"value": bsz * T / full_s, "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
+                               "kind": "oracle",
+                               "sample": f"2 steps of 1 KV head x {tokens} tokens (quantize + {hq // hkv}-head decode), "
+                                         f"extrapolated to {bsz} x {hkv} KV heads x {T} tokens"}
+        res["quantize"]["cpu_baseline"] = quantize_cpu_baseline(w)
+    del kc, vc
+    return res
+
+
+def quantize_cpu_baseline(w, n=2048):
+    """The oracle's quantize of n keys and n values of the workload's law."""
+    from oracle import quantize as oq
+    from oracle import rng as orng
+    from oracle import rotation as orot
+    from online_kv_cache_quantize_gb300 import workloads as W
+
+    d = w["d"]
+    pi = orot.make_rotation(W.ROT_SEED, d, w["rotation"])
+    sm = orng.round_to_bf16(orng.normals(W.QJL_SEED, d * d).reshape(d, d))
+    k, v = W.decode_kv(1, 1, n)
+    t0 = time.perf_counter()
+    oq.quantize(k[0, 0].astype(np.float64), pi, "prod", w["k_bits"], sm, bits2=w.get("k_bits2"))
+    oq.quantize(v[0, 0].astype(np.float64), pi, "mse", w["v_bits"], bits2=w.get("v_bits2"))
+    dt = time.perf_counter() - t0
+    return {"value": 2 * n / dt, "unit": "vectors/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"{n} keys + {n} values of the workload's law"}
+
+
+def search_cpu_baseline(mode, bits, rows=100_000, nq=20):
+    """The oracle's scoring + top-10 of nq queries over a `rows`-row slice of
+    the database (quantized by the oracle untimed), extrapolated to the full
+    search by rows and queries."""
+    from oracle import quantize as oq
+    from oracle import rng as orng
+    from oracle import rotation as orot
+    from oracle import topk as otk
+    from online_kv_cache_quantize_gb300 import workloads as W
+
+    d = SEARCH["d"]
+    db, qs = W.mixture_vectors(rows, d=d, queries=nq)
+    pi = orot.make_rotation(W.ROT_SEED, d, SEARCH["rotation"])
+    sm = orng.round_to_bf16(orng.normals(W.QJL_SEED, d * d).reshape(d, d)) if mode == "prod" else None
+    qz = oq.quantize(db.astype(np.float64), pi, mode, bits, sm)
+    t0 = time.perf_counter()
+    sc = otk.scores(qs.astype(np.float64), pi, sm, qz["idx"], qz["norm16"], qz["centroids"],
+                    qz.get("rnorm16"), qz.get("z") if mode == "prod" else None)
+    otk.topk(sc, SEARCH["k"])
+    dt = time.perf_counter() - t0
+    full = dt * (SEARCH["n_db"] / rows) * (SEARCH["nq"] / nq)
+    return {"value": SEARCH["nq"] / full, "unit": "queries/s", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle", "sample": f"{nq} queries x {rows} database rows, extrapolated to "
+                                        f"{SEARCH['nq']} x {SEARCH['n_db']}"}
+
+
+def run_extra(args):
+    """Every other workload line, each with its roofline and its oracle
+    baseline on the host cores (bounded samples)."""
+    import torch
+
+    out = {}
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    data = {}
+    K = max(3, min(args.steps, 20))
+    for name, w in EXTRA_DECODE.items():
+        try:
+            out[name] = measure_decode(name, w, K, max(3, args.warmup), flush, data, cpu=not args.no_cpu_baseline)
+        except Exception as e:  # noqa: BLE001 - one failing line must not hide the others
+            out[name] = {"error": f"{type(e).__name__}: {e}"}
+    data.clear()
+    # the prefill quantize of the batched workload: 16 x 8 x 8192 K and V
+    for name in ("batched_decode_16x8k_k3v3_rht", "batched_decode_16x8k_k3v3_dense"):
+        if "quantize" in out.get(name, {}):
+            q = dict(out[name]["quantize"])
+            q["workload"] = "prefill quantize-on-append of 16 x 8 KV heads x 8192 tokens, K and V (2,097,152 vectors)"
+            out["prefill_quantize_16x8x8k_" + name.rsplit("_", 1)[1]] = q
+    for tag in ("prod2", "prod4"):
+        try:
+            r = run_search(args, tag[:-1], int(tag[-1]))
+            if not args.no_cpu_baseline:
+                r["cpu_baseline"] = search_cpu_baseline(tag[:-1], int(tag[-1]))
+            out["vector_search_1m_" + tag] = r
+        except Exception as e:  # noqa: BLE001
+            out["vector_search_1m_" + tag] = {"error": f"{type(e).__name__}: {e}"}
+    try:
+        out["llama8b_prefill_512_at_32k"] = run_prefill(args, "llama8b_prefill_512_at_32k")
+    except Exception as e:  # noqa: BLE001
+        out["llama8b_prefill_512_at_32k"] = {"error": f"{type(e).__name__}: {e}"}
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -768,6 +993,8 @@ def main():
                     help="extra time-based warm-up after the --warmup steps (reported as warmup_extra_steps)")
     ap.add_argument("--impl", choices=["tq", "reference"], default="tq")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="only the default decode line (skip the other workload lines)")
     ap.add_argument("--quick", action="store_true", help="short run for profiling: no clock window, no oracle timing")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama8b_decode_32k")
     ap.add_argument("--k-bits", type=int, default=None)
@@ -821,6 +1048,8 @@ def main():
             res["cpu_baseline"] = cpu_baseline_default()
         else:
             res["cpu_baseline"] = None
+        if ws == 1 and not (args.quick or args.no_extra):
+            res["workloads"] = run_extra(args)
         print(json.dumps(res), flush=True)
 
 

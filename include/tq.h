@@ -376,6 +376,11 @@ tq_status tq_score_topk(const tq_topk_args* a, void* workspace, size_t ws_bytes,
 /* Process-wide switch: on != 0 makes tq_score_topk use the SIMT scan for
  * every shape (to compare the two); returns the previous setting. */
 int tq_topk_force_simt(int on);
+/* Process-wide switch: on != 0 makes tq_quantize_kv use the mma.sync kernel
+ * for bf16 input at d = 128 (where it would take the tcgen05 kernel), to
+ * compare the two; returns the previous setting. Both give the same codes,
+ * norms and signs (the exact fp64 decision near every boundary). */
+int tq_quantize_force_mma_sync(int on);
 
 /* ------------------------------------------------------------------------ *
  * Device error word.                                                       *

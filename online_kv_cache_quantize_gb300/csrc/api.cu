@@ -291,6 +291,19 @@ uint16_t bf16_bits_of(double exact_bf16_value) {
     return (uint16_t)(u >> 16);
 }
 
+// A 128 x 128 bf16 operand of tcgen05.mma in the no-swizzle K-major
+// core-matrix layout: element (n, k) at byte (n/8)*2048 + (k/8)*128 +
+// (n%8)*16 + (k%8)*2 (8 x 16-byte core matrices, LBO 128 along K, SBO 2048
+// along N).
+template <typename F>
+std::vector<uint16_t> umma_operand_128(F bits) {
+    std::vector<uint16_t> out((size_t)128 * 128);
+    for (int n = 0; n < 128; ++n)
+        for (int k = 0; k < 128; ++k)
+            out[(size_t)((n >> 3) * 2048 + (k >> 3) * 128 + (n & 7) * 16) / 2 + (k & 7)] = bits(n, k);
+    return out;
+}
+
 }  // namespace
 
 namespace {
@@ -305,10 +318,16 @@ bool g_topk_simt = false;
 // one warp working through a serial chain per tile.
 constexpr int64_t kSmallAppend = 256;
 
+// tq_quantize_kv may take the tcgen05 kernel (tq_quantize_force_mma_sync
+// turns it off, for comparing the two kernels)
+bool g_quant_umma = true;
+
 struct QuantLaunch {
     tqk::QuantParams p;
     int dtype = 0, vpl = 1, cb = 1;
-    bool rht = false, prod = false, mma = false, small = false;
+    bool rht = false, prod = false, mma = false, small = false, umma = false;
+    const void* w_umma = nullptr;
+    const void* s_umma = nullptr;
 };
 
 // the append role of the step-prep launch for one quantize call
@@ -416,6 +435,14 @@ tq_status quant_prepare(const tq_quant_args* a, QuantLaunch* L, bool* empty) {
                         aligned(a->x, 16) && (a->x_stride * (int64_t)esz) % 16 == 0;
     L->small = c.d == 128 && (!prod || c.m == 128) && (a->n <= kSmallAppend || (p.code_bits2 != 0 && !mma_ok));
     L->mma = !L->small && mma_ok;
+    // bf16 input at one code width: the tcgen05 kernel
+    L->w_umma = a->rot->d_w_umma;
+    L->s_umma = prod ? a->qjl->d_s_umma : nullptr;
+    L->umma = L->mma && g_quant_umma && L->w_umma && (!prod || L->s_umma) &&
+              tqk::quantize_umma_supported(p, L->dtype, cb);
+    // the tensor-core rotation (both kinds) rounds only in its fp32
+    // accumulation, like the dense three-limb product: the same guard band
+    if (L->umma) p.guard = (float)(3.0e-8 * c.d);
     return TQ_OK;
 }
 
@@ -426,6 +453,7 @@ cudaError_t quant_launch(const QuantLaunch& L, cudaStream_t st) {
         step_append(L, &sp);
         return tqk::launch_step_prep(sp, st);
     }
+    if (L.umma) return tqk::launch_quantize_umma(L.p, L.w_umma, L.s_umma, L.rht ? 1 : 0, L.prod ? 1 : 0, L.cb, st);
     if (L.mma && L.p.code_bits2)
         return tqk::launch_quantize_mma2(L.p, L.dtype, L.rht ? 1 : 0, L.prod ? 1 : 0, L.cb, st);
     if (L.mma) return tqk::launch_quantize_mma(L.p, L.dtype, L.rht ? 1 : 0, L.prod ? 1 : 0, L.cb, st);
@@ -613,6 +641,19 @@ tq_status tq_rotation_to_device(tq_rotation* rot) {
             frag.insert(frag.end(), f.begin(), f.end());
         }
         if ((s = upload(&rot->d_pi_frag, frag)) != TQ_OK) return s;
+        std::vector<uint16_t> w;
+        for (const std::vector<double>* l : {&l1, &l2, &l3}) {
+            auto t = umma_operand_128([&](int n, int k) { return bf16_bits_of((*l)[(size_t)n * d + k]); });
+            w.insert(w.end(), t.begin(), t.end());
+        }
+        if ((s = upload(&rot->d_w_umma, w)) != TQ_OK) return s;
+    }
+    if (d == 128 && rot->kind == TQ_ROT_RHT) {
+        // sqrt(d) Pi = H diag(s): every entry +-1, exact in bf16
+        auto w = umma_operand_128([&](int n, int k) {
+            return bf16_bits_of(rot->pi[(size_t)n * d + k] > 0.0 ? 1.0 : -1.0);
+        });
+        if ((s = upload(&rot->d_w_umma, w)) != TQ_OK) return s;
     }
     rot->device = dev;
     return TQ_OK;
@@ -629,6 +670,7 @@ tq_status tq_free_rotation(tq_rotation* rot) {
         cudaFree(rot->d_pi64);
         cudaFree(rot->d_sign);
         cudaFree(rot->d_pi_frag);
+        cudaFree(rot->d_w_umma);
         if (cur >= 0) cudaSetDevice(cur);
     }
     delete rot;
@@ -661,6 +703,8 @@ tq_status tq_qjl_to_device(tq_qjl* q) {
         if ((s = upload(&q->d_s16, s16)) != TQ_OK) return s;
         auto frag = mma_b_fragments([&](int o, int k) { return bf16_bits_of(q->s[(size_t)o * d + k]); });
         if ((s = upload(&q->d_s_frag, frag)) != TQ_OK) return s;
+        auto su = umma_operand_128([&](int j, int k) { return bf16_bits_of(q->s[(size_t)j * d + k]); });
+        if ((s = upload(&q->d_s_umma, su)) != TQ_OK) return s;
     }
     q->device = dev;
     return TQ_OK;
@@ -676,6 +720,7 @@ tq_status tq_free_qjl(tq_qjl* q) {
         cudaFree(q->d_s32);
         cudaFree(q->d_s16);
         cudaFree(q->d_s_frag);
+        cudaFree(q->d_s_umma);
         if (cur >= 0) cudaSetDevice(cur);
     }
     delete q;
@@ -812,6 +857,12 @@ tq_status tq_score_topk(const tq_topk_args* a, void* workspace, size_t ws_bytes,
 int tq_topk_force_simt(int on) {
     const int prev = g_topk_simt ? 1 : 0;
     g_topk_simt = on != 0;
+    return prev;
+}
+
+int tq_quantize_force_mma_sync(int on) {
+    const int prev = g_quant_umma ? 0 : 1;
+    g_quant_umma = on == 0;
     return prev;
 }
 

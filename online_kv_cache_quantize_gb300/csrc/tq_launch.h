@@ -56,6 +56,13 @@ cudaError_t launch_quantize_mma(const QuantParams& p, int dtype, int rht, int pr
 // p.code_bits2 = code_bits - 1 for the others
 cudaError_t launch_quantize_mma2(const QuantParams& p, int dtype, int rht, int prod, int code_bits, cudaStream_t s);
 
+// tcgen05 quantize (d = m = 128, bf16 input with 16-byte aligned rows, one
+// code width): w_umma / s_umma are the rotation and S operands in the
+// core-matrix layout (tq_rotation::d_w_umma, tq_qjl::d_s_umma)
+bool quantize_umma_supported(const QuantParams& p, int dtype, int code_bits);
+cudaError_t launch_quantize_umma(const QuantParams& p, const void* w_umma, const void* s_umma, int rht, int prod,
+                                 int code_bits, cudaStream_t s);
+
 // dtype: 0 f32, 1 bf16, 2 f16. rht: 0 dense, 1 RHT. prod: 0 MSE, 1 PROD.
 cudaError_t launch_quantize(const QuantParams& p, int dtype, int rht, int prod, int code_bits,
                             cudaStream_t s);

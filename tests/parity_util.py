@@ -94,7 +94,9 @@ def compare_quantized(got, qz, mode, bits, d, s_matrix=None, label="", bits2=Non
     exempt = []
     for r, i in np.argwhere(mism):
         y = float(qz["y"][r, i])
-        tj = float(t[np.argmin(np.abs(y - t))])
+        trow = t[i] if t.ndim == 2 else t  # a two-group cache has a table per coordinate (NaN-padded)
+        trow = trow[np.isfinite(trow)]
+        tj = float(trow[np.argmin(np.abs(y - trow))])
         exempt.append((int(r), int(i), y, tj, int(gidx[r, i]), int(qz["idx"][r, i])))
         print(f"{label}: exempt code mismatch row {r} coord {i}: y = {y!r}, boundary {tj!r}, "
               f"|y - t| = {abs(y - tj):.3e}, code gpu {gidx[r, i]} / oracle {qz['idx'][r, i]}")

@@ -1,0 +1,169 @@
+"""GPU parity of the tcgen05 quantize kernel (bf16 input, d = 128) against the
+fp64 oracle, through the C ABI: every code width of keys and values, both
+rotations, ragged sizes over one and many tiles (and the persistent loop over
+more tiles than SMs), strided input rows, the three slot modes, bf16 edge
+vectors, and agreement with the mma.sync kernel it replaces."""
+
+import numpy as np
+import pytest
+import torch
+
+import parity_util as P
+from oracle import quantize as oq
+from online_kv_cache_quantize_gb300 import binding as B
+from online_kv_cache_quantize_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from online_kv_cache_quantize_gb300 import build
+    build.build()
+
+
+def _oracle(xb, mode, bits, kind):
+    pi, s = P.oracle_mats(128, kind, None)
+    return oq.quantize(xb.astype(np.float64), pi, mode, bits, s if mode == "prod" else None), s
+
+
+def _run(x, mode, bits, kind, label):
+    xb = W.round_bf16(np.asarray(x, dtype=np.float32))
+    cache = P.gpu_quantize(xb, mode, bits, 128, kind, dtype=torch.bfloat16)
+    got = P.cache_to_numpy(cache, xb.shape[0])
+    qz, s = _oracle(xb, mode, bits, kind)
+    return P.compare_quantized(got, qz, mode, bits, 128, s, label=label)
+
+
+@pytest.mark.parametrize("kind", ["rht", "dense"])
+@pytest.mark.parametrize("mode,bits", [("prod", 2), ("prod", 3), ("prod", 4),
+                                       ("mse", 1), ("mse", 2), ("mse", 3), ("mse", 4)])
+def test_every_width_ragged_tiles(kind, mode, bits):
+    """2 KV heads x 1000 tokens of the decode law (outlier channels, LogNormal
+    token scale, 1 % heavy tokens): 2000 vectors = 15 full tiles + a tail of 80."""
+    k, v = W.decode_kv(1, 2, 1000, heavy_frac=0.01)
+    x = (k if mode == "prod" else v).reshape(-1, 128)
+    rep = _run(x, mode, bits, kind, f"umma-{kind}-{mode}{bits}")
+    assert rep["code_mismatch"] <= 1e-5 * rep["coords"] + 1
+
+
+@pytest.mark.parametrize("n", [257, 300, 384, 511])
+def test_small_counts_one_to_four_tiles(n):
+    x = np.random.default_rng(n).standard_normal((n, 128)).astype(np.float32) * 3
+    _run(x, "prod", 3, "rht", f"umma-n{n}")
+    _run(x, "mse", 3, "dense", f"umma-n{n}-dense")
+
+
+@pytest.mark.parametrize("kind", ["rht", "dense"])
+def test_persistent_loop_more_tiles_than_sms(kind):
+    """2 x 152 x 128 + 77 vectors: each CTA walks several tiles through both
+    TMEM buffers and both input buffers (every barrier phase is reused)."""
+    n = 2 * 152 * 128 + 77
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((n, 128)).astype(np.float32) * rng.lognormal(0, 0.5, (n, 1)).astype(np.float32)
+    for mode, bits in (("prod", 3), ("mse", 3)):
+        rep = _run(x, mode, bits, kind, f"umma-persistent-{kind}-{mode}{bits}")
+        assert rep["code_mismatch"] <= 1e-5 * rep["coords"] + 1
+
+
+def test_bf16_edge_vectors():
+    """Zero vectors, a saturating norm, one-hot rows, tiny values, and norms
+    that are exact fp16 rounding midpoints (subnormal and normal range) in a
+    tile of 300 rows, most of them ordinary."""
+    d, n = 128, 300
+    x = W.round_bf16(np.random.default_rng(8).standard_normal((n, d)).astype(np.float32))
+    x[3] = 0.0
+    x[4] = 8192.0                               # norm 9.27e4 -> fp16 saturates to 65504
+    x[5] = 0.0
+    x[5, 9] = 1.0                               # one-hot
+    x[6] = 2.0 ** -100                          # squares underflow fp32: the norm in fp64
+    x[7] = -2.0
+    planted = {10: [(5, 3 * 2.0 ** -25)],       # 3 * 2^-25: halfway between fp16 subnormals 2^-24 and 2^-23
+               11: [(20, 3 * 2.0 ** -25), (90, 4 * 2.0 ** -25)],   # norm 5 * 2^-25, a midpoint
+               12: [(30, 65.0), (31, -2112.0)],                     # norm 2113: halfway between 2112 and 2114
+               13: [(0, 79.0), (127, 3120.0)]}                      # norm 3121
+    for r, entries in planted.items():
+        x[r] = 0.0
+        for i, val in entries:
+            x[r, i] = val
+    assert np.array_equal(W.round_bf16(x), x)
+    for kind in ("rht", "dense"):
+        for mode, bits in (("prod", 3), ("mse", 4), ("prod", 2)):
+            cache = P.gpu_quantize(x, mode, bits, d, kind, dtype=torch.bfloat16)
+            got = P.cache_to_numpy(cache, n)
+            qz, s = _oracle(x, mode, bits, kind)
+            rows = np.array(sorted(planted))
+            assert np.array_equal(got["norm"][rows], qz["norm16"][rows]), f"{kind} {mode}{bits}: midpoint norms"
+            assert got["norm"][4] == 65504.0
+            P.compare_quantized(got, qz, mode, bits, d, s, label=f"umma-edge-{kind}-{mode}{bits}")
+
+
+def test_strided_rows_and_slot_modes():
+    """Input rows with a 192-element stride; dst_slot scatter (with skipped
+    slots) and append_pos, compared with the contiguous call."""
+    d, n = 128, 700
+    rot, qjl = P.handles(d, "rht")
+    rng = np.random.default_rng(21)
+    x = W.round_bf16(rng.standard_normal((n, d)).astype(np.float32))
+    wide = torch.zeros((n, 192), dtype=torch.bfloat16, device="cuda")
+    wide[:, 32:32 + d] = torch.from_numpy(x).cuda().to(torch.bfloat16)
+    xs = wide[:, 32:32 + d]  # stride 192, 64-byte aligned rows
+    ref = B.Cache("prod", 3, d, rows=1, capacity=n)
+    B.tq_quantize_kv(ref, rot, torch.from_numpy(x).cuda().to(torch.bfloat16), qjl=qjl)
+    got = B.Cache("prod", 3, d, rows=1, capacity=n)
+    B.tq_quantize_kv(got, rot, xs, qjl=qjl)
+    torch.cuda.synchronize()
+    for plane in ("codes", "signs", "norm", "rnorm"):
+        assert torch.equal(getattr(got, plane), getattr(ref, plane)), plane
+    # scatter: slot i -> (7 i) mod cap, every 10th vector skipped (-1), one past the end
+    cap = 7 * n + 3
+    dst = (7 * torch.arange(n, dtype=torch.int64, device="cuda")) % cap
+    dst[::10] = -1
+    dst[1] = cap + 5
+    sc = B.Cache("prod", 3, d, rows=1, capacity=cap)
+    B.tq_quantize_kv(sc, rot, xs, qjl=qjl, dst_slot=dst)
+    torch.cuda.synchronize()
+    keep = (dst >= 0) & (dst < cap)
+    idx = torch.nonzero(keep).flatten()
+    for plane in ("codes", "signs", "norm", "rnorm"):
+        assert torch.equal(getattr(sc, plane)[dst[idx]], getattr(ref, plane)[idx]), plane
+    untouched = torch.ones(cap, dtype=torch.bool, device="cuda")
+    untouched[dst[idx]] = False
+    assert int(sc.codes[untouched].abs().sum()) == 0 and int(sc.norm[untouched].abs().sum()) == 0
+    # append: 350 batch rows x 2 heads, one position per batch row
+    heads, cap2 = 2, 48
+    pos = torch.from_numpy(rng.integers(0, cap2, n // heads).astype(np.int32)).cuda()
+    pos[3] = -1  # skipped
+    ac = B.Cache("prod", 3, d, rows=n, capacity=cap2)
+    B.tq_quantize_kv(ac, rot, xs, qjl=qjl, append_pos=pos, heads=heads)
+    torch.cuda.synchronize()
+    v = torch.arange(n, device="cuda")
+    pv = pos[v // heads].long()
+    ok = pv >= 0
+    slots = v[ok] * cap2 + pv[ok]
+    for plane in ("codes", "signs", "norm", "rnorm"):
+        assert torch.equal(getattr(ac, plane)[slots], getattr(ref, plane)[v[ok]]), plane
+
+
+@pytest.mark.parametrize("kind", ["rht", "dense"])
+def test_agrees_with_the_mma_sync_kernel(kind):
+    """The tcgen05 and mma.sync kernels both decide every code and norm as the
+    fp64 oracle does (a coordinate near a boundary is re-decided in fp64 by
+    each), so codes and norms are identical; gamma and the signs come from
+    fp32 residuals summed in different orders and may differ only inside
+    their parity windows (checked against the oracle for both)."""
+    k, _ = W.decode_kv(1, 4, 1024)
+    x = W.round_bf16(k.reshape(-1, 128))
+    lib = B.load()
+    prev = lib.tq_quantize_force_mma_sync(1)
+    try:
+        old = P.gpu_quantize(x, "prod", 3, 128, kind, dtype=torch.bfloat16)
+    finally:
+        lib.tq_quantize_force_mma_sync(prev)
+    new = P.gpu_quantize(x, "prod", 3, 128, kind, dtype=torch.bfloat16)
+    assert torch.equal(new.codes, old.codes)
+    assert torch.equal(new.norm, old.norm)
+    qz, s = _oracle(x, "prod", 3, kind)
+    for c, lab in ((old, "mma.sync"), (new, "tcgen05")):
+        P.compare_quantized(P.cache_to_numpy(c, x.shape[0]), qz, "prod", 3, 128, s, label=f"{lab}-{kind}")
+    assert float((new.signs != old.signs).float().mean()) < 1e-3
