@@ -16,7 +16,9 @@ float64 NumPy, following the steps in the order the write-ups describe them:
   sketch of the residual;
 * attention - logits from the codes (pre-rotated query), exact softmax, value
   sum in the rotated domain, one un-rotation;
-* topk      - inner-product search scored from the codes.
+* topk      - inner-product search scored from the codes;
+* polar     - the PolarQuant variant of the key quantizer (recursive polar
+  transform of the rotated vector, one Lloyd-Max angle codebook per level).
 
 It shares no code with the CUDA path; the two meet only through seeded inputs
 built by ``online_kv_cache_quantize_gb300.workloads`` (which holds none of the
@@ -26,4 +28,4 @@ sides implement independently.
 Parity status of each function is stated in its module docstring.
 """
 
-from . import rng, rotation, codebook, quantize, attention, topk, footprint  # noqa: F401
+from . import rng, rotation, codebook, quantize, attention, topk, footprint, polar  # noqa: F401
