@@ -291,16 +291,19 @@ uint16_t bf16_bits_of(double exact_bf16_value) {
     return (uint16_t)(u >> 16);
 }
 
-// A 128 x 128 bf16 operand of tcgen05.mma in the no-swizzle K-major
-// core-matrix layout: element (n, k) at byte (n/8)*2048 + (k/8)*128 +
-// (n%8)*16 + (k%8)*2 (8 x 16-byte core matrices, LBO 128 along K, SBO 2048
-// along N).
+// A 128 x 128 bf16 operand of tcgen05.mma, K-major with the 128-byte
+// swizzle: two halves of 64 elements along K (16 KB each), row n of a half
+// at n * 128 bytes, its 16-byte chunk j (elements 8j .. 8j+7) stored at chunk
+// j ^ (n % 8); 8-row atoms of 1024 bytes.
 template <typename F>
 std::vector<uint16_t> umma_operand_128(F bits) {
     std::vector<uint16_t> out((size_t)128 * 128);
     for (int n = 0; n < 128; ++n)
-        for (int k = 0; k < 128; ++k)
-            out[(size_t)((n >> 3) * 2048 + (k >> 3) * 128 + (n & 7) * 16) / 2 + (k & 7)] = bits(n, k);
+        for (int k = 0; k < 128; ++k) {
+            const int half = k >> 6, kk = k & 63;
+            const size_t byte = (size_t)half * 16384 + (size_t)n * 128 + (size_t)(((kk >> 3) ^ (n & 7)) << 4) + (kk & 7) * 2;
+            out[byte / 2] = bits(n, k);
+        }
     return out;
 }
 
@@ -440,9 +443,12 @@ tq_status quant_prepare(const tq_quant_args* a, QuantLaunch* L, bool* empty) {
     L->s_umma = prod ? a->qjl->d_s_umma : nullptr;
     L->umma = L->mma && g_quant_umma && L->w_umma && (!prod || L->s_umma) &&
               tqk::quantize_umma_supported(p, L->dtype, cb);
-    // the tensor-core rotation (both kinds) rounds only in its fp32
-    // accumulation, like the dense three-limb product: the same guard band
-    if (L->umma) p.guard = (float)(3.0e-8 * c.d);
+    // The tensor-core rotation rounds only in its fp32 accumulation (8 steps
+    // of 16 exact products for RHT; 24 with the dense limbs, whose split
+    // itself is good to 2^-25 of each entry): at most about one fp32 ulp of
+    // the largest partial sum per step, under 1e-6 of the unit vector for
+    // RHT and 1.5e-6 dense. The guard bands sit above those bounds.
+    if (L->umma) p.guard = rht ? 1.2e-6f : 2.0e-6f;
     return TQ_OK;
 }
 

@@ -29,6 +29,21 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t smem_addr, uint32_t lbo, 
     return d;
 }
 
+// Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 128
+// bytes (64 bf16 along K), 8-row atoms of 1024 bytes (SBO between atoms), the
+// 16-byte chunk c of row r stored at chunk c ^ (r % 8) (the layout a TMA copy
+// with CU_TENSOR_MAP_SWIZZLE_128B writes). The atoms must be 1024-byte
+// aligned; a K = 16 step inside the 128-byte row moves the start by 32 bytes.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);  // start address / 16
+    d |= (uint64_t)1u << 16;                      // leading byte offset: unused for swizzled K-major
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;  // stride byte offset / 16
+    d |= (uint64_t)1u << 46;                      // descriptor version 1
+    d |= (uint64_t)2u << 61;                      // layout type: 128-byte swizzle
+    return d;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32, A and B fp16,
 // both K-major, dense, M x N.
 __host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N) {
@@ -144,6 +159,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
         "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
         "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
         "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31]));
+}
+
+// 16 consecutive 32-bit columns of this warp's lane quarter, written
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]));
 }
 
 // 2-D tiled TMA load of the box at (x, y) (x: innermost, in elements) of the

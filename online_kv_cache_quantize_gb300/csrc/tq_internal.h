@@ -26,8 +26,8 @@ struct tq_rotation {
     float* d_sign = nullptr;    // RHT signs fp32 (d)
     uint2v* d_pi_frag = nullptr;  // d = 128 dense: 3 bf16 limbs of Pi^T in mma fragment order
     // d = 128: the tcgen05 quantize kernel's rotation operand W (y = W x / n,
-    // scaled by 1/sqrt(d) for RHT) as bf16 128 x 128 tiles in the no-swizzle
-    // K-major core-matrix layout: 3 limbs of Pi (dense), H diag(s) (RHT, +-1)
+    // scaled by 1/sqrt(d) for RHT) as bf16 128 x 128 tiles in the K-major
+    // 128-byte-swizzled layout: 3 limbs of Pi (dense), H diag(s) (RHT, +-1)
     uint16_t* d_w_umma = nullptr;
 };
 
@@ -41,7 +41,7 @@ struct tq_qjl {
     float* d_s32 = nullptr;     // S row-major fp32 [m][d]
     uint16_t* d_s16 = nullptr;  // m = d = 128: S as bf16 bits (exact), 16-byte unit (q, j) = S[j][8q .. 8q+7] at q * 128 + j
     uint2v* d_s_frag = nullptr;   // m = d = 128: S (exact bf16) in mma fragment order
-    uint16_t* d_s_umma = nullptr; // m = d = 128: S as a bf16 tcgen05 operand (core-matrix layout)
+    uint16_t* d_s_umma = nullptr; // m = d = 128: S as a bf16 tcgen05 operand (128-byte-swizzled layout)
 };
 
 namespace tq {
