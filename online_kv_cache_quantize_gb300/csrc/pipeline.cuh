@@ -103,25 +103,4 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     return true;
 }
 
-// As mbar_wait_bounded, for a producer thread that runs ahead of its
-// consumers and may wait long (a TMA or MMA issuing thread): between checks
-// it sleeps (32 ns doubling to 256 ns) instead of polling, so that the warps
-// sharing its scheduler keep their issue slots; it notices completion at most
-// one sleep late.
-__device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity, uint64_t limit_ns, uint32_t* err,
-                                                  uint32_t code) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    uint32_t ns = 32;
-    while (!mbar_try_wait(bar, parity)) {
-        __nanosleep(ns);
-        ns = ns < 256 ? 2 * ns : 256;
-        if (global_ns() - t0 > limit_ns) {
-            if (err) atomicOr(err, code);
-            return false;
-        }
-    }
-    return true;
-}
-
 }  // namespace tqk

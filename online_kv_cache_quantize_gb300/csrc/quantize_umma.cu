@@ -128,7 +128,9 @@ __global__ void __launch_bounds__(QuCfg<NP>::kThreads, 1)
     const QuantParams& p = P.q;
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    // 1024-byte aligned start (the swizzle atoms), derived from smem_raw so
+    // that the compiler keeps the shared address space (plain shared loads)
+    unsigned char* smem = smem_raw + ((1024u - ((uint32_t)__cvta_generic_to_shared(smem_raw) & 1023u)) & 1023u);
     unsigned char* sB1 = smem;                                  // NL x [128 x 128] rotation operand
     unsigned char* sB2 = sB1 + (size_t)NL * kQuBBytes;          // S (keys)
     unsigned char* sX = sB2 + (PROD ? kQuBBytes : 0);           // input tiles
@@ -211,7 +213,7 @@ __global__ void __launch_bounds__(QuCfg<NP>::kThreads, 1)
             for (int64_t it = 0; it < nmine; ++it) {
                 const int xb = (int)(it % kQuXBufs);
                 if (it >= kQuXBufs &&
-                    !mbar_wait_backoff(xfree0 + 8 * xb, (uint32_t)(((it / kQuXBufs) - 1) & 1), kWaitLimitNs, p.err,
+                    !mbar_wait_bounded(xfree0 + 8 * xb, (uint32_t)(((it / kQuXBufs) - 1) & 1), kWaitLimitNs, p.err,
                                        kErrQuantWait)) {
                     *abort_flag = 1;
                     break;
@@ -227,14 +229,14 @@ __global__ void __launch_bounds__(QuCfg<NP>::kThreads, 1)
             }
             // every copy issued lands (bounded) before the CTA's shared memory is released
             for (int64_t it = issued > kQuXBufs ? issued - kQuXBufs : 0; it < issued; ++it)
-                mbar_wait_backoff(xfull0 + 8 * (int)(it % kQuXBufs), (uint32_t)((it / kQuXBufs) & 1), kWaitLimitNs,
+                mbar_wait_bounded(xfull0 + 8 * (int)(it % kQuXBufs), (uint32_t)((it / kQuXBufs) & 1), kWaitLimitNs,
                                   p.err, kErrQuantWait);
-            mbar_wait_backoff(bfull, 0, kWaitLimitNs, p.err, kErrQuantWait);
+            mbar_wait_bounded(bfull, 0, kWaitLimitNs, p.err, kErrQuantWait);
         }
     } else if (warp == 1) {
         // ======================= MMA =======================
         if (lane == 0) {
-            bool ok = mbar_wait_backoff(bfull, 0, kWaitLimitNs, p.err, kErrQuantWait);
+            bool ok = mbar_wait_bounded(bfull, 0, kWaitLimitNs, p.err, kErrQuantWait);
             const uint32_t idesc = umma_idesc_bf16(kQuVec, kQuD);
             // A = input tile, two 128-byte-swizzled halves of 64 coordinates:
             // element (r, k) at (k/64)*16384 + r*128 + (((k%64)/8) ^ (r%8))*16
@@ -248,11 +250,11 @@ __global__ void __launch_bounds__(QuCfg<NP>::kThreads, 1)
             int64_t last_commit = -1;  // tiles whose last MMA was committed
             auto rot = [&](int64_t it) -> bool {
                 const int xb = (int)(it % kQuXBufs), tb = (int)(it % NB1);
-                if (!mbar_wait_backoff(xfull0 + 8 * xb, (uint32_t)((it / kQuXBufs) & 1), kWaitLimitNs, p.err,
+                if (!mbar_wait_bounded(xfull0 + 8 * xb, (uint32_t)((it / kQuXBufs) & 1), kWaitLimitNs, p.err,
                                        kErrQuantWait))
                     return false;
                 // the epilogue has read this accumulator's previous tile
-                if (it >= NB1 && !mbar_wait_backoff(tfree0 + 8 * tb, (uint32_t)(((it / NB1) - 1) & 1), kWaitLimitNs,
+                if (it >= NB1 && !mbar_wait_bounded(tfree0 + 8 * tb, (uint32_t)(((it / NB1) - 1) & 1), kWaitLimitNs,
                                                     p.err, kErrQuantWait))
                     return false;
                 tc_fence_after_sync();
@@ -271,8 +273,8 @@ __global__ void __launch_bounds__(QuCfg<NP>::kThreads, 1)
             };
             auto sgn = [&](int64_t it) -> bool {
                 // R of this tile written; the S r accumulator read by the previous tile's epilogue
-                if (!mbar_wait_backoff(rfull, (uint32_t)(it & 1), kWaitLimitNs, p.err, kErrQuantWait)) return false;
-                if (it >= 1 && !mbar_wait_backoff(a2free, (uint32_t)((it - 1) & 1), kWaitLimitNs, p.err, kErrQuantWait))
+                if (!mbar_wait_bounded(rfull, (uint32_t)(it & 1), kWaitLimitNs, p.err, kErrQuantWait)) return false;
+                if (it >= 1 && !mbar_wait_bounded(a2free, (uint32_t)((it - 1) & 1), kWaitLimitNs, p.err, kErrQuantWait))
                     return false;
                 tc_fence_after_sync();
                 // R of coordinates 16g .. 16g+15: hi halves in columns 16g .. 16g+7,
@@ -306,10 +308,10 @@ __global__ void __launch_bounds__(QuCfg<NP>::kThreads, 1)
             if (nmine > 0) {
                 if constexpr (PROD) {
                     if (last_commit >= 0)
-                        mbar_wait_backoff(a2full, (uint32_t)(last_commit & 1), kWaitLimitNs, p.err, kErrQuantWait);
+                        mbar_wait_bounded(a2full, (uint32_t)(last_commit & 1), kWaitLimitNs, p.err, kErrQuantWait);
                 } else {
                     const int64_t lt = nmine - 1;
-                    mbar_wait_backoff(a1full0 + 8 * (int)(lt % NB1), (uint32_t)((lt / NB1) & 1), kWaitLimitNs, p.err,
+                    mbar_wait_bounded(a1full0 + 8 * (int)(lt % NB1), (uint32_t)((lt / NB1) & 1), kWaitLimitNs, p.err,
                                       kErrQuantWait);
                 }
             }
