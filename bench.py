@@ -363,14 +363,32 @@ def run_tq(args):
     # host wall clock per step, as a caller sees it: submit the step, wait
     # for its stream, the output is then readable in pinned host memory; no
     # flush or other work in front of it (so host submission is not hidden)
+    h_np = h_out.numpy()  # a host view of the pinned output (the read costs no torch op)
     wall = []
     for i in range(ne):
         h0 = time.perf_counter()
         check(L.tq_decode_step(ctypes.byref(sa_h), wsb.data_ptr(), wsz, sp), "decode step (host buffers)")
         stream.synchronize()
-        _ = float(h_out[0, 0, 0])  # the result, read on the host
+        _ = float(h_np[0, 0, 0])  # the result, read on the host
         wall.append(time.perf_counter() - h0)
     e2e_ms = statistics.mean(wall) * 1e3
+    # the same zero-copy step captured once in a CUDA graph and replayed (how a
+    # serving loop issues a fixed step: one launch instead of three)
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        check(L.tq_decode_step(ctypes.byref(sa_h), wsb.data_ptr(), wsz, torch.cuda.current_stream().cuda_stream),
+              "decode step (graph capture)")
+    torch.cuda.synchronize()
+    wall = []
+    for i in range(ne):
+        h0 = time.perf_counter()
+        graph.replay()
+        stream.synchronize()
+        _ = float(h_np[0, 0, 0])
+        wall.append(time.perf_counter() - h0)
+    e2e_graph_ms = statistics.mean(wall) * 1e3
+    del graph
     # (b) the same with explicit copies: host -> device into the step's
     # device buffers, the step, device -> host of the output
     mev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ne)]
@@ -398,8 +416,8 @@ def run_tq(args):
     d2h = h_out.numel() * h_out.element_size()
 
     # the slowest rank's times
-    total_ms, e2e_ms, e2e_copy_ms, q_ms, e2e_dev_ms, e2e_copy_dev_ms = max_over_ranks(
-        [total_ms, e2e_ms, e2e_copy_ms, q_ms, e2e_dev_ms, e2e_copy_dev_ms], "cuda")
+    total_ms, e2e_ms, e2e_copy_ms, q_ms, e2e_dev_ms, e2e_copy_dev_ms, e2e_graph_ms = max_over_ranks(
+        [total_ms, e2e_ms, e2e_copy_ms, q_ms, e2e_dev_ms, e2e_copy_dev_ms, e2e_graph_ms], "cuda")
     tokens_per_step = bsz * T
     value = job_throughput(ws, tokens_per_step, K, total_ms)
 
@@ -441,6 +459,10 @@ def run_tq(args):
                                 "memory and write the output to pinned host memory (CPU-GPU link inside the kernels)",
                     "device_events": {"value": job_throughput(ws, tokens_per_step, 1, e2e_dev_ms), "unit": UNIT,
                                       "clock": "CUDA events around the step on its stream, L2 flushed before each"},
+                    "graph_replay": {"value": job_throughput(ws, tokens_per_step, 1, e2e_graph_ms), "unit": UNIT,
+                                     "ms_per_step": e2e_graph_ms,
+                                     "clock": "host wall clock, as above, per replay of the step captured once in "
+                                              "a CUDA graph (same zero-copy buffers)"},
                     "with_memcpy": {"value": job_throughput(ws, tokens_per_step, 1, e2e_copy_ms), "unit": UNIT,
                                     "ms_per_step": e2e_copy_ms, "clock": "host wall clock, as above",
                                     "device_events": job_throughput(ws, tokens_per_step, 1, e2e_copy_dev_ms),
@@ -903,6 +925,132 @@ def measure_decode(name, w, K, warmup, flush, data, cpu=True):
     return res
 
 
+POLAR = dict(batch=1, hq=32, hkv=8, d=128, seq_len=32768, rotation="rht", k_bits=4, k_bits2=2, v_bits=3)
+
+
+def measure_polar(name, w, K, warmup, flush, cpu=True):
+    """The PolarQuant comparison variant at the 32k decode shape: its key
+    quantize (vectors/s) and decode attention over PolarQuant keys and MSE
+    values (query prep, polar scan, merge; L2 flushed before each step)."""
+    import torch
+    from online_kv_cache_quantize_gb300 import binding as B
+    from online_kv_cache_quantize_gb300 import workloads as W
+
+    bsz, hq, hkv, d, T = w["batch"], w["hq"], w["hkv"], w["d"], w["seq_len"]
+    rows = bsz * hkv
+    kx, vx = W.decode_kv(bsz, hkv, T)
+    kdev = torch.from_numpy(kx.reshape(-1, d)).cuda().to(torch.bfloat16)
+    vdev = torch.from_numpy(vx.reshape(-1, d)).cuda().to(torch.bfloat16)
+    del kx, vx
+    rot = B.tq_rotation_to_device(B.tq_make_rotation(W.ROT_SEED, d, w["rotation"]))
+    kc = B.Cache("polar", w["k_bits"], d, rows=rows, capacity=T, bits2=w["k_bits2"])
+    vc = B.Cache("mse", w["v_bits"], d, rows=rows, capacity=T)
+    stream = torch.cuda.current_stream()
+    qev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(4)]
+    for i, (a, b) in enumerate(qev):
+        flush.fill_(i & 0xFF)
+        a.record(stream)
+        B.tq_quantize_kv(kc, rot, kdev)
+        b.record(stream)
+    B.tq_quantize_kv(vc, rot, vdev)
+    torch.cuda.synchronize()
+    q_ms = statistics.mean(a.elapsed_time(b) for a, b in qev[1:])
+    kb, vb = kc.code_stride + 2, vc.code_stride + 2
+    q_alg = rows * T * (2 * d + kb)
+
+    q = torch.from_numpy(W.query_vectors((bsz, hq, d), dtype="bf16")).cuda().to(torch.bfloat16)
+    lens = torch.full((bsz,), T, dtype=torch.int32, device="cuda")
+    out = torch.empty((bsz, hq, d), dtype=torch.float32, device="cuda")
+    da, _keep = B._decode_struct(q, kc, vc, lens, T, rot, None, out)
+    L = B.load()
+    wsz = L.tq_attn_decode_workspace(ctypes.byref(da))
+    wsb = B.workspace(wsz)
+    sp = stream.cuda_stream
+
+    def step():
+        st = L.tq_attn_decode(ctypes.byref(da), wsb.data_ptr(), wsz, sp)
+        if st != 0:
+            raise RuntimeError(f"{name}: {B.status_name(st)} {L.tq_last_error().decode()}")
+
+    for i in range(warmup):
+        flush.fill_(i & 0xFF)
+        step()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a_, b_ in sev:
+        a_.record(stream)
+        b_.record(stream)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        da.scan_begin = sev[i][0].cuda_event
+        da.scan_end = sev[i][1].cuda_event
+        step()
+    torch.cuda.synchronize()
+    da.scan_begin = da.scan_end = None
+    step_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    scan_s = statistics.mean(a.elapsed_time(b) for a, b in sev) / 1e3
+    peak, peak_kind = _peaks()
+    scan_alg = rows * T * (kb + vb) + bsz * hq * d * 4
+    achieved = scan_alg / scan_s / 1e9
+    q_ach = q_alg / (q_ms / 1e3) / 1e9
+    fp16_bytes = rows * T * 2 * d * 2
+    res = {
+        "value": bsz * T / (step_ms / 1e3), "unit": UNIT, "ms_per_step": step_ms, "steps": K, "warmup": warmup,
+        "config": {"workload": name, **w, "keys": "PolarQuant (level-1 angles at k_bits, higher levels at k_bits2)",
+                   "step": "decode attention only (query prep, polar scan, merge); the keys are appended by "
+                           "tq_quantize_kv", "l2": "flushed before every timed step"},
+        "roofline": {"kernel": "polar_decode_kernel (split-K scan)", "bound": "hbm", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind,
+                     "alg_bytes_per_launch": scan_alg, "avg_launch_us": scan_s * 1e6, "traffic": None},
+        "quantize": {"vectors_per_s": rows * T / (q_ms / 1e3), "vectors_per_call": rows * T, "ms_per_call": q_ms,
+                     "workload": f"PolarQuant key fill: {rows} KV heads x {T} tokens, bf16 in",
+                     "roofline": {"kernel": "polar_quantize_kernel", "bound": "hbm", "achieved": q_ach, "peak": peak,
+                                  "unit": "GB/s", "frac": q_ach / peak, "alg_bytes_per_call": q_alg}},
+        "footprint": {"cache_bytes": rows * T * (kb + vb), "fp16_bytes": fp16_bytes,
+                      "ratio_vs_fp16": fp16_bytes / (rows * T * (kb + vb))},
+        "gpu_launches": 3 * K,
+    }
+    if cpu:
+        res["cpu_baseline"] = polar_cpu_baseline(w)
+    del kc, vc, kdev, vdev
+    return res
+
+
+def polar_cpu_baseline(w, tokens=4096):
+    """The oracle's PolarQuant decode of one KV head's G query heads over
+    `tokens` tokens (keys and values quantized untimed), extrapolated to the
+    full step."""
+    from oracle import codebook as ocb
+    from oracle import polar as op
+    from oracle import quantize as oq
+    from oracle import rotation as orot
+    from online_kv_cache_quantize_gb300 import workloads as W
+
+    d, T, hkv, hq = w["d"], w["seq_len"], w["hkv"], w["hq"]
+    g = hq // hkv
+    pi = orot.make_rotation(W.ROT_SEED, d, w["rotation"])
+    k, v = W.decode_kv(1, 1, tokens)
+    kq = op.quantize(k[0, 0].astype(np.float64), pi, w["k_bits"], w["k_bits2"])
+    vq = oq.quantize(v[0, 0].astype(np.float64), pi, "mse", w["v_bits"])
+    kc = {"packed": op.pack(kq["idx"], d, w["k_bits"], w["k_bits2"])[None, None], "norm16": kq["norm16"][None, None]}
+    vcache = {"idx": vq["idx"][None, None], "norm16": vq["norm16"][None, None]}
+    q = W.query_vectors((1, g, d), dtype="bf16").astype(np.float64)
+    vcent = ocb.lloyd_max(d, w["v_bits"])[0]
+    t0 = time.perf_counter()
+    op.decode(q, kc, vcache, [tokens], pi, w["k_bits"], w["k_bits2"], vcent)
+    dt = time.perf_counter() - t0
+    full = dt * (T / tokens) * hkv * w["batch"]
+    return {"value": w["batch"] * T / full, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"1 KV head x {tokens} tokens ({g}-head PolarQuant decode), extrapolated to "
+                      f"{w['batch']} x {hkv} KV heads x {T} tokens"}
+
+
 def quantize_cpu_baseline(w, n=2048):
     """The oracle's quantize of n keys and n values of the workload's law."""
     from oracle import quantize as oq
@@ -978,6 +1126,11 @@ def run_extra(args):
         except Exception as e:  # noqa: BLE001
             out["vector_search_1m_" + tag] = {"error": f"{type(e).__name__}: {e}"}
     try:
+        out["polar_decode_32k_k4k2_v3"] = measure_polar("polar_decode_32k_k4k2_v3", POLAR, K, max(3, args.warmup), flush,
+                                                        cpu=not args.no_cpu_baseline)
+    except Exception as e:  # noqa: BLE001
+        out["polar_decode_32k_k4k2_v3"] = {"error": f"{type(e).__name__}: {e}"}
+    try:
         out["llama8b_prefill_512_at_32k"] = run_prefill(args, "llama8b_prefill_512_at_32k")
     except Exception as e:  # noqa: BLE001
         out["llama8b_prefill_512_at_32k"] = {"error": f"{type(e).__name__}: {e}"}
@@ -1007,6 +1160,8 @@ def main():
     ap.add_argument("--prefill", choices=sorted(PREFILL), default=None,
                     help="time chunked-prefill attention instead of the decode step")
     ap.add_argument("--prefill-context", type=int, default=None, help="context length (smaller case for profiling)")
+    ap.add_argument("--polar", action="store_true",
+                    help="time only the PolarQuant line (key quantize and decode over PolarQuant keys)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -1035,6 +1190,16 @@ def main():
         if args.prefill_context:
             PREFILL[args.prefill]["context"] = args.prefill_context
         print(json.dumps(run_prefill(args, args.prefill)), flush=True)
+        return
+    if args.polar:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the PolarQuant line has no reference arm here; "
+                              "its oracle parity is in tests/test_gpu_polar.py"}))
+            return
+        import torch
+        flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        print(json.dumps(measure_polar("polar_decode_32k_k4k2_v3", POLAR, max(3, args.steps), args.warmup, flush,
+                                       cpu=not (args.no_cpu_baseline or args.quick))), flush=True)
         return
     if args.impl == "reference":
         res = run_reference(args)

@@ -52,7 +52,7 @@ typedef enum {
 } tq_status;
 
 typedef enum { TQ_ROT_DENSE_QR = 0, TQ_ROT_RHT = 1 } tq_rot_kind;
-typedef enum { TQ_MSE = 0, TQ_PROD = 1 } tq_mode;
+typedef enum { TQ_MSE = 0, TQ_PROD = 1, TQ_POLAR = 2 } tq_mode;
 typedef enum { TQ_F32 = 0, TQ_BF16 = 1, TQ_F16 = 2 } tq_dtype;
 
 typedef struct tq_rotation tq_rotation;
@@ -161,6 +161,36 @@ typedef struct {
     int bits2;        /* 0: every coordinate at `bits`; else the second
                          channel group's bits (fractional rates, see above)  */
 } tq_cache;
+
+/* PolarQuant keys (mode TQ_POLAR; the comparison variant of [DS]
+ * "PolarQuant" and [A2A] "Stage 1" PolarQuant bullets): y = Pi x / ||x||
+ * (the same rotation as the other modes) is taken to polar coordinates by a
+ * recursion over pairs: level 1 pairs (y_2i, y_2i+1) into a radius
+ * rho_1,i = hypot and an angle psi_1,i = atan2(y_2i+1, y_2i) in (-pi, pi];
+ * level l >= 2 pairs the radii of level l - 1 the same way (angles in
+ * [0, pi/2]); log2(d) levels, d - 1 angles. The final radius is ||y|| = 1,
+ * so the only magnitude kept is ||x|| (fp16 in the norm plane). Each angle is
+ * quantized by the Lloyd-Max codebook of its level's law after a Haar
+ * rotation (tq_polar_codebook): level-1 angles at `bits` bits, the others at
+ * `bits2`. Ties go to the upper cell (code = #{j : t_j <= psi}).
+ * Layout: codes[s] holds the angle codes as one LSB-first bit stream, level
+ * 1 first (angle i at bits * i), then levels 2, 3, ... in order, each angle
+ * at its level's width; stride tq_polar_code_bytes(d, bits, bits2). The
+ * signs and rnorm planes are not used (may be NULL); m is ignored.
+ * Supported: d = 128, bits and bits2 in 1..4 (tq_quantize_kv); decode takes
+ * (bits, bits2) in {(2,2), (3,2), (4,2), (4,3), (3,3), (4,4)} with an MSE
+ * value cache. The key logit is l_t = n_t <q', y_hat_t>, y_hat_t the inverse
+ * recursion from the centroid angles (unit norm); no sign sketch. */
+int tq_polar_code_bytes(int d, int bits, int bits2); /* 0 for invalid arguments */
+
+/* Lloyd-Max codebook of the PolarQuant angles of one level (1 = coordinate
+ * pairs, up to 8) after a Haar rotation: level 1 uniform on (-pi, pi] (equal
+ * cells from -pi); level l >= 2 with density proportional to
+ * (sin psi cos psi)^(2^(l-1) - 1) on [0, pi/2], i.e. sin^2 psi ~
+ * Beta(k/2, k/2), k = 2^(l-1). centroids: host, 2^bits doubles ascending;
+ * boundaries: host, 2^bits - 1 doubles, the midpoints. 1 <= bits <= 4.
+ * Computed once per (level, bits), cached. */
+tq_status tq_polar_codebook(int level, int bits, double* centroids, double* boundaries);
 
 int tq_code_bytes(int d, int code_bits); /* per-slot stride of codes, bytes */
 /* per-slot stride of a two-group cache's codes (code bits of the coordinates

@@ -20,11 +20,11 @@ TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED = 1, 2
 TQ_ERR_TIMEOUT = 6
 TQ_ERR_WORKSPACE = 7
 TQ_ROT_DENSE_QR, TQ_ROT_RHT = 0, 1
-TQ_MSE, TQ_PROD = 0, 1
+TQ_MSE, TQ_PROD, TQ_POLAR = 0, 1, 2
 TQ_F32, TQ_BF16, TQ_F16 = 0, 1, 2
 
 ROT_KINDS = {"dense": TQ_ROT_DENSE_QR, "rht": TQ_ROT_RHT}
-MODES = {"mse": TQ_MSE, "prod": TQ_PROD}
+MODES = {"mse": TQ_MSE, "prod": TQ_PROD, "polar": TQ_POLAR}
 
 
 class TQError(RuntimeError):
@@ -97,6 +97,8 @@ _SIGS = {
     "tq_code_bytes": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
     "tq_code_bytes2": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "tq_sign_bytes": (ctypes.c_int, [ctypes.c_int]),
+    "tq_polar_code_bytes": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "tq_polar_codebook": (_STATUS, [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
     "tq_quantize_kv": (_STATUS, [ctypes.POINTER(tq_quant_args), ctypes.c_void_p]),
     "tq_attn_decode_workspace": (ctypes.c_size_t, [ctypes.POINTER(tq_decode_args)]),
     "tq_attn_decode": (_STATUS, [ctypes.POINTER(tq_decode_args), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
@@ -235,23 +237,42 @@ def tq_sign_bytes(m):
     return load().tq_sign_bytes(m)
 
 
+def tq_polar_code_bytes(d, bits1, bits2):
+    return load().tq_polar_code_bytes(d, bits1, bits2)
+
+
+def tq_polar_codebook(level, bits):
+    c = np.empty(1 << bits, dtype=np.float64)
+    t = np.empty((1 << bits) - 1, dtype=np.float64)
+    _check(load().tq_polar_codebook(level, bits, c.ctypes.data, t.ctypes.data), "tq_polar_codebook")
+    return c, t
+
+
 # ------------------------------------------------------- cache planes ---
 class Cache:
     """Device planes of a packed cache (torch tensors owned by this object)."""
 
     def __init__(self, mode, bits, d, rows, capacity, m=None, device="cuda", bits2=None):
         """bits2: the second channel group's bits of a fractional-rate cache
-        (coordinates with i % 16 >= 8), None for one width."""
+        (coordinates with i % 16 >= 8), None for one width; for a PolarQuant
+        cache ("polar") the bits of the angles above level 1 (required)."""
         import torch
 
         self.mode = MODES.get(mode, mode)
         self.bits, self.d, self.rows, self.capacity = bits, d, rows, capacity
-        self.bits2 = bits2 if bits2 and bits2 != bits else None
+        if self.mode == TQ_POLAR:
+            if not bits2:
+                raise ValueError("a PolarQuant cache needs bits2 (the bits of the angles above level 1)")
+            self.bits2 = bits2
+        else:
+            self.bits2 = bits2 if bits2 and bits2 != bits else None
         self.m = (m if m is not None else d) if self.mode == TQ_PROD else 0
         cb = bits - 1 if self.mode == TQ_PROD else bits
         self.code_bits = cb
         n = rows * capacity
-        if self.bits2 is None:
+        if self.mode == TQ_POLAR:
+            self.code_stride = tq_polar_code_bytes(d, bits, bits2)
+        elif self.bits2 is None:
             self.code_stride = tq_code_bytes(d, cb)
         else:
             self.code_stride = load().tq_code_bytes2(d, cb, self.bits2 - 1 if self.mode == TQ_PROD else self.bits2)
@@ -324,7 +345,7 @@ def _decode_struct(q, kcache, vcache, seq_lens, max_seq_len, rot, qjl, out, scal
         keep = np.ascontiguousarray(gqa_map, dtype=np.int32)
         a.gqa_map = keep.ctypes.data
     a.rot = rot.handle
-    a.qjl = qjl.handle
+    a.qjl = qjl.handle if qjl is not None else None
     a.k = kcache.struct()
     a.v = vcache.struct()
     a.scale = scale
@@ -360,7 +381,7 @@ def _prefill_struct(q, kcache, vcache, q_start, max_context, rot, qjl, out, scal
     a.q_start = q_start.data_ptr()
     a.max_context = max_context
     a.rot = rot.handle
-    a.qjl = qjl.handle
+    a.qjl = qjl.handle if qjl is not None else None
     a.k = kcache.struct()
     a.v = vcache.struct()
     a.scale = scale

@@ -58,10 +58,26 @@ tq_status check_qjl(const tq_qjl* q, int m, int d) {
 // Validates a cache descriptor; returns the code bits per coordinate.
 // code bits of the two channel groups (equal for a one-width cache) and
 // the codes' per-slot stride
+// A PolarQuant cache (allow_polar) gives its level-1 and higher-level code
+// widths as code_bits and code_bits2.
 tq_status check_cache(const tq_cache& c, const char* what, int* code_bits, int* code_bits2 = nullptr,
-                      int* code_stride = nullptr) {
+                      int* code_stride = nullptr, bool allow_polar = false) {
     std::string w(what);
-    if (c.mode != TQ_MSE && c.mode != TQ_PROD) return fail(TQ_ERR_INVALID_ARG, w + ": mode must be TQ_MSE or TQ_PROD");
+    if (c.mode == TQ_POLAR) {
+        if (!allow_polar)
+            return fail(TQ_ERR_UNSUPPORTED, w + ": PolarQuant caches are taken by tq_quantize_kv and tq_attn_decode only");
+        if (c.bits < 1 || c.bits > 4 || c.bits2 < 1 || c.bits2 > 4)
+            return fail(TQ_ERR_UNSUPPORTED, w + ": PolarQuant bits and bits2 must be 1..4");
+        if (c.d != 128) return fail(TQ_ERR_UNSUPPORTED, w + ": PolarQuant caches need d = 128");
+        if (c.rows < 0 || c.capacity < 0) return fail(TQ_ERR_INVALID_ARG, w + ": negative rows/capacity");
+        if (!c.codes || !c.norm) return fail(TQ_ERR_INVALID_ARG, w + ": codes/norm plane is NULL");
+        if (!aligned(c.codes, 16) || !aligned(c.norm, 2)) return fail(TQ_ERR_ALIGNMENT, w + ": codes must be 16-byte aligned, norm 2-byte");
+        *code_bits = c.bits;
+        if (code_bits2) *code_bits2 = c.bits2;
+        if (code_stride) *code_stride = tq_polar_code_bytes(c.d, c.bits, c.bits2);
+        return TQ_OK;
+    }
+    if (c.mode != TQ_MSE && c.mode != TQ_PROD) return fail(TQ_ERR_INVALID_ARG, w + ": mode must be TQ_MSE, TQ_PROD or TQ_POLAR");
     if (c.mode == TQ_MSE && (c.bits < 1 || c.bits > 4)) return fail(TQ_ERR_UNSUPPORTED, w + ": MSE bits must be 1..4");
     if (c.mode == TQ_PROD && (c.bits < 2 || c.bits > 5)) return fail(TQ_ERR_UNSUPPORTED, w + ": PROD bits must be 2..5");
     if (c.d < 3 || c.d > 256) return fail(TQ_ERR_UNSUPPORTED, w + ": d must be 3..256");
@@ -328,7 +344,8 @@ bool g_quant_umma = true;
 struct QuantLaunch {
     tqk::QuantParams p;
     int dtype = 0, vpl = 1, cb = 1;
-    bool rht = false, prod = false, mma = false, small = false, umma = false;
+    bool rht = false, prod = false, mma = false, small = false, umma = false, polar = false;
+    tqk::PolarQuantParams pq;  // PolarQuant keys
     const void* w_umma = nullptr;
     const void* s_umma = nullptr;
 };
@@ -356,14 +373,164 @@ struct DecodeLaunch {
     int kb = 0, vb = 0;
     bool two = false;  // fractional-rate key and value caches
     cudaEvent_t scan_begin = nullptr, scan_end = nullptr;
+    bool polar = false;  // PolarQuant keys: the polar scan instead of the tensor-core one
+    tqk::PolarDecodeParams pdp;
 };
+
+// The query heads of each KV head from a host gqa_map (every KV head serving
+// `group` query heads); *use = 0 when gqa_map is NULL.
+tq_status head_table(const tq_decode_args* a, int group, int16_t* table, int* use) {
+    *use = 0;
+    if (!a->gqa_map) return TQ_OK;
+    std::vector<int> count(a->hkv, 0);
+    for (int h = 0; h < a->hq; ++h) {
+        const int g = a->gqa_map[h];
+        if (g < 0 || g >= a->hkv) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: gqa_map entry out of range");
+        if (count[g] >= group) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: every KV head must serve hq/hkv query heads");
+        table[g * group + count[g]++] = (int16_t)h;
+    }
+    *use = 1;
+    return TQ_OK;
+}
+
+// Decode over PolarQuant keys and a one-width MSE value cache: the query
+// prep writes q' (fp32) where the tensor-core scan keeps its B operands,
+// the polar scan writes the same split partials, the merge is shared.
+tq_status polar_decode_prepare(const tq_decode_args* a, void* workspace, size_t ws_bytes, DecodeLaunch* D) {
+    const DecodePlan& pl = D->pl;
+    int kb = 0, kb2 = 0, kstride = 0, vb = 0, vb2 = 0, vstride = 0;
+    tq_status s;
+    if ((s = check_cache(a->k, "tq_attn_decode k", &kb, &kb2, &kstride, true)) != TQ_OK) return s;
+    if ((s = check_cache(a->v, "tq_attn_decode v", &vb, &vb2, &vstride)) != TQ_OK) return s;
+    if (a->v.mode != TQ_MSE || vb2 != vb)
+        return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: PolarQuant keys take a one-width MSE value cache");
+    if (!tqk::polar_decode_supported(kb, kb2))
+        return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: PolarQuant (bits, bits2) must be (2,2), (3,2), (4,2), (4,3), (3,3) or (4,4)");
+    if (a->k.d != a->d || a->v.d != a->d) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: cache d does not match");
+    const int64_t rows = (int64_t)a->batch * a->hkv;
+    if (a->k.rows != rows || a->v.rows != rows) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: cache rows must be batch*hkv");
+    if (a->k.capacity != a->v.capacity) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: k and v capacity differ");
+    if (a->max_seq_len > a->k.capacity) return fail(TQ_ERR_CAPACITY, "tq_attn_decode: max_seq_len exceeds the capacity");
+    if (!aligned(a->v.codes, 16)) return fail(TQ_ERR_ALIGNMENT, "tq_attn_decode: value codes must be 16-byte aligned");
+    if ((s = check_rot(a->rot, a->d)) != TQ_OK) return s;
+    if (!a->q || !a->out || !a->seq_lens) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: q/out/seq_lens is NULL");
+    if (a->q_dtype != TQ_F32 && a->q_dtype != TQ_BF16) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: q_dtype must be F32 or BF16");
+    if (a->out_dtype != TQ_F32 && a->out_dtype != TQ_BF16) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: out_dtype must be F32 or BF16");
+    tqk::PolarDecodeParams& dp = D->pdp;
+    std::memset(&dp, 0, sizeof(dp));
+    if ((s = head_table(a, pl.group, dp.head_table, &dp.use_table)) != TQ_OK) return s;
+    // the workspace last: every other argument error takes precedence
+    if (!workspace || ws_bytes < pl.total) return fail(TQ_ERR_WORKSPACE, "tq_attn_decode: workspace missing or too small");
+    if (!aligned(workspace, 256)) return fail(TQ_ERR_ALIGNMENT, "tq_attn_decode: workspace must be 256-byte aligned");
+    char* ws = (char*)workspace;
+    float* qprime = (float*)(ws + pl.off_frag);  // rows x kFragWords words hold rows x 128 floats
+    float* part = (float*)(ws + pl.off_part);
+
+    tqk::PrepParams& pp = D->pp;
+    std::memset(&pp, 0, sizeof(pp));
+    pp.q = a->q;
+    pp.q_dtype = a->q_dtype == TQ_BF16 ? 1 : 0;
+    pp.rows = (int64_t)a->batch * a->hq;
+    pp.d = a->d;
+    pp.pit32 = a->rot->d_pit32;
+    pp.sgn = a->rot->d_sign;
+    pp.rht = a->rot->kind == TQ_ROT_RHT;
+    pp.inv_sqrt_d = (float)(1.0 / std::sqrt((double)a->d));
+    pp.qprime = qprime;
+
+    std::vector<double> vc, vt;
+    if ((s = tq::codebook(a->d, vb, vc, vt)) != TQ_OK) return s;
+    for (size_t i = 0; i < vc.size(); ++i) dp.vc[i] = (float)vc[i];
+    for (int lev = 1; lev <= tqk::kPolarLevels; ++lev) {
+        std::vector<double> cc, tt;
+        if ((s = tq::polar_codebook(lev, lev == 1 ? kb : kb2, cc, tt)) != TQ_OK) return s;
+        for (size_t i = 0; i < cc.size(); ++i) {
+            const float co = (float)std::cos(cc[i]), si = (float)std::sin(cc[i]);
+            if (lev == 1) {
+                dp.c1cos[i] = co;
+                dp.c1sin[i] = si;
+            } else {
+                dp.ccos[lev - 2][i] = co;
+                dp.csin[lev - 2][i] = si;
+            }
+        }
+    }
+    dp.qprime = qprime;
+    dp.batch = a->batch;
+    dp.hq = a->hq;
+    dp.hkv = a->hkv;
+    dp.group = pl.group;
+    dp.seq_lens = a->seq_lens;
+    dp.capacity = a->k.capacity;
+    dp.kcodes = a->k.codes;
+    dp.kcode_stride = kstride;
+    dp.knorm = a->k.norm;
+    dp.vcodes = a->v.codes;
+    dp.vcode_stride = vstride;
+    dp.vnorm = a->v.norm;
+    dp.vbits = vb;
+    const double scale = a->scale != 0.0f ? (double)a->scale : 1.0 / std::sqrt((double)a->d);
+    dp.scale_log2 = (float)(scale * 1.4426950408889634);
+    dp.n_splits = pl.n_splits;
+    dp.chunk = pl.chunk;
+    dp.partial = part;
+    dp.logits = a->logits;
+    dp.max_seq_len = a->max_seq_len;
+    D->polar = true;
+    D->kb = kb;
+    D->vb = kb2;  // the polar scan's (bits, bits2)
+    D->scan_begin = (cudaEvent_t)a->scan_begin;
+    D->scan_end = (cudaEvent_t)a->scan_end;
+
+    tqk::CombineParams& cp = D->cp;
+    std::memset(&cp, 0, sizeof(cp));
+    cp.partial = part;
+    cp.rows = a->batch * a->hq;
+    cp.d = a->d;
+    cp.n_splits = pl.n_splits;
+    cp.pi32 = a->rot->d_pi32;
+    cp.sgn = a->rot->d_sign;
+    cp.rht = a->rot->kind == TQ_ROT_RHT;
+    cp.inv_sqrt_d = (float)(1.0 / std::sqrt((double)a->d));
+    cp.out = a->out;
+    cp.out_dtype = a->out_dtype == TQ_BF16 ? 1 : 0;
+    return TQ_OK;
+}
+
+// The PolarQuant part of a quantize launch: the angle codebooks of the 7
+// levels (boundaries as fp32 cos/sin pairs and fp64 values) and the guard
+// band. The fp32 rotation is good to a few 1e-7 of the unit vector (RHT
+// butterflies, or a 128-term fp32 dot product for the dense Pi) and a cross
+// product b cos t - a sin t moves by at most the error of its pair; the
+// bands sit an order of magnitude above the typical error.
+tq_status polar_prepare(const tq_cache& c, QuantLaunch* L) {
+    tqk::PolarQuantParams& pq = L->pq;
+    std::memset(&pq.cb, 0, sizeof(pq.cb));
+    for (int lev = 1; lev <= tqk::kPolarLevels; ++lev) {
+        std::vector<double> cc, tt;
+        const tq_status s = tq::polar_codebook(lev, lev == 1 ? c.bits : c.bits2, cc, tt);
+        if (s != TQ_OK) return s;
+        for (size_t j = 0; j < tt.size(); ++j) {
+            pq.cb.tc[lev - 1][j] = (float)std::cos(tt[j]);
+            pq.cb.ts[lev - 1][j] = (float)std::sin(tt[j]);
+            pq.cb.t64[lev - 1][j] = tt[j];
+        }
+    }
+    pq.q = L->p;
+    pq.bits1 = c.bits;
+    pq.bits2 = c.bits2;
+    pq.inv_w1 = (float)((double)(1 << c.bits) / (2.0 * M_PI));
+    pq.guard = L->rht ? 3.0e-6f : 4.0e-6f;
+    L->polar = true;
+    return TQ_OK;
+}
 
 // Validates a quantize call and fills its launch; *empty = nothing to do.
 tq_status quant_prepare(const tq_quant_args* a, QuantLaunch* L, bool* empty) {
     *empty = false;
     if (!a) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_kv: args are NULL");
     int cb = 0, cb2 = 0, cstride = 0;
-    tq_status s = check_cache(a->cache, "tq_quantize_kv cache", &cb, &cb2, &cstride);
+    tq_status s = check_cache(a->cache, "tq_quantize_kv cache", &cb, &cb2, &cstride, true);
     if (s != TQ_OK) return s;
     const tq_cache& c = a->cache;
     if ((s = check_rot(a->rot, c.d)) != TQ_OK) return s;
@@ -418,6 +585,9 @@ tq_status quant_prepare(const tq_quant_args* a, QuantLaunch* L, bool* empty) {
     p.m = prod ? c.m : 0;
     p.inv_sqrt_d = (float)(1.0 / std::sqrt((double)c.d));
     p.guard = rht ? 1.0e-6f : (float)(3.0e-8 * c.d);
+    L->dtype = a->x_dtype == TQ_F32 ? 0 : 1;
+    L->rht = rht;
+    if (c.mode == TQ_POLAR) return polar_prepare(c, L);
     if ((s = fill_codebook(c.d, cb, &p.cb)) != TQ_OK) return s;
     p.code_bits2 = cb2 != cb ? cb2 : 0;
     if (p.code_bits2 && (s = fill_codebook(c.d, cb2, &p.cb2)) != TQ_OK) return s;
@@ -453,6 +623,7 @@ tq_status quant_prepare(const tq_quant_args* a, QuantLaunch* L, bool* empty) {
 }
 
 cudaError_t quant_launch(const QuantLaunch& L, cudaStream_t st) {
+    if (L.polar) return tqk::launch_polar_quantize(L.pq, L.dtype, L.rht ? 1 : 0, st);
     if (L.small) {
         tqk::StepPrepParams sp;
         std::memset(&sp, 0, sizeof(sp));
@@ -472,6 +643,7 @@ tq_status decode_prepare(const tq_decode_args* a, void* workspace, size_t ws_byt
     DecodePlan& pl = D->pl;
     tq_status s = plan_decode(a, &pl);
     if (s != TQ_OK) return s;
+    if (a->k.mode == TQ_POLAR) return polar_decode_prepare(a, workspace, ws_bytes, D);
     int kb = 0, vb = 0, kb2 = 0, vb2 = 0;
     if ((s = check_cache(a->k, "tq_attn_decode k", &kb, &kb2)) != TQ_OK) return s;
     if ((s = check_cache(a->v, "tq_attn_decode v", &vb, &vb2)) != TQ_OK) return s;
@@ -495,16 +667,7 @@ tq_status decode_prepare(const tq_decode_args* a, void* workspace, size_t ws_byt
     if (a->out_dtype != TQ_F32 && a->out_dtype != TQ_BF16) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: out_dtype must be F32 or BF16");
     tqk::DecodeParams& dp = D->dp;
     std::memset(&dp, 0, sizeof(dp));
-    if (a->gqa_map) {
-        std::vector<int> count(a->hkv, 0);
-        for (int h = 0; h < a->hq; ++h) {
-            int g = a->gqa_map[h];
-            if (g < 0 || g >= a->hkv) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: gqa_map entry out of range");
-            if (count[g] >= pl.group) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_decode: every KV head must serve hq/hkv query heads");
-            dp.head_table[g * pl.group + count[g]++] = (int16_t)h;
-        }
-        dp.use_table = 1;
-    }
+    if ((s = head_table(a, pl.group, dp.head_table, &dp.use_table)) != TQ_OK) return s;
     // the workspace last: every other argument error takes precedence
     if (!workspace || ws_bytes < pl.total) return fail(TQ_ERR_WORKSPACE, "tq_attn_decode: workspace missing or too small");
     if (!aligned(workspace, 256)) return fail(TQ_ERR_ALIGNMENT, "tq_attn_decode: workspace must be 256-byte aligned");
@@ -597,7 +760,7 @@ tq_status decode_launch(const DecodeLaunch& D, cudaStream_t st, tqk::StepPrepPar
     if (e != cudaSuccess) return cuda_status(e, "tq_attn_decode query prep");
     if (D.scan_begin && (e = cudaEventRecord(D.scan_begin, st)) != cudaSuccess)
         return cuda_status(e, "tq_attn_decode scan_begin");
-    e = tqk::launch_decode_mma(D.dp, D.kb, D.vb, D.two, st);
+    e = D.polar ? tqk::launch_polar_decode(D.pdp, D.kb, D.vb, st) : tqk::launch_decode_mma(D.dp, D.kb, D.vb, D.two, st);
     if (e != cudaSuccess) return cuda_status(e, "tq_attn_decode scan");
     if (D.scan_end && (e = cudaEventRecord(D.scan_end, st)) != cudaSuccess)
         return cuda_status(e, "tq_attn_decode scan_end");
@@ -877,6 +1040,8 @@ size_t tq_decode_step_workspace(const tq_step_args* a) { return a ? tq_attn_deco
 tq_status tq_decode_step(const tq_step_args* a, void* workspace, size_t ws_bytes, tq_stream stream) {
     if (!a) return fail(TQ_ERR_INVALID_ARG, "tq_decode_step: args are NULL");
     const tq_decode_args& at = a->attn;
+    if (at.k.mode == TQ_POLAR)
+        return fail(TQ_ERR_UNSUPPORTED, "tq_decode_step: PolarQuant keys are appended with tq_quantize_kv, then tq_attn_decode");
     if (!a->k_new || !a->v_new || !a->append_pos) return fail(TQ_ERR_INVALID_ARG, "tq_decode_step: k_new/v_new/append_pos is NULL");
     tq_quant_args qk;
     std::memset(&qk, 0, sizeof(qk));

@@ -273,6 +273,120 @@ tq_status codebook(int d, int bits, std::vector<double>& c_out, std::vector<doub
     return TQ_OK;
 }
 
+// ---------------------------------------------------------------------------
+// PolarQuant angle codebooks. After a Haar rotation the level-1 angle of a
+// coordinate pair is uniform on (-pi, pi]; the level-l angle (l >= 2) pairs
+// the norms of two independent 2^(l-1)-dimensional Gaussian blocks, so its
+// density on [0, pi/2] is proportional to (sin psi cos psi)^(k-1), k =
+// 2^(l-1). Level 1: equal cells from -pi (the Lloyd-Max optimum of a
+// uniform law). Higher levels: the Lloyd-Max fixed point, cell masses and
+// first moments by composite 16-point Gauss-Legendre quadrature of the
+// unnormalised density (the normalisation cancels in each centroid), the
+// centroids kept symmetric about pi/4.
+// ---------------------------------------------------------------------------
+namespace {
+
+struct AngleLaw {
+    double km1, h;
+    explicit AngleLaw(int level) {
+        const double k = std::ldexp(1.0, level - 1);
+        km1 = k - 1.0;
+        // panels well inside the width of the peak at pi/4 (about 1/sqrt(2k))
+        h = std::min(M_PI / 256.0, 0.05 / std::sqrt(k));
+    }
+    double dens(double u) const {  // (sin u cos u)^(k-1) = (sin 2u / 2)^(k-1)
+        const double s = 0.5 * std::sin(2.0 * u);
+        return s <= 0.0 ? 0.0 : std::exp(km1 * std::log(s));
+    }
+    // (mass, first moment) of [a, b]
+    std::pair<double, double> cell(double a, double b) const {
+        if (b <= a) return {0.0, 0.0};
+        int panels = std::max(1, (int)std::ceil((b - a) / h));
+        const double w = (b - a) / panels;
+        const GaussLegendre16& g = gl16();
+        double m0 = 0.0, m1 = 0.0;
+        for (int p = 0; p < panels; ++p) {
+            const double mid = a + (p + 0.5) * w;
+            double s0 = 0.0, s1 = 0.0;
+            for (int i = 0; i < 16; ++i) {
+                const double u = mid + 0.5 * w * g.x[i];
+                const double f = g.w[i] * dens(u);
+                s0 += f;
+                s1 += f * u;
+            }
+            m0 += 0.5 * w * s0;
+            m1 += 0.5 * w * s1;
+        }
+        return {m0, m1};
+    }
+};
+
+std::mutex g_pcb_mutex;
+std::map<std::pair<int, int>, std::pair<std::vector<double>, std::vector<double>>> g_pcb_cache;
+
+}  // namespace
+
+tq_status polar_codebook(int level, int bits, std::vector<double>& c_out, std::vector<double>& t_out) {
+    if (level < 1 || level > 8) return fail(TQ_ERR_INVALID_ARG, "polar codebook: level must be 1..8");
+    if (bits < 1 || bits > 4) return fail(TQ_ERR_INVALID_ARG, "polar codebook: bits must be 1..4");
+    {
+        std::lock_guard<std::mutex> lk(g_pcb_mutex);
+        auto it = g_pcb_cache.find({level, bits});
+        if (it != g_pcb_cache.end()) {
+            c_out = it->second.first;
+            t_out = it->second.second;
+            return TQ_OK;
+        }
+    }
+    const int L = 1 << bits;
+    std::vector<double> c(L), t(L - 1);
+    if (level == 1) {
+        const double w = (M_PI - (-M_PI)) / L;
+        for (int j = 1; j < L; ++j) t[j - 1] = -M_PI + w * j;
+        for (int i = 0; i < L; ++i) c[i] = -M_PI + w * (i + 0.5);
+    } else {
+        const AngleLaw law(level);
+        // start: equal-mass cells of the law (CDF by quadrature and bisection)
+        const double total = law.cell(0.0, 0.5 * M_PI).first;
+        for (int i = 0; i < L; ++i) {
+            const double target = (i + 0.5) / L * total;
+            double lo = 0.0, hi = 0.5 * M_PI;
+            for (int it = 0; it < 80; ++it) {
+                const double mid = 0.5 * (lo + hi);
+                if (law.cell(0.0, mid).first < target) lo = mid; else hi = mid;
+            }
+            c[i] = 0.5 * (lo + hi);
+        }
+        std::vector<double> nc(L);
+        bool done = false;
+        for (int it = 0; it < 100000 && !done; ++it) {
+            double prev = 0.0;
+            for (int i = 0; i < L; ++i) {
+                const double next = i + 1 < L ? 0.5 * (c[i] + c[i + 1]) : 0.5 * M_PI;
+                const auto mm = law.cell(prev, next);
+                nc[i] = mm.first > 0.0 ? mm.second / mm.first : 0.5 * (prev + next);
+                prev = next;
+            }
+            double delta = 0.0;
+            for (int i = 0; i < L; ++i) {
+                const double sym = 0.5 * (nc[i] + (0.5 * M_PI - nc[L - 1 - i]));
+                delta = std::max(delta, std::fabs(sym - c[i]));
+                c[i] = sym;
+            }
+            done = delta < 1e-15;
+        }
+        if (!done) return fail(TQ_ERR_INVALID_ARG, "polar codebook: Lloyd-Max did not converge");
+        for (int j = 0; j < L - 1; ++j) t[j] = 0.5 * (c[j] + c[j + 1]);
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_pcb_mutex);
+        g_pcb_cache[{level, bits}] = {c, t};
+    }
+    c_out = c;
+    t_out = t;
+    return TQ_OK;
+}
+
 }  // namespace tq
 
 // ---------------------------------------------------------------------------
@@ -406,6 +520,23 @@ int tq_code_bytes2(int d, int code_bits, int code_bits2) {
 int tq_sign_bytes(int m) {
     if (m <= 0) return 0;
     return ((m + 7) / 8 + 15) / 16 * 16;
+}
+
+int tq_polar_code_bytes(int d, int bits1, int bits2) {
+    if (d < 2 || (d & (d - 1)) || bits1 < 1 || bits1 > 4 || bits2 < 1 || bits2 > 4) return 0;
+    const int bits = (d / 2) * bits1 + (d / 2 - 1) * bits2;
+    return ((bits + 7) / 8 + 15) / 16 * 16;
+}
+
+tq_status tq_polar_codebook(int level, int bits, double* centroids, double* boundaries) {
+    tq::clear_error();
+    if (!centroids || !boundaries) return tq::fail(TQ_ERR_INVALID_ARG, "tq_polar_codebook: NULL output");
+    std::vector<double> c, t;
+    tq_status s = tq::polar_codebook(level, bits, c, t);
+    if (s != TQ_OK) return s;
+    std::copy(c.begin(), c.end(), centroids);
+    std::copy(t.begin(), t.end(), boundaries);
+    return TQ_OK;
 }
 
 }  // extern "C"

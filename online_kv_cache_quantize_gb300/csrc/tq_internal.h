@@ -52,6 +52,8 @@ void gaussians(uint64_t seed, int64_t count, double* out);
 double round_bf16(double x);
 void householder_haar(const double* g, int d, double* pi_out);  // Pi = Q diag(sign diag R)
 tq_status codebook(int d, int bits, std::vector<double>& c, std::vector<double>& t);
+// PolarQuant angle codebook of one level (1 = the coordinate pairs), ascending
+tq_status polar_codebook(int level, int bits, std::vector<double>& c, std::vector<double>& t);
 
 // thread-local error message
 tq_status fail(tq_status s, const std::string& msg);

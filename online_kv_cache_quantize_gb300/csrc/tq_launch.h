@@ -67,6 +67,53 @@ cudaError_t launch_quantize_umma(const QuantParams& p, const void* w_umma, const
 cudaError_t launch_quantize(const QuantParams& p, int dtype, int rht, int prod, int code_bits,
                             cudaStream_t s);
 
+// PolarQuant keys (d = 128): the angle codebooks of the 7 levels. Decisions
+// of the fp32 path are signs of b cos t - a sin t (= rho sin(psi - t)) for a
+// boundary t of the pair (a, b); the fp64 path compares atan2 with t64.
+constexpr int kPolarLevels = 7;
+struct PolarCodebook {
+    float tc[kPolarLevels][15];     // cos t_j
+    float ts[kPolarLevels][15];     // sin t_j
+    double t64[kPolarLevels][15];   // t_j (fp64)
+};
+
+struct PolarQuantParams {
+    QuantParams q;      // input, slots, codes (the angle stream), norm, rotation, err
+    PolarCodebook cb;
+    int bits1, bits2;   // level-1 and higher-level code widths
+    float inv_w1;       // 2^bits1 / (2 pi): level-1 cell index from the angle
+    float guard;        // |b cos t - a sin t| below this is re-decided in fp64
+};
+
+cudaError_t launch_polar_quantize(const PolarQuantParams& p, int dtype, int rht, cudaStream_t s);
+
+struct PolarDecodeParams {
+    const float* qprime;  // [B*Hq][128] q' = Pi q (written by the query prep)
+    int batch, hq, hkv, group;
+    const int32_t* seq_lens;
+    int16_t head_table[256];  // query heads of KV head kv: head_table[kv * group + j]
+    int use_table;            // 0: head kv * group + j
+    int64_t capacity;
+    const uint8_t* kcodes; int kcode_stride;
+    const uint16_t* knorm;
+    const uint8_t* vcodes; int vcode_stride;
+    const uint16_t* vnorm;
+    int vbits;
+    float vc[kMaxLevels];     // value centroids
+    float c1cos[kMaxLevels], c1sin[kMaxLevels];  // level-1 centroid angles
+    float ccos[kPolarLevels - 1][kMaxLevels];    // levels 2 .. 7
+    float csin[kPolarLevels - 1][kMaxLevels];
+    float scale_log2;     // softmax scale * log2(e)
+    int n_splits, chunk;  // chunk: tokens per split
+    float* partial;       // [B*Hq][n_splits][128 + kPartPad]: a, then M and Z
+    float* logits;        // optional [B*Hq][max_seq_len]
+    int max_seq_len;
+};
+
+// (bits1, bits2) in {(2,2), (3,2), (4,2), (4,3), (3,3), (4,4)}, group in {1, 2, 4, 8}
+bool polar_decode_supported(int bits1, int bits2);
+cudaError_t launch_polar_decode(const PolarDecodeParams& p, int bits1, int bits2, cudaStream_t s);
+
 struct PrepParams {
     const void* q;        // [rows][d]
     int q_dtype;          // 0 f32, 1 bf16

@@ -40,11 +40,16 @@ Packed layout (this project's specification): the angle codes as one LSB-first
 bit stream, level 1 first (angle i at bits1 * i), then levels 2, 3, ... in
 order, each angle at its level's width; row stride rounded up to 16 bytes.
 
+Decode (this library's reading, the same as the TurboQuant decode): the key
+logits above, p = softmax(scale * l) over the visible tokens (scale 1/sqrt(d)
+unless given), a = sum_t p_t nV_t cV[idxV_t] with MSE values, o = Pi^T a.
+
 Pinned by: the exact inverse without quantization; the angle laws against the
 empirical angles of Haar-random unit vectors (KS tests); the Lloyd-Max
 conditions of every level's codebook, checked with an independent quadrature;
 the closed-form distortion of d = 2 (one uniform angle); logits equal to the
-dense reconstruction's dot products; a hand-worked packing example.
+dense reconstruction's dot products; a hand-worked packing example; decode
+equal to textbook softmax attention over the explicit reconstructions.
 """
 
 import functools
@@ -52,6 +57,7 @@ import functools
 import numpy as np
 from scipy import special
 
+from . import attention
 from . import quantize as qmod
 from . import rotation
 
@@ -238,3 +244,37 @@ def key_logits(qprime, idx, norm16, d, bits1, bits2):
     """l_t = n_t <q', y_hat_t> for each query row of qprime [G, d] (or [d])."""
     y_hat = reconstruct_rotated(idx, d, bits1, bits2)
     return (np.atleast_2d(qprime) @ y_hat.T) * np.asarray(norm16)[None, :]
+
+
+def decode(q, kcache, vcache, seq_lens, pi, bits1, bits2, v_centroids, scale=None, gqa_map=None):
+    """Decode attention over PolarQuant keys and MSE values.
+
+    q [B, Hq, d]; kcache: 'packed' [B, Hkv, T, stride] angle streams and
+    'norm16' [B, Hkv, T]; vcache: 'idx' [B, Hkv, T, d] and 'norm16'.
+    Returns (out [B, Hq, d], logits [B][Hq] -> [L_b])."""
+    q = np.asarray(q, dtype=np.float64)
+    bsz, hq, d = q.shape
+    hkv = kcache["norm16"].shape[1]
+    if gqa_map is None:
+        gqa_map = attention.default_gqa_map(hq, hkv)
+    if scale is None or scale == 0:
+        scale = 1.0 / np.sqrt(d)
+    pi = np.asarray(pi, dtype=np.float64)
+    out = np.zeros((bsz, hq, d))
+    logits = [[None] * hq for _ in range(bsz)]
+    for b in range(bsz):
+        L = int(seq_lens[b])
+        for h in range(hq):
+            kv = int(gqa_map[h])
+            if L == 0:
+                continue  # no visible token: output 0
+            qp = pi @ q[b, h]
+            idx = unpack(kcache["packed"][b, kv, :L], d, bits1, bits2)
+            l = key_logits(qp, idx, kcache["norm16"][b, kv, :L], d, bits1, bits2)[0]
+            s = scale * l
+            p = np.exp(s - np.max(s))
+            p = p / np.sum(p)
+            vhat = vcache["norm16"][b, kv, :L, None] * np.asarray(v_centroids)[vcache["idx"][b, kv, :L]]
+            out[b, h] = (p @ vhat) @ pi
+            logits[b][h] = l
+    return out, logits

@@ -147,3 +147,31 @@ def test_argument_errors_are_reported(lib):
     assert L.tq_attn_decode_workspace(None) == 0
     assert L.tq_attn_prefill(None, None, 0, None) == 1
     assert L.tq_attn_prefill_workspace(None) == 0
+
+
+@pytest.mark.parametrize("level", [1, 2, 3, 5, 7, 8])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+def test_polar_codebook_matches_oracle(lib, level, bits):
+    """The library's PolarQuant angle codebooks (its own quadrature) against
+    the oracle's (incomplete-beta masses, Gauss-Legendre moments)."""
+    from oracle import polar
+    c, t = lib.tq_polar_codebook(level, bits)
+    co, to = polar.codebook(level, bits)
+    assert np.max(np.abs(c - co)) < 1e-12 and np.max(np.abs(t - to)) < 1e-12
+    if level >= 2:
+        assert np.max(np.abs(c + c[::-1] - np.pi / 2)) < 1e-13
+
+
+def test_polar_code_bytes(lib):
+    """64 bits1 + 63 bits2 bits at d = 128, rounded up to 16 bytes (the
+    oracle's packing of a row gives the same stride); invalid arguments 0."""
+    from oracle import polar
+    for b1, b2 in ((4, 2), (3, 2), (2, 2), (4, 3), (1, 1), (4, 4), (2, 1)):
+        want = polar.pack([np.zeros((1, n), dtype=np.int64) for n in polar.angle_count(128)], 128, b1, b2).shape[1]
+        assert lib.tq_polar_code_bytes(128, b1, b2) == want
+    assert lib.tq_polar_code_bytes(128, 4, 2) == 48
+    assert lib.tq_polar_code_bytes(100, 4, 2) == 0 and lib.tq_polar_code_bytes(128, 5, 2) == 0
+    with pytest.raises(lib.TQError):
+        lib.tq_polar_codebook(9, 2)
+    with pytest.raises(lib.TQError):
+        lib.tq_polar_codebook(2, 0)

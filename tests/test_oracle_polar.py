@@ -152,3 +152,37 @@ def test_packing_hand_worked_example():
     idx = [rng.integers(0, 1 << w, (10, cnt)) for cnt, w in zip(P.angle_count(128), P.level_bits(128, 4, 2))]
     back = P.unpack(P.pack(idx, 128, 4, 2), 128, 4, 2)
     assert all(np.array_equal(a, b) for a, b in zip(idx, back))
+
+
+def test_decode_is_softmax_attention_over_reconstructions():
+    """polar.decode equals the generic rotated-domain attention (textbook
+    softmax over <q', khat_t>, value sum, un-rotation) fed the explicit key
+    reconstructions n_t y_hat_t, for two batches, GQA 2 and a ragged length."""
+    from oracle import attention as A
+    from oracle import codebook as C
+    d, bsz, hkv, T = 128, 2, 2, 40
+    rng = np.random.default_rng(9)
+    pi = R.make_rotation(4, d, "rht")
+    k = rng.standard_normal((bsz, hkv, T, d)) * 2
+    v = rng.standard_normal((bsz, hkv, T, d))
+    q = rng.standard_normal((bsz, 4, d))
+    qz = P.quantize(k.reshape(-1, d), pi, 4, 2)
+    packed = P.pack(qz["idx"], d, 4, 2).reshape(bsz, hkv, T, -1)
+    vc, vt = C.lloyd_max(d, 3)
+    vy = (v.reshape(-1, d) @ pi.T) / np.linalg.norm(v.reshape(-1, d), axis=1, keepdims=True)
+    vidx = np.searchsorted(vt, vy, side="right").reshape(bsz, hkv, T, d)
+    vn = np.linalg.norm(v, axis=-1)
+    kcache = {"packed": packed, "norm16": qz["norm16"].reshape(bsz, hkv, T)}
+    vcache = {"idx": vidx, "norm16": vn}
+    lens = [T, 17]
+    out, logits = P.decode(q, kcache, vcache, lens, pi, 4, 2, vc)
+    yhat = P.reconstruct_rotated(qz["idx"], d, 4, 2).reshape(bsz, hkv, T, d)
+    for b in range(bsz):
+        for h in range(4):
+            kv = h // 2
+            L = lens[b]
+            khat = kcache["norm16"][b, kv, :L, None] * yhat[b, kv, :L]
+            vhat = vn[b, kv, :L, None] * vc[vidx[b, kv, :L]]
+            want, wl = A.attention_from_rotated(pi @ q[b, h], khat, vhat, 1 / np.sqrt(d), pi)
+            assert np.allclose(out[b, h], want, rtol=1e-12, atol=1e-12)
+            assert np.allclose(logits[b][h], wl, rtol=1e-12, atol=1e-12)
