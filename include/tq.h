@@ -25,6 +25,13 @@
  *     error word and lets the kernel return; tq_device_errors reads it
  *     (TQ_ERR_TIMEOUT).
  *   - tq_last_error() returns a thread-local message for the last failure.
+ *   - tq_attn_decode and tq_decode_step keep, per calling thread, the
+ *     validated plan of their last call: a call whose argument struct is
+ *     byte-for-byte the same (with the same host gqa_map contents, workspace,
+ *     current device, and no handle created, uploaded or freed since) skips
+ *     the validation and goes straight to its launches. A decode loop that
+ *     passes a constant max_seq_len (e.g. the capacity) hits it every step;
+ *     device-side values (lengths, positions, the data) may change freely.
  */
 #ifndef TQ_H
 #define TQ_H

@@ -513,13 +513,13 @@ tq_status polar_prepare(const tq_cache& c, QuantLaunch* L) {
         for (size_t j = 0; j < tt.size(); ++j) {
             pq.cb.tc[lev - 1][j] = (float)std::cos(tt[j]);
             pq.cb.ts[lev - 1][j] = (float)std::sin(tt[j]);
-            pq.cb.t64[lev - 1][j] = tt[j];
+            pq.cb.tc64[lev - 1][j] = std::cos(tt[j]);
+            pq.cb.ts64[lev - 1][j] = std::sin(tt[j]);
         }
     }
     pq.q = L->p;
     pq.bits1 = c.bits;
     pq.bits2 = c.bits2;
-    pq.inv_w1 = (float)((double)(1 << c.bits) / (2.0 * M_PI));
     pq.guard = L->rht ? 3.0e-6f : 4.0e-6f;
     L->polar = true;
     return TQ_OK;
@@ -774,9 +774,57 @@ tq_status decode_launch(const DecodeLaunch& D, cudaStream_t st, tqk::StepPrepPar
 
 }  // namespace
 
+namespace {
+
+// One prepared decode call per thread. A decode loop passes the same
+// arguments every step (only the device-side lengths, positions and the
+// data change), so the last call's validation, split plan, lookup tables and
+// parameter blocks are reused when its argument bytes, the host GQA map, the
+// workspace, the current device and the handle generation all match; any
+// difference prepares the call from scratch.
+struct PreparedCall {
+    bool valid = false;
+    std::vector<unsigned char> key, probe;
+    DecodeLaunch D;
+    tqk::StepPrepParams sp;
+
+    void build(std::vector<unsigned char>& k, const void* args, size_t n, const tq_decode_args& at, const void* ws,
+               size_t wsb) const {
+        int dev = -1;
+        cudaGetDevice(&dev);
+        const uint64_t gen = tq::handle_generation();
+        const size_t nmap = at.gqa_map ? (size_t)std::max(at.hq, 0) * sizeof(int32_t) : 0;
+        k.resize(n + nmap + sizeof(ws) + sizeof(wsb) + sizeof(dev) + sizeof(gen));
+        unsigned char* o = k.data();
+        std::memcpy(o, args, n);
+        o += n;
+        if (nmap) std::memcpy(o, at.gqa_map, nmap);
+        o += nmap;
+        std::memcpy(o, &ws, sizeof(ws));
+        o += sizeof(ws);
+        std::memcpy(o, &wsb, sizeof(wsb));
+        o += sizeof(wsb);
+        std::memcpy(o, &dev, sizeof(dev));
+        o += sizeof(dev);
+        std::memcpy(o, &gen, sizeof(gen));
+    }
+    bool match(const void* args, size_t n, const tq_decode_args& at, const void* ws, size_t wsb) {
+        build(probe, args, n, at, ws, wsb);
+        return valid && probe == key;
+    }
+    void remember() {  // after a successful prepare of the arguments last passed to match()
+        key.swap(probe);
+        valid = true;
+    }
+};
+thread_local PreparedCall t_decode_call, t_step_call;
+
+}  // namespace
+
 extern "C" {
 
 tq_status tq_rotation_to_device(tq_rotation* rot) {
+    tq::bump_handle_generation();
     if (!rot) return fail(TQ_ERR_INVALID_ARG, "tq_rotation_to_device: NULL handle");
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return fail(TQ_ERR_CUDA, "tq_rotation_to_device: no CUDA device");
@@ -829,6 +877,7 @@ tq_status tq_rotation_to_device(tq_rotation* rot) {
 }
 
 tq_status tq_free_rotation(tq_rotation* rot) {
+    tq::bump_handle_generation();
     if (!rot) return TQ_OK;
     if (rot->device >= 0) {
         int cur = -1;
@@ -847,6 +896,7 @@ tq_status tq_free_rotation(tq_rotation* rot) {
 }
 
 tq_status tq_qjl_to_device(tq_qjl* q) {
+    tq::bump_handle_generation();
     if (!q) return fail(TQ_ERR_INVALID_ARG, "tq_qjl_to_device: NULL handle");
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return fail(TQ_ERR_CUDA, "tq_qjl_to_device: no CUDA device");
@@ -880,6 +930,7 @@ tq_status tq_qjl_to_device(tq_qjl* q) {
 }
 
 tq_status tq_free_qjl(tq_qjl* q) {
+    tq::bump_handle_generation();
     if (!q) return TQ_OK;
     if (q->device >= 0) {
         int cur = -1;
@@ -911,9 +962,15 @@ size_t tq_attn_decode_workspace(const tq_decode_args* a) {
 }
 
 tq_status tq_attn_decode(const tq_decode_args* a, void* workspace, size_t ws_bytes, tq_stream stream) {
-    DecodeLaunch D;
+    if (!a) return fail(TQ_ERR_INVALID_ARG, "tq_attn_decode: args are NULL");
+    PreparedCall& pc = t_decode_call;
+    if (pc.match(a, sizeof(*a), *a, workspace, ws_bytes)) return decode_launch(pc.D, (cudaStream_t)stream, nullptr);
+    pc.valid = false;
+    DecodeLaunch D;  // prepared from scratch: no field of an earlier call survives
     tq_status s = decode_prepare(a, workspace, ws_bytes, &D);
     if (s != TQ_OK) return s;
+    pc.D = D;
+    pc.remember();
     return decode_launch(D, (cudaStream_t)stream, nullptr);
 }
 
@@ -1024,12 +1081,14 @@ tq_status tq_score_topk(const tq_topk_args* a, void* workspace, size_t ws_bytes,
 }
 
 int tq_topk_force_simt(int on) {
+    tq::bump_handle_generation();
     const int prev = g_topk_simt ? 1 : 0;
     g_topk_simt = on != 0;
     return prev;
 }
 
 int tq_quantize_force_mma_sync(int on) {
+    tq::bump_handle_generation();
     const int prev = g_quant_umma ? 0 : 1;
     g_quant_umma = on == 0;
     return prev;
@@ -1039,6 +1098,12 @@ size_t tq_decode_step_workspace(const tq_step_args* a) { return a ? tq_attn_deco
 
 tq_status tq_decode_step(const tq_step_args* a, void* workspace, size_t ws_bytes, tq_stream stream) {
     if (!a) return fail(TQ_ERR_INVALID_ARG, "tq_decode_step: args are NULL");
+    PreparedCall& pc = t_step_call;
+    if (pc.match(a, sizeof(*a), a->attn, workspace, ws_bytes)) {
+        tqk::StepPrepParams sp = pc.sp;
+        return decode_launch(pc.D, (cudaStream_t)stream, &sp);
+    }
+    pc.valid = false;
     const tq_decode_args& at = a->attn;
     if (at.k.mode == TQ_POLAR)
         return fail(TQ_ERR_UNSUPPORTED, "tq_decode_step: PolarQuant keys are appended with tq_quantize_kv, then tq_attn_decode");
@@ -1073,6 +1138,9 @@ tq_status tq_decode_step(const tq_step_args* a, void* workspace, size_t ws_bytes
     if (!ek) step_append(LK, &sp);
     if (!ev) step_append(LV, &sp);
     D.dp.append_pos = a->append_pos;
+    pc.D = D;
+    pc.sp = sp;
+    pc.remember();
     return decode_launch(D, (cudaStream_t)stream, &sp);
 }
 

@@ -32,6 +32,7 @@ struct StepSmem {
     __align__(16) float y[128];  // butterfly exchange, then the residual r (append) or q' (query)
     float qp[128];      // query: q' = Pi q
     float u[128];       // query: u = S q'
+    __align__(16) float part[4][128];  // dense rotation: the four warps' partial sums of Pi x
     float cent[kMaxLevels];
     float cent2[kMaxLevels];  // the second channel group's centroids (two-width caches)
     float red[4];
@@ -193,17 +194,24 @@ __device__ __forceinline__ void append_vector(const QuantParams& p, int xdtype, 
     if (rht) {
         y = wht128(xi * p.sgn[i], s) * (p.inv_sqrt_d * inv_n);
     } else {
-        // row i of Pi is column i of Pi^T: coalesced over the threads; four
-        // interleaved partial sums
-        float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-#pragma unroll 8
-        for (int e = 0; e < D; e += 4) {
-            a0 = fmaf(__ldg(p.pit32 + e * D + i), s.x[e], a0);
-            a1 = fmaf(__ldg(p.pit32 + (e + 1) * D + i), s.x[e + 1], a1);
-            a2 = fmaf(__ldg(p.pit32 + (e + 2) * D + i), s.x[e + 2], a2);
-            a3 = fmaf(__ldg(p.pit32 + (e + 3) * D + i), s.x[e + 3], a3);
+        // warp w takes inputs e = 32w .. 32w+31 and lane l outputs 4l .. 4l+3:
+        // the lane's 32 row segments of Pi^T are independent 16-byte loads,
+        // all in flight at once; the four warps' partial sums meet in s.part
+        // (s.x was published by step_sum's barriers)
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+        for (int kk = 0; kk < 32; ++kk) {
+            const int e = 32 * warp + kk;
+            const float4 t = __ldg(reinterpret_cast<const float4*>(p.pit32 + (size_t)e * D) + lane);
+            const float xe = s.x[e];
+            acc.x = fmaf(t.x, xe, acc.x);
+            acc.y = fmaf(t.y, xe, acc.y);
+            acc.z = fmaf(t.z, xe, acc.z);
+            acc.w = fmaf(t.w, xe, acc.w);
         }
-        y = ((a0 + a1) + (a2 + a3)) * inv_n;
+        *reinterpret_cast<float4*>(&s.part[warp][4 * lane]) = acc;
+        step_sync();
+        y = ((s.part[0][i] + s.part[1][i]) + (s.part[2][i] + s.part[3][i])) * inv_n;
     }
 
     // ---- bucketize with the guard band ----

@@ -24,17 +24,27 @@ __device__ __forceinline__ void prep_row128(const PrepParams& p, int64_t row, St
     if (p.rht) {
         y = wht128(qi * p.sgn[i], s) * p.inv_sqrt_d;
     } else {
+        // warp w takes inputs e = 32w .. 32w+31, lane l outputs 4l .. 4l+3:
+        // each lane's 32 row segments of Pi^T are independent 16-byte loads,
+        // issued together (one round of memory latency, not one per
+        // dependent batch), then the four warps' partial sums are added
         s.x[i] = qi;
         step_sync();
-        float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;  // four interleaved partial sums
-#pragma unroll 8
-        for (int e = 0; e < D; e += 4) {
-            a0 = fmaf(__ldg(p.pit32 + e * D + i), s.x[e], a0);
-            a1 = fmaf(__ldg(p.pit32 + (e + 1) * D + i), s.x[e + 1], a1);
-            a2 = fmaf(__ldg(p.pit32 + (e + 2) * D + i), s.x[e + 2], a2);
-            a3 = fmaf(__ldg(p.pit32 + (e + 3) * D + i), s.x[e + 3], a3);
+        const int w = i >> 5, l = i & 31;
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            const int e = 32 * w + k;
+            const float4 t = __ldg(reinterpret_cast<const float4*>(p.pit32 + (size_t)e * D) + l);
+            const float xe = s.x[e];
+            acc.x = fmaf(t.x, xe, acc.x);
+            acc.y = fmaf(t.y, xe, acc.y);
+            acc.z = fmaf(t.z, xe, acc.z);
+            acc.w = fmaf(t.w, xe, acc.w);
         }
-        y = (a0 + a1) + (a2 + a3);
+        *reinterpret_cast<float4*>(&s.part[w][4 * l]) = acc;
+        step_sync();
+        y = (s.part[0][i] + s.part[1][i]) + (s.part[2][i] + s.part[3][i]);
     }
     s.qp[i] = y;
     if (p.qprime) p.qprime[row * D + i] = y;

@@ -277,9 +277,19 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
     } else {
         // o_i = sum_k Pi[k][i] a_k, the k range split over 1024 / d groups of d threads
         const int ug = kCombineThreads / d, i = tid % d, ugrp = tid / d;
+        const int nk = d / ug;  // rows of Pi a thread takes: 4, 16 or 64 for d = 64, 128, 256
         float part = 0.0f;
-#pragma unroll 4
-        for (int k = ugrp; k < d; k += ug) part = fmaf(__ldg(p.pi32 + (size_t)k * d + i), s_a[k], part);
+        // 16 independent loads into registers first, then the products: one
+        // round of memory latency per 16 rows, not one per row
+        for (int k0 = 0; k0 < nk; k0 += 16) {
+            float pv[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                pv[j] = k0 + j < nk ? __ldg(p.pi32 + (size_t)(ugrp + (k0 + j) * ug) * d + i) : 0.0f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (k0 + j < nk) part = fmaf(pv[j], s_a[ugrp + (k0 + j) * ug], part);
+        }
         s_v[tid] = part;
         __syncthreads();
         if (tid < d)
@@ -349,7 +359,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_rows_kernel(const __gr
         *reinterpret_cast<float4*>(&s_a[warp][4 * lane]) = make_float4(y[0], y[1], y[2], y[3]);
         __syncwarp();
         o[0] = o[1] = o[2] = o[3] = 0.0f;
-#pragma unroll 8
+#pragma unroll 32
         for (int k = 0; k < 128; ++k) {
             const float ak = s_a[warp][k];
             const float4 pk = __ldg(reinterpret_cast<const float4*>(p.pi32 + (size_t)k * 128) + lane);

@@ -10,6 +10,7 @@
 // article, "Rotate, then quantize").
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <map>
@@ -30,6 +31,12 @@ tq_status fail(tq_status s, const std::string& msg) {
 }
 
 void clear_error() { g_last_error.clear(); }
+
+namespace {
+std::atomic<uint64_t> g_generation{0};
+}
+uint64_t handle_generation() { return g_generation.load(std::memory_order_acquire); }
+void bump_handle_generation() { g_generation.fetch_add(1, std::memory_order_acq_rel); }
 
 // ---------------------------------------------------------------------------
 // SplitMix64 (Steele, Lea & Flood 2014), counter form: the k-th draw of a
@@ -456,6 +463,7 @@ tq_status tq_make_rotation(uint64_t seed, int d, int kind, tq_rotation** out) {
             }
     }
     *out = r;
+    tq::bump_handle_generation();
     return TQ_OK;
 }
 
@@ -484,6 +492,7 @@ tq_status tq_make_qjl(uint64_t seed, int m, int d, tq_qjl** out) {
     tq::gaussians(seed, (int64_t)m * d, q->s.data());
     for (double& v : q->s) v = tq::round_bf16(v);
     *out = q;
+    tq::bump_handle_generation();
     return TQ_OK;
 }
 

@@ -15,18 +15,19 @@
 // node l, and (level l >= 3) node lane >> (l - 2) with the partner radius
 // from a shuffle. Decisions in fp32 without the angle: for a boundary t of
 // the pair (a, b), psi >= t exactly when b cos t - a sin t >= 0 (the cross
-// product is rho sin(psi - t)); level 1 first places psi by atan2f on the
-// uniform grid, then checks the two boundaries around it. A cross product
-// within `guard` of zero (or a pair next to the cut at +-pi) sends the whole
-// vector to an fp64 recomputation (rotation, atan2, hypot, comparisons with
-// the fp64 boundaries), so every code is the one an fp64 evaluation gives.
+// product is rho sin(psi - t)): level 1 takes the half plane from the sign of
+// the second component, then bisects the cells inside it; the other levels
+// bisect their quarter circle. A cross product within `guard` of zero at an
+// edge of the chosen cell (or a pair next to the cut at +-pi) sends the whole
+// vector to an fp64 recomputation (rotation, the same cross products against
+// the fp64 boundaries' cosines and sines), so every code is the one an fp64
+// evaluation gives. Radii are sqrt(a^2 + b^2): y is a unit vector.
 #include "common.cuh"
 #include "tq_launch.h"
 
 namespace tqk {
 
 constexpr int kPqWarps = 8;
-constexpr float kPi = 3.14159265358979323846f;
 
 // fp64 butterflies of y (4 coordinates per lane): strides 1, 2 in the lane,
 // 4 .. 64 across lanes
@@ -47,6 +48,69 @@ __device__ __forceinline__ void fwht128_f64(double (&y)[4], int lane) {
     }
 }
 
+// psi >= t_j for the pair (a, b) and the boundary t_j = (tc, ts), when
+// |psi - t_j| < pi: the sign of the cross product rho sin(psi - t_j)
+template <typename F>
+__device__ __forceinline__ F cross(F a, F b, F tc, F ts) { return fma(b, tc, -a * ts); }
+
+// The level-1 code of (a, b) (cells of 2 pi / L1 from -pi; boundary j at
+// index j - 1 of tc / ts): the half plane from the sign of b (boundary
+// L1 / 2 is 0, the cut is +-pi), then bisection by cross products inside it,
+// whose boundaries all lie within pi of psi. Flags the pair when b or either
+// edge of the chosen cell is within g of zero.
+__device__ __forceinline__ int level1_code(float a, float b, int L1, const float* tc, const float* ts, float g,
+                                           bool& flag) {
+    int lo = b >= 0.0f ? L1 / 2 : 0;
+    for (int step = L1 / 4; step >= 1; step >>= 1) {
+        const int j = lo + step;
+        if (cross(a, b, tc[j - 1], ts[j - 1]) >= 0.0f) lo = j;
+    }
+    flag |= !(fabsf(b) >= g);
+    if (lo >= 1) flag |= !(cross(a, b, tc[lo - 1], ts[lo - 1]) >= g);
+    if (lo + 1 <= L1 - 1) flag |= !(cross(a, b, tc[lo], ts[lo]) <= -g);
+    return lo;
+}
+
+// The code of a level >= 2 angle (a, b >= 0, psi in [0, pi/2], L cells):
+// bisection by cross products; flags the pair when an edge of the chosen
+// cell is within g of zero (which covers a radius near 0 too).
+__device__ __forceinline__ int upper_code(float a, float b, int L, const float* tc, const float* ts, float g,
+                                          bool& flag) {
+    int lo = 0;
+    for (int step = L / 2; step >= 1; step >>= 1) {
+        const int j = lo + step;
+        if (cross(a, b, tc[j - 1], ts[j - 1]) >= 0.0f) lo = j;
+    }
+    if (lo >= 1) flag |= !(cross(a, b, tc[lo - 1], ts[lo - 1]) >= g);
+    if (lo + 1 <= L - 1) flag |= !(cross(a, b, tc[lo], ts[lo]) <= -g);
+    return lo;
+}
+
+// The same decisions in fp64, with atan2's answers where a component is
+// zero: psi = atan2(b, a) lies in the lower half exactly when b < 0 or b is
+// -0 with a < 0 or a = -0 (psi = -pi); the origin's angle is +-0 (code
+// L1 / 2) or +-pi (code L1 - 1 or 0).
+__device__ __forceinline__ int level1_code64(double a, double b, int L1, const double* tc, const double* ts) {
+    const bool down = b < 0.0 || (b == 0.0 && signbit(b) && signbit(a));
+    if (a == 0.0 && b == 0.0) return down ? 0 : (signbit(a) ? L1 - 1 : L1 / 2);
+    int lo = down ? 0 : L1 / 2;
+    for (int step = L1 / 4; step >= 1; step >>= 1) {
+        const int j = lo + step;
+        if (cross(a, b, tc[j - 1], ts[j - 1]) >= 0.0) lo = j;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ int upper_code64(double a, double b, int L, const double* tc, const double* ts) {
+    if (a == 0.0 && b == 0.0) return 0;  // atan2(0, 0) = 0: below every boundary
+    int lo = 0;
+    for (int step = L / 2; step >= 1; step >>= 1) {
+        const int j = lo + step;
+        if (cross(a, b, tc[j - 1], ts[j - 1]) >= 0.0) lo = j;
+    }
+    return lo;
+}
+
 template <typename XT, bool RHT>
 __global__ void __launch_bounds__(kPqWarps * 32) polar_quantize_kernel(const __grid_constant__ PolarQuantParams P) {
     const QuantParams& p = P.q;
@@ -60,7 +124,7 @@ __global__ void __launch_bounds__(kPqWarps * 32) polar_quantize_kernel(const __g
     }
     __syncthreads();
     const int B1 = P.bits1, B2 = P.bits2;
-    const int L1 = 1 << B1, NB2 = (1 << B2) - 1;
+    const int L1 = 1 << B1, L2 = 1 << B2;
     const float g = P.guard;
     float sg[4];
     if constexpr (RHT) {
@@ -156,49 +220,21 @@ __global__ void __launch_bounds__(kPqWarps * 32) polar_quantize_kernel(const __g
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const float a = y[2 * q], b = y[2 * q + 1];
-            const float psi = atan2f(b, a);
-            int k = (int)floorf((psi + kPi) * P.inv_w1);
-            k = k < 0 ? 0 : (k > L1 - 1 ? L1 - 1 : k);
-            if (k >= 1) {  // psi >= t_k (boundary k - 1 of the list)
-                const float sl = fmaf(b, s_tc[0][k - 1], -a * s_ts[0][k - 1]);
-                flag |= !(sl >= g);
-            }
-            if (k <= L1 - 2) {  // psi < t_(k+1)
-                const float sh = fmaf(b, s_tc[0][k], -a * s_ts[0][k]);
-                flag |= !(sh <= -g);
-            }
-            flag |= a < g && fabsf(b) < g;  // next to the cut at +-pi (or the origin)
-            c1[q] = k;
-            rho[q] = hypotf(a, b);
+            c1[q] = level1_code(a, b, L1, s_tc[0], s_ts[0], g, flag);
+            rho[q] = sqrtf(fmaf(a, a, b * b));  // |y| <= 1: no overflow
         }
-        // level 2: node `lane` from the lane's two level-1 radii
         int cl[kPolarLevels];  // codes of levels 2 .. 7 at index 1 .. 6
-        float r_cur;
-        {
-            const float a = rho[0], b = rho[1];
-            int k = 0;
-            for (int j = 0; j < NB2; ++j) {
-                const float sj = fmaf(b, s_tc[1][j], -a * s_ts[1][j]);
-                k += sj >= 0.0f ? 1 : 0;
-                flag |= !(fabsf(sj) >= g);
-            }
-            cl[1] = k;
-            r_cur = hypotf(a, b);
-        }
+        // level 2: node `lane` from the lane's two level-1 radii
+        cl[1] = upper_code(rho[0], rho[1], L2, s_tc[1], s_ts[1], g, flag);
+        float r_cur = sqrtf(fmaf(rho[0], rho[0], rho[1] * rho[1]));
 #pragma unroll
         for (int lev = 3; lev <= kPolarLevels; ++lev) {
             const int sh = lev - 3;
             const float o = __shfl_xor_sync(TQ_FULL_MASK, r_cur, 1 << sh);
             const bool left = ((lane >> sh) & 1) == 0;
             const float a = left ? r_cur : o, b = left ? o : r_cur;
-            int k = 0;
-            for (int j = 0; j < NB2; ++j) {
-                const float sj = fmaf(b, s_tc[lev - 1][j], -a * s_ts[lev - 1][j]);
-                k += sj >= 0.0f ? 1 : 0;
-                flag |= !(fabsf(sj) >= g);
-            }
-            cl[lev - 1] = k;
-            r_cur = hypotf(a, b);
+            cl[lev - 1] = upper_code(a, b, L2, s_tc[lev - 1], s_ts[lev - 1], g, flag);
+            r_cur = sqrtf(fmaf(a, a, b * b));
         }
 
         // fp16 norm: near a rounding midpoint, decide from the fp64 norm
@@ -239,31 +275,19 @@ __global__ void __launch_bounds__(kPqWarps * 32) polar_quantize_kernel(const __g
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     const double a = y64[2 * q], b = y64[2 * q + 1];
-                    const double psi = atan2(b, a);
-                    int k = 0;
-                    for (int j = 0; j < L1 - 1; ++j) k += P.cb.t64[0][j] <= psi ? 1 : 0;
-                    c1[q] = k;
-                    rr[q] = hypot(a, b);
+                    c1[q] = level1_code64(a, b, L1, P.cb.tc64[0], P.cb.ts64[0]);
+                    rr[q] = sqrt(fma(a, a, b * b));
                 }
-                double r64;
-                {
-                    const double psi = atan2(rr[1], rr[0]);
-                    int k = 0;
-                    for (int j = 0; j < NB2; ++j) k += P.cb.t64[1][j] <= psi ? 1 : 0;
-                    cl[1] = k;
-                    r64 = hypot(rr[0], rr[1]);
-                }
+                cl[1] = upper_code64(rr[0], rr[1], L2, P.cb.tc64[1], P.cb.ts64[1]);
+                double r64 = sqrt(fma(rr[0], rr[0], rr[1] * rr[1]));
 #pragma unroll
                 for (int lev = 3; lev <= kPolarLevels; ++lev) {
                     const int sh = lev - 3;
                     const double o = __shfl_xor_sync(TQ_FULL_MASK, r64, 1 << sh);
                     const bool left = ((lane >> sh) & 1) == 0;
                     const double a = left ? r64 : o, b = left ? o : r64;
-                    const double psi = atan2(b, a);
-                    int k = 0;
-                    for (int j = 0; j < NB2; ++j) k += P.cb.t64[lev - 1][j] <= psi ? 1 : 0;
-                    cl[lev - 1] = k;
-                    r64 = hypot(a, b);
+                    cl[lev - 1] = upper_code64(a, b, L2, P.cb.tc64[lev - 1], P.cb.ts64[lev - 1]);
+                    r64 = sqrt(fma(a, a, b * b));
                 }
             }
         }

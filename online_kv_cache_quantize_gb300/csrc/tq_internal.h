@@ -59,4 +59,9 @@ tq_status polar_codebook(int level, int bits, std::vector<double>& c, std::vecto
 tq_status fail(tq_status s, const std::string& msg);
 void clear_error();
 
+// Bumped by every call that creates, uploads or frees a handle or flips a
+// kernel switch: a prepared call is reused only while it is unchanged.
+uint64_t handle_generation();
+void bump_handle_generation();
+
 }  // namespace tq

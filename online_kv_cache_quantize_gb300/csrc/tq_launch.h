@@ -67,21 +67,22 @@ cudaError_t launch_quantize_umma(const QuantParams& p, const void* w_umma, const
 cudaError_t launch_quantize(const QuantParams& p, int dtype, int rht, int prod, int code_bits,
                             cudaStream_t s);
 
-// PolarQuant keys (d = 128): the angle codebooks of the 7 levels. Decisions
-// of the fp32 path are signs of b cos t - a sin t (= rho sin(psi - t)) for a
-// boundary t of the pair (a, b); the fp64 path compares atan2 with t64.
+// PolarQuant keys (d = 128): the angle codebooks of the 7 levels as the
+// cosines and sines of their boundaries t_j: a decision psi >= t_j is the
+// sign of b cos t_j - a sin t_j (= rho sin(psi - t_j)) for the pair (a, b),
+// in fp32, and in fp64 where the fp32 one is too close to call.
 constexpr int kPolarLevels = 7;
 struct PolarCodebook {
     float tc[kPolarLevels][15];     // cos t_j
     float ts[kPolarLevels][15];     // sin t_j
-    double t64[kPolarLevels][15];   // t_j (fp64)
+    double tc64[kPolarLevels][15];
+    double ts64[kPolarLevels][15];
 };
 
 struct PolarQuantParams {
     QuantParams q;      // input, slots, codes (the angle stream), norm, rotation, err
     PolarCodebook cb;
     int bits1, bits2;   // level-1 and higher-level code widths
-    float inv_w1;       // 2^bits1 / (2 pi): level-1 cell index from the angle
     float guard;        // |b cos t - a sin t| below this is re-decided in fp64
 };
 

@@ -341,3 +341,31 @@ def test_unsupported_calls_are_refused():
     with pytest.raises(B.TQError) as e:
         B.tq_attn_prefill(qp, gk, gv, qs, cap, rot, qjl, op_, ws)
     assert "UNSUPPORTED" in str(e.value)
+
+
+def test_alternating_polar_and_turboquant_decodes_on_one_thread():
+    """The library reuses the last prepared decode call of a thread when the
+    arguments repeat: alternating PolarQuant and TurboQuant key caches (and
+    repeating each) must give each call its own kernels and the same outputs
+    as the first run."""
+    hkv, cap = 2, 256
+    k, v = W.decode_kv(1, hkv, cap, seed=31)
+    kc, vc, gk, gv, pi = _oracle_caches(k, v, 4, 2, 3, "rht")
+    rot, qjl = P.handles(D, "rht")
+    tk = B.Cache("prod", 3, D, rows=hkv, capacity=cap)
+    B.tq_quantize_kv(tk, rot, torch.from_numpy(k.reshape(-1, D)).cuda().to(torch.bfloat16), qjl=qjl)
+    q = torch.from_numpy(W.query_vectors((1, 8, D), seed=32)).cuda()
+    lens = torch.tensor([200], dtype=torch.int32, device="cuda")
+    outs = {}
+    for rep in range(3):
+        for name, kcache, qj in (("polar", gk, None), ("turbo", tk, qjl)):
+            out = torch.empty((1, 8, D), device="cuda")
+            ws = B.workspace(B.tq_attn_decode_workspace(q, kcache, gv, lens, cap, rot, qj, out))
+            B.tq_attn_decode(q, kcache, gv, lens, cap, rot, qj, out, ws)
+            B.tq_attn_decode(q, kcache, gv, lens, cap, rot, qj, out, ws)  # the same arguments again
+            torch.cuda.synchronize()
+            if rep == 0:
+                outs[name] = out.clone()
+            else:
+                assert torch.equal(out, outs[name]), (name, rep)
+    assert not torch.equal(outs["polar"], outs["turbo"])
