@@ -16,12 +16,12 @@
 // from a shuffle. Decisions in fp32 without the angle: for a boundary t of
 // the pair (a, b), psi >= t exactly when b cos t - a sin t >= 0 (the cross
 // product is rho sin(psi - t)): level 1 takes the half plane from the sign of
-// the second component, then bisects the cells inside it; the other levels
-// bisect their quarter circle. A cross product within `guard` of zero at an
-// edge of the chosen cell (or a pair next to the cut at +-pi) sends the whole
+// the second component, then locates psi inside it; the other levels count
+// their boundaries from the squared radii (no square roots). A cross product
+// within `guard` of zero (or a pair next to the cut at +-pi) sends the whole
 // vector to an fp64 recomputation (rotation, the same cross products against
-// the fp64 boundaries' cosines and sines), so every code is the one an fp64
-// evaluation gives. Radii are sqrt(a^2 + b^2): y is a unit vector.
+// the fp64 boundaries' cosines and sines, radii by fp64 square roots), so
+// every code is the one an fp64 evaluation gives.
 #include "common.cuh"
 #include "tq_launch.h"
 
@@ -58,32 +58,68 @@ __device__ __forceinline__ F cross(F a, F b, F tc, F ts) { return fma(b, tc, -a 
 // L1 / 2 is 0, the cut is +-pi), then bisection by cross products inside it,
 // whose boundaries all lie within pi of psi. Flags the pair when b or either
 // edge of the chosen cell is within g of zero.
-__device__ __forceinline__ int level1_code(float a, float b, int L1, const float* tc, const float* ts, float g,
-                                           bool& flag) {
+__device__ __forceinline__ float xcross(float a, float b, float2 t) { return fmaf(b, t.x, -a * t.y); }
+
+// t[j - 1] = (cos t_j, sin t_j). With L1 a compile-time constant (the
+// default widths) the bisection unrolls completely.
+__device__ __forceinline__ int level1_code(float a, float b, int L1, const float2* t, float g, bool& flag) {
     int lo = b >= 0.0f ? L1 / 2 : 0;
+#pragma unroll
     for (int step = L1 / 4; step >= 1; step >>= 1) {
         const int j = lo + step;
-        if (cross(a, b, tc[j - 1], ts[j - 1]) >= 0.0f) lo = j;
+        if (xcross(a, b, t[j - 1]) >= 0.0f) lo = j;
     }
     flag |= !(fabsf(b) >= g);
-    if (lo >= 1) flag |= !(cross(a, b, tc[lo - 1], ts[lo - 1]) >= g);
-    if (lo + 1 <= L1 - 1) flag |= !(cross(a, b, tc[lo], ts[lo]) <= -g);
+    if (lo >= 1) flag |= !(xcross(a, b, t[lo - 1]) >= g);
+    if (lo + 1 <= L1 - 1) flag |= !(xcross(a, b, t[lo]) <= -g);
     return lo;
 }
 
-// The code of a level >= 2 angle (a, b >= 0, psi in [0, pi/2], L cells):
-// bisection by cross products; flags the pair when an edge of the chosen
-// cell is within g of zero (which covers a radius near 0 too).
-__device__ __forceinline__ int upper_code(float a, float b, int L, const float* tc, const float* ts, float g,
-                                          bool& flag) {
-    int lo = 0;
-    for (int step = L / 2; step >= 1; step >>= 1) {
-        const int j = lo + step;
-        if (cross(a, b, tc[j - 1], ts[j - 1]) >= 0.0f) lo = j;
+// Branch-free level 1 for a compile-time width: the lower half plane is the
+// upper one turned by pi (t_j - pi = t_(j + L1/2) and (a, b) -> (-a, -b)
+// negates every cross product), so after the turn the code is L1/2 (upper
+// half) or 0 plus the count of the upper half's L1/2 - 1 boundaries below psi
+// (t = the table from boundary L1/2 + 1 on). Every cross product takes part
+// in the guard (a far boundary is only close to zero when the radius is).
+template <int L1>
+__device__ __forceinline__ int level1_code_lin(float a, float b, const float2* t, float g, bool& flag) {
+    const bool up = b >= 0.0f;
+    const float aa = up ? a : -a, bb = up ? b : -b;
+    int k = up ? L1 / 2 : 0;
+    float m = fabsf(b);
+#pragma unroll
+    for (int j = 0; j < L1 / 2 - 1; ++j) {
+        const float c = xcross(aa, bb, t[j]);
+        k += c >= 0.0f ? 1 : 0;
+        m = fminf(m, fabsf(c));
     }
-    if (lo >= 1) flag |= !(cross(a, b, tc[lo - 1], ts[lo - 1]) >= g);
-    if (lo + 1 <= L - 1) flag |= !(cross(a, b, tc[lo], ts[lo]) <= -g);
-    return lo;
+    flag |= !(m >= g);
+    return k;
+}
+
+// A level >= 2 angle from the squared radii A = a^2, B = b^2 (no square
+// root anywhere in the tree): for a, b >= 0 and t in (0, pi/2) the cross
+// product b cos t - a sin t has the sign of B cos^2 t - A sin^2 t, which is
+// (b cos t - a sin t)(b cos t + a sin t) with a second factor of at most
+// sqrt(A + B). So |b cos t - a sin t| < g implies (B cos^2 t - A sin^2 t)^2 <
+// g^2 (A + B): flagging on the latter (or on equality, which also catches an
+// all-zero block) flags every decision the fp32 values cannot make.
+// t2[j] = (cos^2 t_(j+1), sin^2 t_(j+1)); L = 0: the width from Lr.
+template <int L>
+__device__ __forceinline__ int upper_code_sq(float A, float B, int Lr, const float2* t2, float g2, bool& flag) {
+    const int n = (L > 0 ? L : Lr) - 1;
+    const float thr = g2 * (A + B);
+    int k = 0;
+    bool f = false;
+#pragma unroll
+    for (int j = 0; j < (L > 0 ? L - 1 : 15); ++j) {
+        if (L == 0 && j >= n) break;
+        const float c = fmaf(B, t2[j].x, -A * t2[j].y);
+        k += c >= 0.0f ? 1 : 0;
+        f |= !(c * c > thr);
+    }
+    flag |= f;
+    return k;
 }
 
 // The same decisions in fp64, with atan2's answers where a component is
@@ -111,21 +147,26 @@ __device__ __forceinline__ int upper_code64(double a, double b, int L, const dou
     return lo;
 }
 
-template <typename XT, bool RHT>
+// B1T, B2T: compile-time code widths (the default 4 / 2), or 0 to take them
+// from the parameters
+template <typename XT, bool RHT, int B1T, int B2T>
 __global__ void __launch_bounds__(kPqWarps * 32) polar_quantize_kernel(const __grid_constant__ PolarQuantParams P) {
     const QuantParams& p = P.q;
     __shared__ __align__(16) uint32_t s_w[kPqWarps][16];
     __shared__ float s_x[kPqWarps][128];
-    __shared__ float s_tc[kPolarLevels][16], s_ts[kPolarLevels][16];
+    __shared__ float2 s_t[16];                    // level 1: (cos t_j, sin t_j)
+    __shared__ float2 s_t2[kPolarLevels][16];     // levels >= 2: (cos^2 t_j, sin^2 t_j)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < kPolarLevels * 15; i += blockDim.x) {
-        s_tc[i / 15][i % 15] = P.cb.tc[i / 15][i % 15];
-        s_ts[i / 15][i % 15] = P.cb.ts[i / 15][i % 15];
+        const int lv = i / 15, j = i % 15;
+        if (lv == 0) s_t[j] = make_float2(P.cb.tc[0][j], P.cb.ts[0][j]);
+        else s_t2[lv][j] = make_float2((float)(P.cb.tc64[lv][j] * P.cb.tc64[lv][j]),
+                                       (float)(P.cb.ts64[lv][j] * P.cb.ts64[lv][j]));
     }
     __syncthreads();
-    const int B1 = P.bits1, B2 = P.bits2;
+    const int B1 = B1T > 0 ? B1T : P.bits1, B2 = B2T > 0 ? B2T : P.bits2;
     const int L1 = 1 << B1, L2 = 1 << B2;
-    const float g = P.guard;
+    const float g = P.guard, g2 = g * g;
     float sg[4];
     if constexpr (RHT) {
 #pragma unroll
@@ -216,25 +257,28 @@ __global__ void __launch_bounds__(kPqWarps * 32) polar_quantize_kernel(const __g
         // ---- the polar recursion in fp32 with guarded decisions ----
         bool flag = false;
         int c1[2];
-        float rho[2];
+        float R[2];  // squared level-1 radii
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const float a = y[2 * q], b = y[2 * q + 1];
-            c1[q] = level1_code(a, b, L1, s_tc[0], s_ts[0], g, flag);
-            rho[q] = sqrtf(fmaf(a, a, b * b));  // |y| <= 1: no overflow
+            if constexpr (B1T > 0)
+                c1[q] = level1_code_lin<(1 << B1T)>(a, b, &s_t[(1 << B1T) / 2], g, flag);
+            else
+                c1[q] = level1_code(a, b, L1, s_t, g, flag);
+            R[q] = fmaf(a, a, b * b);
         }
         int cl[kPolarLevels];  // codes of levels 2 .. 7 at index 1 .. 6
         // level 2: node `lane` from the lane's two level-1 radii
-        cl[1] = upper_code(rho[0], rho[1], L2, s_tc[1], s_ts[1], g, flag);
-        float r_cur = sqrtf(fmaf(rho[0], rho[0], rho[1] * rho[1]));
+        cl[1] = upper_code_sq<(B2T > 0 ? (1 << B2T) : 0)>(R[0], R[1], L2, s_t2[1], g2, flag);
+        float r_cur = R[0] + R[1];  // squared radius of the lane's level-2 node
 #pragma unroll
         for (int lev = 3; lev <= kPolarLevels; ++lev) {
             const int sh = lev - 3;
             const float o = __shfl_xor_sync(TQ_FULL_MASK, r_cur, 1 << sh);
             const bool left = ((lane >> sh) & 1) == 0;
             const float a = left ? r_cur : o, b = left ? o : r_cur;
-            cl[lev - 1] = upper_code(a, b, L2, s_tc[lev - 1], s_ts[lev - 1], g, flag);
-            r_cur = sqrtf(fmaf(a, a, b * b));
+            cl[lev - 1] = upper_code_sq<(B2T > 0 ? (1 << B2T) : 0)>(a, b, L2, s_t2[lev - 1], g2, flag);
+            r_cur = a + b;
         }
 
         // fp16 norm: near a rounding midpoint, decide from the fp64 norm
@@ -331,13 +375,16 @@ cudaError_t launch_polar_quantize(const PolarQuantParams& p, int dtype, int rht,
     const int64_t cap = (int64_t)sms * 8;
     if (blocks > cap) blocks = cap;
     const dim3 grid((unsigned)blocks), block(kPqWarps * 32);
+    const bool fast = p.bits1 == 4 && p.bits2 == 2;  // the default widths: compile-time
+#define TQ_PQ(XT, R)                                                              \
+    if (fast) polar_quantize_kernel<XT, R, 4, 2><<<grid, block, 0, s>>>(p);       \
+    else polar_quantize_kernel<XT, R, 0, 0><<<grid, block, 0, s>>>(p);
     if (dtype == 1) {
-        if (rht) polar_quantize_kernel<__nv_bfloat16, true><<<grid, block, 0, s>>>(p);
-        else polar_quantize_kernel<__nv_bfloat16, false><<<grid, block, 0, s>>>(p);
+        if (rht) { TQ_PQ(__nv_bfloat16, true) } else { TQ_PQ(__nv_bfloat16, false) }
     } else {
-        if (rht) polar_quantize_kernel<float, true><<<grid, block, 0, s>>>(p);
-        else polar_quantize_kernel<float, false><<<grid, block, 0, s>>>(p);
+        if (rht) { TQ_PQ(float, true) } else { TQ_PQ(float, false) }
     }
+#undef TQ_PQ
     return cudaGetLastError();
 }
 

@@ -126,20 +126,21 @@ def test_step_rejects_bad_args_before_enqueueing():
     assert torch.equal(kc.codes, before)
 
 
-@pytest.mark.parametrize("bsz,hkv,hq,T,kbits,vbits,heavy,samples", [
+@pytest.mark.parametrize("bsz,hkv,hq,T,kbits,vbits,heavy,samples,kind", [
     # the bench's default line: Llama-3.1-8B decode, 32768 tokens
-    (1, 8, 32, 32768, 3, 3, 0.0, [(0, 0), (0, 17), (0, 31)]),
-    # batched decode: 16 sequences of 8192 tokens
-    (16, 8, 32, 8192, 3, 3, 0.0, [(0, 5), (9, 20), (15, 31)]),
+    (1, 8, 32, 32768, 3, 3, 0.0, [(0, 0), (0, 17), (0, 31)], "rht"),
+    # batched decode: 16 sequences of 8192 tokens, both rotations
+    (16, 8, 32, 8192, 3, 3, 0.0, [(0, 5), (9, 20), (15, 31)], "rht"),
+    (16, 8, 32, 8192, 3, 3, 0.0, [(2, 1), (11, 26), (15, 30)], "dense"),
     # long context: 131072 tokens, 64 q / 8 KV heads, K 3-bit / V 4-bit, 1 % of tokens with norm x 10
-    (1, 8, 64, 131072, 3, 4, 0.01, [(0, 3), (0, 62)]),
+    (1, 8, 64, 131072, 3, 4, 0.01, [(0, 3), (0, 62)], "rht"),
 ])
-def test_full_size_step_sampled(bsz, hkv, hq, T, kbits, vbits, heavy, samples):
+def test_full_size_step_sampled(bsz, hkv, hq, T, kbits, vbits, heavy, samples, kind):
     """The benchmarked step at the workloads' full shapes and in the bench's
-    launch configuration (RHT, the new token appended at the last slot of
-    every sequence): the appended slots' packed records and sampled query
-    heads against the oracle."""
-    d, kind = 128, "rht"
+    launch configuration (the new token appended at the last slot of every
+    sequence): the appended slots' packed records and sampled query heads
+    against the oracle."""
+    d = 128
     k, v = W.decode_kv(bsz, hkv, T, seed=5, heavy_frac=heavy)
     rot, qjl = P.handles(d, kind)
     kc = B.Cache("prod", kbits, d, rows=bsz * hkv, capacity=T)
