@@ -24,14 +24,16 @@
 //  * TMA warp: tiled tensor copies of the 128-vector input tiles (two boxes
 //    of 64 coordinates x 128 rows with the 128-byte swizzle, the K-major
 //    layout the MMA reads) into a ring of shared-memory buffers;
-//  * MMA warp: the rotation MMAs of a tile into one of two TMEM buffers, and
-//    (keys) the sign-sketch MMAs with A = R read from TMEM;
+//  * MMA warp: the rotation MMAs of a tile into one of NB TMEM accumulators
+//    (four for values, two for keys), and (keys) the sign-sketch MMAs with
+//    A = R read from TMEM;
 //  * epilogue warps: thread = vector (its TMEM lane), each of the NP warps of
 //    a lane quarter takes 128 / NP coordinates. Phase 1: the norm from the
-//    staged input, then per 32 coordinates the rotated values from TMEM,
+//    staged input, then per 16 coordinates the rotated values from TMEM,
 //    codes by sign-bit arithmetic (below), the guard test, the residual, and
-//    R hi/lo written back over the columns just read. Phase 2 (keys): the
-//    signs of S r from TMEM.
+//    (keys) R hi/lo written into R's own 128 columns once the previous tile's
+//    sign-sketch MMAs have read them. Phase 2 (keys): the signs of S r from
+//    TMEM.
 // The epilogue runs phase 1 of tile i+1 before phase 2 of tile i, so the
 // sign-sketch MMAs of tile i overlap it.
 //
@@ -68,8 +70,8 @@ constexpr int kQuParts = 4;
 struct QuantUmmaParams {
     CUtensorMap tmap;     // the input: 2-D bf16 [n][128] (row stride x_stride), box 64 x 128, 128-byte swizzle
     QuantParams q;
-    const void* w_umma;   // rotation operand(s), 128 x 128 bf16 each, core-matrix layout
-    const void* s_umma;   // S, 128 x 128 bf16, core-matrix layout (keys)
+    const void* w_umma;   // rotation operand(s), 128 x 128 bf16 each, K-major with the 128-byte swizzle
+    const void* s_umma;   // S, 128 x 128 bf16, the same layout (keys)
 };
 
 template <int NP>

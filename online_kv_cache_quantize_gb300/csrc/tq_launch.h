@@ -57,8 +57,8 @@ cudaError_t launch_quantize_mma(const QuantParams& p, int dtype, int rht, int pr
 cudaError_t launch_quantize_mma2(const QuantParams& p, int dtype, int rht, int prod, int code_bits, cudaStream_t s);
 
 // tcgen05 quantize (d = m = 128, bf16 input with 16-byte aligned rows, one
-// code width): w_umma / s_umma are the rotation and S operands in the
-// core-matrix layout (tq_rotation::d_w_umma, tq_qjl::d_s_umma)
+// code width): w_umma / s_umma are the rotation and S operands, K-major with
+// the 128-byte swizzle (tq_rotation::d_w_umma, tq_qjl::d_s_umma)
 bool quantize_umma_supported(const QuantParams& p, int dtype, int code_bits);
 cudaError_t launch_quantize_umma(const QuantParams& p, const void* w_umma, const void* s_umma, int rht, int prod,
                                  int code_bits, cudaStream_t s);
