@@ -224,12 +224,12 @@ int tq_sign_bytes(int m);                /* per-slot stride of signs, bytes */
  *   else              -> slot0 + i (checked on the host against the cache).
  * Kernels: d = 128 (keys m = 128) and n <= 256, one CTA per vector (an append
  * costs a few microseconds however few vectors it has); d = 128 and more
- * vectors with bf16 input at one code width, tiles of 128 vectors on the
- * 5th-generation tensor cores (the rotation and S r as tcgen05 contractions
- * with TMEM accumulators); other d = 128 cases with 16-byte aligned rows (fp32
- * input, fractional-rate caches), 16 vectors per warp with the rotation and
- * S r on mma.sync; any other d, one warp per vector; PolarQuant caches, one
- * warp per vector. All follow the same precision rules: every code is the
+ * vectors with bf16 input (one code width, or the two widths of a
+ * fractional-rate cache), tiles of 128 vectors on the 5th-generation tensor
+ * cores (the rotation and S r as tcgen05 contractions with TMEM
+ * accumulators); other d = 128 cases with 16-byte aligned rows (fp32 input),
+ * 16 vectors per warp with the rotation and S r on mma.sync; any other d, one
+ * warp per vector; PolarQuant caches, one warp per vector. All follow the same precision rules: every code is the
  * one an fp64 evaluation gives, up to ties within a few fp64 ulps. */
 typedef struct {
     tq_cache cache;

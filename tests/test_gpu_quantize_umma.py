@@ -176,3 +176,29 @@ def test_agrees_with_the_mma_sync_kernel(kind):
     for c, lab in ((old, "mma.sync"), (new, "tcgen05")):
         P.compare_quantized(P.cache_to_numpy(c, x.shape[0]), qz, "prod", 3, 128, s, label=f"{lab}-{kind}")
     assert float((new.signs != old.signs).float().mean()) < 1e-3
+
+
+@pytest.mark.parametrize("kind", ["rht", "dense"])
+@pytest.mark.parametrize("mode,bits", [("prod", 3), ("prod", 4), ("mse", 2), ("mse", 3), ("mse", 4)])
+def test_two_width_persistent_and_agrees_with_mma_sync(kind, mode, bits):
+    """Fractional-rate caches (coordinates with i % 16 < 8 at `bits`, the
+    rest one bit narrower, each group with its own codebook) on the tcgen05
+    kernel over more tiles than SMs: codes, norms (and for keys gamma and the
+    signs) against the oracle, and codes and norms identical to the mma.sync
+    kernel's."""
+    n = 2 * 152 * 128 + 77
+    rng = np.random.default_rng(bits)
+    x = W.round_bf16((rng.standard_normal((n, 128)) * rng.lognormal(0, 0.5, (n, 1))).astype(np.float32))
+    new = P.gpu_quantize(x, mode, bits, 128, kind, dtype=torch.bfloat16, bits2=bits - 1)
+    pi, s = P.oracle_mats(128, kind, None)
+    qz = oq.quantize(x.astype(np.float64), pi, mode, bits, s if mode == "prod" else None, bits2=bits - 1)
+    rep = P.compare_quantized(P.cache_to_numpy(new, n), qz, mode, bits, 128, s, label=f"umma2-{kind}-{mode}{bits}",
+                              bits2=bits - 1)
+    assert rep["code_mismatch"] <= 1e-5 * rep["coords"] + 1
+    lib = B.load()
+    prev = lib.tq_quantize_force_mma_sync(1)
+    try:
+        old = P.gpu_quantize(x, mode, bits, 128, kind, dtype=torch.bfloat16, bits2=bits - 1)
+    finally:
+        lib.tq_quantize_force_mma_sync(prev)
+    assert torch.equal(new.codes, old.codes) and torch.equal(new.norm, old.norm)
