@@ -763,7 +763,8 @@ def run_prefill(args, name):
         "config": {"workload": name, "batch": bsz, "chunk": C, "hq": hq, "hkv": hkv, "d": d, "context": T,
                    "q_start": T - C, "rotation": w["rotation"], "k_bits": w["k_bits"], "v_bits": w["v_bits"],
                    "l2": "flushed (256 MiB write) before every timed step"},
-        "roofline": {"kernel": "prefill_mma_kernel (mma.sync)", "bound": "tensor", "achieved": achieved,
+        "roofline": {"kernel": ("prefill_umma_kernel (tcgen05)" if w["k_bits"] <= 3 else "prefill_mma_kernel (mma.sync)"),
+                     "bound": "tensor", "achieved": achieved,
                      "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_kind,
                      "alg_flops_per_step": flops, "traffic": None},
         "e2e": {"value": bsz * C / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": qpin.numel() * 2,

@@ -359,9 +359,12 @@ tq_status tq_decode_step(const tq_step_args* a, void* workspace, size_t ws_bytes
  * other token. Query head h reads KV head gqa_map[h] (default h / (hq / hkv)). The logits, softmax
  * and value sum are decode's; the write-ups give decode only, so the causal
  * chunk is this library's reading. A query with no visible slot gives 0.
- * Kernels: query prep (q' and u), the tensor-core scan (64 query rows per CTA
- * against 16-token tiles, split over the tokens), and a merge of the splits
- * (one warp per query row) with the un-rotation. */
+ * Kernels: query prep (q' and u), the scan split over the tokens, and a merge
+ * of the splits (one warp per query row) with the un-rotation. The scan runs
+ * on the tcgen05 tensor cores (128 query rows per CTA against 128-token
+ * tiles; scores and the value sum accumulated in TMEM) when the keys have 1
+ * or 2 code bits (PROD bits 2 or 3, or the 3 / 2 fractional rate), else on
+ * mma.sync (64 query rows per CTA against 16-token tiles). */
 typedef struct {
     const void* q;          /* device [batch][chunk][hq][d] of q_dtype         */
     int q_dtype;            /* TQ_F32 or TQ_BF16                              */
@@ -421,6 +424,11 @@ int tq_topk_force_simt(int on);
  * compare the two; returns the previous setting. Both give the same codes,
  * norms and signs (the exact fp64 decision near every boundary). */
 int tq_quantize_force_mma_sync(int on);
+/* Process-wide switch: on != 0 makes tq_attn_prefill use the mma.sync scan
+ * where it would take the tcgen05 one, to compare the two; returns the
+ * previous setting. Query the workspace again after switching (the split
+ * plans differ). */
+int tq_prefill_force_mma_sync(int on);
 
 /* ------------------------------------------------------------------------ *
  * Device error word.                                                       *

@@ -111,6 +111,7 @@ _SIGS = {
     "tq_decode_step": (_STATUS, [ctypes.POINTER(tq_step_args), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "tq_topk_force_simt": (ctypes.c_int, [ctypes.c_int]),
     "tq_quantize_force_mma_sync": (ctypes.c_int, [ctypes.c_int]),
+    "tq_prefill_force_mma_sync": (ctypes.c_int, [ctypes.c_int]),
     "tq_device_errors": (_STATUS, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "tq_selftest_bounded_wait": (_STATUS, [ctypes.c_uint32, ctypes.c_void_p]),
     "tq_selftest_umma_gemm": (_STATUS, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,

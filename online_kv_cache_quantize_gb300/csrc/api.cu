@@ -341,6 +341,10 @@ constexpr int64_t kSmallAppend = 256;
 // turns it off, for comparing the two kernels)
 bool g_quant_umma = true;
 
+// tq_attn_prefill takes the tcgen05 kernel where it applies
+// (tq_prefill_force_mma_sync turns it off, for comparing the two kernels)
+bool g_prefill_umma = true;
+
 struct QuantLaunch {
     tqk::QuantParams p;
     int dtype = 0, vpl = 1, cb = 1;
@@ -1087,6 +1091,13 @@ int tq_topk_force_simt(int on) {
     return prev;
 }
 
+int tq_prefill_force_mma_sync(int on) {
+    tq::bump_handle_generation();
+    const int prev = g_prefill_umma ? 0 : 1;
+    g_prefill_umma = on == 0;
+    return prev;
+}
+
 int tq_quantize_force_mma_sync(int on) {
     tq::bump_handle_generation();
     const int prev = g_quant_umma ? 0 : 1;
@@ -1150,8 +1161,17 @@ namespace {
 
 struct PrefillPlan {
     int group = 0, n_splits = 0, split_tokens = 0, lim_cap = 0;
+    bool umma = false;  // the tcgen05 kernel (128 rows x 128-token tiles per CTA)
     size_t off_u = 0, off_part = 0, total = 0;
 };
+
+// key / value code bits of a prefill's caches as the kernels see them, or -1
+// where the caches are not a PROD / MSE pair (the checks come later)
+void prefill_bits(const tq_prefill_args* a, int* kb, int* vb, bool* two) {
+    *kb = a->k.mode == TQ_PROD ? a->k.bits - 1 : -1;
+    *vb = a->v.mode == TQ_MSE ? a->v.bits : -1;
+    *two = a->k.bits2 != 0 && a->k.bits2 != a->k.bits;
+}
 
 tq_status plan_prefill(const tq_prefill_args* a, PrefillPlan* pl) {
     if (!a) return fail(TQ_ERR_INVALID_ARG, "tq_attn_prefill: args are NULL");
@@ -1166,7 +1186,13 @@ tq_status plan_prefill(const tq_prefill_args* a, PrefillPlan* pl) {
     if (a->hq > 256) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: hq must be <= 256");
     const int64_t rows = (int64_t)a->batch * a->chunk * a->hq;
     if (rows > (1ll << 31) / 128) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: too many query rows");
-    const int64_t qbs = ((int64_t)a->chunk * g + tqk::kPfRows - 1) / tqk::kPfRows;
+    int kb = 0, vb = 0;
+    bool two = false;
+    prefill_bits(a, &kb, &vb, &two);
+    pl->umma = g_prefill_umma && tqk::prefill_umma_supported(kb, vb, two);
+    const int rows_per_cta = pl->umma ? tqk::kPuRows : tqk::kPfRows;
+    const int tile = pl->umma ? tqk::kPuTok : 64;  // split granularity in tokens
+    const int64_t qbs = ((int64_t)a->chunk * g + rows_per_cta - 1) / rows_per_cta;
     if (qbs > 0x7fffffff || (int64_t)a->batch * a->hkv > 65535)
         return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: grid too large");
     pl->group = g;
@@ -1175,14 +1201,31 @@ tq_status plan_prefill(const tq_prefill_args* a, PrefillPlan* pl) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int ctx = std::max(a->max_context, 1);
+    const long long base = std::max<long long>(1, qbs * a->batch * a->hkv);
     long long want = a->n_splits;
-    if (want <= 0) {  // about four CTAs per SM (two resident)
-        const long long base = std::max<long long>(1, qbs * a->batch * a->hkv);
+    if (want <= 0 && !pl->umma) {  // about four CTAs per SM (two resident)
         want = ((long long)sms * 4 + base - 1) / base;
+    } else if (want <= 0) {
+        // one CTA per SM: the split count whose waves of CTAs take the least
+        // time, a wave costing its tiles plus about two tiles of set-up,
+        // merge and tail
+        const long long ntile = (ctx + tile - 1) / tile;
+        double best = 1e300;
+        want = 1;
+        for (long long n = 1; n <= std::min<long long>(ntile, 256); ++n) {
+            const long long per = (ntile + n - 1) / n;
+            const long long nn = (ntile + per - 1) / per;
+            const long long waves = (base * nn + sms - 1) / sms;
+            const double cost = (double)waves * (double)(per + 2);
+            if (cost < best - 1e-9) {
+                best = cost;
+                want = nn;
+            }
+        }
     }
     if (want > 65535) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: too many splits");
     int st = (int)((ctx + want - 1) / want);
-    st = std::max(64, (st + 63) / 64 * 64);
+    st = std::max(tile, (st + tile - 1) / tile * tile);
     pl->split_tokens = st;
     pl->n_splits = (ctx + st - 1) / st;
     const size_t r = (size_t)rows;
@@ -1302,7 +1345,8 @@ tq_status tq_attn_prefill(const tq_prefill_args* a, void* workspace, size_t ws_b
 
     cudaStream_t st = (cudaStream_t)stream;
     if ((e = tqk::launch_rows_prep(pp, st)) != cudaSuccess) return cuda_status(e, "tq_attn_prefill query prep");
-    if ((e = tqk::launch_prefill_mma(fp, kb, vb, two, st)) != cudaSuccess) return cuda_status(e, "tq_attn_prefill scan");
+    e = pl.umma ? tqk::launch_prefill_umma(fp, kb, vb, two, st) : tqk::launch_prefill_mma(fp, kb, vb, two, st);
+    if (e != cudaSuccess) return cuda_status(e, "tq_attn_prefill scan");
     return cuda_status(tqk::launch_merge_rows(cp, st), "tq_attn_prefill merge");
 }
 

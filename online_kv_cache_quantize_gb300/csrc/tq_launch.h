@@ -239,6 +239,13 @@ struct PrefillParams {
 
 // two: keys and values are both fractional-rate caches
 cudaError_t launch_prefill_mma(const PrefillParams& p, int kbits, int vbits, bool two, cudaStream_t s);
+// The tcgen05 version: kPuRows query rows per CTA, split_tokens a multiple
+// of kPuTok, one CTA per SM (all of TMEM); keys at 1 or 2 code bits (2 / 1
+// for fractional rates), values 1..4.
+constexpr int kPuRows = 128;
+constexpr int kPuTok = 128;
+bool prefill_umma_supported(int kbits, int vbits, bool two);
+cudaError_t launch_prefill_umma(const PrefillParams& p, int kbits, int vbits, bool two, cudaStream_t s);
 
 // The library's device error word of the current device (bits kErr* of
 // pipeline.cuh), and a kernel that waits on an mbarrier that nothing
