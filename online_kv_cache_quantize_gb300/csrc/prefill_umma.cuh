@@ -28,14 +28,20 @@
 // All shared-memory operands use the K-major layout without swizzle of
 // tcgen05.cuh (8-row core matrices of 16 bytes along K).
 //
-// Warp roles (320 threads): warps 0-3 run the softmax (thread = query row =
-// TMEM lane), warps 4-7 de-quantize (keys: thread = token; values: stmatrix
-// fragments), warp 8 issues the MMAs (one thread) and owns the TMEM
-// allocation, warp 9 issues the bulk copies of each tile's cache planes into
-// a 3-deep ring. Per tile T the MMA thread issues S(T + 1) as soon as the
-// softmax has read S(T), then O += P(T) V(T), so the tensor pipe runs the next
-// tile's scores while the softmax works. Every wait is bounded; a wait that
-// runs out sets the library's error word and the CTA drains and returns.
+// Warp roles (448 threads, two softmax warps per scheduler):
+//  * warps 0-7: softmax, two threads per query row (warps w and w + 4 share
+//    TMEM lane quarter w and take S columns 0-63 and 64-127; they agree on
+//    the row maximum of each tile through shared memory and a named barrier);
+//  * warps 8-9: Bs, thread t writes the rows of tokens t and t + 64;
+//  * warps 10-11: V, 64 tokens each through stmatrix fragments;
+//  * warp 12: MMA issue (one thread), owner of the TMEM allocation;
+//  * warp 13: the bulk copies of each tile's cache planes into a 3-deep ring.
+// Per tile T the MMA thread issues S(T + 1) as soon as Bs(T + 1) is written
+// and the softmax has read S(T), then O += P(T) V(T), so the tensor pipe runs
+// the next tile's scores while the softmax works; Bs and V are written by
+// separate warps, so neither waits for the other's buffer. Every wait is
+// bounded; a wait that runs out sets the library's error word and the CTA
+// drains and returns.
 #pragma once
 
 #include "decode_mma.cuh"
@@ -44,7 +50,7 @@
 namespace tqk {
 
 constexpr int kPuStages = 3;                     // tiles of cache planes in flight
-constexpr int kPuThreads = 320;                  // 10 warps
+constexpr int kPuThreads = 448;                  // 14 warps
 constexpr int kPuBsBytes = kPuTok * 256 * 2;     // Bs: 128 tokens x 256 fp16
 constexpr int kPuVBytes = kPuTok * 128 * 2;      // V: 128 coordinates x 128 tokens fp16
 constexpr int kPuPBytes = kPuRows * kPuTok * 2;  // one limb of P: 128 rows x 128 tokens fp16
@@ -76,14 +82,19 @@ __device__ __forceinline__ constexpr int code_bit(int i) {
     return (i >> 4) * 8 * (B + B2) + ((i & 15) < 8 ? B * (i & 15) : 8 * B + B2 * ((i & 15) - 8));
 }
 
+// Stores of operand tiles that only the tensor cores read, after the
+// writer's fence.proxy.async and an mbarrier arrival (both volatile asm with
+// memory clobbers, which keep their order relative to these): no memory
+// clobber here, so that the compiler may hoist the table lookups of later
+// stores above earlier ones (shared-memory loads take hundreds of cycles
+// while the tensor cores stream their operands).
 __device__ __forceinline__ void stmatrix_x4_trans(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
     asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(r0),
-                 "r"(r1), "r"(r2), "r"(r3)
-                 : "memory");
+                 "r"(r1), "r"(r2), "r"(r3));
 }
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d));
 }
 
 // fp16 hi/lo limbs of two floats (hi = fp16(x), lo = fp16(x - hi)), packed
@@ -95,13 +106,31 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
     lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
+// Bounded wait for the warps of this kernel: between polls the waiting warp
+// sleeps, so that the de-quantization warps' shared-memory lookups do not
+// queue behind a stream of mbarrier polls (a suspended try_wait wakes on every
+// phase any barrier of the CTA completes, which here is often). At most
+// kWaitLimitNs, then the error word and false.
+__device__ __forceinline__ bool pu_wait(uint32_t bar, uint32_t parity, uint32_t* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        __nanosleep(64);
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 15) == 0 && global_ns() - t0 > kWaitLimitNs) {
+            if (err) atomicOr(err, kErrScanWait);
+            return false;
+        }
+    }
+}
+
 // S(T) = Q Bs(T)^T over K = 256, issued by one thread once Bs(T) is written
 // and the softmax has read S(T - 1): the key part (k-steps 0..7) against the
 // q' limbs, the sign part (8..15) against the kappa lam_k u limbs
 __device__ __forceinline__ bool pu_issue_s(int T, uint32_t tmem, uint32_t bs_s, uint32_t bs_full, uint32_t s_empty,
                                            uint32_t s_done, uint32_t idesc, uint32_t* err) {
-    if (!mbar_wait_bounded(bs_full, (uint32_t)(T & 1), kWaitLimitNs, err, kErrScanWait)) return false;
-    if (T > 0 && !mbar_wait_bounded(s_empty, (uint32_t)((T - 1) & 1), kWaitLimitNs, err, kErrScanWait)) return false;
+    if (!pu_wait(bs_full, (uint32_t)(T & 1), err)) return false;
+    if (T > 0 && !pu_wait(s_empty, (uint32_t)((T - 1) & 1), err)) return false;
     tc_fence_after_sync();
     const uint32_t dS = tmem + kPuColS;
 #pragma unroll
@@ -119,8 +148,8 @@ __device__ __forceinline__ bool pu_issue_s(int T, uint32_t tmem, uint32_t bs_s, 
 // thread once P(T) and V(T) are written
 __device__ __forceinline__ bool pu_issue_o(int T, uint32_t tmem, uint32_t p_s, uint32_t v_s, uint32_t p_full,
                                            uint32_t v_full, uint32_t o_done, uint32_t idesc, uint32_t* err) {
-    if (!mbar_wait_bounded(p_full, (uint32_t)(T & 1), kWaitLimitNs, err, kErrScanWait)) return false;
-    if (!mbar_wait_bounded(v_full, (uint32_t)(T & 1), kWaitLimitNs, err, kErrScanWait)) return false;
+    if (!pu_wait(p_full, (uint32_t)(T & 1), err)) return false;
+    if (!pu_wait(v_full, (uint32_t)(T & 1), err)) return false;
     tc_fence_after_sync();
     const uint32_t dO = tmem + kPuColO;
 #pragma unroll
@@ -131,6 +160,17 @@ __device__ __forceinline__ bool pu_issue_o(int T, uint32_t tmem, uint32_t p_s, u
     }
     umma_commit(o_done);
     return true;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;\n" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// named barrier of the two softmax warps that share a TMEM lane quarter
+__device__ __forceinline__ void pair_sync(int quarter) {
+    asm volatile("bar.sync %0, 64;\n" ::"r"(1 + quarter) : "memory");
 }
 
 template <int KB, int VB, int KB2, int VB2>
@@ -151,6 +191,8 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
     __shared__ uint32_t klut2[KL2];
     __shared__ uint32_t vlut[VL];
     __shared__ uint32_t vlut2[VL2];
+    __shared__ float s_xv[2][2][kPuRows];  // softmax pair exchange: [slot][column half][row]
+    __shared__ int s_xok[2][2][kPuRows];
     __shared__ __align__(8) uint64_t s_bar[3 * kPuStages + 7];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
@@ -164,13 +206,13 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
     auto ring_full = [&](int s) { return bar0 + 8u * (uint32_t)s; };
     auto ring_empty = [&](int s) { return bar0 + 8u * (uint32_t)(kPuStages + s); };
     auto fac_full = [&](int s) { return bar0 + 8u * (uint32_t)(2 * kPuStages + s); };
-    const uint32_t bs_full = bar0 + 8u * (3 * kPuStages + 0);  // Bs(T) written (4 warps)
+    const uint32_t bs_full = bar0 + 8u * (3 * kPuStages + 0);  // Bs(T) written (2 warps)
     const uint32_t s_done = bar0 + 8u * (3 * kPuStages + 1);   // S(T) complete (commit)
-    const uint32_t v_full = bar0 + 8u * (3 * kPuStages + 2);   // V(T) written (4 warps)
+    const uint32_t v_full = bar0 + 8u * (3 * kPuStages + 2);   // V(T) written (2 warps)
     const uint32_t o_done = bar0 + 8u * (3 * kPuStages + 3);   // O += P(T) V(T) complete (commit)
-    const uint32_t s_empty = bar0 + 8u * (3 * kPuStages + 4);  // S(T) read by the softmax (4 warps)
-    const uint32_t p_full = bar0 + 8u * (3 * kPuStages + 5);   // P(T) written, O rescaled (4 warps)
-    const uint32_t q_full = bar0 + 8u * (3 * kPuStages + 6);   // A of S in TMEM (4 warps)
+    const uint32_t s_empty = bar0 + 8u * (3 * kPuStages + 4);  // S(T) read by the softmax (8 warps)
+    const uint32_t p_full = bar0 + 8u * (3 * kPuStages + 5);   // P(T) written, O rescaled (8 warps)
+    const uint32_t q_full = bar0 + 8u * (3 * kPuStages + 6);   // A of S in TMEM (8 warps)
 
     for (int i = tid; i < KL; i += kPuThreads) klut[i] = p.klut[i];
     for (int i = tid; i < VL; i += kPuThreads) vlut[i] = p.vlut[i];
@@ -181,20 +223,20 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
     if (tid == 0) {
         for (int s = 0; s < kPuStages; ++s) {
             mbar_init(ring_full(s), 1);
-            mbar_init(ring_empty(s), 8);  // 4 de-quantization + 4 softmax warps
-            mbar_init(fac_full(s), 4);
+            mbar_init(ring_empty(s), 12);  // 2 Bs + 2 V + 8 softmax warps
+            mbar_init(fac_full(s), 2);
         }
-        mbar_init(bs_full, 4);
+        mbar_init(bs_full, 2);
         mbar_init(s_done, 1);
-        mbar_init(v_full, 4);
+        mbar_init(v_full, 2);
         mbar_init(o_done, 1);
-        mbar_init(s_empty, 4);
-        mbar_init(p_full, 4);
-        mbar_init(q_full, 4);
+        mbar_init(s_empty, 8);
+        mbar_init(p_full, 8);
+        mbar_init(q_full, 8);
         s_abort = 0;
         mbar_init_fence();
     }
-    if (warp == 8) {
+    if (warp == 12) {
         tmem_alloc((uint32_t)__cvta_generic_to_shared(&s_tmem), 512);
         tmem_relinquish();
     }
@@ -219,14 +261,13 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
     const uint32_t v_s = (uint32_t)__cvta_generic_to_shared(sV);
     const uint32_t p_s = (uint32_t)__cvta_generic_to_shared(sP);
 
-    if (warp == 9) {
+    if (warp == 13) {
         // ======================= bulk copies of the cache planes =======================
         if (lane == 0 && ntiles > 0) {
             int issued = 0;
             for (int T = 0; T < ntiles; ++T) {
                 const int s = T % kPuStages;
-                if (T >= kPuStages && !mbar_wait_bounded(ring_empty(s), (uint32_t)((T / kPuStages - 1) & 1),
-                                                         kWaitLimitNs, p.err, kErrScanWait)) {
+                if (T >= kPuStages && !pu_wait(ring_empty(s), (uint32_t)((T / kPuStages - 1) & 1), p.err)) {
                     *abort_flag = 1;
                     break;
                 }
@@ -247,15 +288,14 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
             }
             // every copy issued lands (bounded) before the CTA's shared memory is released
             for (int T = max(0, issued - kPuStages); T < issued; ++T)
-                mbar_wait_bounded(ring_full(T % kPuStages), (uint32_t)((T / kPuStages) & 1), kWaitLimitNs, p.err,
-                                  kErrScanWait);
+                pu_wait(ring_full(T % kPuStages), (uint32_t)((T / kPuStages) & 1), p.err);
         }
-    } else if (warp == 8) {
+    } else if (warp == 12) {
         // ======================= MMA issue (one thread) =======================
         if (lane == 0 && ntiles > 0) {
             const uint32_t idesc = umma_idesc_f16(kPuRows, kPuTok);
             uint32_t last_bar = 0, last_par = 0;
-            bool ok = mbar_wait_bounded(q_full, 0, kWaitLimitNs, p.err, kErrScanWait);
+            bool ok = pu_wait(q_full, 0, p.err);
             if (ok) {
                 ok = pu_issue_s(0, tmem, bs_s, bs_full, s_empty, s_done, idesc, p.err);
                 last_bar = s_done;
@@ -279,28 +319,104 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
             if (!ok) *abort_flag = 1;
             // the MMAs in flight complete (bounded) before TMEM is released:
             // the last commit covers every MMA issued before it
-            if (last_bar != 0) mbar_wait_bounded(last_bar, last_par, kWaitLimitNs, p.err, kErrScanWait);
+            if (last_bar != 0) pu_wait(last_bar, last_par, p.err);
         }
-    } else if (warp >= 4) {
-        // ======================= de-quantization =======================
-        const int dw = warp - 4;
-        const int tau = 32 * dw + lane;  // the token whose Bs row this thread writes
-        const float kfac = p.inv_lam_k * p.scale_log2;
-        constexpr int KW = ST::KS / 4, VW = ST::VS / 4;
-        const int q = lane & 3;  // value fragment: coordinates 2q, 2q + 1 of each 8-coordinate block
+    } else if (warp >= 10) {
+        // ======================= V: values through stmatrix =======================
+        // warp vw writes tokens 64 vw .. 64 vw + 63. Fragments: matrix m of a
+        // stmatrix = token group J (8 tokens) x coordinate block b (8
+        // coordinates); this thread holds token 64 vw + 8 J + lane / 4 at
+        // coordinates 8 b + 2q, 8 b + 2q + 1, and lane l addresses row l % 8 of
+        // matrix l / 8, which after the transposition is coordinate 8 b + l % 8
+        // over tokens 8 J .. 8 J + 7 (one 16-byte row of the K-major B operand).
+        const int vw = warp - 10;
+        const int q = lane & 3;
+        constexpr int VW = ST::VS / 4;
         for (int T = 0; T < ntiles; ++T) {
-            if (*abort_flag) break;
             const int s = T % kPuStages;
-            if (!__all_sync(TQ_FULL_MASK, mbar_wait_bounded(ring_full(s), (uint32_t)((T / kPuStages) & 1),
-                                                            kWaitLimitNs, p.err, kErrScanWait))) {
+            bool ok = !*abort_flag && pu_wait(ring_full(s), (uint32_t)((T / kPuStages) & 1), p.err);
+            // O += P(T - 1) V(T - 1) has read V(T - 1)
+            if (ok && T > 0)
+                ok = pu_wait(o_done, (uint32_t)((T - 1) & 1), p.err);
+            if (!__all_sync(TQ_FULL_MASK, ok)) {
+                *abort_flag = 1;
+                break;
+            }
+            const unsigned char* st = ring + s * ST::BYTES;
+            const int nval = min(kPuTok, t1 - (t0 + T * kPuTok));  // tokens of this tile inside the split
+            // the code words of this thread's token in group J (the next
+            // group's are loaded while this one's lookups are in flight)
+            auto load_row = [&](int J, uint32_t (&w)[VW + 1]) {
+                const unsigned char* vr = st + ST::OFF_VC + (64 * vw + 8 * J + (lane >> 2)) * ST::VS;
+                if constexpr (ST::VS % 16 == 0) {
+#pragma unroll
+                    for (int i = 0; i < VW / 4; ++i) {
+                        const uint4 x = reinterpret_cast<const uint4*>(vr)[i];
+                        w[4 * i] = x.x; w[4 * i + 1] = x.y; w[4 * i + 2] = x.z; w[4 * i + 3] = x.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < VW / 2; ++i) {
+                        const uint2 x = reinterpret_cast<const uint2*>(vr)[i];
+                        w[2 * i] = x.x; w[2 * i + 1] = x.y;
+                    }
+                }
+                w[VW] = 0u;
+            };
+            uint32_t wa[VW + 1], wb[VW + 1];
+            load_row(0, wa);
+#pragma unroll
+            for (int J = 0; J < 8; ++J) {
+                uint32_t(&w)[VW + 1] = (J & 1) ? wb : wa;
+                uint32_t(&wn)[VW + 1] = (J & 1) ? wa : wb;
+                // tokens past the split end get zero values: the loads stay
+                // unconditional (their indices are always inside the table) and
+                // the mask clears them, so no branch splits the lookups (a load
+                // that a branch may skip is waited for where the paths merge)
+                const uint32_t vmask = 64 * vw + 8 * J + (lane >> 2) < nval ? 0xFFFFFFFFu : 0u;
+                uint32_t f[16];
+#pragma unroll
+                for (int bb = 0; bb < 16; ++bb) {
+                    const bool first = !V2 || (bb & 1) == 0;
+                    const int wd = first ? VB : VB2;
+                    const int base = code_bit<VB, VB2>(8 * bb);
+                    const uint32_t y = (base & 31) == 0 ? w[base >> 5]
+                                                        : __funnelshift_r(w[base >> 5], w[(base >> 5) + 1], base & 31);
+                    const uint32_t off = ((y >> (2 * wd * q)) & ((1u << (2 * wd)) - 1u)) << 2;
+                    f[bb] = lds_at<uint32_t>(first ? vlut : vlut2, off) & vmask;
+                }
+                if (J + 1 < 8) load_row(J + 1, wn);
+                const uint32_t rowaddr = v_s + (uint32_t)((lane >> 3) * 2048 + (8 * vw + J) * 128 + (lane & 7) * 16);
+#pragma unroll
+                for (int bq = 0; bq < 4; ++bq)
+                    stmatrix_x4_trans(rowaddr + (uint32_t)(4 * bq * 2048), f[4 * bq], f[4 * bq + 1], f[4 * bq + 2],
+                                      f[4 * bq + 3]);
+            }
+            fence_proxy_async_smem();  // the MMA reads V through the async proxy
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(v_full);
+                mbar_arrive(ring_empty(s));
+            }
+        }
+    } else if (warp >= 8) {
+        // ======================= Bs: keys and signs, thread = two tokens =======================
+        const int bt = 32 * (warp - 8) + lane;  // tokens bt and bt + 64
+        const float kfac = p.inv_lam_k * p.scale_log2;
+        constexpr int KW = ST::KS / 4;
+        for (int T = 0; T < ntiles; ++T) {
+            const int s = T % kPuStages;
+            bool ok = !*abort_flag && pu_wait(ring_full(s), (uint32_t)((T / kPuStages) & 1), p.err);
+            if (!__all_sync(TQ_FULL_MASK, ok)) {
                 *abort_flag = 1;
                 break;
             }
             unsigned char* st = ring + s * ST::BYTES;
-            const int tb = t0 + T * kPuTok;
-            const int nval = min(kPuTok, t1 - tb);  // tokens of this tile inside the split
-            const bool valid = tau < nval;
-            {
+            const int nval = min(kPuTok, t1 - (t0 + T * kPuTok));
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {  // the softmax's per-token factors
+                const int tau = bt + 64 * e;
+                const bool valid = tau < nval;
                 const float kn = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(st + ST::OFF_KN)[tau]);
                 const float vn = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(st + ST::OFF_VN)[tau]);
                 reinterpret_cast<float*>(st + ST::OFF_FK)[tau] = valid ? kn * kfac : 0.0f;
@@ -308,126 +424,76 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(fac_full(s));
-
-            // ---- Bs(T): S(T - 1) has read Bs(T - 1) ----
-            if (T > 0 && !__all_sync(TQ_FULL_MASK, mbar_wait_bounded(s_done, (uint32_t)((T - 1) & 1), kWaitLimitNs,
-                                                                     p.err, kErrScanWait))) {
+            // S(T - 1) has read Bs(T - 1)
+            if (T > 0 && !__all_sync(TQ_FULL_MASK, pu_wait(s_done, (uint32_t)((T - 1) & 1), p.err))) {
                 *abort_flag = 1;
                 break;
             }
-            {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int tau = bt + 64 * e;
+                const uint32_t vmask = tau < nval ? 0xFFFFFFFFu : 0u;  // see the V warps
                 const uint32_t row = bs_s + (uint32_t)((tau >> 3) * 4096 + (tau & 7) * 16);
                 uint32_t kw[KW + 1];
                 const unsigned char* kr = st + ST::OFF_KC + tau * ST::KS;
                 if constexpr (ST::KS % 16 == 0) {
 #pragma unroll
-                    for (int w = 0; w < KW / 4; ++w) {
-                        const uint4 x = reinterpret_cast<const uint4*>(kr)[w];
-                        kw[4 * w] = x.x; kw[4 * w + 1] = x.y; kw[4 * w + 2] = x.z; kw[4 * w + 3] = x.w;
+                    for (int i = 0; i < KW / 4; ++i) {
+                        const uint4 x = reinterpret_cast<const uint4*>(kr)[i];
+                        kw[4 * i] = x.x; kw[4 * i + 1] = x.y; kw[4 * i + 2] = x.z; kw[4 * i + 3] = x.w;
                     }
                 } else {
 #pragma unroll
-                    for (int w = 0; w < KW / 2; ++w) {
-                        const uint2 x = reinterpret_cast<const uint2*>(kr)[w];
-                        kw[2 * w] = x.x; kw[2 * w + 1] = x.y;
+                    for (int i = 0; i < KW / 2; ++i) {
+                        const uint2 x = reinterpret_cast<const uint2*>(kr)[i];
+                        kw[2 * i] = x.x; kw[2 * i + 1] = x.y;
                     }
                 }
                 kw[KW] = 0u;
-                // key part: chunk c holds coordinates 8c .. 8c + 7 (four pairs)
+                const uint4 sg = *reinterpret_cast<const uint4*>(st + ST::OFF_SG + tau * 16);
+                const uint32_t gb = reinterpret_cast<const uint16_t*>(st + ST::OFF_KR)[tau];
+                // key part: chunk c holds coordinates 8c .. 8c + 7 (four pairs);
+                // every lookup of the row goes out before the first store
+                uint32_t x[16][4];
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const bool first = !K2 || (c & 1) == 0;
                     const int wd = first ? KB : KB2;
                     const uint32_t* tab = first ? klut : klut2;
-                    uint32_t e[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        e[j] = valid ? lds_at<uint32_t>(tab, field4(kw, code_bit<KB, KB2>(8 * c + 2 * j), 2 * wd)) : 0u;
-                    sts128(row + 128u * c, e[0], e[1], e[2], e[3]);
+                        x[c][j] = lds_at<uint32_t>(tab, field4(kw, code_bit<KB, KB2>(8 * c + 2 * j), 2 * wd)) & vmask;
                 }
+#pragma unroll
+                for (int c = 0; c < 16; ++c) sts128(row + 128u * c, x[c][0], x[c][1], x[c][2], x[c][3]);
                 // sign part: positions 2i, 2i + 1 of sign word w hold bits i and
                 // i + 16; a set bit is +gamma, a clear one -gamma
-                const uint4 sg = *reinterpret_cast<const uint4*>(st + ST::OFF_SG + tau * 16);
                 const uint32_t sw[4] = {sg.x, sg.y, sg.z, sg.w};
-                const uint32_t gb = reinterpret_cast<const uint16_t*>(st + ST::OFF_KR)[tau];
-                const uint32_t g2 = valid ? (gb | (gb << 16)) & 0x7FFF7FFFu : 0u;
+                const uint32_t g2 = (gb | (gb << 16)) & 0x7FFF7FFFu & vmask;
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const uint32_t w = sw[c >> 2];
-                    uint32_t e[4];
+                    uint32_t y[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int i = 4 * (c & 3) + j;
-                        e[j] = g2 ^ ((~w << (15 - i)) & 0x80008000u);
+                        y[j] = g2 ^ ((~w << (15 - i)) & 0x80008000u);
                     }
-                    sts128(row + 128u * (16 + c), e[0], e[1], e[2], e[3]);
+                    sts128(row + 128u * (16 + c), y[0], y[1], y[2], y[3]);
                 }
             }
             fence_proxy_async_smem();  // the MMA reads Bs through the async proxy
             __syncwarp();
-            if (lane == 0) mbar_arrive(bs_full);
-
-            // ---- V(T): O += P(T - 1) V(T - 1) has read V(T - 1) ----
-            if (T > 0 && !__all_sync(TQ_FULL_MASK, mbar_wait_bounded(o_done, (uint32_t)((T - 1) & 1), kWaitLimitNs,
-                                                                     p.err, kErrScanWait))) {
-                *abort_flag = 1;
-                break;
-            }
-            // stmatrix fragments: matrix m of a group = token group J (8 tokens) x
-            // coordinate block b (8 coordinates); this thread holds token
-            // 32 dw + 8 J + lane / 4, coordinates 8 b + 2q, 8 b + 2q + 1, and
-            // lane l addresses row l % 8 of matrix l / 8 (transposed: coordinate
-            // 8 b + l % 8, tokens 8 J .. 8 J + 7)
-#pragma unroll
-            for (int J = 0; J < 4; ++J) {
-                const int tv = 32 * dw + 8 * J + (lane >> 2);
-                const bool vv = tv < nval;
-                uint32_t vw[VW + 1];
-                const unsigned char* vr = st + ST::OFF_VC + tv * ST::VS;
-                if constexpr (ST::VS % 16 == 0) {
-#pragma unroll
-                    for (int w = 0; w < VW / 4; ++w) {
-                        const uint4 x = reinterpret_cast<const uint4*>(vr)[w];
-                        vw[4 * w] = x.x; vw[4 * w + 1] = x.y; vw[4 * w + 2] = x.z; vw[4 * w + 3] = x.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int w = 0; w < VW / 2; ++w) {
-                        const uint2 x = reinterpret_cast<const uint2*>(vr)[w];
-                        vw[2 * w] = x.x; vw[2 * w + 1] = x.y;
-                    }
-                }
-                vw[VW] = 0u;
-#pragma unroll
-                for (int bq = 0; bq < 4; ++bq) {
-                    uint32_t f[4];
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const int bb = 4 * bq + m;
-                        const bool first = !V2 || (bb & 1) == 0;
-                        const int wd = first ? VB : VB2;
-                        const int base = code_bit<VB, VB2>(8 * bb);
-                        const uint32_t y = (base & 31) == 0 ? vw[base >> 5]
-                                                            : __funnelshift_r(vw[base >> 5], vw[(base >> 5) + 1], base & 31);
-                        const uint32_t idx = (y >> (2 * wd * q)) & ((1u << (2 * wd)) - 1u);
-                        f[m] = vv ? (first ? vlut[idx] : vlut2[idx]) : 0u;
-                    }
-                    const uint32_t addr = v_s + (uint32_t)((4 * bq + (lane >> 3)) * 2048 + (4 * dw + J) * 128 +
-                                                           (lane & 7) * 16);
-                    stmatrix_x4_trans(addr, f[0], f[1], f[2], f[3]);
-                }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
             if (lane == 0) {
-                mbar_arrive(v_full);
+                mbar_arrive(bs_full);
                 mbar_arrive(ring_empty(s));
             }
         }
     } else {
-        // ======================= softmax: thread = query row = TMEM lane =======================
-        const int r = 32 * warp + lane;
-        const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+        // ======================= softmax: two threads per query row =======================
+        const int qd = warp & 3, hc = warp >> 2;  // TMEM lane quarter, column half
+        const int r = 32 * qd + lane;             // query row = TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
         // CTA row r is chunk token i = (qb * 128 + r) / G and the
         // ((qb * 128 + r) % G)-th query head of KV head kv
         const int qg = qb * kPuRows + r;
@@ -438,37 +504,57 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
             rok ? ((int64_t)b * p.chunk + ci) * p.hq + (p.use_table ? (int)p.head_table[hj] : hj) : -1;
         const int rlim = rok ? min(max(0, min(qs + ci + 1, p.lim_cap)), t_end) : 0;  // tokens >= rlim are masked
 
+        // The two threads of a row swap a value and a flag through shared
+        // memory and the pair's named barrier; both take every exchange, so
+        // they leave the tile loop together (a lone warp at the barrier would
+        // wait for ever).
+        int xn = 0;
+        auto exchange = [&](float v, int okv, float& other, int& other_ok) {
+            const int slot = xn & 1;
+            ++xn;
+            s_xv[slot][hc][r] = v;
+            s_xok[slot][hc][r] = okv;
+            pair_sync(qd);
+            other = s_xv[slot][hc ^ 1][r];
+            other_ok = s_xok[slot][hc ^ 1][r];
+        };
+
         // ---- A of S into TMEM: columns 0..63 hold q' (coordinates 2m, 2m + 1
-        // in column m) hi, 64..127 its lo; 128..191 / 192..255 kappa lam_k u,
-        // column 16 w + i holding sign rows 32 w + i and 32 w + i + 16 ----
+        // in column m) hi, 64..127 its lo (written by the hc = 0 warps);
+        // 128..191 / 192..255 kappa lam_k u, column 128 + 16 w + i holding
+        // sign rows 32 w + i and 32 w + i + 16 (the hc = 1 warps) ----
         if (ntiles > 0) {
-            const float su = p.qjl_scale / p.inv_lam_k;
-            const float4* q4 = rok ? reinterpret_cast<const float4*>(p.qprime + qrow * D) : nullptr;
-            const float4* u4 = rok ? reinterpret_cast<const float4*>(p.u + qrow * D) : nullptr;
+            if (hc == 0) {
+                const float4* q4 = rok ? reinterpret_cast<const float4*>(p.qprime + qrow * D) : nullptr;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {  // coordinates 64 h .. 64 h + 63
-                uint32_t hi[32], lo[32];
+                for (int h = 0; h < 4; ++h) {  // coordinates 32 h .. 32 h + 31: columns 16 h .. 16 h + 15
+                    uint32_t hi[16], lo[16];
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float4 a = q4 ? __ldg(q4 + 16 * h + k) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    split2(a.x, a.y, hi[2 * k], lo[2 * k]);
-                    split2(a.z, a.w, hi[2 * k + 1], lo[2 * k + 1]);
+                    for (int k = 0; k < 8; ++k) {
+                        const float4 a = q4 ? __ldg(q4 + 8 * h + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        split2(a.x, a.y, hi[2 * k], lo[2 * k]);
+                        split2(a.z, a.w, hi[2 * k + 1], lo[2 * k + 1]);
+                    }
+                    tmem_st16(lane_base + kPuColQ + 16u * h, hi);
+                    tmem_st16(lane_base + kPuColQ + 64u + 16u * h, lo);
                 }
-                tmem_st32(lane_base + kPuColQ + 32u * h, hi);
-                tmem_st32(lane_base + kPuColQ + 64u + 32u * h, lo);
+            } else {
+                const float su = p.qjl_scale / p.inv_lam_k;
+                const float4* u4 = rok ? reinterpret_cast<const float4*>(p.u + qrow * D) : nullptr;
 #pragma unroll
-                for (int w2 = 0; w2 < 2; ++w2) {  // sign word 2 h + w2: rows 32 w .. 32 w + 31
+                for (int w = 0; w < 4; ++w) {  // sign word w: columns 128 + 16 w .. + 15
                     float uu[32];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const float4 a = u4 ? __ldg(u4 + 16 * h + 8 * w2 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        const float4 a = u4 ? __ldg(u4 + 8 * w + k) : make_float4(0.f, 0.f, 0.f, 0.f);
                         uu[4 * k] = a.x * su; uu[4 * k + 1] = a.y * su; uu[4 * k + 2] = a.z * su; uu[4 * k + 3] = a.w * su;
                     }
+                    uint32_t hi[16], lo[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) split2(uu[i], uu[i + 16], hi[16 * w2 + i], lo[16 * w2 + i]);
+                    for (int i = 0; i < 16; ++i) split2(uu[i], uu[i + 16], hi[i], lo[i]);
+                    tmem_st16(lane_base + kPuColQ + 128u + 16u * w, hi);
+                    tmem_st16(lane_base + kPuColQ + 192u + 16u * w, lo);
                 }
-                tmem_st32(lane_base + kPuColQ + 128u + 32u * h, hi);
-                tmem_st32(lane_base + kPuColQ + 192u + 32u * h, lo);
             }
             tmem_st_wait();
             tc_fence_before_sync();
@@ -478,96 +564,118 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
 
         float M = -INFINITY, Z = 0.0f;
         bool ok = true;
-        int T = 0;
-        for (; T < ntiles; ++T) {
-            if (*abort_flag) {
-                ok = false;
-                break;
-            }
+        for (int T = 0; T < ntiles; ++T) {
             const int s = T % kPuStages;
-            bool w_ok = mbar_wait_bounded(fac_full(s), (uint32_t)((T / kPuStages) & 1), kWaitLimitNs, p.err, kErrScanWait);
-            w_ok = w_ok && mbar_wait_bounded(s_done, (uint32_t)(T & 1), kWaitLimitNs, p.err, kErrScanWait);
-            if (!__all_sync(TQ_FULL_MASK, w_ok)) {
-                ok = false;
-                break;
-            }
+            bool w_ok = !*abort_flag;
+            w_ok = w_ok && pu_wait(fac_full(s), (uint32_t)((T / kPuStages) & 1), p.err);
+            w_ok = w_ok && pu_wait(s_done, (uint32_t)(T & 1), p.err);
+            w_ok = __all_sync(TQ_FULL_MASK, w_ok);
             tc_fence_after_sync();
-            float l[kPuTok];
+            // this thread's 64 columns of S (read even after a failed wait:
+            // TMEM reads stay in bounds, and the values are then dropped)
+            float l[64];
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
+            for (int h = 0; h < 2; ++h) {
                 uint32_t x[32];
-                tmem_ld32(lane_base + kPuColS + 32u * h, x);
+                tmem_ld32(lane_base + kPuColS + 64u * hc + 32u * h, x);
 #pragma unroll
                 for (int k = 0; k < 32; ++k) l[32 * h + k] = __uint_as_float(x[k]);
             }
             tmem_ld_wait();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(s_empty);  // S may be overwritten by the next tile's scores
+            if (w_ok && lane == 0) mbar_arrive(s_empty);  // S may take the next tile's scores
 
             const unsigned char* st = ring + s * ST::BYTES;
-            const float4* fk = reinterpret_cast<const float4*>(st + ST::OFF_FK);
-            const float4* fv = reinterpret_cast<const float4*>(st + ST::OFF_FV);
+            const float2* fk = reinterpret_cast<const float2*>(st + ST::OFF_FK) + 32 * hc;
+            const float2* fv = reinterpret_cast<const float2*>(st + ST::OFF_FV) + 32 * hc;
             // logits in log2 units: S * n_t / lam_k * scale * log2 e
 #pragma unroll
-            for (int k = 0; k < kPuTok / 4; ++k) {
-                const float4 f = fk[k];
-                l[4 * k] *= f.x; l[4 * k + 1] *= f.y; l[4 * k + 2] *= f.z; l[4 * k + 3] *= f.w;
+            for (int k = 0; k < 32; ++k) {
+                const float2 v = __fmul2_rn(make_float2(l[2 * k], l[2 * k + 1]), fk[k]);
+                l[2 * k] = v.x;
+                l[2 * k + 1] = v.y;
             }
-            const int rl = rlim - (t0 + T * kPuTok);  // columns >= rl are masked
-            if (!__all_sync(TQ_FULL_MASK, rl >= kPuTok)) {
+            const int rl = rlim - (t0 + T * kPuTok + 64 * hc);  // columns >= rl are masked
+            if (!__all_sync(TQ_FULL_MASK, rl >= 64)) {
 #pragma unroll
-                for (int k = 0; k < kPuTok; ++k) l[k] = k < rl ? l[k] : -INFINITY;
+                for (int k = 0; k < 64; ++k) l[k] = k < rl ? l[k] : -INFINITY;
             }
-            float mx = -INFINITY;
+            float mt[8];
 #pragma unroll
-            for (int k = 0; k < kPuTok; ++k) mx = fmaxf(mx, l[k]);
-            const float mn = fmaxf(M, mx);
+            for (int k = 0; k < 8; ++k) mt[k] = fmax3(l[8 * k], l[8 * k + 1], fmax3(l[8 * k + 2], l[8 * k + 3], l[8 * k + 4]));
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mt[k] = fmax3(mt[k], l[8 * k + 5], fmax3(l[8 * k + 6], l[8 * k + 7], mt[k]));
+            float mloc = fmax3(fmax3(mt[0], mt[1], mt[2]), fmax3(mt[3], mt[4], mt[5]), fmaxf(mt[6], mt[7]));
+            float mo;
+            int ook;
+            exchange(mloc, w_ok ? 1 : 0, mo, ook);
+            if (!(w_ok && ook)) {
+                ok = false;
+                break;
+            }
+            const float mn = fmax3(M, mloc, mo);
             // nothing seen yet: no rescale; first finite maximum: the (zero) sums scale by 0
             const float corr = mn == -INFINITY ? 1.0f : ex2(M - mn);
             const float mu = mn == -INFINITY ? 0.0f : mn;
-            float zs = 0.0f;
+            float2 z2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int k = 0; k < kPuTok; ++k) {
-                l[k] = ex2(l[k] - mu);  // masked columns: 2^-inf = 0
-                zs += l[k];
+            for (int k = 0; k < 32; ++k) {
+                const float2 d = __fadd2_rn(make_float2(l[2 * k], l[2 * k + 1]), make_float2(-mu, -mu));
+                l[2 * k] = ex2(d.x);  // masked columns: 2^-inf = 0
+                l[2 * k + 1] = ex2(d.y);
+                z2[k & 3] = __fadd2_rn(z2[k & 3], make_float2(l[2 * k], l[2 * k + 1]));
             }
-            Z = fmaf(Z, corr, zs);
+            const float2 zz = __fadd2_rn(__fadd2_rn(z2[0], z2[1]), __fadd2_rn(z2[2], z2[3]));
+            Z = fmaf(Z, corr, zz.x + zz.y);
             M = mn;
 
             // P(T) and the rescale of O wait for O += P(T - 1) V(T - 1)
-            if (T > 0) {
-                if (!__all_sync(TQ_FULL_MASK, mbar_wait_bounded(o_done, (uint32_t)((T - 1) & 1), kWaitLimitNs, p.err,
-                                                                kErrScanWait))) {
+            bool o_ok = true;
+            if (T > 0)
+                o_ok = __all_sync(TQ_FULL_MASK, pu_wait(o_done, (uint32_t)((T - 1) & 1), p.err));
+            {
+                float dummy;
+                int o_ook;
+                exchange(0.0f, o_ok ? 1 : 0, dummy, o_ook);
+                if (!(o_ok && o_ook)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after_sync();
             }
-            // P = p * nV_t as fp16 hi/lo limbs, row r of the K-major A operand
-            const uint32_t prow = p_s + (uint32_t)((r >> 3) * 2048 + (r & 7) * 16);
+            tc_fence_after_sync();
+            // P = p * nV_t as fp16 hi/lo limbs: row r, tokens 64 hc .. 64 hc + 63
+            // of the K-major A operand
+            const uint32_t prow = p_s + (uint32_t)((r >> 3) * 2048 + (r & 7) * 16 + 8 * hc * 128);
 #pragma unroll
-            for (int kc = 0; kc < kPuTok / 8; ++kc) {
-                const float4 v0 = fv[2 * kc], v1 = fv[2 * kc + 1];
+            for (int kc = 0; kc < 8; ++kc) {
                 uint32_t h[4], o[4];
-                split2(l[8 * kc] * v0.x, l[8 * kc + 1] * v0.y, h[0], o[0]);
-                split2(l[8 * kc + 2] * v0.z, l[8 * kc + 3] * v0.w, h[1], o[1]);
-                split2(l[8 * kc + 4] * v1.x, l[8 * kc + 5] * v1.y, h[2], o[2]);
-                split2(l[8 * kc + 6] * v1.z, l[8 * kc + 7] * v1.w, h[3], o[3]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 pv = __fmul2_rn(make_float2(l[8 * kc + 2 * j], l[8 * kc + 2 * j + 1]), fv[4 * kc + j]);
+                    split2(pv.x, pv.y, h[j], o[j]);
+                }
                 sts128(prow + 128u * kc, h[0], h[1], h[2], h[3]);
                 sts128(prow + kPuPBytes + 128u * kc, o[0], o[1], o[2], o[3]);
             }
             // the running maximum of a row rarely moves after the first tiles:
-            // rescale O only when it moved for some row of the warp
+            // rescale this thread's half of O only when it moved for some row
+            // of the warp
             if (T > 0 && __any_sync(TQ_FULL_MASK, corr != 1.0f)) {
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
+                for (int h = 0; h < 2; ++h) {
                     uint32_t x[32];
-                    tmem_ld32(lane_base + kPuColO + 32u * h, x);
+                    const uint32_t a = lane_base + kPuColO + 64u * hc + 32u * h;
+                    tmem_ld32(a, x);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) x[k] = __float_as_uint(__uint_as_float(x[k]) * corr);
-                    tmem_st32(lane_base + kPuColO + 32u * h, x);
+                    for (int k = 0; k < 16; ++k) {
+                        const float2 v = __fmul2_rn(make_float2(__uint_as_float(x[2 * k]), __uint_as_float(x[2 * k + 1])),
+                                                    make_float2(corr, corr));
+                        x[2 * k] = __float_as_uint(v.x);
+                        x[2 * k + 1] = __float_as_uint(v.y);
+                    }
+                    tmem_st32(a, x);
                 }
                 tmem_st_wait();
             }
@@ -582,41 +690,46 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
         if (!ok) *abort_flag = 1;
         asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
-        // ---- this split's partials of row r: a (rotated domain), M and Z ----
+        // ---- this split's partials of row r: a (rotated domain) from both
+        // halves, M, and Z summed over the pair ----
         if (ok && ntiles > 0) {
-            ok = __all_sync(TQ_FULL_MASK, mbar_wait_bounded(o_done, (uint32_t)((ntiles - 1) & 1), kWaitLimitNs, p.err,
-                                                           kErrScanWait));
+            ok = __all_sync(TQ_FULL_MASK, pu_wait(o_done, (uint32_t)((ntiles - 1) & 1), p.err));
             tc_fence_after_sync();
         }
+        float zo;
+        int zok;
+        exchange(Z, ok ? 1 : 0, zo, zok);
+        ok = ok && zok;
         float* out = qrow >= 0 ? p.partial + (qrow * p.n_splits + split) * (D + kPartPad) : nullptr;
         const float inv_lv = p.inv_lam_v;
         if (ok && ntiles > 0) {
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
+            for (int h = 0; h < 2; ++h) {
                 uint32_t x[32];
-                tmem_ld32(lane_base + kPuColO + 32u * h, x);
+                tmem_ld32(lane_base + kPuColO + 64u * hc + 32u * h, x);
                 tmem_ld_wait();
                 if (out) {
+                    float4* o4 = reinterpret_cast<float4*>(out + 64 * hc + 32 * h);
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        reinterpret_cast<float4*>(out + 32 * h)[k] =
-                            make_float4(__uint_as_float(x[4 * k]) * inv_lv, __uint_as_float(x[4 * k + 1]) * inv_lv,
-                                        __uint_as_float(x[4 * k + 2]) * inv_lv, __uint_as_float(x[4 * k + 3]) * inv_lv);
+                        o4[k] = make_float4(__uint_as_float(x[4 * k]) * inv_lv, __uint_as_float(x[4 * k + 1]) * inv_lv,
+                                            __uint_as_float(x[4 * k + 2]) * inv_lv, __uint_as_float(x[4 * k + 3]) * inv_lv);
                 }
             }
         } else if (out) {
+            float4* o4 = reinterpret_cast<float4*>(out + 64 * hc);
 #pragma unroll
-            for (int k = 0; k < D / 4; ++k) reinterpret_cast<float4*>(out)[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int k = 0; k < 16; ++k) o4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        if (out) {
+        if (out && hc == 0) {
             out[D] = M;
-            out[D + 1] = Z;
+            out[D + 1] = Z + zo;
         }
     }
 
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 8) {
+    if (warp == 12) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, 512);
     }
