@@ -12,8 +12,9 @@
 //
 // One CTA: 128 query rows (the MMA M dimension, row r in TMEM lane r) of one
 // KV head against one token split. Operands:
-//  * A of S (TMEM, loaded once): fp16 hi/lo limbs of q' for the key part and
-//    of kappa lam_k u for the sign part (K = 128 + 128);
+//  * A of S (loaded once): fp16 hi/lo limbs of q' for the key part and of
+//    kappa lam_k u for the sign part (K = 128 + 128), the hi limbs in TMEM,
+//    the lo limbs in shared memory;
 //  * Bs (shared memory, rebuilt per tile): token t's row holds lam_k cK[idx]
 //    for the 128 coordinates, then +-gamma_t for the 128 sign bits, so that
 //        S[r][t] = lam_k (<q'_r, cK[idx_t]> + kappa gamma_t <u_r, 2 z_t - 1>)
@@ -21,8 +22,10 @@
 //    (positions 2i, 2i + 1 of each 32-bit sign word hold bits i and i + 16),
 //    so that one shift and one logic op build a register of two signs; A
 //    carries the same permutation;
-//  * P (shared memory, written by the softmax): fp16 hi/lo limbs of
-//    p * nV_t, the A operand of O += P V;
+//  * P (TMEM, written by the softmax): fp16 hi/lo limbs of p * nV_t, the A
+//    operand of O += P V, so that this contraction reads only V from shared
+//    memory (with P there too it read at nearly the full shared-memory
+//    bandwidth, and the de-quantization stores queued behind it);
 //  * V (shared memory, rebuilt per tile): lam_v cV[idx], coordinates x tokens,
 //    written through stmatrix with transposition from pair-table lookups.
 // All shared-memory operands use the K-major layout without swizzle of
@@ -31,7 +34,7 @@
 // Warp roles (448 threads, two softmax warps per scheduler):
 //  * warps 0-7: softmax, two threads per query row (warps w and w + 4 share
 //    TMEM lane quarter w and take S columns 0-63 and 64-127; they agree on
-//    the row maximum of each tile through shared memory and a named barrier);
+//    the row maximum of each tile through shared memory and an mbarrier);
 //  * warps 8-9: Bs, thread t writes the rows of tokens t and t + 64;
 //  * warps 10-11: V, 64 tokens each through stmatrix fragments;
 //  * warp 12: MMA issue (one thread), owner of the TMEM allocation;
@@ -53,10 +56,11 @@ constexpr int kPuStages = 3;                     // tiles of cache planes in fli
 constexpr int kPuThreads = 448;                  // 14 warps
 constexpr int kPuBsBytes = kPuTok * 256 * 2;     // Bs: 128 tokens x 256 fp16
 constexpr int kPuVBytes = kPuTok * 128 * 2;      // V: 128 coordinates x 128 tokens fp16
-constexpr int kPuPBytes = kPuRows * kPuTok * 2;  // one limb of P: 128 rows x 128 tokens fp16
-constexpr uint32_t kPuColQ = 0;    // TMEM: q' hi, q' lo, kappa lam u hi, lo (64 columns each)
-constexpr uint32_t kPuColS = 256;  // S: 128 columns
-constexpr uint32_t kPuColO = 384;  // O: 128 columns
+constexpr int kPuQloBytes = kPuRows * 256 * 2;   // lo limbs of the A operand of S: 128 rows x 256 fp16
+constexpr uint32_t kPuColQ = 0;    // TMEM: hi limbs of the A operand of S, q' then kappa lam u (64 columns each)
+constexpr uint32_t kPuColS = 128;  // S: 128 columns
+constexpr uint32_t kPuColO = 256;  // O: 128 columns
+constexpr uint32_t kPuColP = 384;  // P: hi limb (64 columns), lo limb (64 columns)
 
 // One ring stage: the six cache planes of 128 tokens as the bulk copies
 // deliver them, then the per-token factors the de-quantization warps write
@@ -125,10 +129,11 @@ __device__ __forceinline__ bool pu_wait(uint32_t bar, uint32_t parity, uint32_t*
 }
 
 // S(T) = Q Bs(T)^T over K = 256, issued by one thread once Bs(T) is written
-// and the softmax has read S(T - 1): the key part (k-steps 0..7) against the
-// q' limbs, the sign part (8..15) against the kappa lam_k u limbs
-__device__ __forceinline__ bool pu_issue_s(int T, uint32_t tmem, uint32_t bs_s, uint32_t bs_full, uint32_t s_empty,
-                                           uint32_t s_done, uint32_t idesc, uint32_t* err) {
+// and the softmax has read S(T - 1): the key part (k-steps 0..7) against q',
+// the sign part (8..15) against kappa lam_k u; the hi limbs from TMEM, the lo
+// limbs from shared memory
+__device__ __forceinline__ bool pu_issue_s(int T, uint32_t tmem, uint32_t qlo_s, uint32_t bs_s, uint32_t bs_full,
+                                           uint32_t s_empty, uint32_t s_done, uint32_t idesc, uint32_t* err) {
     if (!pu_wait(bs_full, (uint32_t)(T & 1), err)) return false;
     if (T > 0 && !pu_wait(s_empty, (uint32_t)((T - 1) & 1), err)) return false;
     tc_fence_after_sync();
@@ -136,18 +141,17 @@ __device__ __forceinline__ bool pu_issue_s(int T, uint32_t tmem, uint32_t bs_s, 
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
         const uint64_t bd = umma_desc(bs_s + 256u * k, 128, 4096);
-        const uint32_t a = tmem + kPuColQ + (k < 8 ? 0u : 128u) + 8u * (k & 7);
-        umma_f16_ta(dS, a, bd, idesc, k > 0);       // hi limb
-        umma_f16_ta(dS, a + 64u, bd, idesc, true);  // lo limb
+        umma_f16_ta(dS, tmem + kPuColQ + 8u * k, bd, idesc, k > 0);           // hi limb
+        umma_f16(dS, umma_desc(qlo_s + 256u * k, 128, 4096), bd, idesc, true);  // lo limb
     }
     umma_commit(s_done);
     return true;
 }
 
-// O += P(T) V(T) over K = 128 tokens, P in two fp16 limbs, issued by one
-// thread once P(T) and V(T) are written
-__device__ __forceinline__ bool pu_issue_o(int T, uint32_t tmem, uint32_t p_s, uint32_t v_s, uint32_t p_full,
-                                           uint32_t v_full, uint32_t o_done, uint32_t idesc, uint32_t* err) {
+// O += P(T) V(T) over K = 128 tokens, P in two fp16 limbs in TMEM, issued
+// by one thread once P(T) and V(T) are written
+__device__ __forceinline__ bool pu_issue_o(int T, uint32_t tmem, uint32_t v_s, uint32_t p_full, uint32_t v_full,
+                                           uint32_t o_done, uint32_t idesc, uint32_t* err) {
     if (!pu_wait(p_full, (uint32_t)(T & 1), err)) return false;
     if (!pu_wait(v_full, (uint32_t)(T & 1), err)) return false;
     tc_fence_after_sync();
@@ -155,8 +159,8 @@ __device__ __forceinline__ bool pu_issue_o(int T, uint32_t tmem, uint32_t p_s, u
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const uint64_t bd = umma_desc(v_s + 256u * k, 128, 2048);
-        umma_f16(dO, umma_desc(p_s + 256u * k, 128, 2048), bd, idesc, T > 0 || k > 0);
-        umma_f16(dO, umma_desc(p_s + kPuPBytes + 256u * k, 128, 2048), bd, idesc, true);
+        umma_f16_ta(dO, tmem + kPuColP + 8u * k, bd, idesc, T > 0 || k > 0);
+        umma_f16_ta(dO, tmem + kPuColP + 64u + 8u * k, bd, idesc, true);
     }
     umma_commit(o_done);
     return true;
@@ -168,11 +172,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return r;
 }
 
-// named barrier of the two softmax warps that share a TMEM lane quarter
-__device__ __forceinline__ void pair_sync(int quarter) {
-    asm volatile("bar.sync %0, 64;\n" ::"r"(1 + quarter) : "memory");
-}
-
 template <int KB, int VB, int KB2, int VB2>
 __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __grid_constant__ PrefillParams p) {
     using ST = PuStage<KB, VB, KB2, VB2>;
@@ -182,10 +181,10 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
     constexpr int D = 128;
 
     extern __shared__ __align__(1024) unsigned char pu_smem[];
-    unsigned char* sBs = pu_smem;
+    unsigned char* sQlo = pu_smem;
+    unsigned char* sBs = sQlo + kPuQloBytes;
     unsigned char* sV = sBs + kPuBsBytes;
-    unsigned char* sP = sV + kPuVBytes;  // hi limb, then lo limb
-    unsigned char* ring = sP + 2 * kPuPBytes;
+    unsigned char* ring = sV + kPuVBytes;
 
     __shared__ uint32_t klut[KL];
     __shared__ uint32_t klut2[KL2];
@@ -193,7 +192,7 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
     __shared__ uint32_t vlut2[VL2];
     __shared__ float s_xv[2][2][kPuRows];  // softmax pair exchange: [slot][column half][row]
     __shared__ int s_xok[2][2][kPuRows];
-    __shared__ __align__(8) uint64_t s_bar[3 * kPuStages + 7];
+    __shared__ __align__(8) uint64_t s_bar[3 * kPuStages + 7 + 4];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -213,6 +212,7 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
     const uint32_t s_empty = bar0 + 8u * (3 * kPuStages + 4);  // S(T) read by the softmax (8 warps)
     const uint32_t p_full = bar0 + 8u * (3 * kPuStages + 5);   // P(T) written, O rescaled (8 warps)
     const uint32_t q_full = bar0 + 8u * (3 * kPuStages + 6);   // A of S in TMEM (8 warps)
+    auto pair_bar = [&](int quarter) { return bar0 + 8u * (uint32_t)(3 * kPuStages + 7 + quarter); };  // 2 warps
 
     for (int i = tid; i < KL; i += kPuThreads) klut[i] = p.klut[i];
     for (int i = tid; i < VL; i += kPuThreads) vlut[i] = p.vlut[i];
@@ -233,6 +233,7 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
         mbar_init(s_empty, 8);
         mbar_init(p_full, 8);
         mbar_init(q_full, 8);
+        for (int i = 0; i < 4; ++i) mbar_init(pair_bar(i), 2);
         s_abort = 0;
         mbar_init_fence();
     }
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
     const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
     const uint32_t bs_s = (uint32_t)__cvta_generic_to_shared(sBs);
     const uint32_t v_s = (uint32_t)__cvta_generic_to_shared(sV);
-    const uint32_t p_s = (uint32_t)__cvta_generic_to_shared(sP);
+    const uint32_t qlo_s = (uint32_t)__cvta_generic_to_shared(sQlo);
 
     if (warp == 13) {
         // ======================= bulk copies of the cache planes =======================
@@ -297,7 +298,7 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
             uint32_t last_bar = 0, last_par = 0;
             bool ok = pu_wait(q_full, 0, p.err);
             if (ok) {
-                ok = pu_issue_s(0, tmem, bs_s, bs_full, s_empty, s_done, idesc, p.err);
+                ok = pu_issue_s(0, tmem, qlo_s, bs_s, bs_full, s_empty, s_done, idesc, p.err);
                 last_bar = s_done;
                 last_par = 0;
             }
@@ -308,11 +309,11 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
                 }
                 // the next tile's scores go in while the softmax works on this one
                 if (T + 1 < ntiles) {
-                    if (!(ok = pu_issue_s(T + 1, tmem, bs_s, bs_full, s_empty, s_done, idesc, p.err))) break;
+                    if (!(ok = pu_issue_s(T + 1, tmem, qlo_s, bs_s, bs_full, s_empty, s_done, idesc, p.err))) break;
                     last_bar = s_done;
                     last_par = (uint32_t)((T + 1) & 1);
                 }
-                if (!(ok = pu_issue_o(T, tmem, p_s, v_s, p_full, v_full, o_done, idesc, p.err))) break;
+                if (!(ok = pu_issue_o(T, tmem, v_s, p_full, v_full, o_done, idesc, p.err))) break;
                 last_bar = o_done;
                 last_par = (uint32_t)(T & 1);
             }
@@ -363,12 +364,10 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
                 }
                 w[VW] = 0u;
             };
-            uint32_t wa[VW + 1], wb[VW + 1];
-            load_row(0, wa);
-#pragma unroll
-            for (int J = 0; J < 8; ++J) {
-                uint32_t(&w)[VW + 1] = (J & 1) ? wb : wa;
-                uint32_t(&wn)[VW + 1] = (J & 1) ? wa : wb;
+            // one token group: 16 lookups, then the next group's row loads,
+            // then the four stmatrix stores (a rolled loop over pairs of
+            // groups keeps the code in the instruction cache)
+            auto group = [&](int J, const uint32_t (&w)[VW + 1], uint32_t (&wn)[VW + 1]) {
                 // tokens past the split end get zero values: the loads stay
                 // unconditional (their indices are always inside the table) and
                 // the mask clears them, so no branch splits the lookups (a load
@@ -391,6 +390,13 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
                 for (int bq = 0; bq < 4; ++bq)
                     stmatrix_x4_trans(rowaddr + (uint32_t)(4 * bq * 2048), f[4 * bq], f[4 * bq + 1], f[4 * bq + 2],
                                       f[4 * bq + 3]);
+            };
+            uint32_t wa[VW + 1], wb[VW + 1];
+            load_row(0, wa);
+#pragma unroll 1
+            for (int J = 0; J < 8; J += 2) {
+                group(J, wa, wb);
+                group(J + 1, wb, wa);
             }
             fence_proxy_async_smem();  // the MMA reads V through the async proxy
             __syncwarp();
@@ -429,7 +435,7 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
                 *abort_flag = 1;
                 break;
             }
-#pragma unroll
+#pragma unroll 1
             for (int e = 0; e < 2; ++e) {
                 const int tau = bt + 64 * e;
                 const uint32_t vmask = tau < nval ? 0xFFFFFFFFu : 0u;  // see the V warps
@@ -505,25 +511,30 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
         const int rlim = rok ? min(max(0, min(qs + ci + 1, p.lim_cap)), t_end) : 0;  // tokens >= rlim are masked
 
         // The two threads of a row swap a value and a flag through shared
-        // memory and the pair's named barrier; both take every exchange, so
-        // they leave the tile loop together (a lone warp at the barrier would
-        // wait for ever).
+        // memory and the pair's mbarrier (one arrival per warp, one phase per
+        // exchange, bounded wait). Both take every exchange and decide on the
+        // two flags together, so they leave the tile loop at the same point;
+        // a wait that runs out counts as a failed flag.
         int xn = 0;
         auto exchange = [&](float v, int okv, float& other, int& other_ok) {
             const int slot = xn & 1;
-            ++xn;
             s_xv[slot][hc][r] = v;
             s_xok[slot][hc][r] = okv;
-            pair_sync(qd);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pair_bar(qd));
+            const bool got = __all_sync(TQ_FULL_MASK, pu_wait(pair_bar(qd), (uint32_t)(xn & 1), p.err));
+            ++xn;
             other = s_xv[slot][hc ^ 1][r];
-            other_ok = s_xok[slot][hc ^ 1][r];
+            other_ok = got ? s_xok[slot][hc ^ 1][r] : 0;
         };
 
-        // ---- A of S into TMEM: columns 0..63 hold q' (coordinates 2m, 2m + 1
-        // in column m) hi, 64..127 its lo (written by the hc = 0 warps);
-        // 128..191 / 192..255 kappa lam_k u, column 128 + 16 w + i holding
-        // sign rows 32 w + i and 32 w + i + 16 (the hc = 1 warps) ----
+        // ---- A of S: hi limbs in TMEM (columns 0..63 q', column m holding
+        // coordinates 2m, 2m + 1; 64..127 kappa lam_k u, column 64 + 16 w + i
+        // holding sign rows 32 w + i and 32 w + i + 16), lo limbs in shared
+        // memory at the same K positions (row r of the K-major layout); the
+        // hc = 0 warps write q', the hc = 1 warps kappa lam_k u ----
         if (ntiles > 0) {
+            const uint32_t qrow_s = qlo_s + (uint32_t)((r >> 3) * 4096 + (r & 7) * 16);
             if (hc == 0) {
                 const float4* q4 = rok ? reinterpret_cast<const float4*>(p.qprime + qrow * D) : nullptr;
 #pragma unroll
@@ -536,13 +547,15 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
                         split2(a.z, a.w, hi[2 * k + 1], lo[2 * k + 1]);
                     }
                     tmem_st16(lane_base + kPuColQ + 16u * h, hi);
-                    tmem_st16(lane_base + kPuColQ + 64u + 16u * h, lo);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        sts128(qrow_s + 128u * (4 * h + c), lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
                 }
             } else {
                 const float su = p.qjl_scale / p.inv_lam_k;
                 const float4* u4 = rok ? reinterpret_cast<const float4*>(p.u + qrow * D) : nullptr;
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {  // sign word w: columns 128 + 16 w .. + 15
+                for (int w = 0; w < 4; ++w) {  // sign word w: columns 64 + 16 w .. + 15
                     float uu[32];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
@@ -552,10 +565,13 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
                     uint32_t hi[16], lo[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) split2(uu[i], uu[i + 16], hi[i], lo[i]);
-                    tmem_st16(lane_base + kPuColQ + 128u + 16u * w, hi);
-                    tmem_st16(lane_base + kPuColQ + 192u + 16u * w, lo);
+                    tmem_st16(lane_base + kPuColQ + 64u + 16u * w, hi);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        sts128(qrow_s + 128u * (16 + 4 * w + c), lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
                 }
             }
+            fence_proxy_async_smem();  // the MMA reads the lo limbs through the async proxy
             tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
@@ -644,19 +660,19 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
                 }
             }
             tc_fence_after_sync();
-            // P = p * nV_t as fp16 hi/lo limbs: row r, tokens 64 hc .. 64 hc + 63
-            // of the K-major A operand
-            const uint32_t prow = p_s + (uint32_t)((r >> 3) * 2048 + (r & 7) * 16 + 8 * hc * 128);
+            // P = p * nV_t as fp16 hi/lo limbs into TMEM (the A operand of
+            // O += P V): tokens 64 hc + 2j, + 1 in column 32 hc + j of each limb
 #pragma unroll
-            for (int kc = 0; kc < 8; ++kc) {
-                uint32_t h[4], o[4];
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t hi[16], lo[16];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float2 pv = __fmul2_rn(make_float2(l[8 * kc + 2 * j], l[8 * kc + 2 * j + 1]), fv[4 * kc + j]);
-                    split2(pv.x, pv.y, h[j], o[j]);
+                for (int j = 0; j < 16; ++j) {
+                    const int k = 32 * h2 + 2 * j;
+                    const float2 pv = __fmul2_rn(make_float2(l[k], l[k + 1]), fv[16 * h2 + j]);
+                    split2(pv.x, pv.y, hi[j], lo[j]);
                 }
-                sts128(prow + 128u * kc, h[0], h[1], h[2], h[3]);
-                sts128(prow + kPuPBytes + 128u * kc, o[0], o[1], o[2], o[3]);
+                tmem_st16(lane_base + kPuColP + 32u * hc + 16u * h2, hi);
+                tmem_st16(lane_base + kPuColP + 64u + 32u * hc + 16u * h2, lo);
             }
             // the running maximum of a row rarely moves after the first tiles:
             // rescale this thread's half of O only when it moved for some row
@@ -677,9 +693,8 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
                     }
                     tmem_st32(a, x);
                 }
-                tmem_st_wait();
             }
-            fence_proxy_async_smem();  // the MMA reads P through the async proxy
+            tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
@@ -737,7 +752,7 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
 
 template <int KB, int VB, int KB2, int VB2>
 constexpr size_t prefill_umma_smem() {
-    return (size_t)kPuBsBytes + kPuVBytes + 2 * (size_t)kPuPBytes +
+    return (size_t)kPuQloBytes + kPuBsBytes + kPuVBytes +
            (size_t)kPuStages * PuStage<KB, VB, KB2, VB2>::BYTES;
 }
 
