@@ -31,14 +31,15 @@
 // All shared-memory operands use the K-major layout without swizzle of
 // tcgen05.cuh (8-row core matrices of 16 bytes along K).
 //
-// Warp roles (448 threads, two softmax warps per scheduler):
+// Warp roles (512 threads, four warps per scheduler):
 //  * warps 0-7: softmax, two threads per query row (warps w and w + 4 share
 //    TMEM lane quarter w and take S columns 0-63 and 64-127; they agree on
 //    the row maximum of each tile through shared memory and an mbarrier);
-//  * warps 8-9: Bs, thread t writes the rows of tokens t and t + 64;
-//  * warps 10-11: V, 64 tokens each through stmatrix fragments;
-//  * warp 12: MMA issue (one thread), owner of the TMEM allocation;
-//  * warp 13: the bulk copies of each tile's cache planes into a 3-deep ring.
+//  * warps 8-11: Bs, thread = token;
+//  * warps 12-14: V, token groups of 8 round robin, through stmatrix fragments;
+//  * warp 15: one thread issues the MMAs and the bulk copies of each tile's
+//    cache planes into a 3-deep ring (a stage is refilled once the softmax, Bs
+//    and V warps are done with its tile); the warp owns the TMEM allocation.
 // Per tile T the MMA thread issues S(T + 1) as soon as Bs(T + 1) is written
 // and the softmax has read S(T), then O += P(T) V(T), so the tensor pipe runs
 // the next tile's scores while the softmax works; Bs and V are written by
@@ -53,7 +54,7 @@
 namespace tqk {
 
 constexpr int kPuStages = 3;                     // tiles of cache planes in flight
-constexpr int kPuThreads = 448;                  // 14 warps
+constexpr int kPuThreads = 512;                  // 16 warps
 constexpr int kPuBsBytes = kPuTok * 256 * 2;     // Bs: 128 tokens x 256 fp16
 constexpr int kPuVBytes = kPuTok * 128 * 2;      // V: 128 coordinates x 128 tokens fp16
 constexpr int kPuQloBytes = kPuRows * 256 * 2;   // lo limbs of the A operand of S: 128 rows x 256 fp16
@@ -223,12 +224,12 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
     if (tid == 0) {
         for (int s = 0; s < kPuStages; ++s) {
             mbar_init(ring_full(s), 1);
-            mbar_init(ring_empty(s), 12);  // 2 Bs + 2 V + 8 softmax warps
-            mbar_init(fac_full(s), 2);
+            mbar_init(ring_empty(s), 15);  // 4 Bs + 3 V + 8 softmax warps
+            mbar_init(fac_full(s), 4);
         }
-        mbar_init(bs_full, 2);
+        mbar_init(bs_full, 4);
         mbar_init(s_done, 1);
-        mbar_init(v_full, 2);
+        mbar_init(v_full, 3);
         mbar_init(o_done, 1);
         mbar_init(s_empty, 8);
         mbar_init(p_full, 8);
@@ -237,7 +238,7 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
         s_abort = 0;
         mbar_init_fence();
     }
-    if (warp == 12) {
+    if (warp == 15) {
         tmem_alloc((uint32_t)__cvta_generic_to_shared(&s_tmem), 512);
         tmem_relinquish();
     }
@@ -262,38 +263,28 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
     const uint32_t v_s = (uint32_t)__cvta_generic_to_shared(sV);
     const uint32_t qlo_s = (uint32_t)__cvta_generic_to_shared(sQlo);
 
-    if (warp == 13) {
-        // ======================= bulk copies of the cache planes =======================
+    // the six bulk copies of tile T's cache planes into ring stage T % kPuStages
+    auto issue_copies = [&](int T) {  // one thread
+        const int s = T % kPuStages;
+        const int tb = t0 + T * kPuTok;
+        const uint32_t ntok = (uint32_t)((min(kPuTok, t1 - tb) + 15) & ~15);  // whole 16-slot rows
+        const int64_t slot = rowbase + tb;
+        const uint32_t dst = ring_s + (uint32_t)(s * ST::BYTES), bar = ring_full(s);
+        fence_proxy_async_smem();  // the consumers' reads of this stage come first
+        mbar_arrive_expect_tx(bar, ntok * (uint32_t)(ST::KS + 16 + 2 + 2 + ST::VS + 2));
+        bulk_g2s(dst + ST::OFF_KC, p.kcodes + slot * ST::KS, ntok * ST::KS, bar);
+        bulk_g2s(dst + ST::OFF_SG, p.ksigns + slot * 16, ntok * 16, bar);
+        bulk_g2s(dst + ST::OFF_KN, p.knorm + slot, ntok * 2, bar);
+        bulk_g2s(dst + ST::OFF_KR, p.krnorm + slot, ntok * 2, bar);
+        bulk_g2s(dst + ST::OFF_VC, p.vcodes + slot * ST::VS, ntok * ST::VS, bar);
+        bulk_g2s(dst + ST::OFF_VN, p.vnorm + slot, ntok * 2, bar);
+    };
+
+    if (warp == 15) {
+        // ======================= MMA issue and bulk copies (one thread) =======================
         if (lane == 0 && ntiles > 0) {
             int issued = 0;
-            for (int T = 0; T < ntiles; ++T) {
-                const int s = T % kPuStages;
-                if (T >= kPuStages && !pu_wait(ring_empty(s), (uint32_t)((T / kPuStages - 1) & 1), p.err)) {
-                    *abort_flag = 1;
-                    break;
-                }
-                if (*abort_flag) break;
-                const int tb = t0 + T * kPuTok;
-                const uint32_t ntok = (uint32_t)((min(kPuTok, t1 - tb) + 15) & ~15);  // whole 16-slot rows
-                const int64_t slot = rowbase + tb;
-                const uint32_t dst = ring_s + (uint32_t)(s * ST::BYTES), bar = ring_full(s);
-                fence_proxy_async_smem();  // the consumers' reads of this stage come first
-                mbar_arrive_expect_tx(bar, ntok * (uint32_t)(ST::KS + 16 + 2 + 2 + ST::VS + 2));
-                bulk_g2s(dst + ST::OFF_KC, p.kcodes + slot * ST::KS, ntok * ST::KS, bar);
-                bulk_g2s(dst + ST::OFF_SG, p.ksigns + slot * 16, ntok * 16, bar);
-                bulk_g2s(dst + ST::OFF_KN, p.knorm + slot, ntok * 2, bar);
-                bulk_g2s(dst + ST::OFF_KR, p.krnorm + slot, ntok * 2, bar);
-                bulk_g2s(dst + ST::OFF_VC, p.vcodes + slot * ST::VS, ntok * ST::VS, bar);
-                bulk_g2s(dst + ST::OFF_VN, p.vnorm + slot, ntok * 2, bar);
-                issued = T + 1;
-            }
-            // every copy issued lands (bounded) before the CTA's shared memory is released
-            for (int T = max(0, issued - kPuStages); T < issued; ++T)
-                pu_wait(ring_full(T % kPuStages), (uint32_t)((T / kPuStages) & 1), p.err);
-        }
-    } else if (warp == 12) {
-        // ======================= MMA issue (one thread) =======================
-        if (lane == 0 && ntiles > 0) {
+            for (; issued < kPuStages && issued < ntiles; ++issued) issue_copies(issued);
             const uint32_t idesc = umma_idesc_f16(kPuRows, kPuTok);
             uint32_t last_bar = 0, last_par = 0;
             bool ok = pu_wait(q_full, 0, p.err);
@@ -316,21 +307,32 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
                 if (!(ok = pu_issue_o(T, tmem, v_s, p_full, v_full, o_done, idesc, p.err))) break;
                 last_bar = o_done;
                 last_par = (uint32_t)(T & 1);
+                // tile T's stage is free once its softmax, Bs and V warps are
+                // done with it (just after P(T) and V(T), waited for above):
+                // refill it with tile T + kPuStages
+                if (issued < ntiles) {
+                    if (!(ok = pu_wait(ring_empty(T % kPuStages), (uint32_t)((T / kPuStages) & 1), p.err))) break;
+                    issue_copies(issued++);
+                }
             }
             if (!ok) *abort_flag = 1;
             // the MMAs in flight complete (bounded) before TMEM is released:
-            // the last commit covers every MMA issued before it
+            // the last commit covers every MMA issued before it; every copy
+            // issued lands (bounded) before the shared memory is released
             if (last_bar != 0) pu_wait(last_bar, last_par, p.err);
+            for (int T = max(0, issued - kPuStages); T < issued; ++T)
+                pu_wait(ring_full(T % kPuStages), (uint32_t)((T / kPuStages) & 1), p.err);
         }
-    } else if (warp >= 10) {
+    } else if (warp >= 12) {
         // ======================= V: values through stmatrix =======================
-        // warp vw writes tokens 64 vw .. 64 vw + 63. Fragments: matrix m of a
-        // stmatrix = token group J (8 tokens) x coordinate block b (8
-        // coordinates); this thread holds token 64 vw + 8 J + lane / 4 at
-        // coordinates 8 b + 2q, 8 b + 2q + 1, and lane l addresses row l % 8 of
-        // matrix l / 8, which after the transposition is coordinate 8 b + l % 8
-        // over tokens 8 J .. 8 J + 7 (one 16-byte row of the K-major B operand).
-        const int vw = warp - 10;
+        // warp vw writes the token groups J = vw, vw + 3, ... (8 tokens each,
+        // 16 groups). Fragments: matrix m of a stmatrix = token group J x
+        // coordinate block b (8 coordinates); this thread holds token 8 J +
+        // lane / 4 at coordinates 8 b + 2q, 8 b + 2q + 1, and lane l addresses
+        // row l % 8 of matrix l / 8, which after the transposition is
+        // coordinate 8 b + l % 8 over tokens 8 J .. 8 J + 7 (one 16-byte row of
+        // the K-major B operand).
+        const int vw = warp - 12;
         const int q = lane & 3;
         constexpr int VW = ST::VS / 4;
         for (int T = 0; T < ntiles; ++T) {
@@ -348,7 +350,7 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
             // the code words of this thread's token in group J (the next
             // group's are loaded while this one's lookups are in flight)
             auto load_row = [&](int J, uint32_t (&w)[VW + 1]) {
-                const unsigned char* vr = st + ST::OFF_VC + (64 * vw + 8 * J + (lane >> 2)) * ST::VS;
+                const unsigned char* vr = st + ST::OFF_VC + (8 * J + (lane >> 2)) * ST::VS;
                 if constexpr (ST::VS % 16 == 0) {
 #pragma unroll
                     for (int i = 0; i < VW / 4; ++i) {
@@ -372,7 +374,7 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
                 // unconditional (their indices are always inside the table) and
                 // the mask clears them, so no branch splits the lookups (a load
                 // that a branch may skip is waited for where the paths merge)
-                const uint32_t vmask = 64 * vw + 8 * J + (lane >> 2) < nval ? 0xFFFFFFFFu : 0u;
+                const uint32_t vmask = 8 * J + (lane >> 2) < nval ? 0xFFFFFFFFu : 0u;
                 uint32_t f[16];
 #pragma unroll
                 for (int bb = 0; bb < 16; ++bb) {
@@ -384,20 +386,22 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
                     const uint32_t off = ((y >> (2 * wd * q)) & ((1u << (2 * wd)) - 1u)) << 2;
                     f[bb] = lds_at<uint32_t>(first ? vlut : vlut2, off) & vmask;
                 }
-                if (J + 1 < 8) load_row(J + 1, wn);
-                const uint32_t rowaddr = v_s + (uint32_t)((lane >> 3) * 2048 + (8 * vw + J) * 128 + (lane & 7) * 16);
+                if (J + 3 < 16) load_row(J + 3, wn);
+                const uint32_t rowaddr = v_s + (uint32_t)((lane >> 3) * 2048 + J * 128 + (lane & 7) * 16);
 #pragma unroll
                 for (int bq = 0; bq < 4; ++bq)
                     stmatrix_x4_trans(rowaddr + (uint32_t)(4 * bq * 2048), f[4 * bq], f[4 * bq + 1], f[4 * bq + 2],
                                       f[4 * bq + 3]);
             };
             uint32_t wa[VW + 1], wb[VW + 1];
-            load_row(0, wa);
+            load_row(vw, wa);
+            int J = vw;
 #pragma unroll 1
-            for (int J = 0; J < 8; J += 2) {
+            for (; J + 3 < 16; J += 6) {
                 group(J, wa, wb);
-                group(J + 1, wb, wa);
+                group(J + 3, wb, wa);
             }
+            if (J < 16) group(J, wa, wb);
             fence_proxy_async_smem();  // the MMA reads V through the async proxy
             __syncwarp();
             if (lane == 0) {
@@ -406,8 +410,8 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
             }
         }
     } else if (warp >= 8) {
-        // ======================= Bs: keys and signs, thread = two tokens =======================
-        const int bt = 32 * (warp - 8) + lane;  // tokens bt and bt + 64
+        // ======================= Bs: keys and signs, thread = token =======================
+        const int tau = 32 * (warp - 8) + lane;
         const float kfac = p.inv_lam_k * p.scale_log2;
         constexpr int KW = ST::KS / 4;
         for (int T = 0; T < ntiles; ++T) {
@@ -419,9 +423,7 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
             }
             unsigned char* st = ring + s * ST::BYTES;
             const int nval = min(kPuTok, t1 - (t0 + T * kPuTok));
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {  // the softmax's per-token factors
-                const int tau = bt + 64 * e;
+            {  // the softmax's per-token factors
                 const bool valid = tau < nval;
                 const float kn = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(st + ST::OFF_KN)[tau]);
                 const float vn = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(st + ST::OFF_VN)[tau]);
@@ -435,9 +437,7 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
                 *abort_flag = 1;
                 break;
             }
-#pragma unroll 1
-            for (int e = 0; e < 2; ++e) {
-                const int tau = bt + 64 * e;
+            {
                 const uint32_t vmask = tau < nval ? 0xFFFFFFFFu : 0u;  // see the V warps
                 const uint32_t row = bs_s + (uint32_t)((tau >> 3) * 4096 + (tau & 7) * 16);
                 uint32_t kw[KW + 1];
@@ -744,7 +744,7 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
 
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 12) {
+    if (warp == 15) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, 512);
     }
