@@ -221,23 +221,29 @@ __global__ void __launch_bounds__(kTuThreads, 1) topk_umma_kernel(const __grid_c
             }
             const bool rvalid = r0 + t * kTuRows + r < r1;
             const unsigned char* st = sSt0 + (size_t)b * Lo.stage_bytes;
-            // this thread's half row of codes (16 CB bytes) and of sign bits (16 bytes)
+            // this thread's half row of codes (16 CB bytes) and of sign bits (16
+            // bytes); a row past the end reads stale staging bytes, cleared by
+            // the mask (the loads stay unconditional: a load that a branch may
+            // skip is waited for where the paths merge)
+            const uint32_t rmask = rvalid ? 0xFFFFFFFFu : 0u;
             uint32_t cw[HW + 1];
             {
                 const uint4* src = reinterpret_cast<const uint4*>(st + (size_t)r * cs + 16 * CB * h);
 #pragma unroll
                 for (int q = 0; q < CB; ++q) {
-                    const uint4 v = rvalid ? src[q] : make_uint4(0u, 0u, 0u, 0u);
-                    cw[4 * q] = v.x;
-                    cw[4 * q + 1] = v.y;
-                    cw[4 * q + 2] = v.z;
-                    cw[4 * q + 3] = v.w;
+                    const uint4 v = src[q];
+                    cw[4 * q] = v.x & rmask;
+                    cw[4 * q + 1] = v.y & rmask;
+                    cw[4 * q + 2] = v.z & rmask;
+                    cw[4 * q + 3] = v.w & rmask;
                 }
                 cw[HW] = 0u;
             }
             uint4 sgw = make_uint4(0u, 0u, 0u, 0u);
-            if constexpr (PROD)
-                if (rvalid) sgw = *reinterpret_cast<const uint4*>(st + (size_t)kTuRows * cs + (size_t)r * ss + 16 * h);
+            if constexpr (PROD) {
+                const uint4 v = *reinterpret_cast<const uint4*>(st + (size_t)kTuRows * cs + (size_t)r * ss + 16 * h);
+                sgw = make_uint4(v.x & rmask, v.y & rmask, v.z & rmask, v.w & rmask);
+            }
             const uint16_t g16 = g_next;  // gamma of row r of this tile (fp16 bits)
             if (PROD && t + 1 < ntile && r0 + (t + 1) * kTuRows + r < r1) g_next = p.rnorm[r0 + (t + 1) * kTuRows + r];
             __syncwarp();
