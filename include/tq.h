@@ -384,6 +384,8 @@ typedef struct {
     void* out;              /* device [batch][chunk][hq][d] of out_dtype,
                                16-byte aligned                                */
     int out_dtype;          /* TQ_F32 or TQ_BF16                              */
+    tq_event scan_begin;    /* optional: recorded on `stream` right before and */
+    tq_event scan_end;      /* after the scan kernel (for timing it)           */
 } tq_prefill_args;
 
 /* Workspace bytes of tq_attn_prefill (0 on invalid arguments); the workspace

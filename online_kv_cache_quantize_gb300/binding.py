@@ -68,7 +68,7 @@ class tq_prefill_args(ctypes.Structure):
                 ("d", ctypes.c_int), ("q_start", ctypes.c_void_p), ("max_context", ctypes.c_int),
                 ("gqa_map", ctypes.c_void_p), ("rot", ctypes.c_void_p), ("qjl", ctypes.c_void_p), ("k", tq_cache), ("v", tq_cache),
                 ("scale", ctypes.c_float), ("n_splits", ctypes.c_int), ("out", ctypes.c_void_p),
-                ("out_dtype", ctypes.c_int)]
+                ("out_dtype", ctypes.c_int), ("scan_begin", ctypes.c_void_p), ("scan_end", ctypes.c_void_p)]
 
 
 class tq_topk_args(ctypes.Structure):
@@ -369,7 +369,8 @@ def tq_attn_decode(q, kcache, vcache, seq_lens, max_seq_len, rot, qjl, out, work
                                  _stream_ptr(stream)), "tq_attn_decode")
 
 
-def _prefill_struct(q, kcache, vcache, q_start, max_context, rot, qjl, out, scale=0.0, n_splits=0, gqa_map=None):
+def _prefill_struct(q, kcache, vcache, q_start, max_context, rot, qjl, out, scale=0.0, n_splits=0, gqa_map=None,
+                    scan_events=None):
     b, c, hq, d = q.shape
     a = tq_prefill_args()
     keep = None
@@ -389,6 +390,9 @@ def _prefill_struct(q, kcache, vcache, q_start, max_context, rot, qjl, out, scal
     a.n_splits = n_splits
     a.out = out.data_ptr()
     a.out_dtype = _dtype_code(out)
+    if scan_events is not None:  # (begin, end) torch.cuda.Event pair, recorded around the scan kernel
+        a.scan_begin = scan_events[0].cuda_event
+        a.scan_end = scan_events[1].cuda_event
     return a, keep
 
 

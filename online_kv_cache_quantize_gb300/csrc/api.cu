@@ -1345,8 +1345,12 @@ tq_status tq_attn_prefill(const tq_prefill_args* a, void* workspace, size_t ws_b
 
     cudaStream_t st = (cudaStream_t)stream;
     if ((e = tqk::launch_rows_prep(pp, st)) != cudaSuccess) return cuda_status(e, "tq_attn_prefill query prep");
+    if (a->scan_begin && (e = cudaEventRecord((cudaEvent_t)a->scan_begin, st)) != cudaSuccess)
+        return cuda_status(e, "tq_attn_prefill scan_begin");
     e = pl.umma ? tqk::launch_prefill_umma(fp, kb, vb, two, st) : tqk::launch_prefill_mma(fp, kb, vb, two, st);
     if (e != cudaSuccess) return cuda_status(e, "tq_attn_prefill scan");
+    if (a->scan_end && (e = cudaEventRecord((cudaEvent_t)a->scan_end, st)) != cudaSuccess)
+        return cuda_status(e, "tq_attn_prefill scan_end");
     return cuda_status(tqk::launch_merge_rows(cp, st), "tq_attn_prefill merge");
 }
 
