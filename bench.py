@@ -646,9 +646,7 @@ def run_search(args, mode, bits):
                    "rotation": w["rotation"], "l2": "flushed (256 MiB write) before every timed step"},
         "roofline": {"kernel": "topk_umma_kernel (tcgen05 scan)", "bound": "tensor", "achieved": achieved,
                      "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_kind,
-                     "alg_flops_per_step": flops, "avg_launch_us": scan_s * 1e6,
-                     "step_achieved": flops / step_s / 1e12, "step_frac": flops / step_s / 1e12 / peak,
-                     "traffic": None},
+                     "alg_flops_per_step": flops, "traffic": None},
         "e2e": {"value": nq / (e2e_ms / 1e3), "unit": "queries/s", "h2d_bytes_per_step": qs.nbytes,
                 "d2h_bytes_per_step": hids.numel() * 4 + hsc.numel() * 4, "steps": 3},
         "gpu_launches": 3 * K,  # query prep, scan, merge

@@ -134,3 +134,29 @@ def test_umma_prefill_fractional_rates(vbits):
     sc = _scale(vc)
     assert np.max(np.abs(new - want)) <= OUT_TOL * sc
     assert np.max(np.abs(new - old)) <= PAIR_TOL * sc
+
+
+def test_query_prep_unaligned_view_matches():
+    """The tensor-core query prep (RHT) reads q as 16-byte vectors; a query
+    view that is only 4-byte aligned takes the row kernel instead. Both give
+    the same output within fp32 summation order (u = S q' summed in a
+    different order), and both match the oracle."""
+    k, v = W.decode_kv(1, 2, 512, seed=70)
+    kc, vc, gk, gv, kq, vq, pi, s = _caches(k, v, 3, 3, "rht")
+    q = W.query_vectors((1, 24, 8, 128), seed=71)
+    aligned = _run(q, gk, gv, [480], 504, "rht")
+    rot, qjl = P.handles(128, "rht")
+    flat = torch.empty(q.size + 1, dtype=torch.float32, device="cuda")
+    qv = flat[1:].view(q.shape)  # 4-byte aligned only
+    qv.copy_(torch.from_numpy(np.ascontiguousarray(q, dtype=np.float32)))
+    assert qv.data_ptr() % 16 == 4
+    qs = torch.tensor([480], dtype=torch.int32, device="cuda")
+    out = torch.full(q.shape, float("nan"), dtype=torch.float32, device="cuda")
+    ws = B.workspace(B.tq_attn_prefill_workspace(qv, gk, gv, qs, 504, rot, qjl, out))
+    B.tq_attn_prefill(qv, gk, gv, qs, 504, rot, qjl, out, ws)
+    torch.cuda.synchronize()
+    unaligned = out.cpu().numpy()
+    sc = _scale(vc)
+    assert np.max(np.abs(aligned - unaligned)) <= 1e-5 * sc
+    want = oa.prefill(q.astype(np.float64), kc, vc, [480], pi, s, kq["centroids"], vq["centroids"])
+    assert np.max(np.abs(unaligned - want)) <= OUT_TOL * sc
