@@ -346,7 +346,6 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
                 break;
             }
             const unsigned char* st = ring + s * ST::BYTES;
-            const int nval = min(kPuTok, t1 - (t0 + T * kPuTok));  // tokens of this tile inside the split
             // the code words of this thread's token in group J (the next
             // group's are loaded while this one's lookups are in flight)
             auto load_row = [&](int J, uint32_t (&w)[VW + 1]) {
@@ -370,21 +369,31 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
             // then the four stmatrix stores (a rolled loop over pairs of
             // groups keeps the code in the instruction cache)
             auto group = [&](int J, const uint32_t (&w)[VW + 1], uint32_t (&wn)[VW + 1]) {
-                // tokens past the split end get zero values: the loads stay
-                // unconditional (their indices are always inside the table) and
-                // the mask clears them, so no branch splits the lookups (a load
-                // that a branch may skip is waited for where the paths merge)
-                const uint32_t vmask = 8 * J + (lane >> 2) < nval ? 0xFFFFFFFFu : 0u;
+                // Tokens past the split end (stale staging bytes) still index
+                // inside the table, so their values are finite centroids; their
+                // P is exactly 0, so they add nothing, and no mask is needed.
+                // The loads are unconditional: a load that a branch may skip is
+                // waited for where the paths merge.
                 uint32_t f[16];
 #pragma unroll
                 for (int bb = 0; bb < 16; ++bb) {
                     const bool first = !V2 || (bb & 1) == 0;
                     const int wd = first ? VB : VB2;
                     const int base = code_bit<VB, VB2>(8 * bb);
-                    const uint32_t y = (base & 31) == 0 ? w[base >> 5]
-                                                        : __funnelshift_r(w[base >> 5], w[(base >> 5) + 1], base & 31);
-                    const uint32_t off = ((y >> (2 * wd * q)) & ((1u << (2 * wd)) - 1u)) << 2;
-                    f[bb] = lds_at<uint32_t>(first ? vlut : vlut2, off) & vmask;
+                    uint32_t off;
+                    if (8 * wd + 2 <= 32 && base >= 2) {
+                        // the window starts 2 bits early, so the field lands
+                        // pre-scaled to a byte offset (the 2 low bits masked off)
+                        const int b2 = base - 2;
+                        const uint32_t y2 = (b2 & 31) == 0 ? w[b2 >> 5]
+                                                           : __funnelshift_r(w[b2 >> 5], w[(b2 >> 5) + 1], b2 & 31);
+                        off = (y2 >> (2 * wd * q)) & (((1u << (2 * wd)) - 1u) << 2);
+                    } else {
+                        const uint32_t y = (base & 31) == 0 ? w[base >> 5]
+                                                            : __funnelshift_r(w[base >> 5], w[(base >> 5) + 1], base & 31);
+                        off = ((y >> (2 * wd * q)) & ((1u << (2 * wd)) - 1u)) << 2;
+                    }
+                    f[bb] = lds_at<uint32_t>(first ? vlut : vlut2, off);
                 }
                 if (J + 3 < 16) load_row(J + 3, wn);
                 const uint32_t rowaddr = v_s + (uint32_t)((lane >> 3) * 2048 + J * 128 + (lane & 7) * 16);
@@ -438,7 +447,9 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
                 break;
             }
             {
-                const uint32_t vmask = tau < nval ? 0xFFFFFFFFu : 0u;  // see the V warps
+                // a token past the split end gets finite key values and signs
+                // of stale gamma bits: its logits are masked (a select, not
+                // arithmetic) before the softmax uses them, so no mask here
                 const uint32_t row = bs_s + (uint32_t)((tau >> 3) * 4096 + (tau & 7) * 16);
                 uint32_t kw[KW + 1];
                 const unsigned char* kr = st + ST::OFF_KC + tau * ST::KS;
@@ -468,14 +479,14 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
                     const uint32_t* tab = first ? klut : klut2;
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        x[c][j] = lds_at<uint32_t>(tab, field4(kw, code_bit<KB, KB2>(8 * c + 2 * j), 2 * wd)) & vmask;
+                        x[c][j] = lds_at<uint32_t>(tab, field4(kw, code_bit<KB, KB2>(8 * c + 2 * j), 2 * wd));
                 }
 #pragma unroll
                 for (int c = 0; c < 16; ++c) sts128(row + 128u * c, x[c][0], x[c][1], x[c][2], x[c][3]);
                 // sign part: positions 2i, 2i + 1 of sign word w hold bits i and
                 // i + 16; a set bit is +gamma, a clear one -gamma
                 const uint32_t sw[4] = {sg.x, sg.y, sg.z, sg.w};
-                const uint32_t g2 = (gb | (gb << 16)) & 0x7FFF7FFFu & vmask;
+                const uint32_t g2 = (gb | (gb << 16)) & 0x7FFF7FFFu;
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const uint32_t w = sw[c >> 2];
