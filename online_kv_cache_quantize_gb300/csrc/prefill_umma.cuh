@@ -189,6 +189,10 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
 
     __shared__ uint32_t klut[KL];
     __shared__ uint32_t klut2[KL2];
+    // 2-bit keys at one width: four codes (one byte of the row) per lookup,
+    // entry x = the pair entries of its low and high nibbles
+    constexpr bool KQ = KB == 2 && !K2;
+    __shared__ __align__(8) uint2 kquad[KQ ? 256 : 1];
     __shared__ uint32_t vlut[VL];
     __shared__ uint32_t vlut2[VL2];
     __shared__ float s_xv[2][2][kPuRows];  // softmax pair exchange: [slot][column half][row]
@@ -216,6 +220,8 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
     auto pair_bar = [&](int quarter) { return bar0 + 8u * (uint32_t)(3 * kPuStages + 7 + quarter); };  // 2 warps
 
     for (int i = tid; i < KL; i += kPuThreads) klut[i] = p.klut[i];
+    if constexpr (KQ)
+        for (int i = tid; i < 256; i += kPuThreads) kquad[i] = make_uint2(p.klut[i & 15], p.klut[i >> 4]);
     for (int i = tid; i < VL; i += kPuThreads) vlut[i] = p.vlut[i];
     if constexpr (K2)
         for (int i = tid; i < KL2; i += kPuThreads) klut2[i] = p.klut2[i];
@@ -472,6 +478,22 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
                 // key part: chunk c holds coordinates 8c .. 8c + 7 (four pairs);
                 // every lookup of the row goes out before the first store
                 uint32_t x[16][4];
+                if constexpr (KQ) {
+                    // byte b of the row = codes 4b .. 4b + 3; chunk c = bytes 2c, 2c + 1
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int bit = 8 * (2 * c + h);
+                            const uint32_t wv = kw[bit >> 5];
+                            const int sh = bit & 31;
+                            const uint32_t off = (sh >= 3 ? (wv >> (sh - 3)) : (wv << (3 - sh))) & 0x7F8u;
+                            const uint2 e = lds_at<uint2>(kquad, off);
+                            x[c][2 * h] = e.x;
+                            x[c][2 * h + 1] = e.y;
+                        }
+                    }
+                } else {
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const bool first = !K2 || (c & 1) == 0;
@@ -480,6 +502,7 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
                         x[c][j] = lds_at<uint32_t>(tab, field4(kw, code_bit<KB, KB2>(8 * c + 2 * j), 2 * wd));
+                }
                 }
 #pragma unroll
                 for (int c = 0; c < 16; ++c) sts128(row + 128u * c, x[c][0], x[c][1], x[c][2], x[c][3]);
