@@ -743,6 +743,7 @@ tq_status decode_prepare(const tq_decode_args* a, void* workspace, size_t ws_byt
     cp.n_splits = pl.n_splits;
     cp.pi32 = a->rot->d_pi32;
     cp.sgn = a->rot->d_sign;
+    cp.err = dp.err;
     cp.rht = a->rot->kind == TQ_ROT_RHT;
     cp.inv_sqrt_d = (float)(1.0 / std::sqrt((double)a->d));
     cp.out = a->out;

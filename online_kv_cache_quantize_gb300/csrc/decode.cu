@@ -302,6 +302,22 @@ cudaError_t launch_decode_mma(const DecodeParams& p, int kbits, int vbits, bool 
 // reads a partial (griddepcontrol.wait).
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
     if (p.rows <= 0) return cudaSuccess;
+    const bool bulk = p.d == 128 && p.rht && p.err != nullptr && p.n_splits >= 1 &&
+                      p.n_splits <= kCombBulkMaxSplits && (reinterpret_cast<uintptr_t>(p.partial) & 15) == 0;
+    if (bulk) {
+        const size_t smem = (size_t)p.n_splits * (128 + kPartPad) * sizeof(float);  // <= 48 KB
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)p.rows);
+        cfg.blockDim = dim3(kCombBulkThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, combine_bulk_kernel, p);
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.rows);
     cfg.blockDim = dim3(kCombineThreads);

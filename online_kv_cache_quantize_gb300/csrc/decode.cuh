@@ -9,6 +9,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "pipeline.cuh"
 #include "tq_launch.h"
 
 namespace tqk {
@@ -172,8 +173,12 @@ __global__ void __launch_bounds__(kPrepWarps * 32) query_prep_kernel(const __gri
 // CTA of 1024 threads = 1024 / (d / 4) groups of d / 4 threads, thread c4 of
 // a group owning coordinates 4 c4 .. 4 c4 + 3. Group k merges the splits
 // k, k + groups, ... (online max, sum and a), loading kCombinePer of them at
-// once so that their loads are in flight together; then the groups are
-// merged through shared memory. d in {64, 128, 256}.
+// once so that their loads are in flight together. The groups are then
+// merged in parallel, not one after another: one warp reduction gives M* and
+// the groups' weights 2^(m_k - M*), and the 1024 threads sum the weighted
+// group vectors as 1024 / d parts per coordinate. The RHT signs the
+// un-rotation needs are loaded before the wait for the scan. d in {64, 128,
+// 256}.
 // ---------------------------------------------------------------------------
 constexpr int kCombineThreads = 1024;
 constexpr int kCombinePer = 4;
@@ -181,15 +186,22 @@ constexpr int kCombinePer = 4;
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ CombineParams p) {
     __shared__ float s_m[64];
     __shared__ float s_z[64];
+    __shared__ float s_w[64];
+    __shared__ float s_zt;
     __shared__ __align__(16) float s_v[kCombineThreads * 4];
+    __shared__ float s_p[kCombineThreads];
     __shared__ float s_a[256];
-    // launched as a programmatic dependent of the scan: wait for its grid to
-    // complete and its partials to be visible (a no-op on a plain launch)
-    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     const int row = blockIdx.x, tid = threadIdx.x, d = p.d, ns = p.n_splits;
     const int tpr = d >> 2, groups = kCombineThreads / tpr;
     const int grp = tid / tpr, c4 = tid % tpr;
     const int stride = d + kPartPad;
+    // dense Pi: thread (ugrp, ci) takes rows ugrp + k ug of column ci
+    const int ug = kCombineThreads / d, ci = tid % d, ugrp = tid / d;
+    const int nk = d / ug;  // rows of Pi a thread takes: 4, 16 or 64 for d = 64, 128, 256
+    const float sg = (p.rht && tid < d) ? p.sgn[tid] : 0.0f;
+    // launched as a programmatic dependent of the scan: wait for its grid to
+    // complete and its partials to be visible (a no-op on a plain launch)
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     const float* base = p.partial + (int64_t)row * ns * stride;
 
     float m = -INFINITY, z = 0.0f;
@@ -197,18 +209,17 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
     for (int s0 = grp; s0 < ns; s0 += groups * kCombinePer) {
         float4 av[kCombinePer];
         float mv[kCombinePer], zv[kCombinePer];
+        // unconditional loads (an index past the last split reads the last
+        // one again and is then dropped): a load behind a branch is waited
+        // for where the paths merge, which would serialise them
 #pragma unroll
         for (int k = 0; k < kCombinePer; ++k) {
             const int s = s0 + k * groups;
-            mv[k] = -INFINITY;
-            zv[k] = 0.0f;
-            av[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            if (s < ns) {
-                const float* ps = base + (int64_t)s * stride;
-                av[k] = *reinterpret_cast<const float4*>(ps + 4 * c4);
-                mv[k] = ps[d];
-                zv[k] = ps[d + 1];
-            }
+            const float* ps = base + (int64_t)min(s, ns - 1) * stride;
+            av[k] = *reinterpret_cast<const float4*>(ps + 4 * c4);
+            const float2 mz = *reinterpret_cast<const float2*>(ps + d);
+            mv[k] = s < ns ? mz.x : -INFINITY;
+            zv[k] = mz.y;
         }
 #pragma unroll
         for (int k = 0; k < kCombinePer; ++k) {
@@ -238,17 +249,39 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
         s_z[grp] = z;
     }
     __syncthreads();
-    if (tid < d) {
-        float mstar = -INFINITY;
-        for (int k = 0; k < groups; ++k) mstar = fmaxf(mstar, s_m[k]);
-        float zt = 0.0f, at = 0.0f;
-        for (int k = 0; k < groups; ++k) {
-            const float mk = s_m[k];
-            if (mk == -INFINITY) continue;
-            const float w = exp2f(mk - mstar);
-            zt = fmaf(s_z[k], w, zt);
-            at = fmaf(s_v[k * d + tid], w, at);
+    if (tid < 32) {
+        // M* over the groups (lane l holds groups l and l + 32), their weights
+        // and Z = sum_k z_k 2^(m_k - M*)
+        const int lane = tid;
+        const float m0 = lane < groups ? s_m[lane] : -INFINITY;
+        const float m1 = lane + 32 < groups ? s_m[lane + 32] : -INFINITY;
+        const float mstar = warp_max(fmaxf(m0, m1));
+        const float w0 = (m0 == -INFINITY) ? 0.0f : exp2f(m0 - mstar);
+        const float w1 = (m1 == -INFINITY) ? 0.0f : exp2f(m1 - mstar);
+        float zt = 0.0f;
+        if (lane < groups) {
+            s_w[lane] = w0;
+            zt = s_z[lane] * w0;
         }
+        if (lane + 32 < groups) {
+            s_w[lane + 32] = w1;
+            zt = fmaf(s_z[lane + 32], w1, zt);
+        }
+        zt = warp_sum(zt);
+        if (lane == 0) s_zt = zt;
+    }
+    __syncthreads();
+    {
+        // part q of coordinate ci: the groups q, q + ug, ... (groups / ug of them)
+        float acc = 0.0f;
+        for (int k = ugrp; k < groups; k += ug) acc = fmaf(s_v[k * d + ci], s_w[k], acc);
+        s_p[tid] = acc;
+    }
+    __syncthreads();
+    if (tid < d) {
+        float at = 0.0f;
+        for (int q = 0; q < ug; ++q) at += s_p[q * d + tid];
+        const float zt = s_zt;
         s_a[tid] = (zt > 0.0f) ? at / zt : 0.0f;
     }
     __syncthreads();
@@ -272,12 +305,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
                 const float t = s_v[lane + 32 * k];
                 acc += (__popc(w & k) & 1) ? -t : t;
             }
-            o = acc * p.sgn[tid] * p.inv_sqrt_d;
+            o = acc * sg * p.inv_sqrt_d;
         }
     } else {
-        // o_i = sum_k Pi[k][i] a_k, the k range split over 1024 / d groups of d threads
-        const int ug = kCombineThreads / d, i = tid % d, ugrp = tid / d;
-        const int nk = d / ug;  // rows of Pi a thread takes: 4, 16 or 64 for d = 64, 128, 256
+        // o_i = sum_k Pi[k][i] a_k, the k range split over ug groups of d threads
         float part = 0.0f;
         // 16 independent loads into registers first, then the products: one
         // round of memory latency per 16 rows, not one per row
@@ -285,7 +316,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
             float pv[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-                pv[j] = k0 + j < nk ? __ldg(p.pi32 + (size_t)(ugrp + (k0 + j) * ug) * d + i) : 0.0f;
+                pv[j] = k0 + j < nk ? __ldg(p.pi32 + (size_t)(ugrp + (k0 + j) * ug) * d + ci) : 0.0f;
 #pragma unroll
             for (int j = 0; j < 16; ++j)
                 if (k0 + j < nk) part = fmaf(pv[j], s_a[ugrp + (k0 + j) * ug], part);
@@ -301,6 +332,90 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
         else
             reinterpret_cast<float*>(p.out)[(int64_t)row * d + tid] = o;
     }
+}
+
+// ---------------------------------------------------------------------------
+// The same merge for d = 128 with the random-sign Hadamard un-rotation and at
+// most kCombBulkMaxSplits splits (a decode step): one CTA of 128 threads per
+// query row. The row's partials are contiguous (n_splits x (d + pad)
+// floats), so one bulk copy brings all of them into shared memory at once,
+// one round of latency for the whole row. Then thread t takes split t for
+// M* = max M_s (a block reduction), the weights w_s = 2^(M_s - M*) (0 for a
+// split that saw no token) and Z = sum w_s Z_s, and thread i sums
+// a_i = sum_s w_s a_s[i] over the splits in order; o = s * (H a) / sqrt(d)
+// with H by warp butterflies and one exchange through shared memory. The CTA
+// is small (128 threads, the partials in shared memory), so it fits beside
+// the scan's CTAs and is resident, waiting, before the scan ends.
+// ---------------------------------------------------------------------------
+constexpr int kCombBulkThreads = 128;
+constexpr int kCombBulkMaxSplits = 93;  // (d + pad) * 4 bytes per split: at most 48 KB of shared memory
+
+__global__ void __launch_bounds__(kCombBulkThreads) combine_bulk_kernel(const __grid_constant__ CombineParams p) {
+    constexpr int D = 128, stride = D + kPartPad;
+    extern __shared__ __align__(128) unsigned char cb_smem[];
+    __shared__ __align__(8) uint64_t s_bar;
+    __shared__ float s_w[kCombBulkThreads];
+    __shared__ float s_red[2][4];
+    __shared__ float s_y[D];
+    const float* part = reinterpret_cast<const float*>(cb_smem);
+    const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, ns = p.n_splits;
+    const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&s_bar);
+    const float sg = p.sgn[tid];  // does not depend on the scan: read while it runs
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    // launched as a programmatic dependent of the scan: wait for its grid to
+    // complete and its partials to be visible (a no-op on a plain launch)
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    if (tid == 0) {
+        const uint32_t bytes = (uint32_t)(ns * stride * 4);
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s((uint32_t)__cvta_generic_to_shared(cb_smem), p.partial + (int64_t)row * ns * stride, bytes, bar);
+    }
+    if (!__syncthreads_and(mbar_wait_bounded(bar, 0, kWaitLimitNs, p.err, kErrScanWait))) {
+        // the copy did not land in time (the error word says so): it must
+        // still land before the shared memory is released
+        mbar_wait_bounded(bar, 0, kWaitLimitNs, p.err, kErrScanWait);
+        return;
+    }
+    // M* over the splits (thread t holds split t)
+    const float ms = tid < ns ? part[tid * stride + D] : -INFINITY;
+    const float mw = warp_max(ms);
+    if (lane == 0) s_red[0][warp] = mw;
+    __syncthreads();
+    const float mstar = fmaxf(fmaxf(s_red[0][0], s_red[0][1]), fmaxf(s_red[0][2], s_red[0][3]));
+    const float w = (ms == -INFINITY) ? 0.0f : exp2f(ms - mstar);
+    const float zw = warp_sum(tid < ns ? part[tid * stride + D + 1] * w : 0.0f);
+    s_w[tid] = w;
+    if (lane == 0) s_red[1][warp] = zw;
+    __syncthreads();
+    const float z = (s_red[1][0] + s_red[1][1]) + (s_red[1][2] + s_red[1][3]);
+    float at = 0.0f;
+#pragma unroll 8
+    for (int k = 0; k < ns; ++k) at = fmaf(part[k * stride + tid], s_w[k], at);
+    // o = s * (H a) / sqrt(d): strides 1..16 across the lanes, 32 and 64 as a
+    // 4-point transform over the warps through shared memory
+    float y = z > 0.0f ? at / z : 0.0f;
+#pragma unroll
+    for (int h = 1; h < 32; h <<= 1) {
+        const float t = __shfl_xor_sync(TQ_FULL_MASK, y, h);
+        y = (lane & h) ? (t - y) : (y + t);
+    }
+    s_y[tid] = y;
+    __syncthreads();
+    float acc = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float t = s_y[lane + 32 * k];
+        acc += (__popc(warp & k) & 1) ? -t : t;
+    }
+    const float o = acc * sg * p.inv_sqrt_d;
+    if (p.out_dtype == 1)
+        reinterpret_cast<__nv_bfloat16*>(p.out)[(int64_t)row * D + tid] = __float2bfloat16_rn(o);
+    else
+        reinterpret_cast<float*>(p.out)[(int64_t)row * D + tid] = o;
 }
 
 // ---------------------------------------------------------------------------
@@ -321,22 +436,40 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_rows_kernel(const __gr
     if (row >= p.rows) return;
     const int ns = p.n_splits, stride = 128 + kPartPad;
     const float* base = p.partial + (int64_t)row * ns * stride;
+    // 8 splits at a time, every load unconditional (an index past the last
+    // split reads the last one again; a branch around a load would serialise
+    // the loads), the splits summed in order with weight 0 for the dropped
+    constexpr int kB = 8;
     float mstar = -INFINITY;
-    for (int s = 0; s < ns; ++s) mstar = fmaxf(mstar, base[(int64_t)s * stride + 128]);
+    for (int s0 = 0; s0 < ns; s0 += kB) {
+        float mv[kB];
+#pragma unroll
+        for (int k = 0; k < kB; ++k) mv[k] = base[(int64_t)min(s0 + k, ns - 1) * stride + 128];
+#pragma unroll
+        for (int k = 0; k < kB; ++k) mstar = fmaxf(mstar, mv[k]);
+    }
     float z = 0.0f;
     float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     if (mstar != -INFINITY) {
-        for (int s = 0; s < ns; ++s) {
-            const float* ps = base + (int64_t)s * stride;
-            const float ms = ps[128];
-            if (ms == -INFINITY) continue;
-            const float w = exp2f(ms - mstar);
-            const float4 av = *reinterpret_cast<const float4*>(ps + 4 * lane);
-            z = fmaf(ps[129], w, z);
-            a.x = fmaf(av.x, w, a.x);
-            a.y = fmaf(av.y, w, a.y);
-            a.z = fmaf(av.z, w, a.z);
-            a.w = fmaf(av.w, w, a.w);
+        for (int s0 = 0; s0 < ns; s0 += kB) {
+            float4 av[kB];
+            float2 mz[kB];
+#pragma unroll
+            for (int k = 0; k < kB; ++k) {
+                const float* ps = base + (int64_t)min(s0 + k, ns - 1) * stride;
+                av[k] = *reinterpret_cast<const float4*>(ps + 4 * lane);
+                mz[k] = *reinterpret_cast<const float2*>(ps + 128);
+            }
+#pragma unroll
+            for (int k = 0; k < kB; ++k) {
+                const bool use = s0 + k < ns && mz[k].x != -INFINITY;
+                const float w = exp2f(use ? mz[k].x - mstar : -INFINITY);
+                z = use ? fmaf(mz[k].y, w, z) : z;
+                a.x = use ? fmaf(av[k].x, w, a.x) : a.x;
+                a.y = use ? fmaf(av[k].y, w, a.y) : a.y;
+                a.z = use ? fmaf(av[k].z, w, a.z) : a.z;
+                a.w = use ? fmaf(av[k].w, w, a.w) : a.w;
+            }
         }
     }
     const float inv = z > 0.0f ? 1.0f / z : 0.0f;

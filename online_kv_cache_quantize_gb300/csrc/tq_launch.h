@@ -269,6 +269,7 @@ struct CombineParams {
     float inv_sqrt_d;
     void* out;
     int out_dtype;        // 0 f32, 1 bf16
+    uint32_t* err;        // device error word (null: the merge without bounded waits)
 };
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
