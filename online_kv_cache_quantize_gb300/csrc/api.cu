@@ -1163,6 +1163,7 @@ namespace {
 struct PrefillPlan {
     int group = 0, n_splits = 0, split_tokens = 0, lim_cap = 0;
     bool umma = false;  // the tcgen05 kernel (128 rows x 128-token tiles per CTA)
+    int qbs = 0, unit_tiles = 0, tiles_per_cta = 0;  // its stream-K plan
     size_t off_u = 0, off_part = 0, total = 0;
 };
 
@@ -1203,32 +1204,45 @@ tq_status plan_prefill(const tq_prefill_args* a, PrefillPlan* pl) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int ctx = std::max(a->max_context, 1);
     const long long base = std::max<long long>(1, qbs * a->batch * a->hkv);
-    long long want = a->n_splits;
-    if (want <= 0 && !pl->umma) {  // about four CTAs per SM (two resident)
-        want = ((long long)sms * 4 + base - 1) / base;
-    } else if (want <= 0) {
-        // one CTA per SM: the split count whose waves of CTAs take the least
-        // time, a wave costing its tiles plus about two tiles of set-up,
-        // merge and tail
+    if (pl->umma) {
+        // Stream-K over the (unit, tile) sequence: unit u = (batch row, KV
+        // head, query block) owns ntile 128-token tiles; one CTA per SM takes
+        // an equal share of the whole sequence, crossing unit boundaries, so
+        // no SM idles when the units do not fill whole waves. An explicit
+        // split count instead pads each unit to n equal splits, one per CTA.
         const long long ntile = (ctx + tile - 1) / tile;
-        double best = 1e300;
-        want = 1;
-        for (long long n = 1; n <= std::min<long long>(ntile, 256); ++n) {
-            const long long per = (ntile + n - 1) / n;
-            const long long nn = (ntile + per - 1) / per;
-            const long long waves = (base * nn + sms - 1) / sms;
-            const double cost = (double)waves * (double)(per + 2);
-            if (cost < best - 1e-9) {
-                best = cost;
-                want = nn;
-            }
+        long long nt_unit = ntile, tpc;
+        if (a->n_splits > 0) {
+            const long long per = (ntile + a->n_splits - 1) / a->n_splits;
+            nt_unit = per * ((ntile + per - 1) / per);
+            tpc = per;
+        } else {
+            const long long c = std::min<long long>(sms, base * ntile);
+            tpc = (base * ntile + c - 1) / c;
+            // at most kPuMaxSeg - 1 segments per CTA
+            tpc = std::max(1LL, std::min(tpc, (long long)(tqk::kPuMaxSeg - 2) * ntile));
         }
+        const long long ctas = (base * nt_unit + tpc - 1) / tpc;
+        if (ctas > 0x7fffffff || nt_unit > 0x7fffffff) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: grid too large");
+        // slots per row: the most CTAs one unit spans
+        long long slots = 1;
+        for (long long u = 0; u < base; ++u)
+            slots = std::max(slots, ((u + 1) * nt_unit - 1) / tpc - (u * nt_unit) / tpc + 1);
+        if (slots > 65535) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: too many splits");
+        pl->qbs = (int)qbs;
+        pl->unit_tiles = (int)nt_unit;
+        pl->tiles_per_cta = (int)tpc;
+        pl->n_splits = (int)slots;
+        pl->split_tokens = (int)std::min<long long>(tpc * tile, 0x7fffffff);
+    } else {
+        long long want = a->n_splits;
+        if (want <= 0) want = ((long long)sms * 4 + base - 1) / base;  // about four CTAs per SM (two resident)
+        if (want > 65535) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: too many splits");
+        int st = (int)((ctx + want - 1) / want);
+        st = std::max(tile, (st + tile - 1) / tile * tile);
+        pl->split_tokens = st;
+        pl->n_splits = (ctx + st - 1) / st;
     }
-    if (want > 65535) return fail(TQ_ERR_UNSUPPORTED, "tq_attn_prefill: too many splits");
-    int st = (int)((ctx + want - 1) / want);
-    st = std::max(tile, (st + tile - 1) / tile * tile);
-    pl->split_tokens = st;
-    pl->n_splits = (ctx + st - 1) / st;
     const size_t r = (size_t)rows;
     pl->off_u = round_up(r * 128 * sizeof(float), 256);
     pl->off_part = pl->off_u + round_up(r * 128 * sizeof(float), 256);
@@ -1328,6 +1342,9 @@ tq_status tq_attn_prefill(const tq_prefill_args* a, void* workspace, size_t ws_b
     fp.n_splits = pl.n_splits;
     fp.split_tokens = pl.split_tokens;
     fp.partial = (float*)(ws + pl.off_part);
+    fp.qbs = pl.qbs;
+    fp.unit_tiles = pl.unit_tiles;
+    fp.tiles_per_cta = pl.tiles_per_cta;
     cudaError_t e = tqk::device_error_word(&fp.err);
     if (e != cudaSuccess) return cuda_status(e, "tq_attn_prefill error word");
 

@@ -150,9 +150,10 @@ __device__ __forceinline__ bool pu_issue_s(int T, uint32_t tmem, uint32_t qlo_s,
 }
 
 // O += P(T) V(T) over K = 128 tokens, P in two fp16 limbs in TMEM, issued
-// by one thread once P(T) and V(T) are written
-__device__ __forceinline__ bool pu_issue_o(int T, uint32_t tmem, uint32_t v_s, uint32_t p_full, uint32_t v_full,
-                                           uint32_t o_done, uint32_t idesc, uint32_t* err) {
+// by one thread once P(T) and V(T) are written (T counts the CTA's tiles;
+// first: the segment's first tile, which starts O afresh)
+__device__ __forceinline__ bool pu_issue_o(int T, bool first, uint32_t tmem, uint32_t v_s, uint32_t p_full,
+                                           uint32_t v_full, uint32_t o_done, uint32_t idesc, uint32_t* err) {
     if (!pu_wait(p_full, (uint32_t)(T & 1), err)) return false;
     if (!pu_wait(v_full, (uint32_t)(T & 1), err)) return false;
     tc_fence_after_sync();
@@ -160,12 +161,24 @@ __device__ __forceinline__ bool pu_issue_o(int T, uint32_t tmem, uint32_t v_s, u
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const uint64_t bd = umma_desc(v_s + 256u * k, 128, 2048);
-        umma_f16_ta(dO, tmem + kPuColP + 8u * k, bd, idesc, T > 0 || k > 0);
+        umma_f16_ta(dO, tmem + kPuColP + 8u * k, bd, idesc, !first || k > 0);
         umma_f16_ta(dO, tmem + kPuColP + 64u + 8u * k, bd, idesc, true);
     }
     umma_commit(o_done);
     return true;
 }
+
+// One unit's share of a CTA's tile range (stream-K): query block qb of KV
+// head kv of batch row b, tokens [t0, t_end) of its sequence, visible up to
+// t1 (the causal limit of the block's last chunk token), ntiles tiles with
+// visible tokens; tg0 = the CTA's tiles before this segment (the barrier
+// phases run on across segments); the unit's rows' partials go to slot, and
+// the unit spans nslot slots.
+struct PuSeg {
+    int qb, b, kv;
+    int t0, t_end, t1;
+    int ntiles, tg0, slot, nslot;
+};
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float r;
@@ -200,10 +213,10 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
     __shared__ __align__(8) uint64_t s_bar[3 * kPuStages + 7 + 4];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
+    __shared__ PuSeg s_seg[kPuMaxSeg];
+    __shared__ int s_nseg, s_ntot;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int qb = blockIdx.x, split = blockIdx.y;
-    const int b = blockIdx.z / p.hkv, kv = blockIdx.z % p.hkv;
     const int G = p.group;
 
     const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(&s_bar[0]);
@@ -243,6 +256,43 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
         for (int i = 0; i < 4; ++i) mbar_init(pair_bar(i), 2);
         s_abort = 0;
         mbar_init_fence();
+        // this CTA's segments: tiles [g0, g1) of the (unit, tile) sequence
+        const int64_t total = (int64_t)p.qbs * p.batch * p.hkv * p.unit_tiles;
+        const int64_t g0 = (int64_t)blockIdx.x * p.tiles_per_cta;
+        const int64_t g1 = min(g0 + p.tiles_per_cta, total);
+        int n = 0, tg = 0;
+        int64_t g = g0;
+        for (; g < g1 && n < kPuMaxSeg; ++n) {
+            const int64_t u = g / p.unit_tiles;
+            const int a = (int)(g - u * p.unit_tiles);
+            const int bend = (int)min((int64_t)p.unit_tiles, a + (g1 - g));
+            PuSeg sg;
+            sg.qb = (int)(u % p.qbs);
+            const int bkv = (int)(u / p.qbs);
+            sg.b = bkv / p.hkv;
+            sg.kv = bkv % p.hkv;
+            // rows see at most the slots before the limit of the block's last chunk token
+            const int i_last = min(p.chunk - 1, (sg.qb * kPuRows + kPuRows - 1) / G);
+            const int lim = max(0, min(p.q_start[sg.b] + i_last + 1, p.lim_cap));
+            sg.t0 = a * kPuTok;
+            sg.t_end = bend * kPuTok;
+            sg.t1 = min(sg.t_end, lim);
+            sg.ntiles = sg.t1 > sg.t0 ? (sg.t1 - sg.t0 + kPuTok - 1) / kPuTok : 0;
+            sg.tg0 = tg;
+            const int64_t fc = (u * p.unit_tiles) / p.tiles_per_cta;
+            sg.slot = (int)(blockIdx.x - fc);
+            sg.nslot = (int)(((u + 1) * p.unit_tiles - 1) / p.tiles_per_cta - fc + 1);
+            s_seg[n] = sg;
+            tg += sg.ntiles;
+            g += bend - a;
+        }
+        if (g < g1) {  // more units than the plan allows (the host bounds it): report, do nothing
+            atomicOr(p.err, kErrScanWait);
+            n = 0;
+            tg = 0;
+        }
+        s_nseg = n;
+        s_ntot = tg;
     }
     if (warp == 15) {
         tmem_alloc((uint32_t)__cvta_generic_to_shared(&s_tmem), 512);
@@ -254,27 +304,18 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
     const uint32_t tmem = s_tmem;
     volatile int* abort_flag = &s_abort;
 
-    // ---- the CTA's tokens: rows see at most the slots before the limit of
-    // its last chunk token; the split covers [t0, t0 + split_tokens) ----
-    const int qs = p.q_start[b];
-    const int i_last = min(p.chunk - 1, (qb * kPuRows + kPuRows - 1) / G);
-    const int cta_lim = max(0, min(qs + i_last + 1, p.lim_cap));
-    const int t0 = split * p.split_tokens;
-    const int t_end = t0 + p.split_tokens;
-    const int t1 = min(t_end, cta_lim);
-    const int ntiles = t1 > t0 ? (t1 - t0 + kPuTok - 1) / kPuTok : 0;
-    const int64_t rowbase = ((int64_t)b * p.hkv + kv) * p.capacity;
+    const int nseg = s_nseg;      // segments of this CTA
+    const int ntot = s_ntot;      // tiles over all of them
     const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
     const uint32_t bs_s = (uint32_t)__cvta_generic_to_shared(sBs);
     const uint32_t v_s = (uint32_t)__cvta_generic_to_shared(sV);
     const uint32_t qlo_s = (uint32_t)__cvta_generic_to_shared(sQlo);
 
-    // the six bulk copies of tile T's cache planes into ring stage T % kPuStages
-    auto issue_copies = [&](int T) {  // one thread
-        const int s = T % kPuStages;
-        const int tb = t0 + T * kPuTok;
-        const uint32_t ntok = (uint32_t)((min(kPuTok, t1 - tb) + 15) & ~15);  // whole 16-slot rows
-        const int64_t slot = rowbase + tb;
+    // the six bulk copies of the tile starting at cache slot `slot` with
+    // ntok (whole 16-slot rows) to fetch into ring stage Tg % kPuStages (the
+    // CTA's tile Tg)
+    auto issue_copies = [&](int64_t slot, uint32_t ntok, int Tg) {  // one thread
+        const int s = Tg % kPuStages;
         const uint32_t dst = ring_s + (uint32_t)(s * ST::BYTES), bar = ring_full(s);
         fence_proxy_async_smem();  // the consumers' reads of this stage come first
         mbar_arrive_expect_tx(bar, ntok * (uint32_t)(ST::KS + 16 + 2 + 2 + ST::VS + 2));
@@ -288,37 +329,64 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
 
     if (warp == 15) {
         // ======================= MMA issue and bulk copies (one thread) =======================
-        if (lane == 0 && ntiles > 0) {
-            int issued = 0;
-            for (; issued < kPuStages && issued < ntiles; ++issued) issue_copies(issued);
+        if (lane == 0 && ntot > 0) {
+            // the copy cursor: the next tile to fetch is tile ct of segment
+            // cs (its fields cached in registers: this thread also issues the
+            // MMAs, so its per-tile path stays short), the CTA's tile issued
+            int cs = -1, ct = 0, cnt = 0, issued = 0, ctb = 0, ct1 = 0;
+            int64_t crow = 0;
+            auto next_copy = [&]() {
+                while (ct >= cnt) {
+                    const PuSeg& sg = s_seg[++cs];
+                    ct = 0;
+                    cnt = sg.ntiles;
+                    ctb = sg.t0;
+                    ct1 = sg.t1;
+                    crow = ((int64_t)sg.b * p.hkv + sg.kv) * p.capacity;
+                }
+                const int tb = ctb + ct * kPuTok;
+                issue_copies(crow + tb, (uint32_t)((min(kPuTok, ct1 - tb) + 15) & ~15), issued);
+                ++ct;
+                ++issued;
+            };
+            while (issued < kPuStages && issued < ntot) next_copy();
             const uint32_t idesc = umma_idesc_f16(kPuRows, kPuTok);
             uint32_t last_bar = 0, last_par = 0;
-            bool ok = pu_wait(q_full, 0, p.err);
-            if (ok) {
-                ok = pu_issue_s(0, tmem, qlo_s, bs_s, bs_full, s_empty, s_done, idesc, p.err);
+            int qn = 0;  // segments whose query operands were loaded
+            bool ok = true;
+            for (int si = 0; ok && si < nseg; ++si) {
+                const PuSeg sg = s_seg[si];
+                if (sg.ntiles == 0) continue;
+                // the softmax warps loaded this segment's query operands
+                if (!(ok = pu_wait(q_full, (uint32_t)(qn & 1), p.err))) break;
+                ++qn;
+                if (!(ok = pu_issue_s(sg.tg0, tmem, qlo_s, bs_s, bs_full, s_empty, s_done, idesc, p.err))) break;
                 last_bar = s_done;
-                last_par = 0;
-            }
-            for (int T = 0; ok && T < ntiles; ++T) {
-                if (*abort_flag) {
-                    ok = false;
-                    break;
-                }
-                // the next tile's scores go in while the softmax works on this one
-                if (T + 1 < ntiles) {
-                    if (!(ok = pu_issue_s(T + 1, tmem, qlo_s, bs_s, bs_full, s_empty, s_done, idesc, p.err))) break;
-                    last_bar = s_done;
-                    last_par = (uint32_t)((T + 1) & 1);
-                }
-                if (!(ok = pu_issue_o(T, tmem, v_s, p_full, v_full, o_done, idesc, p.err))) break;
-                last_bar = o_done;
-                last_par = (uint32_t)(T & 1);
-                // tile T's stage is free once its softmax, Bs and V warps are
-                // done with it (just after P(T) and V(T), waited for above):
-                // refill it with tile T + kPuStages
-                if (issued < ntiles) {
-                    if (!(ok = pu_wait(ring_empty(T % kPuStages), (uint32_t)((T / kPuStages) & 1), p.err))) break;
-                    issue_copies(issued++);
+                last_par = (uint32_t)(sg.tg0 & 1);
+                for (int T = 0; ok && T < sg.ntiles; ++T) {
+                    const int Tg = sg.tg0 + T;
+                    if (*abort_flag) {
+                        ok = false;
+                        break;
+                    }
+                    // the next tile's scores go in while the softmax works on this one
+                    if (T + 1 < sg.ntiles) {
+                        if (!(ok = pu_issue_s(Tg + 1, tmem, qlo_s, bs_s, bs_full, s_empty, s_done, idesc, p.err)))
+                            break;
+                        last_bar = s_done;
+                        last_par = (uint32_t)((Tg + 1) & 1);
+                    }
+                    if (!(ok = pu_issue_o(Tg, T == 0, tmem, v_s, p_full, v_full, o_done, idesc, p.err))) break;
+                    last_bar = o_done;
+                    last_par = (uint32_t)(Tg & 1);
+                    // tile Tg's stage is free once its softmax, Bs and V warps are
+                    // done with it (just after P(Tg) and V(Tg), waited for above):
+                    // refill it with tile Tg + kPuStages, possibly of a later segment
+                    if (issued < ntot) {
+                        if (!(ok = pu_wait(ring_empty(Tg % kPuStages), (uint32_t)((Tg / kPuStages) & 1), p.err)))
+                            break;
+                        next_copy();
+                    }
                 }
             }
             if (!ok) *abort_flag = 1;
@@ -341,7 +409,9 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
         const int vw = warp - 12;
         const int q = lane & 3;
         constexpr int VW = ST::VS / 4;
-        for (int T = 0; T < ntiles; ++T) {
+        // T: the CTA's tile count over all its segments (the values need no
+        // per-segment state)
+        for (int T = 0; T < ntot; ++T) {
             const int s = T % kPuStages;
             bool ok = !*abort_flag && pu_wait(ring_full(s), (uint32_t)((T / kPuStages) & 1), p.err);
             // O += P(T - 1) V(T - 1) has read V(T - 1)
@@ -429,7 +499,17 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
         const int tau = 32 * (warp - 8) + lane;
         const float kfac = p.inv_lam_k * p.scale_log2;
         constexpr int KW = ST::KS / 4;
-        for (int T = 0; T < ntiles; ++T) {
+        // T: the CTA's tile count; the segment cursor (si, Tl) gives the
+        // tile's tokens (the segment's fields cached in registers)
+        int si = -1, Tl = 0, snt = 0, st0 = 0, st1 = 0;
+        for (int T = 0; T < ntot; ++T, ++Tl) {
+            while (Tl >= snt) {
+                const PuSeg& sg = s_seg[++si];
+                Tl = 0;
+                snt = sg.ntiles;
+                st0 = sg.t0;
+                st1 = sg.t1;
+            }
             const int s = T % kPuStages;
             bool ok = !*abort_flag && pu_wait(ring_full(s), (uint32_t)((T / kPuStages) & 1), p.err);
             if (!__all_sync(TQ_FULL_MASK, ok)) {
@@ -437,7 +517,7 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
                 break;
             }
             unsigned char* st = ring + s * ST::BYTES;
-            const int nval = min(kPuTok, t1 - (t0 + T * kPuTok));
+            const int nval = min(kPuTok, st1 - (st0 + Tl * kPuTok));
             {  // the softmax's per-token factors
                 const bool valid = tau < nval;
                 const float kn = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(st + ST::OFF_KN)[tau]);
@@ -534,15 +614,6 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
         const int qd = warp & 3, hc = warp >> 2;  // TMEM lane quarter, column half
         const int r = 32 * qd + lane;             // query row = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
-        // CTA row r is chunk token i = (qb * 128 + r) / G and the
-        // ((qb * 128 + r) % G)-th query head of KV head kv
-        const int qg = qb * kPuRows + r;
-        const int ci = qg / G;
-        const bool rok = ci < p.chunk;
-        const int hj = kv * G + (qg - ci * G);
-        const int64_t qrow =
-            rok ? ((int64_t)b * p.chunk + ci) * p.hq + (p.use_table ? (int)p.head_table[hj] : hj) : -1;
-        const int rlim = rok ? min(max(0, min(qs + ci + 1, p.lim_cap)), t_end) : 0;  // tokens >= rlim are masked
 
         // The two threads of a row swap a value and a flag through shared
         // memory and the pair's mbarrier (one arrival per warp, one phase per
@@ -562,11 +633,28 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
             other_ok = got ? s_xok[slot][hc ^ 1][r] : 0;
         };
 
+        bool ok = true;
+        for (int si = 0; ok && si < nseg; ++si) {
+        const PuSeg& sg = s_seg[si];  // read from shared memory where used (registers are at the cap)
+        const int ntiles = sg.ntiles, t0 = sg.t0, tgb = sg.tg0;
+        // CTA row r is chunk token i = (qb * 128 + r) / G and the
+        // ((qb * 128 + r) % G)-th query head of KV head kv
+        const int qg = sg.qb * kPuRows + r;
+        const int ci = qg / G;
+        const bool rok = ci < p.chunk;
+        const int hj = sg.kv * G + (qg - ci * G);
+        const int64_t qrow =
+            rok ? ((int64_t)sg.b * p.chunk + ci) * p.hq + (p.use_table ? (int)p.head_table[hj] : hj) : -1;
+        // tokens >= rlim are masked
+        const int rlim = rok ? min(max(0, min(p.q_start[sg.b] + ci + 1, p.lim_cap)), sg.t_end) : 0;
+
         // ---- A of S: hi limbs in TMEM (columns 0..63 q', column m holding
         // coordinates 2m, 2m + 1; 64..127 kappa lam_k u, column 64 + 16 w + i
         // holding sign rows 32 w + i and 32 w + i + 16), lo limbs in shared
         // memory at the same K positions (row r of the K-major layout); the
-        // hc = 0 warps write q', the hc = 1 warps kappa lam_k u ----
+        // hc = 0 warps write q', the hc = 1 warps kappa lam_k u. A later
+        // segment overwrites them once the last scores of the one before
+        // (waited for in its tile loop) are complete ----
         if (ntiles > 0) {
             const uint32_t qrow_s = qlo_s + (uint32_t)((r >> 3) * 4096 + (r & 7) * 16);
             if (hc == 0) {
@@ -613,12 +701,12 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
         }
 
         float M = -INFINITY, Z = 0.0f;
-        bool ok = true;
         for (int T = 0; T < ntiles; ++T) {
-            const int s = T % kPuStages;
+            const int Tg = tgb + T;  // the CTA's tile count: stage and barrier phases
+            const int s = Tg % kPuStages;
             bool w_ok = !*abort_flag;
-            w_ok = w_ok && pu_wait(fac_full(s), (uint32_t)((T / kPuStages) & 1), p.err);
-            w_ok = w_ok && pu_wait(s_done, (uint32_t)(T & 1), p.err);
+            w_ok = w_ok && pu_wait(fac_full(s), (uint32_t)((Tg / kPuStages) & 1), p.err);
+            w_ok = w_ok && pu_wait(s_done, (uint32_t)(Tg & 1), p.err);
             w_ok = __all_sync(TQ_FULL_MASK, w_ok);
             tc_fence_after_sync();
             // this thread's 64 columns of S (read even after a failed wait:
@@ -680,10 +768,11 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
             Z = fmaf(Z, corr, zz.x + zz.y);
             M = mn;
 
-            // P(T) and the rescale of O wait for O += P(T - 1) V(T - 1)
+            // P(T) and the rescale of O wait for O += P(T - 1) V(T - 1) (the
+            // previous segment's last one, for a segment's first tile)
             bool o_ok = true;
-            if (T > 0)
-                o_ok = __all_sync(TQ_FULL_MASK, pu_wait(o_done, (uint32_t)((T - 1) & 1), p.err));
+            if (Tg > 0)
+                o_ok = __all_sync(TQ_FULL_MASK, pu_wait(o_done, (uint32_t)((Tg - 1) & 1), p.err));
             {
                 float dummy;
                 int o_ook;
@@ -737,19 +826,19 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
             }
         }
         if (!ok) *abort_flag = 1;
-        asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+        if (si == nseg - 1) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
-        // ---- this split's partials of row r: a (rotated domain) from both
+        // ---- this segment's partials of row r: a (rotated domain) from both
         // halves, M, and Z summed over the pair ----
         if (ok && ntiles > 0) {
-            ok = __all_sync(TQ_FULL_MASK, pu_wait(o_done, (uint32_t)((ntiles - 1) & 1), p.err));
+            ok = __all_sync(TQ_FULL_MASK, pu_wait(o_done, (uint32_t)((tgb + ntiles - 1) & 1), p.err));
             tc_fence_after_sync();
         }
         float zo;
         int zok;
         exchange(Z, ok ? 1 : 0, zo, zok);
         ok = ok && zok;
-        float* out = qrow >= 0 ? p.partial + (qrow * p.n_splits + split) * (D + kPartPad) : nullptr;
+        float* out = qrow >= 0 ? p.partial + (qrow * p.n_splits + sg.slot) * (D + kPartPad) : nullptr;
         const float inv_lv = p.inv_lam_v;
         if (ok && ntiles > 0) {
 #pragma unroll
@@ -774,6 +863,20 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
             out[D] = M;
             out[D + 1] = Z + zo;
         }
+        // the unit's first segment also writes the slots no CTA of the unit
+        // fills as empty partials (M = -inf, Z = 0, a = 0)
+        if (sg.slot == 0 && qrow >= 0)
+            for (int e = sg.nslot; e < p.n_splits; ++e) {
+                float* oe = p.partial + (qrow * p.n_splits + e) * (D + kPartPad);
+                float4* o4 = reinterpret_cast<float4*>(oe + 64 * hc);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) o4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (hc == 0) {
+                    oe[D] = -INFINITY;
+                    oe[D + 1] = 0.0f;
+                }
+            }
+        }  // segments
     }
 
     tc_fence_before_sync();
@@ -797,9 +900,12 @@ cudaError_t launch_prefill_umma_t(const PrefillParams& p, cudaStream_t s) {
     static_assert(smem <= 227 * 1024 - 4096, "prefill tile buffers exceed shared memory");
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const unsigned qbs = (unsigned)((p.chunk * p.group + kPuRows - 1) / kPuRows);
-    dim3 grid(qbs, (unsigned)p.n_splits, (unsigned)(p.batch * p.hkv));
-    kern<<<grid, kPuThreads, smem, s>>>(p);
+    // stream-K: ceil(units x unit_tiles / tiles_per_cta) CTAs
+    const int64_t total = (int64_t)p.qbs * p.batch * p.hkv * p.unit_tiles;
+    if (p.tiles_per_cta < 1 || p.unit_tiles < 1 || total < 1) return cudaErrorInvalidValue;
+    const int64_t ctas = (total + p.tiles_per_cta - 1) / p.tiles_per_cta;
+    if (ctas > 0x7fffffff) return cudaErrorInvalidValue;
+    kern<<<dim3((unsigned)ctas), kPuThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 

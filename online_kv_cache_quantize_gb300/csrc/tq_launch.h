@@ -235,6 +235,15 @@ struct PrefillParams {
     int split_tokens;     // tokens per split (a multiple of 64)
     float* partial;       // [rows][n_splits][128 + kPartPad]: a, then M and Z
     uint32_t* err;
+    // the tcgen05 kernel's stream-K plan: unit u = (batch row, KV head, query
+    // block), u = (b * hkv + kv) * qbs + qb, owns tiles [u * unit_tiles,
+    // (u + 1) * unit_tiles) of one sequence; CTA c takes tiles [c *
+    // tiles_per_cta, (c + 1) * tiles_per_cta) of it, one segment per unit it
+    // touches, and writes the unit's rows' partials into slot (c - the unit's
+    // first CTA); n_splits = the most CTAs a unit spans
+    int qbs;
+    int unit_tiles;
+    int tiles_per_cta;
 };
 
 // two: keys and values are both fractional-rate caches
@@ -244,6 +253,7 @@ cudaError_t launch_prefill_mma(const PrefillParams& p, int kbits, int vbits, boo
 // for fractional rates), values 1..4.
 constexpr int kPuRows = 128;
 constexpr int kPuTok = 128;
+constexpr int kPuMaxSeg = 8;  // segments (units) one CTA may touch
 bool prefill_umma_supported(int kbits, int vbits, bool two);
 cudaError_t launch_prefill_umma(const PrefillParams& p, int kbits, int vbits, bool two, cudaStream_t s);
 
