@@ -1,9 +1,10 @@
 """The tcgen05 chunked-prefill scan (keys at PROD 2 / 3 bits or the 3 / 2
 fractional rate): against the fp64 oracle, and against the mma.sync scan on
 the same oracle-packed caches, over shapes that exercise its tiling: several
-128-row CTAs with a ragged last one, 128-token tiles with a ragged tail, many
-tiles per split (the 3-deep copy ring wraps many times), splits that see no
-token at all, and repeated runs.
+128-row query blocks with a ragged last one, 128-token tiles with a ragged
+tail, many tiles per split (the 3-deep copy ring wraps many times), splits
+that see no token at all, stream-K CTAs whose tile range crosses from one
+unit (batch row, KV head, query block) into the next, and repeated runs.
 
 Tolerances: both scans are checked against the oracle at the decode output
 tolerance (1e-3 of max nV / sqrt(d)). Against each other they differ only by
@@ -160,3 +161,23 @@ def test_query_prep_unaligned_view_matches():
     assert np.max(np.abs(aligned - unaligned)) <= 1e-5 * sc
     want = oa.prefill(q.astype(np.float64), kc, vc, [480], pi, s, kq["centroids"], vq["centroids"])
     assert np.max(np.abs(unaligned - want)) <= OUT_TOL * sc
+
+
+def test_umma_prefill_stream_k_segments_cross_units():
+    """Stream-K: 2 batch rows x 4 KV heads x one 128-row query block (64
+    chunk tokens, G = 2) = 8 units of 25 tiles each (3200 tokens), so 200
+    tiles over at most one CTA per SM. Each CTA takes 2 tiles, so some start
+    in one unit and end in the next, and a unit's rows fill up to 13 partial
+    slots. The second row's chunk sits at 1500, so most of its units' tiles
+    lie past the causal limit: those segments have no tile and write empty
+    partials. Checked against the oracle and the mma.sync scan."""
+    k, v = W.decode_kv(2, 4, 3200, heavy_frac=0.02, seed=80)
+    kc, vc, gk, gv, kq, vq, pi, s = _caches(k, v, 3, 3, "rht")
+    q = W.query_vectors((2, 64, 8, 128), seed=81)
+    q_start = [3136, 1500]
+    new = _run(q, gk, gv, q_start, 3200, "rht")
+    old = _run(q, gk, gv, q_start, 3200, "rht", mma_sync=True)
+    want = oa.prefill(q.astype(np.float64), kc, vc, q_start, pi, s, kq["centroids"], vq["centroids"])
+    sc = _scale(vc)
+    assert np.max(np.abs(new - want)) <= OUT_TOL * sc
+    assert np.max(np.abs(new - old)) <= PAIR_TOL * sc
