@@ -10,8 +10,13 @@
 // contraction into TMEM, an online softmax over its rows, and O += P V
 // accumulated in TMEM.
 //
-// One CTA: 128 query rows (the MMA M dimension, row r in TMEM lane r) of one
-// KV head against one token split. Operands:
+// Work split (stream-K): a unit is 128 query rows (the MMA M dimension, row r
+// in TMEM lane r) of one KV head with all its 128-token tiles; the units'
+// tiles form one sequence, and each CTA (one per SM) takes an equal run of
+// it, which may start and end inside units. Each unit the run touches is a
+// segment with its own query operands, softmax state and partial slot; the
+// barrier phases run on across segments and the copy ring prefetches into
+// the next one. Operands:
 //  * A of S (loaded once): fp16 hi/lo limbs of q' for the key part and of
 //    kappa lam_k u for the sign part (K = 128 + 128), the hi limbs in TMEM,
 //    the lo limbs in shared memory;
@@ -42,7 +47,8 @@
 //    and V warps are done with its tile); the warp owns the TMEM allocation.
 // Per tile T the MMA thread issues S(T + 1) as soon as Bs(T + 1) is written
 // and the softmax has read S(T), then O += P(T) V(T), so the tensor pipe runs
-// the next tile's scores while the softmax works; Bs and V are written by
+// the next tile's scores while the softmax works (a segment's first scores
+// wait for its query operands); Bs and V are written by
 // separate warps, so neither waits for the other's buffer. Every wait is
 // bounded; a wait that runs out sets the library's error word and the CTA
 // drains and returns.
@@ -287,7 +293,7 @@ __global__ void __launch_bounds__(kPuThreads, 1) prefill_umma_kernel(const __gri
             g += bend - a;
         }
         if (g < g1) {  // more units than the plan allows (the host bounds it): report, do nothing
-            atomicOr(p.err, kErrScanWait);
+            if (p.err) atomicOr(p.err, kErrScanWait);
             n = 0;
             tg = 0;
         }
