@@ -130,6 +130,30 @@ def test_prefill_workspace_plan_on_the_host(lib):
     assert L.tq_attn_prefill_workspace(ctypes.byref(a)) == 0
 
 
+def test_prefill_stream_k_plan_on_the_host(lib):
+    """The tcgen05 prefill's stream-K plan, read through its workspace (q' and
+    u rows plus rows x slots partials). 2 units (2 KV heads x one 128-row
+    query block) of 8 tiles (1000 tokens) are 16 tiles, at most one per SM,
+    so each CTA takes one tile and a unit's rows fill one slot per tile. An
+    explicit split count of 3 pads each unit to 3 splits of 3 tiles: three
+    slots."""
+    import ctypes
+    L = lib.load()
+    a = lib.tq_prefill_args()
+    a.batch, a.chunk, a.hq, a.hkv, a.d, a.max_context = 1, 32, 8, 2, 128, 1000
+    a.k.capacity = 1024
+    a.k.mode, a.k.bits, a.v.mode, a.v.bits = lib.TQ_PROD, 3, lib.TQ_MSE, 3  # the tcgen05 widths
+    rows = 32 * 8
+
+    def want(slots):
+        return 2 * rows * 128 * 4 + rows * slots * (128 + 4) * 4
+
+    a.n_splits = 0
+    assert L.tq_attn_prefill_workspace(ctypes.byref(a)) == want(8)
+    a.n_splits = 3
+    assert L.tq_attn_prefill_workspace(ctypes.byref(a)) == want(3)
+
+
 def test_argument_errors_are_reported(lib):
     with pytest.raises(lib.TQError) as e:
         lib.tq_make_rotation(1, 200, "rht")
